@@ -1,0 +1,417 @@
+#!/usr/bin/env python
+"""Benchmark: block-sparse attention throughput on one GB300 (per rank).
+
+One step = one block-sparse attention forward, O = softmax(scale Q K^T on the
+layout) V, over one batch of the workload (default: the banded workload,
+Z=4 H=16 S=8192 D=128 B=128 bf16, block band |i-j| <= 4).  The fused kernel
+does SDD -> softmax -> DSD in one pass.  Throughput counts nonzero-block FLOPs
+only: 4 * B^2 * D per present block per batch entry.
+
+Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+on a bounded sample of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "block-sparse attention TFLOP/s (nonzero-block FLOPs) and % of GB300 peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="band", choices=["band", "strided", "bigbird", "tiny"])
+    p.add_argument("--no-ops", action="store_true", help="skip the per-op section")
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="target oracle CPU time")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        if self.proc is None or not self.lines:
+            return None
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ helpers --
+
+def workload(name):
+    from sparse_attention_layout_gb300 import workloads as W
+    return W.ATTENTION_WORKLOADS[name]
+
+
+def nonzero_flops(lay, B, D, Z):
+    return 4.0 * B * B * D * int(lay.sum()) * Z
+
+
+def config_of(w, lay, path_name):
+    nnz = int(lay.sum())
+    return {
+        "workload": f"{w.name}: Z{w.Z} H{w.H} S{w.S} D{w.D} B{w.B} {w.dtype}, "
+                    f"{nnz} of {w.H * w.nb * w.nb} blocks present ({100.0 * nnz / (w.H * w.nb * w.nb):.1f}%)",
+        "Z": w.Z, "H": w.H, "S": w.S, "D": w.D, "block": w.B, "nnz_blocks": nnz,
+        "mask": ["none", "dense", "diag_causal"][w.mask_kind], "scale": w.scale,
+        "path": path_name,
+        "l2": "inputs larger than L2: Q, K, V, O total "
+              f"{4 * w.Z * w.H * w.S * w.D * (2 if w.dtype != 'f32' else 4) / 1e6:.0f} MB, no flush",
+    }
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(os.path.join(ROOT, "sparse_attention_layout_gb300", "csrc"))):
+        with open(os.path.join(ROOT, "sparse_attention_layout_gb300", "csrc", f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel, wname):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(f"{kernel}:{wname}")
+    if not e or e.get("source_sha") != kernel_source_sha():
+        return None
+    return e.get("bytes_per_launch")
+
+
+def cpu_oracle_sample(w, lay, Q, K, V, target_s, seed=0):
+    """Time the oracle on a seeded sample of rows; returns (TFLOP/s, rows, seconds)."""
+    import oracle
+    orc = oracle.Oracle()
+    rng = np.random.default_rng(seed)
+    total_rows = w.Z * w.H * w.S
+    rows_blocks = lay.sum(axis=2)  # [H, nb]
+
+    def flops_of(sel):
+        zh, r = sel // w.S, sel % w.S
+        h = zh % w.H
+        return float(np.sum(4.0 * w.B * w.D * rows_blocks[h, r // w.B]))
+
+    n = 64
+    while True:
+        sel = np.sort(rng.choice(total_rows, size=min(n, total_rows), replace=False))
+        t0 = time.perf_counter()
+        orc.attention(lay, w.B, Q, K, V, w.scale, w.mask_kind, None, sel=sel)
+        dt = time.perf_counter() - t0
+        if dt >= target_s or n >= total_rows:
+            return flops_of(sel) / dt / 1e12, int(sel.size), dt, orc.num_threads()
+        n = min(total_rows, int(n * max(2.0, min(16.0, 1.2 * target_s / max(dt, 1e-3)))))
+
+
+# --------------------------------------------------------------- reference --
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = workload(args.workload)
+    lay = w.layout()
+    Q, K, V = w.qkv()
+    import oracle
+    orc = oracle.Oracle()
+    rng = np.random.default_rng(123)
+    total_rows = w.Z * w.H * w.S
+    rows_blocks = lay.sum(axis=2)
+    per_step = max(16, min(total_rows, 256))
+    # calibrate the sample so one step is about 0.5 s of CPU work
+    sel = np.sort(rng.choice(total_rows, size=per_step, replace=False))
+    t0 = time.perf_counter()
+    orc.attention(lay, w.B, Q, K, V, w.scale, w.mask_kind, None, sel=sel)
+    dt = time.perf_counter() - t0
+    per_step = int(max(16, min(total_rows, per_step * 0.5 / max(dt, 1e-4))))
+    flops = 0.0
+    for _ in range(args.warmup):
+        sel = np.sort(rng.choice(total_rows, size=per_step, replace=False))
+        orc.attention(lay, w.B, Q, K, V, w.scale, w.mask_kind, None, sel=sel)
+    t_total = 0.0
+    for _ in range(args.steps):
+        sel = np.sort(rng.choice(total_rows, size=per_step, replace=False))
+        zh, r = sel // w.S, sel % w.S
+        flops += float(np.sum(4.0 * w.B * w.D * rows_blocks[zh % w.H, r // w.B]))
+        t0 = time.perf_counter()
+        orc.attention(lay, w.B, Q, K, V, w.scale, w.mask_kind, None, sel=sel)
+        t_total += time.perf_counter() - t0
+    value = flops / t_total / 1e12
+    sample = f"{per_step} random rows of {total_rows} per step (all heads and batch entries)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(w, lay, "fp64 CPU oracle (dense-mask definition)"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------- ours --
+
+def time_launches(fn, n, stream):
+    import torch
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(n):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / n  # ms per launch
+
+
+def per_op_section(w, lay, L, q, k, v, pk, bsp, stream):
+    """Times each step of the unfused chain and the general spMM modes."""
+    import torch
+    from sparse_attention_layout_gb300 import workloads as W
+    out = {}
+    elt = 2 if w.dtype != "f32" else 4
+    Z, B, D, nnz = w.Z, w.B, w.D, int(lay.sum())
+    P = bsp.bsp_sdd(L, q, k)
+    ms = time_launches(lambda: bsp.bsp_sdd(L, q, k, P), 10, stream)
+    out["sdd"] = {"ms": ms, "TFLOP/s": 2.0 * B * B * D * nnz * Z / ms / 1e9,
+                  "GB/s": (Z * nnz * B * B * elt) / ms / 1e6}
+    X = P.clone()
+    ms = time_launches(lambda: bsp.bsp_softmax(L, X, P, w.scale, w.mask_kind), 10, stream)
+    sbytes = 2.0 * Z * nnz * B * B * elt
+    out["softmax"] = {"ms": ms, "GB/s": sbytes / ms / 1e6,
+                      "frac_of_hbm": sbytes / ms / 1e6 / pk["hbm_gbs"],
+                      "algorithmic_bytes": sbytes}
+    O = torch.empty_like(q)
+    ms = time_launches(lambda: bsp.bsp_dsd(L, P, v, O), 10, stream)
+    out["dsd"] = {"ms": ms, "TFLOP/s": 2.0 * B * B * D * nnz * Z / ms / 1e9}
+    ms = time_launches(lambda: bsp.attention_unfused(L, q, k, v, w.scale, w.mask_kind), 5, stream)
+    out["attention_unfused_chain"] = {"ms": ms, "TFLOP/s": nonzero_flops(lay, B, D, Z) / ms / 1e9}
+    del P, X, O
+    # general spMM at 10 % density (8192^2 sparse, 8192x4096 dense, block 32)
+    sp = W.SPMM
+    lay4 = sp.layout(0.10)
+    L4 = bsp.bsp_layout_compile(lay4, sp.B)
+    A = sp.sparse_values(L4.nnz, 0.10).cuda()
+    Bd = sp.dense_dsd(0.10).cuda()
+    Ad = sp.dense_dds(0.10).cuda()
+    C1 = bsp.bsp_dsd(L4, A, Bd)
+    ms = time_launches(lambda: bsp.bsp_dsd(L4, A, Bd, C1), 10, stream)
+    fl = 2.0 * sp.B * sp.B * sp.N * L4.nnz
+    out["dsd_spmm_10pct"] = {"ms": ms, "TFLOP/s": fl / ms / 1e9, "frac_of_bf16_peak": fl / ms / 1e9 / pk["bf16_tflops"]}
+    C2 = bsp.bsp_dds(L4, Ad, A)
+    ms = time_launches(lambda: bsp.bsp_dds(L4, Ad, A, C2), 10, stream)
+    out["dds_spmm_10pct"] = {"ms": ms, "TFLOP/s": fl / ms / 1e9, "frac_of_bf16_peak": fl / ms / 1e9 / pk["bf16_tflops"]}
+    return out
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from sparse_attention_layout_gb300 import build as b
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if rank == 0 or world == 1:
+        b.build()
+    if world > 1:
+        dist.barrier()
+    from sparse_attention_layout_gb300 import bsp
+
+    w = workload(args.workload)
+    lay = w.layout()
+    Qc, Kc, Vc = w.qkv()
+    stream = torch.cuda.current_stream()
+    L = bsp.bsp_layout_compile(lay, w.B)
+    q, k, v = (t.cuda() for t in (Qc, Kc, Vc))
+    o = torch.empty_like(q)
+    pk, pk_kind = peaks()
+
+    def step():
+        bsp.bsp_attention(L, q, k, v, o, w.scale, w.mask_kind)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    status = bsp.bsp_status_check(L)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    flops = nonzero_flops(lay, w.B, w.D, w.Z)
+    value = flops * world / (ms_step * 1e-3) / 1e12
+    achieved = flops / (ms_step * 1e-3) / 1e12  # one attention launch per step
+
+    # end to end through the public API: pinned host inputs -> device ->
+    # attention -> host output, every step
+    Qh, Kh, Vh = (t.pin_memory() for t in (Qc, Kc, Vc))
+    Oh = torch.empty_like(Qc).pin_memory()
+
+    def e2e_step():
+        q.copy_(Qh, non_blocking=True)
+        k.copy_(Kh, non_blocking=True)
+        v.copy_(Vh, non_blocking=True)
+        bsp.bsp_attention(L, q, k, v, o, w.scale, w.mask_kind)
+        Oh.copy_(o, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        e2e_step()
+    e2e_ms = time_launches(e2e_step, e2e_steps, stream)
+    h2d = 3 * Qc.numel() * Qc.element_size()
+    d2h = Oh.numel() * Oh.element_size()
+
+    ops = None
+    if not args.no_ops and rank == 0:
+        ops = per_op_section(w, lay, L, q, k, v, pk, bsp, stream)
+    torch.cuda.synchronize()
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+        return
+    cpu_val, cpu_rows, cpu_s, cores = cpu_oracle_sample(w, lay, Qc, Kc, Vc, args.cpu_seconds)
+    if world > 1:
+        dist.barrier()
+    peak = pk["bf16_tflops"] if w.dtype != "f32" else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": config_of(w, lay, "fused attention kernel"),
+        "gpu_launches": args.steps,
+        "roofline": {
+            "bound": "tensor", "kernel": "attention", "achieved": achieved, "peak": peak,
+            "peak_source": f"bf16_tflops (burst) of {pk_kind}", "unit": "TFLOP/s",
+            "frac": (achieved / peak) if peak else None,
+            "traffic": traffic_for("attention", w.name),
+            "algorithmic_flops_per_launch": flops,
+        },
+        "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "cpu_baseline": {"value": cpu_val, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{cpu_rows} random rows of {w.Z * w.H * w.S} "
+                                   f"({cpu_s:.1f} s, fp64, OpenMP)"},
+        "clocks": clk.summary(),
+        "lib": bsp.lib_path(),
+    }
+    if ops is not None:
+        line["ops"] = ops
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * bsp.h — C ABI of libbsp: block-sparse matrix multiply (SDD, DSD, DDS),
+ * block-sparse row softmax and block-sparse attention on one GB300 GPU.
+ *
+ * Source of the operations: "question on blocksparse" (openai/triton issue
+ * 117).  The sparsity layout is a tensor of 0s and 1s in which each entry
+ * stands for one square block of 16, 32, 64 or 128 elements; blocks never
+ * overlap.  There are three matmul modes: SDD (a sampled dense x dense
+ * product whose output is block-sparse), DSD (dense = sparse x dense) and DDS
+ * (dense = dense x sparse).  The SDD output is the input of the block-sparse
+ * softmax, which reduces each row across the row's blocks and equals the dense
+ * softmax of the present entries; dense masks may be passed for the entries
+ * inside blocks (the diagonal blocks of a block-causal layout are full).
+ * Chained, SDD -> softmax -> DSD is block-sparse attention.
+ *
+ * Conventions for every call:
+ *  - Layout: host array uint8 [H][nb][nb] with values 0/1, S = nb * block.
+ *    The layout is shared by all Z batch entries.
+ *  - Block-sparse tensors are [Z][nnz][block][block], row-major inside a
+ *    block; block n is the n-th present block in row-major (h, i, j) order
+ *    (nnz counts all heads).
+ *  - Dense tensors are contiguous row-major [Z][H][rows][cols].
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller, 16-byte
+ *    aligned (else BSP_ERR_ALIGNMENT); the library never frees it.  With an
+ *    empty batch (Z == 0) a call does nothing and its pointers may be NULL.
+ *  - dtype (bsp_dtype_t) is the type of every floating-point input and output
+ *    of the call; accumulation is always fp32.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every compute
+ *    call only enqueues work on it and returns; results are ready when the
+ *    stream is.
+ *  - Argument errors are detected before anything is launched; nothing aborts,
+ *    throws or traps.  Kernels that detect an impossible state (a bounded wait
+ *    that ran out, a bounds check that failed) skip the access, record a code
+ *    in the handle's device status word and return; bsp_status_check reads it.
+ *  - The handle is immutable after compilation and may be used concurrently
+ *    from several streams of the device it was compiled on.
+ */
+#ifndef BSP_H
+#define BSP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct bsp_layout_s* bsp_layout_t;
+
+typedef enum { BSP_F32 = 0, BSP_BF16 = 1, BSP_F16 = 2 } bsp_dtype_t;
+
+/* Mask applied inside present blocks by the softmax and attention.
+ * NONE: keep everything.  DENSE: keep (r, c) iff mask[r * S + c] != 0, mask a
+ * DEVICE uint8 [S][S] shared by all heads and batch entries.  DIAG_CAUSAL:
+ * inside the diagonal blocks (block-row == block-column) keep c <= r only. */
+typedef enum {
+    BSP_MASK_NONE = 0,
+    BSP_MASK_DENSE = 1,
+    BSP_MASK_DIAG_CAUSAL = 2
+} bsp_mask_kind_t;
+
+enum {
+    BSP_OK = 0,
+    BSP_ERR_INVALID_ARG = -1,  /* bad value, size, handle or NULL pointer   */
+    BSP_ERR_UNSUPPORTED = -2,  /* valid but not implemented combination      */
+    BSP_ERR_ALIGNMENT = -3,    /* a tensor pointer is not 16-byte aligned    */
+    BSP_ERR_OOM = -4,          /* device or host allocation failed           */
+    BSP_ERR_CUDA = -5,         /* a CUDA runtime call or launch failed       */
+    BSP_ERR_TIMEOUT = -6,      /* a kernel's bounded wait ran out            */
+    BSP_ERR_DEVICE_CHECK = -7  /* a kernel's bounds check failed             */
+};
+
+/* ---- layout ------------------------------------------------------------ */
+
+/* Validate a 0/1 layout and build its lookup tables on the host only.
+ * Produces per-row (CSR) and per-column (CSC) block tables and the work lists
+ * the kernels consume.  The handle owns host memory only; compute calls reject
+ * it with BSP_ERR_INVALID_ARG.  Used to inspect the tables without a GPU.
+ * layout: host uint8 [H][nb][nb], each value 0 or 1 (else INVALID_ARG).
+ * block: 16, 32, 64 or 128 (else INVALID_ARG).  H, nb >= 1.
+ * On success *out receives a new handle (free with bsp_layout_destroy). */
+int bsp_layout_plan(const uint8_t* layout, int H, int nb, int block, bsp_layout_t* out);
+
+/* bsp_layout_plan followed by an upload of every table to the current device,
+ * enqueued on `stream` (the host copies stay owned by the handle, so the
+ * upload may still be in flight when the call returns).  The handle owns its
+ * device memory (one allocation) and its device status word. */
+int bsp_layout_compile(const uint8_t* layout, int H, int nb, int block, void* stream,
+                       bsp_layout_t* out);
+
+/* Free a handle (synchronises the device first if it owns device memory).
+ * NULL is accepted and ignored. */
+int bsp_layout_destroy(bsp_layout_t layout);
+
+/* Sizes of a handle; any output pointer may be NULL. */
+int bsp_layout_info(bsp_layout_t layout, int* H, int* nb, int* block, int64_t* nnz);
+
+/* Copy the lookup tables into caller-owned HOST arrays (any may be NULL).
+ * For a compiled handle they are read back from the device copies the
+ * kernels use.  Sizes: row_ptr, col_ptr [H*(nb+1)]; the others [nnz].
+ * row_ptr[h*(nb+1)+i] is the position (global over heads) of the first block
+ * of block-row i of head h in col_idx / blk_id, columns ascending; col_ptr,
+ * row_idx, blk_id_csc describe the same blocks column by column, rows
+ * ascending.  blk_id and blk_id_csc hold block ids (row-major rank). */
+int bsp_layout_get_luts(bsp_layout_t layout, int32_t* row_ptr, int32_t* col_idx,
+                        int32_t* blk_id, int32_t* col_ptr, int32_t* row_idx,
+                        int32_t* blk_id_csc);
+
+/* Row-tile work list used by the tensor-core SDD and attention kernels (host
+ * copies, for inspection; any pointer may be NULL, call first with NULL
+ * arrays to get the sizes).  A tile is G = 128/block consecutive block-rows of
+ * one head (tile t = h * ceil(nb/G) + g); the union of their block-columns is
+ * cut into steps of G slots.  tile_step_ptr [n_tiles+1]: first step of each
+ * tile; tile_order [n_tiles]: tiles with the most steps first; step_col
+ * [n_steps*G]: block-column of each slot (-1 = padding); step_blk
+ * [n_steps*G*G]: block id at (row a of the tile, slot b), -1 when absent. */
+int bsp_layout_tiles(bsp_layout_t layout, int* G, int* n_tiles, int64_t* n_steps,
+                     int32_t* tile_step_ptr, int32_t* tile_order, int32_t* step_col,
+                     int32_t* step_blk);
+
+/* ---- matmul modes ------------------------------------------------------ */
+
+/* SDD: C = op(A) . op(B) evaluated on the present blocks only.
+ * A: [Z][H][S][K] (trans_a = 0) or [Z][H][K][S] (trans_a = 1).
+ * B: [Z][H][K][S] (trans_b = 0) or [Z][H][S][K] (trans_b = 1).
+ * C: [Z][nnz][block][block] (output).  Attention scores use trans_b = 1
+ * (C = Q K^T with Q, K both [S][K]).  K >= 1. */
+int bsp_sdd(bsp_layout_t layout, int dtype, const void* A, const void* B, void* C,
+            int Z, int K, int trans_a, int trans_b, void* stream);
+
+/* DSD: C = op(A_sp) . op(B), A_sp the S x S block-sparse matrix.
+ * A_sp: [Z][nnz][block][block]; trans_a = 1 uses its transpose.
+ * B: [Z][H][S][N] (trans_b = 0) or [Z][H][N][S] (trans_b = 1).
+ * C: [Z][H][S][N] (output); rows of empty block-rows are written as 0. */
+int bsp_dsd(bsp_layout_t layout, int dtype, const void* A_sp, const void* B, void* C,
+            int Z, int N, int trans_a, int trans_b, void* stream);
+
+/* DDS: C = op(A) . op(B_sp), B_sp the S x S block-sparse matrix.
+ * A: [Z][H][M][S] (trans_a = 0) or [Z][H][S][M] (trans_a = 1).
+ * B_sp: [Z][nnz][block][block]; trans_b = 1 uses its transpose.
+ * C: [Z][H][M][S] (output); columns of empty block-columns are written as 0. */
+int bsp_dds(bsp_layout_t layout, int dtype, const void* A, const void* B_sp, void* C,
+            int Z, int M, int trans_a, int trans_b, void* stream);
+
+/* ---- softmax ----------------------------------------------------------- */
+
+/* Row softmax of scale * X over the kept entries of each row, on SDD output.
+ * X, Y: [Z][nnz][block][block]; Y may equal X (in place).  Entries of
+ * present blocks that the mask removes are written as 0, and so is every
+ * entry of a row with nothing kept.  scale > 0 and finite.
+ * mask: DEVICE uint8 [S][S] for BSP_MASK_DENSE, ignored otherwise. */
+int bsp_softmax(bsp_layout_t layout, int dtype, const void* X, void* Y, int Z, float scale,
+                int mask_kind, const uint8_t* mask, void* stream);
+
+/* ---- attention --------------------------------------------------------- */
+
+/* Fused block-sparse attention: O = softmax(scale Q K^T restricted to the
+ * layout and mask) V, the SDD -> softmax -> DSD chain in one pass that never
+ * writes the scores.  Q, K, V, O: [Z][H][S][D]; rows with nothing kept are 0.
+ * D: 16..128, a multiple of 16.  mask as for bsp_softmax. */
+int bsp_attention(bsp_layout_t layout, int dtype, const void* Q, const void* K, const void* V,
+                  void* O, int Z, int D, float scale, int mask_kind, const uint8_t* mask,
+                  void* stream);
+
+/* ---- status ------------------------------------------------------------ */
+
+/* Synchronise `stream`, then return and clear the handle's device status
+ * word: BSP_OK, BSP_ERR_TIMEOUT or BSP_ERR_DEVICE_CHECK (or BSP_ERR_CUDA if
+ * the synchronisation itself failed). */
+int bsp_status_check(bsp_layout_t layout, void* stream);
+
+/* Static text for a status code. */
+const char* bsp_status_string(int status);
+
+/* Library build identification (static text). */
+const char* bsp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSP_H */

@@ -1,0 +1,241 @@
+"""Thin ctypes binding of libbsp (the C ABI declared in include/bsp.h).
+
+Argument marshalling only: every step of every operation runs in the CUDA
+library.  PyTorch supplies device memory (output allocation) and the current
+stream.  If the library is missing the first call raises: there is no CPU
+fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+MASK_NONE, MASK_DENSE, MASK_DIAG_CAUSAL = 0, 1, 2
+F32, BF16, F16 = 0, 1, 2
+_DTYPES = {torch.float32: F32, torch.bfloat16: BF16, torch.float16: F16}
+
+STATUS = {0: "BSP_OK", -1: "BSP_ERR_INVALID_ARG", -2: "BSP_ERR_UNSUPPORTED",
+          -3: "BSP_ERR_ALIGNMENT", -4: "BSP_ERR_OOM", -5: "BSP_ERR_CUDA",
+          -6: "BSP_ERR_TIMEOUT", -7: "BSP_ERR_DEVICE_CHECK"}
+
+_lib = None
+
+
+class BspError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {STATUS.get(code, code)} ({lib().bsp_status_string(code).decode()})")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded libbsp (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libbsp.so not found at {path}; build it with "
+                               "sparse_attention_layout_gb300.build.build()")
+        L = ctypes.CDLL(path)
+        P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+        L.bsp_layout_plan.argtypes = [P, i32, i32, i32, ctypes.POINTER(P)]
+        L.bsp_layout_compile.argtypes = [P, i32, i32, i32, P, ctypes.POINTER(P)]
+        L.bsp_layout_destroy.argtypes = [P]
+        L.bsp_layout_info.argtypes = [P, P, P, P, P]
+        L.bsp_layout_get_luts.argtypes = [P] * 7
+        L.bsp_layout_tiles.argtypes = [P] * 8
+        L.bsp_sdd.argtypes = [P, i32, P, P, P, i32, i32, i32, i32, P]
+        L.bsp_dsd.argtypes = [P, i32, P, P, P, i32, i32, i32, i32, P]
+        L.bsp_dds.argtypes = [P, i32, P, P, P, i32, i32, i32, i32, P]
+        L.bsp_softmax.argtypes = [P, i32, P, P, i32, f32, i32, P, P]
+        L.bsp_attention.argtypes = [P, i32, P, P, P, P, i32, i32, f32, i32, P, P]
+        L.bsp_status_check.argtypes = [P, P]
+        L.bsp_status_string.restype = ctypes.c_char_p
+        L.bsp_status_string.argtypes = [i32]
+        L.bsp_version.restype = ctypes.c_char_p
+        for name in ("bsp_layout_plan", "bsp_layout_compile", "bsp_layout_destroy", "bsp_layout_info",
+                     "bsp_layout_get_luts", "bsp_layout_tiles", "bsp_sdd", "bsp_dsd", "bsp_dds", "bsp_softmax",
+                     "bsp_attention", "bsp_status_check"):
+            getattr(L, name).restype = i32
+        _lib = L
+    return _lib
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise BspError(rc, what)
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _dtype(*ts):
+    d = ts[0].dtype
+    for t in ts:
+        if t.dtype != d:
+            raise TypeError("all tensors of a call must share one dtype")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    if d not in _DTYPES:
+        raise TypeError(f"unsupported dtype {d}")
+    return _DTYPES[d]
+
+
+class Layout:
+    """Owning wrapper of a bsp_layout_t handle."""
+
+    def __init__(self, handle: ctypes.c_void_p, layout: np.ndarray, block: int):
+        self.handle = handle
+        self.layout = layout
+        self.block = block
+        H, nb, B, nnz = (ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int64())
+        _check(lib().bsp_layout_info(handle, ctypes.byref(H), ctypes.byref(nb), ctypes.byref(B),
+                                     ctypes.byref(nnz)), "bsp_layout_info")
+        self.H, self.nb, self.B, self.nnz = H.value, nb.value, B.value, nnz.value
+        self.S = self.nb * self.B
+
+    def __del__(self):
+        if getattr(self, "handle", None) and _lib is not None:
+            _lib.bsp_layout_destroy(self.handle)
+            self.handle = None
+
+    def luts(self) -> dict:
+        H, nb, nnz = self.H, self.nb, self.nnz
+        out = {k: np.zeros(H * (nb + 1) if k.endswith("ptr") else max(nnz, 1), np.int32)
+               for k in ("row_ptr", "col_idx", "blk_id", "col_ptr", "row_idx", "blk_id_csc")}
+        _check(lib().bsp_layout_get_luts(self.handle, *[ctypes.c_void_p(out[k].ctypes.data) for k in
+                                                        ("row_ptr", "col_idx", "blk_id", "col_ptr",
+                                                         "row_idx", "blk_id_csc")]),
+               "bsp_layout_get_luts")
+        for k in ("col_idx", "blk_id", "row_idx", "blk_id_csc"):
+            out[k] = out[k][:nnz]
+        return out
+
+    def tiles(self) -> dict:
+        G, nt, ns = ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
+        f = lib().bsp_layout_tiles
+        _check(f(self.handle, ctypes.byref(G), ctypes.byref(nt), ctypes.byref(ns), None, None, None, None),
+               "bsp_layout_tiles")
+        G, nt, ns = G.value, nt.value, ns.value
+        out = {"tile_step_ptr": np.zeros(nt + 1, np.int32), "tile_order": np.zeros(max(nt, 1), np.int32),
+               "step_col": np.zeros(max(ns * G, 1), np.int32), "step_blk": np.zeros(max(ns * G * G, 1), np.int32)}
+        _check(f(self.handle, None, None, None, *[ctypes.c_void_p(out[k].ctypes.data) for k in
+                                                  ("tile_step_ptr", "tile_order", "step_col", "step_blk")]),
+               "bsp_layout_tiles")
+        out["step_col"] = out["step_col"][:ns * G].reshape(ns, G)
+        out["step_blk"] = out["step_blk"][:ns * G * G].reshape(ns, G, G)
+        out["tile_order"] = out["tile_order"][:nt]
+        out.update(G=G, n_tiles=nt, n_steps=ns)
+        return out
+
+
+def _layout_args(layout, block):
+    lay = np.ascontiguousarray(layout, dtype=np.uint8)
+    if lay.ndim != 3 or lay.shape[1] != lay.shape[2]:
+        raise ValueError("layout must be [H, nb, nb]")
+    return lay, lay.shape[0], lay.shape[1], int(block)
+
+
+def bsp_layout_plan(layout, block: int) -> Layout:
+    lay, H, nb, B = _layout_args(layout, block)
+    h = ctypes.c_void_p()
+    _check(lib().bsp_layout_plan(ctypes.c_void_p(lay.ctypes.data), H, nb, B, ctypes.byref(h)),
+           "bsp_layout_plan")
+    return Layout(h, lay, B)
+
+
+def bsp_layout_compile(layout, block: int, stream=None) -> Layout:
+    lay, H, nb, B = _layout_args(layout, block)
+    h = ctypes.c_void_p()
+    _check(lib().bsp_layout_compile(ctypes.c_void_p(lay.ctypes.data), H, nb, B, _stream(stream),
+                                    ctypes.byref(h)), "bsp_layout_compile")
+    return Layout(h, lay, B)
+
+
+def bsp_sdd(L: Layout, A, B, C=None, trans_a: int = 0, trans_b: int = 1, stream=None):
+    """C[z, n] = block n of op(A) op(B).  A, B: [Z, H, ., .] device tensors."""
+    Z = A.shape[0]
+    K = A.shape[2] if trans_a else A.shape[3]
+    if C is None:
+        C = torch.empty((Z, L.nnz, L.B, L.B), dtype=A.dtype, device=A.device)
+    dt = _dtype(A, B, C)
+    _check(lib().bsp_sdd(L.handle, dt, _ptr(A), _ptr(B), _ptr(C), Z, K, int(trans_a), int(trans_b),
+                         _stream(stream)), "bsp_sdd")
+    return C
+
+
+def bsp_dsd(L: Layout, A_sp, B, C=None, trans_a: int = 0, trans_b: int = 0, stream=None):
+    """C = op(A_sp) op(B).  A_sp [Z, nnz, B, B]; B [Z, H, S, N] or [Z, H, N, S]."""
+    Z = B.shape[0]
+    N = B.shape[2] if trans_b else B.shape[3]
+    if C is None:
+        C = torch.empty((Z, L.H, L.S, N), dtype=B.dtype, device=B.device)
+    dt = _dtype(A_sp, B, C)
+    _check(lib().bsp_dsd(L.handle, dt, _ptr(A_sp), _ptr(B), _ptr(C), Z, N, int(trans_a), int(trans_b),
+                         _stream(stream)), "bsp_dsd")
+    return C
+
+
+def bsp_dds(L: Layout, A, B_sp, C=None, trans_a: int = 0, trans_b: int = 0, stream=None):
+    """C = op(A) op(B_sp).  A [Z, H, M, S] or [Z, H, S, M]; B_sp [Z, nnz, B, B]."""
+    Z = A.shape[0]
+    M = A.shape[3] if trans_a else A.shape[2]
+    if C is None:
+        C = torch.empty((Z, L.H, M, L.S), dtype=A.dtype, device=A.device)
+    dt = _dtype(A, B_sp, C)
+    _check(lib().bsp_dds(L.handle, dt, _ptr(A), _ptr(B_sp), _ptr(C), Z, M, int(trans_a), int(trans_b),
+                         _stream(stream)), "bsp_dds")
+    return C
+
+
+def bsp_softmax(L: Layout, X, Y=None, scale: float = 1.0, mask_kind: int = MASK_NONE, mask=None,
+                stream=None):
+    """Row softmax of scale * X on the layout.  Y = X for in place."""
+    if Y is None:
+        Y = torch.empty_like(X)
+    dt = _dtype(X, Y)
+    _check(lib().bsp_softmax(L.handle, dt, _ptr(X), _ptr(Y), X.shape[0], float(scale), int(mask_kind),
+                             _ptr(mask), _stream(stream)), "bsp_softmax")
+    return Y
+
+
+def bsp_attention(L: Layout, Q, K, V, O=None, scale: float = 1.0, mask_kind: int = MASK_NONE,
+                  mask=None, stream=None):
+    """Fused block-sparse attention.  Q, K, V, O: [Z, H, S, D]."""
+    if O is None:
+        O = torch.empty_like(Q)
+    dt = _dtype(Q, K, V, O)
+    _check(lib().bsp_attention(L.handle, dt, _ptr(Q), _ptr(K), _ptr(V), _ptr(O), Q.shape[0], Q.shape[3],
+                               float(scale), int(mask_kind), _ptr(mask), _stream(stream)),
+           "bsp_attention")
+    return O
+
+
+def bsp_status_check(L: Layout, stream=None) -> int:
+    return int(lib().bsp_status_check(L.handle, _stream(stream)))
+
+
+def attention_unfused(L: Layout, Q, K, V, scale: float, mask_kind: int = MASK_NONE, mask=None,
+                      stream=None):
+    """The SDD -> softmax -> DSD chain: scores and probabilities go through HBM."""
+    P = bsp_sdd(L, Q, K, trans_a=0, trans_b=1, stream=stream)
+    bsp_softmax(L, P, P, scale, mask_kind, mask, stream=stream)
+    return bsp_dsd(L, P, V, stream=stream)

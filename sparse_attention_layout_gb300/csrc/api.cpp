@@ -1,0 +1,162 @@
+// C ABI entry points of libbsp: argument validation, dispatch between the
+// tensor-core and CUDA-core kernels, status reporting.
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "bsp_internal.h"
+
+namespace bsp {
+
+int sm_count() {
+    static std::mutex mu;
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cached[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n > 0 ? n : 1;
+    }
+    return cached[dev];
+}
+
+}  // namespace bsp
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+bool valid_dtype(int d) { return d == BSP_F32 || d == BSP_BF16 || d == BSP_F16; }
+bool valid_kind(int k) { return k == BSP_MASK_NONE || k == BSP_MASK_DENSE || k == BSP_MASK_DIAG_CAUSAL; }
+
+// Common checks for a compute call: a device handle, the right device, a
+// valid dtype, non-NULL 16-byte-aligned tensors (any pointer may be NULL when
+// the batch is empty, Z == 0).
+int check_common(bsp_layout_t L, int dtype, int Z, std::initializer_list<const void*> ptrs) {
+    if (!L || !L->on_device) return BSP_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype) || Z < 0) return BSP_ERR_INVALID_ARG;
+    if (Z == 0) return BSP_OK;
+    for (const void* p : ptrs)
+        if (!p) return BSP_ERR_INVALID_ARG;
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return BSP_ERR_ALIGNMENT;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BSP_ERR_CUDA;
+    if (dev != L->device) return BSP_ERR_INVALID_ARG;
+    return BSP_OK;
+}
+
+// Environment switch (read at every call) that forces the CUDA-core kernels;
+// the tests use it to cover both paths in one process.
+bool force_simt() {
+    const char* e = std::getenv("BSP_FORCE_SIMT");
+    return e && e[0] == '1';
+}
+
+}  // namespace
+
+extern "C" int bsp_sdd(bsp_layout_t L, int dtype, const void* A, const void* B, void* C, int Z,
+                       int K, int trans_a, int trans_b, void* stream) {
+    int rc = check_common(L, dtype, Z, {A, B, C});
+    if (rc) return rc;
+    if (Z < 0 || K < 1 || (trans_a & ~1) || (trans_b & ~1)) return BSP_ERR_INVALID_ARG;
+    if (Z == 0 || L->nnz == 0) return BSP_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (!force_simt()) {
+        rc = bsp::launch_sdd_tc(L, dtype, A, B, C, Z, K, trans_a, trans_b, s);
+        if (rc != BSP_ERR_UNSUPPORTED) return rc;
+    }
+    return bsp::launch_sdd_simt(L, dtype, A, B, C, Z, K, trans_a, trans_b, s);
+}
+
+extern "C" int bsp_dsd(bsp_layout_t L, int dtype, const void* A_sp, const void* B, void* C, int Z,
+                       int N, int trans_a, int trans_b, void* stream) {
+    int rc = check_common(L, dtype, Z, {A_sp, B, C});
+    if (rc) return rc;
+    if (Z < 0 || N < 1 || (trans_a & ~1) || (trans_b & ~1)) return BSP_ERR_INVALID_ARG;
+    if (Z == 0) return BSP_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (!force_simt()) {
+        rc = bsp::launch_dsd_tc(L, dtype, A_sp, B, C, Z, N, trans_a, trans_b, s);
+        if (rc != BSP_ERR_UNSUPPORTED) return rc;
+    }
+    return bsp::launch_dsd_simt(L, dtype, A_sp, B, C, Z, N, trans_a, trans_b, s);
+}
+
+extern "C" int bsp_dds(bsp_layout_t L, int dtype, const void* A, const void* B_sp, void* C, int Z,
+                       int M, int trans_a, int trans_b, void* stream) {
+    int rc = check_common(L, dtype, Z, {A, B_sp, C});
+    if (rc) return rc;
+    if (Z < 0 || M < 1 || (trans_a & ~1) || (trans_b & ~1)) return BSP_ERR_INVALID_ARG;
+    if (Z == 0) return BSP_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (!force_simt()) {
+        rc = bsp::launch_dds_tc(L, dtype, A, B_sp, C, Z, M, trans_a, trans_b, s);
+        if (rc != BSP_ERR_UNSUPPORTED) return rc;
+    }
+    return bsp::launch_dds_simt(L, dtype, A, B_sp, C, Z, M, trans_a, trans_b, s);
+}
+
+extern "C" int bsp_softmax(bsp_layout_t L, int dtype, const void* X, void* Y, int Z, float scale,
+                           int mask_kind, const uint8_t* mask, void* stream) {
+    int rc = check_common(L, dtype, Z, {X, Y});
+    if (rc) return rc;
+    if (Z < 0 || !valid_kind(mask_kind) || !(scale > 0.f) || scale > 3.0e38f) return BSP_ERR_INVALID_ARG;
+    if (mask_kind == BSP_MASK_DENSE && !mask) return BSP_ERR_INVALID_ARG;
+    if (mask_kind == BSP_MASK_DENSE && ((uintptr_t)mask & 15u)) return BSP_ERR_ALIGNMENT;
+    if (Z == 0 || L->nnz == 0) return BSP_OK;
+    return bsp::launch_softmax(L, dtype, X, Y, Z, scale, mask_kind,
+                               mask_kind == BSP_MASK_DENSE ? mask : nullptr, (cudaStream_t)stream);
+}
+
+extern "C" int bsp_attention(bsp_layout_t L, int dtype, const void* Q, const void* K, const void* V,
+                             void* O, int Z, int D, float scale, int mask_kind, const uint8_t* mask,
+                             void* stream) {
+    int rc = check_common(L, dtype, Z, {Q, K, V, O});
+    if (rc) return rc;
+    if (Z < 0 || D < 16 || D > 128 || D % 16 || !valid_kind(mask_kind) || !(scale > 0.f) ||
+        scale > 3.0e38f)
+        return BSP_ERR_INVALID_ARG;
+    if (mask_kind == BSP_MASK_DENSE && !mask) return BSP_ERR_INVALID_ARG;
+    if (mask_kind == BSP_MASK_DENSE && ((uintptr_t)mask & 15u)) return BSP_ERR_ALIGNMENT;
+    if (Z == 0) return BSP_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    const uint8_t* m = mask_kind == BSP_MASK_DENSE ? mask : nullptr;
+    if (!force_simt()) {
+        rc = bsp::launch_attention_tc(L, dtype, Q, K, V, O, Z, D, scale, mask_kind, m, s);
+        if (rc != BSP_ERR_UNSUPPORTED) return rc;
+    }
+    return bsp::launch_attention_simt(L, dtype, Q, K, V, O, Z, D, scale, mask_kind, m, s);
+}
+
+extern "C" int bsp_status_check(bsp_layout_t L, void* stream) {
+    if (!L || !L->on_device) return BSP_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return BSP_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpy(&word, L->view.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return BSP_ERR_CUDA;
+    if (word != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(L->view.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+            return BSP_ERR_CUDA;
+    }
+    return word;
+}
+
+extern "C" const char* bsp_status_string(int status) {
+    switch (status) {
+        case BSP_OK: return "ok";
+        case BSP_ERR_INVALID_ARG: return "invalid argument";
+        case BSP_ERR_UNSUPPORTED: return "unsupported combination";
+        case BSP_ERR_ALIGNMENT: return "tensor pointer not 16-byte aligned";
+        case BSP_ERR_OOM: return "out of memory";
+        case BSP_ERR_CUDA: return "CUDA runtime error";
+        case BSP_ERR_TIMEOUT: return "device wait timed out";
+        case BSP_ERR_DEVICE_CHECK: return "device bounds check failed";
+        default: return "unknown status";
+    }
+}
+
+extern "C" const char* bsp_version(void) { return "libbsp 0.1 (sm_103a)"; }

@@ -1,0 +1,83 @@
+// Internal definitions shared by the host code and the kernels of libbsp.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <vector>
+
+#include "../../include/bsp.h"
+
+// Device-side view of a compiled layout: plain pointers into the handle's
+// single device allocation plus the sizes.  Passed to kernels by value.
+struct LayoutView {
+    const int32_t* row_ptr;       // [H*(nb+1)] CSR row starts (global positions)
+    const int32_t* col_idx;       // [nnz] block-column of each CSR entry
+    const int32_t* blk_id;        // [nnz] block id of each CSR entry
+    const int32_t* col_ptr;       // [H*(nb+1)] CSC column starts
+    const int32_t* row_idx;       // [nnz] block-row of each CSC entry
+    const int32_t* blk_id_csc;    // [nnz] block id of each CSC entry
+    const int32_t* blk_key;       // [nnz] h*nb + i of block id n (its row key)
+    const int32_t* row_order;     // [H*nb] row keys h*nb+i, longest rows first
+    const int32_t* col_order;     // [H*nb] column keys h*nb+j, longest columns first
+    // row tiles of G = 128/B consecutive block-rows (same head) with the union
+    // of their block-columns cut into steps of G slots
+    const int32_t* tile_step_ptr; // [n_tiles+1]
+    const int32_t* tile_order;    // [n_tiles] tile ids, most steps first
+    const int32_t* step_col;      // [n_steps*G] block-column of each slot, -1 = padding
+    const int32_t* step_blk;      // [n_steps*G*G] block id at (row a, slot b), -1 = absent
+    int* status;                  // device status word (0 = OK, else a BSP_ERR_* code)
+    int H, nb, B, S, G, ngroups, n_tiles;
+    int64_t nnz;
+};
+
+struct bsp_layout_s {
+    int H = 0, nb = 0, B = 0, S = 0;
+    int64_t nnz = 0;
+    int device = -1;
+    bool on_device = false;
+
+    std::vector<int32_t> row_ptr, col_idx, blk_id, col_ptr, row_idx, blk_id_csc, blk_key;
+    std::vector<int32_t> row_order, col_order;
+    int max_row_nnz = 0, max_col_nnz = 0;
+
+    int G = 1, ngroups = 0, n_tiles = 0;
+    int64_t n_steps = 0;
+    int max_tile_steps = 0;
+    std::vector<int32_t> tile_step_ptr, tile_order, step_col, step_blk;
+
+    void* dmem = nullptr;  // one device allocation holding every table
+    LayoutView view{};
+};
+
+namespace bsp {
+
+// kernel launchers (return BSP_OK or an error code; they only enqueue work)
+int launch_softmax(const bsp_layout_s* L, int dtype, const void* X, void* Y, int Z, float scale,
+                   int kind, const uint8_t* mask, cudaStream_t s);
+
+int launch_sdd_simt(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z,
+                    int K, int ta, int tb, cudaStream_t s);
+int launch_dsd_simt(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z,
+                    int N, int ta, int tb, cudaStream_t s);
+int launch_dds_simt(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z,
+                    int M, int ta, int tb, cudaStream_t s);
+int launch_attention_simt(const bsp_layout_s* L, int dtype, const void* Q, const void* K,
+                          const void* V, void* O, int Z, int D, float scale, int kind,
+                          const uint8_t* mask, cudaStream_t s);
+
+// tensor-core (tcgen05) paths; return BSP_ERR_UNSUPPORTED when the shape is
+// not covered so that the caller can take the SIMT path instead
+int launch_attention_tc(const bsp_layout_s* L, int dtype, const void* Q, const void* K,
+                        const void* V, void* O, int Z, int D, float scale, int kind,
+                        const uint8_t* mask, cudaStream_t s);
+int launch_sdd_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z,
+                  int K, int ta, int tb, cudaStream_t s);
+int launch_dsd_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z,
+                  int N, int ta, int tb, cudaStream_t s);
+int launch_dds_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z,
+                  int M, int ta, int tb, cudaStream_t s);
+
+int sm_count();  // multiprocessors of the current device (cached per device)
+
+}  // namespace bsp

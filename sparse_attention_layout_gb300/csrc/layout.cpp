@@ -1,0 +1,307 @@
+// Layout compiler: validates a 0/1 block layout and builds the lookup tables
+// and work lists the kernels read.
+//
+// The layout is the tensor of 0s and 1s of "question on blocksparse"
+// (openai/triton issue 117, answer on how a block is defined): one entry per
+// non-overlapping square block of 16, 32, 64 or 128 elements.  Blocks are
+// numbered by their rank in row-major (h, i, j) order, the order in which the
+// block-sparse SDD output stores them.
+#include <algorithm>
+#include <cstring>
+#include <new>
+#include <numeric>
+
+#include "bsp_internal.h"
+
+namespace {
+
+bool valid_block(int B) { return B == 16 || B == 32 || B == 64 || B == 128; }
+
+// Stable order of keys 0..n-1 by descending weight (longest-processing-time
+// first), ties by key.
+std::vector<int32_t> order_by_weight_desc(const std::vector<int32_t>& weight) {
+    std::vector<int32_t> ord(weight.size());
+    std::iota(ord.begin(), ord.end(), 0);
+    std::stable_sort(ord.begin(), ord.end(),
+                     [&](int32_t a, int32_t b) { return weight[a] > weight[b]; });
+    return ord;
+}
+
+int build_tables(bsp_layout_s* L, const uint8_t* lay) {
+    const int H = L->H, nb = L->nb;
+    const int64_t cells = (int64_t)H * nb * nb;
+    std::vector<int64_t> ids(cells, -1);
+    int64_t next = 0;
+    for (int64_t e = 0; e < cells; ++e) {
+        if (lay[e] > 1) return BSP_ERR_INVALID_ARG;
+        if (lay[e]) ids[e] = next++;
+    }
+    if (next > INT32_MAX / 2) return BSP_ERR_UNSUPPORTED;
+    L->nnz = next;
+    const int nnz = (int)next;
+    auto id_at = [&](int h, int i, int j) { return ids[((int64_t)h * nb + i) * nb + j]; };
+
+    // CSR (row) tables
+    L->row_ptr.assign((size_t)H * (nb + 1), 0);
+    L->col_idx.resize(nnz);
+    L->blk_id.resize(nnz);
+    L->blk_key.resize(nnz);
+    std::vector<int32_t> row_len((size_t)H * nb, 0), col_len((size_t)H * nb, 0);
+    int32_t p = 0;
+    for (int h = 0; h < H; ++h) {
+        for (int i = 0; i < nb; ++i) {
+            L->row_ptr[(size_t)h * (nb + 1) + i] = p;
+            for (int j = 0; j < nb; ++j) {
+                int64_t id = id_at(h, i, j);
+                if (id < 0) continue;
+                L->col_idx[p] = j;
+                L->blk_id[p] = (int32_t)id;
+                L->blk_key[id] = h * nb + i;
+                ++p;
+            }
+            row_len[(size_t)h * nb + i] = p - L->row_ptr[(size_t)h * (nb + 1) + i];
+        }
+        L->row_ptr[(size_t)h * (nb + 1) + nb] = p;
+    }
+    // CSC (column) tables
+    L->col_ptr.assign((size_t)H * (nb + 1), 0);
+    L->row_idx.resize(nnz);
+    L->blk_id_csc.resize(nnz);
+    int32_t q = 0;
+    for (int h = 0; h < H; ++h) {
+        for (int j = 0; j < nb; ++j) {
+            L->col_ptr[(size_t)h * (nb + 1) + j] = q;
+            for (int i = 0; i < nb; ++i) {
+                int64_t id = id_at(h, i, j);
+                if (id < 0) continue;
+                L->row_idx[q] = i;
+                L->blk_id_csc[q] = (int32_t)id;
+                ++q;
+            }
+            col_len[(size_t)h * nb + j] = q - L->col_ptr[(size_t)h * (nb + 1) + j];
+        }
+        L->col_ptr[(size_t)h * (nb + 1) + nb] = q;
+    }
+    L->row_order = order_by_weight_desc(row_len);
+    L->col_order = order_by_weight_desc(col_len);
+    L->max_row_nnz = row_len.empty() ? 0 : *std::max_element(row_len.begin(), row_len.end());
+    L->max_col_nnz = col_len.empty() ? 0 : *std::max_element(col_len.begin(), col_len.end());
+
+    // Row tiles for the tensor-core kernels: G = 128/B consecutive block-rows
+    // of one head form a 128-row tile.  Its block-columns are the union of the
+    // rows' columns, cut into steps of G slots (128 key rows per step).
+    const int G = 128 / L->B;
+    L->G = G;
+    L->ngroups = (nb + G - 1) / G;
+    L->n_tiles = H * L->ngroups;
+    L->tile_step_ptr.assign((size_t)L->n_tiles + 1, 0);
+    L->step_col.clear();
+    L->step_blk.clear();
+    std::vector<int32_t> tile_steps((size_t)L->n_tiles, 0);
+    std::vector<uint8_t> in_union((size_t)nb);
+    int64_t steps = 0;
+    for (int h = 0; h < H; ++h) {
+        for (int g = 0; g < L->ngroups; ++g) {
+            const int t = h * L->ngroups + g;
+            std::fill(in_union.begin(), in_union.end(), 0);
+            for (int a = 0; a < G; ++a) {
+                const int i = g * G + a;
+                if (i >= nb) break;
+                for (int pp = L->row_ptr[(size_t)h * (nb + 1) + i];
+                     pp < L->row_ptr[(size_t)h * (nb + 1) + i + 1]; ++pp)
+                    in_union[L->col_idx[pp]] = 1;
+            }
+            std::vector<int32_t> cols;
+            for (int j = 0; j < nb; ++j)
+                if (in_union[j]) cols.push_back(j);
+            const int ns = (int)((cols.size() + G - 1) / G);
+            L->tile_step_ptr[t] = (int32_t)steps;
+            tile_steps[t] = ns;
+            for (int s = 0; s < ns; ++s) {
+                for (int b = 0; b < G; ++b) {
+                    const size_t k = (size_t)s * G + b;
+                    L->step_col.push_back(k < cols.size() ? cols[k] : -1);
+                }
+                for (int a = 0; a < G; ++a) {
+                    const int i = g * G + a;
+                    for (int b = 0; b < G; ++b) {
+                        const size_t k = (size_t)s * G + b;
+                        int32_t id = -1;
+                        if (i < nb && k < cols.size()) id = (int32_t)id_at(h, i, cols[k]);
+                        L->step_blk.push_back(id);
+                    }
+                }
+            }
+            steps += ns;
+        }
+    }
+    L->tile_step_ptr[L->n_tiles] = (int32_t)steps;
+    L->n_steps = steps;
+    L->tile_order = order_by_weight_desc(tile_steps);
+    L->max_tile_steps = tile_steps.empty() ? 0 : *std::max_element(tile_steps.begin(), tile_steps.end());
+    return BSP_OK;
+}
+
+template <typename T>
+size_t padded(size_t n) {
+    return ((n * sizeof(T) + 255) / 256) * 256;
+}
+
+}  // namespace
+
+extern "C" int bsp_layout_plan(const uint8_t* layout, int H, int nb, int block, bsp_layout_t* out) {
+    if (!out) return BSP_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!layout || H < 1 || nb < 1 || !valid_block(block)) return BSP_ERR_INVALID_ARG;
+    if ((int64_t)nb * block > (1 << 24) || (int64_t)H * nb * nb > ((int64_t)1 << 31))
+        return BSP_ERR_UNSUPPORTED;
+    bsp_layout_s* L = new (std::nothrow) bsp_layout_s();
+    if (!L) return BSP_ERR_OOM;
+    L->H = H;
+    L->nb = nb;
+    L->B = block;
+    L->S = nb * block;
+    int rc;
+    try {
+        rc = build_tables(L, layout);
+    } catch (const std::bad_alloc&) {
+        rc = BSP_ERR_OOM;
+    }
+    if (rc != BSP_OK) {
+        delete L;
+        return rc;
+    }
+    *out = L;
+    return BSP_OK;
+}
+
+extern "C" int bsp_layout_compile(const uint8_t* layout, int H, int nb, int block, void* stream,
+                                  bsp_layout_t* out) {
+    int rc = bsp_layout_plan(layout, H, nb, block, out);
+    if (rc != BSP_OK) return rc;
+    bsp_layout_s* L = *out;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaGetDevice(&L->device) != cudaSuccess) {
+        delete L;
+        *out = nullptr;
+        return BSP_ERR_CUDA;
+    }
+    struct Part { const std::vector<int32_t>* v; const int32_t** dst; };
+    LayoutView& V = L->view;
+    Part parts[] = {
+        {&L->row_ptr, &V.row_ptr},       {&L->col_idx, &V.col_idx},
+        {&L->blk_id, &V.blk_id},         {&L->col_ptr, &V.col_ptr},
+        {&L->row_idx, &V.row_idx},       {&L->blk_id_csc, &V.blk_id_csc},
+        {&L->blk_key, &V.blk_key},       {&L->row_order, &V.row_order},
+        {&L->col_order, &V.col_order},   {&L->tile_step_ptr, &V.tile_step_ptr},
+        {&L->tile_order, &V.tile_order}, {&L->step_col, &V.step_col},
+        {&L->step_blk, &V.step_blk},
+    };
+    size_t total = padded<int>(4);  // status word first
+    for (const Part& pt : parts) total += padded<int32_t>(pt.v->size() + 1);
+    char* base = nullptr;
+    if (cudaMalloc((void**)&base, total) != cudaSuccess) {
+        cudaGetLastError();
+        delete L;
+        *out = nullptr;
+        return BSP_ERR_OOM;
+    }
+    L->dmem = base;
+    V.status = (int*)base;
+    size_t off = padded<int>(4);
+    bool ok = cudaMemsetAsync(base, 0, padded<int>(4), s) == cudaSuccess;
+    for (const Part& pt : parts) {
+        int32_t* dst = (int32_t*)(base + off);
+        *pt.dst = dst;
+        if (!pt.v->empty())
+            ok = ok && cudaMemcpyAsync(dst, pt.v->data(), pt.v->size() * sizeof(int32_t),
+                                       cudaMemcpyHostToDevice, s) == cudaSuccess;
+        off += padded<int32_t>(pt.v->size() + 1);
+    }
+    V.H = L->H;
+    V.nb = L->nb;
+    V.B = L->B;
+    V.S = L->S;
+    V.G = L->G;
+    V.ngroups = L->ngroups;
+    V.n_tiles = L->n_tiles;
+    V.nnz = L->nnz;
+    if (!ok) {
+        cudaGetLastError();
+        cudaStreamSynchronize(s);
+        cudaFree(base);
+        delete L;
+        *out = nullptr;
+        return BSP_ERR_CUDA;
+    }
+    L->on_device = true;
+    return BSP_OK;
+}
+
+extern "C" int bsp_layout_destroy(bsp_layout_t L) {
+    if (!L) return BSP_OK;
+    int rc = BSP_OK;
+    if (L->dmem) {
+        int cur = -1;
+        cudaGetDevice(&cur);
+        if (cur != L->device) cudaSetDevice(L->device);
+        if (cudaDeviceSynchronize() != cudaSuccess) rc = BSP_ERR_CUDA;
+        if (cudaFree(L->dmem) != cudaSuccess) rc = BSP_ERR_CUDA;
+        if (cur >= 0 && cur != L->device) cudaSetDevice(cur);
+    }
+    delete L;
+    return rc;
+}
+
+extern "C" int bsp_layout_info(bsp_layout_t L, int* H, int* nb, int* block, int64_t* nnz) {
+    if (!L) return BSP_ERR_INVALID_ARG;
+    if (H) *H = L->H;
+    if (nb) *nb = L->nb;
+    if (block) *block = L->B;
+    if (nnz) *nnz = L->nnz;
+    return BSP_OK;
+}
+
+extern "C" int bsp_layout_get_luts(bsp_layout_t L, int32_t* row_ptr, int32_t* col_idx,
+                                   int32_t* blk_id, int32_t* col_ptr, int32_t* row_idx,
+                                   int32_t* blk_id_csc) {
+    if (!L) return BSP_ERR_INVALID_ARG;
+    struct Out { int32_t* dst; const std::vector<int32_t>* host; const int32_t* dev; };
+    Out outs[] = {{row_ptr, &L->row_ptr, L->view.row_ptr},
+                  {col_idx, &L->col_idx, L->view.col_idx},
+                  {blk_id, &L->blk_id, L->view.blk_id},
+                  {col_ptr, &L->col_ptr, L->view.col_ptr},
+                  {row_idx, &L->row_idx, L->view.row_idx},
+                  {blk_id_csc, &L->blk_id_csc, L->view.blk_id_csc}};
+    if (L->on_device) {
+        if (cudaDeviceSynchronize() != cudaSuccess) return BSP_ERR_CUDA;
+    }
+    for (const Out& o : outs) {
+        if (!o.dst || o.host->empty()) continue;
+        const size_t bytes = o.host->size() * sizeof(int32_t);
+        if (L->on_device) {
+            if (cudaMemcpy(o.dst, o.dev, bytes, cudaMemcpyDeviceToHost) != cudaSuccess)
+                return BSP_ERR_CUDA;
+        } else {
+            std::memcpy(o.dst, o.host->data(), bytes);
+        }
+    }
+    return BSP_OK;
+}
+
+extern "C" int bsp_layout_tiles(bsp_layout_t L, int* G, int* n_tiles, int64_t* n_steps,
+                                int32_t* tile_step_ptr, int32_t* tile_order, int32_t* step_col,
+                                int32_t* step_blk) {
+    if (!L) return BSP_ERR_INVALID_ARG;
+    if (G) *G = L->G;
+    if (n_tiles) *n_tiles = L->n_tiles;
+    if (n_steps) *n_steps = L->n_steps;
+    auto put = [](int32_t* dst, const std::vector<int32_t>& v) {
+        if (dst && !v.empty()) std::memcpy(dst, v.data(), v.size() * sizeof(int32_t));
+    };
+    put(tile_step_ptr, L->tile_step_ptr);
+    put(tile_order, L->tile_order);
+    put(step_col, L->step_col);
+    put(step_blk, L->step_blk);
+    return BSP_OK;
+}

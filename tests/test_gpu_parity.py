@@ -1,0 +1,254 @@
+"""GPU parity: every op through the C ABI against the fp64 oracle on the same
+seeded inputs, at sizes spanning several tiles with ragged tails, each block
+size, each dtype, each mask kind and both kernel paths (tensor-core where it
+applies, CUDA-core forced with BSP_FORCE_SIMT=1).
+
+Tolerance (normwise max |g - r| / max |r|): 1e-5 for fp32 outputs, 2e-2 for
+bf16 / fp16 outputs."""
+
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import TOL, assert_close, dev, normwise_err, to_np
+from sparse_attention_layout_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+
+
+@pytest.fixture(scope="module")
+def bsp():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from sparse_attention_layout_gb300 import build
+    build.build()
+    from sparse_attention_layout_gb300 import bsp as m
+    return m
+
+
+@pytest.fixture(params=["tc", "simt"])
+def path(request, monkeypatch):
+    if request.param == "simt":
+        monkeypatch.setenv("BSP_FORCE_SIMT", "1")
+    else:
+        monkeypatch.delenv("BSP_FORCE_SIMT", raising=False)
+    return request.param
+
+
+def rlayout(H, nb, p, seed, diag=False):
+    lay = (np.random.default_rng(seed).random((H, nb, nb)) < p).astype(np.uint8)
+    if diag:
+        lay[:, np.arange(nb), np.arange(nb)] = 1
+    if nb > 3:
+        lay[0, 2, :] = 0   # an empty block-row
+        lay[0, :, 1] = 0   # an empty block-column
+    return lay
+
+
+def randn(shape, dtype, seed):
+    return W.randn(shape, {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}[dtype], seed)
+
+
+# ----------------------------------------------------------- softmax ----
+
+@pytest.mark.parametrize("B", [16, 32, 64, 128])
+@pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("kind", [0, 1, 2])
+def test_softmax(bsp, oracle, B, dt, kind):
+    dtype = DTYPES[dt]
+    H, Z = 2, 2
+    nb = max(3, 512 // B) + 1
+    S = nb * B
+    lay = rlayout(H, nb, 0.4, B + kind, diag=True)
+    L = bsp.bsp_layout_compile(lay, B)
+    mask = W.random_mask(S, 0.8, 3) if kind == 1 else None
+    X = randn((Z, L.nnz, B, B), dtype, 10 + B)
+    Y = bsp.bsp_softmax(L, dev(X), scale=0.3, mask_kind=kind,
+                        mask=None if mask is None else dev(torch.from_numpy(mask)))
+    torch.cuda.synchronize()
+    want = oracle.softmax(lay, B, X, 0.3, kind, mask)
+    assert_close(to_np(Y), want, dtype, f"softmax B={B} {dt} kind={kind}")
+    assert bsp.bsp_status_check(L) == 0
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_softmax_long_rows_and_in_place(bsp, oracle, dt):
+    # rows longer than the register-resident path (two-pass online path)
+    dtype = DTYPES[dt]
+    B, nb, H = 16, 80, 1
+    lay = np.ones((H, nb, nb), np.uint8)
+    lay[0, 5, 7:] = 0
+    L = bsp.bsp_layout_compile(lay, B)
+    X = randn((1, L.nnz, B, B), dtype, 21)
+    Xd = dev(X)
+    bsp.bsp_softmax(L, Xd, Xd, scale=1.7, mask_kind=2)
+    torch.cuda.synchronize()
+    want = oracle.softmax(lay, B, X, 1.7, 2)
+    assert_close(to_np(Xd), want, dtype, "softmax long/in-place")
+
+
+# --------------------------------------------------------------- SDD ----
+
+@pytest.mark.parametrize("B", [16, 32, 64, 128])
+@pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("trans", [(0, 1), (0, 0), (1, 0), (1, 1)])
+def test_sdd(bsp, oracle, path, B, dt, trans):
+    dtype = DTYPES[dt]
+    ta, tb = trans
+    Z, H, K = 2, 3, 64 if B < 128 else 128
+    nb = max(3, 384 // B) + 1
+    S = nb * B
+    lay = rlayout(H, nb, 0.35, B, diag=True)
+    L = bsp.bsp_layout_compile(lay, B)
+    A = randn((Z, H, K, S) if ta else (Z, H, S, K), dtype, 31)
+    Bm = randn((Z, H, S, K) if tb else (Z, H, K, S), dtype, 32)
+    C = bsp.bsp_sdd(L, dev(A), dev(Bm), trans_a=ta, trans_b=tb)
+    torch.cuda.synchronize()
+    want = oracle.sdd(lay, B, A, Bm, ta, tb)
+    assert_close(to_np(C), want, dtype, f"sdd B={B} {dt} trans={trans} {path}")
+
+
+def test_sdd_leaves_absent_blocks_untouched(bsp, path):
+    # the output has exactly nnz blocks; guard regions around it keep a canary
+    B, H, nb, Z, K = 64, 2, 6, 2, 64
+    lay = rlayout(H, nb, 0.3, 5, diag=True)
+    L = bsp.bsp_layout_compile(lay, B)
+    n = Z * L.nnz * B * B
+    guard = 4096
+    buf = torch.full((n + 2 * guard,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    C = buf[guard:guard + n].view(Z, L.nnz, B, B)
+    A = dev(randn((Z, H, nb * B, K), torch.bfloat16, 6))
+    bsp.bsp_sdd(L, A, A, C)
+    torch.cuda.synchronize()
+    assert torch.isnan(buf[:guard]).all() and torch.isnan(buf[guard + n:]).all()
+    assert torch.isfinite(C).all()
+
+
+# --------------------------------------------------------------- DSD ----
+
+@pytest.mark.parametrize("B", [16, 32, 64, 128])
+@pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("trans", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_dsd(bsp, oracle, path, B, dt, trans):
+    dtype = DTYPES[dt]
+    ta, tb = trans
+    Z, H, N = 2, 2, 200  # N not a multiple of the column tile
+    nb = max(3, 384 // B) + 1
+    S = nb * B
+    lay = rlayout(H, nb, 0.35, 40 + B)
+    L = bsp.bsp_layout_compile(lay, B)
+    Asp = randn((Z, L.nnz, B, B), dtype, 41)
+    Bd = randn((Z, H, N, S) if tb else (Z, H, S, N), dtype, 42)
+    C = bsp.bsp_dsd(L, dev(Asp), dev(Bd), trans_a=ta, trans_b=tb)
+    torch.cuda.synchronize()
+    want = oracle.dsd(lay, B, Asp, Bd, ta, tb)
+    assert_close(to_np(C), want, dtype, f"dsd B={B} {dt} trans={trans} {path}")
+
+
+# --------------------------------------------------------------- DDS ----
+
+@pytest.mark.parametrize("B", [16, 32, 64, 128])
+@pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("trans", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_dds(bsp, oracle, path, B, dt, trans):
+    dtype = DTYPES[dt]
+    ta, tb = trans
+    Z, H, M = 2, 2, 200
+    nb = max(3, 384 // B) + 1
+    S = nb * B
+    lay = rlayout(H, nb, 0.35, 50 + B)
+    L = bsp.bsp_layout_compile(lay, B)
+    Bsp = randn((Z, L.nnz, B, B), dtype, 51)
+    Ad = randn((Z, H, S, M) if ta else (Z, H, M, S), dtype, 52)
+    C = bsp.bsp_dds(L, dev(Ad), dev(Bsp), trans_a=ta, trans_b=tb)
+    torch.cuda.synchronize()
+    want = oracle.dds(lay, B, Ad, Bsp, ta, tb)
+    assert_close(to_np(C), want, dtype, f"dds B={B} {dt} trans={trans} {path}")
+
+
+# --------------------------------------------------------- attention ----
+
+@pytest.mark.parametrize("B", [16, 32, 64, 128])
+@pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("kind", [0, 1, 2])
+def test_attention(bsp, oracle, path, B, dt, D, kind):
+    dtype = DTYPES[dt]
+    Z, H = 2, 2
+    nb = max(3, 512 // B) + 1
+    S = nb * B
+    lay = rlayout(H, nb, 0.3, 60 + B + kind, diag=(kind == 2))
+    L = bsp.bsp_layout_compile(lay, B)
+    mask = W.random_mask(S, 0.8, 61) if kind == 1 else None
+    Q, K, V = (randn((Z, H, S, D), dtype, 62 + k) for k in range(3))
+    scale = 1.0 / np.sqrt(D)
+    O = bsp.bsp_attention(L, dev(Q), dev(K), dev(V), scale=scale, mask_kind=kind,
+                          mask=None if mask is None else dev(torch.from_numpy(mask)))
+    torch.cuda.synchronize()
+    want = oracle.attention(lay, B, Q, K, V, scale, kind, mask)
+    assert_close(to_np(O), want, dtype, f"attention B={B} {dt} D={D} kind={kind} {path}")
+    assert bsp.bsp_status_check(L) == 0
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_unfused_chain_matches_oracle(bsp, oracle, dt):
+    dtype = DTYPES[dt]
+    B, H, Z, D = 64, 2, 2, 64
+    nb = 7
+    lay = rlayout(H, nb, 0.4, 70, diag=True)
+    L = bsp.bsp_layout_compile(lay, B)
+    Q, K, V = (randn((Z, H, nb * B, D), dtype, 71 + k) for k in range(3))
+    O = bsp.attention_unfused(L, dev(Q), dev(K), dev(V), 0.125, 2)
+    torch.cuda.synchronize()
+    want = oracle.attention(lay, B, Q, K, V, 0.125, 2)
+    assert_close(to_np(O), want, dtype, "unfused chain")
+
+
+def test_edge_empty_layout_and_zero_batch(bsp, oracle):
+    B, H, nb, D = 64, 2, 4, 64
+    lay = np.zeros((H, nb, nb), np.uint8)
+    L = bsp.bsp_layout_compile(lay, B)
+    Q = torch.randn(1, H, nb * B, D, device="cuda", dtype=torch.bfloat16)
+    O = torch.full_like(Q, 7.0)
+    bsp.bsp_attention(L, Q, Q, Q, O, scale=0.1)
+    torch.cuda.synchronize()
+    assert (O == 0).all()  # no kept entries: rows are 0
+    C = torch.full((1, H, nb * B, 32), 5.0, device="cuda", dtype=torch.bfloat16)
+    bsp.bsp_dsd(L, torch.zeros(1, 1, B, B, device="cuda", dtype=torch.bfloat16),
+                torch.randn(1, H, nb * B, 32, device="cuda", dtype=torch.bfloat16), C)
+    torch.cuda.synchronize()
+    assert (C == 0).all()
+    # Z = 0 is a no-op
+    empty = torch.empty(0, H, nb * B, D, device="cuda", dtype=torch.bfloat16)
+    bsp.bsp_attention(L, empty, empty, empty, empty, scale=0.1)
+
+
+def test_error_codes_on_device(bsp):
+    B, H, nb = 32, 1, 4
+    L = bsp.bsp_layout_compile(np.ones((H, nb, nb), np.uint8), B)
+    Q = torch.randn(1, H, nb * B, 64, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(bsp.BspError) as e:   # D not a multiple of 16
+        bsp.bsp_attention(L, Q[..., :40].contiguous(), Q[..., :40].contiguous(),
+                          Q[..., :40].contiguous(), scale=0.1)
+    assert e.value.code == -1
+    raw = torch.empty(Q.numel() * 2 + 8, dtype=torch.bfloat16, device="cuda")
+    mis = raw[1:1 + Q.numel()].view_as(Q)    # 2-byte offset: not 16-byte aligned
+    with pytest.raises(bsp.BspError) as e:
+        bsp.bsp_attention(L, mis, Q, Q, scale=0.1)
+    assert e.value.code == -3
+    with pytest.raises(bsp.BspError) as e:   # dense mask kind without a mask
+        bsp.bsp_softmax(L, torch.empty(1, L.nnz, B, B, device="cuda"), scale=1.0, mask_kind=1)
+    assert e.value.code == -1
+
+
+def test_device_luts_bit_exact(bsp, oracle):
+    for w in W.ATTENTION_WORKLOADS.values():
+        lay = w.layout()
+        L = bsp.bsp_layout_compile(lay, w.B)
+        got, want = L.luts(), oracle.luts(lay)
+        for k in want:
+            assert np.array_equal(got[k], want[k]), (w.name, k)
