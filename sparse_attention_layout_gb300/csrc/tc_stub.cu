@@ -2,8 +2,6 @@
 #include "bsp_internal.h"
 
 namespace bsp {
-int launch_attention_tc(const bsp_layout_s*, int, const void*, const void*, const void*, void*, int,
-                        int, float, int, const uint8_t*, cudaStream_t) { return BSP_ERR_UNSUPPORTED; }
 int launch_sdd_tc(const bsp_layout_s*, int, const void*, const void*, void*, int, int, int, int,
                   cudaStream_t) { return BSP_ERR_UNSUPPORTED; }
 int launch_dsd_tc(const bsp_layout_s*, int, const void*, const void*, void*, int, int, int, int,
