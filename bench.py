@@ -43,6 +43,8 @@ def parse():
     p.add_argument("--workload", default="band", choices=["band", "strided", "bigbird", "tiny"])
     p.add_argument("--no-ops", action="store_true", help="skip the per-op section")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="target oracle CPU time")
+    p.add_argument("--skip-cpu", action="store_true", help="no CPU-baseline leg (profiling runs)")
+    p.add_argument("--skip-e2e", action="store_true", help="no end-to-end leg (profiling runs)")
     return p.parse_args()
 
 
@@ -359,10 +361,12 @@ def run_ours(args):
         bsp.bsp_attention(L, q, k, v, o, w.scale, w.mask_kind)
         Oh.copy_(o, non_blocking=True)
 
-    e2e_steps = max(3, min(args.steps, 20))
-    for _ in range(2):
-        e2e_step()
-    e2e_ms = time_launches(e2e_step, e2e_steps, stream)
+    e2e_ms = None
+    if not args.skip_e2e:
+        e2e_steps = max(3, min(args.steps, 20))
+        for _ in range(2):
+            e2e_step()
+        e2e_ms = time_launches(e2e_step, e2e_steps, stream)
     h2d = 3 * Qc.numel() * Qc.element_size()
     d2h = Oh.numel() * Oh.element_size()
 
@@ -375,7 +379,11 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
         return
-    cpu_val, cpu_rows, cpu_s, cores = cpu_oracle_sample(w, lay, Qc, Kc, Vc, args.cpu_seconds)
+    cpu = None
+    if not args.skip_cpu:
+        cpu_val, cpu_rows, cpu_s, cores = cpu_oracle_sample(w, lay, Qc, Kc, Vc, args.cpu_seconds)
+        cpu = {"value": cpu_val, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{cpu_rows} random rows of {w.Z * w.H * w.S} ({cpu_s:.1f} s, fp64, OpenMP)"}
     if world > 1:
         dist.barrier()
     peak = pk["bf16_tflops"] if w.dtype != "f32" else None
@@ -392,11 +400,10 @@ def run_ours(args):
             "traffic": traffic_for("attention", w.name),
             "algorithmic_flops_per_launch": flops,
         },
-        "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "cpu_baseline": {"value": cpu_val, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"{cpu_rows} random rows of {w.Z * w.H * w.S} "
-                                   f"({cpu_s:.1f} s, fp64, OpenMP)"},
+        "e2e": None if e2e_ms is None else {
+            "value": flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "cpu_baseline": cpu,
         "clocks": clk.summary(),
         "lib": bsp.lib_path(),
     }

@@ -1,0 +1,428 @@
+// Fused block-sparse attention on tcgen05 tensor cores (bf16 / fp16 in,
+// fp32 accumulate): the SDD -> softmax -> DSD chain of "question on
+// blocksparse" (openai/triton issue 117) in one pass that never writes the
+// scores, with the online-softmax recurrence of the Triton-Puzzles blog,
+// Puzzle 9 "Simple FlashAttention" (running max m, running sum l, output
+// rescaled by exp(m_old - m_new), divided by l at the end).
+//
+// Work: one row tile = 128 query rows (G = 128/B consecutive block-rows of one
+// head) x one batch entry.  Its key blocks are the union of the block-rows'
+// columns, visited 128 key rows (G blocks) per step; a (row block, key block)
+// pair that is not in the layout is masked to -inf, as are entries the intra-
+// block mask removes.  Persistent CTAs walk the tiles longest-first.
+//
+// Roles (192 threads, one CTA per SM):
+//   warp 0      TMA producer: Q tile (2 stages), K and V tiles (2 stages each)
+//   warp 1      TMEM owner and MMA issuer (one thread):
+//                 S[g%2] = Q K^T   (M=128, N=128, K=D)
+//                 O     += P V     (M=128, N=D,   K=128), V taken MN-major
+//   warps 2..5  softmax: thread = one query row = one TMEM lane.  Reads S from
+//               TMEM, masks, keeps (m, l), writes P (bf16/fp16) to shared
+//               memory in the K-major swizzled layout, rescales O in TMEM only
+//               when the row max grew by more than 2^8 (the final O / l is
+//               exact either way), and runs the epilogue O / l -> global.
+// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D).
+#pragma once
+
+#include <algorithm>
+#include <type_traits>
+
+#include "common.cuh"
+#include "tc_common.cuh"
+
+namespace bsp {
+namespace attn {
+
+using namespace tc;
+
+constexpr int kThreads = 192;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when max grows by > 256x
+
+template <int D>
+struct AttnSmem {
+    static constexpr int KP = D / 64;                 // 64-column panels per 128-row tile
+    static constexpr int kTile = 128 * D * 2;         // bytes of one 128 x D tile
+    static constexpr int kQ = 0;                      // 2 stages
+    static constexpr int kK = kQ + 2 * kTile;         // 2 stages
+    static constexpr int kV = kK + 2 * kTile;         // 2 stages
+    static constexpr int kP = kV + 2 * kTile;         // 128 x 128 probabilities
+    static constexpr int kBytes = kP + 128 * 128 * 2;
+    static constexpr int kAlloc = kBytes + 1024;      // slack for 1024-byte alignment
+};
+
+struct AttnArgs {
+    LayoutView L;
+    void* O;
+    const uint8_t* mask;
+    int Z;
+    int kind;
+    float c2;  // scale * log2(e)
+};
+
+template <typename T, int BLK, int D, int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const AttnArgs args) {
+    using SM = AttnSmem<D>;
+    constexpr int G = 128 / BLK;
+    constexpr int KP = SM::KP;
+    constexpr uint32_t kTileBytes = SM::kTile;
+    constexpr uint32_t kIdescQK = idesc_f16(128, 128, std::is_same<T, __nv_bfloat16>::value, 0, 0);
+    constexpr uint32_t kIdescPV = idesc_f16(128, D, std::is_same<T, __nv_bfloat16>::value, 0, 1);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    __shared__ uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2];
+    __shared__ uint64_t s_full[2], p_full, pv_done;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+
+    const LayoutView& L = args.L;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    Abort ab{&abort_flag, L.status};
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_empty[i], 1);
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+        }
+        mbar_init(&p_full, 4);
+        mbar_init(&pv_done, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tS = tmem_base;        // S buffers at columns 0 and 128
+    const uint32_t tO = tmem_base + 256;  // O at column 256
+
+    const int64_t total = (int64_t)args.Z * L.n_tiles;
+    const int S = L.S;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer ----
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            uint32_t q_it = 0, kv_it = 0;
+            for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+                const int tile = L.tile_order[w / args.Z];
+                const int z = (int)(w % args.Z);
+                const int h = tile / L.ngroups, gq = tile % L.ngroups;
+                const int s0 = L.tile_step_ptr[tile], ns = L.tile_step_ptr[tile + 1] - s0;
+                if (ns == 0) continue;
+                const int64_t zh = (int64_t)z * L.H + h;
+                const uint32_t qs = q_it & 1;
+                if (!mbar_wait(&q_empty[qs], ((q_it >> 1) & 1) ^ 1, ab)) break;
+                mbar_arrive_expect_tx(&q_full[qs], kTileBytes);
+                for (int p = 0; p < KP; ++p)
+                    tma_load_2d(smem_u32(smem + SM::kQ + qs * kTileBytes + p * 16384), &tmQ, p * 64,
+                                (int32_t)(zh * S + gq * 128), &q_full[qs]);
+                ++q_it;
+                for (int n = 0; n < ns; ++n) {
+                    const int s = s0 + n;
+                    const uint32_t st = kv_it & 1, ph = ((kv_it >> 1) & 1) ^ 1;
+                    int cols[G];
+#pragma unroll
+                    for (int b = 0; b < G; ++b) {
+                        const int c = L.step_col[s * G + b];
+                        cols[b] = c >= 0 ? c : L.step_col[s * G];  // padding slot: any valid block
+                    }
+                    if (!mbar_wait(&k_empty[st], ph, ab)) goto producer_done;
+                    mbar_arrive_expect_tx(&k_full[st], kTileBytes);
+#pragma unroll
+                    for (int b = 0; b < G; ++b)
+                        for (int p = 0; p < KP; ++p)
+                            tma_load_2d(smem_u32(smem + SM::kK + st * kTileBytes + p * 16384 + b * BLK * 128), &tmK,
+                                        p * 64, (int32_t)(zh * S + (int64_t)cols[b] * BLK), &k_full[st]);
+                    if (!mbar_wait(&v_empty[st], ph, ab)) goto producer_done;
+                    mbar_arrive_expect_tx(&v_full[st], kTileBytes);
+#pragma unroll
+                    for (int b = 0; b < G; ++b)
+                        for (int p = 0; p < KP; ++p)
+                            tma_load_2d(smem_u32(smem + SM::kV + st * kTileBytes + p * 16384 + b * BLK * 128), &tmV,
+                                        p * 64, (int32_t)(zh * S + (int64_t)cols[b] * BLK), &v_full[st]);
+                    ++kv_it;
+                }
+            }
+        producer_done:;
+        }
+    } else if (warp == 1) {
+        // --------------------------------------------------- MMA issuer ----
+        if (lane == 0) {
+            uint32_t q_it = 0, g = 0;
+            bool pending = false, pending_first = false;
+            uint32_t pending_g = 0;
+            auto issue_pv = [&](uint32_t gp, bool first) -> bool {
+                if (!mbar_wait(&p_full, gp & 1, ab)) return false;
+                if (!mbar_wait(&v_full[gp & 1], (gp >> 1) & 1, ab)) return false;
+                tc_fence_after();
+                const uint32_t pbase = smem_u32(smem + SM::kP);
+                const uint32_t vbase = smem_u32(smem + SM::kV + (gp & 1) * kTileBytes);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t ad = smem_desc(pbase + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, kSw128);
+                    const uint64_t bd = smem_desc(vbase + ks * 2048, 128 * 128, 1024, kSw128);
+                    mma_f16(tO, ad, bd, kIdescPV, (ks > 0 || !first) ? 1u : 0u);
+                }
+                mma_commit(&pv_done);
+                mma_commit(&v_empty[gp & 1]);
+                return true;
+            };
+            for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+                const int tile = L.tile_order[w / args.Z];
+                const int ns = L.tile_step_ptr[tile + 1] - L.tile_step_ptr[tile];
+                if (ns == 0) continue;
+                const uint32_t qs = q_it & 1;
+                if (!mbar_wait(&q_full[qs], (q_it >> 1) & 1, ab)) goto mma_done;
+                for (int n = 0; n < ns; ++n, ++g) {
+                    const uint32_t st = g & 1;
+                    if (!mbar_wait(&k_full[st], (g >> 1) & 1, ab)) goto mma_done;
+                    tc_fence_after();
+                    const uint32_t qbase = smem_u32(smem + SM::kQ + qs * kTileBytes);
+                    const uint32_t kbase = smem_u32(smem + SM::kK + st * kTileBytes);
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_f16(tS + (g & 1) * 128, smem_desc(qbase + off, 16, 1024, kSw128),
+                                smem_desc(kbase + off, 16, 1024, kSw128), kIdescQK, ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&s_full[g & 1]);
+                    mma_commit(&k_empty[st]);
+                    if (n == ns - 1) mma_commit(&q_empty[qs]);
+                    if (pending && !issue_pv(pending_g, pending_first)) goto mma_done;
+                    pending = true;
+                    pending_g = g;
+                    pending_first = (n == 0);
+                }
+                ++q_it;
+            }
+            if (pending) issue_pv(pending_g, pending_first);
+        mma_done:;
+        }
+    } else {
+        // ------------------------------------------- softmax / epilogue ----
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;  // query row inside the tile = TMEM lane
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const int r_in = row % BLK, a = row / BLK;
+        uint32_t g = 0;
+        for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+            const int tile = L.tile_order[w / args.Z];
+            const int z = (int)(w % args.Z);
+            const int h = tile / L.ngroups, gq = tile % L.ngroups;
+            const int s0 = L.tile_step_ptr[tile], ns = L.tile_step_ptr[tile + 1] - s0;
+            const int rb = gq * G + a;        // block-row of this thread's query row
+            const bool row_valid = rb < L.nb;
+            const int rseq = gq * 128 + row;  // query position inside the sequence
+            T* orow = reinterpret_cast<T*>(args.O) + (((int64_t)z * L.H + h) * S + rseq) * D;
+            float m = -INFINITY, l = 0.f;
+            for (int n = 0; n < ns; ++n, ++g) {
+                const int s = s0 + n;
+                bool ok = mbar_wait(&s_full[g & 1], (g >> 1) & 1, ab);
+                if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
+                tc_fence_after();
+                // raw scores (the scale is applied inside the exponent below)
+                float x[128];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    tmem_ld32(tS + (g & 1) * 128 + lane_base + c * 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(reinterpret_cast<uint32_t*>(x) + 32 * c));
+                tmem_wait_ld();
+                // masks: absent (row block, key block) pairs and intra-block masks
+#pragma unroll
+                for (int b = 0; b < G; ++b) {
+                    const int blk = L.step_blk[(s * G + a) * G + b];
+                    const int cb = L.step_col[s * G + b];
+                    if (blk < 0) {
+#pragma unroll
+                        for (int k = 0; k < BLK; ++k) x[b * BLK + k] = -INFINITY;
+                    } else if (KIND == BSP_MASK_DIAG_CAUSAL) {
+                        if (cb == rb) {
+#pragma unroll
+                            for (int k = 0; k < BLK; ++k)
+                                if (k > r_in) x[b * BLK + k] = -INFINITY;
+                        }
+                    } else if (KIND == BSP_MASK_DENSE) {
+                        const uint8_t* mp = args.mask + (int64_t)rseq * S + (int64_t)cb * BLK;
+#pragma unroll
+                        for (int v = 0; v < BLK / 16; ++v) {
+                            uint4 mv = *reinterpret_cast<const uint4*>(mp + v * 16);
+                            const uint8_t* mb = reinterpret_cast<const uint8_t*>(&mv);
+#pragma unroll
+                            for (int k = 0; k < 16; ++k)
+                                if (!mb[k]) x[b * BLK + v * 16 + k] = -INFINITY;
+                        }
+                    }
+                }
+                // row max of the raw scores: 8 independent chains, then a tree
+                float mx8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mx8[k] = x[k];
+#pragma unroll
+                for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                // m is kept in the scaled log2 domain (scale > 0 commutes with max)
+                const float m_new = fmaxf(m, mx * args.c2);
+                const bool need = m_new > m + kRescaleThreshold;  // also true for the first finite max
+                const float alpha = need ? ((m == -INFINITY) ? 0.f : ex2_approx(m - m_new)) : 1.f;
+                if (need) m = m_new;
+                const float msub = (m == -INFINITY) ? 0.f : m;
+                // p = 2^(s * c2 - m): one FFMA and one MUFU.EX2 per entry
+                float rs8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) rs8[k] = 0.f;
+                uint32_t pk[64];
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const float p0 = ex2_approx(fmaf(x[2 * c], args.c2, -msub));
+                    const float p1 = ex2_approx(fmaf(x[2 * c + 1], args.c2, -msub));
+                    rs8[(2 * c) & 7] += p0;
+                    rs8[(2 * c + 1) & 7] += p1;
+                    pk[c] = Pack2<T>::pack(p0, p1);
+                }
+                const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+                l = l * alpha + rs;
+                // P buffer and O are free once the previous P V has completed
+                if (g > 0) {
+                    ok = mbar_wait(&pv_done, (g - 1) & 1, ab);
+                    if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
+                    tc_fence_after();
+                }
+                if (n > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(tO + lane_base + c * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
+                        tmem_st32(tO + lane_base + c * 32, r);
+                    }
+                    tmem_wait_st();
+                }
+                // P row -> shared memory, K-major 128-byte swizzle: panel = 64 keys
+                {
+                    uint8_t* prow = smem + SM::kP + row * 128;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const int panel = c >> 3, chunk = c & 7;
+                        uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                        *reinterpret_cast<uint4*>(prow + panel * 16384 + ((chunk ^ (row & 7)) << 4)) = v;
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full);
+            }
+            // epilogue: O / l -> global (rows with nothing kept are 0)
+            if (ns > 0) {
+                bool ok = mbar_wait(&pv_done, (g - 1) & 1, ab);
+                if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
+                tc_fence_after();
+            }
+            {
+                const float inv = l > 0.f ? 1.0f / l : 0.f;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    if (ns > 0) {
+                        tmem_ld32(tO + lane_base + c * 32, r);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) r[k] = 0u;
+                    }
+                    uint32_t o[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        o[k] = Pack2<T>::pack(__uint_as_float(r[2 * k]) * inv, __uint_as_float(r[2 * k + 1]) * inv);
+                    if (row_valid) {
+                        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            dst[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                    }
+                }
+                tc_fence_before();
+            }
+        }
+    softmax_done:;
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+template <typename T, int BLK, int D, int KIND>
+int launch_attn(const bsp_layout_s* Lh, const void* Q, const void* K, const void* V, void* O, int Z,
+                float scale, int kind, const uint8_t* mask, cudaStream_t s) {
+    const int is_bf16 = std::is_same<T, __nv_bfloat16>::value;
+    const uint64_t rows = (uint64_t)Z * Lh->H * Lh->S;
+    CUtensorMap mq, mk, mv;
+    int rc = make_tmap_2d(&mq, Q, is_bf16, rows, D, 128, 64, 128);
+    if (!rc) rc = make_tmap_2d(&mk, K, is_bf16, rows, D, BLK, 64, 128);
+    if (!rc) rc = make_tmap_2d(&mv, V, is_bf16, rows, D, BLK, 64, 128);
+    if (rc) return rc;
+    AttnArgs args{Lh->view, O, mask, Z, kind, scale * kLog2e};
+    auto kern = attention_tc_kernel<T, BLK, D, KIND>;
+    constexpr int smem = AttnSmem<D>::kAlloc;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return BSP_ERR_CUDA;
+    const int64_t total = (int64_t)Z * Lh->n_tiles;
+    const int grid = (int)std::min<int64_t>(total, sm_count());
+    kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, args);
+    return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
+}
+
+template <typename T, int BLK, int KIND>
+int by_d(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, int Z, int D, float scale,
+         int kind, const uint8_t* mask, cudaStream_t s) {
+    if (D == 128) return launch_attn<T, BLK, 128, KIND>(L, Q, K, V, O, Z, scale, kind, mask, s);
+    if (D == 64) return launch_attn<T, BLK, 64, KIND>(L, Q, K, V, O, Z, scale, kind, mask, s);
+    return BSP_ERR_UNSUPPORTED;
+}
+
+template <typename T, int BLK>
+int by_kind(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, int Z, int D,
+            float scale, int kind, const uint8_t* mask, cudaStream_t s) {
+    switch (kind) {
+        case BSP_MASK_NONE: return by_d<T, BLK, BSP_MASK_NONE>(L, Q, K, V, O, Z, D, scale, kind, mask, s);
+        case BSP_MASK_DENSE: return by_d<T, BLK, BSP_MASK_DENSE>(L, Q, K, V, O, Z, D, scale, kind, mask, s);
+        case BSP_MASK_DIAG_CAUSAL:
+            return by_d<T, BLK, BSP_MASK_DIAG_CAUSAL>(L, Q, K, V, O, Z, D, scale, kind, mask, s);
+        default: return BSP_ERR_INVALID_ARG;
+    }
+}
+
+template <typename T>
+int by_block(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, int Z, int D,
+             float scale, int kind, const uint8_t* mask, cudaStream_t s) {
+    switch (L->B) {
+        case 128: return by_kind<T, 128>(L, Q, K, V, O, Z, D, scale, kind, mask, s);
+        case 64: return by_kind<T, 64>(L, Q, K, V, O, Z, D, scale, kind, mask, s);
+        case 32: return by_kind<T, 32>(L, Q, K, V, O, Z, D, scale, kind, mask, s);
+        case 16: return by_kind<T, 16>(L, Q, K, V, O, Z, D, scale, kind, mask, s);
+        default: return BSP_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace attn
+}  // namespace bsp
