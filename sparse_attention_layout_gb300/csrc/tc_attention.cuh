@@ -11,16 +11,18 @@
 // pair that is not in the layout is masked to -inf, as are entries the intra-
 // block mask removes.  Persistent CTAs walk the tiles longest-first.
 //
-// Roles (192 threads, one CTA per SM):
+// Roles (320 threads, one CTA per SM):
 //   warp 0      TMA producer: Q tile (2 stages), K and V tiles (2 stages each)
 //   warp 1      TMEM owner and MMA issuer (one thread):
 //                 S[g%2] = Q K^T   (M=128, N=128, K=D)
 //                 O     += P V     (M=128, N=D,   K=128), V taken MN-major
-//   warps 2..5  softmax: thread = one query row = one TMEM lane.  Reads S from
-//               TMEM, masks, keeps (m, l), writes P (bf16/fp16) to shared
-//               memory in the K-major swizzled layout, rescales O in TMEM only
-//               when the row max grew by more than 2^8 (the final O / l is
-//               exact either way), and runs the epilogue O / l -> global.
+//   warps 2..9  softmax, two warpgroups: thread = one query row = one TMEM
+//               lane, each warpgroup owning half of the row's 128 scores.
+//               Reads S from TMEM, masks, keeps (m, l) (both groups take the
+//               full-row max; partial sums meet per tile), writes P to shared
+//               memory in the K-major swizzled layout, rescales its half of O
+//               in TMEM only when the row max grew by more than 2^8 (the final
+//               O / l is exact either way), and runs the epilogue O / l.
 // TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D).
 #pragma once
 
@@ -35,7 +37,7 @@ namespace attn {
 
 using namespace tc;
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when max grows by > 256x
 
 template <int D>
@@ -73,7 +75,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     __shared__ uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2];
-    __shared__ uint64_t s_full[2], p_full, pv_done;
+    __shared__ uint64_t s_full[2], p_full, pv_done, xchg;
+    __shared__ float lsum[2][128];  // partial row sums [warpgroup][row]
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
@@ -92,7 +95,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
         }
-        mbar_init(&p_full, 4);
+        mbar_init(&p_full, 8);
+        mbar_init(&xchg, 8);
         mbar_init(&pv_done, 1);
         fence_barrier_init();
     }
@@ -213,11 +217,67 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         }
     } else {
         // ------------------------------------------- softmax / epilogue ----
+        // Two warpgroups split each row: both read all 128 scores and take the
+        // full row max (so they make identical decisions without talking), but
+        // warpgroup wg exponentiates and stores only columns [64 wg, 64 wg + 64)
+        // (P panel wg) and owns output columns [wg D/2, wg D/2 + D/2).  The two
+        // partial row sums meet once per tile through shared memory, ordered by
+        // the xchg mbarrier (8 warp arrivals).
+        constexpr int W = BLK < 64 ? BLK : 64;  // columns of one slot inside a half
+        constexpr int LS = 64 / W;              // slots (or slot parts) per half
+        const int sw = warp - 2, wg = sw >> 2;
         const int quad = warp & 3;
         const int row = quad * 32 + lane;  // query row inside the tile = TMEM lane
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const int r_in = row % BLK, a = row / BLK;
-        uint32_t g = 0;
+        uint32_t g = 0, xg = 0;
+        // metadata of one half: block id at (row block a, slot) and block-column, per slot part
+        struct Half {
+            int blk[LS], cb[LS];
+        };
+        auto fetch = [&](int s, int hf, Half& o) {
+#pragma unroll
+            for (int ls = 0; ls < LS; ++ls) {
+                const int b = (hf * 64 + ls * W) / BLK;
+                o.blk[ls] = L.step_blk[(s * G + a) * G + b];
+                o.cb[ls] = L.step_col[s * G + b];
+            }
+        };
+        // mask one half (64 columns) of the row in place
+        auto mask_half = [&](float (&v)[64], int hf, const Half& md, int rb, int rseq) {
+#pragma unroll
+            for (int ls = 0; ls < LS; ++ls) {
+                const int kbase = (hf * 64 + ls * W) % BLK;  // in-block column of v[ls * W]
+                if (KIND == BSP_MASK_DIAG_CAUSAL) {
+                    // keep columns j <= lim: none if the block is absent, j <= r_in - kbase
+                    // inside the diagonal block, all otherwise (branch-free selects)
+                    const int lim = md.blk[ls] < 0 ? -1 : (md.cb[ls] == rb ? r_in - kbase : W);
+#pragma unroll
+                    for (int j = 0; j < W; ++j) v[ls * W + j] = j > lim ? -INFINITY : v[ls * W + j];
+                } else if (md.blk[ls] < 0) {
+#pragma unroll
+                    for (int j = 0; j < W; ++j) v[ls * W + j] = -INFINITY;
+                } else if (KIND == BSP_MASK_DENSE) {
+                    const uint8_t* mp = args.mask + (int64_t)rseq * S + (int64_t)md.cb[ls] * BLK + kbase;
+#pragma unroll
+                    for (int q = 0; q < W / 16; ++q) {
+                        uint4 mv = *reinterpret_cast<const uint4*>(mp + q * 16);
+                        const uint8_t* mb = reinterpret_cast<const uint8_t*>(&mv);
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            if (!mb[k]) v[ls * W + q * 16 + k] = -INFINITY;
+                    }
+                }
+            }
+        };
+        auto max64 = [](const float (&v)[64]) {
+            float m8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m8[k] = v[k];
+#pragma unroll
+            for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], v[c]);
+            return fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        };
         for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
             const int tile = L.tile_order[w / args.Z];
             const int z = (int)(w % args.Z);
@@ -226,55 +286,39 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const int rb = gq * G + a;        // block-row of this thread's query row
             const bool row_valid = rb < L.nb;
             const int rseq = gq * 128 + row;  // query position inside the sequence
-            T* orow = reinterpret_cast<T*>(args.O) + (((int64_t)z * L.H + h) * S + rseq) * D;
+            T* orow = reinterpret_cast<T*>(args.O) + (((int64_t)z * L.H + h) * S + rseq) * D + wg * (D / 2);
             float m = -INFINITY, l = 0.f;
+            Half own, oth, nown, noth;
+            if (ns > 0) {
+                fetch(s0, wg, nown);
+                fetch(s0, wg ^ 1, noth);
+            }
             for (int n = 0; n < ns; ++n, ++g) {
-                const int s = s0 + n;
+                own = nown;
+                oth = noth;
+                if (n + 1 < ns) {  // next step's metadata: latency hidden behind this step
+                    fetch(s0 + n + 1, wg, nown);
+                    fetch(s0 + n + 1, wg ^ 1, noth);
+                }
                 bool ok = mbar_wait(&s_full[g & 1], (g >> 1) & 1, ab);
                 if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
                 tc_fence_after();
-                // raw scores (the scale is applied inside the exponent below)
-                float x[128];
+                // raw scores (the scale is applied inside the exponent): own half x, other half y
+                float x[64], y[64];
+                const uint32_t srow = tS + (g & 1) * 128 + lane_base;
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    tmem_ld32(tS + (g & 1) * 128 + lane_base + c * 32,
+                for (int c = 0; c < 2; ++c) {
+                    tmem_ld32(srow + wg * 64 + c * 32,
                               *reinterpret_cast<uint32_t(*)[32]>(reinterpret_cast<uint32_t*>(x) + 32 * c));
-                tmem_wait_ld();
-                // masks: absent (row block, key block) pairs and intra-block masks
-#pragma unroll
-                for (int b = 0; b < G; ++b) {
-                    const int blk = L.step_blk[(s * G + a) * G + b];
-                    const int cb = L.step_col[s * G + b];
-                    if (blk < 0) {
-#pragma unroll
-                        for (int k = 0; k < BLK; ++k) x[b * BLK + k] = -INFINITY;
-                    } else if (KIND == BSP_MASK_DIAG_CAUSAL) {
-                        if (cb == rb) {
-#pragma unroll
-                            for (int k = 0; k < BLK; ++k)
-                                if (k > r_in) x[b * BLK + k] = -INFINITY;
-                        }
-                    } else if (KIND == BSP_MASK_DENSE) {
-                        const uint8_t* mp = args.mask + (int64_t)rseq * S + (int64_t)cb * BLK;
-#pragma unroll
-                        for (int v = 0; v < BLK / 16; ++v) {
-                            uint4 mv = *reinterpret_cast<const uint4*>(mp + v * 16);
-                            const uint8_t* mb = reinterpret_cast<const uint8_t*>(&mv);
-#pragma unroll
-                            for (int k = 0; k < 16; ++k)
-                                if (!mb[k]) x[b * BLK + v * 16 + k] = -INFINITY;
-                        }
-                    }
+                    tmem_ld32(srow + (wg ^ 1) * 64 + c * 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(reinterpret_cast<uint32_t*>(y) + 32 * c));
                 }
-                // row max of the raw scores: 8 independent chains, then a tree
-                float mx8[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) mx8[k] = x[k];
-#pragma unroll
-                for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-                // m is kept in the scaled log2 domain (scale > 0 commutes with max)
+                tmem_wait_ld();
+                mask_half(x, wg, own, rb, rseq);
+                mask_half(y, wg ^ 1, oth, rb, rseq);
+                const float mx = fmaxf(max64(x), max64(y));
+                // m is kept in the scaled log2 domain (scale > 0 commutes with max); both
+                // warpgroups see the same maxima, so they take the same decisions
                 const float m_new = fmaxf(m, mx * args.c2);
                 const bool need = m_new > m + kRescaleThreshold;  // also true for the first finite max
                 const float alpha = need ? ((m == -INFINITY) ? 0.f : ex2_approx(m - m_new)) : 1.f;
@@ -284,9 +328,9 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 float rs8[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) rs8[k] = 0.f;
-                uint32_t pk[64];
+                uint32_t pk[32];
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
+                for (int c = 0; c < 32; ++c) {
                     const float p0 = ex2_approx(fmaf(x[2 * c], args.c2, -msub));
                     const float p1 = ex2_approx(fmaf(x[2 * c + 1], args.c2, -msub));
                     rs8[(2 * c) & 7] += p0;
@@ -294,7 +338,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     pk[c] = Pack2<T>::pack(p0, p1);
                 }
                 const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-                l = l * alpha + rs;
+                l = l * alpha + rs;  // partial sum of this half
                 // P buffer and O are free once the previous P V has completed
                 if (g > 0) {
                     ok = mbar_wait(&pv_done, (g - 1) & 1, ab);
@@ -303,24 +347,24 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 }
                 if (n > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int c = 0; c < D / 64; ++c) {
                         uint32_t r[32];
-                        tmem_ld32(tO + lane_base + c * 32, r);
+                        const uint32_t ta = tO + lane_base + wg * (D / 2) + c * 32;
+                        tmem_ld32(ta, r);
                         tmem_wait_ld();
 #pragma unroll
                         for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
-                        tmem_st32(tO + lane_base + c * 32, r);
+                        tmem_st32(ta, r);
                     }
                     tmem_wait_st();
                 }
-                // P row -> shared memory, K-major 128-byte swizzle: panel = 64 keys
+                // this half of the P row -> panel wg (K-major, 128-byte swizzle)
                 {
-                    uint8_t* prow = smem + SM::kP + row * 128;
+                    uint8_t* prow = smem + SM::kP + wg * 16384 + row * 128;
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const int panel = c >> 3, chunk = c & 7;
+                    for (int c = 0; c < 8; ++c) {
                         uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                        *reinterpret_cast<uint4*>(prow + panel * 16384 + ((chunk ^ (row & 7)) << 4)) = v;
+                        *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) = v;
                     }
                 }
                 fence_proxy_async_smem();
@@ -329,36 +373,41 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 if (lane == 0) mbar_arrive(&p_full);
             }
             // epilogue: O / l -> global (rows with nothing kept are 0)
+            float inv = 0.f;
             if (ns > 0) {
+                lsum[wg][row] = l;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&xchg);
+                bool okx = mbar_wait(&xchg, xg & 1, ab);
+                ++xg;
+                if (!__all_sync(0xffffffffu, okx)) goto softmax_done;
+                const float lt = l + lsum[wg ^ 1][row];
+                inv = lt > 0.f ? 1.0f / lt : 0.f;
                 bool ok = mbar_wait(&pv_done, (g - 1) & 1, ab);
                 if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
                 tc_fence_after();
             }
-            {
-                const float inv = l > 0.f ? 1.0f / l : 0.f;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    if (ns > 0) {
-                        tmem_ld32(tO + lane_base + c * 32, r);
-                        tmem_wait_ld();
-                    } else {
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t r[32];
+                if (ns > 0) {
+                    tmem_ld32(tO + lane_base + wg * (D / 2) + c * 32, r);
+                    tmem_wait_ld();
+                } else {
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) r[k] = 0u;
-                    }
-                    uint32_t o[16];
-#pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        o[k] = Pack2<T>::pack(__uint_as_float(r[2 * k]) * inv, __uint_as_float(r[2 * k + 1]) * inv);
-                    if (row_valid) {
-                        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            dst[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-                    }
+                    for (int k = 0; k < 32; ++k) r[k] = 0u;
                 }
-                tc_fence_before();
+                uint32_t o[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    o[k] = Pack2<T>::pack(__uint_as_float(r[2 * k]) * inv, __uint_as_float(r[2 * k + 1]) * inv);
+                if (row_valid) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) dst[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                }
             }
+            tc_fence_before();
         }
     softmax_done:;
     }
