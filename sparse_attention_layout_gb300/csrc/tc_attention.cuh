@@ -19,11 +19,14 @@
 //   warps 2..9  softmax, two warpgroups: thread = one query row = one TMEM
 //               lane, each warpgroup owning half of the row's 128 scores.
 //               Reads S from TMEM, masks, keeps (m, l) (both groups take the
-//               full-row max; partial sums meet per tile), writes P to shared
-//               memory in the K-major swizzled layout, rescales its half of O
-//               in TMEM only when the row max grew by more than 2^8 (the final
-//               O / l is exact either way), and runs the epilogue O / l.
-// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D).
+//               full-row max; partial sums meet per tile), writes its half of
+//               P (bf16/fp16) into the TMEM P buffer of the step (two
+//               buffers, so step g only waits for P V of step g-2), rescales
+//               its half of O in TMEM only when the row max grew by more than
+//               2^8 (the final O / l is exact either way), and runs the
+//               epilogue O / l.
+// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D), P0 [384,448), P1 [448,512)
+// (P packed two 16-bit values per column; P V takes its A operand from TMEM).
 #pragma once
 
 #include <algorithm>
@@ -47,8 +50,7 @@ struct AttnSmem {
     static constexpr int kQ = 0;                      // 2 stages
     static constexpr int kK = kQ + 2 * kTile;         // 2 stages
     static constexpr int kV = kK + 2 * kTile;         // 2 stages
-    static constexpr int kP = kV + 2 * kTile;         // 128 x 128 probabilities
-    static constexpr int kBytes = kP + 128 * 128 * 2;
+    static constexpr int kBytes = kV + 2 * kTile;
     static constexpr int kAlloc = kBytes + 1024;      // slack for 1024-byte alignment
 };
 
@@ -75,7 +77,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     __shared__ uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2];
-    __shared__ uint64_t s_full[2], p_full, pv_done, xchg;
+    __shared__ uint64_t s_full[2], p_full[2], pv_done[2], xchg;
     __shared__ float lsum[2][128];  // partial row sums [warpgroup][row]
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
@@ -95,9 +97,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
         }
-        mbar_init(&p_full, 8);
+        mbar_init(&p_full[0], 8);  // one per P buffer: a warp re-arrives on a buffer only
+        mbar_init(&p_full[1], 8);  // after P V two steps back, i.e. after every warp arrived
         mbar_init(&xchg, 8);
-        mbar_init(&pv_done, 1);
+        mbar_init(&pv_done[0], 1);
+        mbar_init(&pv_done[1], 1);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -109,6 +113,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     tc_fence_after();
     const uint32_t tS = tmem_base;        // S buffers at columns 0 and 128
     const uint32_t tO = tmem_base + 256;  // O at column 256
+    const uint32_t tP = tmem_base + 384;  // P buffers (bf16 pairs) at columns 384 and 448
 
     const int64_t total = (int64_t)args.Z * L.n_tiles;
     const int S = L.S;
@@ -169,18 +174,17 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             bool pending = false, pending_first = false;
             uint32_t pending_g = 0;
             auto issue_pv = [&](uint32_t gp, bool first) -> bool {
-                if (!mbar_wait(&p_full, gp & 1, ab)) return false;
+                if (!mbar_wait(&p_full[gp & 1], (gp >> 1) & 1, ab)) return false;
                 if (!mbar_wait(&v_full[gp & 1], (gp >> 1) & 1, ab)) return false;
                 tc_fence_after();
-                const uint32_t pbase = smem_u32(smem + SM::kP);
                 const uint32_t vbase = smem_u32(smem + SM::kV + (gp & 1) * kTileBytes);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t ad = smem_desc(pbase + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, kSw128);
+                    // P (A operand) from TMEM buffer gp % 2: 8 columns per 16 keys
                     const uint64_t bd = smem_desc(vbase + ks * 2048, 128 * 128, 1024, kSw128);
-                    mma_f16(tO, ad, bd, kIdescPV, (ks > 0 || !first) ? 1u : 0u);
+                    mma_f16_tmem_a(tO, tP + (gp & 1) * 64 + ks * 8, bd, kIdescPV, (ks > 0 || !first) ? 1u : 0u);
                 }
-                mma_commit(&pv_done);
+                mma_commit(&pv_done[gp & 1]);
                 mma_commit(&v_empty[gp & 1]);
                 return true;
             };
@@ -306,14 +310,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 // raw scores (the scale is applied inside the exponent): own half x, other half y
                 float x[64], y[64];
                 const uint32_t srow = tS + (g & 1) * 128 + lane_base;
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    tmem_ld32(srow + wg * 64 + c * 32,
-                              *reinterpret_cast<uint32_t(*)[32]>(reinterpret_cast<uint32_t*>(x) + 32 * c));
-                    tmem_ld32(srow + (wg ^ 1) * 64 + c * 32,
-                              *reinterpret_cast<uint32_t(*)[32]>(reinterpret_cast<uint32_t*>(y) + 32 * c));
-                }
-                tmem_wait_ld();
+                tmem_ld64_sync(srow + wg * 64, srow + wg * 64 + 32, *reinterpret_cast<uint32_t(*)[64]>(x));
+                tmem_ld64_sync(srow + (wg ^ 1) * 64, srow + (wg ^ 1) * 64 + 32, *reinterpret_cast<uint32_t(*)[64]>(y));
                 mask_half(x, wg, own, rb, rseq);
                 mask_half(y, wg ^ 1, oth, rb, rseq);
                 const float mx = fmaxf(max64(x), max64(y));
@@ -339,38 +337,32 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 }
                 const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
                 l = l * alpha + rs;  // partial sum of this half
-                // P buffer and O are free once the previous P V has completed
-                if (g > 0) {
-                    ok = mbar_wait(&pv_done, (g - 1) & 1, ab);
+                // TMEM P buffer g % 2 is free once P V of step g - 2 has completed
+                if (g >= 2) {
+                    ok = mbar_wait(&pv_done[g & 1], ((g - 2) >> 1) & 1, ab);
                     if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
-                    tc_fence_after();
                 }
                 if (n > 0 && __any_sync(0xffffffffu, need)) {
+                    // O may be rescaled only after P V of step g - 1 (same tile) has completed
+                    ok = mbar_wait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, ab);
+                    if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
+                    tc_fence_after();
 #pragma unroll
                     for (int c = 0; c < D / 64; ++c) {
                         uint32_t r[32];
                         const uint32_t ta = tO + lane_base + wg * (D / 2) + c * 32;
-                        tmem_ld32(ta, r);
-                        tmem_wait_ld();
+                        tmem_ld32_sync(ta, r);
 #pragma unroll
                         for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
-                        tmem_st32(ta, r);
-                    }
-                    tmem_wait_st();
-                }
-                // this half of the P row -> panel wg (K-major, 128-byte swizzle)
-                {
-                    uint8_t* prow = smem + SM::kP + wg * 16384 + row * 128;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                        *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) = v;
+                        tmem_st32_sync(ta, r);
                     }
                 }
-                fence_proxy_async_smem();
+                // this half of the P row -> TMEM P buffer g % 2, columns [32 wg, 32 wg + 32)
+                tc_fence_after();
+                tmem_st32_sync(tP + (g & 1) * 64 + wg * 32 + lane_base, pk);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full);
+                if (lane == 0) mbar_arrive(&p_full[g & 1]);
             }
             // epilogue: O / l -> global (rows with nothing kept are 0)
             float inv = 0.f;
@@ -383,7 +375,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 if (!__all_sync(0xffffffffu, okx)) goto softmax_done;
                 const float lt = l + lsum[wg ^ 1][row];
                 inv = lt > 0.f ? 1.0f / lt : 0.f;
-                bool ok = mbar_wait(&pv_done, (g - 1) & 1, ab);
+                bool ok = mbar_wait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, ab);
                 if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
                 tc_fence_after();
             }
@@ -391,8 +383,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             for (int c = 0; c < D / 64; ++c) {
                 uint32_t r[32];
                 if (ns > 0) {
-                    tmem_ld32(tO + lane_base + wg * (D / 2) + c * 32, r);
-                    tmem_wait_ld();
+                    tmem_ld32_sync(tO + lane_base + wg * (D / 2) + c * 32, r);
                 } else {
 #pragma unroll
                     for (int k = 0; k < 32; ++k) r[k] = 0u;

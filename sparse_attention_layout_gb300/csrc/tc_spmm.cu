@@ -214,8 +214,7 @@ spmm_tc_kernel(const __grid_constant__ CUtensorMap tmDense, const __grid_constan
                 uint32_t r[32];
 #pragma unroll
                 for (int c = 0; c < (BLK + 31) / 32; ++c) {
-                    tmem_ld32(tacc + buf * 128 + lane_base + c * 32, r);
-                    tmem_wait_ld();
+                    tmem_ld32_sync(tacc + buf * 128 + lane_base + c * 32, r);
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         if (c * 32 + j < BLK) v[c * 32 + j] = __uint_as_float(r[j]);
@@ -404,8 +403,7 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t r[32];
-                    tmem_ld32(tS + st * 128 + lane_base + c * 32, r);
-                    tmem_wait_ld();
+                    tmem_ld32_sync(tS + st * 128 + lane_base + c * 32, r);
                     // columns c*32 .. c*32+31 belong to slot (c*32)/BLK (BLK >= 32) or to
                     // 32/BLK consecutive slots (BLK = 16)
 #pragma unroll
