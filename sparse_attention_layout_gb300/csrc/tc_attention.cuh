@@ -12,7 +12,8 @@
 // block mask removes.  Persistent CTAs walk the tiles longest-first.
 //
 // Roles (320 threads, one CTA per SM):
-//   warp 0      TMA producer: Q tile (2 stages), K and V tiles (2 stages each)
+//   warp 0      TMA producer: Q tile (2 stages), K and V tiles (2 stages each at
+//               D = 128, 4 at D = 64)
 //   warp 1      TMEM owner and MMA issuer (one thread):
 //                 S[g%2] = Q K^T   (M=128, N=128, K=D)
 //                 O     += P V     (M=128, N=D,   K=128), V taken MN-major
@@ -47,10 +48,12 @@ template <int D>
 struct AttnSmem {
     static constexpr int KP = D / 64;                 // 64-column panels per 128-row tile
     static constexpr int kTile = 128 * D * 2;         // bytes of one 128 x D tile
-    static constexpr int kQ = 0;                      // 2 stages
-    static constexpr int kK = kQ + 2 * kTile;         // 2 stages
-    static constexpr int kV = kK + 2 * kTile;         // 2 stages
-    static constexpr int kBytes = kV + 2 * kTile;
+    static constexpr int QST = 2;                     // Q tile stages
+    static constexpr int KVST = D == 128 ? 2 : 4;     // K and V step-tile stages each
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQ + QST * kTile;
+    static constexpr int kV = kK + KVST * kTile;
+    static constexpr int kBytes = kV + KVST * kTile;
     static constexpr int kAlloc = kBytes + 1024;      // slack for 1024-byte alignment
 };
 
@@ -76,7 +79,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    __shared__ uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2];
+    constexpr int QST = SM::QST, KVST = SM::KVST;
+    __shared__ uint64_t q_full[QST], q_empty[QST], k_full[KVST], k_empty[KVST], v_full[KVST], v_empty[KVST];
     __shared__ uint64_t s_full[2], p_full[2], pv_done[2], xchg;
     __shared__ float lsum[2][128];  // partial row sums [warpgroup][row]
     __shared__ uint32_t tmem_base;
@@ -88,15 +92,17 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < QST; ++i) {
             mbar_init(&q_full[i], 1);
             mbar_init(&q_empty[i], 1);
+        }
+        for (int i = 0; i < KVST; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&k_empty[i], 1);
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
-            mbar_init(&s_full[i], 1);
         }
+        for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
         mbar_init(&p_full[0], 8);  // one per P buffer: a warp re-arrives on a buffer only
         mbar_init(&p_full[1], 8);  // after P V two steps back, i.e. after every warp arrived
         mbar_init(&xchg, 8);
@@ -132,8 +138,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 const int s0 = L.tile_step_ptr[tile], ns = L.tile_step_ptr[tile + 1] - s0;
                 if (ns == 0) continue;
                 const int64_t zh = (int64_t)z * L.H + h;
-                const uint32_t qs = q_it & 1;
-                if (!mbar_wait(&q_empty[qs], ((q_it >> 1) & 1) ^ 1, ab)) break;
+                const uint32_t qs = q_it % QST;
+                if (!mbar_wait(&q_empty[qs], ((q_it / QST) & 1) ^ 1, ab)) break;
                 mbar_arrive_expect_tx(&q_full[qs], kTileBytes);
                 for (int p = 0; p < KP; ++p)
                     tma_load_2d(smem_u32(smem + SM::kQ + qs * kTileBytes + p * 16384), &tmQ, p * 64,
@@ -141,7 +147,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 ++q_it;
                 for (int n = 0; n < ns; ++n) {
                     const int s = s0 + n;
-                    const uint32_t st = kv_it & 1, ph = ((kv_it >> 1) & 1) ^ 1;
+                    const uint32_t st = kv_it % KVST, ph = ((kv_it / KVST) & 1) ^ 1;
                     int cols[G];
 #pragma unroll
                     for (int b = 0; b < G; ++b) {
@@ -175,9 +181,9 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             uint32_t pending_g = 0;
             auto issue_pv = [&](uint32_t gp, bool first) -> bool {
                 if (!mbar_wait(&p_full[gp & 1], (gp >> 1) & 1, ab)) return false;
-                if (!mbar_wait(&v_full[gp & 1], (gp >> 1) & 1, ab)) return false;
+                if (!mbar_wait(&v_full[gp % KVST], (gp / KVST) & 1, ab)) return false;
                 tc_fence_after();
-                const uint32_t vbase = smem_u32(smem + SM::kV + (gp & 1) * kTileBytes);
+                const uint32_t vbase = smem_u32(smem + SM::kV + (gp % KVST) * kTileBytes);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     // P (A operand) from TMEM buffer gp % 2: 8 columns per 16 keys
@@ -185,18 +191,18 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     mma_f16_tmem_a(tO, tP + (gp & 1) * 64 + ks * 8, bd, kIdescPV, (ks > 0 || !first) ? 1u : 0u);
                 }
                 mma_commit(&pv_done[gp & 1]);
-                mma_commit(&v_empty[gp & 1]);
+                mma_commit(&v_empty[gp % KVST]);
                 return true;
             };
             for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
                 const int tile = L.tile_order[w / args.Z];
                 const int ns = L.tile_step_ptr[tile + 1] - L.tile_step_ptr[tile];
                 if (ns == 0) continue;
-                const uint32_t qs = q_it & 1;
-                if (!mbar_wait(&q_full[qs], (q_it >> 1) & 1, ab)) goto mma_done;
+                const uint32_t qs = q_it % QST;
+                if (!mbar_wait(&q_full[qs], (q_it / QST) & 1, ab)) goto mma_done;
                 for (int n = 0; n < ns; ++n, ++g) {
-                    const uint32_t st = g & 1;
-                    if (!mbar_wait(&k_full[st], (g >> 1) & 1, ab)) goto mma_done;
+                    const uint32_t st = g % KVST;
+                    if (!mbar_wait(&k_full[st], (g / KVST) & 1, ab)) goto mma_done;
                     tc_fence_after();
                     const uint32_t qbase = smem_u32(smem + SM::kQ + qs * kTileBytes);
                     const uint32_t kbase = smem_u32(smem + SM::kK + st * kTileBytes);
