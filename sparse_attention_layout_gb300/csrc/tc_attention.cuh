@@ -11,12 +11,12 @@
 // pair that is not in the layout is masked to -inf, as are entries the intra-
 // block mask removes.  Persistent CTAs walk the tiles longest-first.
 //
-// Roles (320 threads, one CTA per SM):
-//   warp 0      TMA producer: Q tile (2 stages), K and V tiles (2 stages each at
-//               D = 128, 4 at D = 64)
-//   warp 1      TMEM owner and MMA issuer (one thread):
-//                 S[g%2] = Q K^T   (M=128, N=128, K=D)
-//                 O     += P V     (M=128, N=D,   K=128), V taken MN-major
+// Roles (352 threads, one CTA per SM):
+//   warp 0      TMA producer: Q tile (2 stages), K and V tiles (2 stages each)
+//   warp 1      TMEM owner; one thread issues S[g%2] = Q K^T (M=128, N=128, K=D)
+//   warp 10     one thread issues O += P V (M=128, N=D, K=128; P from TMEM, V
+//               MN-major).  Two issuing threads halve each one's per-step
+//               barrier waits and commits, which cost about as much as the MMAs.
 //   warps 2..9  softmax, two warpgroups: thread = one query row = one TMEM
 //               lane, each warpgroup owning half of the row's 128 scores.
 //               Reads S from TMEM, masks, keeps (m, l) (both groups take the
@@ -41,7 +41,7 @@ namespace attn {
 
 using namespace tc;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when max grows by > 256x
 
 template <int D>
@@ -49,7 +49,7 @@ struct AttnSmem {
     static constexpr int KP = D / 64;                 // 64-column panels per 128-row tile
     static constexpr int kTile = 128 * D * 2;         // bytes of one 128 x D tile
     static constexpr int QST = 2;                     // Q tile stages
-    static constexpr int KVST = D == 128 ? 2 : 4;     // K and V step-tile stages each
+    static constexpr int KVST = 2;                    // K and V step-tile stages each
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + QST * kTile;
     static constexpr int kV = kK + KVST * kTile;
@@ -79,8 +79,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    constexpr int QST = SM::QST, KVST = SM::KVST;
-    __shared__ uint64_t q_full[QST], q_empty[QST], k_full[KVST], k_empty[KVST], v_full[KVST], v_empty[KVST];
+    constexpr int QST = SM::QST;
+    // K and V stage b (= step % 2) is tied to S buffer and P buffer b: s_full[b]
+    // (Q K^T of the step done) also frees its K tile, pv_done[b] (P V of the step
+    // done) also frees its V tile and its P buffer.
+    __shared__ uint64_t q_full[QST], q_empty[QST], k_full[2], v_full[2];
     __shared__ uint64_t s_full[2], p_full[2], pv_done[2], xchg;
     __shared__ float lsum[2][128];  // partial row sums [warpgroup][row]
     __shared__ uint32_t tmem_base;
@@ -96,18 +99,16 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             mbar_init(&q_full[i], 1);
             mbar_init(&q_empty[i], 1);
         }
-        for (int i = 0; i < KVST; ++i) {
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&k_full[i], 1);
-            mbar_init(&k_empty[i], 1);
             mbar_init(&v_full[i], 1);
-            mbar_init(&v_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&pv_done[i], 1);
+            // one per P buffer: a warp re-arrives on a buffer only after P V two
+            // steps back has completed, i.e. after every warp arrived
+            mbar_init(&p_full[i], 8);
         }
-        for (int i = 0; i < 2; ++i) mbar_init(&s_full[i], 1);
-        mbar_init(&p_full[0], 8);  // one per P buffer: a warp re-arrives on a buffer only
-        mbar_init(&p_full[1], 8);  // after P V two steps back, i.e. after every warp arrived
         mbar_init(&xchg, 8);
-        mbar_init(&pv_done[0], 1);
-        mbar_init(&pv_done[1], 1);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -130,7 +131,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            uint32_t q_it = 0, kv_it = 0;
+            uint32_t q_it = 0, g = 0;
             for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
                 const int tile = L.tile_order[w / args.Z];
                 const int z = (int)(w % args.Z);
@@ -145,85 +146,91 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     tma_load_2d(smem_u32(smem + SM::kQ + qs * kTileBytes + p * 16384), &tmQ, p * 64,
                                 (int32_t)(zh * S + gq * 128), &q_full[qs]);
                 ++q_it;
-                for (int n = 0; n < ns; ++n) {
+                for (int n = 0; n < ns; ++n, ++g) {
                     const int s = s0 + n;
-                    const uint32_t st = kv_it % KVST, ph = ((kv_it / KVST) & 1) ^ 1;
+                    const uint32_t st = g & 1;
                     int cols[G];
 #pragma unroll
                     for (int b = 0; b < G; ++b) {
                         const int c = L.step_col[s * G + b];
                         cols[b] = c >= 0 ? c : L.step_col[s * G];  // padding slot: any valid block
                     }
-                    if (!mbar_wait(&k_empty[st], ph, ab)) goto producer_done;
+                    // K tile of step g - 2 is free once its Q K^T has completed
+                    if (g >= 2 && !mbar_wait(&s_full[st], ((g - 2) >> 1) & 1, ab)) goto producer_done;
                     mbar_arrive_expect_tx(&k_full[st], kTileBytes);
 #pragma unroll
                     for (int b = 0; b < G; ++b)
                         for (int p = 0; p < KP; ++p)
                             tma_load_2d(smem_u32(smem + SM::kK + st * kTileBytes + p * 16384 + b * BLK * 128), &tmK,
                                         p * 64, (int32_t)(zh * S + (int64_t)cols[b] * BLK), &k_full[st]);
-                    if (!mbar_wait(&v_empty[st], ph, ab)) goto producer_done;
+                    // V tile of step g - 2 is free once its P V has completed
+                    if (g >= 2 && !mbar_wait(&pv_done[st], ((g - 2) >> 1) & 1, ab)) goto producer_done;
                     mbar_arrive_expect_tx(&v_full[st], kTileBytes);
 #pragma unroll
                     for (int b = 0; b < G; ++b)
                         for (int p = 0; p < KP; ++p)
                             tma_load_2d(smem_u32(smem + SM::kV + st * kTileBytes + p * 16384 + b * BLK * 128), &tmV,
                                         p * 64, (int32_t)(zh * S + (int64_t)cols[b] * BLK), &v_full[st]);
-                    ++kv_it;
                 }
             }
         producer_done:;
         }
     } else if (warp == 1) {
-        // --------------------------------------------------- MMA issuer ----
+        // ------------------------------------------- Q K^T issuer (one thread) ----
         if (lane == 0) {
+            // descriptors of the first stage; stage / K-step offsets are added to the
+            // start-address field (addresses stay below 2^18, so no carry leaves it)
+            const uint64_t dq = smem_desc(smem_u32(smem + SM::kQ), 16, 1024, kSw128);
+            const uint64_t dk = smem_desc(smem_u32(smem + SM::kK), 16, 1024, kSw128);
             uint32_t q_it = 0, g = 0;
-            bool pending = false, pending_first = false;
-            uint32_t pending_g = 0;
-            auto issue_pv = [&](uint32_t gp, bool first) -> bool {
-                if (!mbar_wait(&p_full[gp & 1], (gp >> 1) & 1, ab)) return false;
-                if (!mbar_wait(&v_full[gp % KVST], (gp / KVST) & 1, ab)) return false;
-                tc_fence_after();
-                const uint32_t vbase = smem_u32(smem + SM::kV + (gp % KVST) * kTileBytes);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    // P (A operand) from TMEM buffer gp % 2: 8 columns per 16 keys
-                    const uint64_t bd = smem_desc(vbase + ks * 2048, 128 * 128, 1024, kSw128);
-                    mma_f16_tmem_a(tO, tP + (gp & 1) * 64 + ks * 8, bd, kIdescPV, (ks > 0 || !first) ? 1u : 0u);
-                }
-                mma_commit(&pv_done[gp & 1]);
-                mma_commit(&v_empty[gp % KVST]);
-                return true;
-            };
             for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
                 const int tile = L.tile_order[w / args.Z];
                 const int ns = L.tile_step_ptr[tile + 1] - L.tile_step_ptr[tile];
                 if (ns == 0) continue;
                 const uint32_t qs = q_it % QST;
-                if (!mbar_wait(&q_full[qs], (q_it / QST) & 1, ab)) goto mma_done;
+                if (!mbar_wait(&q_full[qs], (q_it / QST) & 1, ab)) goto qk_done;
                 for (int n = 0; n < ns; ++n, ++g) {
-                    const uint32_t st = g % KVST;
-                    if (!mbar_wait(&k_full[st], (g / KVST) & 1, ab)) goto mma_done;
+                    const uint32_t st = g & 1;
+                    // S buffer g % 2 is free once the softmax of step g - 2 has read it
+                    if (g >= 2 && !mbar_wait(&p_full[st], ((g - 2) >> 1) & 1, ab)) goto qk_done;
+                    if (!mbar_wait(&k_full[st], (g >> 1) & 1, ab)) goto qk_done;
                     tc_fence_after();
-                    const uint32_t qbase = smem_u32(smem + SM::kQ + qs * kTileBytes);
-                    const uint32_t kbase = smem_u32(smem + SM::kK + st * kTileBytes);
+                    const uint64_t aq = dq + ((qs * kTileBytes) >> 4), bk = dk + ((st * kTileBytes) >> 4);
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_f16(tS + (g & 1) * 128, smem_desc(qbase + off, 16, 1024, kSw128),
-                                smem_desc(kbase + off, 16, 1024, kSw128), kIdescQK, ks > 0 ? 1u : 0u);
+                        const uint32_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+                        mma_f16(tS + st * 128, aq + off, bk + off, kIdescQK, ks > 0 ? 1u : 0u);
                     }
-                    mma_commit(&s_full[g & 1]);
-                    mma_commit(&k_empty[st]);
+                    mma_commit(&s_full[st]);
                     if (n == ns - 1) mma_commit(&q_empty[qs]);
-                    if (pending && !issue_pv(pending_g, pending_first)) goto mma_done;
-                    pending = true;
-                    pending_g = g;
-                    pending_first = (n == 0);
                 }
                 ++q_it;
             }
-            if (pending) issue_pv(pending_g, pending_first);
-        mma_done:;
+        qk_done:;
+        }
+    } else if (warp == 10) {
+        // --------------------------------------------- P V issuer (one thread) ----
+        if (lane == 0) {
+            const uint64_t dv = smem_desc(smem_u32(smem + SM::kV), 128 * 128, 1024, kSw128);
+            uint32_t g = 0;
+            for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+                const int tile = L.tile_order[w / args.Z];
+                const int ns = L.tile_step_ptr[tile + 1] - L.tile_step_ptr[tile];
+                for (int n = 0; n < ns; ++n, ++g) {
+                    const uint32_t st = g & 1;
+                    // P of step g written (and O rescaled) by all softmax warps; V landed
+                    if (!mbar_wait(&p_full[st], (g >> 1) & 1, ab)) goto pv_done_label;
+                    if (!mbar_wait(&v_full[st], (g >> 1) & 1, ab)) goto pv_done_label;
+                    tc_fence_after();
+                    const uint64_t bv = dv + ((st * kTileBytes) >> 4);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)  // P (A operand) from TMEM: 8 columns per 16 keys
+                        mma_f16_tmem_a(tO, tP + st * 64 + ks * 8, bv + ((ks * 2048) >> 4), kIdescPV,
+                                       (ks > 0 || n > 0) ? 1u : 0u);
+                    mma_commit(&pv_done[st]);
+                }
+            }
+        pv_done_label:;
         }
     } else {
         // ------------------------------------------- softmax / epilogue ----
