@@ -1,0 +1,153 @@
+"""GPU parity at the workloads' full sizes, in the launch configuration the
+bench times, on sampled outputs the oracle computes one by one (plus whole-
+tensor properties that hold at any size: finiteness, softmax rows summing to 1,
+exact zeros of empty rows).
+
+Workloads: tiny (Z1 H1 S256 D64 B16 fp32), bigbird (Z2 H12 S4096 D64 B64
+fp32, diagonal-causal), band (Z4 H16 S8192 D128 B128 bf16), strided (Z1 H32
+S16384 D128 B64 bf16, diagonal-causal) and the spMM workload (8192^2 sparse,
+block 32, bf16, 10/25/50 % density).  Tolerance: normwise max |g - r| / max |r|
+<= 1e-5 (fp32) or 2e-2 (bf16)."""
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import TOL, assert_close, to_np
+from sparse_attention_layout_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+
+
+@pytest.fixture(scope="module")
+def bsp():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from sparse_attention_layout_gb300 import build
+    build.build()
+    from sparse_attention_layout_gb300 import bsp as m
+    return m
+
+
+def sample_rows(w, lay, n, seed):
+    """Random rows plus edge rows: first/last row of every sampled (z, h), rows
+    of the last block-row and of the longest block-row."""
+    rng = np.random.default_rng(seed)
+    total = w.Z * w.H * w.S
+    rows = set(rng.choice(total, size=n, replace=False).tolist())
+    counts = lay.sum(axis=2)  # [H, nb]
+    h_long, i_long = np.unravel_index(np.argmax(counts), counts.shape)
+    for z in range(w.Z):
+        for h in (0, w.H - 1, int(h_long)):
+            base = (z * w.H + h) * w.S
+            rows.update([base, base + w.S - 1, base + w.S - w.B, base + int(i_long) * w.B + w.B // 2])
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+@pytest.mark.parametrize("name", ["tiny", "bigbird", "band", "strided"])
+def test_attention_workload(bsp, oracle, name):
+    w = W.ATTENTION_WORKLOADS[name]
+    lay = w.layout()
+    L = bsp.bsp_layout_compile(lay, w.B)
+    Q, K, V = w.qkv()
+    q, k, v = (t.cuda() for t in (Q, K, V))
+    o = torch.empty_like(q)
+    bsp.bsp_attention(L, q, k, v, o, w.scale, w.mask_kind)  # the bench's call
+    torch.cuda.synchronize()
+    assert bsp.bsp_status_check(L) == 0
+    assert torch.isfinite(o).all()
+    sel = sample_rows(w, lay, 48, 7)
+    got = to_np(o.reshape(-1, w.D)[torch.from_numpy(sel).cuda()])
+    want = oracle.attention(lay, w.B, Q, K, V, w.scale, w.mask_kind, sel=sel)
+    assert_close(got, want, DT[w.dtype], f"{name} fused attention, {sel.size} sampled rows")
+
+
+@pytest.mark.parametrize("name", ["tiny", "bigbird", "band", "strided"])
+def test_unfused_chain_workload(bsp, oracle, name):
+    """SDD -> softmax -> DSD at full size: sampled SDD blocks and sampled rows
+    of the chain's output against the oracle."""
+    w = W.ATTENTION_WORKLOADS[name]
+    lay = w.layout()
+    L = bsp.bsp_layout_compile(lay, w.B)
+    Q, K, V = w.qkv()
+    q, k, v = (t.cuda() for t in (Q, K, V))
+    P = bsp.bsp_sdd(L, q, k)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(3)
+    blocks = np.unique(np.concatenate([rng.choice(w.Z * L.nnz, size=24, replace=False),
+                                       [0, w.Z * L.nnz - 1]])).astype(np.int64)
+    got_s = to_np(P.reshape(-1, w.B, w.B)[torch.from_numpy(blocks).cuda()])
+    want_s = oracle.sdd(lay, w.B, Q, K, sel=blocks)
+    assert_close(got_s, want_s, DT[w.dtype], f"{name} SDD, {blocks.size} sampled blocks")
+    bsp.bsp_softmax(L, P, P, w.scale, w.mask_kind)
+    O = bsp.bsp_dsd(L, P, v)
+    torch.cuda.synchronize()
+    assert torch.isfinite(O).all()
+    sel = sample_rows(w, lay, 48, 11)
+    got = to_np(O.reshape(-1, w.D)[torch.from_numpy(sel).cuda()])
+    want = oracle.attention(lay, w.B, Q, K, V, w.scale, w.mask_kind, sel=sel)
+    # the chain rounds the scores and the probabilities to the data type once more
+    # than the fused kernel; both stay inside the same bound
+    assert_close(got, want, DT[w.dtype], f"{name} unfused chain, {sel.size} sampled rows")
+
+
+@pytest.mark.parametrize("name", ["tiny", "bigbird"])
+def test_softmax_workload(bsp, oracle, name):
+    """The softmax alone on random SDD-shaped input at full size: sampled rows
+    against the oracle, every row of the whole output sums to 1."""
+    w = W.ATTENTION_WORKLOADS[name]
+    lay = w.layout()
+    L = bsp.bsp_layout_compile(lay, w.B)
+    X = W.randn((w.Z, L.nnz, w.B, w.B), w.dtype, 77)
+    Y = bsp.bsp_softmax(L, X.cuda(), None, w.scale, w.mask_kind)
+    torch.cuda.synchronize()
+    assert torch.isfinite(Y).all()
+    # row sums over the whole output: gather each row's slices through the layout
+    hs, is_, js = np.nonzero(lay)
+    key = torch.from_numpy(hs * w.nb + is_).cuda()
+    rowsum = torch.zeros(w.Z, w.H * w.nb, w.B, device="cuda", dtype=torch.float64)
+    rowsum.index_add_(1, key, Y.double().sum(dim=3))
+    present = torch.from_numpy(lay.sum(axis=2).reshape(-1) > 0).cuda()
+    tol = 1e-5 if w.dtype == "f32" else 2e-2
+    assert torch.allclose(rowsum[:, present], torch.ones_like(rowsum[:, present]), atol=tol * 8, rtol=0)
+    sel = sample_rows(w, lay, 48, 5)
+    want = oracle.softmax_rows(lay, w.B, X, w.scale, w.mask_kind, sel=sel)  # dense rows [n, S]
+    Yh = to_np(Y)
+    ids = -np.ones(lay.shape, np.int64)
+    ids[hs, is_, js] = np.arange(hs.size)
+    got = np.zeros_like(want)
+    for t, u in enumerate(sel):
+        zh, r = divmod(int(u), w.S)
+        z, h = divmod(zh, w.H)
+        i, a = divmod(r, w.B)
+        for j in np.flatnonzero(lay[h, i]):
+            got[t, j * w.B:(j + 1) * w.B] = Yh[z, ids[h, i, j], a]
+    assert_close(got, want, DT[w.dtype], f"{name} softmax, {sel.size} sampled rows")
+
+
+@pytest.mark.parametrize("density", W.SPMM_DENSITIES)
+def test_spmm_workload(bsp, oracle, density):
+    sp = W.SPMM
+    lay = sp.layout(density)
+    L = bsp.bsp_layout_compile(lay, sp.B)
+    A = sp.sparse_values(L.nnz, density)
+    Bd = sp.dense_dsd(density)
+    Ad = sp.dense_dds(density)
+    C1 = bsp.bsp_dsd(L, A.cuda(), Bd.cuda())
+    C2 = bsp.bsp_dds(L, Ad.cuda(), A.cuda())
+    torch.cuda.synchronize()
+    assert torch.isfinite(C1).all() and torch.isfinite(C2).all()
+    rng = np.random.default_rng(int(density * 100))
+    empty_rows = np.flatnonzero(lay[0].sum(axis=1) == 0)
+    rows = np.unique(np.concatenate([rng.choice(sp.S, 10, replace=False), [0, sp.S - 1],
+                                     empty_rows[:2] * sp.B])).astype(np.int64)
+    got = to_np(C1[0, 0][torch.from_numpy(rows).cuda()])
+    assert_close(got, oracle.dsd(lay, sp.B, A, Bd, sel=rows), torch.bfloat16, f"DSD spMM {density}")
+    mrows = np.unique(np.concatenate([rng.choice(sp.N, 6, replace=False), [0, sp.N - 1]])).astype(np.int64)
+    got = to_np(C2[0, 0][torch.from_numpy(mrows).cuda()])
+    assert_close(got, oracle.dds(lay, sp.B, Ad, A, sel=mrows), torch.bfloat16, f"DDS spMM {density}")
+    # block-rows without any block are exactly zero in the DSD output
+    for i in empty_rows[:4]:
+        assert (C1[0, 0, i * sp.B:(i + 1) * sp.B] == 0).all()
