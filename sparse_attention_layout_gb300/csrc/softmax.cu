@@ -8,14 +8,18 @@
 // prescale, divide by the sum; rows too long for registers merge per-lane
 // (max, sum) pairs with the online update sum' = sum * exp(m1 - m2) + ...
 //
-// Design: one warp per row, 16-byte vector loads.  A row of block-row i spans
-// nnz_i separate B-element slices (one per present block), each a contiguous
-// run inside its block.  Rows that fit in registers (<= 32*MAXV vectors) are
-// read once and written once: exactly the algorithmic bytes.  Longer rows take
-// an online (max, sum) pass and a normalising pass.
+// Design.  A row of block-row i spans nnz_i separate B-element slices (one per
+// present block); R consecutive rows of one block are contiguous.  The main
+// kernel (softmax_chunk_kernel) moves an R-row chunk of a block-row with one
+// bulk copy per block into shared memory and back, so every byte crosses HBM
+// once in large transfers.  Rows too long for a 64 KB chunk fall back to
+// softmax_rows_kernel: one warp per row with 16-byte loads straight from
+// global memory (register-resident when the row fits, else an online pass and
+// a normalising pass).
 #include <cfloat>
 
 #include "common.cuh"
+#include "tc_common.cuh"
 
 namespace bsp {
 namespace {
@@ -179,9 +183,166 @@ softmax_rows_kernel(LayoutView L, const T* X, T* Y, int64_t rows_total, float c2
     }
 }
 
+// ---------------------------------------------------------------- chunks ----
+// One CTA per (z, h, block-row i, chunk of R consecutive rows).  Rows r0..r0+R-1
+// of one block are R*B contiguous elements, so the chunk arrives as nnz_i bulk
+// copies (one per present block) into shared memory and leaves the same way:
+// every HBM byte moves once, in large contiguous transfers.  Warps then own
+// rows: an online (max, sum) pass and a normalising pass over shared memory.
+// Several CTAs per SM overlap one CTA's transfers with another's arithmetic.
+constexpr int kChunkThreads = 256;
+constexpr int kChunkBudget = 64 * 1024;  // bytes of one chunk
+
+template <typename T, int BLK>
+__global__ void __launch_bounds__(kChunkThreads)
+softmax_chunk_kernel(LayoutView L, const T* X, T* Y, int R, int max_nnz, float c2, int kind,
+                     const uint8_t* __restrict__ mask) {
+    constexpr int VEC = 16 / sizeof(T);
+    constexpr int VPB = BLK / VEC;  // 16-byte vectors per row slice of one block
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    const int chunks = BLK / R;
+    int64_t t = blockIdx.x;
+    const int c = (int)(t % chunks);
+    t /= chunks;
+    const int i = (int)(t % L.nb);
+    t /= L.nb;
+    const int h = (int)(t % L.H);
+    const int64_t z = t / L.H;
+    const int p0 = L.row_ptr[h * (L.nb + 1) + i];
+    const int nq = L.row_ptr[h * (L.nb + 1) + i + 1] - p0;
+    if (nq == 0) return;
+    const int r0 = c * R;
+    const uint32_t slice = (uint32_t)R * BLK * sizeof(T);  // bytes of one block's part of the chunk
+    T* buf = reinterpret_cast<T*>(smem_raw);
+    int* scol = reinterpret_cast<int*>(smem_raw + (size_t)max_nnz * slice);
+    tc::Abort ab{&abort_flag, L.status};
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        tc::mbar_init(&bar, 1);
+        tc::fence_barrier_init();
+    }
+    for (int q = threadIdx.x; q < nq; q += kChunkThreads) scol[q] = L.col_idx[p0 + q];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        tc::mbar_arrive_expect_tx(&bar, slice * nq);
+        for (int q = 0; q < nq; ++q) {
+            const int64_t n = L.blk_id[p0 + q];
+            tc::bulk_load(tc::smem_u32(smem_raw + (size_t)q * slice), X + ((z * L.nnz + n) * BLK + r0) * BLK, slice,
+                          &bar);
+        }
+    }
+    const bool ok = tc::mbar_wait(&bar, 0, ab);
+    if (__syncthreads_and(ok)) {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const int nvec = nq * VPB;
+        for (int rr = warp; rr < R; rr += kChunkThreads / 32) {
+            const int r = r0 + rr;           // row inside the block-row
+            const int rseq = i * BLK + r;    // row inside the sequence
+            auto load = [&](int v, float (&x)[VEC], T*& p) {
+                const int q = v / VPB, e = v % VPB;
+                p = buf + ((size_t)q * R + rr) * BLK + e * VEC;
+                Vec16<T>::load(p, x);
+                const int col = scol[q] * BLK + e * VEC;
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) x[k] *= c2;
+                if (kind == BSP_MASK_DIAG_CAUSAL) {
+                    if (scol[q] == i) {
+#pragma unroll
+                        for (int k = 0; k < VEC; ++k)
+                            if (e * VEC + k > r) x[k] = -INFINITY;
+                    }
+                } else if (kind == BSP_MASK_DENSE) {
+                    const uint8_t* mp = mask + (int64_t)rseq * L.S + col;
+#pragma unroll
+                    for (int k = 0; k < VEC; ++k)
+                        if (!mp[k]) x[k] = -INFINITY;
+                }
+            };
+            // pass 1: online (max, sum) per lane, merged across the warp
+            float m = -INFINITY, l = 0.f;
+            for (int v = lane; v < nvec; v += 32) {
+                float x[VEC];
+                T* p;
+                load(v, x, p);
+                float vm = -INFINITY;
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) vm = fmaxf(vm, x[k]);
+                if (vm > m) {
+                    l = (m == -INFINITY) ? 0.f : l * exp2f(m - vm);
+                    m = vm;
+                }
+                if (m != -INFINITY) {
+#pragma unroll
+                    for (int k = 0; k < VEC; ++k) l += exp2f(x[k] - m);
+                }
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+                const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+                const float mn = fmaxf(m, m2);
+                l = ((m == -INFINITY) ? 0.f : l * exp2f(m - mn)) + ((m2 == -INFINITY) ? 0.f : l2 * exp2f(m2 - mn));
+                m = mn;
+            }
+            const float inv = l > 0.f ? 1.0f / l : 0.f;
+            // pass 2: normalise in place
+            for (int v = lane; v < nvec; v += 32) {
+                float x[VEC];
+                T* p;
+                load(v, x, p);
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) x[k] = (m != -INFINITY) ? exp2f(x[k] - m) * inv : 0.f;
+                Vec16<T>::store(p, x);
+            }
+        }
+        tc::fence_proxy_async_smem();  // generic-proxy writes -> visible to the bulk copy engine
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int q = 0; q < nq; ++q) {
+                const int64_t n = L.blk_id[p0 + q];
+                tc::bulk_store(Y + ((z * L.nnz + n) * BLK + r0) * BLK, tc::smem_u32(smem_raw + (size_t)q * slice),
+                               slice);
+            }
+            tc::bulk_commit();
+            tc::bulk_wait_read_all();  // shared memory must outlive the reads of the stores
+        }
+    }
+}
+
+template <typename T, int BLK>
+int launch_chunk(const bsp_layout_s* Lh, const void* X, void* Y, int Z, float scale, int kind,
+                 const uint8_t* mask, cudaStream_t s) {
+    const int64_t per_row = (int64_t)Lh->max_row_nnz * BLK * sizeof(T);
+    if (per_row == 0) return BSP_OK;
+    int R = BLK;
+    while (R > 1 && R * per_row > kChunkBudget) R >>= 1;
+    if (R * per_row > kChunkBudget) return BSP_ERR_UNSUPPORTED;  // one row does not fit
+    const size_t smem = (size_t)R * per_row + (size_t)Lh->max_row_nnz * sizeof(int);
+    const int64_t grid = (int64_t)Z * Lh->H * Lh->nb * (BLK / R);
+    if (grid > INT32_MAX) return BSP_ERR_UNSUPPORTED;
+    auto kern = softmax_chunk_kernel<T, BLK>;
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return BSP_ERR_CUDA;
+    kern<<<(unsigned)grid, kChunkThreads, smem, s>>>(Lh->view, (const T*)X, (T*)Y, R, Lh->max_row_nnz,
+                                                      scale * kLog2e, kind, mask);
+    return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
+}
+
 template <typename T>
 int launch_t(const bsp_layout_s* Lh, const void* X, void* Y, int Z, float scale, int kind,
              const uint8_t* mask, cudaStream_t s) {
+    int rc = BSP_ERR_UNSUPPORTED;
+    switch (Lh->B) {
+        case 16: rc = launch_chunk<T, 16>(Lh, X, Y, Z, scale, kind, mask, s); break;
+        case 32: rc = launch_chunk<T, 32>(Lh, X, Y, Z, scale, kind, mask, s); break;
+        case 64: rc = launch_chunk<T, 64>(Lh, X, Y, Z, scale, kind, mask, s); break;
+        case 128: rc = launch_chunk<T, 128>(Lh, X, Y, Z, scale, kind, mask, s); break;
+    }
+    if (rc != BSP_ERR_UNSUPPORTED) return rc;
+    // rows too long for one chunk: one warp per row, streaming from global memory
     const int64_t rows = (int64_t)Z * Lh->H * Lh->S;
     if (rows == 0) return BSP_OK;
     const int64_t blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
