@@ -192,9 +192,10 @@ softmax_rows_kernel(LayoutView L, const T* X, T* Y, int64_t rows_total, float c2
 // Several CTAs per SM overlap one CTA's transfers with another's arithmetic.
 constexpr int kChunkThreads = 256;
 constexpr int kChunkBudget = 64 * 1024;  // bytes of one chunk
+constexpr int kChunkRegElems = 40;       // row elements per lane held in registers
 
 template <typename T, int BLK>
-__global__ void __launch_bounds__(kChunkThreads)
+__global__ void __launch_bounds__(kChunkThreads, 4)
 softmax_chunk_kernel(LayoutView L, const T* X, T* Y, int R, int max_nnz, float c2, int kind,
                      const uint8_t* __restrict__ mask) {
     constexpr int VEC = 16 / sizeof(T);
@@ -240,13 +241,12 @@ softmax_chunk_kernel(LayoutView L, const T* X, T* Y, int R, int max_nnz, float c
         for (int rr = warp; rr < R; rr += kChunkThreads / 32) {
             const int r = r0 + rr;           // row inside the block-row
             const int rseq = i * BLK + r;    // row inside the sequence
+            // raw values (the scale is folded into the exponent), masked -> -inf
             auto load = [&](int v, float (&x)[VEC], T*& p) {
                 const int q = v / VPB, e = v % VPB;
                 p = buf + ((size_t)q * R + rr) * BLK + e * VEC;
                 Vec16<T>::load(p, x);
                 const int col = scol[q] * BLK + e * VEC;
-#pragma unroll
-                for (int k = 0; k < VEC; ++k) x[k] *= c2;
                 if (kind == BSP_MASK_DIAG_CAUSAL) {
                     if (scol[q] == i) {
 #pragma unroll
@@ -260,7 +260,49 @@ softmax_chunk_kernel(LayoutView L, const T* X, T* Y, int R, int max_nnz, float c
                         if (!mp[k]) x[k] = -INFINITY;
                 }
             };
-            // pass 1: online (max, sum) per lane, merged across the warp
+            constexpr int kRegVec = kChunkRegElems / VEC;  // vectors per lane kept in registers
+            if (nvec <= 32 * kRegVec) {
+                // the row in registers: max, then 2^(x c2 - m c2) (one FFMA + one
+                // MUFU per entry), sum, normalise, store -- one pass over shared memory
+                float x[kRegVec][VEC];
+                float m = -INFINITY;
+#pragma unroll
+                for (int k = 0; k < kRegVec; ++k) {
+                    if (lane + 32 * k < nvec) {
+                        T* p;
+                        load(lane + 32 * k, x[k], p);
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) m = fmaxf(m, x[k][e]);
+                    }
+                }
+                m = warp_max(m);
+                const float ms = (m == -INFINITY) ? 0.f : m * c2;
+                float l = 0.f;
+#pragma unroll
+                for (int k = 0; k < kRegVec; ++k) {
+                    if (lane + 32 * k < nvec) {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) {
+                            x[k][e] = tc::ex2_approx(fmaf(x[k][e], c2, -ms));
+                            l += x[k][e];
+                        }
+                    }
+                }
+                l = warp_sum(l);
+                const float inv = l > 0.f ? 1.0f / l : 0.f;
+#pragma unroll
+                for (int k = 0; k < kRegVec; ++k) {
+                    const int v = lane + 32 * k;
+                    if (v < nvec) {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) x[k][e] *= inv;
+                        Vec16<T>::store(buf + ((size_t)(v / VPB) * R + rr) * BLK + (v % VPB) * VEC, x[k]);
+                    }
+                }
+                continue;
+            }
+            // long row: online (max, sum) per lane in the scaled log2 domain,
+            // merged across the warp, then a normalising pass
             float m = -INFINITY, l = 0.f;
             for (int v = lane; v < nvec; v += 32) {
                 float x[VEC];
@@ -269,13 +311,14 @@ softmax_chunk_kernel(LayoutView L, const T* X, T* Y, int R, int max_nnz, float c
                 float vm = -INFINITY;
 #pragma unroll
                 for (int k = 0; k < VEC; ++k) vm = fmaxf(vm, x[k]);
+                vm *= c2;
                 if (vm > m) {
-                    l = (m == -INFINITY) ? 0.f : l * exp2f(m - vm);
+                    l = (m == -INFINITY) ? 0.f : l * tc::ex2_approx(m - vm);
                     m = vm;
                 }
                 if (m != -INFINITY) {
 #pragma unroll
-                    for (int k = 0; k < VEC; ++k) l += exp2f(x[k] - m);
+                    for (int k = 0; k < VEC; ++k) l += tc::ex2_approx(fmaf(x[k], c2, -m));
                 }
             }
 #pragma unroll
@@ -283,17 +326,18 @@ softmax_chunk_kernel(LayoutView L, const T* X, T* Y, int R, int max_nnz, float c
                 const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
                 const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
                 const float mn = fmaxf(m, m2);
-                l = ((m == -INFINITY) ? 0.f : l * exp2f(m - mn)) + ((m2 == -INFINITY) ? 0.f : l2 * exp2f(m2 - mn));
+                l = ((m == -INFINITY) ? 0.f : l * tc::ex2_approx(m - mn)) +
+                    ((m2 == -INFINITY) ? 0.f : l2 * tc::ex2_approx(m2 - mn));
                 m = mn;
             }
             const float inv = l > 0.f ? 1.0f / l : 0.f;
-            // pass 2: normalise in place
+            const float ms = (m == -INFINITY) ? 0.f : m;
             for (int v = lane; v < nvec; v += 32) {
                 float x[VEC];
                 T* p;
                 load(v, x, p);
 #pragma unroll
-                for (int k = 0; k < VEC; ++k) x[k] = (m != -INFINITY) ? exp2f(x[k] - m) * inv : 0.f;
+                for (int k = 0; k < VEC; ++k) x[k] = tc::ex2_approx(fmaf(x[k], c2, -ms)) * inv;
                 Vec16<T>::store(p, x);
             }
         }
