@@ -26,6 +26,14 @@ struct LayoutView {
     const int32_t* tile_order;    // [n_tiles] tile ids, most steps first
     const int32_t* step_col;      // [n_steps*G] block-column of each slot, -1 = padding
     const int32_t* step_blk;      // [n_steps*G*G] block id at (row a, slot b), -1 = absent
+    // softmax chunks for 2- and 4-byte elements: int4 (h*nb+i, p0, nnz_i,
+    // r0 | R << 16): R rows of block-row i from row r0, whose blocks have ids
+    // p0 .. p0+nnz_i-1 (ids are CSR positions), R the largest power of two with
+    // R * nnz_i * B * elt <= kSoftmaxChunkBudget (block-rows in memory order)
+    const int32_t* sm_items[2];
+    int sm_n_items[2];
+    int sm_max_bytes[2];          // largest chunk of the list, in bytes
+    int sm_fits[2];               // 0: some single row exceeds the budget
     int* status;                  // device status word (0 = OK, else a BSP_ERR_* code)
     int H, nb, B, S, G, ngroups, n_tiles;
     int64_t nnz;
@@ -45,10 +53,15 @@ struct bsp_layout_s {
     int64_t n_steps = 0;
     int max_tile_steps = 0;
     std::vector<int32_t> tile_step_ptr, tile_order, step_col, step_blk;
+    std::vector<int32_t> sm_items[2];
+    int sm_max_bytes[2] = {0, 0};
+    bool sm_fits[2] = {true, true};
 
     void* dmem = nullptr;  // one device allocation holding every table
     LayoutView view{};
 };
+
+constexpr int kSoftmaxChunkBudget = 64 * 1024;  // shared-memory bytes of one softmax chunk
 
 namespace bsp {
 

@@ -138,6 +138,29 @@ int build_tables(bsp_layout_s* L, const uint8_t* lay) {
     L->tile_step_ptr[L->n_tiles] = (int32_t)steps;
     L->n_steps = steps;
     L->tile_order = order_by_weight_desc(tile_steps);
+
+    // softmax chunk lists (element sizes 2 and 4 bytes)
+    for (int e = 0; e < 2; ++e) {
+        const int64_t elt = e ? 4 : 2;
+        L->sm_items[e].clear();
+        L->sm_max_bytes[e] = 0;
+        L->sm_fits[e] = true;
+        for (int key = 0; key < H * nb; ++key) {
+            const int64_t per_row = (int64_t)row_len[key] * L->B * elt;
+            if (per_row == 0) continue;
+            int R = L->B;
+            while (R > 1 && R * per_row > kSoftmaxChunkBudget) R >>= 1;
+            if (R * per_row > kSoftmaxChunkBudget) L->sm_fits[e] = false;
+            L->sm_max_bytes[e] = std::max<int>(L->sm_max_bytes[e], (int)std::min<int64_t>(R * per_row, INT32_MAX));
+            const int h = key / nb, i = key % nb;
+            for (int r0 = 0; r0 < L->B; r0 += R) {
+                L->sm_items[e].push_back(key);
+                L->sm_items[e].push_back(L->row_ptr[(size_t)h * (nb + 1) + i]);  // = first block id
+                L->sm_items[e].push_back(row_len[key]);
+                L->sm_items[e].push_back(r0 | (R << 16));
+            }
+        }
+    }
     L->max_tile_steps = tile_steps.empty() ? 0 : *std::max_element(tile_steps.begin(), tile_steps.end());
     return BSP_OK;
 }
@@ -195,7 +218,8 @@ extern "C" int bsp_layout_compile(const uint8_t* layout, int H, int nb, int bloc
         {&L->blk_key, &V.blk_key},       {&L->row_order, &V.row_order},
         {&L->col_order, &V.col_order},   {&L->tile_step_ptr, &V.tile_step_ptr},
         {&L->tile_order, &V.tile_order}, {&L->step_col, &V.step_col},
-        {&L->step_blk, &V.step_blk},
+        {&L->step_blk, &V.step_blk},      {&L->sm_items[0], &V.sm_items[0]},
+        {&L->sm_items[1], &V.sm_items[1]},
     };
     size_t total = padded<int>(4);  // status word first
     for (const Part& pt : parts) total += padded<int32_t>(pt.v->size() + 1);
@@ -226,6 +250,11 @@ extern "C" int bsp_layout_compile(const uint8_t* layout, int H, int nb, int bloc
     V.ngroups = L->ngroups;
     V.n_tiles = L->n_tiles;
     V.nnz = L->nnz;
+    for (int e = 0; e < 2; ++e) {
+        V.sm_n_items[e] = (int)(L->sm_items[e].size() / 4);
+        V.sm_max_bytes[e] = L->sm_max_bytes[e];
+        V.sm_fits[e] = L->sm_fits[e] ? 1 : 0;
+    }
     if (!ok) {
         cudaGetLastError();
         cudaStreamSynchronize(s);

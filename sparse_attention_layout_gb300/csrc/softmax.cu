@@ -191,49 +191,44 @@ softmax_rows_kernel(LayoutView L, const T* X, T* Y, int64_t rows_total, float c2
 // rows: an online (max, sum) pass and a normalising pass over shared memory.
 // Several CTAs per SM overlap one CTA's transfers with another's arithmetic.
 constexpr int kChunkThreads = 256;
-constexpr int kChunkBudget = 64 * 1024;  // bytes of one chunk
-constexpr int kChunkRegElems = 40;       // row elements per lane held in registers
+constexpr int kChunkRegElems = 40;  // row elements per lane held in registers
 
+// Chunks come from the layout's list for this element size: each block-row is
+// cut into chunks of the largest power-of-two row count that fits the budget.
 template <typename T, int BLK>
 __global__ void __launch_bounds__(kChunkThreads, 4)
-softmax_chunk_kernel(LayoutView L, const T* X, T* Y, int R, int max_nnz, float c2, int kind,
-                     const uint8_t* __restrict__ mask) {
+softmax_chunk_kernel(LayoutView L, const T* X, T* Y, float c2, int kind, const uint8_t* __restrict__ mask) {
     constexpr int VEC = 16 / sizeof(T);
     constexpr int VPB = BLK / VEC;  // 16-byte vectors per row slice of one block
+    constexpr int E = sizeof(T) == 4 ? 1 : 0;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     __shared__ uint64_t bar;
     __shared__ int abort_flag;
-    const int chunks = BLK / R;
-    int64_t t = blockIdx.x;
-    const int c = (int)(t % chunks);
-    t /= chunks;
-    const int i = (int)(t % L.nb);
-    t /= L.nb;
-    const int h = (int)(t % L.H);
-    const int64_t z = t / L.H;
-    const int p0 = L.row_ptr[h * (L.nb + 1) + i];
-    const int nq = L.row_ptr[h * (L.nb + 1) + i + 1] - p0;
-    if (nq == 0) return;
-    const int r0 = c * R;
+    const int n_items = L.sm_n_items[E];
+    const int64_t z = blockIdx.x / n_items;
+    const int it = (int)(blockIdx.x % n_items);
+    // one 16-byte load describes the chunk; the blocks of block-row i are the
+    // consecutive ids p0 .. p0+nq-1 (ids are CSR positions)
+    const int4 item = reinterpret_cast<const int4*>(L.sm_items[E])[it];
+    const int key = item.x, p0 = item.y, nq = item.z;
+    const int r0 = item.w & 0xffff, R = item.w >> 16;
+    const int h = key / L.nb, i = key % L.nb;
     const uint32_t slice = (uint32_t)R * BLK * sizeof(T);  // bytes of one block's part of the chunk
     T* buf = reinterpret_cast<T*>(smem_raw);
-    int* scol = reinterpret_cast<int*>(smem_raw + (size_t)max_nnz * slice);
+    int* scol = reinterpret_cast<int*>(smem_raw + L.sm_max_bytes[E]);
     tc::Abort ab{&abort_flag, L.status};
     if (threadIdx.x == 0) {
         abort_flag = 0;
         tc::mbar_init(&bar, 1);
         tc::fence_barrier_init();
-    }
-    for (int q = threadIdx.x; q < nq; q += kChunkThreads) scol[q] = L.col_idx[p0 + q];
-    __syncthreads();
-    if (threadIdx.x == 0) {
         tc::mbar_arrive_expect_tx(&bar, slice * nq);
-        for (int q = 0; q < nq; ++q) {
-            const int64_t n = L.blk_id[p0 + q];
-            tc::bulk_load(tc::smem_u32(smem_raw + (size_t)q * slice), X + ((z * L.nnz + n) * BLK + r0) * BLK, slice,
-                          &bar);
-        }
+        const T* src = X + ((z * L.nnz + p0) * BLK + r0) * BLK;
+        for (int q = 0; q < nq; ++q)
+            tc::bulk_load(tc::smem_u32(smem_raw + (size_t)q * slice), src + (size_t)q * BLK * BLK, slice, &bar);
     }
+    if (kind != BSP_MASK_NONE)
+        for (int q = threadIdx.x; q < nq; q += kChunkThreads) scol[q] = L.col_idx[p0 + q];
+    __syncthreads();
     const bool ok = tc::mbar_wait(&bar, 0, ab);
     if (__syncthreads_and(ok)) {
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -344,11 +339,9 @@ softmax_chunk_kernel(LayoutView L, const T* X, T* Y, int R, int max_nnz, float c
         tc::fence_proxy_async_smem();  // generic-proxy writes -> visible to the bulk copy engine
         __syncthreads();
         if (threadIdx.x == 0) {
-            for (int q = 0; q < nq; ++q) {
-                const int64_t n = L.blk_id[p0 + q];
-                tc::bulk_store(Y + ((z * L.nnz + n) * BLK + r0) * BLK, tc::smem_u32(smem_raw + (size_t)q * slice),
-                               slice);
-            }
+            T* dst = Y + ((z * L.nnz + p0) * BLK + r0) * BLK;
+            for (int q = 0; q < nq; ++q)
+                tc::bulk_store(dst + (size_t)q * BLK * BLK, tc::smem_u32(smem_raw + (size_t)q * slice), slice);
             tc::bulk_commit();
             tc::bulk_wait_read_all();  // shared memory must outlive the reads of the stores
         }
@@ -358,20 +351,18 @@ softmax_chunk_kernel(LayoutView L, const T* X, T* Y, int R, int max_nnz, float c
 template <typename T, int BLK>
 int launch_chunk(const bsp_layout_s* Lh, const void* X, void* Y, int Z, float scale, int kind,
                  const uint8_t* mask, cudaStream_t s) {
-    const int64_t per_row = (int64_t)Lh->max_row_nnz * BLK * sizeof(T);
-    if (per_row == 0) return BSP_OK;
-    int R = BLK;
-    while (R > 1 && R * per_row > kChunkBudget) R >>= 1;
-    if (R * per_row > kChunkBudget) return BSP_ERR_UNSUPPORTED;  // one row does not fit
-    const size_t smem = (size_t)R * per_row + (size_t)Lh->max_row_nnz * sizeof(int);
-    const int64_t grid = (int64_t)Z * Lh->H * Lh->nb * (BLK / R);
+    constexpr int E = sizeof(T) == 4 ? 1 : 0;
+    const LayoutView& V = Lh->view;
+    if (!V.sm_fits[E]) return BSP_ERR_UNSUPPORTED;  // some row longer than one chunk
+    if (V.sm_n_items[E] == 0) return BSP_OK;
+    const size_t smem = (size_t)V.sm_max_bytes[E] + (size_t)Lh->max_row_nnz * sizeof(int);
+    const int64_t grid = (int64_t)Z * V.sm_n_items[E];
     if (grid > INT32_MAX) return BSP_ERR_UNSUPPORTED;
     auto kern = softmax_chunk_kernel<T, BLK>;
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return BSP_ERR_CUDA;
-    kern<<<(unsigned)grid, kChunkThreads, smem, s>>>(Lh->view, (const T*)X, (T*)Y, R, Lh->max_row_nnz,
-                                                      scale * kLog2e, kind, mask);
+    kern<<<(unsigned)grid, kChunkThreads, smem, s>>>(V, (const T*)X, (T*)Y, scale * kLog2e, kind, mask);
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }
 
