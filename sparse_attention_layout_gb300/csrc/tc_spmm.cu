@@ -60,8 +60,12 @@ struct SpmmCfg {
     static constexpr int RB = W * 2;                    // bytes per such row (= swizzle span)
     static constexpr int kDense = 128 * BLK * 2;        // dense tile bytes
     static constexpr int kSparse = BLK * BLK * 2;       // block bytes
-    static constexpr int kStage = ((kDense + kSparse + 1023) / 1024) * 1024;  // 1024-aligned stages
-    static constexpr int ST = (196608 / kStage) < 8 ? (196608 / kStage) : 8;
+    static constexpr int kSlot = ((kDense + kSparse + 1023) / 1024) * 1024;  // one block's operands
+    // blocks per pipeline stage: one barrier wait and one commit per stage, so
+    // small blocks are batched (the per-step overhead dwarfs a 32-wide MMA)
+    static constexpr int KB = (81920 / kSlot) < 1 ? 1 : ((81920 / kSlot) > 8 ? 8 : (81920 / kSlot));
+    static constexpr int kStage = KB * kSlot;
+    static constexpr int ST = (196608 / kStage) > 4 ? 4 : (196608 / kStage);
     static constexpr int kAlloc = ST * kStage + 1024;
 };
 
@@ -123,33 +127,37 @@ spmm_tc_kernel(const __grid_constant__ CUtensorMap tmDense, const __grid_constan
         if (lane == 0) {
             tma_prefetch_desc(&tmDense);
             tma_prefetch_desc(&tmSparse);
-            uint32_t it = 0;
+            uint32_t it = 0;  // stage uses
             for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
                 int h, u, z, t, q0, q1;
                 item(w, h, u, z, t, q0, q1);
                 const int64_t zh = (int64_t)z * L.H + h;
                 const int e0 = t * 128;
-                for (int q = q0; q < q1; ++q, ++it) {
+                for (int c0 = q0; c0 < q1; c0 += C::KB, ++it) {
+                    const int nblk = min(C::KB, q1 - c0);
                     const int st = it % ST;
                     if (!mbar_wait(&empty[st], ((it / ST) & 1) ^ 1, ab)) goto producer_done;
-                    mbar_arrive_expect_tx(&full[st], C::kDense + C::kSparse);
-                    uint8_t* dd = smem + st * C::kStage;
-                    uint8_t* sp = dd + C::kDense;
-                    const int kb = args.idx[q] * BLK;  // first contraction index of this block
-                    if (args.dense_mn) {
-                        // rows = contraction index, columns = dense free index
-                        const int64_t y = zh * S + kb;
-                        for (int p = 0; p < 2; ++p)
-                            tma_load_2d(smem_u32(dd + p * (BLK * 128)), &tmDense, e0 + 64 * p, (int32_t)y, &full[st]);
-                    } else {
-                        // rows = dense free index, columns = contraction index
-                        const int64_t y = zh * args.ext + e0;
+                    mbar_arrive_expect_tx(&full[st], nblk * (C::kDense + C::kSparse));
+                    for (int sl = 0; sl < nblk; ++sl) {
+                        const int q = c0 + sl;
+                        uint8_t* dd = smem + st * C::kStage + sl * C::kSlot;
+                        uint8_t* sp = dd + C::kDense;
+                        const int kb = args.idx[q] * BLK;  // first contraction index of this block
+                        if (args.dense_mn) {
+                            // rows = contraction index, columns = dense free index
+                            for (int p = 0; p < 2; ++p)
+                                tma_load_2d(smem_u32(dd + p * (BLK * 128)), &tmDense, e0 + 64 * p,
+                                            (int32_t)(zh * S + kb), &full[st]);
+                        } else {
+                            // rows = dense free index, columns = contraction index
+                            for (int p = 0; p < BLK / W; ++p)
+                                tma_load_2d(smem_u32(dd + p * (128 * RB)), &tmDense, kb + W * p,
+                                            (int32_t)(zh * args.ext + e0), &full[st]);
+                        }
+                        const int64_t yb = ((int64_t)z * L.nnz + args.bid[q]) * BLK;
                         for (int p = 0; p < BLK / W; ++p)
-                            tma_load_2d(smem_u32(dd + p * (128 * RB)), &tmDense, kb + W * p, (int32_t)y, &full[st]);
+                            tma_load_2d(smem_u32(sp + p * (BLK * RB)), &tmSparse, W * p, (int32_t)yb, &full[st]);
                     }
-                    const int64_t yb = ((int64_t)z * L.nnz + args.bid[q]) * BLK;
-                    for (int p = 0; p < BLK / W; ++p)
-                        tma_load_2d(smem_u32(sp + p * (BLK * RB)), &tmSparse, W * p, (int32_t)yb, &full[st]);
                 }
             }
         producer_done:;
@@ -157,6 +165,19 @@ spmm_tc_kernel(const __grid_constant__ CUtensorMap tmDense, const __grid_constan
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = idesc_f16(128, BLK, kBf16, args.dense_mn, args.sparse_mn);
+            // descriptors of stage 0, slot 0; per K-step / slot / stage offsets are added
+            // to the start-address field (shared addresses stay below 2^18: no carry)
+            const uint32_t s0 = smem_u32(smem);
+            const uint64_t dA = args.dense_mn ? smem_desc(s0, BLK * 128, 1024, kSw128)
+                                              : smem_desc(s0, 16, 8 * RB, swz_code(RB));
+            const uint64_t dB = args.sparse_mn ? smem_desc(s0 + C::kDense, BLK * RB, 8 * RB, swz_code(RB))
+                                               : smem_desc(s0 + C::kDense, 16, 8 * RB, swz_code(RB));
+            uint32_t offA[BLK / 16], offB[BLK / 16];
+#pragma unroll
+            for (int ks = 0; ks < BLK / 16; ++ks) {
+                offA[ks] = (args.dense_mn ? ks * 16 * 128 : (16 * ks / W) * (128 * RB) + (16 * ks % W) * 2) >> 4;
+                offB[ks] = (args.sparse_mn ? ks * 16 * RB : (16 * ks / W) * (BLK * RB) + (16 * ks % W) * 2) >> 4;
+            }
             uint32_t it = 0, k = 0;
             for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
                 int h, u, z, t, q0, q1;
@@ -165,26 +186,17 @@ spmm_tc_kernel(const __grid_constant__ CUtensorMap tmDense, const __grid_constan
                 const uint32_t buf = k & 1;
                 if (!mbar_wait(&acc_empty[buf], ((k >> 1) & 1) ^ 1, ab)) goto mma_done;
                 tc_fence_after();
-                for (int q = q0; q < q1; ++q, ++it) {
+                for (int c0 = q0; c0 < q1; c0 += C::KB, ++it) {
+                    const int nblk = min(C::KB, q1 - c0);
                     const int st = it % ST;
                     if (!mbar_wait(&full[st], (it / ST) & 1, ab)) goto mma_done;
                     tc_fence_after();
-                    const uint32_t dd = smem_u32(smem + st * C::kStage);
-                    const uint32_t sp = dd + C::kDense;
+                    for (int sl = 0; sl < nblk; ++sl) {
+                        const uint32_t so = (uint32_t)(st * C::kStage + sl * C::kSlot) >> 4;
 #pragma unroll
-                    for (int ks = 0; ks < BLK / 16; ++ks) {
-                        uint64_t ad, bd;
-                        if (args.dense_mn)
-                            ad = smem_desc(dd + ks * 16 * 128, BLK * 128, 1024, kSw128);
-                        else
-                            ad = smem_desc(dd + (16 * ks / W) * (128 * RB) + (16 * ks % W) * 2, 16, 8 * RB,
-                                           swz_code(RB));
-                        if (args.sparse_mn)
-                            bd = smem_desc(sp + ks * 16 * RB, BLK * RB, 8 * RB, swz_code(RB));
-                        else
-                            bd = smem_desc(sp + (16 * ks / W) * (BLK * RB) + (16 * ks % W) * 2, 16, 8 * RB,
-                                           swz_code(RB));
-                        mma_f16(tacc + buf * 128, ad, bd, idesc, (q > q0 || ks > 0) ? 1u : 0u);
+                        for (int ks = 0; ks < BLK / 16; ++ks)
+                            mma_f16(tacc + buf * 128, dA + so + offA[ks], dB + so + offB[ks], idesc,
+                                    (c0 > q0 || sl > 0 || ks > 0) ? 1u : 0u);
                     }
                     mma_commit(&empty[st]);
                 }
