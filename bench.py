@@ -240,6 +240,23 @@ def run_reference(args):
 
 # --------------------------------------------------------------------- ours --
 
+def max_over_ranks(ms: float, world: int, device: str) -> float:
+    """Slowest rank's time: the job finishes when the last rank does.  The
+    only collective of the multi-GPU path (no data-path exchange)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_value(flops_per_rank: float, world: int, ms_step: float) -> float:
+    """Whole-job TFLOP/s: every rank processes its own batch of the workload."""
+    return flops_per_rank * world / (ms_step * 1e-3) / 1e12
+
+
 def time_launches(fn, n, stream):
     import torch
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -310,7 +327,7 @@ def run_ours(args):
 
     w = workload(args.workload)
     lay = w.layout()
-    Qc, Kc, Vc = w.qkv()
+    Qc, Kc, Vc = w.qkv(shard=rank)  # each rank: its own batch (weak scaling)
     stream = torch.cuda.current_stream()
     L = bsp.bsp_layout_compile(lay, w.B)
     q, k, v = (t.cuda() for t in (Qc, Kc, Vc))
@@ -339,14 +356,10 @@ def run_ours(args):
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
-    ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(end), world, "cuda")
     ms_step = ms / args.steps
     flops = nonzero_flops(lay, w.B, w.D, w.Z)
-    value = flops * world / (ms_step * 1e-3) / 1e12
+    value = weak_value(flops, world, ms_step)
     achieved = flops / (ms_step * 1e-3) / 1e12  # one attention launch per step
 
     # end to end through the public API: pinned host inputs -> device ->

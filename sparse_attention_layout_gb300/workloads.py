@@ -162,9 +162,11 @@ class AttentionWorkload:
             return layout_strided_causal(nb, local_blocks=256 // self.B, stride=16, H=H)
         raise KeyError(self.name)
 
-    def qkv(self):
+    def qkv(self, shard: int = 0):
+        """Q, K, V of the workload; `shard` selects an independent draw (one per
+        rank when several GPUs each process their own batch)."""
         shape = (self.Z, self.H, self.S, self.D)
-        base = 1000 + 10 * self.index
+        base = 1000 + 10 * self.index + 7919 * shard
         return (randn(shape, self.dtype, base + 0),
                 randn(shape, self.dtype, base + 1),
                 randn(shape, self.dtype, base + 2))
