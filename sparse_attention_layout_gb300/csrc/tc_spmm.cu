@@ -278,25 +278,29 @@ struct SddArgs {
     int Z;
 };
 
-template <int KP>
+template <int KP, int BLK>
 struct SddCfg {
     static constexpr int kTile = 128 * 64 * KP * 2;  // 128 rows x K (KP panels of 64)
-    static constexpr int kA = 0;                     // 2 stages
-    static constexpr int kB = 2 * kTile;             // 4 stages
-    static constexpr int kAlloc = 6 * kTile + 1024;
+    static constexpr int BST = 3;                    // key-tile stages
+    static constexpr int kA = 0;                     // 2 query-tile stages
+    static constexpr int kB = 2 * kTile;
+    static constexpr int kPitch = BLK * 2 + 16;      // staging row pitch (padded: no bank conflicts)
+    static constexpr int kStg = kB + BST * kTile;    // per-warp staging, 32 rows
+    static constexpr int kAlloc = kStg + 4 * 32 * kPitch + 1024;
 };
 
 template <typename T, int BLK, int KP>
 __global__ void __launch_bounds__(kThreads, 1)
 sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const SddArgs args) {
-    using C = SddCfg<KP>;
+    using C = SddCfg<KP, BLK>;
     constexpr int G = 128 / BLK;
+    constexpr int BST = C::BST;
     constexpr uint32_t kTileBytes = C::kTile;
     constexpr uint32_t kIdesc = idesc_f16(128, 128, std::is_same<T, __nv_bfloat16>::value, 0, 0);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    __shared__ uint64_t a_full[2], a_empty[2], b_full[4], b_empty[4], s_full[4], s_empty[4];
+    __shared__ uint64_t a_full[2], a_empty[2], b_full[BST], b_empty[BST], s_full[4], s_empty[4];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
@@ -309,9 +313,11 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             mbar_init(&a_full[i], 1);
             mbar_init(&a_empty[i], 1);
         }
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < BST; ++i) {
             mbar_init(&b_full[i], 1);
             mbar_init(&b_empty[i], 1);
+        }
+        for (int i = 0; i < 4; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&s_empty[i], 4);
         }
@@ -350,8 +356,8 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 ++a_it;
                 for (int n = 0; n < ns; ++n, ++g) {
                     const int s = s0 + n;
-                    const uint32_t st = g & 3;
-                    if (!mbar_wait(&b_empty[st], ((g >> 2) & 1) ^ 1, ab)) goto producer_done;
+                    const uint32_t st = g % BST;
+                    if (!mbar_wait(&b_empty[st], ((g / BST) & 1) ^ 1, ab)) goto producer_done;
                     mbar_arrive_expect_tx(&b_full[st], kTileBytes);
 #pragma unroll
                     for (int b = 0; b < G; ++b) {
@@ -375,19 +381,19 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 const uint32_t as = a_it & 1;
                 if (!mbar_wait(&a_full[as], (a_it >> 1) & 1, ab)) goto mma_done;
                 for (int n = 0; n < ns; ++n, ++g) {
-                    const uint32_t st = g & 3;
-                    if (!mbar_wait(&s_empty[st], ((g >> 2) & 1) ^ 1, ab)) goto mma_done;
-                    if (!mbar_wait(&b_full[st], (g >> 2) & 1, ab)) goto mma_done;
+                    const uint32_t sb = g & 3, st = g % BST;  // TMEM accumulator, key-tile stage
+                    if (!mbar_wait(&s_empty[sb], ((g >> 2) & 1) ^ 1, ab)) goto mma_done;
+                    if (!mbar_wait(&b_full[st], (g / BST) & 1, ab)) goto mma_done;
                     tc_fence_after();
                     const uint32_t abase = smem_u32(smem + C::kA + as * kTileBytes);
                     const uint32_t bbase = smem_u32(smem + C::kB + st * kTileBytes);
 #pragma unroll
                     for (int ks = 0; ks < KP * 4; ++ks) {
                         const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_f16(tS + st * 128, smem_desc(abase + off, 16, 1024, kSw128),
+                        mma_f16(tS + sb * 128, smem_desc(abase + off, 16, 1024, kSw128),
                                 smem_desc(bbase + off, 16, 1024, kSw128), kIdesc, ks > 0 ? 1u : 0u);
                     }
-                    mma_commit(&s_full[st]);
+                    mma_commit(&s_full[sb]);
                     mma_commit(&b_empty[st]);
                     if (n == ns - 1) mma_commit(&a_empty[as]);
                 }
@@ -396,10 +402,17 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         mma_done:;
         }
     } else {
+        // Epilogue: each warp owns 32 rows of the tile (TMEM lanes 32q..32q+31).
+        // Per present block it stages its rows in shared memory, then copies
+        // them out together: the warp's rows of one block are RS = min(32, B)
+        // consecutive rows, i.e. one contiguous RS*B run of the output.
+        constexpr int RS = BLK < 32 ? BLK : 32;
+        constexpr int C16 = BLK * 2 / 16;  // 16-byte chunks per block row
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        const int r_in = row % BLK, a = row / BLK;
+        const int a = row / BLK;
+        uint8_t* stg = smem + C::kStg + quad * 32 * C::kPitch;
         T* Cp = reinterpret_cast<T*>(args.C);
         uint32_t g = 0;
         for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
@@ -408,39 +421,48 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             const int s0 = L.tile_step_ptr[tile], ns = L.tile_step_ptr[tile + 1] - s0;
             for (int n = 0; n < ns; ++n, ++g) {
                 const int s = s0 + n;
-                const uint32_t st = g & 3;
-                bool ok = mbar_wait(&s_full[st], (g >> 2) & 1, ab);
+                const uint32_t sb = g & 3;
+                bool ok = mbar_wait(&s_full[sb], (g >> 2) & 1, ab);
                 if (!__all_sync(0xffffffffu, ok)) goto epi_done;
                 tc_fence_after();
+                uint32_t x[128];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32_sync(tS + st * 128 + lane_base + c * 32, r);
-                    // columns c*32 .. c*32+31 belong to slot (c*32)/BLK (BLK >= 32) or to
-                    // 32/BLK consecutive slots (BLK = 16)
-#pragma unroll
-                    for (int part = 0; part < (BLK < 32 ? 32 / BLK : 1); ++part) {
-                        const int col0 = c * 32 + part * BLK;
-                        const int b = col0 / BLK;
-                        const int blk = L.step_blk[(s * G + a) * G + b];
-                        if (blk < 0) continue;
-                        const int len = BLK < 32 ? BLK : 32;
-                        T* dst = Cp + (((int64_t)z * L.nnz + blk) * BLK + r_in) * BLK + (col0 % BLK);
-#pragma unroll
-                        for (int j = 0; j < len; j += 8) {
-                            const int o = part * BLK + j;
-                            uint4 pk;
-                            pk.x = Pack2<T>::pack(__uint_as_float(r[o]), __uint_as_float(r[o + 1]));
-                            pk.y = Pack2<T>::pack(__uint_as_float(r[o + 2]), __uint_as_float(r[o + 3]));
-                            pk.z = Pack2<T>::pack(__uint_as_float(r[o + 4]), __uint_as_float(r[o + 5]));
-                            pk.w = Pack2<T>::pack(__uint_as_float(r[o + 6]), __uint_as_float(r[o + 7]));
-                            *reinterpret_cast<uint4*>(dst + j) = pk;
-                        }
-                    }
-                }
+                for (int c = 0; c < 4; ++c)
+                    tmem_ld32_sync(tS + sb * 128 + lane_base + c * 32,
+                                   *reinterpret_cast<uint32_t(*)[32]>(x + 32 * c));
+                // the accumulator is free as soon as it is in registers
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&s_empty[st]);
+                if (lane == 0) mbar_arrive(&s_empty[sb]);
+#pragma unroll
+                for (int b = 0; b < G; ++b) {
+                    const int blk = L.step_blk[(s * G + a) * G + b];
+                    if (__all_sync(0xffffffffu, blk < 0)) continue;
+                    if (blk >= 0) {
+                        uint4* srow = reinterpret_cast<uint4*>(stg + lane * C::kPitch);
+#pragma unroll
+                        for (int j = 0; j < C16; ++j) {
+                            const int o = b * BLK + 8 * j;
+                            srow[j] = make_uint4(
+                                Pack2<T>::pack(__uint_as_float(x[o]), __uint_as_float(x[o + 1])),
+                                Pack2<T>::pack(__uint_as_float(x[o + 2]), __uint_as_float(x[o + 3])),
+                                Pack2<T>::pack(__uint_as_float(x[o + 4]), __uint_as_float(x[o + 5])),
+                                Pack2<T>::pack(__uint_as_float(x[o + 6]), __uint_as_float(x[o + 7])));
+                        }
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int seg = 0; seg < 32 / RS; ++seg) {
+                        const int sblk = __shfl_sync(0xffffffffu, blk, seg * RS);
+                        if (sblk < 0) continue;
+                        const int r_in0 = (quad * 32 + seg * RS) % BLK;
+                        uint4* dst = reinterpret_cast<uint4*>(Cp + (((int64_t)z * L.nnz + sblk) * BLK + r_in0) * BLK);
+                        for (int k = lane; k < RS * C16; k += 32)
+                            dst[k] = *reinterpret_cast<const uint4*>(stg + (seg * RS + k / C16) * C::kPitch +
+                                                                     (k % C16) * 16);
+                    }
+                    __syncwarp();
+                }
             }
         }
     epi_done:;
@@ -519,7 +541,7 @@ int sdd_launch(const bsp_layout_s* Lh, const void* A, const void* B, void* Cout,
     if (rc) return rc;
     SddArgs a{Lh->view, Cout, Z};
     auto kern = sdd_tc_kernel<T, BLK, KP>;
-    constexpr int smem = SddCfg<KP>::kAlloc;
+    constexpr int smem = SddCfg<KP, BLK>::kAlloc;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return BSP_ERR_CUDA;
     const int64_t total = (int64_t)Z * Lh->n_tiles;
