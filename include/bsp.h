@@ -151,6 +151,33 @@ int bsp_dds(bsp_layout_t layout, int dtype, const void* A, const void* B_sp, voi
 int bsp_softmax(bsp_layout_t layout, int dtype, const void* X, void* Y, int Z, float scale,
                 int mask_kind, const uint8_t* mask, void* stream);
 
+/* Allocation-free variant of bsp_softmax (the pages have no counterpart: this
+ * entry point exists for deployment, not for the method).  Some callers cannot
+ * allocate device memory -- a serving runtime that reserves the whole GPU for
+ * its own memory pool, a plugin that is handed only its input and output
+ * buffers -- and so cannot create a compiled layout handle, whose tables live
+ * in memory bsp_layout_compile allocates.  This call takes the HOST layout
+ * (uint8 [H][nb][nb], as for bsp_layout_compile), builds the tables on the
+ * host on every call and uploads them into a fixed array of device memory
+ * that the library declares itself (4 MiB, held by every GPU that loads the
+ * library until the process exits).  It calls no cudaMalloc / cudaFree and no
+ * allocating library routine; the caller still passes X and Y (device,
+ * [Z][nnz][block][block], Y may equal X) and, for BSP_MASK_DENSE, the mask.
+ * Results equal bsp_softmax's.
+ *  - Layouts whose tables (row pointers, block columns, block ids and the
+ *    softmax chunk list) exceed the array return BSP_ERR_OOM and launch
+ *    nothing.
+ *  - The first call on a device looks up the array's device address with that
+ *    device current; make that first call before any stream capture.
+ *  - Every call shares the array and it keeps the last call's tables; calls
+ *    that overlap on the GPU (e.g. on two streams) race.  Calls ordered on one
+ *    stream are safe.
+ *  - Device-side timeouts are recorded in the array's status word, which this
+ *    entry point clears at the start of each call but does not report. */
+int bsp_softmax_noalloc(const uint8_t* layout, int H, int nb, int block, int dtype, const void* X,
+                        void* Y, int Z, float scale, int mask_kind, const uint8_t* mask,
+                        void* stream);
+
 /* ---- attention --------------------------------------------------------- */
 
 /* Fused block-sparse attention: O = softmax(scale Q K^T restricted to the
