@@ -19,8 +19,8 @@
 //               barrier waits and commits, which cost about as much as the MMAs.
 //   warps 2..9  softmax, two warpgroups: thread = one query row = one TMEM
 //               lane, each warpgroup owning half of the row's 128 scores.
-//               Reads S from TMEM, masks, keeps (m, l) (both groups take the
-//               full-row max; partial sums meet per tile), writes its half of
+//               Reads S from TMEM, masks, keeps (m, l) (the half-row maxima
+//               meet every step, partial sums per tile), writes its half of
 //               P (bf16/fp16) into the TMEM P buffer of the step (two
 //               buffers, so step g only waits for P V of step g-2), rescales
 //               its half of O in TMEM only when the row max grew by more than
@@ -85,7 +85,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     // done) also frees its V tile and its P buffer.
     __shared__ uint64_t q_full[QST], q_empty[QST], k_full[2], v_full[2];
     __shared__ uint64_t s_full[2], p_full[2], pv_done[2], xchg;
-    __shared__ float lsum[2][128];  // partial row sums [warpgroup][row]
+    __shared__ float lsum[2][128];     // partial row sums [warpgroup][row]
+    // half-row maxima [step parity][warpgroup][row]; a warp rewrites a parity only
+    // after every warp has passed the other parity's exchange, i.e. read this one
+    __shared__ float xmax[2][2][128];
+    __shared__ uint64_t xm[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
@@ -109,6 +113,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             mbar_init(&p_full[i], 8);
         }
         mbar_init(&xchg, 8);
+        mbar_init(&xm[0], 8);
+        mbar_init(&xm[1], 8);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -234,12 +240,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         }
     } else {
         // ------------------------------------------- softmax / epilogue ----
-        // Two warpgroups split each row: both read all 128 scores and take the
-        // full row max (so they make identical decisions without talking), but
-        // warpgroup wg exponentiates and stores only columns [64 wg, 64 wg + 64)
-        // (P panel wg) and owns output columns [wg D/2, wg D/2 + D/2).  The two
-        // partial row sums meet once per tile through shared memory, ordered by
-        // the xchg mbarrier (8 warp arrivals).
+        // Two warpgroups split each row: warpgroup wg owns score columns
+        // [64 wg, 64 wg + 64) (its half of P) and output columns
+        // [wg D/2, wg D/2 + D/2).  The half-row maxima meet every step through
+        // shared memory (xm barriers, 8 warp arrivals), so both groups take the
+        // same decisions; the partial row sums meet once per tile (xchg).
         constexpr int W = BLK < 64 ? BLK : 64;  // columns of one slot inside a half
         constexpr int LS = 64 / W;              // slots (or slot parts) per half
         const int sw = warp - 2, wg = sw >> 2;
@@ -305,29 +310,30 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const int rseq = gq * 128 + row;  // query position inside the sequence
             T* orow = reinterpret_cast<T*>(args.O) + (((int64_t)z * L.H + h) * S + rseq) * D + wg * (D / 2);
             float m = -INFINITY, l = 0.f;
-            Half own, oth, nown, noth;
-            if (ns > 0) {
-                fetch(s0, wg, nown);
-                fetch(s0, wg ^ 1, noth);
-            }
+            Half own, nown;
+            if (ns > 0) fetch(s0, wg, nown);
             for (int n = 0; n < ns; ++n, ++g) {
                 own = nown;
-                oth = noth;
-                if (n + 1 < ns) {  // next step's metadata: latency hidden behind this step
-                    fetch(s0 + n + 1, wg, nown);
-                    fetch(s0 + n + 1, wg ^ 1, noth);
-                }
+                if (n + 1 < ns) fetch(s0 + n + 1, wg, nown);  // next step: latency hidden behind this one
                 bool ok = mbar_wait(&s_full[g & 1], (g >> 1) & 1, ab);
                 if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
                 tc_fence_after();
-                // raw scores (the scale is applied inside the exponent): own half x, other half y
-                float x[64], y[64];
+                // raw scores of this half (the scale is applied inside the exponent)
+                float x[64];
                 const uint32_t srow = tS + (g & 1) * 128 + lane_base;
                 tmem_ld64_sync(srow + wg * 64, srow + wg * 64 + 32, *reinterpret_cast<uint32_t(*)[64]>(x));
-                tmem_ld64_sync(srow + (wg ^ 1) * 64, srow + (wg ^ 1) * 64 + 32, *reinterpret_cast<uint32_t(*)[64]>(y));
                 mask_half(x, wg, own, rb, rseq);
-                mask_half(y, wg ^ 1, oth, rb, rseq);
-                const float mx = fmaxf(max64(x), max64(y));
+                // row max: this half's, then the partner half's through shared memory
+                float mx = max64(x);
+                {
+                    const uint32_t xp = g & 1;
+                    xmax[xp][wg][row] = mx;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&xm[xp]);
+                    ok = mbar_wait(&xm[xp], (g >> 1) & 1, ab);
+                    if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
+                    mx = fmaxf(mx, xmax[xp][wg ^ 1][row]);
+                }
                 // m is kept in the scaled log2 domain (scale > 0 commutes with max); both
                 // warpgroups see the same maxima, so they take the same decisions
                 const float m_new = fmaxf(m, mx * args.c2);
