@@ -11,21 +11,28 @@
 // pair that is not in the layout is masked to -inf, as are entries the intra-
 // block mask removes.  Persistent CTAs walk the tiles longest-first.
 //
-// Roles (352 threads, one CTA per SM):
+// Roles (512 threads, one CTA per SM):
 //   warp 0      TMA producer: Q tile (2 stages), K and V tiles (2 stages each)
 //   warp 1      TMEM owner; one thread issues S[g%2] = Q K^T (M=128, N=128, K=D)
-//   warp 10     one thread issues O += P V (M=128, N=D, K=128; P from TMEM, V
+//   warp 2      one thread issues O += P V (M=128, N=D, K=128; P from TMEM, V
 //               MN-major).  Two issuing threads halve each one's per-step
 //               barrier waits and commits, which cost about as much as the MMAs.
-//   warps 2..9  softmax, two warpgroups: thread = one query row = one TMEM
+//   warp 3      idle
+//   warps 4..7  epilogue: as soon as the last P V of a tile has completed they
+//               read O out of TMEM (thread = row), hand the accumulator back to
+//               the next tile, scale by 1 / l and write the tile through a
+//               128-byte-swizzled shared-memory panel with TMA stores.  The
+//               next tile's softmax runs meanwhile, so the tensor core does not
+//               wait for the output write.
+//   warps 8..15 softmax, two warpgroups: thread = one query row = one TMEM
 //               lane, each warpgroup owning half of the row's 128 scores.
 //               Reads S from TMEM, masks, keeps (m, l) (the half-row maxima
 //               meet every step, partial sums per tile), writes its half of
 //               P (bf16/fp16) into the TMEM P buffer of the step (two
 //               buffers, so step g only waits for P V of step g-2), rescales
 //               its half of O in TMEM only when the row max grew by more than
-//               2^8 (the final O / l is exact either way), and runs the
-//               epilogue O / l.
+//               2^8 (the final O / l is exact either way), and hands the
+//               tile's partial sums to the epilogue.
 // TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D), P0 [384,448), P1 [448,512)
 // (P packed two 16-bit values per column; P V takes its A operand from TMEM).
 #pragma once
@@ -41,7 +48,7 @@ namespace attn {
 
 using namespace tc;
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when max grows by > 256x
 
 template <int D>
@@ -53,7 +60,8 @@ struct AttnSmem {
     static constexpr int kQ = 0;
     static constexpr int kK = kQ + QST * kTile;
     static constexpr int kV = kK + KVST * kTile;
-    static constexpr int kBytes = kV + KVST * kTile;
+    static constexpr int kEpi = kV + KVST * kTile;    // epilogue staging: one 32 x 64 panel per warp
+    static constexpr int kBytes = kEpi + 4 * 4096;
     static constexpr int kAlloc = kBytes + 1024;      // slack for 1024-byte alignment
 };
 
@@ -69,7 +77,8 @@ struct AttnArgs {
 template <typename T, int BLK, int D, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
 attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const AttnArgs args) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const AttnArgs args) {
     using SM = AttnSmem<D>;
     constexpr int G = 128 / BLK;
     constexpr int KP = SM::KP;
@@ -84,8 +93,12 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     // (Q K^T of the step done) also frees its K tile, pv_done[b] (P V of the step
     // done) also frees its V tile and its P buffer.
     __shared__ uint64_t q_full[QST], q_empty[QST], k_full[2], v_full[2];
-    __shared__ uint64_t s_full[2], p_full[2], pv_done[2], xchg;
-    __shared__ float lsum[2][128];     // partial row sums [warpgroup][row]
+    __shared__ uint64_t s_full[2], p_full[2], pv_done[2];
+    // O accumulator: o_full = last P V of the tile completed, o_empty = the
+    // epilogue has read it.  Row sums: lsum[tile parity][warpgroup][row], with
+    // l_full (softmax wrote them) and l_empty (the epilogue read them).
+    __shared__ uint64_t o_full, o_empty, l_full[2], l_empty[2];
+    __shared__ float lsum[2][2][128];
     // half-row maxima [step parity][warpgroup][row]; a warp rewrites a parity only
     // after every warp has passed the other parity's exchange, i.e. read this one
     __shared__ float xmax[2][2][128];
@@ -112,9 +125,13 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             // steps back has completed, i.e. after every warp arrived
             mbar_init(&p_full[i], 8);
         }
-        mbar_init(&xchg, 8);
-        mbar_init(&xm[0], 8);
-        mbar_init(&xm[1], 8);
+        mbar_init(&o_full, 1);
+        mbar_init(&o_empty, 4);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&l_full[i], 8);
+            mbar_init(&l_empty[i], 4);
+            mbar_init(&xm[i], 8);
+        }
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -214,14 +231,17 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             }
         qk_done:;
         }
-    } else if (warp == 10) {
+    } else if (warp == 2) {
         // --------------------------------------------- P V issuer (one thread) ----
         if (lane == 0) {
             const uint64_t dv = smem_desc(smem_u32(smem + SM::kV), 128 * 128, 1024, kSw128);
-            uint32_t g = 0;
+            uint32_t g = 0, tc = 0;  // tc: tiles with at least one step so far
             for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
                 const int tile = L.tile_order[w / args.Z];
                 const int ns = L.tile_step_ptr[tile + 1] - L.tile_step_ptr[tile];
+                if (ns == 0) continue;
+                // the previous tile's O must have been read by the epilogue
+                if (tc > 0 && !mbar_wait(&o_empty, (tc - 1) & 1, ab)) goto pv_done_label;
                 for (int n = 0; n < ns; ++n, ++g) {
                     const uint32_t st = g & 1;
                     // P of step g written (and O rescaled) by all softmax warps; V landed
@@ -235,24 +255,101 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                                        (ks > 0 || n > 0) ? 1u : 0u);
                     mma_commit(&pv_done[st]);
                 }
+                mma_commit(&o_full);
+                ++tc;
             }
         pv_done_label:;
         }
-    } else {
-        // ------------------------------------------- softmax / epilogue ----
+    } else if (warp >= 4 && warp < 8) {
+        // ---------------------------------------------------- epilogue ----
+        // Warp q owns rows [32 q, 32 q + 32) of the tile (TMEM lanes of its
+        // quadrant).  O / l leaves through a 32 x 64 staging panel per warp in
+        // the 128-byte-swizzled layout (16-byte chunk j of row r at chunk
+        // j ^ (r % 8), so the row-per-thread writes hit distinct banks) and
+        // one TMA store per panel; rows past the sequence end are clipped by
+        // the tensor map.
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        uint8_t* stage = smem + SM::kEpi + quad * 4096;
+        const uint32_t stage_s = smem_u32(stage);
+        uint32_t tc = 0;
+        for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+            const int tile = L.tile_order[w / args.Z];
+            const int z = (int)(w % args.Z);
+            const int h = tile / L.ngroups, gq = tile % L.ngroups;
+            const int ns = L.tile_step_ptr[tile + 1] - L.tile_step_ptr[tile];
+            const int y0 = gq * 128 + quad * 32;  // first sequence row of this warp
+            const int32_t zh = (int32_t)((int64_t)z * L.H + h);
+            const bool live = ns > 0;
+            const uint32_t lb = tc & 1;
+            float inv = 0.f;  // rows with nothing kept are 0
+            if (live) {
+                bool ok = mbar_wait(&l_full[lb], (tc >> 1) & 1, ab);
+                if (!__all_sync(0xffffffffu, ok)) goto epilogue_done;
+                const float lt = lsum[lb][0][row] + lsum[lb][1][row];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&l_empty[lb]);
+                inv = lt > 0.f ? 1.0f / lt : 0.f;
+                ok = mbar_wait(&o_full, tc & 1, ab);
+                if (!__all_sync(0xffffffffu, ok)) goto epilogue_done;
+                tc_fence_after();
+            }
+            // one 64-column panel at a time: TMEM -> registers (scaled, packed) ->
+            // staging panel -> TMA store; O is handed back after the last load
+#pragma unroll
+            for (int p = 0; p < KP; ++p) {
+                uint32_t pk[32];
+                if (live) {
+                    uint32_t r[64];
+                    tmem_ld64_sync(tO + lane_base + p * 64, tO + lane_base + p * 64 + 32, r);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        pk[k] = Pack2<T>::pack(__uint_as_float(r[2 * k]) * inv, __uint_as_float(r[2 * k + 1]) * inv);
+                    if (p == KP - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&o_empty);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) pk[k] = 0u;
+                }
+                if (y0 < S) {
+                    if (lane == 0) bulk_wait_read_all();  // the panel's previous store has read it
+                    __syncwarp();
+                    uint8_t* rp = stage + lane * 128;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<uint4*>(rp + ((j ^ (lane & 7)) << 4)) =
+                            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&tmO, stage_s, p * 64, y0, zh);
+                        bulk_commit();
+                    }
+                }
+            }
+            if (live) ++tc;
+        }
+    epilogue_done:
+        if (lane == 0) bulk_wait_all();
+    } else if (warp >= 8) {
+        // ---------------------------------------------------- softmax ----
         // Two warpgroups split each row: warpgroup wg owns score columns
         // [64 wg, 64 wg + 64) (its half of P) and output columns
         // [wg D/2, wg D/2 + D/2).  The half-row maxima meet every step through
         // shared memory (xm barriers, 8 warp arrivals), so both groups take the
-        // same decisions; the partial row sums meet once per tile (xchg).
+        // same decisions; the partial row sums go to the epilogue once per tile.
         constexpr int W = BLK < 64 ? BLK : 64;  // columns of one slot inside a half
         constexpr int LS = 64 / W;              // slots (or slot parts) per half
-        const int sw = warp - 2, wg = sw >> 2;
+        const int sw = warp - 8, wg = sw >> 2;
         const int quad = warp & 3;
         const int row = quad * 32 + lane;  // query row inside the tile = TMEM lane
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const int r_in = row % BLK, a = row / BLK;
-        uint32_t g = 0, xg = 0;
+        uint32_t g = 0, tc = 0;
         // metadata of one half: block id at (row block a, slot) and block-column, per slot part
         struct Half {
             int blk[LS], cb[LS];
@@ -302,16 +399,14 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         };
         for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
             const int tile = L.tile_order[w / args.Z];
-            const int z = (int)(w % args.Z);
-            const int h = tile / L.ngroups, gq = tile % L.ngroups;
+            const int gq = tile % L.ngroups;
             const int s0 = L.tile_step_ptr[tile], ns = L.tile_step_ptr[tile + 1] - s0;
+            if (ns == 0) continue;            // the epilogue writes the zero rows
             const int rb = gq * G + a;        // block-row of this thread's query row
-            const bool row_valid = rb < L.nb;
             const int rseq = gq * 128 + row;  // query position inside the sequence
-            T* orow = reinterpret_cast<T*>(args.O) + (((int64_t)z * L.H + h) * S + rseq) * D + wg * (D / 2);
             float m = -INFINITY, l = 0.f;
             Half own, nown;
-            if (ns > 0) fetch(s0, wg, nown);
+            fetch(s0, wg, nown);
             for (int n = 0; n < ns; ++n, ++g) {
                 own = nown;
                 if (n + 1 < ns) fetch(s0 + n + 1, wg, nown);  // next step: latency hidden behind this one
@@ -328,6 +423,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 {
                     const uint32_t xp = g & 1;
                     xmax[xp][wg][row] = mx;
+                    tc_fence_before();  // this warp's S loads are complete before the other half writes P
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&xm[xp]);
                     ok = mbar_wait(&xm[xp], (g >> 1) & 1, ab);
@@ -383,41 +479,19 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[g & 1]);
             }
-            // epilogue: O / l -> global (rows with nothing kept are 0)
-            float inv = 0.f;
-            if (ns > 0) {
-                lsum[wg][row] = l;
+            // partial row sums of the tile -> epilogue (buffer tc % 2, free once
+            // the epilogue has read the sums of tile tc - 2)
+            {
+                const uint32_t lb = tc & 1;
+                if (tc >= 2) {
+                    bool ok = mbar_wait(&l_empty[lb], ((tc - 2) >> 1) & 1, ab);
+                    if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
+                }
+                lsum[lb][wg][row] = l;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&xchg);
-                bool okx = mbar_wait(&xchg, xg & 1, ab);
-                ++xg;
-                if (!__all_sync(0xffffffffu, okx)) goto softmax_done;
-                const float lt = l + lsum[wg ^ 1][row];
-                inv = lt > 0.f ? 1.0f / lt : 0.f;
-                bool ok = mbar_wait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, ab);
-                if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
-                tc_fence_after();
+                if (lane == 0) mbar_arrive(&l_full[lb]);
+                ++tc;
             }
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-                uint32_t r[32];
-                if (ns > 0) {
-                    tmem_ld32_sync(tO + lane_base + wg * (D / 2) + c * 32, r);
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) r[k] = 0u;
-                }
-                uint32_t o[16];
-#pragma unroll
-                for (int k = 0; k < 16; ++k)
-                    o[k] = Pack2<T>::pack(__uint_as_float(r[2 * k]) * inv, __uint_as_float(r[2 * k + 1]) * inv);
-                if (row_valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) dst[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-                }
-            }
-            tc_fence_before();
         }
     softmax_done:;
     }
@@ -439,6 +513,8 @@ int launch_attn(const bsp_layout_s* Lh, const void* Q, const void* K, const void
     int rc = make_tmap_2d(&mq, Q, is_bf16, rows, D, 128, 64, 128);
     if (!rc) rc = make_tmap_2d(&mk, K, is_bf16, rows, D, BLK, 64, 128);
     if (!rc) rc = make_tmap_2d(&mv, V, is_bf16, rows, D, BLK, 64, 128);
+    CUtensorMap mo;
+    if (!rc) rc = make_tmap_3d(&mo, O, is_bf16, D, Lh->S, (uint64_t)Z * Lh->H, 64, 32);
     if (rc) return rc;
     AttnArgs args{Lh->view, O, mask, Z, kind, scale * kLog2e};
     auto kern = attention_tc_kernel<T, BLK, D, KIND>;
@@ -447,7 +523,7 @@ int launch_attn(const bsp_layout_s* Lh, const void* Q, const void* K, const void
         return BSP_ERR_CUDA;
     const int64_t total = (int64_t)Z * Lh->n_tiles;
     const int grid = (int)std::min<int64_t>(total, sm_count());
-    kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, args);
+    kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, mo, args);
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }
 

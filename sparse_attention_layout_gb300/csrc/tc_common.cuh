@@ -129,6 +129,17 @@ __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Tiled 3-D store shared -> global (bulk group; coordinates innermost first).
+// Rows past the tensor's extent in any dimension are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y,
+                                             int32_t z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(src)
+                 : "memory");
+}
+// wait until every committed bulk store has completed (its writes included)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -298,5 +309,9 @@ template <> struct Pack2<__half> {
 // elements, box [box_rows][box_cols], 128-byte swizzle unless given)
 int make_tmap_2d(CUtensorMap* map, const void* base, int is_bf16, uint64_t rows, uint64_t cols,
                  uint32_t box_rows, uint32_t box_cols, int swizzle_bytes);
+// host: 3-D tiled tensor map of 2-byte elements [d2][d1][d0] (d0 contiguous),
+// box [1][box1][box0], 128-byte swizzle
+int make_tmap_3d(CUtensorMap* map, const void* base, int is_bf16, uint64_t d0, uint64_t d1, uint64_t d2,
+                 uint32_t box0, uint32_t box1);
 
 }  // namespace bsp

@@ -43,4 +43,18 @@ int make_tmap_2d(CUtensorMap* map, const void* base, int is_bf16, uint64_t rows,
     return r == CUDA_SUCCESS ? BSP_OK : BSP_ERR_UNSUPPORTED;
 }
 
+int make_tmap_3d(CUtensorMap* map, const void* base, int is_bf16, uint64_t d0, uint64_t d1, uint64_t d2,
+                 uint32_t box0, uint32_t box1) {
+    auto fn = encode_fn();
+    if (!fn) return BSP_ERR_CUDA;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    const cuuint32_t box[3] = {box0, box1, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? BSP_OK : BSP_ERR_UNSUPPORTED;
+}
+
 }  // namespace bsp
