@@ -188,6 +188,16 @@ int bsp_attention(bsp_layout_t layout, int dtype, const void* Q, const void* K, 
                   void* O, int Z, int D, float scale, int mask_kind, const uint8_t* mask,
                   void* stream);
 
+/* ---- diagnostics ------------------------------------------------------- */
+
+/* Evaluate, on n DEVICE floats x, the software 2^x that the attention softmax
+ * computes on the FMA pipe for part of its score columns (range reduction to
+ * x = j + f, |f| <= 1/2, a cubic for 2^f, j added to the exponent; maximum
+ * relative error 1.02e-4 for x >= -125; inputs below -125, -inf included,
+ * give a value in (0, 2^-124.5]).  y: DEVICE float [n] (output).  Enqueued on
+ * `stream`.  The method is the implementation's, not the pages'. */
+int bsp_diag_exp2(const float* x, float* y, int64_t n, void* stream);
+
 /* ---- status ------------------------------------------------------------ */
 
 /* Synchronise `stream`, then return and clear the handle's device status

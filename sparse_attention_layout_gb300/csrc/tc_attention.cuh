@@ -12,27 +12,27 @@
 // block mask removes.  Persistent CTAs walk the tiles longest-first.
 //
 // Roles (512 threads, one CTA per SM):
-//   warp 0      TMA producer: Q tile (2 stages), K and V tiles (2 stages each)
+//   warps 0, 3  TMA producers: warp 0 the Q tile (2 stages) and K tiles, warp 3
+//               the V tiles (2 stages each), so that K never waits behind V
 //   warp 1      TMEM owner; one thread issues S[g%2] = Q K^T (M=128, N=128, K=D)
 //   warp 2      one thread issues O += P V (M=128, N=D, K=128; P from TMEM, V
 //               MN-major).  Two issuing threads halve each one's per-step
 //               barrier waits and commits, which cost about as much as the MMAs.
-//   warp 3      idle
 //   warps 4..7  epilogue: as soon as the last P V of a tile has completed they
 //               read O out of TMEM (thread = row), hand the accumulator back to
 //               the next tile, scale by 1 / l and write the tile through a
 //               128-byte-swizzled shared-memory panel with TMA stores.  The
 //               next tile's softmax runs meanwhile, so the tensor core does not
 //               wait for the output write.
-//   warps 8..15 softmax, two warpgroups: thread = one query row = one TMEM
-//               lane, each warpgroup owning half of the row's 128 scores.
-//               Reads S from TMEM, masks, keeps (m, l) (the half-row maxima
-//               meet every step, partial sums per tile), writes its half of
-//               P (bf16/fp16) into the TMEM P buffer of the step (two
-//               buffers, so step g only waits for P V of step g-2), rescales
-//               its half of O in TMEM only when the row max grew by more than
+//   warps 8..15 softmax, two warpgroups taking alternate steps: thread = one
+//               query row = one TMEM lane, whole rows of 128 scores.  Reads S
+//               from TMEM, masks, takes the row max, receives the running max
+//               of the previous step from the other warpgroup and passes its
+//               own on, writes P (bf16/fp16) into the TMEM P buffer of the
+//               step (two buffers, so step g only waits for P V of step g-2),
+//               rescales O in TMEM only when the running max grew by more than
 //               2^8 (the final O / l is exact either way), and hands the
-//               tile's partial sums to the epilogue.
+//               tile's row sums to the epilogue.
 // TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D), P0 [384,448), P1 [448,512)
 // (P packed two 16-bit values per column; P V takes its A operand from TMEM).
 #pragma once
@@ -49,7 +49,21 @@ namespace attn {
 using namespace tc;
 
 constexpr int kThreads = 512;
+// Registers per thread after the split at kernel start (launched with 128):
+// warps 0-3 (producers, issuers) and 4-7 (epilogue) give some to the two
+// softmax warpgroups.  128 threads x (56 + 88 + 184 + 184) = 65536 =
+// 512 threads x 128, the block's allocation at launch.
+constexpr uint32_t kRegsLaunch = 128, kRegsCtl = 56, kRegsEpi = 88, kRegsSoftmax = 184;
+static_assert(kRegsCtl + kRegsEpi + 2 * kRegsSoftmax <= 4 * kRegsLaunch, "register split exceeds the launch allocation");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when max grows by > 256x
+// Of every 8 column pairs of a score row, this many take 2^x from the FMA-pipe
+// polynomial and the rest from the special-function unit: with one thread per
+// row, the special-function unit alone would need as long per step as both
+// matrix products.
+#ifndef BSP_ATTN_POLY_PAIRS
+#define BSP_ATTN_POLY_PAIRS 0
+#endif
+constexpr int kPolyPairs = BSP_ATTN_POLY_PAIRS;
 
 template <int D>
 struct AttnSmem {
@@ -98,11 +112,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     // epilogue has read it.  Row sums: lsum[tile parity][warpgroup][row], with
     // l_full (softmax wrote them) and l_empty (the epilogue read them).
     __shared__ uint64_t o_full, o_empty, l_full[2], l_empty[2];
-    __shared__ float lsum[2][2][128];
-    // half-row maxima [step parity][warpgroup][row]; a warp rewrites a parity only
-    // after every warp has passed the other parity's exchange, i.e. read this one
-    __shared__ float xmax[2][2][128];
-    __shared__ uint64_t xm[2];
+    __shared__ float lsum[2][2][128], lref[2][2][128];  // each warpgroup's sum and its reference max
+    // running max after step g, handed to the warpgroup of step g + 1:
+    // mrun[g % 2][row], published by m_pub[g % 2] (4 warp arrivals)
+    __shared__ float mrun[2][128];
+    __shared__ uint64_t m_pub[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
 
@@ -121,16 +135,15 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             mbar_init(&v_full[i], 1);
             mbar_init(&s_full[i], 1);
             mbar_init(&pv_done[i], 1);
-            // one per P buffer: a warp re-arrives on a buffer only after P V two
-            // steps back has completed, i.e. after every warp arrived
-            mbar_init(&p_full[i], 8);
+            // the 4 warps of the warpgroup that owns steps of this parity
+            mbar_init(&p_full[i], 4);
         }
         mbar_init(&o_full, 1);
         mbar_init(&o_empty, 4);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&l_full[i], 8);
             mbar_init(&l_empty[i], 4);
-            mbar_init(&xm[i], 8);
+            mbar_init(&m_pub[i], 4);
         }
         fence_barrier_init();
     }
@@ -148,12 +161,20 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const int64_t total = (int64_t)args.Z * L.n_tiles;
     const int S = L.S;
 
-    if (warp == 0) {
-        // ------------------------------------------------ TMA producer ----
+    // Each warpgroup changes its register share first thing in its own branch
+    // (so the new limit holds for all of the role's code), before any role can
+    // leave early.
+    if (warp < 4) {
+    regs_dec<kRegsCtl>();
+    if (warp == 0 || warp == 3) {
+        // ----------------------------------------------- TMA producers ----
+        // warp 0 loads Q and K, warp 3 loads V: the K tile of a step waits only
+        // for Q K^T two steps back, never behind a V tile whose P V is late.
         if (lane == 0) {
-            tma_prefetch_desc(&tmQ);
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
+            const bool is_v = warp == 3;
+            const CUtensorMap* tm = is_v ? &tmV : &tmK;
+            if (!is_v) tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(tm);
             uint32_t q_it = 0, g = 0;
             for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
                 const int tile = L.tile_order[w / args.Z];
@@ -162,13 +183,15 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 const int s0 = L.tile_step_ptr[tile], ns = L.tile_step_ptr[tile + 1] - s0;
                 if (ns == 0) continue;
                 const int64_t zh = (int64_t)z * L.H + h;
-                const uint32_t qs = q_it % QST;
-                if (!mbar_wait(&q_empty[qs], ((q_it / QST) & 1) ^ 1, ab)) break;
-                mbar_arrive_expect_tx(&q_full[qs], kTileBytes);
-                for (int p = 0; p < KP; ++p)
-                    tma_load_2d(smem_u32(smem + SM::kQ + qs * kTileBytes + p * 16384), &tmQ, p * 64,
-                                (int32_t)(zh * S + gq * 128), &q_full[qs]);
-                ++q_it;
+                if (!is_v) {
+                    const uint32_t qs = q_it % QST;
+                    if (!mbar_wait(&q_empty[qs], ((q_it / QST) & 1) ^ 1, ab)) break;
+                    mbar_arrive_expect_tx(&q_full[qs], kTileBytes);
+                    for (int p = 0; p < KP; ++p)
+                        tma_load_2d(smem_u32(smem + SM::kQ + qs * kTileBytes + p * 16384), &tmQ, p * 64,
+                                    (int32_t)(zh * S + gq * 128), &q_full[qs]);
+                    ++q_it;
+                }
                 for (int n = 0; n < ns; ++n, ++g) {
                     const int s = s0 + n;
                     const uint32_t st = g & 1;
@@ -178,22 +201,18 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                         const int c = L.step_col[s * G + b];
                         cols[b] = c >= 0 ? c : L.step_col[s * G];  // padding slot: any valid block
                     }
-                    // K tile of step g - 2 is free once its Q K^T has completed
-                    if (g >= 2 && !mbar_wait(&s_full[st], ((g - 2) >> 1) & 1, ab)) goto producer_done;
-                    mbar_arrive_expect_tx(&k_full[st], kTileBytes);
+                    // stage g % 2 is free once step g - 2 has used it: Q K^T for a K
+                    // tile, P V for a V tile
+                    uint64_t* full = is_v ? &v_full[st] : &k_full[st];
+                    uint64_t* freed = is_v ? &pv_done[st] : &s_full[st];
+                    if (g >= 2 && !mbar_wait(freed, ((g - 2) >> 1) & 1, ab)) goto producer_done;
+                    mbar_arrive_expect_tx(full, kTileBytes);
+                    const uint32_t base = smem_u32(smem + (is_v ? SM::kV : SM::kK) + st * kTileBytes);
 #pragma unroll
                     for (int b = 0; b < G; ++b)
                         for (int p = 0; p < KP; ++p)
-                            tma_load_2d(smem_u32(smem + SM::kK + st * kTileBytes + p * 16384 + b * BLK * 128), &tmK,
-                                        p * 64, (int32_t)(zh * S + (int64_t)cols[b] * BLK), &k_full[st]);
-                    // V tile of step g - 2 is free once its P V has completed
-                    if (g >= 2 && !mbar_wait(&pv_done[st], ((g - 2) >> 1) & 1, ab)) goto producer_done;
-                    mbar_arrive_expect_tx(&v_full[st], kTileBytes);
-#pragma unroll
-                    for (int b = 0; b < G; ++b)
-                        for (int p = 0; p < KP; ++p)
-                            tma_load_2d(smem_u32(smem + SM::kV + st * kTileBytes + p * 16384 + b * BLK * 128), &tmV,
-                                        p * 64, (int32_t)(zh * S + (int64_t)cols[b] * BLK), &v_full[st]);
+                            tma_load_2d(base + p * 16384 + b * BLK * 128, tm, p * 64,
+                                        (int32_t)(zh * S + (int64_t)cols[b] * BLK), full);
                 }
             }
         producer_done:;
@@ -260,7 +279,9 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             }
         pv_done_label:;
         }
-    } else if (warp >= 4 && warp < 8) {
+    }
+    } else if (warp < 8) {
+        regs_dec<kRegsEpi>();
         // ---------------------------------------------------- epilogue ----
         // Warp q owns rows [32 q, 32 q + 32) of the tile (TMEM lanes of its
         // quadrant).  O / l leaves through a 32 x 64 staging panel per warp in
@@ -287,9 +308,14 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             if (live) {
                 bool ok = mbar_wait(&l_full[lb], (tc >> 1) & 1, ab);
                 if (!__all_sync(0xffffffffu, ok)) goto epilogue_done;
-                const float lt = lsum[lb][0][row] + lsum[lb][1][row];
+                // O is scaled by the tile's final running max, the larger reference;
+                // a warpgroup without a kept entry has reference -inf and sum 0
+                const float m0 = lref[lb][0][row], m1 = lref[lb][1][row];
+                const float l0 = lsum[lb][0][row], l1 = lsum[lb][1][row];
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&l_empty[lb]);
+                const float mf = fmaxf(m0, m1);
+                const float lt = mf == -INFINITY ? 0.f : l0 * ex2_approx(m0 - mf) + l1 * ex2_approx(m1 - mf);
                 inv = lt > 0.f ? 1.0f / lt : 0.f;
                 ok = mbar_wait(&o_full, tc & 1, ab);
                 if (!__all_sync(0xffffffffu, ok)) goto epilogue_done;
@@ -301,11 +327,15 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             for (int p = 0; p < KP; ++p) {
                 uint32_t pk[32];
                 if (live) {
-                    uint32_t r[64];
-                    tmem_ld64_sync(tO + lane_base + p * 64, tO + lane_base + p * 64 + 32, r);
 #pragma unroll
-                    for (int k = 0; k < 32; ++k)
-                        pk[k] = Pack2<T>::pack(__uint_as_float(r[2 * k]) * inv, __uint_as_float(r[2 * k + 1]) * inv);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t r[32];
+                        tmem_ld32_sync(tO + lane_base + p * 64 + hh * 32, r);
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            pk[hh * 16 + k] =
+                                Pack2<T>::pack(__uint_as_float(r[2 * k]) * inv, __uint_as_float(r[2 * k + 1]) * inv);
+                    }
                     if (p == KP - 1) {
                         tc_fence_before();
                         __syncwarp();
@@ -335,22 +365,26 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         }
     epilogue_done:
         if (lane == 0) bulk_wait_all();
-    } else if (warp >= 8) {
+    } else {
+        regs_inc<kRegsSoftmax>();
         // ---------------------------------------------------- softmax ----
-        // Two warpgroups split each row: warpgroup wg owns score columns
-        // [64 wg, 64 wg + 64) (its half of P) and output columns
-        // [wg D/2, wg D/2 + D/2).  The half-row maxima meet every step through
-        // shared memory (xm barriers, 8 warp arrivals), so both groups take the
-        // same decisions; the partial row sums go to the epilogue once per tile.
-        constexpr int W = BLK < 64 ? BLK : 64;  // columns of one slot inside a half
-        constexpr int LS = 64 / W;              // slots (or slot parts) per half
+        // Warpgroup wg takes the steps g with g % 2 == wg, whole rows (thread =
+        // query row = TMEM lane): the two warps that share a sub-partition are
+        // then in different phases of their steps, one loading and reducing while
+        // the other exponentiates.  The running max m is handed from step g - 1 to
+        // step g through shared memory (m_pub barriers): every step waits for the
+        // previous step's hand-off, across tiles too, so each parity's value is
+        // read before it is rewritten.  Each warpgroup keeps its partial row sum
+        // against the last max it used; the epilogue rebases the two.
+        constexpr int W = BLK < 64 ? BLK : 64;  // columns of one slot inside a half row
+        constexpr int LS = 64 / W;              // slots (or slot parts) per half row
         const int sw = warp - 8, wg = sw >> 2;
         const int quad = warp & 3;
         const int row = quad * 32 + lane;  // query row inside the tile = TMEM lane
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const int r_in = row % BLK, a = row / BLK;
         uint32_t g = 0, tc = 0;
-        // metadata of one half: block id at (row block a, slot) and block-column, per slot part
+        // metadata of one half row: block id at (row block a, slot) and block-column, per slot part
         struct Half {
             int blk[LS], cb[LS];
         };
@@ -369,10 +403,15 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 const int kbase = (hf * 64 + ls * W) % BLK;  // in-block column of v[ls * W]
                 if (KIND == BSP_MASK_DIAG_CAUSAL) {
                     // keep columns j <= lim: none if the block is absent, j <= r_in - kbase
-                    // inside the diagonal block, all otherwise (branch-free selects)
+                    // inside the diagonal block, all otherwise.  Only a diagonal or an
+                    // absent block removes anything, so the selects run only when some
+                    // lane of the warp has one (for blocks of 32 and more a warp's rows
+                    // are in one block-row, so the test is usually uniform).
                     const int lim = md.blk[ls] < 0 ? -1 : (md.cb[ls] == rb ? r_in - kbase : W);
+                    if (__any_sync(0xffffffffu, lim < W - 1)) {
 #pragma unroll
-                    for (int j = 0; j < W; ++j) v[ls * W + j] = j > lim ? -INFINITY : v[ls * W + j];
+                        for (int j = 0; j < W; ++j) v[ls * W + j] = j > lim ? -INFINITY : v[ls * W + j];
+                    }
                 } else if (md.blk[ls] < 0) {
 #pragma unroll
                     for (int j = 0; j < W; ++j) v[ls * W + j] = -INFINITY;
@@ -390,12 +429,31 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             }
         };
         auto max64 = [](const float (&v)[64]) {
+            // 8 independent chains of three-input maxima
             float m8[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) m8[k] = v[k];
+            for (int k = 0; k < 8; ++k) m8[k] = fmax3(v[k], v[k + 8], v[k + 16]);
 #pragma unroll
-            for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], v[c]);
-            return fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            for (int c = 24; c < 64; c += 16)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) m8[k] = fmax3(m8[k], v[c + k], c + 8 + k < 64 ? v[c + 8 + k] : v[c + k]);
+            return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+        };
+        // p = 2^(s * c2 - msub) for 64 entries -> 32 packed pairs; returns their sum
+        auto exp64 = [&](const float (&v)[64], float msub, uint32_t (&pk)[32]) {
+            const float2 c2v = make_float2(args.c2, args.c2), nm = make_float2(-msub, -msub);
+            float2 rs4[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) rs4[k] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float2 y = __ffma2_rn(make_float2(v[2 * c], v[2 * c + 1]), c2v, nm);
+                const float2 p = (c & 7) < kPolyPairs ? exp2_poly2(y) : make_float2(ex2_approx(y.x), ex2_approx(y.y));
+                rs4[c & 3] = __fadd2_rn(rs4[c & 3], p);
+                pk[c] = Pack2<T>::pack(p.x, p.y);
+            }
+            const float2 r2 = __fadd2_rn(__fadd2_rn(rs4[0], rs4[1]), __fadd2_rn(rs4[2], rs4[3]));
+            return r2.x + r2.y;
         };
         for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
             const int tile = L.tile_order[w / args.Z];
@@ -404,90 +462,103 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             if (ns == 0) continue;            // the epilogue writes the zero rows
             const int rb = gq * G + a;        // block-row of this thread's query row
             const int rseq = gq * 128 + row;  // query position inside the sequence
-            float m = -INFINITY, l = 0.f;
-            Half own, nown;
-            fetch(s0, wg, nown);
-            for (int n = 0; n < ns; ++n, ++g) {
-                own = nown;
-                if (n + 1 < ns) fetch(s0 + n + 1, wg, nown);  // next step: latency hidden behind this one
+            float l = 0.f, mref = -INFINITY;  // this warpgroup's sum and the max it is relative to
+            // first own step of the tile and its metadata
+            int n = (int)((wg - g) & 1u);
+            g += n;
+            Half h0, h1;
+            if (n < ns) {
+                fetch(s0 + n, 0, h0);
+                fetch(s0 + n, 1, h1);
+            }
+            for (; n < ns; n += 2, g += 2) {
+                const Half c0 = h0, c1 = h1;
+                if (n + 2 < ns) {  // next own step: latency hidden behind this one
+                    fetch(s0 + n + 2, 0, h0);
+                    fetch(s0 + n + 2, 1, h1);
+                }
                 bool ok = mbar_wait(&s_full[g & 1], (g >> 1) & 1, ab);
                 if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
                 tc_fence_after();
-                // raw scores of this half (the scale is applied inside the exponent)
-                float x[64];
                 const uint32_t srow = tS + (g & 1) * 128 + lane_base;
-                tmem_ld64_sync(srow + wg * 64, srow + wg * 64 + 32, *reinterpret_cast<uint32_t(*)[64]>(x));
-                mask_half(x, wg, own, rb, rseq);
-                // row max: this half's, then the partner half's through shared memory
+                // row max over both halves; the second half stays in registers
+                float x[64];
+                tmem_ld64_sync(srow, srow + 32, *reinterpret_cast<uint32_t(*)[64]>(x));
+                mask_half(x, 0, c0, rb, rseq);
                 float mx = max64(x);
-                {
-                    const uint32_t xp = g & 1;
-                    xmax[xp][wg][row] = mx;
-                    tc_fence_before();  // this warp's S loads are complete before the other half writes P
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&xm[xp]);
-                    ok = mbar_wait(&xm[xp], (g >> 1) & 1, ab);
+                tmem_ld64_sync(srow + 64, srow + 96, *reinterpret_cast<uint32_t(*)[64]>(x));
+                mask_half(x, 1, c1, rb, rseq);
+                mx = fmaxf(mx, max64(x));
+                // running max after step g - 1 (the other warpgroup's step)
+                float mprev = -INFINITY;
+                if (g > 0) {
+                    ok = mbar_wait(&m_pub[(g - 1) & 1], ((g - 1) >> 1) & 1, ab);
                     if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
-                    mx = fmaxf(mx, xmax[xp][wg ^ 1][row]);
+                    if (n > 0) mprev = mrun[(g - 1) & 1][row];
                 }
-                // m is kept in the scaled log2 domain (scale > 0 commutes with max); both
-                // warpgroups see the same maxima, so they take the same decisions
-                const float m_new = fmaxf(m, mx * args.c2);
-                const bool need = m_new > m + kRescaleThreshold;  // also true for the first finite max
-                const float alpha = need ? ((m == -INFINITY) ? 0.f : ex2_approx(m - m_new)) : 1.f;
-                if (need) m = m_new;
+                // m in the scaled log2 domain (scale > 0 commutes with max); it moves
+                // only when the row max grew by more than the threshold
+                const float m_new = fmaxf(mprev, mx * args.c2);
+                const bool need = m_new > mprev + kRescaleThreshold;  // also true for the first finite max
+                const float m = need ? m_new : mprev;
+                mrun[g & 1][row] = m;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&m_pub[g & 1]);
                 const float msub = (m == -INFINITY) ? 0.f : m;
-                // p = 2^(s * c2 - m): one FFMA and one MUFU.EX2 per entry
-                float rs8[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) rs8[k] = 0.f;
                 uint32_t pk[32];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const float p0 = ex2_approx(fmaf(x[2 * c], args.c2, -msub));
-                    const float p1 = ex2_approx(fmaf(x[2 * c + 1], args.c2, -msub));
-                    rs8[(2 * c) & 7] += p0;
-                    rs8[(2 * c + 1) & 7] += p1;
-                    pk[c] = Pack2<T>::pack(p0, p1);
-                }
-                const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-                l = l * alpha + rs;  // partial sum of this half
+                float rs = exp64(x, msub, pk);
                 // TMEM P buffer g % 2 is free once P V of step g - 2 has completed
                 if (g >= 2) {
                     ok = mbar_wait(&pv_done[g & 1], ((g - 2) >> 1) & 1, ab);
                     if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
                 }
+                tc_fence_after();
+                tmem_st32_sync(tP + (g & 1) * 64 + 32 + lane_base, pk);
+                // first half again
+                tmem_ld64_sync(srow, srow + 32, *reinterpret_cast<uint32_t(*)[64]>(x));
+                mask_half(x, 0, c0, rb, rseq);
+                rs += exp64(x, msub, pk);
+                tmem_st32_sync(tP + (g & 1) * 64 + lane_base, pk);
+                // this warpgroup's sum, rebased from its previous reference to m
+                l = (mref == -INFINITY ? 0.f : l * ex2_approx(mref - msub)) + rs;
+                mref = m;
                 if (n > 0 && __any_sync(0xffffffffu, need)) {
-                    // O may be rescaled only after P V of step g - 1 (same tile) has completed
+                    // O (scaled by mprev) is rescaled after P V of step g - 1 has completed
                     ok = mbar_wait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, ab);
                     if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
                     tc_fence_after();
+                    const float alpha = need ? (mprev == -INFINITY ? 0.f : ex2_approx(mprev - m)) : 1.f;
 #pragma unroll
-                    for (int c = 0; c < D / 64; ++c) {
+                    for (int c = 0; c < D / 32; ++c) {
                         uint32_t r[32];
-                        const uint32_t ta = tO + lane_base + wg * (D / 2) + c * 32;
+                        const uint32_t ta = tO + lane_base + c * 32;
                         tmem_ld32_sync(ta, r);
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
+                        for (int k = 0; k < 32; k += 2) {
+                            const float2 v = __fmul2_rn(make_float2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])),
+                                                        make_float2(alpha, alpha));
+                            r[k] = __float_as_uint(v.x);
+                            r[k + 1] = __float_as_uint(v.y);
+                        }
                         tmem_st32_sync(ta, r);
                     }
                 }
-                // this half of the P row -> TMEM P buffer g % 2, columns [32 wg, 32 wg + 32)
-                tc_fence_after();
-                tmem_st32_sync(tP + (g & 1) * 64 + wg * 32 + lane_base, pk);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[g & 1]);
             }
-            // partial row sums of the tile -> epilogue (buffer tc % 2, free once
-            // the epilogue has read the sums of tile tc - 2)
+            g -= (uint32_t)(n - ns);  // back to the first step of the next tile
+            // this warpgroup's sum and reference max -> epilogue (buffer tc % 2,
+            // free once the epilogue has read the values of tile tc - 2)
             {
                 const uint32_t lb = tc & 1;
                 if (tc >= 2) {
                     bool ok = mbar_wait(&l_empty[lb], ((tc - 2) >> 1) & 1, ab);
                     if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
                 }
-                lsum[lb][wg][row] = l;
+                // with nothing kept the sum holds only the polynomial's tiny values
+                lsum[lb][wg][row] = mref == -INFINITY ? 0.f : l;
+                lref[lb][wg][row] = mref;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&l_full[lb]);
                 ++tc;
@@ -521,6 +592,10 @@ int launch_attn(const bsp_layout_s* Lh, const void* Q, const void* K, const void
     constexpr int smem = AttnSmem<D>::kAlloc;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return BSP_ERR_CUDA;
+    // the register split at kernel start needs the full launch allocation
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return BSP_ERR_CUDA;
+    if ((uint32_t)fa.numRegs != kRegsLaunch) return BSP_ERR_UNSUPPORTED;
     const int64_t total = (int64_t)Z * Lh->n_tiles;
     const int grid = (int)std::min<int64_t>(total, sm_count());
     kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, mo, args);

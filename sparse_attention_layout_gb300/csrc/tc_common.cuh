@@ -168,6 +168,17 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// Change the registers a warp owns (all warps of a warpgroup execute the same
+// one).  inc waits until other warpgroups of the block have released enough
+// with dec, so the shares of all warpgroups must add up to no more than the
+// block was launched with; the launcher checks that before the first launch.
+template <uint32_t N> __device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N> __device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16 (bf16 / fp16 in, fp32 accumulate)
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                         uint32_t accumulate) {
@@ -285,6 +296,41 @@ __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// 2^y for two values on the FMA pipe instead of the special-function unit
+// (the attention softmax evaluates part of its exponentials here so that the
+// two units share the work).  Method: Cody-Waite style range reduction
+// y = j + f with j = round-to-nearest(y), found by adding and subtracting
+// 1.5 * 2^23 (which leaves j in the low mantissa bits of the sum), and
+// f in [-1/2, 1/2]; 2^f by the cubic 1 + f (c1 + f (c2 + f c3)), its
+// coefficients fitted here by iteratively reweighted least squares for the
+// smallest maximum relative error over [-1/2, 1/2] with p(0) = 1 held (so
+// integer y give exact powers of two); 2^j is added to the exponent field.
+// Maximum relative error 1.02e-4, far below the 2^-9 of the 16-bit P it
+// feeds.  y is clamped to >= -125 (the exponent field stays normal), so -inf
+// and very negative inputs give a value <= 2^-124.5 instead of 0: callers
+// must not rely on exact zeros from masked entries.
+__device__ __forceinline__ float2 exp2_poly2(float2 y) {
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+    constexpr float c1 = 0.6932829f, c2 = 0.24221097f, c3 = 0.055008933f;
+    y.x = fmaxf(y.x, -125.0f);
+    y.y = fmaxf(y.y, -125.0f);
+    const float2 t = __fadd2_rn(y, make_float2(kMagic, kMagic));
+    const float2 j = __fadd2_rn(t, make_float2(-kMagic, -kMagic));
+    const float2 f = __fadd2_rn(y, make_float2(-j.x, -j.y));
+    float2 p = __ffma2_rn(f, make_float2(c3, c3), make_float2(c2, c2));
+    p = __ffma2_rn(p, f, make_float2(c1, c1));
+    p = __ffma2_rn(p, f, make_float2(1.0f, 1.0f));
+    return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)),
+                       __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)));
+}
+
+// max of three (one instruction on sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 // ---------------------------------------------------------- conversions --
