@@ -28,13 +28,16 @@
 //               query row = one TMEM lane, whole rows of 128 scores.  Reads S
 //               from TMEM, masks, takes the row max, receives the running max
 //               of the previous step from the other warpgroup and passes its
-//               own on, writes P (bf16/fp16) into the TMEM P buffer of the
-//               step (two buffers, so step g only waits for P V of step g-2),
+//               own on, writes P (bf16/fp16) over the step's scores in TMEM,
 //               rescales O in TMEM only when the running max grew by more than
 //               2^8 (the final O / l is exact either way), and hands the
 //               tile's row sums to the epilogue.
-// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D), P0 [384,448), P1 [448,512)
-// (P packed two 16-bit values per column; P V takes its A operand from TMEM).
+// TMEM columns: S0 [0,128), S1 [128,256), S2 [256,384), O [384, 384+D).  Step g
+// uses S buffer g % 3; its P (two 16-bit values per column) overwrites the
+// first 64 columns of the same buffer once the scores are in registers, and
+// P V takes its A operand from there.  With three buffers Q K^T of step g
+// waits only for P V of step g - 3, so the next scores are ready when a
+// softmax warpgroup finishes a step.
 #pragma once
 
 #include <algorithm>
@@ -50,10 +53,10 @@ using namespace tc;
 
 constexpr int kThreads = 512;
 // Registers per thread after the split at kernel start (launched with 128):
-// warps 0-3 (producers, issuers) and 4-7 (epilogue) give some to the two
-// softmax warpgroups.  128 threads x (56 + 88 + 184 + 184) = 65536 =
+// warps 0-3 (producers, issuers) give some to the two softmax warpgroups, the
+// epilogue keeps its share.  128 threads x (80 + 128 + 152 + 152) = 65536 =
 // 512 threads x 128, the block's allocation at launch.
-constexpr uint32_t kRegsLaunch = 128, kRegsCtl = 56, kRegsEpi = 88, kRegsSoftmax = 184;
+constexpr uint32_t kRegsLaunch = 128, kRegsCtl = 80, kRegsEpi = 128, kRegsSoftmax = 152;
 static_assert(kRegsCtl + kRegsEpi + 2 * kRegsSoftmax <= 4 * kRegsLaunch, "register split exceeds the launch allocation");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when max grows by > 256x
 // Of every 8 column pairs of a score row, this many take 2^x from the FMA-pipe
@@ -103,11 +106,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     constexpr int QST = SM::QST;
-    // K and V stage b (= step % 2) is tied to S buffer and P buffer b: s_full[b]
-    // (Q K^T of the step done) also frees its K tile, pv_done[b] (P V of the step
-    // done) also frees its V tile and its P buffer.
+    // K and V tiles of step g sit in stage g % 2; S buffer g % 3 has s_full
+    // (Q K^T done, which also frees the K stage of that step), p_full (P
+    // written) and pv_done (P V done, which frees the buffer and the V stage).
     __shared__ uint64_t q_full[QST], q_empty[QST], k_full[2], v_full[2];
-    __shared__ uint64_t s_full[2], p_full[2], pv_done[2];
+    __shared__ uint64_t s_full[3], p_full[3], pv_done[3];
     // O accumulator: o_full = last P V of the tile completed, o_empty = the
     // epilogue has read it.  Row sums: lsum[tile parity][warpgroup][row], with
     // l_full (softmax wrote them) and l_empty (the epilogue read them).
@@ -133,9 +136,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         for (int i = 0; i < 2; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&v_full[i], 1);
+        }
+        for (int i = 0; i < 3; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&pv_done[i], 1);
-            // the 4 warps of the warpgroup that owns steps of this parity
+            // the 4 warps of the warpgroup that owns the step
             mbar_init(&p_full[i], 4);
         }
         mbar_init(&o_full, 1);
@@ -154,9 +159,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tS = tmem_base;        // S buffers at columns 0 and 128
-    const uint32_t tO = tmem_base + 256;  // O at column 256
-    const uint32_t tP = tmem_base + 384;  // P buffers (bf16 pairs) at columns 384 and 448
+    const uint32_t tS = tmem_base;        // S buffers at columns 0, 128 and 256
+    const uint32_t tO = tmem_base + 384;  // O at column 384
 
     const int64_t total = (int64_t)args.Z * L.n_tiles;
     const int S = L.S;
@@ -204,8 +208,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     // stage g % 2 is free once step g - 2 has used it: Q K^T for a K
                     // tile, P V for a V tile
                     uint64_t* full = is_v ? &v_full[st] : &k_full[st];
-                    uint64_t* freed = is_v ? &pv_done[st] : &s_full[st];
-                    if (g >= 2 && !mbar_wait(freed, ((g - 2) >> 1) & 1, ab)) goto producer_done;
+                    if (g >= 2) {
+                        const uint32_t gp = g - 2;
+                        uint64_t* freed = is_v ? &pv_done[gp % 3] : &s_full[gp % 3];
+                        if (!mbar_wait(freed, (gp / 3) & 1, ab)) goto producer_done;
+                    }
                     mbar_arrive_expect_tx(full, kTileBytes);
                     const uint32_t base = smem_u32(smem + (is_v ? SM::kV : SM::kK) + st * kTileBytes);
 #pragma unroll
@@ -232,18 +239,18 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 const uint32_t qs = q_it % QST;
                 if (!mbar_wait(&q_full[qs], (q_it / QST) & 1, ab)) goto qk_done;
                 for (int n = 0; n < ns; ++n, ++g) {
-                    const uint32_t st = g & 1;
-                    // S buffer g % 2 is free once the softmax of step g - 2 has read it
-                    if (g >= 2 && !mbar_wait(&p_full[st], ((g - 2) >> 1) & 1, ab)) goto qk_done;
+                    const uint32_t st = g & 1, sb = g % 3;
+                    // S buffer g % 3 is free once P V of step g - 3 has read its P
+                    if (g >= 3 && !mbar_wait(&pv_done[sb], ((g - 3) / 3) & 1, ab)) goto qk_done;
                     if (!mbar_wait(&k_full[st], (g >> 1) & 1, ab)) goto qk_done;
                     tc_fence_after();
                     const uint64_t aq = dq + ((qs * kTileBytes) >> 4), bk = dk + ((st * kTileBytes) >> 4);
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
                         const uint32_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-                        mma_f16(tS + st * 128, aq + off, bk + off, kIdescQK, ks > 0 ? 1u : 0u);
+                        mma_f16(tS + sb * 128, aq + off, bk + off, kIdescQK, ks > 0 ? 1u : 0u);
                     }
-                    mma_commit(&s_full[st]);
+                    mma_commit(&s_full[sb]);
                     if (n == ns - 1) mma_commit(&q_empty[qs]);
                 }
                 ++q_it;
@@ -262,17 +269,17 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 // the previous tile's O must have been read by the epilogue
                 if (tc > 0 && !mbar_wait(&o_empty, (tc - 1) & 1, ab)) goto pv_done_label;
                 for (int n = 0; n < ns; ++n, ++g) {
-                    const uint32_t st = g & 1;
-                    // P of step g written (and O rescaled) by all softmax warps; V landed
-                    if (!mbar_wait(&p_full[st], (g >> 1) & 1, ab)) goto pv_done_label;
+                    const uint32_t st = g & 1, sb = g % 3;
+                    // P of step g written (and O rescaled) by its warpgroup; V landed
+                    if (!mbar_wait(&p_full[sb], (g / 3) & 1, ab)) goto pv_done_label;
                     if (!mbar_wait(&v_full[st], (g >> 1) & 1, ab)) goto pv_done_label;
                     tc_fence_after();
                     const uint64_t bv = dv + ((st * kTileBytes) >> 4);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)  // P (A operand) from TMEM: 8 columns per 16 keys
-                        mma_f16_tmem_a(tO, tP + st * 64 + ks * 8, bv + ((ks * 2048) >> 4), kIdescPV,
+                        mma_f16_tmem_a(tO, tS + sb * 128 + ks * 8, bv + ((ks * 2048) >> 4), kIdescPV,
                                        (ks > 0 || n > 0) ? 1u : 0u);
-                    mma_commit(&pv_done[st]);
+                    mma_commit(&pv_done[sb]);
                 }
                 mma_commit(&o_full);
                 ++tc;
@@ -281,7 +288,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         }
     }
     } else if (warp < 8) {
-        regs_dec<kRegsEpi>();
+        if (kRegsEpi < kRegsLaunch) regs_dec<kRegsEpi>();
         // ---------------------------------------------------- epilogue ----
         // Warp q owns rows [32 q, 32 q + 32) of the tile (TMEM lanes of its
         // quadrant).  O / l leaves through a 32 x 64 staging panel per warp in
@@ -477,17 +484,18 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     fetch(s0 + n + 2, 0, h0);
                     fetch(s0 + n + 2, 1, h1);
                 }
-                bool ok = mbar_wait(&s_full[g & 1], (g >> 1) & 1, ab);
+                const uint32_t sb = g % 3;
+                bool ok = mbar_wait(&s_full[sb], (g / 3) & 1, ab);
                 if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
                 tc_fence_after();
-                const uint32_t srow = tS + (g & 1) * 128 + lane_base;
-                // row max over both halves; the second half stays in registers
+                const uint32_t srow = tS + sb * 128 + lane_base;
+                // row max over both halves; the first half stays in registers
                 float x[64];
-                tmem_ld64_sync(srow, srow + 32, *reinterpret_cast<uint32_t(*)[64]>(x));
-                mask_half(x, 0, c0, rb, rseq);
-                float mx = max64(x);
                 tmem_ld64_sync(srow + 64, srow + 96, *reinterpret_cast<uint32_t(*)[64]>(x));
                 mask_half(x, 1, c1, rb, rseq);
+                float mx = max64(x);
+                tmem_ld64_sync(srow, srow + 32, *reinterpret_cast<uint32_t(*)[64]>(x));
+                mask_half(x, 0, c0, rb, rseq);
                 mx = fmaxf(mx, max64(x));
                 // running max after step g - 1 (the other warpgroup's step)
                 float mprev = -INFINITY;
@@ -505,26 +513,22 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&m_pub[g & 1]);
                 const float msub = (m == -INFINITY) ? 0.f : m;
+                // P over the scores: keys [0, 64) -> columns [0, 32) (those scores are
+                // in registers), then keys [64, 128) -> columns [32, 64) (scores of
+                // keys [32, 64), already consumed)
                 uint32_t pk[32];
                 float rs = exp64(x, msub, pk);
-                // TMEM P buffer g % 2 is free once P V of step g - 2 has completed
-                if (g >= 2) {
-                    ok = mbar_wait(&pv_done[g & 1], ((g - 2) >> 1) & 1, ab);
-                    if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
-                }
-                tc_fence_after();
-                tmem_st32_sync(tP + (g & 1) * 64 + 32 + lane_base, pk);
-                // first half again
-                tmem_ld64_sync(srow, srow + 32, *reinterpret_cast<uint32_t(*)[64]>(x));
-                mask_half(x, 0, c0, rb, rseq);
+                tmem_st32_sync(srow, pk);
+                tmem_ld64_sync(srow + 64, srow + 96, *reinterpret_cast<uint32_t(*)[64]>(x));
+                mask_half(x, 1, c1, rb, rseq);
                 rs += exp64(x, msub, pk);
-                tmem_st32_sync(tP + (g & 1) * 64 + lane_base, pk);
+                tmem_st32_sync(srow + 32, pk);
                 // this warpgroup's sum, rebased from its previous reference to m
                 l = (mref == -INFINITY ? 0.f : l * ex2_approx(mref - msub)) + rs;
                 mref = m;
                 if (n > 0 && __any_sync(0xffffffffu, need)) {
                     // O (scaled by mprev) is rescaled after P V of step g - 1 has completed
-                    ok = mbar_wait(&pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, ab);
+                    ok = mbar_wait(&pv_done[(g - 1) % 3], ((g - 1) / 3) & 1, ab);
                     if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
                     tc_fence_after();
                     const float alpha = need ? (mprev == -INFINITY ? 0.f : ex2_approx(mprev - m)) : 1.f;
@@ -545,7 +549,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[g & 1]);
+                if (lane == 0) mbar_arrive(&p_full[sb]);
             }
             g -= (uint32_t)(n - ns);  // back to the first step of the next tile
             // this warpgroup's sum and reference max -> epilogue (buffer tc % 2,
