@@ -523,9 +523,6 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 mask_half(x, 1, c1, rb, rseq);
                 rs += exp64(x, msub, pk);
                 tmem_st32_sync(srow + 32, pk);
-                // this warpgroup's sum, rebased from its previous reference to m
-                l = (mref == -INFINITY ? 0.f : l * ex2_approx(mref - msub)) + rs;
-                mref = m;
                 if (n > 0 && __any_sync(0xffffffffu, need)) {
                     // O (scaled by mprev) is rescaled after P V of step g - 1 has completed
                     ok = mbar_wait(&pv_done[(g - 1) % 3], ((g - 1) / 3) & 1, ab);
@@ -550,6 +547,9 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[sb]);
+                // this warpgroup's sum, rebased from its previous reference to m
+                l = (mref == -INFINITY ? 0.f : l * ex2_approx(mref - msub)) + rs;
+                mref = m;
             }
             g -= (uint32_t)(n - ns);  // back to the first step of the next tile
             // this warpgroup's sum and reference max -> epilogue (buffer tc % 2,
