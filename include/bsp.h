@@ -117,6 +117,19 @@ int bsp_layout_tiles(bsp_layout_t layout, int* G, int* n_tiles, int64_t* n_steps
                      int32_t* tile_step_ptr, int32_t* tile_order, int32_t* step_col,
                      int32_t* step_blk);
 
+/* Line groups used by the tensor-core DSD / DDS kernels (host copies, for
+ * inspection; any pointer may be NULL, call first with NULL arrays to get the
+ * sizes).  orient 0: a group is G = 128/block consecutive block-rows of one
+ * head (group t = h * ceil(nb/G) + g); orient 1: G consecutive block-columns.
+ * Each group has one slot per block index of the union of its lines' blocks,
+ * ascending.  grp_ptr [n_groups+1]: first slot of each group; grp_order
+ * [n_groups]: groups with the most slots first; slot_idx [n_slots]: the block
+ * index along the contraction (block-column for orient 0, block-row for 1);
+ * slot_blk [n_slots*G]: block id of line a of the group at slot s, at
+ * [s*G + a], -1 when absent.  orient not 0 or 1: BSP_ERR_INVALID_ARG. */
+int bsp_layout_groups(bsp_layout_t layout, int orient, int* G, int* n_groups, int64_t* n_slots,
+                      int32_t* grp_ptr, int32_t* grp_order, int32_t* slot_idx, int32_t* slot_blk);
+
 /* ---- matmul modes ------------------------------------------------------ */
 
 /* SDD: C = op(A) . op(B) evaluated on the present blocks only.

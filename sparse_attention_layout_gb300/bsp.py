@@ -147,6 +147,26 @@ class Layout:
         return out
 
 
+    def groups(self, orient: int) -> dict:
+        """Line groups of the tensor-core DSD / DDS kernels (orient 0: block-rows,
+        1: block-columns)."""
+        G, ng, ns = ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
+        f = lib().bsp_layout_groups
+        _check(f(self.handle, int(orient), ctypes.byref(G), ctypes.byref(ng), ctypes.byref(ns), None, None,
+                 None, None), "bsp_layout_groups")
+        G, ng, ns = G.value, ng.value, ns.value
+        out = {"grp_ptr": np.zeros(ng + 1, np.int32), "grp_order": np.zeros(max(ng, 1), np.int32),
+               "slot_idx": np.zeros(max(ns, 1), np.int32), "slot_blk": np.zeros(max(ns * G, 1), np.int32)}
+        _check(f(self.handle, int(orient), None, None, None,
+                 *[ctypes.c_void_p(out[k].ctypes.data) for k in ("grp_ptr", "grp_order", "slot_idx", "slot_blk")]),
+               "bsp_layout_groups")
+        out["grp_order"] = out["grp_order"][:ng]
+        out["slot_idx"] = out["slot_idx"][:ns]
+        out["slot_blk"] = out["slot_blk"][:ns * G].reshape(ns, G)
+        out.update(G=G, n_groups=ng, n_slots=ns)
+        return out
+
+
 def _layout_args(layout, block):
     lay = np.ascontiguousarray(layout, dtype=np.uint8)
     if lay.ndim != 3 or lay.shape[1] != lay.shape[2]:

@@ -26,6 +26,13 @@ struct LayoutView {
     const int32_t* tile_order;    // [n_tiles] tile ids, most steps first
     const int32_t* step_col;      // [n_steps*G] block-column of each slot, -1 = padding
     const int32_t* step_blk;      // [n_steps*G*G] block id at (row a, slot b), -1 = absent
+    // line groups for the block-sparse matmuls, o = 0: G consecutive block-rows,
+    // o = 1: G consecutive block-columns (same head).  One slot per block index
+    // of the union of the lines' blocks (ascending, no padding).
+    const int32_t* gl_ptr[2];     // [n_tiles+1] first slot of each group
+    const int32_t* gl_order[2];   // [n_tiles] groups, most slots first
+    const int32_t* gl_idx[2];     // [slots] block index along the contraction
+    const int32_t* gl_blk[2];     // [slots*G] block id of line a at slot s ([s*G + a]), -1 = absent
     // softmax chunks for 2- and 4-byte elements: int4 (h*nb+i, p0, nnz_i,
     // r0 | R << 16): R rows of block-row i from row r0, whose blocks have ids
     // p0 .. p0+nnz_i-1 (ids are CSR positions), R the largest power of two with
@@ -53,6 +60,7 @@ struct bsp_layout_s {
     int64_t n_steps = 0;
     int max_tile_steps = 0;
     std::vector<int32_t> tile_step_ptr, tile_order, step_col, step_blk;
+    std::vector<int32_t> gl_ptr[2], gl_order[2], gl_idx[2], gl_blk[2];
     std::vector<int32_t> sm_items[2];
     int sm_max_bytes[2] = {0, 0};
     bool sm_fits[2] = {true, true};

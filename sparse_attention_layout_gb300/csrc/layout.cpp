@@ -139,6 +139,45 @@ int build_tables(bsp_layout_s* L, const uint8_t* lay) {
     L->n_steps = steps;
     L->tile_order = order_by_weight_desc(tile_steps);
 
+    // Line groups for the block-sparse matmuls: G consecutive block-rows (o = 0,
+    // CSR) or block-columns (o = 1, CSC) of one head, one slot per block index
+    // of the union of their blocks.
+    for (int o = 0; o < 2; ++o) {
+        const std::vector<int32_t>& lp = o ? L->col_ptr : L->row_ptr;
+        const std::vector<int32_t>& li = o ? L->row_idx : L->col_idx;
+        L->gl_ptr[o].assign((size_t)L->n_tiles + 1, 0);
+        L->gl_idx[o].clear();
+        L->gl_blk[o].clear();
+        std::vector<int32_t> sizes((size_t)L->n_tiles, 0);
+        int64_t slots = 0;
+        for (int h = 0; h < H; ++h) {
+            for (int g = 0; g < L->ngroups; ++g) {
+                const int t = h * L->ngroups + g;
+                std::fill(in_union.begin(), in_union.end(), 0);
+                for (int a = 0; a < G && g * G + a < nb; ++a) {
+                    const int line = g * G + a;
+                    for (int pp = lp[(size_t)h * (nb + 1) + line]; pp < lp[(size_t)h * (nb + 1) + line + 1]; ++pp)
+                        in_union[li[pp]] = 1;
+                }
+                L->gl_ptr[o][t] = (int32_t)slots;
+                for (int u = 0; u < nb; ++u) {
+                    if (!in_union[u]) continue;
+                    L->gl_idx[o].push_back(u);
+                    for (int a = 0; a < G; ++a) {
+                        const int line = g * G + a;
+                        int32_t id = -1;
+                        if (line < nb) id = (int32_t)(o ? id_at(h, u, line) : id_at(h, line, u));
+                        L->gl_blk[o].push_back(id);
+                    }
+                    ++slots;
+                    ++sizes[t];
+                }
+            }
+        }
+        L->gl_ptr[o][L->n_tiles] = (int32_t)slots;
+        L->gl_order[o] = order_by_weight_desc(sizes);
+    }
+
     // softmax chunk lists (element sizes 2 and 4 bytes)
     for (int e = 0; e < 2; ++e) {
         const int64_t elt = e ? 4 : 2;
@@ -220,6 +259,10 @@ extern "C" int bsp_layout_compile(const uint8_t* layout, int H, int nb, int bloc
         {&L->tile_order, &V.tile_order}, {&L->step_col, &V.step_col},
         {&L->step_blk, &V.step_blk},      {&L->sm_items[0], &V.sm_items[0]},
         {&L->sm_items[1], &V.sm_items[1]},
+        {&L->gl_ptr[0], &V.gl_ptr[0]},   {&L->gl_order[0], &V.gl_order[0]},
+        {&L->gl_idx[0], &V.gl_idx[0]},   {&L->gl_blk[0], &V.gl_blk[0]},
+        {&L->gl_ptr[1], &V.gl_ptr[1]},   {&L->gl_order[1], &V.gl_order[1]},
+        {&L->gl_idx[1], &V.gl_idx[1]},   {&L->gl_blk[1], &V.gl_blk[1]},
     };
     size_t total = padded<int>(4);  // status word first
     for (const Part& pt : parts) total += padded<int32_t>(pt.v->size() + 1);
@@ -315,6 +358,22 @@ extern "C" int bsp_layout_get_luts(bsp_layout_t L, int32_t* row_ptr, int32_t* co
             std::memcpy(o.dst, o.host->data(), bytes);
         }
     }
+    return BSP_OK;
+}
+
+extern "C" int bsp_layout_groups(bsp_layout_t L, int orient, int* G, int* n_groups, int64_t* n_slots,
+                                 int32_t* grp_ptr, int32_t* grp_order, int32_t* slot_idx, int32_t* slot_blk) {
+    if (!L || (orient != 0 && orient != 1)) return BSP_ERR_INVALID_ARG;
+    if (G) *G = L->G;
+    if (n_groups) *n_groups = L->n_tiles;
+    if (n_slots) *n_slots = (int64_t)L->gl_idx[orient].size();
+    auto put = [](int32_t* dst, const std::vector<int32_t>& v) {
+        if (dst && !v.empty()) std::copy(v.begin(), v.end(), dst);
+    };
+    put(grp_ptr, L->gl_ptr[orient]);
+    put(grp_order, L->gl_order[orient]);
+    put(slot_idx, L->gl_idx[orient]);
+    put(slot_blk, L->gl_blk[orient]);
     return BSP_OK;
 }
 

@@ -111,6 +111,51 @@ def test_tiles_cover_every_block_once(lib, name):
     assert np.all(np.diff(steps_per_tile[order]) <= 0)
 
 
+@pytest.mark.parametrize("orient", [0, 1])
+@pytest.mark.parametrize("name", sorted(LAYOUTS))
+def test_groups_cover_every_block_once(lib, name, orient):
+    """The DSD / DDS line groups: per group the ascending union of its lines'
+    block indices, the id of every present (line, index) block, each block
+    exactly once, groups ordered by size."""
+    lay, B = LAYOUTS[name]
+    L = bsp.bsp_layout_plan(lay, B)
+    T = L.groups(orient)
+    H, nb = lay.shape[0], lay.shape[1]
+    G = T["G"]
+    ngroups = -(-nb // G)
+    assert T["n_groups"] == H * ngroups
+    ids = -np.ones(lay.shape, np.int64)
+    hs, is_, js = np.nonzero(lay)
+    ids[hs, is_, js] = np.arange(hs.size)
+    lines = lay if orient == 0 else lay.transpose(0, 2, 1)   # [h, line, index]
+    lids = ids if orient == 0 else ids.transpose(0, 2, 1)
+    seen = np.zeros(hs.size, np.int64)
+    ptr = T["grp_ptr"]
+    for t in range(T["n_groups"]):
+        h, g = divmod(t, ngroups)
+        members = [g * G + a for a in range(G) if g * G + a < nb]
+        union = sorted({u for m in members for u in np.flatnonzero(lines[h, m])})
+        slots = range(ptr[t], ptr[t + 1])
+        assert [T["slot_idx"][s] for s in slots] == union
+        for s in slots:
+            u = T["slot_idx"][s]
+            for a in range(G):
+                m = g * G + a
+                want = lids[h, m, u] if m < nb else -1
+                assert T["slot_blk"][s][a] == want
+                if want >= 0:
+                    seen[want] += 1
+    assert np.all(seen == 1)
+    order = T["grp_order"]
+    assert sorted(order.tolist()) == list(range(T["n_groups"]))
+    assert np.all(np.diff(np.diff(ptr)[order]) <= 0)
+
+
+def test_groups_reject_bad_orient(lib):
+    L = bsp.bsp_layout_plan(np.ones((1, 2, 2), np.uint8), 64)
+    assert lib.bsp_layout_groups(L.handle, 2, None, None, None, None, None, None, None) == -1
+
+
 def test_plan_rejects_bad_arguments(lib):
     h = ctypes.c_void_p()
     lay = np.ones((1, 4, 4), np.uint8)
