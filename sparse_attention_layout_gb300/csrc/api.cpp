@@ -78,7 +78,7 @@ extern "C" int bsp_dsd(bsp_layout_t L, int dtype, const void* A_sp, const void* 
     if (Z == 0) return BSP_OK;
     cudaStream_t s = (cudaStream_t)stream;
     if (!force_simt()) {
-        rc = bsp::launch_dsd_tc(L, dtype, A_sp, B, C, Z, N, trans_a, trans_b, s);
+        rc = bsp::launch_dsd_group_tc(L, dtype, A_sp, B, C, Z, N, trans_a, trans_b, s);
         if (rc != BSP_ERR_UNSUPPORTED) return rc;
     }
     return bsp::launch_dsd_simt(L, dtype, A_sp, B, C, Z, N, trans_a, trans_b, s);
@@ -92,7 +92,7 @@ extern "C" int bsp_dds(bsp_layout_t L, int dtype, const void* A, const void* B_s
     if (Z == 0) return BSP_OK;
     cudaStream_t s = (cudaStream_t)stream;
     if (!force_simt()) {
-        rc = bsp::launch_dds_tc(L, dtype, A, B_sp, C, Z, M, trans_a, trans_b, s);
+        rc = bsp::launch_dds_group_tc(L, dtype, A, B_sp, C, Z, M, trans_a, trans_b, s);
         if (rc != BSP_ERR_UNSUPPORTED) return rc;
     }
     return bsp::launch_dds_simt(L, dtype, A, B_sp, C, Z, M, trans_a, trans_b, s);

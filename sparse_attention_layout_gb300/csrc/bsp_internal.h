@@ -98,6 +98,10 @@ int launch_dsd_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B
                   int N, int ta, int tb, cudaStream_t s);
 int launch_dds_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z,
                   int M, int ta, int tb, cudaStream_t s);
+int launch_dsd_group_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z,
+                        int N, int ta, int tb, cudaStream_t s);
+int launch_dds_group_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z,
+                        int M, int ta, int tb, cudaStream_t s);
 
 int sm_count();  // multiprocessors of the current device (cached per device)
 

@@ -44,7 +44,7 @@ int make_tmap_2d(CUtensorMap* map, const void* base, int is_bf16, uint64_t rows,
 }
 
 int make_tmap_3d(CUtensorMap* map, const void* base, int is_bf16, uint64_t d0, uint64_t d1, uint64_t d2,
-                 uint32_t box0, uint32_t box1) {
+                 uint32_t box0, uint32_t box1, int swizzle_bytes) {
     auto fn = encode_fn();
     if (!fn) return BSP_ERR_CUDA;
     const cuuint64_t dims[3] = {d0, d1, d2};
@@ -53,7 +53,11 @@ int make_tmap_3d(CUtensorMap* map, const void* base, int is_bf16, uint64_t d0, u
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                     const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                         : (swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                                : (swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                                                       : CU_TENSOR_MAP_SWIZZLE_NONE)),
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? BSP_OK : BSP_ERR_UNSUPPORTED;
 }
 

@@ -133,10 +133,11 @@ def test_sdd_leaves_absent_blocks_untouched(bsp, path):
 @pytest.mark.parametrize("B", [16, 32, 64, 128])
 @pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("trans", [(0, 0), (0, 1), (1, 0), (1, 1)])
-def test_dsd(bsp, oracle, path, B, dt, trans):
+@pytest.mark.parametrize("N", [200, 72])
+def test_dsd(bsp, oracle, path, B, dt, trans, N):
     dtype = DTYPES[dt]
     ta, tb = trans
-    Z, H, N = 2, 2, 200  # N not a multiple of the column tile
+    Z, H = 2, 2  # N not a multiple of the column tile; 72 takes the 128-wide tile
     nb = max(3, 384 // B) + 1
     S = nb * B
     lay = rlayout(H, nb, 0.35, 40 + B)
@@ -154,10 +155,11 @@ def test_dsd(bsp, oracle, path, B, dt, trans):
 @pytest.mark.parametrize("B", [16, 32, 64, 128])
 @pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("trans", [(0, 0), (0, 1), (1, 0), (1, 1)])
-def test_dds(bsp, oracle, path, B, dt, trans):
+@pytest.mark.parametrize("M", [200, 72])
+def test_dds(bsp, oracle, path, B, dt, trans, M):
     dtype = DTYPES[dt]
     ta, tb = trans
-    Z, H, M = 2, 2, 200
+    Z, H = 2, 2
     nb = max(3, 384 // B) + 1
     S = nb * B
     lay = rlayout(H, nb, 0.35, 50 + B)
