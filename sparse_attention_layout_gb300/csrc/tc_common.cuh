@@ -59,6 +59,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
+// raise the phase's expected transaction bytes without arriving
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
@@ -107,6 +113,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
 }
 
@@ -359,5 +373,11 @@ int make_tmap_2d(CUtensorMap* map, const void* base, int is_bf16, uint64_t rows,
 // box [1][box1][box0], swizzle 128 / 64 / 32 bytes or 0 (none)
 int make_tmap_3d(CUtensorMap* map, const void* base, int is_bf16, uint64_t d0, uint64_t d1, uint64_t d2,
                  uint32_t box0, uint32_t box1, int swizzle_bytes = 128);
+// host: a row-major [rows][cols] matrix of 2-byte elements (cols a multiple of
+// 64) seen as [cols/64 panels][rows][64]: one box of box_panels panels x
+// box_rows rows lands panel after panel, 128-byte swizzled (else
+// BSP_ERR_UNSUPPORTED)
+int make_tmap_panels(CUtensorMap* map, const void* base, int is_bf16, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows, uint32_t box_panels);
 
 }  // namespace bsp

@@ -8,8 +8,8 @@
 //    transposed: C^T = op(B_sp)^T op(A)^T), so the sparse slab fills the
 //    MMA's M = 128 rows;
 //  - its slots are the union of the lines' block indices along the
-//    contraction; a slot's slab stacks the G lines' blocks at that index, with
-//    absent blocks zero-filled by the TMA (an out-of-range coordinate);
+//    contraction; a slot's slab stacks the G lines' blocks at that index
+//    (TMA loads), absent blocks written as zeros by the producer warp;
 //  - the dense tile is the B rows of the dense operand at that index times
 //    NT = 256 of its free columns (128 when the free extent is at most 128),
 //    so one dense tile serves G lines and every MMA is 128 x NT x 16.
@@ -23,8 +23,10 @@
 // write through 4 KB staging panels with TMA stores, so rows or columns past
 // the end of C are clipped by the tensor map.
 //
-// Roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner and
-// single-thread MMA issuer, warps 2..5 epilogue.
+// Roles (288 threads): warps 0, 6, 7, 8 TMA producers, each filling every
+// fourth pipeline stage (one issuing thread moves only ~24 bytes per clock of
+// these tiles), warp 1 TMEM owner and single-thread MMA issuer, warps 2..5
+// epilogue.
 #include <algorithm>
 #include <type_traits>
 
@@ -36,7 +38,8 @@ namespace {
 
 using namespace tc;
 
-constexpr int kGThreads = 192;
+constexpr int kProducers = 4;                  // warps 0, 6, 7, 8
+constexpr int kGThreads = (6 + kProducers - 1) * 32;
 
 struct GroupArgs {
     LayoutView L;
@@ -46,6 +49,7 @@ struct GroupArgs {
     int ntiles;  // ceil(ext / NT)
     int sp_mn;   // sparse slab MN-major (block stored [k][line index]) else K-major
     int dn_mn;   // dense tile MN-major (stored [k][free]) else K-major ([free][k])
+    int dn_one;  // MN-major dense tile as one box of NT/64 panels (free extent a multiple of 64)
 };
 
 __host__ __device__ constexpr int gswz(int row_bytes) {
@@ -115,44 +119,87 @@ spmm_group_kernel(const __grid_constant__ CUtensorMap tmSp, const __grid_constan
     const int32_t* gptr = L.gl_ptr[o];
     const int32_t* gidx = L.gl_idx[o];
     const int32_t* gblk = L.gl_blk[o];
-    const int64_t per_group = (int64_t)args.Z * args.ntiles;
-    const int64_t total = (int64_t)L.n_tiles * per_group;
+    const int64_t total = (int64_t)L.n_tiles * args.Z * args.ntiles;
     const int S = L.S;
-    // first row of the block storage past its end: a TMA load there reads zeros
-    const int32_t y_absent = (int32_t)((int64_t)args.Z * L.nnz * BLK);
 
+    // Items run dense-tile-major (all groups and batch entries of one 256-wide
+    // stripe of the dense operand, largest groups first, then the next
+    // stripe): the CTAs working at any moment share a few MB of the dense
+    // operand, which then stays in L2.
+    const int64_t per_stripe = (int64_t)L.n_tiles * args.Z;
     auto item = [&](int64_t w, int& t, int& z, int& nt) {
-        t = L.gl_order[o][w / per_group];
-        const int rem = (int)(w % per_group);
-        z = rem / args.ntiles;
-        nt = rem % args.ntiles;
+        nt = (int)(w / per_stripe);
+        const int64_t rem = w % per_stripe;
+        t = L.gl_order[o][rem / args.Z];
+        z = (int)(rem % args.Z);
     };
 
-    if (warp == 0) {
-        // ---------------------------------------------------- TMA producer ----
+    if (warp == 0 || warp >= 6) {
+        // --------------------------------------------------- TMA producers ----
+        // The whole warp walks the slots: every 32 slots each lane loads one
+        // slot's index and block ids (one round trip instead of one per slot),
+        // lane 0 issues the TMA loads (the dense tile and the present blocks),
+        // and the warp zeroes the absent blocks' rows of the slab with shared
+        // stores, made visible to the tensor core before the stage's arrival.
+        // A stage's barrier gets one arrival (after its last slot) and one
+        // expected-bytes increase per slot.  Producer pid fills the stages
+        // with it % NP == pid; all walk every slot to keep the count.  NP is at
+        // most the number of stages: a producer's parity wait on its next
+        // stage (NP uses later) is only sound if its previous wait already
+        // ensured that the stage's use before last was consumed, i.e. NP <= ST.
+        constexpr uint32_t NP = kProducers < ST ? kProducers : ST;
+        const uint32_t pid = warp == 0 ? 0u : (uint32_t)(warp - 5);
         if (lane == 0) {
             tma_prefetch_desc(&tmSp);
             tma_prefetch_desc(&tmDn);
-            uint32_t it = 0;
-            for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
-                int t, z, nt;
-                item(w, t, z, nt);
-                const int h = t / L.ngroups;
-                const int64_t zh = (int64_t)z * L.H + h;
-                const int n0 = nt * kNT;
-                const int q0 = gptr[t], q1 = gptr[t + 1];
-                for (int c0 = q0; c0 < q1; c0 += KB, ++it) {
-                    const int ns = min(KB, q1 - c0);
+        }
+        uint32_t it = 0;  // stages begun
+        for (int64_t w = pid < NP ? blockIdx.x : total; w < total; w += gridDim.x) {
+            int t, z, nt;
+            item(w, t, z, nt);
+            const int h = t / L.ngroups;
+            const int64_t zh = (int64_t)z * L.H + h;
+            const int n0 = nt * kNT;
+            const int q0 = gptr[t], q1 = gptr[t + 1];
+            for (int base = q0; base < q1; base += 32) {
+                const int nq = min(32, q1 - base);
+                int my_idx = 0, my_blk[G];
+                if (lane < nq) {
+                    my_idx = gidx[base + lane];
+#pragma unroll
+                    for (int a = 0; a < G; ++a) my_blk[a] = gblk[(int64_t)(base + lane) * G + a];
+                }
+                for (int j = 0; j < nq; ++j) {
+                    const int q = base + j, rel = q - q0, sl = rel % KB;
+                    const int kb = __shfl_sync(0xffffffffu, my_idx, j) * BLK;  // first contraction index
+                    int bid[G];
+#pragma unroll
+                    for (int a = 0; a < G; ++a) bid[a] = __shfl_sync(0xffffffffu, my_blk[a], j);
                     const int st = it % ST;
-                    if (!mbar_wait(&empty[st], ((it / ST) & 1) ^ 1, ab)) goto producer_done;
-                    mbar_arrive_expect_tx(&full[st], ns * C::kSlot);
-                    for (int sl = 0; sl < ns; ++sl) {
-                        const int q = c0 + sl;
-                        uint8_t* sp = smem + st * C::kStage + sl * C::kSlot;
-                        uint8_t* dn = sp + C::kSp;
-                        const int kb = gidx[q] * BLK;  // first contraction index of the slot
-                        if (args.dn_mn) {
-                            // [k rows][free cols]: NT/64 panels of 64 free columns, B rows each
+                    const bool mine = it % NP == pid;
+                    if (sl == 0 && mine) {
+                        bool ok = true;
+                        if (lane == 0) ok = mbar_wait(&empty[st], ((it / ST) & 1) ^ 1, ab);
+                        if (!__shfl_sync(0xffffffffu, ok, 0)) goto producer_done;
+                        __syncwarp();  // the stage's previous MMAs are done before any lane writes it
+                    }
+                    uint8_t* sp = smem + st * C::kStage + sl * C::kSlot;
+                    uint8_t* dn = sp + C::kSp;
+                    if (!mine) {
+                        if (sl == KB - 1 || q == q1 - 1) ++it;
+                        continue;
+                    }
+                    int present = 0;
+#pragma unroll
+                    for (int a = 0; a < G; ++a) present += bid[a] >= 0;
+                    if (lane == 0) {
+                        mbar_expect_tx(&full[st], C::kDn + present * (BLK * BLK * 2));
+                        if (args.dn_one) {
+                            // [k rows][free cols]: NT/64 panels of 64 free columns, B rows each,
+                            // in one box (each TMA instruction costs the issuing thread ~60
+                            // cycles on top of its bytes, so fewer, larger boxes)
+                            tma_load_3d(smem_u32(dn), &tmDn, 0, (int32_t)(zh * S + kb), n0 / 64, &full[st]);
+                        } else if (args.dn_mn) {
 #pragma unroll
                             for (int p = 0; p < kNT / 64; ++p)
                                 tma_load_2d(smem_u32(dn + p * (BLK * 128)), &tmDn, n0 + 64 * p,
@@ -164,22 +211,36 @@ spmm_group_kernel(const __grid_constant__ CUtensorMap tmSp, const __grid_constan
                                 tma_load_2d(smem_u32(dn + p * (kNT * RB)), &tmDn, kb + W * p,
                                             (int32_t)(zh * args.ext + n0), &full[st]);
                         }
+                    }
 #pragma unroll
-                        for (int a = 0; a < G; ++a) {
-                            const int bid = gblk[(int64_t)q * G + a];
-                            const int32_t y = bid >= 0 ? (int32_t)(((int64_t)z * L.nnz + bid) * BLK) : y_absent;
+                    for (int a = 0; a < G; ++a) {
 #pragma unroll
-                            for (int p = 0; p < KPp; ++p) {
-                                // K-major: panel p of the slab, rows a*B..; MN-major: M-panel a*KPp + p
-                                const int off = args.sp_mn ? (a * KPp + p) * (BLK * RB) : p * (128 * RB) + a * (BLK * RB);
-                                tma_load_2d(smem_u32(sp + off), &tmSp, W * p, y, &full[st]);
+                        for (int p = 0; p < KPp; ++p) {
+                            // K-major: panel p of the slab, rows a*B..; MN-major: M-panel a*KPp + p.
+                            // Either way BLK * RB contiguous bytes.
+                            const int off = args.sp_mn ? (a * KPp + p) * (BLK * RB) : p * (128 * RB) + a * (BLK * RB);
+                            if (bid[a] >= 0) {
+                                if (lane == 0)
+                                    tma_load_2d(smem_u32(sp + off), &tmSp, W * p,
+                                                (int32_t)(((int64_t)z * L.nnz + bid[a]) * BLK), &full[st]);
+                            } else {
+#pragma unroll
+                                for (int i = lane * 16; i < BLK * RB; i += 32 * 16)
+                                    *reinterpret_cast<uint4*>(sp + off + i) = make_uint4(0u, 0u, 0u, 0u);
                             }
                         }
                     }
+                    if (sl == KB - 1 || q == q1 - 1) {
+                        // stage complete: zeroes visible to the tensor core, then one arrival
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&full[st]);
+                        ++it;
+                    }
                 }
             }
-        producer_done:;
         }
+    producer_done:;
     } else if (warp == 1) {
         // ---------------------------------------------- MMA issuer (one thread) ----
         if (lane == 0) {
@@ -317,8 +378,10 @@ int group_launch(const bsp_layout_s* Lh, const void* dense, const void* sparse, 
     const uint64_t ZH = (uint64_t)Z * Lh->H;
     CUtensorMap msp, mdn, mc;
     int rc = make_tmap_2d(&msp, sparse, bf, (uint64_t)Z * Lh->nnz * BLK, BLK, BLK, Cfg::W, Cfg::RB);
+    const int dn_one = dn_mn && ext % 64 == 0;
     if (!rc) {
-        if (dn_mn) rc = make_tmap_2d(&mdn, dense, bf, ZH * Lh->S, ext, BLK, 64, 128);
+        if (dn_one) rc = make_tmap_panels(&mdn, dense, bf, ZH * Lh->S, ext, BLK, kNT / 64);
+        else if (dn_mn) rc = make_tmap_2d(&mdn, dense, bf, ZH * Lh->S, ext, BLK, 64, 128);
         else rc = make_tmap_2d(&mdn, dense, bf, ZH * ext, Lh->S, kNT, Cfg::W, Cfg::RB);
     }
     if (!rc) {
@@ -326,7 +389,7 @@ int group_launch(const bsp_layout_s* Lh, const void* dense, const void* sparse, 
         else rc = make_tmap_3d(&mc, Cout, bf, Lh->S, ext, ZH, 32, 64, 0);
     }
     if (rc) return rc;
-    GroupArgs a{Lh->view, Z, orient, ext, (ext + kNT - 1) / kNT, sp_mn, dn_mn};
+    GroupArgs a{Lh->view, Z, orient, ext, (ext + kNT - 1) / kNT, sp_mn, dn_mn, dn_one};
     auto kern = spmm_group_kernel<T, BLK, NT, OUT_T>;
     constexpr int smem = Cfg::kAlloc;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)

@@ -61,4 +61,19 @@ int make_tmap_3d(CUtensorMap* map, const void* base, int is_bf16, uint64_t d0, u
     return r == CUDA_SUCCESS ? BSP_OK : BSP_ERR_UNSUPPORTED;
 }
 
+int make_tmap_panels(CUtensorMap* map, const void* base, int is_bf16, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows, uint32_t box_panels) {
+    auto fn = encode_fn();
+    if (!fn) return BSP_ERR_CUDA;
+    if (cols % 64 != 0) return BSP_ERR_UNSUPPORTED;
+    const cuuint64_t dims[3] = {64, rows, cols / 64};
+    const cuuint64_t strides[2] = {cols * 2, 128};
+    const cuuint32_t box[3] = {64, box_rows, box_panels};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? BSP_OK : BSP_ERR_UNSUPPORTED;
+}
+
 }  // namespace bsp
