@@ -1,0 +1,280 @@
+// Tensor-core (tcgen05) SDD for bf16 / fp16 with fp32 accumulation: the
+// sampled dense x dense product of "question on blocksparse" (openai/triton
+// issue 117), evaluated on the layout's blocks only.
+//
+// Row tiles of 128 query rows (the attention work list); each step computes
+// the 128 x 128 score tile against G = 128/B key blocks into one of four TMEM
+// accumulators; four epilogue warps write the present blocks while the MMA
+// works ahead.
+//
+// Roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner and
+// single-thread MMA issuer, warps 2..5 epilogue (thread = TMEM lane).
+#include <algorithm>
+#include <type_traits>
+
+#include "common.cuh"
+#include "tc_common.cuh"
+
+namespace bsp {
+namespace {
+
+using namespace tc;
+
+constexpr int kThreads = 192;
+
+// ------------------------------------------------------------------ SDD ----
+
+struct SddArgs {
+    LayoutView L;
+    void* C;
+    int Z;
+};
+
+template <int KP, int BLK>
+struct SddCfg {
+    static constexpr int kTile = 128 * 64 * KP * 2;  // 128 rows x K (KP panels of 64)
+    static constexpr int BST = 3;                    // key-tile stages
+    static constexpr int kA = 0;                     // 2 query-tile stages
+    static constexpr int kB = 2 * kTile;
+    static constexpr int kPitch = BLK * 2 + 16;      // staging row pitch (padded: no bank conflicts)
+    static constexpr int kStg = kB + BST * kTile;    // per-warp staging, 32 rows
+    static constexpr int kAlloc = kStg + 4 * 32 * kPitch + 1024;
+};
+
+template <typename T, int BLK, int KP>
+__global__ void __launch_bounds__(kThreads, 1)
+sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const SddArgs args) {
+    using C = SddCfg<KP, BLK>;
+    constexpr int G = 128 / BLK;
+    constexpr int BST = C::BST;
+    constexpr uint32_t kTileBytes = C::kTile;
+    constexpr uint32_t kIdesc = idesc_f16(128, 128, std::is_same<T, __nv_bfloat16>::value, 0, 0);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    __shared__ uint64_t a_full[2], a_empty[2], b_full[BST], b_empty[BST], s_full[4], s_empty[4];
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+
+    const LayoutView& L = args.L;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    Abort ab{&abort_flag, L.status};
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&a_full[i], 1);
+            mbar_init(&a_empty[i], 1);
+        }
+        for (int i = 0; i < BST; ++i) {
+            mbar_init(&b_full[i], 1);
+            mbar_init(&b_empty[i], 1);
+        }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], 4);
+        }
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tS = tmem_base;
+
+    const int64_t total = (int64_t)args.Z * L.n_tiles;
+    const int S = L.S;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            uint32_t a_it = 0, g = 0;
+            for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+                const int tile = L.tile_order[w / args.Z];
+                const int z = (int)(w % args.Z);
+                const int h = tile / L.ngroups, gq = tile % L.ngroups;
+                const int s0 = L.tile_step_ptr[tile], ns = L.tile_step_ptr[tile + 1] - s0;
+                if (ns == 0) continue;
+                const int64_t zh = (int64_t)z * L.H + h;
+                const uint32_t as = a_it & 1;
+                if (!mbar_wait(&a_empty[as], ((a_it >> 1) & 1) ^ 1, ab)) goto producer_done;
+                mbar_arrive_expect_tx(&a_full[as], kTileBytes);
+                for (int p = 0; p < KP; ++p)
+                    tma_load_2d(smem_u32(smem + C::kA + as * kTileBytes + p * 16384), &tmA, p * 64,
+                                (int32_t)(zh * S + gq * 128), &a_full[as]);
+                ++a_it;
+                for (int n = 0; n < ns; ++n, ++g) {
+                    const int s = s0 + n;
+                    const uint32_t st = g % BST;
+                    if (!mbar_wait(&b_empty[st], ((g / BST) & 1) ^ 1, ab)) goto producer_done;
+                    mbar_arrive_expect_tx(&b_full[st], kTileBytes);
+#pragma unroll
+                    for (int b = 0; b < G; ++b) {
+                        int c = L.step_col[s * G + b];
+                        if (c < 0) c = L.step_col[s * G];
+                        for (int p = 0; p < KP; ++p)
+                            tma_load_2d(smem_u32(smem + C::kB + st * kTileBytes + p * 16384 + b * BLK * 128), &tmB,
+                                        p * 64, (int32_t)(zh * S + (int64_t)c * BLK), &b_full[st]);
+                    }
+                }
+            }
+        producer_done:;
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            uint32_t a_it = 0, g = 0;
+            for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+                const int tile = L.tile_order[w / args.Z];
+                const int ns = L.tile_step_ptr[tile + 1] - L.tile_step_ptr[tile];
+                if (ns == 0) continue;
+                const uint32_t as = a_it & 1;
+                if (!mbar_wait(&a_full[as], (a_it >> 1) & 1, ab)) goto mma_done;
+                for (int n = 0; n < ns; ++n, ++g) {
+                    const uint32_t sb = g & 3, st = g % BST;  // TMEM accumulator, key-tile stage
+                    if (!mbar_wait(&s_empty[sb], ((g >> 2) & 1) ^ 1, ab)) goto mma_done;
+                    if (!mbar_wait(&b_full[st], (g / BST) & 1, ab)) goto mma_done;
+                    tc_fence_after();
+                    const uint32_t abase = smem_u32(smem + C::kA + as * kTileBytes);
+                    const uint32_t bbase = smem_u32(smem + C::kB + st * kTileBytes);
+#pragma unroll
+                    for (int ks = 0; ks < KP * 4; ++ks) {
+                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+                        mma_f16(tS + sb * 128, smem_desc(abase + off, 16, 1024, kSw128),
+                                smem_desc(bbase + off, 16, 1024, kSw128), kIdesc, ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&s_full[sb]);
+                    mma_commit(&b_empty[st]);
+                    if (n == ns - 1) mma_commit(&a_empty[as]);
+                }
+                ++a_it;
+            }
+        mma_done:;
+        }
+    } else {
+        // Epilogue: each warp owns 32 rows of the tile (TMEM lanes 32q..32q+31).
+        // Per present block it stages its rows in shared memory, then copies
+        // them out together: the warp's rows of one block are RS = min(32, B)
+        // consecutive rows, i.e. one contiguous RS*B run of the output.
+        constexpr int RS = BLK < 32 ? BLK : 32;
+        constexpr int C16 = BLK * 2 / 16;  // 16-byte chunks per block row
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const int a = row / BLK;
+        uint8_t* stg = smem + C::kStg + quad * 32 * C::kPitch;
+        T* Cp = reinterpret_cast<T*>(args.C);
+        uint32_t g = 0;
+        for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+            const int tile = L.tile_order[w / args.Z];
+            const int z = (int)(w % args.Z);
+            const int s0 = L.tile_step_ptr[tile], ns = L.tile_step_ptr[tile + 1] - s0;
+            for (int n = 0; n < ns; ++n, ++g) {
+                const int s = s0 + n;
+                const uint32_t sb = g & 3;
+                bool ok = mbar_wait(&s_full[sb], (g >> 2) & 1, ab);
+                if (!__all_sync(0xffffffffu, ok)) goto epi_done;
+                tc_fence_after();
+                uint32_t x[128];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    tmem_ld32_sync(tS + sb * 128 + lane_base + c * 32,
+                                   *reinterpret_cast<uint32_t(*)[32]>(x + 32 * c));
+                // the accumulator is free as soon as it is in registers
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_empty[sb]);
+#pragma unroll
+                for (int b = 0; b < G; ++b) {
+                    const int blk = L.step_blk[(s * G + a) * G + b];
+                    if (__all_sync(0xffffffffu, blk < 0)) continue;
+                    if (blk >= 0) {
+                        uint4* srow = reinterpret_cast<uint4*>(stg + lane * C::kPitch);
+#pragma unroll
+                        for (int j = 0; j < C16; ++j) {
+                            const int o = b * BLK + 8 * j;
+                            srow[j] = make_uint4(
+                                Pack2<T>::pack(__uint_as_float(x[o]), __uint_as_float(x[o + 1])),
+                                Pack2<T>::pack(__uint_as_float(x[o + 2]), __uint_as_float(x[o + 3])),
+                                Pack2<T>::pack(__uint_as_float(x[o + 4]), __uint_as_float(x[o + 5])),
+                                Pack2<T>::pack(__uint_as_float(x[o + 6]), __uint_as_float(x[o + 7])));
+                        }
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int seg = 0; seg < 32 / RS; ++seg) {
+                        const int sblk = __shfl_sync(0xffffffffu, blk, seg * RS);
+                        if (sblk < 0) continue;
+                        const int r_in0 = (quad * 32 + seg * RS) % BLK;
+                        uint4* dst = reinterpret_cast<uint4*>(Cp + (((int64_t)z * L.nnz + sblk) * BLK + r_in0) * BLK);
+                        for (int k = lane; k < RS * C16; k += 32)
+                            dst[k] = *reinterpret_cast<const uint4*>(stg + (seg * RS + k / C16) * C::kPitch +
+                                                                     (k % C16) * 16);
+                    }
+                    __syncwarp();
+                }
+            }
+        }
+    epi_done:;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+// --------------------------------------------------------------- launch ----
+
+template <typename T, int BLK, int KP>
+int sdd_launch(const bsp_layout_s* Lh, const void* A, const void* B, void* Cout, int Z, int K, cudaStream_t s) {
+    const int bf = std::is_same<T, __nv_bfloat16>::value;
+    const uint64_t rows = (uint64_t)Z * Lh->H * Lh->S;
+    CUtensorMap ma, mb;
+    int rc = make_tmap_2d(&ma, A, bf, rows, K, 128, 64, 128);
+    if (!rc) rc = make_tmap_2d(&mb, B, bf, rows, K, BLK, 64, 128);
+    if (rc) return rc;
+    SddArgs a{Lh->view, Cout, Z};
+    auto kern = sdd_tc_kernel<T, BLK, KP>;
+    constexpr int smem = SddCfg<KP, BLK>::kAlloc;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return BSP_ERR_CUDA;
+    const int64_t total = (int64_t)Z * Lh->n_tiles;
+    const int grid = (int)std::min<int64_t>(total, sm_count());
+    kern<<<grid, kThreads, smem, s>>>(ma, mb, a);
+    return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
+}
+
+template <typename T, int BLK>
+int sdd_by_k(const bsp_layout_s* L, const void* A, const void* B, void* C, int Z, int K, cudaStream_t s) {
+    if (K <= 64) return sdd_launch<T, BLK, 1>(L, A, B, C, Z, K, s);
+    return sdd_launch<T, BLK, 2>(L, A, B, C, Z, K, s);
+}
+
+template <typename T>
+int sdd_by_block(const bsp_layout_s* L, const void* A, const void* B, void* C, int Z, int K, cudaStream_t s) {
+    switch (L->B) {
+        case 16: return sdd_by_k<T, 16>(L, A, B, C, Z, K, s);
+        case 32: return sdd_by_k<T, 32>(L, A, B, C, Z, K, s);
+        case 64: return sdd_by_k<T, 64>(L, A, B, C, Z, K, s);
+        case 128: return sdd_by_k<T, 128>(L, A, B, C, Z, K, s);
+        default: return BSP_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace
+
+int launch_sdd_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z, int K, int ta,
+                  int tb, cudaStream_t s) {
+    // scores Q K^T: both operands [S][K] (K-major); K a multiple of 8, at most 128
+    if (ta != 0 || tb != 1 || K % 8 != 0 || K > 128) return BSP_ERR_UNSUPPORTED;
+    if ((uint64_t)Z * L->H * L->S >= (1ull << 31)) return BSP_ERR_UNSUPPORTED;
+    if (dtype == BSP_BF16) return sdd_by_block<__nv_bfloat16>(L, A, B, C, Z, K, s);
+    if (dtype == BSP_F16) return sdd_by_block<__half>(L, A, B, C, Z, K, s);
+    return BSP_ERR_UNSUPPORTED;
+}
+
+}  // namespace bsp
