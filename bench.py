@@ -146,9 +146,14 @@ def config_of(w, lay, path_name):
 
 
 def kernel_source_sha():
+    """Hash of the fused attention kernel's own sources (the kernel whose DRAM
+    traffic profiles/traffic.json records)."""
     h = hashlib.sha256()
-    for f in sorted(os.listdir(os.path.join(ROOT, "sparse_attention_layout_gb300", "csrc"))):
-        with open(os.path.join(ROOT, "sparse_attention_layout_gb300", "csrc", f), "rb") as fh:
+    d = os.path.join(ROOT, "sparse_attention_layout_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if not f.startswith("tc_attention"):
+            continue
+        with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
@@ -257,8 +262,10 @@ def weak_value(flops_per_rank: float, world: int, ms_step: float) -> float:
     return flops_per_rank * world / (ms_step * 1e-3) / 1e12
 
 
-def time_launches(fn, n, stream):
+def time_launches(fn, n, stream, warmup=3):
     import torch
+    for _ in range(warmup):  # first launches load the module and build tensor maps
+        fn()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     start.record(stream)
