@@ -406,7 +406,16 @@ def run_ours(args):
                "sample": f"{cpu_rows} random rows of {w.Z * w.H * w.S} ({cpu_s:.1f} s, fp64, OpenMP)"}
     if world > 1:
         dist.barrier()
-    peak = pk["bf16_tflops"] if w.dtype != "f32" else None
+    clocks = clk.summary()
+    if w.dtype != "f32":
+        bound, peak, peak_src = "tensor", pk["bf16_tflops"], f"bf16_tflops (burst) of {pk_kind}"
+    else:
+        # fp32 runs on the FFMA path: 128 FP32 lanes per SM, 2 FLOP per FMA, at
+        # the highest SM clock the sampler saw (else the GB300's 2070 MHz)
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        mhz = clocks["sm_max_mhz"] if clocks else 2070.0
+        bound, peak = "alu", sms * 128 * 2 * mhz * 1e6 / 1e12
+        peak_src = f"derived: {sms} SMs x 128 FFMA/clk x 2 FLOP x {mhz:.0f} MHz"
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -414,8 +423,8 @@ def run_ours(args):
         "config": config_of(w, lay, "fused attention kernel"),
         "gpu_launches": args.steps,
         "roofline": {
-            "bound": "tensor", "kernel": "attention", "achieved": achieved, "peak": peak,
-            "peak_source": f"bf16_tflops (burst) of {pk_kind}", "unit": "TFLOP/s",
+            "bound": bound, "kernel": "attention", "achieved": achieved, "peak": peak,
+            "peak_source": peak_src, "unit": "TFLOP/s",
             "frac": (achieved / peak) if peak else None,
             "traffic": traffic_for("attention", w.name),
             "algorithmic_flops_per_launch": flops,
@@ -424,7 +433,7 @@ def run_ours(args):
             "value": flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "cpu_baseline": cpu,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "lib": bsp.lib_path(),
     }
     if ops is not None:

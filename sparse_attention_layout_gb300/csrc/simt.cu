@@ -440,6 +440,188 @@ int dds_t(const bsp_layout_s* L, const void* A, const void* B, void* C, int Z, i
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }
 
+// Register-tiled variant for B >= 64 and D = 64 or 128 (the fp32 workloads'
+// head sizes).  Same work split, online recurrence and masks as above, but the
+// shared-memory traffic is vectorised: rows are padded to D + 4 floats (an odd
+// number of 16-byte units, so the strided row reads below hit distinct banks),
+// Q K^T reads float4 along D (8 vector loads per 64 FMAs instead of one scalar
+// load per 2 FMAs), and each thread owns 4 contiguous output columns per 64 so
+// that P V reads V and P as float4 too.
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, 2)
+attention_simt_v4_kernel(LayoutView L, const T* __restrict__ Q, const T* __restrict__ K,
+                         const T* __restrict__ V, T* __restrict__ O, int Z, float c2, int kind,
+                         const uint8_t* __restrict__ mask) {
+    constexpr int TR = 64, R = 4, DP = D + 4, PP = TR + 4, NG = D / 64, D4 = D / 4;
+    extern __shared__ float4 smem_v4[];
+    float* Qs = reinterpret_cast<float*>(smem_v4);  // [TR][DP], pre-scaled by c2
+    float* Ks = Qs + TR * DP;                        // [TR][DP]
+    float* Vs = Ks + TR * DP;                        // [TR][DP]
+    float* Ps = Vs + TR * DP;                        // [TR][PP]
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int B = L.B, S = L.S;
+    const int nsub = B / TR;
+    const int64_t total = (int64_t)L.H * L.nb * Z * nsub;
+    auto load_tile = [&](float* dst, const T* src, float mul) {
+        for (int e = threadIdx.x; e < TR * D4; e += kThreads) {
+            const int rr = e / D4, c4 = e % D4;
+            const T* p = src + (int64_t)rr * D + 4 * c4;
+            *reinterpret_cast<float4*>(dst + rr * DP + 4 * c4) =
+                make_float4(to_f32(p[0]) * mul, to_f32(p[1]) * mul, to_f32(p[2]) * mul, to_f32(p[3]) * mul);
+        }
+    };
+    for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+        const int64_t rank = w / ((int64_t)Z * nsub);
+        const int rem = (int)(w % ((int64_t)Z * nsub));
+        const int64_t z = rem / nsub;
+        const int sub = rem % nsub;
+        const int key = L.row_order[rank];
+        const int h = key / L.nb, i = key % L.nb;
+        const int64_t zh = z * L.H + h;
+        const int r0 = i * B + sub * TR;  // first query row of this CTA
+        load_tile(Qs, Q + (zh * S + r0) * D, c2);
+        float m[R], l[R], acc[R][NG][4];
+#pragma unroll
+        for (int u = 0; u < R; ++u) {
+            m[u] = -INFINITY;
+            l[u] = 0.f;
+#pragma unroll
+            for (int g = 0; g < NG; ++g)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[u][g][c] = 0.f;
+        }
+        const int q0 = L.row_ptr[h * (L.nb + 1) + i], q1 = L.row_ptr[h * (L.nb + 1) + i + 1];
+        for (int q = q0; q < q1; ++q) {
+            const int j = L.col_idx[q];
+            for (int kc = 0; kc < B; kc += TR) {
+                const int c0 = j * B + kc;  // first key row of the chunk
+                __syncthreads();            // previous chunk fully consumed (and Qs written)
+                load_tile(Ks, K + (zh * S + c0) * D, 1.f);
+                load_tile(Vs, V + (zh * S + c0) * D, 1.f);
+                __syncthreads();
+                float s[R][R];
+#pragma unroll
+                for (int u = 0; u < R; ++u)
+#pragma unroll
+                    for (int v = 0; v < R; ++v) s[u][v] = 0.f;
+#pragma unroll 4
+                for (int d4 = 0; d4 < D4; ++d4) {
+                    float4 qa[R], kb[R];
+#pragma unroll
+                    for (int u = 0; u < R; ++u) qa[u] = *reinterpret_cast<const float4*>(Qs + (ty + 16 * u) * DP + 4 * d4);
+#pragma unroll
+                    for (int v = 0; v < R; ++v) kb[v] = *reinterpret_cast<const float4*>(Ks + (tx + 16 * v) * DP + 4 * d4);
+#pragma unroll
+                    for (int u = 0; u < R; ++u)
+#pragma unroll
+                        for (int v = 0; v < R; ++v) {
+                            s[u][v] = fmaf(qa[u].x, kb[v].x, s[u][v]);
+                            s[u][v] = fmaf(qa[u].y, kb[v].y, s[u][v]);
+                            s[u][v] = fmaf(qa[u].z, kb[v].z, s[u][v]);
+                            s[u][v] = fmaf(qa[u].w, kb[v].w, s[u][v]);
+                        }
+                }
+                // intra-block mask
+#pragma unroll
+                for (int u = 0; u < R; ++u) {
+                    const int r = r0 + ty + 16 * u;
+#pragma unroll
+                    for (int v = 0; v < R; ++v) {
+                        const int c = c0 + tx + 16 * v;
+                        bool keep = true;
+                        if (kind == BSP_MASK_DIAG_CAUSAL) keep = (j != i) || (c <= r);
+                        else if (kind == BSP_MASK_DENSE) keep = mask[(int64_t)r * S + c] != 0;
+                        if (!keep) s[u][v] = -INFINITY;
+                    }
+                }
+                // online softmax update per row (a row's 16 threads form a half-warp)
+#pragma unroll
+                for (int u = 0; u < R; ++u) {
+                    float cm = -INFINITY;
+#pragma unroll
+                    for (int v = 0; v < R; ++v) cm = fmaxf(cm, s[u][v]);
+#pragma unroll
+                    for (int o = 8; o; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+                    const float mn = fmaxf(m[u], cm);
+                    float alpha = 1.f, rs = 0.f;
+                    if (mn != -INFINITY) {
+                        alpha = (m[u] == -INFINITY) ? 0.f : exp2f(m[u] - mn);
+#pragma unroll
+                        for (int v = 0; v < R; ++v) {
+                            s[u][v] = exp2f(s[u][v] - mn);
+                            rs += s[u][v];
+                        }
+                    } else {
+#pragma unroll
+                        for (int v = 0; v < R; ++v) s[u][v] = 0.f;
+                    }
+#pragma unroll
+                    for (int o = 8; o; o >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
+                    l[u] = l[u] * alpha + rs;
+                    m[u] = mn;
+#pragma unroll
+                    for (int g = 0; g < NG; ++g)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) acc[u][g][c] *= alpha;
+#pragma unroll
+                    for (int v = 0; v < R; ++v) Ps[(ty + 16 * u) * PP + tx + 16 * v] = s[u][v];
+                }
+                __syncthreads();
+#pragma unroll 2
+                for (int cc4 = 0; cc4 < TR / 4; ++cc4) {
+                    float4 pa[R];
+#pragma unroll
+                    for (int u = 0; u < R; ++u) pa[u] = *reinterpret_cast<const float4*>(Ps + (ty + 16 * u) * PP + 4 * cc4);
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        float4 vv[NG];
+#pragma unroll
+                        for (int g = 0; g < NG; ++g)
+                            vv[g] = *reinterpret_cast<const float4*>(Vs + (4 * cc4 + k4) * DP + 64 * g + 4 * tx);
+#pragma unroll
+                        for (int u = 0; u < R; ++u) {
+                            const float p = k4 == 0 ? pa[u].x : k4 == 1 ? pa[u].y : k4 == 2 ? pa[u].z : pa[u].w;
+#pragma unroll
+                            for (int g = 0; g < NG; ++g) {
+                                acc[u][g][0] = fmaf(p, vv[g].x, acc[u][g][0]);
+                                acc[u][g][1] = fmaf(p, vv[g].y, acc[u][g][1]);
+                                acc[u][g][2] = fmaf(p, vv[g].z, acc[u][g][2]);
+                                acc[u][g][3] = fmaf(p, vv[g].w, acc[u][g][3]);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < R; ++u) {
+            const float inv = l[u] > 0.f ? 1.0f / l[u] : 0.f;
+            const int64_t r = r0 + ty + 16 * u;
+#pragma unroll
+            for (int g = 0; g < NG; ++g) {
+                T* dst = O + (zh * S + r) * D + 64 * g + 4 * tx;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) dst[c] = from_f32<T>(acc[u][g][c] * inv);
+            }
+        }
+        __syncthreads();  // Qs reused by the next work item
+    }
+}
+
+template <typename T, int D>
+int attn_v4(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, int Z, float scale,
+            int kind, const uint8_t* mask, cudaStream_t s) {
+    const int64_t total = (int64_t)L->H * L->nb * Z * (L->B / 64);
+    if (total == 0) return BSP_OK;
+    const size_t smem = sizeof(float) * ((size_t)3 * 64 * (D + 4) + (size_t)64 * (64 + 4));
+    auto kern = attention_simt_v4_kernel<T, D>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return BSP_ERR_CUDA;
+    kern<<<grid_for(total), kThreads, smem, s>>>(L->view, (const T*)Q, (const T*)K, (const T*)V, (T*)O, Z,
+                                                  scale * kLog2e, kind, mask);
+    return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
+}
+
 template <typename T, int TR>
 int attn_tr(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, int Z,
             int D, float scale, int kind, const uint8_t* mask, cudaStream_t s) {
@@ -457,6 +639,8 @@ int attn_tr(const bsp_layout_s* L, const void* Q, const void* K, const void* V, 
 template <typename T>
 int attn_t(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, int Z, int D,
            float scale, int kind, const uint8_t* mask, cudaStream_t s) {
+    if (L->B >= 64 && D == 64) return attn_v4<T, 64>(L, Q, K, V, O, Z, scale, kind, mask, s);
+    if (L->B >= 64 && D == 128) return attn_v4<T, 128>(L, Q, K, V, O, Z, scale, kind, mask, s);
     switch (L->B) {
         case 16: return attn_tr<T, 16>(L, Q, K, V, O, Z, D, scale, kind, mask, s);
         case 32: return attn_tr<T, 32>(L, Q, K, V, O, Z, D, scale, kind, mask, s);
