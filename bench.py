@@ -313,6 +313,23 @@ def per_op_section(w, lay, L, q, k, v, pk, bsp, stream):
     C2 = bsp.bsp_dds(L4, Ad, A)
     ms = time_launches(lambda: bsp.bsp_dds(L4, Ad, A, C2), 10, stream)
     out["dds_spmm_10pct"] = {"ms": ms, "TFLOP/s": fl / ms / 1e9, "frac_of_bf16_peak": fl / ms / 1e9 / pk["bf16_tflops"]}
+    del A, Bd, Ad, C1, C2
+    # the same shapes at the other block sizes, 10 % and 50 % density
+    out["spmm_blocks"] = {}
+    for bs, spb in W.SPMM_BLOCKS.items():
+        for dens in W.SPMM_BLOCK_DENSITIES:
+            layb = spb.layout(dens)
+            Lb = bsp.bsp_layout_compile(layb, bs)
+            A = spb.sparse_values(Lb.nnz, dens).cuda()
+            Bd, Ad = spb.dense_dsd(dens).cuda(), spb.dense_dds(dens).cuda()
+            C1, C2 = bsp.bsp_dsd(Lb, A, Bd), bsp.bsp_dds(Lb, Ad, A)
+            fl = 2.0 * bs * bs * spb.N * Lb.nnz
+            ms1 = time_launches(lambda: bsp.bsp_dsd(Lb, A, Bd, C1), 10, stream)
+            ms2 = time_launches(lambda: bsp.bsp_dds(Lb, Ad, A, C2), 10, stream)
+            out["spmm_blocks"][f"B{bs}_{int(round(dens * 100))}pct"] = {
+                "dsd_ms": ms1, "dsd_TFLOP/s": fl / ms1 / 1e9, "dds_ms": ms2, "dds_TFLOP/s": fl / ms2 / 1e9,
+                "frac_of_bf16_peak": [fl / ms1 / 1e9 / pk["bf16_tflops"], fl / ms2 / 1e9 / pk["bf16_tflops"]]}
+            del A, Bd, Ad, C1, C2, Lb
     return out
 
 

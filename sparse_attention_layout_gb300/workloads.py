@@ -191,18 +191,27 @@ class SpmmWorkload:
     dtype: str = "bf16"
     index: int = 4
 
+    def _salt(self, density: float) -> int:
+        # the block size enters the seeds only for the other block sizes, so the
+        # 32-wide workload keeps its original draws
+        return int(round(density * 100)) + (0 if self.B == 32 else 1000 * self.B)
+
     def layout(self, density: float) -> np.ndarray:
-        return layout_uniform(self.S // self.B, density, H=1, seed=self.index * 100 + int(round(density * 100)))
+        return layout_uniform(self.S // self.B, density, H=1, seed=self.index * 100 + self._salt(density))
 
     def sparse_values(self, nnz: int, density: float) -> torch.Tensor:
-        return uniform((1, nnz, self.B, self.B), self.dtype, 4000 + int(round(density * 100)))
+        return uniform((1, nnz, self.B, self.B), self.dtype, 4000 + self._salt(density))
 
     def dense_dsd(self, density: float) -> torch.Tensor:
-        return uniform((1, 1, self.S, self.N), self.dtype, 4100 + int(round(density * 100)))
+        return uniform((1, 1, self.S, self.N), self.dtype, 4100 + self._salt(density))
 
     def dense_dds(self, density: float) -> torch.Tensor:
-        return uniform((1, 1, self.N, self.S), self.dtype, 4200 + int(round(density * 100)))
+        return uniform((1, 1, self.N, self.S), self.dtype, 4200 + self._salt(density))
 
 
 SPMM = SpmmWorkload()
 SPMM_DENSITIES = (0.10, 0.25, 0.50)
+# the same spMM shapes at the other block sizes (8192 x 8192 sparse operand,
+# 4096-wide dense operand), densities 10 % and 50 %
+SPMM_BLOCKS = {b: SpmmWorkload(B=b) for b in (16, 32, 64, 128)}
+SPMM_BLOCK_DENSITIES = (0.10, 0.50)

@@ -127,9 +127,10 @@ def test_softmax_workload(bsp, oracle, name):
     assert_close(got, want, DT[w.dtype], f"{name} softmax, {sel.size} sampled rows")
 
 
-@pytest.mark.parametrize("density", W.SPMM_DENSITIES)
-def test_spmm_workload(bsp, oracle, density):
-    sp = W.SPMM
+@pytest.mark.parametrize("B,density", [(32, d) for d in W.SPMM_DENSITIES] +
+                         [(b, d) for b in (16, 64, 128) for d in W.SPMM_BLOCK_DENSITIES])
+def test_spmm_workload(bsp, oracle, B, density):
+    sp = W.SPMM_BLOCKS[B]
     lay = sp.layout(density)
     L = bsp.bsp_layout_compile(lay, sp.B)
     A = sp.sparse_values(L.nnz, density)
@@ -144,10 +145,10 @@ def test_spmm_workload(bsp, oracle, density):
     rows = np.unique(np.concatenate([rng.choice(sp.S, 10, replace=False), [0, sp.S - 1],
                                      empty_rows[:2] * sp.B])).astype(np.int64)
     got = to_np(C1[0, 0][torch.from_numpy(rows).cuda()])
-    assert_close(got, oracle.dsd(lay, sp.B, A, Bd, sel=rows), torch.bfloat16, f"DSD spMM {density}")
+    assert_close(got, oracle.dsd(lay, sp.B, A, Bd, sel=rows), torch.bfloat16, f"DSD spMM B={B} {density}")
     mrows = np.unique(np.concatenate([rng.choice(sp.N, 6, replace=False), [0, sp.N - 1]])).astype(np.int64)
     got = to_np(C2[0, 0][torch.from_numpy(mrows).cuda()])
-    assert_close(got, oracle.dds(lay, sp.B, Ad, A, sel=mrows), torch.bfloat16, f"DDS spMM {density}")
+    assert_close(got, oracle.dds(lay, sp.B, Ad, A, sel=mrows), torch.bfloat16, f"DDS spMM B={B} {density}")
     # block-rows without any block are exactly zero in the DSD output
     for i in empty_rows[:4]:
         assert (C1[0, 0, i * sp.B:(i + 1) * sp.B] == 0).all()
