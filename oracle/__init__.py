@@ -56,6 +56,8 @@ def _bind(lib):
     lib.oracle_dsd.argtypes = [P, i32, i32, i32, i32, i32, i32, i32, P, P, i64, P, P]
     lib.oracle_dds.argtypes = [P, i32, i32, i32, i32, i32, i32, i32, P, P, i64, P, P]
     lib.oracle_attention.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, dbl, i32, P, i64, P, P]
+    lib.oracle_softmax_backward.argtypes = [P, i32, i32, i32, i32, P, P, dbl, P]
+    lib.oracle_attention_backward.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, dbl, i32, P, P, P, P]
     return lib
 
 
@@ -198,3 +200,25 @@ class Oracle:
         self.lib.oracle_attention(_ptr(lay), H, nb, B, Z, D, _ptr(Q), _ptr(K), _ptr(V),
                                   float(scale), int(kind), _ptr(m), ns, _ptr(s), _ptr(out))
         return out.reshape(Z, H, S, D) if sel is None else out
+
+    def softmax_backward(self, layout, B, Y, dY, scale):
+        """Softmax backward in the block format: Y (the forward's output) and
+        dY [Z, nnz, B, B] -> dX [Z, nnz, B, B]."""
+        lay, Y, dY = _u8(layout), _f32(Y), _f32(dY)
+        H, nb = lay.shape[0], lay.shape[1]
+        out = np.zeros(Y.shape, dtype=np.float64)
+        self.lib.oracle_softmax_backward(_ptr(lay), H, nb, B, Y.shape[0], _ptr(Y), _ptr(dY), float(scale),
+                                         _ptr(out))
+        return out
+
+    def attention_backward(self, layout, B, Q, K, V, dO, scale, kind=MASK_NONE, mask=None):
+        """Gradients (dQ, dK, dV) [Z, H, S, D] of block-sparse attention for
+        the output gradient dO.  Dense S x S work per (z, h): small sizes."""
+        lay, Q, K, V, dO = _u8(layout), _f32(Q), _f32(K), _f32(V), _f32(dO)
+        m = None if mask is None else _u8(mask)
+        H, nb = lay.shape[0], lay.shape[1]
+        Z, D = Q.shape[0], Q.shape[3]
+        outs = [np.zeros(Q.shape, dtype=np.float64) for _ in range(3)]
+        self.lib.oracle_attention_backward(_ptr(lay), H, nb, B, Z, D, _ptr(Q), _ptr(K), _ptr(V), _ptr(dO),
+                                           float(scale), int(kind), _ptr(m), *[_ptr(o) for o in outs])
+        return tuple(outs)

@@ -399,3 +399,113 @@ void oracle_attention(const uint8_t* layout, int H, int nb, int B, int Z, int D,
     }
     (void)Z;
 }
+
+/* ---------------------------------------------------------------------- */
+/* backward  [next row: dV = P^T dO, dP = dO V^T, softmax backward,        */
+/*            dQ / dK from dS]; the chain rule applied to the definitions  */
+/*            above, written out without reuse of the forward code paths   */
+/* ---------------------------------------------------------------------- */
+/* Softmax backward in the block format.  Y = softmax rows (the forward's
+ * output, 0 at masked entries and outside the layout), dY its gradient; for
+ * y = softmax(scale * x) over the kept set R of a row,
+ *     dx_c = scale * y_c * (dy_c - sum_{c' in R} y_c' dy_c').
+ * Entries with y_c = 0 (masked) get dx_c = 0. */
+void oracle_softmax_backward(const uint8_t* layout, int H, int nb, int B, int Z,
+                             const float* Y, const float* dY, double scale, double* dX) {
+    const int64_t S = (int64_t)nb * B;
+    const int64_t nnz = oracle_count_nnz(layout, H, nb);
+    int64_t* ids = block_ids(layout, H, nb);
+    #pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t u = 0; u < (int64_t)Z * H * S; ++u) {
+        int64_t r = u % S, zh = u / S, z = zh / H;
+        int h = (int)(zh % H);
+        int64_t i = r / B, a = r % B;
+        double dot = 0.0;
+        for (int j = 0; j < nb; ++j) {
+            int64_t id = ids[((int64_t)h * nb + i) * nb + j];
+            if (id < 0) continue;
+            const int64_t off = ((int64_t)z * nnz + id) * B * B + a * B;
+            for (int b = 0; b < B; ++b) dot += (double)Y[off + b] * (double)dY[off + b];
+        }
+        for (int j = 0; j < nb; ++j) {
+            int64_t id = ids[((int64_t)h * nb + i) * nb + j];
+            if (id < 0) continue;
+            const int64_t off = ((int64_t)z * nnz + id) * B * B + a * B;
+            for (int b = 0; b < B; ++b)
+                dX[off + b] = scale * (double)Y[off + b] * ((double)dY[off + b] - dot);
+        }
+    }
+    free(ids);
+}
+
+/* Attention backward from the dense-mask definition.  Given dO = dL/dO for
+ * O = softmax_R(scale Q K^T) V (rows of R empty -> O row 0), returns
+ *     dV = P^T dO,  dP = dO V^T,  dS = P .* (dP - rowsum(P .* dP)),
+ *     dQ = scale dS K,  dK = scale dS^T Q.
+ * Q, K, V, dO: [Z][H][S][D]; dQ, dK, dV: [Z][H][S][D] (double).  One (z, h)
+ * slice per thread (dK and dV sum over rows); P and dS are dense S x S. */
+void oracle_attention_backward(const uint8_t* layout, int H, int nb, int B, int Z, int D,
+                               const float* Q, const float* K, const float* V, const float* dO,
+                               double scale, int kind, const uint8_t* mask,
+                               double* dQ, double* dK, double* dV) {
+    const int64_t S = (int64_t)nb * B;
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t zh = 0; zh < (int64_t)Z * H; ++zh) {
+        const int h = (int)(zh % H);
+        const float* q = Q + zh * S * D;
+        const float* k = K + zh * S * D;
+        const float* v = V + zh * S * D;
+        const float* go = dO + zh * S * D;
+        double* gq = dQ + zh * S * D;
+        double* gk = dK + zh * S * D;
+        double* gv = dV + zh * S * D;
+        for (int64_t e = 0; e < S * D; ++e) gq[e] = gk[e] = gv[e] = 0.0;
+        double* P = (double*)calloc((size_t)(S * S), sizeof(double));
+        uint8_t* inR = (uint8_t*)malloc((size_t)S);
+        for (int64_t r = 0; r < S; ++r) {
+            double m = -INFINITY;
+            int64_t count = 0;
+            for (int64_t c = 0; c < S; ++c) {
+                const uint8_t present = layout[((int64_t)h * nb + r / B) * nb + c / B];
+                inR[c] = present && keep(kind, mask, S, B, r, c);
+                if (!inR[c]) continue;
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d) dot += (double)q[r * D + d] * (double)k[c * D + d];
+                P[r * S + c] = scale * dot;
+                if (P[r * S + c] > m) m = P[r * S + c];
+                ++count;
+            }
+            if (count == 0) continue;
+            double sum = 0.0;
+            for (int64_t c = 0; c < S; ++c)
+                if (inR[c]) sum += exp(P[r * S + c] - m);
+            for (int64_t c = 0; c < S; ++c)
+                P[r * S + c] = inR[c] ? exp(P[r * S + c] - m) / sum : 0.0;
+        }
+        for (int64_t r = 0; r < S; ++r) {
+            /* dP_rc = dO_r . V_c over the support of P's row; delta_r */
+            double delta = 0.0;
+            for (int64_t c = 0; c < S; ++c) {
+                const double p = P[r * S + c];
+                if (p == 0.0) continue;
+                double dp = 0.0;
+                for (int d = 0; d < D; ++d) dp += (double)go[r * D + d] * (double)v[c * D + d];
+                delta += p * dp;
+            }
+            for (int64_t c = 0; c < S; ++c) {
+                const double p = P[r * S + c];
+                if (p == 0.0) continue;
+                double dp = 0.0;
+                for (int d = 0; d < D; ++d) dp += (double)go[r * D + d] * (double)v[c * D + d];
+                const double ds = p * (dp - delta);
+                for (int d = 0; d < D; ++d) {
+                    gv[c * D + d] += p * (double)go[r * D + d];
+                    gq[r * D + d] += scale * ds * (double)k[c * D + d];
+                    gk[c * D + d] += scale * ds * (double)q[r * D + d];
+                }
+            }
+        }
+        free(P);
+        free(inR);
+    }
+}

@@ -44,6 +44,17 @@ MUTANTS = {
     "attention_dropped_scale": ("sc[c] = scale * dot;", "sc[c] = dot;"),
     "csc_wrong_row": ("if (id >= 0) { row_idx[q] = i;", "if (id >= 0) { row_idx[q] = j;"),
     "sdd_wrong_block_row": ("int64_t r = (int64_t)bi[id] * B + a;", "int64_t r = (int64_t)bj[id] * B + a;"),
+    "softmax_bwd_no_delta": ("dX[off + b] = scale * (double)Y[off + b] * ((double)dY[off + b] - dot);",
+                             "dX[off + b] = scale * (double)Y[off + b] * ((double)dY[off + b]);"),
+    "softmax_bwd_no_scale": ("dX[off + b] = scale * (double)Y[off + b] * ((double)dY[off + b] - dot);",
+                             "dX[off + b] = (double)Y[off + b] * ((double)dY[off + b] - dot);"),
+    "attention_bwd_dk_wrong_operand": ("gk[c * D + d] += scale * ds * (double)q[r * D + d];",
+                                       "gk[c * D + d] += scale * ds * (double)k[c * D + d];"),
+    "attention_bwd_dv_uses_ds": ("gv[c * D + d] += p * (double)go[r * D + d];",
+                                 "gv[c * D + d] += ds * (double)go[r * D + d];"),
+    "attention_bwd_unweighted_delta": ("delta += p * dp;", "delta += dp;"),
+    "attention_bwd_transposed_layout": ("const uint8_t present = layout[((int64_t)h * nb + r / B) * nb + c / B];",
+                                        "const uint8_t present = layout[((int64_t)h * nb + c / B) * nb + r / B];"),
 }
 
 

@@ -321,3 +321,100 @@ def test_attention_selection_matches_full(oracle):
     full = oracle.attention(lay, B, Q, K, V, 0.5)
     sel = np.array([3, S + 5, 3 * S + 31])
     np.testing.assert_array_equal(oracle.attention(lay, B, Q, K, V, 0.5, sel=sel), full.reshape(-1, D)[sel])
+
+
+# ------------------------------------------------------------ backward ----
+# The backward functions follow the chain rule applied to the forward
+# definitions; they are pinned to the oracle's own forward by central finite
+# differences (inputs on a 2^-6 grid, steps of 2^-10: exact in fp32), to
+# closed forms, and to the composition of the other oracle functions.
+
+def grid(*shape, seed=0, lo=-2.0, hi=2.0):
+    x = np.random.default_rng(seed).uniform(lo, hi, shape)
+    return (np.round(x * 64) / 64).astype(np.float32)
+
+
+def _fd(f, x, eps=2.0 ** -10):
+    """Central differences of the scalar f at every element of x (float32)."""
+    g = np.zeros(x.shape, np.float64)
+    flat, gf = x.reshape(-1), g.reshape(-1)
+    for e in range(flat.size):
+        keep = flat[e]
+        flat[e] = keep + eps
+        fp = f(x)
+        flat[e] = keep - eps
+        fm = f(x)
+        flat[e] = keep
+        gf[e] = (fp - fm) / (2 * eps)
+    return g
+
+
+@pytest.mark.parametrize("kind", [W.MASK_NONE, W.MASK_DENSE, W.MASK_DIAG_CAUSAL])
+def test_softmax_backward_matches_finite_differences(oracle, kind):
+    Z, H, nb, B, scale = 1, 2, 3, 4, 0.7
+    lay = random_layout(H, nb, 0.6, 21)
+    lay[1, 0, 0] = 1
+    nnz = int(lay.sum())
+    X = grid(Z, nnz, B, B, seed=22)
+    dY = grid(Z, nnz, B, B, seed=23)
+    mask = (np.random.default_rng(24).random((nb * B, nb * B)) < 0.8).astype(np.uint8) if kind == W.MASK_DENSE else None
+    f = lambda x: float(np.sum(oracle.softmax(lay, B, x, scale, kind, mask) * dY))
+    want = _fd(f, X)
+    Y = oracle.softmax(lay, B, X, scale, kind, mask)
+    got = oracle.softmax_backward(lay, B, Y, dY, scale)
+    np.testing.assert_allclose(got, want, rtol=1e-4, atol=2e-6)
+
+
+def test_softmax_backward_constant_gradient_is_zero(oracle):
+    # sum_c y_c = 1 on every non-empty row, so a constant dY has no effect
+    lay = random_layout(2, 4, 0.5, 25)
+    nnz = int(lay.sum())
+    Y = oracle.softmax(lay, 8, grid(2, nnz, 8, 8, seed=26), 0.5)
+    got = oracle.softmax_backward(lay, 8, Y, np.full(Y.shape, 3.25, np.float32), 0.5)
+    np.testing.assert_allclose(got, 0.0, atol=1e-6)
+
+
+@pytest.mark.parametrize("kind", [W.MASK_NONE, W.MASK_DENSE, W.MASK_DIAG_CAUSAL])
+def test_attention_backward_matches_finite_differences(oracle, kind):
+    Z, H, nb, B, D, scale = 1, 1, 3, 4, 4, 0.6
+    S = nb * B
+    lay = np.array([[[1, 0, 1], [0, 0, 0], [1, 1, 1]]], np.uint8)  # block-row 1 empty
+    Q, K, V = grid(Z, H, S, D, seed=31), grid(Z, H, S, D, seed=32), grid(Z, H, S, D, seed=33)
+    G = grid(Z, H, S, D, seed=34)
+    mask = (np.random.default_rng(35).random((S, S)) < 0.7).astype(np.uint8) if kind == W.MASK_DENSE else None
+    dQ, dK, dV = oracle.attention_backward(lay, B, Q, K, V, G, scale, kind, mask)
+    loss = lambda q, k, v: float(np.sum(oracle.attention(lay, B, q, k, v, scale, kind, mask) * G))
+    np.testing.assert_allclose(dQ, _fd(lambda x: loss(x, K, V), Q.copy()), rtol=1e-4, atol=2e-6)
+    np.testing.assert_allclose(dK, _fd(lambda x: loss(Q, x, V), K.copy()), rtol=1e-4, atol=2e-6)
+    np.testing.assert_allclose(dV, _fd(lambda x: loss(Q, K, x), V.copy()), rtol=1e-4, atol=2e-6)
+    # the empty block-row has no gradient into Q
+    assert np.all(dQ[0, 0, B:2 * B] == 0)
+
+
+def test_attention_backward_constant_values_give_no_score_gradient(oracle):
+    # V constant over keys: O does not depend on the scores, so dQ = dK = 0
+    Z, H, nb, B, D = 1, 2, 4, 8, 8
+    S = nb * B
+    lay = random_layout(H, nb, 0.5, 36)
+    Q, K = grid(Z, H, S, D, seed=37), grid(Z, H, S, D, seed=38)
+    V = np.broadcast_to(grid(Z, H, 1, D, seed=39), (Z, H, S, D)).copy()
+    dQ, dK, _ = oracle.attention_backward(lay, B, Q, K, V, grid(Z, H, S, D, seed=40), 0.4)
+    np.testing.assert_allclose(dQ, 0.0, atol=1e-9)
+    np.testing.assert_allclose(dK, 0.0, atol=1e-9)
+
+
+@pytest.mark.parametrize("kind", [W.MASK_NONE, W.MASK_DIAG_CAUSAL])
+def test_attention_backward_equals_unfused_chain(oracle, kind):
+    # dV = DSD(P^T, dO), dS = softmax_backward(P, SDD(dO, V)), dQ = DSD(dS, K),
+    # dK = DSD(dS^T, Q) with P = softmax(SDD(Q, K)): other oracle functions
+    Z, H, nb, B, D, scale = 2, 2, 4, 8, 16, 0.25
+    lay = random_layout(H, nb, 0.5, 41)
+    S = nb * B
+    Q, K, V, G = (grid(Z, H, S, D, seed=s) for s in (42, 43, 44, 45))
+    P = oracle.softmax(lay, B, oracle.sdd(lay, B, Q, K), scale, kind)
+    dS = oracle.softmax_backward(lay, B, P, oracle.sdd(lay, B, G, V), scale)
+    dQ, dK, dV = oracle.attention_backward(lay, B, Q, K, V, G, scale, kind)
+    # P and dS pass through fp32 between the chain's steps
+    np.testing.assert_allclose(dV, oracle.dsd(lay, B, P, G, trans_a=1), rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(dQ, oracle.dsd(lay, B, dS, K), rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(dK, oracle.dsd(lay, B, dS, Q, trans_a=1), rtol=1e-5, atol=1e-6)
