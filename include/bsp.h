@@ -201,6 +201,32 @@ int bsp_attention(bsp_layout_t layout, int dtype, const void* Q, const void* K, 
                   void* O, int Z, int D, float scale, int mask_kind, const uint8_t* mask,
                   void* stream);
 
+/* ---- backward ---------------------------------------------------------- */
+
+/* Backward of bsp_softmax.  Y: the forward's output (0 at masked entries),
+ * dY: the gradient of Y; writes the gradient of X,
+ *     dX = scale * Y .* (dY - rowsum(Y .* dY))   (row sums over the row's blocks),
+ * which is 0 wherever Y is 0.  Y, dY, dX: DEVICE [Z][nnz][block][block];
+ * dX may equal dY (in place).  scale > 0 and finite, as in the forward.  The
+ * pages state no backward; this is the chain rule applied to the softmax
+ * they define. */
+int bsp_softmax_backward(bsp_layout_t layout, int dtype, const void* Y, const void* dY, void* dX, int Z,
+                         float scale, void* stream);
+
+/* Gradients of bsp_attention for the output gradient dO, as the unfused chain
+ *     P = softmax(scale Q K^T on the layout and mask)   (recomputed)
+ *     dV = P^T dO,  dP = dO V^T (on the layout),  dX = bsp_softmax_backward(P, dP),
+ *     dQ = dX K,  dK = dX^T Q
+ * of this library's SDD, softmax, softmax backward and DSD calls, enqueued on
+ * `stream`.  Q, K, V, dO, dQ, dK, dV: DEVICE [Z][H][S][D], D and the mask as for
+ * bsp_attention.  P_ws, dP_ws: caller-owned DEVICE workspace of Z * nnz *
+ * block * block elements each (P and dP / dX live there afterwards); they may
+ * be NULL when the layout has no block, in which case dQ, dK, dV are zeroed.
+ * The pages state no backward (the chain rule on their definitions). */
+int bsp_attention_backward(bsp_layout_t layout, int dtype, const void* Q, const void* K, const void* V,
+                           const void* dO, void* dQ, void* dK, void* dV, int Z, int D, float scale,
+                           int mask_kind, const uint8_t* mask, void* P_ws, void* dP_ws, void* stream);
+
 /* ---- diagnostics ------------------------------------------------------- */
 
 /* Evaluate, on n DEVICE floats x, the software 2^x that the attention softmax

@@ -58,13 +58,17 @@ def lib():
         L.bsp_dds.argtypes = [P, i32, P, P, P, i32, i32, i32, i32, P]
         L.bsp_softmax.argtypes = [P, i32, P, P, i32, f32, i32, P, P]
         L.bsp_attention.argtypes = [P, i32, P, P, P, P, i32, i32, f32, i32, P, P]
+        L.bsp_softmax_backward.argtypes = [P, i32, P, P, P, i32, f32, P]
+        L.bsp_attention_backward.argtypes = [P, i32, P, P, P, P, P, P, P, i32, i32, f32, i32, P, P, P, P]
+        L.bsp_layout_groups.argtypes = [P, i32, P, P, P, P, P, P, P]
         L.bsp_status_check.argtypes = [P, P]
         L.bsp_status_string.restype = ctypes.c_char_p
         L.bsp_status_string.argtypes = [i32]
         L.bsp_version.restype = ctypes.c_char_p
         for name in ("bsp_layout_plan", "bsp_layout_compile", "bsp_layout_destroy", "bsp_layout_info",
                      "bsp_layout_get_luts", "bsp_layout_tiles", "bsp_sdd", "bsp_dsd", "bsp_dds", "bsp_softmax",
-                     "bsp_attention", "bsp_status_check"):
+                     "bsp_attention", "bsp_softmax_backward", "bsp_attention_backward", "bsp_layout_groups",
+                     "bsp_status_check"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -259,3 +263,54 @@ def attention_unfused(L: Layout, Q, K, V, scale: float, mask_kind: int = MASK_NO
     P = bsp_sdd(L, Q, K, trans_a=0, trans_b=1, stream=stream)
     bsp_softmax(L, P, P, scale, mask_kind, mask, stream=stream)
     return bsp_dsd(L, P, V, stream=stream)
+
+
+# --------------------------------------------------------------- backward --
+
+def bsp_softmax_backward(L: Layout, Y, dY, dX=None, scale: float = 1.0, stream=None):
+    """Gradient of the softmax input: scale * Y * (dY - rowsum(Y * dY)).
+    dX = dY for in place."""
+    if dX is None:
+        dX = torch.empty_like(dY)
+    dt = _dtype(Y, dY, dX)
+    _check(lib().bsp_softmax_backward(L.handle, dt, _ptr(Y), _ptr(dY), _ptr(dX), Y.shape[0], float(scale),
+                                      _stream(stream)), "bsp_softmax_backward")
+    return dX
+
+
+def attention_backward(L: Layout, Q, K, V, dO, scale: float, mask_kind: int = MASK_NONE, mask=None,
+                       stream=None):
+    """(dQ, dK, dV) of block-sparse attention for the output gradient dO.
+    Allocates the two [Z, nnz, B, B] workspaces the C call takes."""
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    ws = (Q.shape[0], max(L.nnz, 1), L.B, L.B)
+    P_ws = torch.empty(ws, dtype=Q.dtype, device=Q.device) if L.nnz else None
+    dP_ws = torch.empty(ws, dtype=Q.dtype, device=Q.device) if L.nnz else None
+    dt = _dtype(Q, K, V, dO, dQ, dK, dV)
+    _check(lib().bsp_attention_backward(L.handle, dt, _ptr(Q), _ptr(K), _ptr(V), _ptr(dO), _ptr(dQ), _ptr(dK),
+                                        _ptr(dV), Q.shape[0], Q.shape[3], float(scale), int(mask_kind),
+                                        _ptr(mask), _ptr(P_ws), _ptr(dP_ws), _stream(stream)),
+           "bsp_attention_backward")
+    return dQ, dK, dV
+
+
+class _BlockSparseAttention(torch.autograd.Function):
+    """Fused forward (bsp_attention); backward through bsp_attention_backward."""
+
+    @staticmethod
+    def forward(ctx, Q, K, V, L, scale, mask_kind, mask):
+        Q, K, V = Q.contiguous(), K.contiguous(), V.contiguous()
+        ctx.save_for_backward(Q, K, V)
+        ctx.L, ctx.scale, ctx.mask_kind, ctx.mask = L, scale, mask_kind, mask
+        return bsp_attention(L, Q, K, V, None, scale, mask_kind, mask)
+
+    @staticmethod
+    def backward(ctx, dO):
+        Q, K, V = ctx.saved_tensors
+        dQ, dK, dV = attention_backward(ctx.L, Q, K, V, dO.contiguous(), ctx.scale, ctx.mask_kind, ctx.mask)
+        return dQ, dK, dV, None, None, None, None
+
+
+def block_sparse_attention(L: Layout, Q, K, V, scale: float, mask_kind: int = MASK_NONE, mask=None):
+    """Differentiable block-sparse attention (torch autograd) on a compiled layout."""
+    return _BlockSparseAttention.apply(Q, K, V, L, float(scale), int(mask_kind), mask)

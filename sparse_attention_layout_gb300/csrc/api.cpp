@@ -160,3 +160,45 @@ extern "C" const char* bsp_status_string(int status) {
 }
 
 extern "C" const char* bsp_version(void) { return "libbsp 0.1 (sm_103a)"; }
+
+extern "C" int bsp_softmax_backward(bsp_layout_t L, int dtype, const void* Y, const void* dY, void* dX, int Z,
+                                    float scale, void* stream) {
+    int rc = check_common(L, dtype, Z, {Y, dY, dX});
+    if (rc) return rc;
+    if (!(scale > 0.f) || scale > 3.0e38f) return BSP_ERR_INVALID_ARG;
+    if (Z == 0 || L->nnz == 0) return BSP_OK;
+    return bsp::launch_softmax_backward(L, dtype, Y, dY, dX, Z, scale, (cudaStream_t)stream);
+}
+
+extern "C" int bsp_attention_backward(bsp_layout_t L, int dtype, const void* Q, const void* K, const void* V,
+                                      const void* dO, void* dQ, void* dK, void* dV, int Z, int D, float scale,
+                                      int mask_kind, const uint8_t* mask, void* P_ws, void* dP_ws,
+                                      void* stream) {
+    int rc = check_common(L, dtype, Z, {Q, K, V, dO, dQ, dK, dV});
+    if (rc) return rc;
+    if (D < 16 || D > 128 || D % 16 || !valid_kind(mask_kind) || !(scale > 0.f) || scale > 3.0e38f)
+        return BSP_ERR_INVALID_ARG;
+    if (mask_kind == BSP_MASK_DENSE && !mask) return BSP_ERR_INVALID_ARG;
+    if (mask_kind == BSP_MASK_DENSE && ((uintptr_t)mask & 15u)) return BSP_ERR_ALIGNMENT;
+    if (Z == 0) return BSP_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (L->nnz == 0) {  // nothing attends to anything: every gradient is 0
+        const size_t bytes = (size_t)Z * L->H * L->S * D * (dtype == BSP_F32 ? 4 : 2);
+        for (void* p : {dQ, dK, dV})
+            if (cudaMemsetAsync(p, 0, bytes, s) != cudaSuccess) return BSP_ERR_CUDA;
+        return BSP_OK;
+    }
+    if (!P_ws || !dP_ws) return BSP_ERR_INVALID_ARG;
+    if (!aligned16(P_ws) || !aligned16(dP_ws)) return BSP_ERR_ALIGNMENT;
+    // P = softmax(scale Q K^T) on the layout, as the forward computes it
+    if ((rc = bsp_sdd(L, dtype, Q, K, P_ws, Z, D, 0, 1, stream))) return rc;
+    if ((rc = bsp_softmax(L, dtype, P_ws, P_ws, Z, scale, mask_kind, mask, stream))) return rc;
+    // dV = P^T dO
+    if ((rc = bsp_dsd(L, dtype, P_ws, dO, dV, Z, D, 1, 0, stream))) return rc;
+    // dP = dO V^T on the layout, then the gradient of the raw scores Q K^T in place
+    if ((rc = bsp_sdd(L, dtype, dO, V, dP_ws, Z, D, 0, 1, stream))) return rc;
+    if ((rc = bsp_softmax_backward(L, dtype, P_ws, dP_ws, dP_ws, Z, scale, stream))) return rc;
+    // dQ = dX K,  dK = dX^T Q
+    if ((rc = bsp_dsd(L, dtype, dP_ws, K, dQ, Z, D, 0, 0, stream))) return rc;
+    return bsp_dsd(L, dtype, dP_ws, Q, dK, Z, D, 1, 0, stream);
+}

@@ -99,6 +99,10 @@ int launch_dsd_group_tc(const bsp_layout_s* L, int dtype, const void* A, const v
 int launch_dds_group_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z,
                         int M, int ta, int tb, cudaStream_t s);
 
+// backward of the block-sparse softmax (CUDA cores; HBM-bound)
+int launch_softmax_backward(const bsp_layout_s* L, int dtype, const void* Y, const void* dY, void* dX, int Z,
+                            float scale, cudaStream_t s);
+
 int sm_count();  // multiprocessors of the current device (cached per device)
 
 }  // namespace bsp

@@ -1,0 +1,115 @@
+// Backward of the block-sparse row softmax: with Y = softmax(scale X) over the
+// kept entries of each row ("question on blocksparse", openai/triton issue
+// 117: the softmax of the SDD output across the row's blocks) and dY the
+// gradient of Y, the gradient of X is
+//     dX = scale * Y .* (dY - rowsum(Y .* dY)),
+// which is 0 wherever Y is 0 (masked entries, rows with nothing kept).
+//
+// One warp per query row.  A row is nnz_i segments of B contiguous elements
+// (row a of each of its block-row's blocks; the blocks of a block-row are
+// consecutive in storage).  Pass 1 reads the row's Y and dY with 16-byte
+// loads and reduces the dot product; pass 2 reads them again (from L2: the
+// row was just read) and writes dX.  A lane touches the same 16-byte chunks in
+// both passes, so dX may alias dY.  HBM-bound: 2 reads and 1 write of
+// Z * nnz * B^2 elements.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace bsp {
+namespace {
+
+constexpr int kBwdThreads = 256;
+
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4& v, float (&f)[16 / sizeof(T)]) {
+    const T* p = reinterpret_cast<const T*>(&v);
+#pragma unroll
+    for (int k = 0; k < (int)(16 / sizeof(T)); ++k) f[k] = to_f32(p[k]);
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 pack16(const float (&f)[16 / sizeof(T)]) {
+    uint4 v;
+    T* p = reinterpret_cast<T*>(&v);
+#pragma unroll
+    for (int k = 0; k < (int)(16 / sizeof(T)); ++k) p[k] = from_f32<T>(f[k]);
+    return v;
+}
+
+template <typename T, int BLK>
+__global__ void __launch_bounds__(kBwdThreads)
+softmax_bwd_kernel(LayoutView L, const T* __restrict__ Y, const T* dY, T* dX, int Z, float scale) {
+    constexpr int E = 16 / sizeof(T);           // elements per 16-byte chunk
+    constexpr int CH = BLK * (int)sizeof(T) / 16;  // chunks per row segment
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = (int64_t)Z * L.H * L.nb * BLK;
+    const int64_t nwarps = (int64_t)gridDim.x * (kBwdThreads / 32);
+    for (int64_t row = ((int64_t)blockIdx.x * kBwdThreads + threadIdx.x) / 32; row < rows; row += nwarps) {
+        const int a = (int)(row % BLK);
+        const int64_t rest = row / BLK;
+        const int key = (int)(rest % ((int64_t)L.H * L.nb));
+        const int64_t z = rest / ((int64_t)L.H * L.nb);
+        const int h = key / L.nb, i = key % L.nb;
+        const int p0 = L.row_ptr[h * (L.nb + 1) + i];
+        const int nq = L.row_ptr[h * (L.nb + 1) + i + 1] - p0;
+        if (nq == 0) continue;
+        const int64_t base = (((int64_t)z * L.nnz + p0) * BLK + a) * BLK;  // element offset of segment 0
+        auto off = [&](int c) { return base + (int64_t)(c / CH) * BLK * BLK + (int64_t)(c % CH) * E; };
+        float dot = 0.f;
+        for (int c = lane; c < nq * CH; c += 32) {
+            float y[E], g[E];
+            unpack16<T>(*reinterpret_cast<const uint4*>(Y + off(c)), y);
+            unpack16<T>(*reinterpret_cast<const uint4*>(dY + off(c)), g);
+#pragma unroll
+            for (int k = 0; k < E; ++k) dot = fmaf(y[k], g[k], dot);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        for (int c = lane; c < nq * CH; c += 32) {
+            float y[E], g[E], x[E];
+            unpack16<T>(*reinterpret_cast<const uint4*>(Y + off(c)), y);
+            unpack16<T>(*reinterpret_cast<const uint4*>(dY + off(c)), g);
+#pragma unroll
+            for (int k = 0; k < E; ++k) x[k] = scale * y[k] * (g[k] - dot);
+            *reinterpret_cast<uint4*>(dX + off(c)) = pack16<T>(x);
+        }
+    }
+}
+
+template <typename T, int BLK>
+int bwd_launch(const bsp_layout_s* L, const void* Y, const void* dY, void* dX, int Z, float scale,
+               cudaStream_t s) {
+    const int64_t rows = (int64_t)Z * L->H * L->nb * BLK;
+    const int64_t blocks = std::min<int64_t>((rows + 7) / 8, (int64_t)sm_count() * 16);
+    softmax_bwd_kernel<T, BLK><<<(unsigned)std::max<int64_t>(blocks, 1), kBwdThreads, 0, s>>>(
+        L->view, (const T*)Y, (const T*)dY, (T*)dX, Z, scale);
+    return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
+}
+
+template <typename T>
+int bwd_t(const bsp_layout_s* L, const void* Y, const void* dY, void* dX, int Z, float scale, cudaStream_t s) {
+    switch (L->B) {
+        case 16: return bwd_launch<T, 16>(L, Y, dY, dX, Z, scale, s);
+        case 32: return bwd_launch<T, 32>(L, Y, dY, dX, Z, scale, s);
+        case 64: return bwd_launch<T, 64>(L, Y, dY, dX, Z, scale, s);
+        case 128: return bwd_launch<T, 128>(L, Y, dY, dX, Z, scale, s);
+        default: return BSP_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace
+
+int launch_softmax_backward(const bsp_layout_s* L, int dtype, const void* Y, const void* dY, void* dX, int Z,
+                            float scale, cudaStream_t s) {
+    switch (dtype) {
+        case BSP_F32: return bwd_t<float>(L, Y, dY, dX, Z, scale, s);
+        case BSP_BF16: return bwd_t<__nv_bfloat16>(L, Y, dY, dX, Z, scale, s);
+        case BSP_F16: return bwd_t<__half>(L, Y, dY, dX, Z, scale, s);
+        default: return BSP_ERR_INVALID_ARG;
+    }
+}
+
+}  // namespace bsp

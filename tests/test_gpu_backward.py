@@ -1,0 +1,132 @@
+"""GPU parity of the backward pass through the C ABI against the fp64 oracle:
+the block-sparse softmax backward (every block size and dtype, in place and
+not), the attention backward (dQ, dK, dV; block sizes, dtypes, head sizes,
+mask kinds, tensor-core and CUDA-core paths of the forward ops it chains) and
+the torch autograd wrapper.
+
+Tolerance (normwise): 1e-5 for fp32 outputs; 2e-2 for bf16 / fp16 softmax
+backward outputs and 3e-2 for bf16 / fp16 attention gradients, whose chain
+rounds four intermediates (P, dP, dX and the output) to the 16-bit type
+(each a relative 2^-9 for bf16) and subtracts a row mean from dP."""
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import TOL, dev, normwise_err, to_np
+from sparse_attention_layout_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+GRAD_TOL = {torch.float32: 1e-5, torch.bfloat16: 3e-2, torch.float16: 3e-2}
+
+
+@pytest.fixture(scope="module")
+def bsp():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from sparse_attention_layout_gb300 import build
+    build.build()
+    from sparse_attention_layout_gb300 import bsp as m
+    return m
+
+
+@pytest.fixture(params=["tc", "simt"])
+def path(request, monkeypatch):
+    if request.param == "simt":
+        monkeypatch.setenv("BSP_FORCE_SIMT", "1")
+    else:
+        monkeypatch.delenv("BSP_FORCE_SIMT", raising=False)
+    return request.param
+
+
+def rlayout(H, nb, p, seed):
+    lay = (np.random.default_rng(seed).random((H, nb, nb)) < p).astype(np.uint8)
+    lay[:, np.arange(nb), np.arange(nb)] = 1
+    if nb > 3:
+        lay[0, 2, :] = 0   # an empty block-row
+    return lay
+
+
+def randn(shape, dtype, seed):
+    return W.randn(shape, {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}[dtype], seed)
+
+
+def check(got, want, tol, what):
+    err = normwise_err(to_np(got), want)
+    assert err <= tol, f"{what}: normwise error {err:.3e} > {tol:.0e}"
+
+
+@pytest.mark.parametrize("B", [16, 32, 64, 128])
+@pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("in_place", [False, True])
+def test_softmax_backward(bsp, oracle, B, dt, in_place):
+    dtype = DTYPES[dt]
+    Z, H, scale = 2, 2, 0.3
+    nb = max(3, 512 // B)
+    lay = rlayout(H, nb, 0.3, 60 + B)
+    L = bsp.bsp_layout_compile(lay, B)
+    # Y: a softmax output (rows sum to 1, zeros at masked entries)
+    Y = bsp.bsp_softmax(L, dev(randn((Z, L.nnz, B, B), dtype, 61)), None, 0.5, W.MASK_DIAG_CAUSAL)
+    dY = dev(randn((Z, L.nnz, B, B), dtype, 62))
+    want = oracle.softmax_backward(lay, B, Y, dY, scale)
+    got = bsp.bsp_softmax_backward(L, Y, dY, dY if in_place else None, scale)
+    torch.cuda.synchronize()
+    check(got, want, TOL[dtype], f"softmax backward B={B} {dt} in_place={in_place}")
+
+
+@pytest.mark.parametrize("B", [16, 32, 64, 128])
+@pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("kind", [0, 1, 2])
+def test_attention_backward(bsp, oracle, path, B, dt, D, kind):
+    dtype = DTYPES[dt]
+    Z, H, scale = 2, 2, 1.0 / np.sqrt(D)
+    nb = max(4, 384 // B)  # >= 4: block-row 2 is empty
+    S = nb * B
+    lay = rlayout(H, nb, 0.4, 70 + B)
+    L = bsp.bsp_layout_compile(lay, B)
+    Q, K, V, G = (randn((Z, H, S, D), dtype, s) for s in (71, 72, 73, 74))
+    mask = W.random_mask(S, 0.7, 75) if kind == W.MASK_DENSE else None
+    dmask = None if mask is None else torch.from_numpy(mask).cuda()
+    dQ, dK, dV = bsp.attention_backward(L, dev(Q), dev(K), dev(V), dev(G), scale, kind, dmask)
+    torch.cuda.synchronize()
+    wQ, wK, wV = oracle.attention_backward(lay, B, Q, K, V, G, scale, kind, mask)
+    tol = GRAD_TOL[dtype]
+    check(dV, wV, tol, f"dV B={B} {dt} D={D} kind={kind} {path}")
+    check(dQ, wQ, tol, f"dQ B={B} {dt} D={D} kind={kind} {path}")
+    check(dK, wK, tol, f"dK B={B} {dt} D={D} kind={kind} {path}")
+    # the empty block-row gets no query gradient
+    assert (dQ[0, 0, 2 * B:3 * B] == 0).all()
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_autograd_wrapper(bsp, oracle, dt):
+    dtype = DTYPES[dt]
+    Z, H, B, D, scale = 1, 3, 64, 64, 0.125
+    nb = 6
+    S = nb * B
+    lay = W.layout_strided_causal(nb, local_blocks=2, stride=3, H=H)
+    L = bsp.bsp_layout_compile(lay, B)
+    Q, K, V, G = (randn((Z, H, S, D), dtype, s) for s in (81, 82, 83, 84))
+    q, k, v = (dev(t).requires_grad_() for t in (Q, K, V))
+    out = bsp.block_sparse_attention(L, q, k, v, scale, W.MASK_DIAG_CAUSAL)
+    out.backward(dev(G))
+    torch.cuda.synchronize()
+    check(out, oracle.attention(lay, B, Q, K, V, scale, W.MASK_DIAG_CAUSAL), TOL[dtype], f"autograd forward {dt}")
+    wQ, wK, wV = oracle.attention_backward(lay, B, Q, K, V, G, scale, W.MASK_DIAG_CAUSAL)
+    for got, want, name in ((q.grad, wQ, "dQ"), (k.grad, wK, "dK"), (v.grad, wV, "dV")):
+        check(got, want, GRAD_TOL[dtype], f"autograd {name} {dt}")
+
+
+def test_backward_empty_layout_and_zero_batch(bsp):
+    lay = np.zeros((2, 4, 4), np.uint8)
+    L = bsp.bsp_layout_compile(lay, 32)
+    Q = torch.randn(1, 2, 128, 64, device="cuda", dtype=torch.bfloat16)
+    dQ, dK, dV = bsp.attention_backward(L, Q, Q, Q, Q, 0.1)
+    torch.cuda.synchronize()
+    assert all((t == 0).all() for t in (dQ, dK, dV))
+    E = torch.empty(0, 2, 128, 64, device="cuda", dtype=torch.bfloat16)
+    dQ, dK, dV = bsp.attention_backward(bsp.bsp_layout_compile(np.ones((2, 4, 4), np.uint8), 32), E, E, E, E, 0.1)
+    assert dQ.shape == E.shape
