@@ -298,7 +298,20 @@ def per_op_section(w, lay, L, q, k, v, pk, bsp, stream):
     out["dsd"] = {"ms": ms, "TFLOP/s": 2.0 * B * B * D * nnz * Z / ms / 1e9}
     ms = time_launches(lambda: bsp.attention_unfused(L, q, k, v, w.scale, w.mask_kind), 5, stream)
     out["attention_unfused_chain"] = {"ms": ms, "TFLOP/s": nonzero_flops(lay, B, D, Z) / ms / 1e9}
-    del P, X, O
+    # backward: softmax backward on the chain's P, and the whole attention
+    # backward (recomputes P; 5 block matmuls of 2 B^2 D each per block)
+    dY = torch.randn_like(P)
+    dX = torch.empty_like(P)
+    ms = time_launches(lambda: bsp.bsp_softmax_backward(L, P, dY, dX, w.scale), 10, stream)
+    byt = 3.0 * P.numel() * P.element_size()
+    out["softmax_backward"] = {"ms": ms, "GB/s": byt / ms / 1e6, "frac_of_hbm": byt / ms / 1e6 / pk["hbm_gbs"],
+                               "algorithmic_bytes": byt}
+    del dY, dX
+    gO = torch.randn_like(q)
+    ms = time_launches(lambda: bsp.attention_backward(L, q, k, v, gO, w.scale, w.mask_kind), 5, stream)
+    fl = 10.0 * B * B * D * nnz * Z
+    out["attention_backward"] = {"ms": ms, "TFLOP/s": fl / ms / 1e9, "flops_counted": "10 B^2 D per block"}
+    del P, X, O, gO
     # general spMM at 10 % density (8192^2 sparse, 8192x4096 dense, block 32)
     sp = W.SPMM
     lay4 = sp.layout(0.10)

@@ -7,11 +7,11 @@
 //
 // One warp per query row.  A row is nnz_i segments of B contiguous elements
 // (row a of each of its block-row's blocks; the blocks of a block-row are
-// consecutive in storage).  Pass 1 reads the row's Y and dY with 16-byte
-// loads and reduces the dot product; pass 2 reads them again (from L2: the
-// row was just read) and writes dX.  A lane touches the same 16-byte chunks in
-// both passes, so dX may alias dY.  HBM-bound: 2 reads and 1 write of
-// Z * nnz * B^2 elements.
+// consecutive in storage), read with 16-byte loads.  Rows of up to 160 chunks
+// stay in registers (one pass: load, reduce the dot product, write dX); longer
+// rows take two passes, the second re-reading the row.  A lane touches the
+// same chunks for reading and writing, so dX may alias dY.  HBM-bound: 2
+// reads and 1 write of Z * nnz * B^2 elements.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -22,6 +22,10 @@ namespace bsp {
 namespace {
 
 constexpr int kBwdThreads = 256;
+// 16-byte chunks per lane kept in registers (rows up to 160 chunks, e.g. 9 blocks
+// of 128 bf16); few enough registers for 3 blocks of 256 threads per SM, which
+// a memory-bound kernel needs (8 chunks and 1 block per SM ran at 3.8 TB/s)
+constexpr int kRegChunks = 5;
 
 template <typename T>
 __device__ __forceinline__ void unpack16(const uint4& v, float (&f)[16 / sizeof(T)]) {
@@ -40,7 +44,7 @@ __device__ __forceinline__ uint4 pack16(const float (&f)[16 / sizeof(T)]) {
 }
 
 template <typename T, int BLK>
-__global__ void __launch_bounds__(kBwdThreads)
+__global__ void __launch_bounds__(kBwdThreads, 3)
 softmax_bwd_kernel(LayoutView L, const T* __restrict__ Y, const T* dY, T* dX, int Z, float scale) {
     constexpr int E = 16 / sizeof(T);           // elements per 16-byte chunk
     constexpr int CH = BLK * (int)sizeof(T) / 16;  // chunks per row segment
@@ -58,6 +62,46 @@ softmax_bwd_kernel(LayoutView L, const T* __restrict__ Y, const T* dY, T* dX, in
         if (nq == 0) continue;
         const int64_t base = (((int64_t)z * L.nnz + p0) * BLK + a) * BLK;  // element offset of segment 0
         auto off = [&](int c) { return base + (int64_t)(c / CH) * BLK * BLK + (int64_t)(c % CH) * E; };
+        const int nch = nq * CH;
+        if (nch <= 32 * kRegChunks) {
+            // the row fits in registers: one pass, all loads in flight together
+            uint4 yv[kRegChunks], gv[kRegChunks];
+            float dot = 0.f;
+#pragma unroll
+            for (int t = 0; t < kRegChunks; ++t) {
+                const int c = lane + 32 * t;
+                if (c < nch) {
+                    yv[t] = *reinterpret_cast<const uint4*>(Y + off(c));
+                    gv[t] = *reinterpret_cast<const uint4*>(dY + off(c));
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < kRegChunks; ++t) {
+                if (lane + 32 * t < nch) {
+                    float y[E], g[E];
+                    unpack16<T>(yv[t], y);
+                    unpack16<T>(gv[t], g);
+#pragma unroll
+                    for (int k = 0; k < E; ++k) dot = fmaf(y[k], g[k], dot);
+                }
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+#pragma unroll
+            for (int t = 0; t < kRegChunks; ++t) {
+                const int c = lane + 32 * t;
+                if (c < nch) {
+                    float y[E], g[E], x[E];
+                    unpack16<T>(yv[t], y);
+                    unpack16<T>(gv[t], g);
+#pragma unroll
+                    for (int k = 0; k < E; ++k) x[k] = scale * y[k] * (g[k] - dot);
+                    *reinterpret_cast<uint4*>(dX + off(c)) = pack16<T>(x);
+                }
+            }
+            continue;
+        }
+        // long rows: two passes (the second read mostly from L2)
         float dot = 0.f;
         for (int c = lane; c < nq * CH; c += 32) {
             float y[E], g[E];
