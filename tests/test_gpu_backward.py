@@ -130,3 +130,19 @@ def test_backward_empty_layout_and_zero_batch(bsp):
     E = torch.empty(0, 2, 128, 64, device="cuda", dtype=torch.bfloat16)
     dQ, dK, dV = bsp.attention_backward(bsp.bsp_layout_compile(np.ones((2, 4, 4), np.uint8), 32), E, E, E, E, 0.1)
     assert dQ.shape == E.shape
+
+
+@pytest.mark.parametrize("B,dt,nb", [(128, "bf16", 16), (64, "f32", 16), (32, "f16", 48)])
+def test_softmax_backward_long_rows(bsp, oracle, B, dt, nb):
+    """Rows longer than the register-resident limit (160 chunks of 16 bytes)
+    take the two-pass path."""
+    dtype = DTYPES[dt]
+    scale = 0.2
+    lay = np.ones((1, nb, nb), np.uint8)
+    L = bsp.bsp_layout_compile(lay, B)
+    assert nb * B * torch.tensor([], dtype=dtype).element_size() // 16 > 160
+    Y = bsp.bsp_softmax(L, dev(randn((1, L.nnz, B, B), dtype, 91)), None, 0.4)
+    dY = dev(randn((1, L.nnz, B, B), dtype, 92))
+    got = bsp.bsp_softmax_backward(L, Y, dY, None, scale)
+    torch.cuda.synchronize()
+    check(got, oracle.softmax_backward(lay, B, Y, dY, scale), TOL[dtype], f"long rows B={B} {dt}")
