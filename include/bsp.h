@@ -87,6 +87,19 @@ int bsp_layout_plan(const uint8_t* layout, int H, int nb, int block, bsp_layout_
 int bsp_layout_compile(const uint8_t* layout, int H, int nb, int block, void* stream,
                        bsp_layout_t* out);
 
+/* bsp_layout_compile for a layout that is already in DEVICE memory (uint8
+ * [H][nb][nb], values 0/1), e.g. one that changes every step: every table is
+ * built by kernels on `stream` (no host copy of the layout, no host loop over
+ * it).  The call reads back the table sizes once, so it synchronises `stream`,
+ * and makes one allocation of scratch and one for the tables.  The tables
+ * equal bsp_layout_compile's for the same layout, so every compute call
+ * behaves the same; the inspection getters read them from the device.
+ * Values other than 0/1: BSP_ERR_INVALID_ARG.  nb > 4096 or H * nb^2 > 2^30:
+ * BSP_ERR_UNSUPPORTED.  The pages build layouts on the host; this entry point
+ * is an implementation addition for dynamic layouts. */
+int bsp_layout_compile_device(const uint8_t* layout, int H, int nb, int block, void* stream,
+                              bsp_layout_t* out);
+
 /* Free a handle (synchronises the device first if it owns device memory).
  * NULL is accepted and ignored. */
 int bsp_layout_destroy(bsp_layout_t layout);

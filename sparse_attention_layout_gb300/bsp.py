@@ -49,6 +49,7 @@ def lib():
         P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
         L.bsp_layout_plan.argtypes = [P, i32, i32, i32, ctypes.POINTER(P)]
         L.bsp_layout_compile.argtypes = [P, i32, i32, i32, P, ctypes.POINTER(P)]
+        L.bsp_layout_compile_device.argtypes = [P, i32, i32, i32, P, ctypes.POINTER(P)]
         L.bsp_layout_destroy.argtypes = [P]
         L.bsp_layout_info.argtypes = [P, P, P, P, P]
         L.bsp_layout_get_luts.argtypes = [P] * 7
@@ -65,7 +66,8 @@ def lib():
         L.bsp_status_string.restype = ctypes.c_char_p
         L.bsp_status_string.argtypes = [i32]
         L.bsp_version.restype = ctypes.c_char_p
-        for name in ("bsp_layout_plan", "bsp_layout_compile", "bsp_layout_destroy", "bsp_layout_info",
+        for name in ("bsp_layout_plan", "bsp_layout_compile", "bsp_layout_compile_device", "bsp_layout_destroy",
+                     "bsp_layout_info",
                      "bsp_layout_get_luts", "bsp_layout_tiles", "bsp_sdd", "bsp_dsd", "bsp_dds", "bsp_softmax",
                      "bsp_attention", "bsp_softmax_backward", "bsp_attention_backward", "bsp_layout_groups",
                      "bsp_status_check"):
@@ -192,6 +194,20 @@ def bsp_layout_compile(layout, block: int, stream=None) -> Layout:
     _check(lib().bsp_layout_compile(ctypes.c_void_p(lay.ctypes.data), H, nb, B, _stream(stream),
                                     ctypes.byref(h)), "bsp_layout_compile")
     return Layout(h, lay, B)
+
+
+def bsp_layout_compile_device(layout, block: int, stream=None) -> Layout:
+    """Compile a layout held in device memory (torch uint8 CUDA tensor
+    [H, nb, nb]) on the device."""
+    if not (isinstance(layout, torch.Tensor) and layout.is_cuda and layout.dtype == torch.uint8):
+        raise TypeError("layout must be a CUDA uint8 tensor")
+    lay = layout.contiguous()
+    if lay.dim() != 3 or lay.shape[1] != lay.shape[2]:
+        raise ValueError("layout must be [H, nb, nb]")
+    h = ctypes.c_void_p()
+    _check(lib().bsp_layout_compile_device(ctypes.c_void_p(lay.data_ptr()), lay.shape[0], lay.shape[1], int(block),
+                                           _stream(stream), ctypes.byref(h)), "bsp_layout_compile_device")
+    return Layout(h, None, int(block))
 
 
 def bsp_sdd(L: Layout, A, B, C=None, trans_a: int = 0, trans_b: int = 1, stream=None):

@@ -67,6 +67,11 @@ struct bsp_layout_s {
 
     void* dmem = nullptr;  // one device allocation holding every table
     LayoutView view{};
+    // false for a handle compiled on the device: the host vectors above stay
+    // empty and the inspection getters read the device tables (sizes below)
+    bool host_tables = true;
+    int64_t gl_slots[2] = {0, 0};
+    int sm_n_items_dev[2] = {0, 0};
 };
 
 constexpr int kSoftmaxChunkBudget = 64 * 1024;  // shared-memory bytes of one softmax chunk

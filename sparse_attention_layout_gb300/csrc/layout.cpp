@@ -348,9 +348,14 @@ extern "C" int bsp_layout_get_luts(bsp_layout_t L, int32_t* row_ptr, int32_t* co
     if (L->on_device) {
         if (cudaDeviceSynchronize() != cudaSuccess) return BSP_ERR_CUDA;
     }
+    const size_t ptr_len = (size_t)L->H * (L->nb + 1), nnz = (size_t)L->nnz;
+    const size_t lens[] = {ptr_len, nnz, nnz, ptr_len, nnz, nnz};
+    int k = 0;
     for (const Out& o : outs) {
-        if (!o.dst || o.host->empty()) continue;
-        const size_t bytes = o.host->size() * sizeof(int32_t);
+        const size_t len = L->host_tables ? o.host->size() : lens[k];
+        ++k;
+        if (!o.dst || len == 0) continue;
+        const size_t bytes = len * sizeof(int32_t);
         if (L->on_device) {
             if (cudaMemcpy(o.dst, o.dev, bytes, cudaMemcpyDeviceToHost) != cudaSuccess)
                 return BSP_ERR_CUDA;
@@ -366,6 +371,18 @@ extern "C" int bsp_layout_groups(bsp_layout_t L, int orient, int* G, int* n_grou
     if (!L || (orient != 0 && orient != 1)) return BSP_ERR_INVALID_ARG;
     if (G) *G = L->G;
     if (n_groups) *n_groups = L->n_tiles;
+    if (!L->host_tables) {
+        const size_t g = (size_t)L->G, nt = (size_t)L->n_tiles, sl = (size_t)L->gl_slots[orient];
+        if (n_slots) *n_slots = (int64_t)sl;
+        if (cudaDeviceSynchronize() != cudaSuccess) return BSP_ERR_CUDA;
+        struct D { int32_t* dst; const int32_t* src; size_t n; };
+        const D ds[] = {{grp_ptr, L->view.gl_ptr[orient], nt + 1}, {grp_order, L->view.gl_order[orient], nt},
+                        {slot_idx, L->view.gl_idx[orient], sl}, {slot_blk, L->view.gl_blk[orient], sl * g}};
+        for (const D& d : ds)
+            if (d.dst && d.n && cudaMemcpy(d.dst, d.src, d.n * sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+                return BSP_ERR_CUDA;
+        return BSP_OK;
+    }
     if (n_slots) *n_slots = (int64_t)L->gl_idx[orient].size();
     auto put = [](int32_t* dst, const std::vector<int32_t>& v) {
         if (dst && !v.empty()) std::copy(v.begin(), v.end(), dst);
@@ -384,6 +401,17 @@ extern "C" int bsp_layout_tiles(bsp_layout_t L, int* G, int* n_tiles, int64_t* n
     if (G) *G = L->G;
     if (n_tiles) *n_tiles = L->n_tiles;
     if (n_steps) *n_steps = L->n_steps;
+    if (!L->host_tables) {
+        const size_t G = (size_t)L->G, ns = (size_t)L->n_steps, nt = (size_t)L->n_tiles;
+        if (cudaDeviceSynchronize() != cudaSuccess) return BSP_ERR_CUDA;
+        struct D { int32_t* dst; const int32_t* src; size_t n; };
+        const D ds[] = {{tile_step_ptr, L->view.tile_step_ptr, nt + 1}, {tile_order, L->view.tile_order, nt},
+                        {step_col, L->view.step_col, ns * G}, {step_blk, L->view.step_blk, ns * G * G}};
+        for (const D& d : ds)
+            if (d.dst && d.n && cudaMemcpy(d.dst, d.src, d.n * sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+                return BSP_ERR_CUDA;
+        return BSP_OK;
+    }
     auto put = [](int32_t* dst, const std::vector<int32_t>& v) {
         if (dst && !v.empty()) std::memcpy(dst, v.data(), v.size() * sizeof(int32_t));
     };
