@@ -58,6 +58,9 @@ def _bind(lib):
     lib.oracle_attention.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, dbl, i32, P, i64, P, P]
     lib.oracle_softmax_backward.argtypes = [P, i32, i32, i32, i32, P, P, dbl, P]
     lib.oracle_attention_backward.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, dbl, i32, P, P, P, P]
+    lib.oracle_affine_expand.argtypes = [P, P, i32, i32, P]
+    lib.oracle_affine_describable.restype = i32
+    lib.oracle_affine_describable.argtypes = [P, i32]
     return lib
 
 
@@ -222,3 +225,18 @@ class Oracle:
         self.lib.oracle_attention_backward(_ptr(lay), H, nb, B, Z, D, _ptr(Q), _ptr(K), _ptr(V), _ptr(dO),
                                            float(scale), int(kind), _ptr(m), *[_ptr(o) for o in outs])
         return tuple(outs)
+
+    def affine_expand(self, n_terms, terms, nb):
+        """0/1 layout [H, nb, nb] of per-head affine terms: n_terms [H] (0..2),
+        terms [H, 2, 5] rows (alpha, beta, sigma, kappa, causal)."""
+        n = np.ascontiguousarray(n_terms, dtype=np.int32)
+        t = np.ascontiguousarray(terms, dtype=np.int32).reshape(n.size, 2, 5)
+        out = np.zeros((n.size, nb, nb), dtype=np.uint8)
+        self.lib.oracle_affine_expand(_ptr(n), _ptr(t), n.size, nb, _ptr(out))
+        return out
+
+    def affine_describable(self, head) -> bool:
+        """Whether a band term and / or a column term reproduce one head's
+        [nb, nb] layout exactly (exhaustive search: nb up to about 10)."""
+        lay = _u8(head)
+        return bool(self.lib.oracle_affine_describable(_ptr(lay), lay.shape[0]))

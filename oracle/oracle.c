@@ -509,3 +509,70 @@ void oracle_attention_backward(const uint8_t* layout, int H, int nb, int B, int 
         free(inR);
     }
 }
+
+/* ----------------------------------------------------------------------
+ * Affine block-row geometry.  [SPLAT] (the SPLAT / ACSR abstract, NSF PAR
+ * record): the regular sparse-attention patterns (banded, strided, ...) have
+ * rows whose column sets follow a formula in the row index, which a format can
+ * store instead of per-block indices.  The abstract gives no format; the
+ * reading used here: a head is described by at most two terms, each a column
+ * progression whose start moves with the row,
+ *     term (alpha, beta, sigma, kappa, causal) puts block (i, j) in the layout
+ *     when j = alpha * i + beta + sigma * k for some 0 <= k < kappa, j inside
+ *     [0, nb), and (causal == 0 or j <= i),
+ * a "band" term (alpha = 1, sigma = 1, causal = 0: offsets beta .. beta+kappa-1
+ * from the diagonal) and a "column" term (alpha = 0: the same progression of
+ * columns in every row, or in every row at or below it when causal).  A head's
+ * layout is the union of its terms.
+ * ---------------------------------------------------------------------- */
+
+static int term_has(const int32_t* t, int64_t i, int64_t j) {
+    const int64_t alpha = t[0], beta = t[1], sigma = t[2], kappa = t[3], causal = t[4];
+    if (causal && j > i) return 0;
+    const int64_t d = j - alpha * i - beta;
+    if (d < 0 || sigma <= 0 || d % sigma != 0) return 0;
+    return d / sigma < kappa;
+}
+
+/* terms: int32 [H][2][5]; n_terms[h] terms of head h are used (0..2).
+ * out: uint8 [H][nb][nb]. */
+void oracle_affine_expand(const int32_t* n_terms, const int32_t* terms, int H, int nb, uint8_t* out) {
+    for (int h = 0; h < H; ++h)
+        for (int64_t i = 0; i < nb; ++i)
+            for (int64_t j = 0; j < nb; ++j) {
+                uint8_t v = 0;
+                for (int t = 0; t < n_terms[h]; ++t)
+                    if (term_has(terms + ((int64_t)h * 2 + t) * 5, i, j)) v = 1;
+                out[((int64_t)h * nb + i) * nb + j] = v;
+            }
+}
+
+static int head_equals(const uint8_t* head, int nb, const int32_t* band, const int32_t* col) {
+    for (int64_t i = 0; i < nb; ++i)
+        for (int64_t j = 0; j < nb; ++j) {
+            const int v = (band && term_has(band, i, j)) || (col && term_has(col, i, j));
+            if (v != (head[i * nb + j] != 0)) return 0;
+        }
+    return 1;
+}
+
+/* 1 if some band term and / or column term (each optional) reproduces the
+ * head's [nb][nb] layout exactly, found by trying every parameter set: for
+ * small nb only (about nb^6 candidates). */
+int oracle_affine_describable(const uint8_t* head, int nb) {
+    for (int with_band = 0; with_band <= 1; ++with_band)
+        for (int bb = -(nb - 1); bb <= (with_band ? nb - 1 : -(nb - 1)); ++bb)
+            for (int bk = 1; bk <= (with_band ? 2 * nb - 1 : 1); ++bk) {
+                const int32_t band[5] = {1, bb, 1, bk, 0};
+                const int32_t* pb = with_band ? band : NULL;
+                if (head_equals(head, nb, pb, NULL)) return 1;
+                for (int cb = 0; cb < nb; ++cb)
+                    for (int cs = 1; cs <= nb; ++cs)
+                        for (int ck = 1; ck <= nb; ++ck)
+                            for (int cc = 0; cc <= 1; ++cc) {
+                                const int32_t col[5] = {0, cb, cs, ck, cc};
+                                if (head_equals(head, nb, pb, col)) return 1;
+                            }
+            }
+    return 0;
+}

@@ -55,6 +55,9 @@ MUTANTS = {
     "attention_bwd_unweighted_delta": ("delta += p * dp;", "delta += dp;"),
     "attention_bwd_transposed_layout": ("const uint8_t present = layout[((int64_t)h * nb + r / B) * nb + c / B];",
                                         "const uint8_t present = layout[((int64_t)h * nb + c / B) * nb + r / B];"),
+    "affine_causal_ignored": ("if (causal && j > i) return 0;", "(void)causal;"),
+    "affine_kappa_off_by_one": ("return d / sigma < kappa;", "return d / sigma <= kappa;"),
+    "affine_row_slope_dropped": ("const int64_t d = j - alpha * i - beta;", "const int64_t d = j - beta;"),
 }
 
 

@@ -418,3 +418,69 @@ def test_attention_backward_equals_unfused_chain(oracle, kind):
     np.testing.assert_allclose(dV, oracle.dsd(lay, B, P, G, trans_a=1), rtol=1e-5, atol=1e-6)
     np.testing.assert_allclose(dQ, oracle.dsd(lay, B, dS, K), rtol=1e-5, atol=1e-6)
     np.testing.assert_allclose(dK, oracle.dsd(lay, B, dS, Q, trans_a=1), rtol=1e-5, atol=1e-6)
+
+
+# ------------------------------------------------------ affine geometry ----
+# SPLAT / ACSR abstract (NSF PAR record): banded and strided attention layouts
+# have rows whose columns follow a formula in the row index.  The pins build
+# the same layouts by independent numpy constructions.
+
+def _terms(*ts):
+    t = np.zeros((1, 2, 5), np.int32)
+    for k, v in enumerate(ts):
+        t[0, k] = v
+    return np.array([len(ts)], np.int32), t
+
+
+@pytest.mark.parametrize("nb,w", [(1, 0), (6, 0), (9, 2), (12, 4), (5, 7)])
+def test_affine_band_is_numpy_band(oracle, nb, w):
+    n, t = _terms((1, -w, 1, 2 * w + 1, 0))
+    want = W.layout_band(nb, w)
+    assert np.array_equal(oracle.affine_expand(n, t, nb), want)
+
+
+@pytest.mark.parametrize("nb", [3, 10])
+def test_affine_lower_triangle_is_tril(oracle, nb):
+    n, t = _terms((1, -(nb - 1), 1, nb, 0))
+    assert np.array_equal(oracle.affine_expand(n, t, nb)[0], np.tril(np.ones((nb, nb), np.uint8)))
+
+
+@pytest.mark.parametrize("nb,local,stride", [(256, 4, 16), (40, 3, 8), (17, 1, 5)])
+def test_affine_strided_is_sparse_transformer_fixed(oracle, nb, local, stride):
+    # local window (offsets -(local-1) .. 0) plus every stride-th column, causal
+    n, t = _terms((1, -(local - 1), 1, local, 0), (0, 0, stride, (nb - 1) // stride + 1, 1))
+    assert np.array_equal(oracle.affine_expand(n, t, nb), W.layout_strided_causal(nb, local, stride))
+
+
+def test_affine_column_terms_causal_and_not(oracle):
+    nb = 10
+    cols = np.zeros(nb, bool)
+    cols[[2, 5, 8]] = True
+    n, t = _terms((0, 2, 3, 3, 0))
+    assert np.array_equal(oracle.affine_expand(n, t, nb)[0], np.broadcast_to(cols, (nb, nb)).astype(np.uint8))
+    n, t = _terms((0, 2, 3, 3, 1))
+    want = (np.broadcast_to(cols, (nb, nb)) & (np.arange(nb)[None, :] <= np.arange(nb)[:, None]))
+    assert np.array_equal(oracle.affine_expand(n, t, nb)[0], want.astype(np.uint8))
+    n, t = _terms()
+    assert not oracle.affine_expand(n, t, nb).any()
+
+
+def test_affine_describable_known_cases(oracle):
+    nb = 8
+    i, j = np.meshgrid(np.arange(nb), np.arange(nb), indexing="ij")
+    assert oracle.affine_describable(W.layout_band(nb, 2)[0])
+    assert oracle.affine_describable(W.layout_strided_causal(nb, 2, 4)[0])
+    assert oracle.affine_describable(np.zeros((nb, nb), np.uint8))
+    assert oracle.affine_describable(np.ones((nb, nb), np.uint8))
+    # a band plus one full column
+    lay = W.layout_band(nb, 1)[0]
+    lay[:, 5] = 1
+    assert oracle.affine_describable(lay)
+    # parity checkerboard: rows alternate between two column sets
+    assert not oracle.affine_describable(((i + j) % 2 == 0).astype(np.uint8))
+    # two separate diagonals
+    assert not oracle.affine_describable(((j == i) | (j == i + 5)).astype(np.uint8))
+    # a band plus one full row
+    lay = W.layout_band(nb, 1)[0]
+    lay[3, :] = 1
+    assert not oracle.affine_describable(lay)
