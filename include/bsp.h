@@ -100,6 +100,52 @@ int bsp_layout_compile(const uint8_t* layout, int H, int nb, int block, void* st
 int bsp_layout_compile_device(const uint8_t* layout, int H, int nb, int block, void* stream,
                               bsp_layout_t* out);
 
+/* ---- affine geometry ----------------------------------------------------
+ * The SPLAT / ACSR abstract (NSF PAR record, "affine-compressed-sparse-row"):
+ * regular attention layouts (banded, strided) have block-rows whose columns
+ * follow a formula in the row index, so a kernel can compute them instead of
+ * reading per-block tables.  Reading used here (the abstract gives no
+ * format): a head is the union of at most BSP_MAX_AFFINE_TERMS terms, one of
+ * each kind, where a term (alpha, beta, sigma, kappa, causal) holds block
+ * (i, j) when j = alpha*i + beta + sigma*k for some 0 <= k < kappa, with
+ * 0 <= j < nb and (causal == 0 or j <= i):
+ *   band term   alpha = 1, sigma = 1, causal = 0, kappa >= 1,
+ *               -(nb-1) <= beta <= nb-1, beta + kappa - 1 <= nb - 1
+ *               (offsets beta .. beta+kappa-1 from the diagonal);
+ *   column term alpha = 0, sigma >= 1 (sigma = 1 when kappa = 1), kappa >= 1,
+ *               0 <= beta, beta + sigma*(kappa-1) <= nb - 1, causal 0 or 1
+ *               (the same columns in every row, or in the rows at or below
+ *               each column when causal).
+ * A head's band term, when it has one, comes first. */
+#define BSP_MAX_AFFINE_TERMS 2
+typedef struct {
+    int32_t alpha, beta, sigma, kappa, causal;
+} bsp_affine_term_t;
+
+/* Build a compiled handle from per-head affine terms (HOST arrays): n_terms
+ * [H] (0 .. 2; 0 = an empty head) and terms [H][BSP_MAX_AFFINE_TERMS] (the
+ * first n_terms[h] of head h are used).  The layout is expanded on the
+ * device and compiled as by bsp_layout_compile_device (same tables, same
+ * limits, synchronises `stream`); the handle records the terms, so the
+ * attention kernel computes its key blocks from them.  Terms that break the
+ * rules above: BSP_ERR_INVALID_ARG. */
+int bsp_layout_compile_affine(const int32_t* n_terms, const bsp_affine_term_t* terms, int H, int nb,
+                              int block, void* stream, bsp_layout_t* out);
+
+/* The handle's affine description, into HOST arrays n_terms [H] and terms
+ * [H][BSP_MAX_AFFINE_TERMS] (unused entries zeroed).  n_terms[h] = -1: head h
+ * has no description of this form.  bsp_layout_plan / bsp_layout_compile
+ * analyse every head (exact: the terms reproduce the head's layout; complete
+ * for nb <= 256, i.e. a head is reported -1 only when no band / column pair
+ * describes it; for larger nb the eight longest candidate bands are tried);
+ * bsp_layout_compile_affine records the terms it was given;
+ * bsp_layout_compile_device does not analyse (every head -1).  With the
+ * environment variable BSP_GEOMETRY=1, and every head described, the fused
+ * attention kernel's TMA producers compute each step's key blocks from the
+ * terms instead of reading the step tables (same results; off by default
+ * because it measured slower: the table loads are issued ahead of use). */
+int bsp_layout_geometry(bsp_layout_t layout, int32_t* n_terms, bsp_affine_term_t* terms);
+
 /* Free a handle (synchronises the device first if it owns device memory).
  * NULL is accepted and ignored. */
 int bsp_layout_destroy(bsp_layout_t layout);
@@ -249,6 +295,15 @@ int bsp_attention_backward(bsp_layout_t layout, int dtype, const void* Q, const 
  * give a value in (0, 2^-124.5]).  y: DEVICE float [n] (output).  Enqueued on
  * `stream`.  The method is the implementation's, not the pages'. */
 int bsp_diag_exp2(const float* x, float* y, int64_t n, void* stream);
+
+/* For a host-planned or compiled handle whose every head has an affine
+ * description: evaluate ON THE HOST the routines with which the geometry
+ * variant of the attention kernel computes each step's key blocks and their
+ * presence, into HOST arrays shaped like bsp_layout_tiles' step_col [n_steps*G]
+ * (block-column of each slot, -1 = padding) and step_blk [n_steps*G*G] (1 when
+ * (row a, slot b) is in the layout, else 0), so that tests can compare them
+ * with the step tables without a GPU.  Other handles: BSP_ERR_UNSUPPORTED. */
+int bsp_diag_geometry_steps(bsp_layout_t layout, int32_t* step_col, int32_t* step_blk);
 
 /* ---- status ------------------------------------------------------------ */
 

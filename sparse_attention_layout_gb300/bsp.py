@@ -62,6 +62,8 @@ def lib():
         L.bsp_softmax_backward.argtypes = [P, i32, P, P, P, i32, f32, P]
         L.bsp_attention_backward.argtypes = [P, i32, P, P, P, P, P, P, P, i32, i32, f32, i32, P, P, P, P]
         L.bsp_layout_groups.argtypes = [P, i32, P, P, P, P, P, P, P]
+        L.bsp_layout_geometry.argtypes = [P, P, P]
+        L.bsp_layout_compile_affine.argtypes = [P, P, i32, i32, i32, P, ctypes.POINTER(P)]
         L.bsp_status_check.argtypes = [P, P]
         L.bsp_status_string.restype = ctypes.c_char_p
         L.bsp_status_string.argtypes = [i32]
@@ -70,7 +72,7 @@ def lib():
                      "bsp_layout_info",
                      "bsp_layout_get_luts", "bsp_layout_tiles", "bsp_sdd", "bsp_dsd", "bsp_dds", "bsp_softmax",
                      "bsp_attention", "bsp_softmax_backward", "bsp_attention_backward", "bsp_layout_groups",
-                     "bsp_status_check"):
+                     "bsp_status_check", "bsp_layout_geometry", "bsp_layout_compile_affine"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -172,6 +174,15 @@ class Layout:
         out.update(G=G, n_groups=ng, n_slots=ns)
         return out
 
+    def geometry(self):
+        """Affine description per head: (n_terms [H] int32, -1 = none;
+        terms [H, 2, 5] int32 rows (alpha, beta, sigma, kappa, causal))."""
+        n = np.zeros(self.H, np.int32)
+        t = np.zeros((self.H, MAX_AFFINE_TERMS, 5), np.int32)
+        _check(lib().bsp_layout_geometry(self.handle, ctypes.c_void_p(n.ctypes.data), ctypes.c_void_p(t.ctypes.data)),
+               "bsp_layout_geometry")
+        return n, t
+
 
 def _layout_args(layout, block):
     lay = np.ascontiguousarray(layout, dtype=np.uint8)
@@ -207,6 +218,21 @@ def bsp_layout_compile_device(layout, block: int, stream=None) -> Layout:
     h = ctypes.c_void_p()
     _check(lib().bsp_layout_compile_device(ctypes.c_void_p(lay.data_ptr()), lay.shape[0], lay.shape[1], int(block),
                                            _stream(stream), ctypes.byref(h)), "bsp_layout_compile_device")
+    return Layout(h, None, int(block))
+
+
+MAX_AFFINE_TERMS = 2
+
+
+def bsp_layout_compile_affine(n_terms, terms, nb: int, block: int, stream=None) -> Layout:
+    """Compile a layout given by per-head affine terms (n_terms [H], terms
+    [H, 2, 5] rows (alpha, beta, sigma, kappa, causal)) on the device."""
+    n = np.ascontiguousarray(n_terms, dtype=np.int32)
+    t = np.ascontiguousarray(terms, dtype=np.int32).reshape(n.size, MAX_AFFINE_TERMS, 5)
+    h = ctypes.c_void_p()
+    _check(lib().bsp_layout_compile_affine(ctypes.c_void_p(n.ctypes.data), ctypes.c_void_p(t.ctypes.data), n.size,
+                                           int(nb), int(block), _stream(stream), ctypes.byref(h)),
+           "bsp_layout_compile_affine")
     return Layout(h, None, int(block))
 
 

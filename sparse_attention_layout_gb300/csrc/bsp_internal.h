@@ -41,6 +41,10 @@ struct LayoutView {
     int sm_n_items[2];
     int sm_max_bytes[2];          // largest chunk of the list, in bytes
     int sm_fits[2];               // 0: some single row exceeds the budget
+    // affine geometry when every head has one, else nullptr: per head 8 ints
+    // (band on, band beta, band kappa, column on, column beta, sigma, kappa,
+    // causal); see bsp_affine_term_t
+    const int32_t* geo;
     int* status;                  // device status word (0 = OK, else a BSP_ERR_* code)
     int H, nb, B, S, G, ngroups, n_tiles;
     int64_t nnz;
@@ -72,7 +76,16 @@ struct bsp_layout_s {
     bool host_tables = true;
     int64_t gl_slots[2] = {0, 0};
     int sm_n_items_dev[2] = {0, 0};
+    // affine description per head (n = -1: none), the kernels' 8-int records
+    // when every head has one (uploaded into dmem, or geo_dmem for a handle
+    // compiled from terms)
+    std::vector<int32_t> geo_n;
+    std::vector<bsp_affine_term_t> geo_terms;  // [H * BSP_MAX_AFFINE_TERMS]
+    std::vector<int32_t> geo_rec;              // [H * kGeoRec] or empty
+    void* geo_dmem = nullptr;
 };
+
+constexpr int kGeoRec = 8;  // ints per head in LayoutView::geo
 
 constexpr int kSoftmaxChunkBudget = 64 * 1024;  // shared-memory bytes of one softmax chunk
 
@@ -109,5 +122,13 @@ int launch_softmax_backward(const bsp_layout_s* L, int dtype, const void* Y, con
                             float scale, cudaStream_t s);
 
 int sm_count();  // multiprocessors of the current device (cached per device)
+
+// affine geometry (geometry.cpp)
+int affine_validate(int nb, int n, const bsp_affine_term_t* t);
+int affine_detect(const uint8_t* head, int nb, bsp_affine_term_t* t);
+// per-head descriptions of a [H][nb][nb] host layout into L->geo_n / geo_terms / geo_rec
+void affine_analyse(bsp_layout_s* L, const uint8_t* lay);
+// L->geo_rec from L->geo_n / geo_terms (left empty unless every head is described)
+void affine_records(bsp_layout_s* L);
 
 }  // namespace bsp

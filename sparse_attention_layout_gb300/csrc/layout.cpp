@@ -226,6 +226,7 @@ extern "C" int bsp_layout_plan(const uint8_t* layout, int H, int nb, int block, 
     int rc;
     try {
         rc = build_tables(L, layout);
+        if (rc == BSP_OK) bsp::affine_analyse(L, layout);
     } catch (const std::bad_alloc&) {
         rc = BSP_ERR_OOM;
     }
@@ -263,6 +264,7 @@ extern "C" int bsp_layout_compile(const uint8_t* layout, int H, int nb, int bloc
         {&L->gl_idx[0], &V.gl_idx[0]},   {&L->gl_blk[0], &V.gl_blk[0]},
         {&L->gl_ptr[1], &V.gl_ptr[1]},   {&L->gl_order[1], &V.gl_order[1]},
         {&L->gl_idx[1], &V.gl_idx[1]},   {&L->gl_blk[1], &V.gl_blk[1]},
+        {&L->geo_rec, &V.geo},
     };
     size_t total = padded<int>(4);  // status word first
     for (const Part& pt : parts) total += padded<int32_t>(pt.v->size() + 1);
@@ -285,6 +287,7 @@ extern "C" int bsp_layout_compile(const uint8_t* layout, int H, int nb, int bloc
                                        cudaMemcpyHostToDevice, s) == cudaSuccess;
         off += padded<int32_t>(pt.v->size() + 1);
     }
+    if (L->geo_rec.empty()) V.geo = nullptr;  // some head has no affine description
     V.H = L->H;
     V.nb = L->nb;
     V.B = L->B;
@@ -319,6 +322,7 @@ extern "C" int bsp_layout_destroy(bsp_layout_t L) {
         if (cur != L->device) cudaSetDevice(L->device);
         if (cudaDeviceSynchronize() != cudaSuccess) rc = BSP_ERR_CUDA;
         if (cudaFree(L->dmem) != cudaSuccess) rc = BSP_ERR_CUDA;
+        if (L->geo_dmem && cudaFree(L->geo_dmem) != cudaSuccess) rc = BSP_ERR_CUDA;
         if (cur >= 0 && cur != L->device) cudaSetDevice(cur);
     }
     delete L;

@@ -297,6 +297,24 @@ __global__ void k_orders(const OrderJob* jobs, int wmax) {
     }
 }
 
+// [H][nb][nb] 0/1 layout of per-head affine records (8 ints per head: band
+// on, beta, kappa; column on, beta, sigma, kappa, causal)
+__global__ void k_expand_affine(const int32_t* __restrict__ rec, int H, int nb, uint8_t* __restrict__ out) {
+    const int64_t total = (int64_t)H * nb * nb;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
+        const int j = (int)(e % nb);
+        const int64_t hi = e / nb;
+        const int i = (int)(hi % nb), h = (int)(hi / nb);
+        const int32_t* r = rec + (size_t)h * kGeoRec;
+        bool v = r[0] && j - i >= r[1] && j - i < r[1] + r[2];
+        if (r[3] && !v && j >= r[4] && (!r[7] || j <= i)) {
+            const int d = j - r[4];
+            v = d % r[5] == 0 && d / r[5] < r[6];
+        }
+        out[e] = v ? 1 : 0;
+    }
+}
+
 template <typename T>
 size_t padded(size_t n) {
     return ((n * sizeof(T) + 255) / 256) * 256;
@@ -466,5 +484,65 @@ extern "C" int bsp_layout_compile_device(const uint8_t* layout, int H, int nb, i
     }
     L->on_device = true;
     *out = L;
+    return BSP_OK;
+}
+
+extern "C" int bsp_layout_compile_affine(const int32_t* n_terms, const bsp_affine_term_t* terms, int H, int nb,
+                                         int block, void* stream, bsp_layout_t* out) {
+    using namespace bsp;
+    if (!out) return BSP_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!n_terms || !terms || H < 1 || nb < 1 || !valid_block(block)) return BSP_ERR_INVALID_ARG;
+    if (nb > 4096 || (int64_t)nb * block > (1 << 24) || (int64_t)H * nb * nb > ((int64_t)1 << 30))
+        return BSP_ERR_UNSUPPORTED;
+    // the description, checked and turned into the kernels' records
+    bsp_layout_s desc;
+    desc.H = H;
+    desc.nb = nb;
+    desc.geo_n.assign(n_terms, n_terms + H);
+    desc.geo_terms.assign((size_t)H * BSP_MAX_AFFINE_TERMS, bsp_affine_term_t{0, 0, 0, 0, 0});
+    for (int h = 0; h < H; ++h) {
+        const int rc = affine_validate(nb, n_terms[h], terms + (size_t)h * BSP_MAX_AFFINE_TERMS);
+        if (rc != BSP_OK) return rc;
+        std::copy_n(terms + (size_t)h * BSP_MAX_AFFINE_TERMS, n_terms[h],
+                    &desc.geo_terms[(size_t)h * BSP_MAX_AFFINE_TERMS]);
+    }
+    affine_records(&desc);
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t rec_bytes = desc.geo_rec.size() * sizeof(int32_t);
+    int32_t* rec = nullptr;
+    uint8_t* lay = nullptr;
+    if (cudaMalloc((void**)&rec, rec_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return BSP_ERR_OOM;
+    }
+    if (cudaMalloc((void**)&lay, (size_t)H * nb * nb) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(rec);
+        return BSP_ERR_OOM;
+    }
+    int rc = BSP_OK;
+    if (cudaMemcpyAsync(rec, desc.geo_rec.data(), rec_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) rc = BSP_ERR_CUDA;
+    if (rc == BSP_OK) {
+        const int64_t blocks = std::min<int64_t>(((int64_t)H * nb * nb + 255) / 256, (int64_t)sm_count() * 8);
+        k_expand_affine<<<(unsigned)blocks, 256, 0, s>>>(rec, H, nb, lay);
+        if (cudaGetLastError() != cudaSuccess) rc = BSP_ERR_CUDA;
+    }
+    // compiles the expanded layout and synchronises the stream, after which
+    // the layout buffer is no longer read
+    if (rc == BSP_OK) rc = bsp_layout_compile_device(lay, H, nb, block, stream, out);
+    if (rc != BSP_OK) cudaStreamSynchronize(s);
+    cudaFree(lay);
+    if (rc != BSP_OK) {
+        cudaGetLastError();
+        cudaFree(rec);
+        return rc;
+    }
+    bsp_layout_s* L = *out;
+    L->geo_n = std::move(desc.geo_n);
+    L->geo_terms = std::move(desc.geo_terms);
+    L->geo_rec = std::move(desc.geo_rec);
+    L->geo_dmem = rec;
+    L->view.geo = rec;
     return BSP_OK;
 }

@@ -1,0 +1,12 @@
+// f16 instantiations of the fused tensor-core attention kernel for layouts
+// whose every head has an affine description.
+#include "tc_attention.cuh"
+
+namespace bsp {
+
+int launch_attention_tc_f16_geo(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O,
+                              int Z, int D, float scale, int kind, const uint8_t* mask, cudaStream_t s) {
+    return attn::by_block<__half, true>(L, Q, K, V, O, Z, D, scale, kind, mask, s);
+}
+
+}  // namespace bsp

@@ -188,3 +188,171 @@ def test_info_reports_sizes(lib):
     lay = W.layout_band(10, 2, H=3)
     L = bsp.bsp_layout_plan(lay, 32)
     assert (L.H, L.nb, L.B, L.nnz, L.S) == (3, 10, 32, int(lay.sum()), 320)
+
+
+# ------------------------------------------------------ affine geometry ----
+
+def _affine_cases():
+    """Small heads: every band / column-term family member the rules allow on
+    nb = 6, random affine pairs, and random layouts (mostly not affine)."""
+    rng = np.random.default_rng(11)
+    heads = []
+    nb = 6
+    for bb in range(-(nb - 1), nb):
+        for bk in range(1, nb - bb + 1):
+            heads.append(("band", nb, [(1, bb, 1, bk, 0)]))
+    for _ in range(60):
+        nb = int(rng.integers(2, 10))
+        bb = int(rng.integers(-(nb - 1), nb))
+        bk = int(rng.integers(1, nb - bb + 1))
+        cb = int(rng.integers(0, nb))
+        cs = int(rng.integers(1, nb))
+        ck = int(rng.integers(1, (nb - 1 - cb) // cs + 2))
+        cs = 1 if ck == 1 else cs
+        terms = [(0, cb, cs, ck, int(rng.integers(0, 2)))]
+        if rng.random() < 0.7:
+            terms.insert(0, (1, bb, 1, bk, 0))
+        heads.append(("pair", nb, terms))
+    for k in range(60):
+        nb = int(rng.integers(1, 9))
+        heads.append(("random", nb, (rng.random((nb, nb)) < rng.choice([0.2, 0.5, 0.8])).astype(np.uint8)))
+    return heads
+
+
+AFFINE_CASES = _affine_cases()
+
+
+def _check_terms(nb, n, t):
+    """The rules of bsp_affine_term_t for the first n rows of t [2, 5]."""
+    kinds = [int(x[0]) for x in t[:n]]
+    assert kinds in ([], [1], [0], [1, 0])
+    for a, b, s, k, c in t[:n]:
+        assert k >= 1
+        if a == 1:
+            assert s == 1 and c == 0 and -(nb - 1) <= b and b + k - 1 <= nb - 1
+        else:
+            assert s >= 1 and c in (0, 1) and b >= 0 and b + s * (k - 1) <= nb - 1 and (k > 1 or s == 1)
+    assert not t[n:].any()
+
+
+@pytest.mark.parametrize("idx", range(len(AFFINE_CASES)))
+def test_geometry_exact_and_complete(lib, oracle, idx):
+    # exact: the terms the library reports expand (oracle) to the head; complete:
+    # it reports none only when the oracle's exhaustive search finds none
+    kind, nb, spec = AFFINE_CASES[idx]
+    if kind == "random":
+        head = spec
+    else:
+        n0 = np.array([len(spec)], np.int32)
+        t0 = np.zeros((1, 2, 5), np.int32)
+        t0[0, :len(spec)] = spec
+        head = oracle.affine_expand(n0, t0, nb)[0]
+    L = bsp.bsp_layout_plan(head[None], 16)
+    n, t = L.geometry()
+    if n[0] < 0:
+        assert not oracle.affine_describable(head), f"{kind}: a description exists but none was found"
+    else:
+        _check_terms(nb, n[0], t[0])
+        assert np.array_equal(oracle.affine_expand(n, t, nb)[0], head)
+        if kind != "random":
+            assert oracle.affine_describable(head)
+
+
+def test_geometry_of_the_workloads(lib):
+    want = {"band": (1, [(1, -4, 1, 9, 0)]), "strided": (2, [(1, -3, 1, 4, 0), (0, 0, 16, 16, 1)]),
+            "tiny": (-1, []), "bigbird": (-1, [])}
+    for name, (n_want, terms) in want.items():
+        w = W.ATTENTION_WORKLOADS[name]
+        n, t = bsp.bsp_layout_plan(w.layout(), w.B).geometry()
+        assert (n == n_want).all(), name
+        for h in range(len(n)):
+            for k, term in enumerate(terms):
+                assert tuple(t[h, k]) == term, (name, h, k)
+    n, _ = bsp.bsp_layout_plan(W.SPMM.layout(0.1), W.SPMM.B).geometry()
+    assert (n == -1).all()
+
+
+def test_geometry_mixed_heads(lib):
+    lay = np.stack([W.layout_band(8, 1)[0], np.eye(8, dtype=np.uint8)[::-1].copy(), np.zeros((8, 8), np.uint8)])
+    n, t = bsp.bsp_layout_plan(lay, 32).geometry()
+    assert list(n) == [1, -1, 0]
+    assert tuple(t[0, 0]) == (1, -1, 1, 3, 0) and not t[1:].any()
+
+
+@pytest.mark.parametrize("terms", [
+    [(2, 0, 1, 1, 0)],                         # alpha not 0 / 1
+    [(1, 0, 2, 2, 0)],                         # band with stride
+    [(1, 0, 1, 2, 1)],                         # causal band
+    [(1, -8, 1, 1, 0)],                        # band offset below -(nb - 1)
+    [(1, 6, 1, 3, 0)],                         # band past the last column
+    [(0, -1, 1, 1, 0)],                        # column before 0
+    [(0, 4, 2, 3, 0)],                         # column past nb
+    [(0, 1, 2, 1, 0)],                         # one column with a stride
+    [(0, 1, 1, 0, 0)],                         # kappa 0
+    [(0, 1, 1, 2, 2)],                         # causal not 0 / 1
+    [(1, 0, 1, 1, 0), (1, 1, 1, 1, 0)],        # two bands
+    [(0, 0, 1, 1, 0), (1, 0, 1, 1, 0)],        # band not first
+])
+def test_compile_affine_rejects_bad_terms(lib, terms):
+    # checked on the host before any device work
+    nb = 8
+    n = np.array([len(terms)], np.int32)
+    t = np.zeros((1, 2, 5), np.int32)
+    t[0, :len(terms)] = terms
+    with pytest.raises(bsp.BspError) as e:
+        bsp.bsp_layout_compile_affine(n, t, nb, 32, stream=0)
+    assert e.value.code == -1
+    with pytest.raises(bsp.BspError) as e:
+        bsp.bsp_layout_compile_affine(np.array([3], np.int32), np.zeros((1, 2, 5), np.int32), nb, 32, stream=0)
+    assert e.value.code == -1
+
+
+@pytest.mark.parametrize("B", [16, 32, 64, 128])
+@pytest.mark.parametrize("seed", range(6))
+def test_geometry_steps_equal_step_tables(lib, oracle, B, seed):
+    # the attention kernel's column / presence arithmetic (evaluated on the
+    # host by bsp_diag_geometry_steps) against the compiler's step tables
+    rng = np.random.default_rng(500 + seed)
+    nb = int(rng.integers(3, 70))
+    H = 3
+    n = np.zeros(H, np.int32)
+    t = np.zeros((H, 2, 5), np.int32)
+    for h in range(H):
+        bb = int(rng.integers(-(nb - 1), nb))
+        bk = int(rng.integers(1, nb - bb + 1))
+        cb = int(rng.integers(0, nb))
+        cs = int(rng.integers(1, nb))
+        ck = int(rng.integers(1, (nb - 1 - cb) // cs + 2))
+        cs = 1 if ck == 1 else cs
+        terms = [[(1, bb, 1, bk, 0)], [(0, cb, cs, ck, int(rng.integers(0, 2)))],
+                 [(1, bb, 1, bk, 0), (0, cb, cs, ck, int(rng.integers(0, 2)))], []][int(rng.integers(0, 4))]
+        n[h] = len(terms)
+        if terms:
+            t[h, :len(terms)] = terms
+    lay = oracle.affine_expand(n, t, nb)
+    L = bsp.bsp_layout_plan(lay, B)
+    assert (L.geometry()[0] >= 0).all()
+    tab = L.tiles()
+    G, ns = tab["G"], tab["n_steps"]
+    col = np.zeros(max(ns * G, 1), np.int32)
+    blk = np.zeros(max(ns * G * G, 1), np.int32)
+    assert lib.bsp_diag_geometry_steps(L.handle, ctypes.c_void_p(col.ctypes.data), ctypes.c_void_p(blk.ctypes.data)) == 0
+    assert np.array_equal(col[:ns * G].reshape(ns, G), tab["step_col"])
+    assert np.array_equal(blk[:ns * G * G].reshape(ns, G, G), (tab["step_blk"] >= 0).astype(np.int32))
+
+
+def test_geometry_steps_of_the_workloads(lib):
+    for name in ("band", "strided"):
+        w = W.ATTENTION_WORKLOADS[name]
+        L = bsp.bsp_layout_plan(w.layout(), w.B)
+        tab = L.tiles()
+        G, ns = tab["G"], tab["n_steps"]
+        col = np.zeros(ns * G, np.int32)
+        blk = np.zeros(ns * G * G, np.int32)
+        assert lib.bsp_diag_geometry_steps(L.handle, ctypes.c_void_p(col.ctypes.data),
+                                           ctypes.c_void_p(blk.ctypes.data)) == 0
+        assert np.array_equal(col.reshape(ns, G), tab["step_col"]), name
+        assert np.array_equal(blk.reshape(ns, G, G), (tab["step_blk"] >= 0).astype(np.int32)), name
+    L = bsp.bsp_layout_plan(W.ATTENTION_WORKLOADS["bigbird"].layout(), 64)
+    z = np.zeros(4, np.int32)
+    assert lib.bsp_diag_geometry_steps(L.handle, ctypes.c_void_p(z.ctypes.data), ctypes.c_void_p(z.ctypes.data)) == -2
