@@ -287,6 +287,15 @@ def per_op_section(w, lay, L, q, k, v, pk, bsp, stream):
     ms = time_launches(lambda: bsp.bsp_sdd(L, q, k, P), 10, stream)
     out["sdd"] = {"ms": ms, "TFLOP/s": 2.0 * B * B * D * nnz * Z / ms / 1e9,
                   "GB/s": (Z * nnz * B * B * elt) / ms / 1e6}
+    # the other operand orientations: an operand stored [K][S] is read MN-major
+    if w.dtype != "f32":
+        qt, kt = q.transpose(-1, -2).contiguous(), k.transpose(-1, -2).contiguous()
+        out["sdd_trans"] = {}
+        for ta, tb in ((0, 0), (1, 0), (1, 1)):
+            a_op, b_op = (qt if ta else q), (k if tb else kt)
+            ms = time_launches(lambda: bsp.bsp_sdd(L, a_op, b_op, P, trans_a=ta, trans_b=tb), 10, stream)
+            out["sdd_trans"][f"ta{ta}_tb{tb}"] = {"ms": ms, "GB/s": (Z * nnz * B * B * elt) / ms / 1e6}
+        del qt, kt
     X = P.clone()
     ms = time_launches(lambda: bsp.bsp_softmax(L, X, P, w.scale, w.mask_kind), 10, stream)
     sbytes = 2.0 * Z * nnz * B * B * elt

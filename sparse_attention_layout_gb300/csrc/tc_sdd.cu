@@ -7,6 +7,14 @@
 // accumulators; four epilogue warps write the present blocks while the MMA
 // works ahead.
 //
+// Operand orientation: op(A) rows and op(B) columns are what the tiles hold.
+// trans_a = 0 / trans_b = 1 store them as rows ([S][K]: K-major tiles, 64-column
+// panels); trans_a = 1 / trans_b = 0 store them as columns ([K][S]): the tile is
+// then loaded as it lies, MN-major (panels of 64 rows, or of one key block of
+// 16 / 32 columns with a 32 / 64-byte swizzle), and only the shared-memory
+// descriptor and the instruction's major-ness bits change.  No transpose
+// happens in memory.
+//
 // Roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner and
 // single-thread MMA issuer, warps 2..5 epilogue (thread = TMEM lane).
 #include <algorithm>
@@ -28,7 +36,13 @@ struct SddArgs {
     LayoutView L;
     void* C;
     int Z;
+    int kd;      // contraction length K
+    int ta, tb;  // trans flags (ta = 1: A tile MN-major; tb = 0: B tile MN-major)
 };
+
+__host__ __device__ constexpr uint32_t swz_of(int row_bytes) {
+    return row_bytes == 128 ? kSw128 : (row_bytes == 64 ? kSw64 : kSw32);
+}
 
 template <int KP, int BLK>
 struct SddCfg {
@@ -48,7 +62,13 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     constexpr int G = 128 / BLK;
     constexpr int BST = C::BST;
     constexpr uint32_t kTileBytes = C::kTile;
-    constexpr uint32_t kIdesc = idesc_f16(128, 128, std::is_same<T, __nv_bfloat16>::value, 0, 0);
+    // MN-major key tiles: panels of W keys (RB bytes per K row), KPB per block
+    constexpr int W = BLK < 64 ? BLK : 64, RB = 2 * W, KPB = BLK / W;
+    const int kd = args.kd;
+    const bool a_mn = args.ta != 0, b_mn = args.tb == 0;
+    // bytes one stage's copies deliver: K-major boxes are 64 * KP columns wide
+    // (zero-filled past K), MN-major ones exactly K rows
+    const uint32_t a_bytes = a_mn ? 256u * kd : kTileBytes, b_bytes = b_mn ? 256u * kd : kTileBytes;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -101,23 +121,37 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 const int64_t zh = (int64_t)z * L.H + h;
                 const uint32_t as = a_it & 1;
                 if (!mbar_wait(&a_empty[as], ((a_it >> 1) & 1) ^ 1, ab)) goto producer_done;
-                mbar_arrive_expect_tx(&a_full[as], kTileBytes);
-                for (int p = 0; p < KP; ++p)
-                    tma_load_2d(smem_u32(smem + C::kA + as * kTileBytes + p * 16384), &tmA, p * 64,
-                                (int32_t)(zh * S + gq * 128), &a_full[as]);
+                mbar_arrive_expect_tx(&a_full[as], a_bytes);
+                if (a_mn) {
+                    // [K rows][128 query columns]: two panels of 64 columns
+                    for (int p = 0; p < 2; ++p)
+                        tma_load_2d(smem_u32(smem + C::kA + as * kTileBytes + p * (kd * 128)), &tmA,
+                                    gq * 128 + 64 * p, (int32_t)(zh * kd), &a_full[as]);
+                } else {
+                    for (int p = 0; p < KP; ++p)
+                        tma_load_2d(smem_u32(smem + C::kA + as * kTileBytes + p * 16384), &tmA, p * 64,
+                                    (int32_t)(zh * S + gq * 128), &a_full[as]);
+                }
                 ++a_it;
                 for (int n = 0; n < ns; ++n, ++g) {
                     const int s = s0 + n;
                     const uint32_t st = g % BST;
                     if (!mbar_wait(&b_empty[st], ((g / BST) & 1) ^ 1, ab)) goto producer_done;
-                    mbar_arrive_expect_tx(&b_full[st], kTileBytes);
+                    mbar_arrive_expect_tx(&b_full[st], b_bytes);
 #pragma unroll
                     for (int b = 0; b < G; ++b) {
                         int c = L.step_col[s * G + b];
                         if (c < 0) c = L.step_col[s * G];
-                        for (int p = 0; p < KP; ++p)
-                            tma_load_2d(smem_u32(smem + C::kB + st * kTileBytes + p * 16384 + b * BLK * 128), &tmB,
-                                        p * 64, (int32_t)(zh * S + (int64_t)c * BLK), &b_full[st]);
+                        if (b_mn) {
+                            // [K rows][B key columns]: KPB panels of W columns
+                            for (int p = 0; p < KPB; ++p)
+                                tma_load_2d(smem_u32(smem + C::kB + st * kTileBytes + (b * KPB + p) * (kd * RB)),
+                                            &tmB, c * BLK + W * p, (int32_t)(zh * kd), &b_full[st]);
+                        } else {
+                            for (int p = 0; p < KP; ++p)
+                                tma_load_2d(smem_u32(smem + C::kB + st * kTileBytes + p * 16384 + b * BLK * 128),
+                                            &tmB, p * 64, (int32_t)(zh * S + (int64_t)c * BLK), &b_full[st]);
+                        }
                     }
                 }
             }
@@ -125,6 +159,10 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         }
     } else if (warp == 1) {
         if (lane == 0) {
+            const uint32_t idesc = idesc_f16(128, 128, std::is_same<T, __nv_bfloat16>::value, a_mn ? 1 : 0, b_mn ? 1 : 0);
+            // 16-deep contraction steps: every K-major panel of 64 (zeros past K)
+            // when both tiles are K-major, else exactly K / 16
+            const int nks = (a_mn || b_mn) ? kd / 16 : KP * 4;
             uint32_t a_it = 0, g = 0;
             for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
                 const int tile = L.tile_order[w / args.Z];
@@ -139,11 +177,13 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     tc_fence_after();
                     const uint32_t abase = smem_u32(smem + C::kA + as * kTileBytes);
                     const uint32_t bbase = smem_u32(smem + C::kB + st * kTileBytes);
-#pragma unroll
-                    for (int ks = 0; ks < KP * 4; ++ks) {
-                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-                        mma_f16(tS + sb * 128, smem_desc(abase + off, 16, 1024, kSw128),
-                                smem_desc(bbase + off, 16, 1024, kSw128), kIdesc, ks > 0 ? 1u : 0u);
+                    for (int ks = 0; ks < nks; ++ks) {
+                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;  // K-major step
+                        const uint64_t da = a_mn ? smem_desc(abase + ks * 2048, kd * 128, 1024, kSw128)
+                                                 : smem_desc(abase + off, 16, 1024, kSw128);
+                        const uint64_t db = b_mn ? smem_desc(bbase + ks * 16 * RB, kd * RB, 8 * RB, swz_of(RB))
+                                                 : smem_desc(bbase + off, 16, 1024, kSw128);
+                        mma_f16(tS + sb * 128, da, db, idesc, ks > 0 ? 1u : 0u);
                     }
                     mma_commit(&s_full[sb]);
                     mma_commit(&b_empty[st]);
@@ -230,14 +270,19 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
 // --------------------------------------------------------------- launch ----
 
 template <typename T, int BLK, int KP>
-int sdd_launch(const bsp_layout_s* Lh, const void* A, const void* B, void* Cout, int Z, int K, cudaStream_t s) {
+int sdd_launch(const bsp_layout_s* Lh, const void* A, const void* B, void* Cout, int Z, int K, int ta, int tb,
+               cudaStream_t s) {
     const int bf = std::is_same<T, __nv_bfloat16>::value;
-    const uint64_t rows = (uint64_t)Z * Lh->H * Lh->S;
+    const uint64_t ZH = (uint64_t)Z * Lh->H, rows = ZH * Lh->S;
+    constexpr int W = BLK < 64 ? BLK : 64;
     CUtensorMap ma, mb;
-    int rc = make_tmap_2d(&ma, A, bf, rows, K, 128, 64, 128);
-    if (!rc) rc = make_tmap_2d(&mb, B, bf, rows, K, BLK, 64, 128);
+    // [S][K] operands: boxes of 128 (A) or B (B) rows x 64 columns; [K][S]
+    // operands: boxes of K rows x 64 (A) or W (B) columns
+    int rc = ta ? make_tmap_2d(&ma, A, bf, ZH * K, Lh->S, K, 64, 128) : make_tmap_2d(&ma, A, bf, rows, K, 128, 64, 128);
+    if (!rc)
+        rc = tb ? make_tmap_2d(&mb, B, bf, rows, K, BLK, 64, 128) : make_tmap_2d(&mb, B, bf, ZH * K, Lh->S, K, W, 2 * W);
     if (rc) return rc;
-    SddArgs a{Lh->view, Cout, Z};
+    SddArgs a{Lh->view, Cout, Z, K, ta, tb};
     auto kern = sdd_tc_kernel<T, BLK, KP>;
     constexpr int smem = SddCfg<KP, BLK>::kAlloc;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -249,18 +294,20 @@ int sdd_launch(const bsp_layout_s* Lh, const void* A, const void* B, void* Cout,
 }
 
 template <typename T, int BLK>
-int sdd_by_k(const bsp_layout_s* L, const void* A, const void* B, void* C, int Z, int K, cudaStream_t s) {
-    if (K <= 64) return sdd_launch<T, BLK, 1>(L, A, B, C, Z, K, s);
-    return sdd_launch<T, BLK, 2>(L, A, B, C, Z, K, s);
+int sdd_by_k(const bsp_layout_s* L, const void* A, const void* B, void* C, int Z, int K, int ta, int tb,
+             cudaStream_t s) {
+    if (K <= 64) return sdd_launch<T, BLK, 1>(L, A, B, C, Z, K, ta, tb, s);
+    return sdd_launch<T, BLK, 2>(L, A, B, C, Z, K, ta, tb, s);
 }
 
 template <typename T>
-int sdd_by_block(const bsp_layout_s* L, const void* A, const void* B, void* C, int Z, int K, cudaStream_t s) {
+int sdd_by_block(const bsp_layout_s* L, const void* A, const void* B, void* C, int Z, int K, int ta, int tb,
+                 cudaStream_t s) {
     switch (L->B) {
-        case 16: return sdd_by_k<T, 16>(L, A, B, C, Z, K, s);
-        case 32: return sdd_by_k<T, 32>(L, A, B, C, Z, K, s);
-        case 64: return sdd_by_k<T, 64>(L, A, B, C, Z, K, s);
-        case 128: return sdd_by_k<T, 128>(L, A, B, C, Z, K, s);
+        case 16: return sdd_by_k<T, 16>(L, A, B, C, Z, K, ta, tb, s);
+        case 32: return sdd_by_k<T, 32>(L, A, B, C, Z, K, ta, tb, s);
+        case 64: return sdd_by_k<T, 64>(L, A, B, C, Z, K, ta, tb, s);
+        case 128: return sdd_by_k<T, 128>(L, A, B, C, Z, K, ta, tb, s);
         default: return BSP_ERR_UNSUPPORTED;
     }
 }
@@ -269,11 +316,13 @@ int sdd_by_block(const bsp_layout_s* L, const void* A, const void* B, void* C, i
 
 int launch_sdd_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z, int K, int ta,
                   int tb, cudaStream_t s) {
-    // scores Q K^T: both operands [S][K] (K-major); K a multiple of 8, at most 128
-    if (ta != 0 || tb != 1 || K % 8 != 0 || K > 128) return BSP_ERR_UNSUPPORTED;
-    if ((uint64_t)Z * L->H * L->S >= (1ull << 31)) return BSP_ERR_UNSUPPORTED;
-    if (dtype == BSP_BF16) return sdd_by_block<__nv_bfloat16>(L, A, B, C, Z, K, s);
-    if (dtype == BSP_F16) return sdd_by_block<__half>(L, A, B, C, Z, K, s);
+    // K at most 128 (one shared-memory tile); both operands [S][K]: K a
+    // multiple of 8 (the row pitch of a TMA map is a multiple of 16 bytes);
+    // an operand stored [K][S]: K a multiple of 16 (its tile has exactly K rows)
+    if (K > 128 || K % 8 != 0 || ((ta || !tb) && K % 16 != 0)) return BSP_ERR_UNSUPPORTED;
+    if ((uint64_t)Z * L->H * std::max(L->S, K) >= (1ull << 31)) return BSP_ERR_UNSUPPORTED;
+    if (dtype == BSP_BF16) return sdd_by_block<__nv_bfloat16>(L, A, B, C, Z, K, ta, tb, s);
+    if (dtype == BSP_F16) return sdd_by_block<__half>(L, A, B, C, Z, K, ta, tb, s);
     return BSP_ERR_UNSUPPORTED;
 }
 

@@ -112,6 +112,27 @@ def test_sdd(bsp, oracle, path, B, dt, trans):
     assert_close(to_np(C), want, dtype, f"sdd B={B} {dt} trans={trans} {path}")
 
 
+@pytest.mark.parametrize("B", [32, 128])
+@pytest.mark.parametrize("K", [16, 40, 48, 96, 128])
+@pytest.mark.parametrize("trans", [(0, 1), (0, 0), (1, 0), (1, 1)])
+def test_sdd_contraction_lengths(bsp, oracle, path, B, K, trans):
+    # the tensor-core kernel takes an operand stored [K][S] for K a multiple
+    # of 16 (K = 40 runs on the CUDA cores); ragged last row tile (S = 5 * 64
+    # or 3 * 128 + ... rows)
+    dtype = torch.bfloat16
+    ta, tb = trans
+    Z, H = 1, 2
+    nb = 10 if B == 32 else 5
+    S = nb * B
+    lay = rlayout(H, nb, 0.4, B + K, diag=True)
+    L = bsp.bsp_layout_compile(lay, B)
+    A = randn((Z, H, K, S) if ta else (Z, H, S, K), dtype, 33)
+    Bm = randn((Z, H, S, K) if tb else (Z, H, K, S), dtype, 34)
+    C = bsp.bsp_sdd(L, dev(A), dev(Bm), trans_a=ta, trans_b=tb)
+    torch.cuda.synchronize()
+    assert_close(to_np(C), oracle.sdd(lay, B, A, Bm, ta, tb), dtype, f"sdd B={B} K={K} trans={trans} {path}")
+
+
 def test_sdd_leaves_absent_blocks_untouched(bsp, path):
     # the output has exactly nnz blocks; guard regions around it keep a canary
     B, H, nb, Z, K = 64, 2, 6, 2, 64
