@@ -16,7 +16,9 @@
 // happens in memory.
 //
 // Roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner and
-// single-thread MMA issuer, warps 2..5 epilogue (thread = TMEM lane).
+// single-thread MMA issuer, warps 2..5 epilogue (thread = TMEM lane).  The
+// epilogue stages each present block's rows in shared memory and writes them
+// with asynchronous bulk copies, so its warps never wait on the global writes.
 #include <algorithm>
 #include <type_traits>
 
@@ -50,14 +52,15 @@ struct SddCfg {
     static constexpr int BST = 3;                    // key-tile stages
     static constexpr int kA = 0;                     // 2 query-tile stages
     static constexpr int kB = 2 * kTile;
-    static constexpr int kPitch = BLK * 2 + 16;      // staging row pitch (padded: no bank conflicts)
-    static constexpr int kStg = kB + BST * kTile;    // per-warp staging, 32 rows
-    static constexpr int kAlloc = kStg + 4 * 32 * kPitch + 1024;
+    static constexpr int kStg = kB + BST * kTile;    // staging: 2 buffers per epilogue warp
+    static constexpr int kBuf = 32 * BLK * 2;        // one buffer: a warp's 32 rows of one block
+    static constexpr int kAlloc = kStg + 4 * 2 * kBuf + 1024;
 };
 
 template <typename T, int BLK, int KP>
 __global__ void __launch_bounds__(kThreads, 1)
-sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const SddArgs args) {
+sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CUtensorMap tmC, const SddArgs args) {
     using C = SddCfg<KP, BLK>;
     constexpr int G = 128 / BLK;
     constexpr int BST = C::BST;
@@ -195,18 +198,28 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         }
     } else {
         // Epilogue: each warp owns 32 rows of the tile (TMEM lanes 32q..32q+31).
-        // Per present block it stages its rows in shared memory, then copies
-        // them out together: the warp's rows of one block are RS = min(32, B)
-        // consecutive rows, i.e. one contiguous RS*B run of the output.
+        // Per present block it stages its rows in one of its two buffers, laid
+        // out as the output rows they become (RS = min(32, B) consecutive rows
+        // of one output block per copy unit), and lane 0 issues the copies: a
+        // 128-byte-swizzled tensor store per 64 columns for blocks of 64 and
+        // 128 (conflict-free row-per-lane staging), one contiguous bulk copy
+        // otherwise.  Before refilling a buffer the warp waits only until the
+        // copy issued from it two uses ago has read it.
         constexpr int RS = BLK < 32 ? BLK : 32;
-        constexpr int C16 = BLK * 2 / 16;  // 16-byte chunks per block row
+        constexpr int BW = BLK < 64 ? BLK : 64;  // columns per staged row of one box
+        constexpr int RBY = BW * 2;              // bytes per such row
+        constexpr int NBX = BLK / BW;            // boxes across a block row
+        constexpr int C16 = BLK * 2 / 16;        // 16-byte chunks per block row
+        constexpr int kSeg = RS * BLK * 2;       // one copy unit
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const int a = row / BLK;
-        uint8_t* stg = smem + C::kStg + quad * 32 * C::kPitch;
+        const int seg = lane / RS, rin = lane % RS;
+        uint8_t* stg = smem + C::kStg + quad * 2 * C::kBuf;
         T* Cp = reinterpret_cast<T*>(args.C);
-        uint32_t g = 0;
+        if (lane == 0) tma_prefetch_desc(&tmC);
+        uint32_t g = 0, uses = 0;
         for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
             const int tile = L.tile_order[w / args.Z];
             const int z = (int)(w % args.Z);
@@ -230,34 +243,51 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 for (int b = 0; b < G; ++b) {
                     const int blk = L.step_blk[(s * G + a) * G + b];
                     if (__all_sync(0xffffffffu, blk < 0)) continue;
+                    int sblk[32 / RS];
+#pragma unroll
+                    for (int sg = 0; sg < 32 / RS; ++sg) sblk[sg] = __shfl_sync(0xffffffffu, blk, sg * RS);
+                    uint8_t* buf = stg + (uses & 1) * C::kBuf;
+                    if (lane == 0) bulk_wait_read<1>();  // the copy from this buffer two uses ago has read it
+                    __syncwarp();
                     if (blk >= 0) {
-                        uint4* srow = reinterpret_cast<uint4*>(stg + lane * C::kPitch);
+                        uint8_t* rbase = buf + seg * kSeg + rin * RBY;
 #pragma unroll
                         for (int j = 0; j < C16; ++j) {
                             const int o = b * BLK + 8 * j;
-                            srow[j] = make_uint4(
+                            const int box = j / (BW / 8), jj = j % (BW / 8);
+                            const int pos = BLK >= 64 ? (jj ^ (rin & 7)) : jj;
+                            *reinterpret_cast<uint4*>(rbase + box * (RS * RBY) + pos * 16) = make_uint4(
                                 Pack2<T>::pack(__uint_as_float(x[o]), __uint_as_float(x[o + 1])),
                                 Pack2<T>::pack(__uint_as_float(x[o + 2]), __uint_as_float(x[o + 3])),
                                 Pack2<T>::pack(__uint_as_float(x[o + 4]), __uint_as_float(x[o + 5])),
                                 Pack2<T>::pack(__uint_as_float(x[o + 6]), __uint_as_float(x[o + 7])));
                         }
                     }
+                    fence_proxy_async_smem();
                     __syncwarp();
+                    if (lane == 0) {
 #pragma unroll
-                    for (int seg = 0; seg < 32 / RS; ++seg) {
-                        const int sblk = __shfl_sync(0xffffffffu, blk, seg * RS);
-                        if (sblk < 0) continue;
-                        const int r_in0 = (quad * 32 + seg * RS) % BLK;
-                        uint4* dst = reinterpret_cast<uint4*>(Cp + (((int64_t)z * L.nnz + sblk) * BLK + r_in0) * BLK);
-                        for (int k = lane; k < RS * C16; k += 32)
-                            dst[k] = *reinterpret_cast<const uint4*>(stg + (seg * RS + k / C16) * C::kPitch +
-                                                                     (k % C16) * 16);
+                        for (int sg = 0; sg < 32 / RS; ++sg) {
+                            if (sblk[sg] < 0) continue;
+                            const int r_in0 = (quad * 32 + sg * RS) % BLK;
+                            const int64_t orow = ((int64_t)z * L.nnz + sblk[sg]) * BLK + r_in0;
+                            if (BLK >= 64) {
+#pragma unroll
+                                for (int bx = 0; bx < NBX; ++bx)
+                                    tma_store_3d(&tmC, smem_u32(buf + sg * kSeg + bx * (RS * RBY)), bx * BW,
+                                                 (int32_t)orow, 0);
+                            } else {
+                                bulk_store(Cp + orow * BLK, smem_u32(buf + sg * kSeg), kSeg);
+                            }
+                        }
+                        bulk_commit();
                     }
-                    __syncwarp();
+                    ++uses;
                 }
             }
         }
-    epi_done:;
+    epi_done:
+        if (lane == 0) bulk_wait_all();
     }
     tc_fence_before();
     __syncthreads();
@@ -275,12 +305,17 @@ int sdd_launch(const bsp_layout_s* Lh, const void* A, const void* B, void* Cout,
     const int bf = std::is_same<T, __nv_bfloat16>::value;
     const uint64_t ZH = (uint64_t)Z * Lh->H, rows = ZH * Lh->S;
     constexpr int W = BLK < 64 ? BLK : 64;
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mc;
     // [S][K] operands: boxes of 128 (A) or B (B) rows x 64 columns; [K][S]
     // operands: boxes of K rows x 64 (A) or W (B) columns
     int rc = ta ? make_tmap_2d(&ma, A, bf, ZH * K, Lh->S, K, 64, 128) : make_tmap_2d(&ma, A, bf, rows, K, 128, 64, 128);
     if (!rc)
         rc = tb ? make_tmap_2d(&mb, B, bf, rows, K, BLK, 64, 128) : make_tmap_2d(&mb, B, bf, ZH * K, Lh->S, K, W, 2 * W);
+    // output rows: [Z * nnz * B][B], boxes of min(32, B) rows x W columns
+    // (128-byte swizzle for W = 64)
+    if (!rc)
+        rc = make_tmap_3d(&mc, Cout, bf, BLK, (uint64_t)Z * Lh->nnz * BLK, 1, W, BLK < 32 ? BLK : 32,
+                          BLK >= 64 ? 128 : 0);
     if (rc) return rc;
     SddArgs a{Lh->view, Cout, Z, K, ta, tb};
     auto kern = sdd_tc_kernel<T, BLK, KP>;
@@ -289,7 +324,7 @@ int sdd_launch(const bsp_layout_s* Lh, const void* A, const void* B, void* Cout,
         return BSP_ERR_CUDA;
     const int64_t total = (int64_t)Z * Lh->n_tiles;
     const int grid = (int)std::min<int64_t>(total, sm_count());
-    kern<<<grid, kThreads, smem, s>>>(ma, mb, a);
+    kern<<<grid, kThreads, smem, s>>>(ma, mb, mc, a);
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }
 
