@@ -38,6 +38,7 @@
 #ifndef BSP_H
 #define BSP_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -285,6 +286,26 @@ int bsp_softmax_backward(bsp_layout_t layout, int dtype, const void* Y, const vo
 int bsp_attention_backward(bsp_layout_t layout, int dtype, const void* Q, const void* K, const void* V,
                            const void* dO, void* dQ, void* dK, void* dV, int Z, int D, float scale,
                            int mask_kind, const uint8_t* mask, void* P_ws, void* dP_ws, void* stream);
+
+/* Attention on HOST tensors (Q, K, V, O as in bsp_attention, in host memory;
+ * pinned memory lets the copies overlap the kernels, pageable memory works
+ * but serialises them).  The batch is processed in slices of whole batch
+ * entries (at least two slices when Z >= 2, as many entries per slice as the
+ * workspace holds) through a caller-owned DEVICE workspace (256-byte aligned,
+ * bsp_attention_host_workspace(layout, dtype, D, z_slice) bytes for slices of
+ * z_slice entries); each slice's host-to-device copies, kernel and
+ * device-to-host copy run on three streams owned by the handle, so copies of
+ * neighbouring slices overlap each kernel.  Asynchronous like the other
+ * calls: it starts after the work queued on `stream` and `stream` waits for
+ * its end; the host buffers and the workspace must stay valid until then.
+ * mask: DEVICE [S][S] as in bsp_attention.  Calls that share a handle must
+ * not run concurrently from several host threads.  Workspace smaller than
+ * one slice: BSP_ERR_INVALID_ARG.  (Not from the pages: the end-to-end path
+ * through host memory.) */
+int bsp_attention_host(bsp_layout_t layout, int dtype, const void* Q, const void* K, const void* V, void* O,
+                       int Z, int D, float scale, int mask_kind, const uint8_t* mask, void* workspace,
+                       size_t workspace_bytes, void* stream);
+size_t bsp_attention_host_workspace(bsp_layout_t layout, int dtype, int D, int z_slice);
 
 /* ---- diagnostics ------------------------------------------------------- */
 

@@ -64,6 +64,9 @@ def lib():
         L.bsp_layout_groups.argtypes = [P, i32, P, P, P, P, P, P, P]
         L.bsp_layout_geometry.argtypes = [P, P, P]
         L.bsp_layout_compile_affine.argtypes = [P, P, i32, i32, i32, P, ctypes.POINTER(P)]
+        L.bsp_attention_host.argtypes = [P, i32, P, P, P, P, i32, i32, f32, i32, P, P, ctypes.c_size_t, P]
+        L.bsp_attention_host_workspace.argtypes = [P, i32, i32, i32]
+        L.bsp_attention_host_workspace.restype = ctypes.c_size_t
         L.bsp_status_check.argtypes = [P, P]
         L.bsp_status_string.restype = ctypes.c_char_p
         L.bsp_status_string.argtypes = [i32]
@@ -72,7 +75,7 @@ def lib():
                      "bsp_layout_info",
                      "bsp_layout_get_luts", "bsp_layout_tiles", "bsp_sdd", "bsp_dsd", "bsp_dds", "bsp_softmax",
                      "bsp_attention", "bsp_softmax_backward", "bsp_attention_backward", "bsp_layout_groups",
-                     "bsp_status_check", "bsp_layout_geometry", "bsp_layout_compile_affine"):
+                     "bsp_status_check", "bsp_layout_geometry", "bsp_layout_compile_affine", "bsp_attention_host"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -292,6 +295,32 @@ def bsp_attention(L: Layout, Q, K, V, O=None, scale: float = 1.0, mask_kind: int
     _check(lib().bsp_attention(L.handle, dt, _ptr(Q), _ptr(K), _ptr(V), _ptr(O), Q.shape[0], Q.shape[3],
                                float(scale), int(mask_kind), _ptr(mask), _stream(stream)),
            "bsp_attention")
+    return O
+
+
+def bsp_attention_host_workspace(L: Layout, dtype, D: int, z_slice: int) -> int:
+    """Device workspace bytes of bsp_attention_host for slices of z_slice batch entries."""
+    return int(lib().bsp_attention_host_workspace(L.handle, _DTYPES[dtype], int(D), int(z_slice)))
+
+
+def bsp_attention_host(L: Layout, Q, K, V, O=None, scale: float = 1.0, mask_kind: int = MASK_NONE,
+                       mask=None, workspace=None, stream=None):
+    """Fused attention on HOST tensors Q, K, V (O allocated pinned when None);
+    the library copies slices of the batch in and out on its own streams,
+    overlapped with the kernels.  workspace: device uint8 tensor (allocated for
+    slices of one batch entry when None)."""
+    if O is None:
+        O = torch.empty(Q.shape, dtype=Q.dtype, pin_memory=True)
+    if any(t.is_cuda for t in (Q, K, V, O)):
+        raise ValueError("bsp_attention_host takes host tensors")
+    dt = _dtype(Q, K, V, O)
+    if workspace is None:
+        nbytes = bsp_attention_host_workspace(L, Q.dtype, Q.shape[3], 1)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    _check(lib().bsp_attention_host(L.handle, dt, _ptr(Q), _ptr(K), _ptr(V), _ptr(O), Q.shape[0], Q.shape[3],
+                                    float(scale), int(mask_kind), _ptr(mask), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream)),
+           "bsp_attention_host")
     return O
 
 

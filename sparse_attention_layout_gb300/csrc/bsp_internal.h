@@ -83,6 +83,8 @@ struct bsp_layout_s {
     std::vector<bsp_affine_term_t> geo_terms;  // [H * BSP_MAX_AFFINE_TERMS]
     std::vector<int32_t> geo_rec;              // [H * kGeoRec] or empty
     void* geo_dmem = nullptr;
+    // streams and events of bsp_attention_host (created on first use)
+    struct HostPipe* pipe = nullptr;
 };
 
 constexpr int kGeoRec = 8;  // ints per head in LayoutView::geo
@@ -122,6 +124,9 @@ int launch_softmax_backward(const bsp_layout_s* L, int dtype, const void* Y, con
                             float scale, cudaStream_t s);
 
 int sm_count();  // multiprocessors of the current device (cached per device)
+
+// streams and events of bsp_attention_host (host_pipeline.cpp)
+void host_pipe_destroy(bsp_layout_s* L);
 
 // affine geometry (geometry.cpp)
 int affine_validate(int nb, int n, const bsp_affine_term_t* t);

@@ -180,6 +180,10 @@ def test_compute_calls_reject_host_only_handle(lib):
     assert lib.bsp_softmax(L.handle, 1, a, a, 1, ctypes.c_float(1.0), 0, None, None) == -1
     assert lib.bsp_attention(L.handle, 1, a, a, a, a, 1, 64, ctypes.c_float(1.0), 0, None, None) == -1
     assert lib.bsp_status_check(L.handle, None) == -1
+    assert lib.bsp_attention_host(L.handle, 1, a, a, a, a, 1, 64, ctypes.c_float(1.0), 0, None, a,
+                                  ctypes.c_size_t(1 << 20), None) == -1
+    # workspace for slices of one batch entry: 2 slots x (Q, K, V, O) x H S D x 2 bytes
+    assert lib.bsp_attention_host_workspace(L.handle, 1, 64, 1) == 2 * 4 * 1 * 32 * 64 * 2
     assert lib.bsp_sdd(None, 1, a, a, a, 1, 16, 0, 1, None) == -1
     assert lib.bsp_layout_destroy(None) == 0
 
