@@ -307,6 +307,12 @@ def per_op_section(w, lay, L, q, k, v, pk, bsp, stream):
     out["dsd"] = {"ms": ms, "TFLOP/s": 2.0 * B * B * D * nnz * Z / ms / 1e9}
     ms = time_launches(lambda: bsp.attention_unfused(L, q, k, v, w.scale, w.mask_kind), 5, stream)
     out["attention_unfused_chain"] = {"ms": ms, "TFLOP/s": nonzero_flops(lay, B, D, Z) / ms / 1e9}
+    # SDD and softmax fused (scores never in HBM), then DSD
+    ms = time_launches(lambda: bsp.bsp_sdd_softmax(L, q, k, P, w.scale, w.mask_kind), 10, stream)
+    out["sdd_softmax"] = {"ms": ms, "GB/s_of_P": (Z * nnz * B * B * elt) / ms / 1e6}
+    ms = time_launches(lambda: bsp.bsp_dsd(L, bsp.bsp_sdd_softmax(L, q, k, P, w.scale, w.mask_kind), v, O), 5,
+                       stream)
+    out["attention_sdd_softmax_dsd"] = {"ms": ms, "TFLOP/s": nonzero_flops(lay, B, D, Z) / ms / 1e9}
     # backward: softmax backward on the chain's P, and the whole attention
     # backward (recomputes P; 5 block matmuls of 2 B^2 D each per block)
     dY = torch.randn_like(P)

@@ -200,6 +200,17 @@ int bsp_layout_groups(bsp_layout_t layout, int orient, int* G, int* n_groups, in
 int bsp_sdd(bsp_layout_t layout, int dtype, const void* A, const void* B, void* C,
             int Z, int K, int trans_a, int trans_b, void* stream);
 
+/* Fused SDD + row softmax: P = softmax(scale * SDD(op(A), op(B))) on the
+ * layout's blocks, with the mask kinds and masked-entry rules of
+ * bsp_softmax, in one pass whose scores never reach memory (tensor cores for
+ * bf16 / fp16 and the shapes bsp_sdd runs there; otherwise bsp_sdd followed by
+ * bsp_softmax in place).  Arguments as bsp_sdd (P is its C: [Z][nnz][B][B]),
+ * plus scale > 0, mask_kind and mask as bsp_softmax.  This is the first two
+ * steps of the unfused attention chain of "question on blocksparse" (issue
+ * 117) fused; the result equals bsp_softmax(bsp_sdd(...)) up to rounding. */
+int bsp_sdd_softmax(bsp_layout_t layout, int dtype, const void* A, const void* B, void* P, int Z, int K,
+                    int trans_a, int trans_b, float scale, int mask_kind, const uint8_t* mask, void* stream);
+
 /* DSD: C = op(A_sp) . op(B), A_sp the S x S block-sparse matrix.
  * A_sp: [Z][nnz][block][block]; trans_a = 1 uses its transpose.
  * B: [Z][H][S][N] (trans_b = 0) or [Z][H][N][S] (trans_b = 1).
@@ -277,7 +288,8 @@ int bsp_softmax_backward(bsp_layout_t layout, int dtype, const void* Y, const vo
  *     P = softmax(scale Q K^T on the layout and mask)   (recomputed)
  *     dV = P^T dO,  dP = dO V^T (on the layout),  dX = bsp_softmax_backward(P, dP),
  *     dQ = dX K,  dK = dX^T Q
- * of this library's SDD, softmax, softmax backward and DSD calls, enqueued on
+ * of this library's fused SDD + softmax, DSD, SDD and softmax backward calls
+ * (bsp_sdd_softmax, bsp_dsd, bsp_sdd, bsp_softmax_backward), enqueued on
  * `stream`.  Q, K, V, dO, dQ, dK, dV: DEVICE [Z][H][S][D], D and the mask as for
  * bsp_attention.  P_ws, dP_ws: caller-owned DEVICE workspace of Z * nnz *
  * block * block elements each (P and dP / dX live there afterwards); they may

@@ -55,6 +55,7 @@ def lib():
         L.bsp_layout_get_luts.argtypes = [P] * 7
         L.bsp_layout_tiles.argtypes = [P] * 8
         L.bsp_sdd.argtypes = [P, i32, P, P, P, i32, i32, i32, i32, P]
+        L.bsp_sdd_softmax.argtypes = [P, i32, P, P, P, i32, i32, i32, i32, f32, i32, P, P]
         L.bsp_dsd.argtypes = [P, i32, P, P, P, i32, i32, i32, i32, P]
         L.bsp_dds.argtypes = [P, i32, P, P, P, i32, i32, i32, i32, P]
         L.bsp_softmax.argtypes = [P, i32, P, P, i32, f32, i32, P, P]
@@ -75,7 +76,7 @@ def lib():
                      "bsp_layout_info",
                      "bsp_layout_get_luts", "bsp_layout_tiles", "bsp_sdd", "bsp_dsd", "bsp_dds", "bsp_softmax",
                      "bsp_attention", "bsp_softmax_backward", "bsp_attention_backward", "bsp_layout_groups",
-                     "bsp_status_check", "bsp_layout_geometry", "bsp_layout_compile_affine", "bsp_attention_host"):
+                     "bsp_status_check", "bsp_layout_geometry", "bsp_layout_compile_affine", "bsp_attention_host", "bsp_sdd_softmax"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -249,6 +250,19 @@ def bsp_sdd(L: Layout, A, B, C=None, trans_a: int = 0, trans_b: int = 1, stream=
     _check(lib().bsp_sdd(L.handle, dt, _ptr(A), _ptr(B), _ptr(C), Z, K, int(trans_a), int(trans_b),
                          _stream(stream)), "bsp_sdd")
     return C
+
+
+def bsp_sdd_softmax(L: Layout, A, B, P=None, scale: float = 1.0, mask_kind: int = MASK_NONE, mask=None,
+                    trans_a: int = 0, trans_b: int = 1, stream=None):
+    """P = softmax(scale * SDD(op(A), op(B))) in one fused pass."""
+    Z = A.shape[0]
+    K = A.shape[2] if trans_a else A.shape[3]
+    if P is None:
+        P = torch.empty((Z, L.nnz, L.B, L.B), dtype=A.dtype, device=A.device)
+    dt = _dtype(A, B, P)
+    _check(lib().bsp_sdd_softmax(L.handle, dt, _ptr(A), _ptr(B), _ptr(P), Z, K, int(trans_a), int(trans_b),
+                                 float(scale), int(mask_kind), _ptr(mask), _stream(stream)), "bsp_sdd_softmax")
+    return P
 
 
 def bsp_dsd(L: Layout, A_sp, B, C=None, trans_a: int = 0, trans_b: int = 0, stream=None):

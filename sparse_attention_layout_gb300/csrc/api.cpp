@@ -70,6 +70,29 @@ extern "C" int bsp_sdd(bsp_layout_t L, int dtype, const void* A, const void* B, 
     return bsp::launch_sdd_simt(L, dtype, A, B, C, Z, K, trans_a, trans_b, s);
 }
 
+extern "C" int bsp_sdd_softmax(bsp_layout_t L, int dtype, const void* A, const void* B, void* P, int Z, int K,
+                               int trans_a, int trans_b, float scale, int mask_kind, const uint8_t* mask,
+                               void* stream) {
+    int rc = check_common(L, dtype, Z, {A, B, P});
+    if (rc) return rc;
+    if (Z < 0 || K < 1 || (trans_a & ~1) || (trans_b & ~1) || !valid_kind(mask_kind) || !(scale > 0.f) ||
+        scale > 3.0e38f)
+        return BSP_ERR_INVALID_ARG;
+    if (mask_kind == BSP_MASK_DENSE && !mask) return BSP_ERR_INVALID_ARG;
+    if (mask_kind == BSP_MASK_DENSE && ((uintptr_t)mask & 15u)) return BSP_ERR_ALIGNMENT;
+    if (Z == 0 || L->nnz == 0) return BSP_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    const uint8_t* m = mask_kind == BSP_MASK_DENSE ? mask : nullptr;
+    if (!force_simt()) {
+        rc = bsp::launch_sdd_softmax_tc(L, dtype, A, B, P, Z, K, trans_a, trans_b, scale, mask_kind, m, s);
+        if (rc != BSP_ERR_UNSUPPORTED) return rc;
+    }
+    // the two steps one after the other (scores through HBM, softmax in place)
+    rc = bsp_sdd(L, dtype, A, B, P, Z, K, trans_a, trans_b, stream);
+    if (rc) return rc;
+    return bsp::launch_softmax(L, dtype, P, P, Z, scale, mask_kind, m, s);
+}
+
 extern "C" int bsp_dsd(bsp_layout_t L, int dtype, const void* A_sp, const void* B, void* C, int Z,
                        int N, int trans_a, int trans_b, void* stream) {
     int rc = check_common(L, dtype, Z, {A_sp, B, C});
@@ -190,9 +213,9 @@ extern "C" int bsp_attention_backward(bsp_layout_t L, int dtype, const void* Q, 
     }
     if (!P_ws || !dP_ws) return BSP_ERR_INVALID_ARG;
     if (!aligned16(P_ws) || !aligned16(dP_ws)) return BSP_ERR_ALIGNMENT;
-    // P = softmax(scale Q K^T) on the layout, as the forward computes it
-    if ((rc = bsp_sdd(L, dtype, Q, K, P_ws, Z, D, 0, 1, stream))) return rc;
-    if ((rc = bsp_softmax(L, dtype, P_ws, P_ws, Z, scale, mask_kind, mask, stream))) return rc;
+    // P = softmax(scale Q K^T) on the layout, as the forward computes it (one
+    // fused pass: the scores never reach memory)
+    if ((rc = bsp_sdd_softmax(L, dtype, Q, K, P_ws, Z, D, 0, 1, scale, mask_kind, mask, stream))) return rc;
     // dV = P^T dO
     if ((rc = bsp_dsd(L, dtype, P_ws, dO, dV, Z, D, 1, 0, stream))) return rc;
     // dP = dO V^T on the layout, then the gradient of the raw scores Q K^T in place

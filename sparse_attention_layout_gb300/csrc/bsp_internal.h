@@ -114,6 +114,9 @@ int launch_attention_tc(const bsp_layout_s* L, int dtype, const void* Q, const v
                         const uint8_t* mask, cudaStream_t s);
 int launch_sdd_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z,
                   int K, int ta, int tb, cudaStream_t s);
+// fused SDD + row softmax (P = softmax(scale * SDD) on the layout's blocks)
+int launch_sdd_softmax_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* P, int Z, int K,
+                          int ta, int tb, float scale, int kind, const uint8_t* mask, cudaStream_t s);
 int launch_dsd_group_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z,
                         int N, int ta, int tb, cudaStream_t s);
 int launch_dds_group_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z,

@@ -19,6 +19,15 @@
 // single-thread MMA issuer, warps 2..5 epilogue (thread = TMEM lane).  The
 // epilogue stages each present block's rows in shared memory and writes them
 // with asynchronous bulk copies, so its warps never wait on the global writes.
+//
+// SMX (fused SDD + row softmax): the whole key stream of a row tile is one
+// CTA's, and an epilogue thread owns one query row, so the row softmax fits
+// in the epilogue: every tile's steps run twice, the first pass keeping each
+// row's running max and sum of 2^(scale log2(e) s - max) (masked entries
+// excluded), the second recomputing the scores and writing
+// P = 2^(scale log2(e) s - max) / sum instead of S.  The scores never reach
+// HBM; the second pass repeats the matrix products, which cost less than the
+// round trip of S they replace.
 #include <algorithm>
 #include <type_traits>
 
@@ -40,6 +49,10 @@ struct SddArgs {
     int Z;
     int kd;      // contraction length K
     int ta, tb;  // trans flags (ta = 1: A tile MN-major; tb = 0: B tile MN-major)
+    // fused softmax only: scale * log2(e), mask kind, dense keep-mask [S][S]
+    float c2;
+    int kind;
+    const uint8_t* mask;
 };
 
 __host__ __device__ constexpr uint32_t swz_of(int row_bytes) {
@@ -57,7 +70,7 @@ struct SddCfg {
     static constexpr int kAlloc = kStg + 4 * 2 * kBuf + 1024;
 };
 
-template <typename T, int BLK, int KP>
+template <typename T, int BLK, int KP, bool SMX>
 __global__ void __launch_bounds__(kThreads, 1)
 sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, const SddArgs args) {
@@ -72,6 +85,7 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     // bytes one stage's copies deliver: K-major boxes are 64 * KP columns wide
     // (zero-filled past K), MN-major ones exactly K rows
     const uint32_t a_bytes = a_mn ? 256u * kd : kTileBytes, b_bytes = b_mn ? 256u * kd : kTileBytes;
+    constexpr int NPASS = SMX ? 2 : 1;  // passes over a tile's steps
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -136,8 +150,8 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                                     (int32_t)(zh * S + gq * 128), &a_full[as]);
                 }
                 ++a_it;
-                for (int n = 0; n < ns; ++n, ++g) {
-                    const int s = s0 + n;
+                for (int it = 0; it < NPASS * ns; ++it, ++g) {
+                    const int s = s0 + it % ns;
                     const uint32_t st = g % BST;
                     if (!mbar_wait(&b_empty[st], ((g / BST) & 1) ^ 1, ab)) goto producer_done;
                     mbar_arrive_expect_tx(&b_full[st], b_bytes);
@@ -173,7 +187,7 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 if (ns == 0) continue;
                 const uint32_t as = a_it & 1;
                 if (!mbar_wait(&a_full[as], (a_it >> 1) & 1, ab)) goto mma_done;
-                for (int n = 0; n < ns; ++n, ++g) {
+                for (int it = 0; it < NPASS * ns; ++it, ++g) {
                     const uint32_t sb = g & 3, st = g % BST;  // TMEM accumulator, key-tile stage
                     if (!mbar_wait(&s_empty[sb], ((g >> 2) & 1) ^ 1, ab)) goto mma_done;
                     if (!mbar_wait(&b_full[st], (g / BST) & 1, ab)) goto mma_done;
@@ -190,7 +204,7 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     }
                     mma_commit(&s_full[sb]);
                     mma_commit(&b_empty[st]);
-                    if (n == ns - 1) mma_commit(&a_empty[as]);
+                    if (it == NPASS * ns - 1) mma_commit(&a_empty[as]);
                 }
                 ++a_it;
             }
@@ -224,8 +238,12 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             const int tile = L.tile_order[w / args.Z];
             const int z = (int)(w % args.Z);
             const int s0 = L.tile_step_ptr[tile], ns = L.tile_step_ptr[tile + 1] - s0;
-            for (int n = 0; n < ns; ++n, ++g) {
-                const int s = s0 + n;
+            // fused softmax: this row's running max (scaled log2 domain) and sum
+            const int gq = tile % L.ngroups, rb = gq * G + a, r_in = row % BLK;
+            float m = -INFINITY, l = 0.f, msub = 0.f, inv = 0.f;
+            for (int it = 0; it < NPASS * ns; ++it, ++g) {
+                const int n = it % ns, s = s0 + n;
+                const bool write = !SMX || it >= ns;  // the pass that writes
                 const uint32_t sb = g & 3;
                 bool ok = mbar_wait(&s_full[sb], (g >> 2) & 1, ab);
                 if (!__all_sync(0xffffffffu, ok)) goto epi_done;
@@ -239,6 +257,54 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s_empty[sb]);
+                if constexpr (SMX) {
+                    // masked entries -> -inf: absent (row block, key block) pairs,
+                    // columns past the diagonal inside diagonal blocks, dense-mask zeros
+                    float* xf = reinterpret_cast<float*>(x);
+#pragma unroll
+                    for (int b = 0; b < G; ++b) {
+                        const int blk = L.step_blk[(s * G + a) * G + b];
+                        const int col = L.step_col[s * G + b];
+                        const int lim = blk < 0 ? -1 : ((args.kind == BSP_MASK_DIAG_CAUSAL && col == rb) ? r_in : BLK);
+                        if (__any_sync(0xffffffffu, lim < BLK - 1)) {
+#pragma unroll
+                            for (int j = 0; j < BLK; ++j) xf[b * BLK + j] = j > lim ? -INFINITY : xf[b * BLK + j];
+                        }
+                        if (args.kind == BSP_MASK_DENSE && blk >= 0) {
+                            const uint8_t* mp = args.mask + (int64_t)(gq * 128 + row) * S + (int64_t)col * BLK;
+#pragma unroll
+                            for (int q = 0; q < BLK / 16; ++q) {
+                                const uint4 mv = *reinterpret_cast<const uint4*>(mp + q * 16);
+                                const uint8_t* mb = reinterpret_cast<const uint8_t*>(&mv);
+#pragma unroll
+                                for (int k = 0; k < 16; ++k)
+                                    if (!mb[k]) xf[b * BLK + q * 16 + k] = -INFINITY;
+                            }
+                        }
+                    }
+                    if (!write) {
+                        // first pass: running max and sum
+                        float mx = -INFINITY;
+#pragma unroll
+                        for (int j = 0; j < 128; ++j) mx = fmaxf(mx, xf[j]);
+                        const float mn = fmaxf(m, mx * args.c2);
+                        if (mn != -INFINITY) {
+                            float acc = 0.f;
+#pragma unroll
+                            for (int j = 0; j < 128; ++j) acc += ex2_approx(fmaf(xf[j], args.c2, -mn));
+                            l = (m == -INFINITY ? 0.f : l * ex2_approx(m - mn)) + acc;
+                            m = mn;
+                        }
+                        if (it == ns - 1) {
+                            msub = m == -INFINITY ? 0.f : m;
+                            inv = l > 0.f ? 1.0f / l : 0.f;
+                        }
+                        continue;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 128; ++j) xf[j] = ex2_approx(fmaf(xf[j], args.c2, -msub)) * inv;
+                }
+
 #pragma unroll
                 for (int b = 0; b < G; ++b) {
                     const int blk = L.step_blk[(s * G + a) * G + b];
@@ -299,9 +365,9 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
 
 // --------------------------------------------------------------- launch ----
 
-template <typename T, int BLK, int KP>
+template <typename T, int BLK, int KP, bool SMX>
 int sdd_launch(const bsp_layout_s* Lh, const void* A, const void* B, void* Cout, int Z, int K, int ta, int tb,
-               cudaStream_t s) {
+               float c2, int kind, const uint8_t* mask, cudaStream_t s) {
     const int bf = std::is_same<T, __nv_bfloat16>::value;
     const uint64_t ZH = (uint64_t)Z * Lh->H, rows = ZH * Lh->S;
     constexpr int W = BLK < 64 ? BLK : 64;
@@ -317,8 +383,8 @@ int sdd_launch(const bsp_layout_s* Lh, const void* A, const void* B, void* Cout,
         rc = make_tmap_3d(&mc, Cout, bf, BLK, (uint64_t)Z * Lh->nnz * BLK, 1, W, BLK < 32 ? BLK : 32,
                           BLK >= 64 ? 128 : 0);
     if (rc) return rc;
-    SddArgs a{Lh->view, Cout, Z, K, ta, tb};
-    auto kern = sdd_tc_kernel<T, BLK, KP>;
+    SddArgs a{Lh->view, Cout, Z, K, ta, tb, c2, kind, mask};
+    auto kern = sdd_tc_kernel<T, BLK, KP, SMX>;
     constexpr int smem = SddCfg<KP, BLK>::kAlloc;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return BSP_ERR_CUDA;
@@ -328,36 +394,50 @@ int sdd_launch(const bsp_layout_s* Lh, const void* A, const void* B, void* Cout,
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }
 
-template <typename T, int BLK>
-int sdd_by_k(const bsp_layout_s* L, const void* A, const void* B, void* C, int Z, int K, int ta, int tb,
-             cudaStream_t s) {
-    if (K <= 64) return sdd_launch<T, BLK, 1>(L, A, B, C, Z, K, ta, tb, s);
-    return sdd_launch<T, BLK, 2>(L, A, B, C, Z, K, ta, tb, s);
+template <typename T, int BLK, bool SMX>
+int sdd_by_k(const bsp_layout_s* L, const void* A, const void* B, void* C, int Z, int K, int ta, int tb, float c2,
+             int kind, const uint8_t* mask, cudaStream_t s) {
+    if (K <= 64) return sdd_launch<T, BLK, 1, SMX>(L, A, B, C, Z, K, ta, tb, c2, kind, mask, s);
+    return sdd_launch<T, BLK, 2, SMX>(L, A, B, C, Z, K, ta, tb, c2, kind, mask, s);
 }
 
-template <typename T>
+template <typename T, bool SMX>
 int sdd_by_block(const bsp_layout_s* L, const void* A, const void* B, void* C, int Z, int K, int ta, int tb,
-                 cudaStream_t s) {
+                 float c2, int kind, const uint8_t* mask, cudaStream_t s) {
     switch (L->B) {
-        case 16: return sdd_by_k<T, 16>(L, A, B, C, Z, K, ta, tb, s);
-        case 32: return sdd_by_k<T, 32>(L, A, B, C, Z, K, ta, tb, s);
-        case 64: return sdd_by_k<T, 64>(L, A, B, C, Z, K, ta, tb, s);
-        case 128: return sdd_by_k<T, 128>(L, A, B, C, Z, K, ta, tb, s);
+        case 16: return sdd_by_k<T, 16, SMX>(L, A, B, C, Z, K, ta, tb, c2, kind, mask, s);
+        case 32: return sdd_by_k<T, 32, SMX>(L, A, B, C, Z, K, ta, tb, c2, kind, mask, s);
+        case 64: return sdd_by_k<T, 64, SMX>(L, A, B, C, Z, K, ta, tb, c2, kind, mask, s);
+        case 128: return sdd_by_k<T, 128, SMX>(L, A, B, C, Z, K, ta, tb, c2, kind, mask, s);
         default: return BSP_ERR_UNSUPPORTED;
     }
+}
+
+// shapes the tensor-core SDD covers: K at most 128 (one shared-memory tile);
+// both operands [S][K]: K a multiple of 8 (the row pitch of a TMA map is a
+// multiple of 16 bytes); an operand stored [K][S]: K a multiple of 16 (its
+// tile has exactly K rows)
+bool sdd_tc_shape(const bsp_layout_s* L, int Z, int K, int ta, int tb) {
+    if (K > 128 || K % 8 != 0 || ((ta || !tb) && K % 16 != 0)) return false;
+    return (uint64_t)Z * L->H * std::max(L->S, K) < (1ull << 31);
 }
 
 }  // namespace
 
 int launch_sdd_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z, int K, int ta,
                   int tb, cudaStream_t s) {
-    // K at most 128 (one shared-memory tile); both operands [S][K]: K a
-    // multiple of 8 (the row pitch of a TMA map is a multiple of 16 bytes);
-    // an operand stored [K][S]: K a multiple of 16 (its tile has exactly K rows)
-    if (K > 128 || K % 8 != 0 || ((ta || !tb) && K % 16 != 0)) return BSP_ERR_UNSUPPORTED;
-    if ((uint64_t)Z * L->H * std::max(L->S, K) >= (1ull << 31)) return BSP_ERR_UNSUPPORTED;
-    if (dtype == BSP_BF16) return sdd_by_block<__nv_bfloat16>(L, A, B, C, Z, K, ta, tb, s);
-    if (dtype == BSP_F16) return sdd_by_block<__half>(L, A, B, C, Z, K, ta, tb, s);
+    if (!sdd_tc_shape(L, Z, K, ta, tb)) return BSP_ERR_UNSUPPORTED;
+    if (dtype == BSP_BF16) return sdd_by_block<__nv_bfloat16, false>(L, A, B, C, Z, K, ta, tb, 0.f, 0, nullptr, s);
+    if (dtype == BSP_F16) return sdd_by_block<__half, false>(L, A, B, C, Z, K, ta, tb, 0.f, 0, nullptr, s);
+    return BSP_ERR_UNSUPPORTED;
+}
+
+int launch_sdd_softmax_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* P, int Z, int K,
+                          int ta, int tb, float scale, int kind, const uint8_t* mask, cudaStream_t s) {
+    if (!sdd_tc_shape(L, Z, K, ta, tb)) return BSP_ERR_UNSUPPORTED;
+    const float c2 = scale * kLog2e;
+    if (dtype == BSP_BF16) return sdd_by_block<__nv_bfloat16, true>(L, A, B, P, Z, K, ta, tb, c2, kind, mask, s);
+    if (dtype == BSP_F16) return sdd_by_block<__half, true>(L, A, B, P, Z, K, ta, tb, c2, kind, mask, s);
     return BSP_ERR_UNSUPPORTED;
 }
 

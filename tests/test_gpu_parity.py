@@ -134,6 +134,44 @@ def test_sdd_contraction_lengths(bsp, oracle, path, B, K, trans):
     assert_close(to_np(C), oracle.sdd(lay, B, A, Bm, ta, tb), dtype, f"sdd B={B} K={K} trans={trans} {path}")
 
 
+@pytest.mark.parametrize("B", [16, 32, 64, 128])
+@pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("kind", [0, 1, 2])
+def test_sdd_softmax(bsp, oracle, path, B, dt, kind):
+    # fused SDD + softmax against the oracle's softmax of its SDD (fp64); the
+    # tensor-core path keeps the scores in fp32, the fallback rounds them to
+    # the dtype between the two steps
+    dtype = DTYPES[dt]
+    Z, H, K = 2, 3, 64 if B < 128 else 128
+    nb = max(3, 384 // B) + 1
+    S = nb * B
+    lay = rlayout(H, nb, 0.35, 3 * B + kind, diag=True)
+    L = bsp.bsp_layout_compile(lay, B)
+    A, Bm = randn((Z, H, S, K), dtype, 35), randn((Z, H, S, K), dtype, 36)
+    mask = W.random_mask(S, 0.7, 37) if kind == 1 else None
+    P = bsp.bsp_sdd_softmax(L, dev(A), dev(Bm), scale=0.2, mask_kind=kind,
+                            mask=None if mask is None else dev(torch.from_numpy(mask)))
+    torch.cuda.synchronize()
+    want = oracle.softmax(lay, B, oracle.sdd(lay, B, A, Bm), 0.2, kind, mask)
+    assert_close(to_np(P), want, dtype, f"sdd_softmax B={B} {dt} kind={kind} {path}")
+    assert bsp.bsp_status_check(L) == 0
+
+
+@pytest.mark.parametrize("trans", [(0, 0), (1, 0), (1, 1)])
+def test_sdd_softmax_orientations(bsp, oracle, path, trans):
+    ta, tb = trans
+    B, Z, H, K, nb = 64, 1, 2, 64, 7
+    S = nb * B
+    lay = rlayout(H, nb, 0.4, 90, diag=True)
+    L = bsp.bsp_layout_compile(lay, B)
+    A = randn((Z, H, K, S) if ta else (Z, H, S, K), torch.bfloat16, 38)
+    Bm = randn((Z, H, S, K) if tb else (Z, H, K, S), torch.bfloat16, 39)
+    P = bsp.bsp_sdd_softmax(L, dev(A), dev(Bm), scale=0.15, mask_kind=2, trans_a=ta, trans_b=tb)
+    torch.cuda.synchronize()
+    want = oracle.softmax(lay, B, oracle.sdd(lay, B, A, Bm, ta, tb), 0.15, 2)
+    assert_close(to_np(P), want, torch.bfloat16, f"sdd_softmax trans={trans} {path}")
+
+
 def test_sdd_leaves_absent_blocks_untouched(bsp, path):
     # the output has exactly nnz blocks; guard regions around it keep a canary
     B, H, nb, Z, K = 64, 2, 6, 2, 64

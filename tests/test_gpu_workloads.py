@@ -93,6 +93,32 @@ def test_unfused_chain_workload(bsp, oracle, name):
     assert_close(got, want, DT[w.dtype], f"{name} unfused chain, {sel.size} sampled rows")
 
 
+@pytest.mark.parametrize("name", ["tiny", "bigbird", "band", "strided"])
+def test_sdd_softmax_chain_workload(bsp, oracle, name):
+    """Fused SDD + softmax, then DSD, at full size: every present row of P sums
+    to 1, sampled rows of the output against the oracle's attention."""
+    w = W.ATTENTION_WORKLOADS[name]
+    lay = w.layout()
+    L = bsp.bsp_layout_compile(lay, w.B)
+    Q, K, V = w.qkv()
+    q, k, v = (t.cuda() for t in (Q, K, V))
+    P = bsp.bsp_sdd_softmax(L, q, k, None, w.scale, w.mask_kind)
+    O = bsp.bsp_dsd(L, P, v)
+    torch.cuda.synchronize()
+    assert torch.isfinite(P).all() and torch.isfinite(O).all()
+    hs, is_, _ = np.nonzero(lay)
+    key = torch.from_numpy(hs * w.nb + is_).cuda()
+    rowsum = torch.zeros(w.Z, w.H * w.nb, w.B, device="cuda", dtype=torch.float64)
+    rowsum.index_add_(1, key, P.double().sum(dim=3))
+    present = torch.from_numpy(lay.sum(axis=2).reshape(-1) > 0).cuda()
+    tol = 1e-5 if w.dtype == "f32" else 2e-2
+    assert torch.allclose(rowsum[:, present], torch.ones_like(rowsum[:, present]), atol=tol * 8, rtol=0)
+    sel = sample_rows(w, lay, 48, 13)
+    got = to_np(O.reshape(-1, w.D)[torch.from_numpy(sel).cuda()])
+    want = oracle.attention(lay, w.B, Q, K, V, w.scale, w.mask_kind, sel=sel)
+    assert_close(got, want, DT[w.dtype], f"{name} fused SDD+softmax chain, {sel.size} sampled rows")
+
+
 @pytest.mark.parametrize("name", ["tiny", "bigbird"])
 def test_softmax_workload(bsp, oracle, name):
     """The softmax alone on random SDD-shaped input at full size: sampled rows
