@@ -9,12 +9,26 @@
 // recurrence of the Triton-Puzzles blog, Puzzle 9 "Simple FlashAttention":
 //   m2 = max(m1, rowmax(s)),  l2 = l1 exp(m1 - m2) + sum exp(s - m2),
 //   o2 = o1 exp(m1 - m2) + sum exp(s - m2) v       (divided by l at the end).
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace bsp {
 namespace {
 
 constexpr int kThreads = 256;  // 16 x 16 thread grid in every kernel here
+
+// asynchronous 16-byte global -> shared copies (both addresses 16-byte aligned)
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
+                 "l"(gsrc)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 constexpr int KC = 16;         // contraction chunk staged in shared memory
 
 // ---------------------------------------------------------------- SDD ----
@@ -453,11 +467,16 @@ attention_simt_v4_kernel(LayoutView L, const T* __restrict__ Q, const T* __restr
                          const T* __restrict__ V, T* __restrict__ O, int Z, float c2, int kind,
                          const uint8_t* __restrict__ mask) {
     constexpr int TR = 64, R = 4, DP = D + 4, PP = TR + 4, NG = D / 64, D4 = D / 4;
+    // fp32 inputs: K and V chunks arrive by asynchronous 16-byte copies into two
+    // buffers, the next chunk's while the current one is computed; 16-bit
+    // inputs are converted on the way in (one buffer)
+    constexpr bool ASYNC = std::is_same<T, float>::value;
+    constexpr int NBUF = ASYNC ? 2 : 1;
     extern __shared__ float4 smem_v4[];
     float* Qs = reinterpret_cast<float*>(smem_v4);  // [TR][DP], pre-scaled by c2
-    float* Ks = Qs + TR * DP;                        // [TR][DP]
-    float* Vs = Ks + TR * DP;                        // [TR][DP]
-    float* Ps = Vs + TR * DP;                        // [TR][PP]
+    float* Ks = Qs + TR * DP;                        // [NBUF][TR][DP]
+    float* Vs = Ks + NBUF * TR * DP;                 // [NBUF][TR][DP]
+    float* Ps = Vs + NBUF * TR * DP;                 // [TR][PP]
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     const int B = L.B, S = L.S;
     const int nsub = B / TR;
@@ -480,7 +499,8 @@ attention_simt_v4_kernel(LayoutView L, const T* __restrict__ Q, const T* __restr
         const int64_t zh = z * L.H + h;
         const int r0 = i * B + sub * TR;  // first query row of this CTA
         load_tile(Qs, Q + (zh * S + r0) * D, c2);
-        float m[R], l[R], acc[R][NG][4];
+        float m[R], l[R];
+        float2 acc[R][NG][2];  // output columns 4 tx + 64 g + {0, 1}, {2, 3}
 #pragma unroll
         for (int u = 0; u < R; ++u) {
             m[u] = -INFINITY;
@@ -488,39 +508,73 @@ attention_simt_v4_kernel(LayoutView L, const T* __restrict__ Q, const T* __restr
 #pragma unroll
             for (int g = 0; g < NG; ++g)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) acc[u][g][c] = 0.f;
+                for (int c = 0; c < 2; ++c) acc[u][g][c] = make_float2(0.f, 0.f);
         }
         const int q0 = L.row_ptr[h * (L.nb + 1) + i], q1 = L.row_ptr[h * (L.nb + 1) + i + 1];
-        for (int q = q0; q < q1; ++q) {
-            const int j = L.col_idx[q];
-            for (int kc = 0; kc < B; kc += TR) {
-                const int c0 = j * B + kc;  // first key row of the chunk
-                __syncthreads();            // previous chunk fully consumed (and Qs written)
-                load_tile(Ks, K + (zh * S + c0) * D, 1.f);
-                load_tile(Vs, V + (zh * S + c0) * D, 1.f);
+        // chunks of TR key rows: nsub per present block, in CSR order
+        const int nch = (q1 - q0) * nsub;
+        auto chunk_row = [&](int t) { return L.col_idx[q0 + t / nsub] * B + (t % nsub) * TR; };
+        auto issue = [&](int t, int buf) {
+            const int c = chunk_row(t);
+            const float* ks = reinterpret_cast<const float*>(K) + (zh * S + c) * D;
+            const float* vs = reinterpret_cast<const float*>(V) + (zh * S + c) * D;
+            for (int e = threadIdx.x; e < TR * D4; e += kThreads) {
+                const int rr = e / D4, c4 = e % D4;
+                cp_async16(Ks + (buf * TR + rr) * DP + 4 * c4, ks + (int64_t)rr * D + 4 * c4);
+                cp_async16(Vs + (buf * TR + rr) * DP + 4 * c4, vs + (int64_t)rr * D + 4 * c4);
+            }
+            cp_async_commit();
+        };
+        if constexpr (ASYNC) {
+            if (nch > 0) issue(0, 0);
+        }
+        {
+            for (int t = 0; t < nch; ++t) {
+                const int j = L.col_idx[q0 + t / nsub];
+                const int c0 = chunk_row(t);  // first key row of the chunk
+                const int buf = ASYNC ? (t & 1) : 0;
+                const float* Kb = Ks + buf * TR * DP;
+                const float* Vb = Vs + buf * TR * DP;
+                __syncthreads();  // previous chunk fully consumed (and Qs written)
+                if constexpr (ASYNC) {
+                    if (t + 1 < nch) {
+                        issue(t + 1, buf ^ 1);
+                        cp_async_wait<1>();  // this chunk's copies have landed
+                    } else {
+                        cp_async_wait<0>();
+                    }
+                } else {
+                    load_tile(Ks, K + (zh * S + c0) * D, 1.f);
+                    load_tile(Vs, V + (zh * S + c0) * D, 1.f);
+                }
                 __syncthreads();
+                // scores with paired FMAs (even and odd d in the two halves of a
+                // float2, added at the end): half the FMA instructions
                 float s[R][R];
+                float2 s2[R][R];
 #pragma unroll
                 for (int u = 0; u < R; ++u)
 #pragma unroll
-                    for (int v = 0; v < R; ++v) s[u][v] = 0.f;
+                    for (int v = 0; v < R; ++v) s2[u][v] = make_float2(0.f, 0.f);
 #pragma unroll 4
                 for (int d4 = 0; d4 < D4; ++d4) {
                     float4 qa[R], kb[R];
 #pragma unroll
                     for (int u = 0; u < R; ++u) qa[u] = *reinterpret_cast<const float4*>(Qs + (ty + 16 * u) * DP + 4 * d4);
 #pragma unroll
-                    for (int v = 0; v < R; ++v) kb[v] = *reinterpret_cast<const float4*>(Ks + (tx + 16 * v) * DP + 4 * d4);
+                    for (int v = 0; v < R; ++v) kb[v] = *reinterpret_cast<const float4*>(Kb + (tx + 16 * v) * DP + 4 * d4);
 #pragma unroll
                     for (int u = 0; u < R; ++u)
 #pragma unroll
                         for (int v = 0; v < R; ++v) {
-                            s[u][v] = fmaf(qa[u].x, kb[v].x, s[u][v]);
-                            s[u][v] = fmaf(qa[u].y, kb[v].y, s[u][v]);
-                            s[u][v] = fmaf(qa[u].z, kb[v].z, s[u][v]);
-                            s[u][v] = fmaf(qa[u].w, kb[v].w, s[u][v]);
+                            s2[u][v] = __ffma2_rn(make_float2(qa[u].x, qa[u].y), make_float2(kb[v].x, kb[v].y), s2[u][v]);
+                            s2[u][v] = __ffma2_rn(make_float2(qa[u].z, qa[u].w), make_float2(kb[v].z, kb[v].w), s2[u][v]);
                         }
                 }
+#pragma unroll
+                for (int u = 0; u < R; ++u)
+#pragma unroll
+                    for (int v = 0; v < R; ++v) s[u][v] = s2[u][v].x + s2[u][v].y;
                 // intra-block mask
 #pragma unroll
                 for (int u = 0; u < R; ++u) {
@@ -562,7 +616,7 @@ attention_simt_v4_kernel(LayoutView L, const T* __restrict__ Q, const T* __restr
 #pragma unroll
                     for (int g = 0; g < NG; ++g)
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) acc[u][g][c] *= alpha;
+                        for (int c = 0; c < 2; ++c) acc[u][g][c] = __fmul2_rn(acc[u][g][c], make_float2(alpha, alpha));
 #pragma unroll
                     for (int v = 0; v < R; ++v) Ps[(ty + 16 * u) * PP + tx + 16 * v] = s[u][v];
                 }
@@ -577,16 +631,15 @@ attention_simt_v4_kernel(LayoutView L, const T* __restrict__ Q, const T* __restr
                         float4 vv[NG];
 #pragma unroll
                         for (int g = 0; g < NG; ++g)
-                            vv[g] = *reinterpret_cast<const float4*>(Vs + (4 * cc4 + k4) * DP + 64 * g + 4 * tx);
+                            vv[g] = *reinterpret_cast<const float4*>(Vb + (4 * cc4 + k4) * DP + 64 * g + 4 * tx);
 #pragma unroll
                         for (int u = 0; u < R; ++u) {
                             const float p = k4 == 0 ? pa[u].x : k4 == 1 ? pa[u].y : k4 == 2 ? pa[u].z : pa[u].w;
+                            const float2 pp = make_float2(p, p);
 #pragma unroll
                             for (int g = 0; g < NG; ++g) {
-                                acc[u][g][0] = fmaf(p, vv[g].x, acc[u][g][0]);
-                                acc[u][g][1] = fmaf(p, vv[g].y, acc[u][g][1]);
-                                acc[u][g][2] = fmaf(p, vv[g].z, acc[u][g][2]);
-                                acc[u][g][3] = fmaf(p, vv[g].w, acc[u][g][3]);
+                                acc[u][g][0] = __ffma2_rn(pp, make_float2(vv[g].x, vv[g].y), acc[u][g][0]);
+                                acc[u][g][1] = __ffma2_rn(pp, make_float2(vv[g].z, vv[g].w), acc[u][g][1]);
                             }
                         }
                     }
@@ -600,8 +653,10 @@ attention_simt_v4_kernel(LayoutView L, const T* __restrict__ Q, const T* __restr
 #pragma unroll
             for (int g = 0; g < NG; ++g) {
                 T* dst = O + (zh * S + r) * D + 64 * g + 4 * tx;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) dst[c] = from_f32<T>(acc[u][g][c] * inv);
+                dst[0] = from_f32<T>(acc[u][g][0].x * inv);
+                dst[1] = from_f32<T>(acc[u][g][0].y * inv);
+                dst[2] = from_f32<T>(acc[u][g][1].x * inv);
+                dst[3] = from_f32<T>(acc[u][g][1].y * inv);
             }
         }
         __syncthreads();  // Qs reused by the next work item
@@ -613,7 +668,8 @@ int attn_v4(const bsp_layout_s* L, const void* Q, const void* K, const void* V, 
             int kind, const uint8_t* mask, cudaStream_t s) {
     const int64_t total = (int64_t)L->H * L->nb * Z * (L->B / 64);
     if (total == 0) return BSP_OK;
-    const size_t smem = sizeof(float) * ((size_t)3 * 64 * (D + 4) + (size_t)64 * (64 + 4));
+    constexpr int nbuf = std::is_same<T, float>::value ? 2 : 1;  // K / V buffers (see the kernel)
+    const size_t smem = sizeof(float) * ((size_t)(1 + 2 * nbuf) * 64 * (D + 4) + (size_t)64 * (64 + 4));
     auto kern = attention_simt_v4_kernel<T, D>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return BSP_ERR_CUDA;
