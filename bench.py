@@ -274,22 +274,36 @@ def weak_value(flops_per_rank: float, world: int, ms_step: float) -> float:
     return flops_per_rank * world / (ms_step * 1e-3) / 1e12
 
 
+_FLUSH = None
+
+
 def time_launches(fn, n, stream, warmup=3):
+    """Average device time of fn over n calls, each timed by its own events
+    after a write of twice the L2 size (outside the timed span), so that no
+    call finds its inputs in L2 left there by the previous one."""
     import torch
+    global _FLUSH
+    if _FLUSH is None:
+        _FLUSH = torch.empty(2 * torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size,
+                             dtype=torch.uint8, device="cuda")
     for _ in range(warmup):  # first launches load the module and build tensor maps
         fn()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    start.record(stream)
+    spans = []
     for _ in range(n):
+        _FLUSH.fill_(1)
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
         fn()
-    end.record(stream)
+        b_.record(stream)
+        spans.append((a, b_))
     torch.cuda.synchronize()
-    return start.elapsed_time(end) / n  # ms per launch
+    return sum(a.elapsed_time(b_) for a, b_ in spans) / n  # ms per call
 
 
 def per_op_section(w, lay, L, q, k, v, pk, bsp, stream):
-    """Times each step of the unfused chain and the general spMM modes."""
+    """Times each step of the unfused chain and the general spMM modes (every
+    call cold in L2)."""
     import torch
     from sparse_attention_layout_gb300 import workloads as W
     out = {}
