@@ -2,14 +2,16 @@
 block-sparse attention for GB300 (sm_103a).
 
 The compute path is the C-ABI library ``libbsp.so`` (hand-written CUDA);
-``sparse_attention_layout_gb300.bsp`` is its thin Python binding.  The
+``sparse_attention_layout_gb300.bsp`` is its thin Python binding and
+``sparse_attention_layout_gb300.blocksparse`` the differentiable matmul /
+softmax objects built on it.  The
 library is loaded on first use and its absence is an error: there is no CPU
 fallback.
 """
 
 import importlib
 
-__all__ = ["bsp", "workloads"]
+__all__ = ["bsp", "blocksparse", "workloads"]
 
 
 def __getattr__(name):

@@ -360,3 +360,10 @@ def test_geometry_steps_of_the_workloads(lib):
     L = bsp.bsp_layout_plan(W.ATTENTION_WORKLOADS["bigbird"].layout(), 64)
     z = np.zeros(4, np.int32)
     assert lib.bsp_diag_geometry_steps(L.handle, ctypes.c_void_p(z.ctypes.data), ctypes.c_void_p(z.ctypes.data)) == -2
+
+
+def test_blocksparse_module_rejects_unknown_mode(lib):
+    from sparse_attention_layout_gb300 import blocksparse
+    assert blocksparse.MODES == ("sdd", "dsd", "dds")
+    with pytest.raises(ValueError):
+        blocksparse.matmul(np.ones((1, 2, 2), np.uint8), 32, "sds")
