@@ -128,6 +128,9 @@ int launch_softmax_backward(const bsp_layout_s* L, int dtype, const void* Y, con
 
 int sm_count();  // multiprocessors of the current device (cached per device)
 
+// bsp_layout_plan, the affine-geometry analysis optional (layout.cpp)
+int layout_plan(const uint8_t* layout, int H, int nb, int block, bool analyse, bsp_layout_t* out);
+
 // streams and events of bsp_attention_host (host_pipeline.cpp)
 void host_pipe_destroy(bsp_layout_s* L);
 

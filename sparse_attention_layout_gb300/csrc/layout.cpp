@@ -211,7 +211,11 @@ size_t padded(size_t n) {
 
 }  // namespace
 
-extern "C" int bsp_layout_plan(const uint8_t* layout, int H, int nb, int block, bsp_layout_t* out) {
+namespace bsp {
+
+// bsp_layout_plan with the affine-geometry analysis optional (callers that
+// only need the tables skip it)
+int layout_plan(const uint8_t* layout, int H, int nb, int block, bool analyse, bsp_layout_t* out) {
     if (!out) return BSP_ERR_INVALID_ARG;
     *out = nullptr;
     if (!layout || H < 1 || nb < 1 || !valid_block(block)) return BSP_ERR_INVALID_ARG;
@@ -226,7 +230,7 @@ extern "C" int bsp_layout_plan(const uint8_t* layout, int H, int nb, int block, 
     int rc;
     try {
         rc = build_tables(L, layout);
-        if (rc == BSP_OK) bsp::affine_analyse(L, layout);
+        if (rc == BSP_OK && analyse) affine_analyse(L, layout);
     } catch (const std::bad_alloc&) {
         rc = BSP_ERR_OOM;
     }
@@ -236,6 +240,12 @@ extern "C" int bsp_layout_plan(const uint8_t* layout, int H, int nb, int block, 
     }
     *out = L;
     return BSP_OK;
+}
+
+}  // namespace bsp
+
+extern "C" int bsp_layout_plan(const uint8_t* layout, int H, int nb, int block, bsp_layout_t* out) {
+    return bsp::layout_plan(layout, H, nb, block, true, out);
 }
 
 extern "C" int bsp_layout_compile(const uint8_t* layout, int H, int nb, int block, void* stream,

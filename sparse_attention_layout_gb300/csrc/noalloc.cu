@@ -65,7 +65,7 @@ extern "C" int bsp_softmax_noalloc(const uint8_t* layout, int H, int nb, int blo
         return BSP_ERR_ALIGNMENT;
 
     bsp_layout_t L = nullptr;
-    int rc = bsp_layout_plan(layout, H, nb, block, &L);  // host tables only
+    int rc = bsp::layout_plan(layout, H, nb, block, false, &L);  // host tables only, no geometry analysis
     if (rc != BSP_OK) return rc;
     const int E = dtype == BSP_F32 ? 1 : 0;
     // what the softmax kernels read: status word, CSR tables, this dtype's chunk list
