@@ -367,3 +367,22 @@ def test_blocksparse_module_rejects_unknown_mode(lib):
     assert blocksparse.MODES == ("sdd", "dsd", "dds")
     with pytest.raises(ValueError):
         blocksparse.matmul(np.ones((1, 2, 2), np.uint8), 32, "sds")
+
+
+def test_new_entry_points_validate_arguments(lib):
+    # checked on the host before any device work: NULL handle / host-only
+    # handle, bad scale, bad mask kind, missing dense mask
+    L = bsp.bsp_layout_plan(np.ones((1, 2, 2), np.uint8), 16)
+    buf = (ctypes.c_char * 4096)()
+    a = ctypes.c_void_p(ctypes.addressof(buf) + (-ctypes.addressof(buf)) % 16)
+    one = ctypes.c_float(1.0)
+    f = lib.bsp_sdd_softmax
+    assert f(None, 1, a, a, a, 1, 16, 0, 1, one, 0, None, None) == -1
+    assert f(L.handle, 1, a, a, a, 1, 16, 0, 1, one, 0, None, None) == -1       # host-only handle
+    assert lib.bsp_layout_geometry(None, None, None) == -1
+    n = np.zeros(1, np.int32)
+    assert lib.bsp_layout_geometry(L.handle, ctypes.c_void_p(n.ctypes.data), None) == 0 and n[0] == 1  # a full 2 x 2 head is one band
+    assert lib.bsp_attention_host(None, 1, a, a, a, a, 1, 64, one, 0, None, a, ctypes.c_size_t(1 << 20), None) == -1
+    assert lib.bsp_attention_host_workspace(None, 1, 64, 1) == 0
+    assert lib.bsp_attention_host_workspace(L.handle, 1, 64, 0) == 0
+    assert lib.bsp_diag_geometry_steps(None, a, a) == -1
