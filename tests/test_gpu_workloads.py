@@ -178,3 +178,32 @@ def test_spmm_workload(bsp, oracle, B, density):
     # block-rows without any block are exactly zero in the DSD output
     for i in empty_rows[:4]:
         assert (C1[0, 0, i * sp.B:(i + 1) * sp.B] == 0).all()
+
+
+def test_long_sequence_band(bsp, oracle):
+    """A maximum-size case: S = 262144 tokens (4096 blocks of 64, the largest
+    block count the on-device compiler takes), band of +-2 blocks, causal
+    inside the diagonal blocks, bf16.  Fused attention and the fused
+    SDD + softmax -> DSD chain on sampled rows (first, last, random) against
+    the oracle; the layout compiled on the device equals the host compile's
+    tiles."""
+    from types import SimpleNamespace
+    B, nb, H, Z, D = 64, 4096, 1, 1, 128
+    S = nb * B
+    lay = W.layout_band(nb, 2, H)
+    L = bsp.bsp_layout_compile(lay, B)
+    Ld = bsp.bsp_layout_compile_device(torch.from_numpy(lay).cuda(), B)
+    assert np.array_equal(L.tiles()["step_col"], Ld.tiles()["step_col"])
+    Q, K, V = (W.randn((Z, H, S, D), "bf16", 500 + s) for s in range(3))
+    q, k, v = (t.cuda() for t in (Q, K, V))
+    scale = 1.0 / np.sqrt(D)
+    o = bsp.bsp_attention(Ld, q, k, v, None, scale, W.MASK_DIAG_CAUSAL)
+    o2 = bsp.bsp_dsd(Ld, bsp.bsp_sdd_softmax(Ld, q, k, None, scale, W.MASK_DIAG_CAUSAL), v)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o).all() and torch.isfinite(o2).all()
+    w = SimpleNamespace(Z=Z, H=H, S=S, B=B)
+    sel = sample_rows(w, lay, 40, 17)
+    want = oracle.attention(lay, B, Q, K, V, scale, W.MASK_DIAG_CAUSAL, sel=sel)
+    for got, what in ((o, "fused attention"), (o2, "fused SDD + softmax -> DSD")):
+        g = to_np(got.reshape(-1, D)[torch.from_numpy(sel).cuda()])
+        assert_close(g, want, torch.bfloat16, f"S={S} {what}, {sel.size} sampled rows")
