@@ -3,8 +3,10 @@
 // in the row index).  A head's record holds at most a band term (offsets
 // beta .. beta+kappa-1 from the diagonal) and a column term (columns
 // beta + sigma*k, k < kappa, causal: only in rows at or below the column);
-// from it a kernel computes the key blocks of a row tile and their presence
-// instead of reading the step tables.
+// from it the attention kernel's TMA producers compute the key blocks of a
+// row tile instead of reading the step tables (geo_col), and the host-side
+// check of that arithmetic also evaluates each block's presence (geo_has).
+// The helpers compile for the host too, so that check needs no GPU.
 #pragma once
 
 #include <cstdint>
