@@ -310,13 +310,19 @@ int bsp_attention_backward(bsp_layout_t layout, int dtype, const void* Q, const 
  * neighbouring slices overlap each kernel.  Asynchronous like the other
  * calls: it starts after the work queued on `stream` and `stream` waits for
  * its end; the host buffers and the workspace must stay valid until then.
- * mask: DEVICE [S][S] as in bsp_attention.  Calls that share a handle must
- * not run concurrently from several host threads.  Workspace smaller than
- * one slice: BSP_ERR_INVALID_ARG.  (Not from the pages: the end-to-end path
- * through host memory.) */
+ * mask: DEVICE [S][S] as in bsp_attention.  flags: 0, or
+ * BSP_HOST_RESERVED_WORKSPACE — the caller promises that nothing but this
+ * handle's calls touches the workspace between them; a call given the same
+ * workspace as the handle's previous call then starts its input copies as
+ * soon as the slots they fill are free (overlapping the previous call's last
+ * kernel and output copy) instead of after all the work on `stream`.  Calls
+ * that share a handle must not run concurrently from several host threads.
+ * Workspace smaller than one slice or unknown flags: BSP_ERR_INVALID_ARG.
+ * (Not from the pages: the end-to-end path through host memory.) */
+#define BSP_HOST_RESERVED_WORKSPACE 1
 int bsp_attention_host(bsp_layout_t layout, int dtype, const void* Q, const void* K, const void* V, void* O,
                        int Z, int D, float scale, int mask_kind, const uint8_t* mask, void* workspace,
-                       size_t workspace_bytes, void* stream);
+                       size_t workspace_bytes, int flags, void* stream);
 size_t bsp_attention_host_workspace(bsp_layout_t layout, int dtype, int D, int z_slice);
 
 /* ---- diagnostics ------------------------------------------------------- */

@@ -65,7 +65,7 @@ def lib():
         L.bsp_layout_groups.argtypes = [P, i32, P, P, P, P, P, P, P]
         L.bsp_layout_geometry.argtypes = [P, P, P]
         L.bsp_layout_compile_affine.argtypes = [P, P, i32, i32, i32, P, ctypes.POINTER(P)]
-        L.bsp_attention_host.argtypes = [P, i32, P, P, P, P, i32, i32, f32, i32, P, P, ctypes.c_size_t, P]
+        L.bsp_attention_host.argtypes = [P, i32, P, P, P, P, i32, i32, f32, i32, P, P, ctypes.c_size_t, i32, P]
         L.bsp_attention_host_workspace.argtypes = [P, i32, i32, i32]
         L.bsp_attention_host_workspace.restype = ctypes.c_size_t
         L.bsp_status_check.argtypes = [P, P]
@@ -317,12 +317,17 @@ def bsp_attention_host_workspace(L: Layout, dtype, D: int, z_slice: int) -> int:
     return int(lib().bsp_attention_host_workspace(L.handle, _DTYPES[dtype], int(D), int(z_slice)))
 
 
+HOST_RESERVED_WORKSPACE = 1
+
+
 def bsp_attention_host(L: Layout, Q, K, V, O=None, scale: float = 1.0, mask_kind: int = MASK_NONE,
-                       mask=None, workspace=None, stream=None):
+                       mask=None, workspace=None, reserved_workspace: bool = False, stream=None):
     """Fused attention on HOST tensors Q, K, V (O allocated pinned when None);
     the library copies slices of the batch in and out on its own streams,
     overlapped with the kernels.  workspace: device uint8 tensor (allocated for
-    slices of one batch entry when None)."""
+    slices of one batch entry when None).  reserved_workspace: the workspace is
+    used by nothing but this handle's calls in between, so a call may start its
+    input copies during the previous call's tail."""
     if O is None:
         O = torch.empty(Q.shape, dtype=Q.dtype, pin_memory=True)
     if any(t.is_cuda for t in (Q, K, V, O)):
@@ -333,7 +338,8 @@ def bsp_attention_host(L: Layout, Q, K, V, O=None, scale: float = 1.0, mask_kind
         workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     _check(lib().bsp_attention_host(L.handle, dt, _ptr(Q), _ptr(K), _ptr(V), _ptr(O), Q.shape[0], Q.shape[3],
                                     float(scale), int(mask_kind), _ptr(mask), _ptr(workspace),
-                                    workspace.numel() * workspace.element_size(), _stream(stream)),
+                                    workspace.numel() * workspace.element_size(),
+                                    HOST_RESERVED_WORKSPACE if reserved_workspace else 0, _stream(stream)),
            "bsp_attention_host")
     return O
 

@@ -15,6 +15,7 @@
 
 struct HostPipe {
     cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
+    const void* last_ws = nullptr;  // workspace of the previous call
     cudaEvent_t start = nullptr, done = nullptr, in[2] = {nullptr, nullptr}, out[2] = {nullptr, nullptr},
                 freed[2] = {nullptr, nullptr};
 };
@@ -68,9 +69,9 @@ extern "C" size_t bsp_attention_host_workspace(bsp_layout_t L, int dtype, int D,
 
 extern "C" int bsp_attention_host(bsp_layout_t L, int dtype, const void* Qh, const void* Kh, const void* Vh,
                                   void* Oh, int Z, int D, float scale, int mask_kind, const uint8_t* mask,
-                                  void* workspace, size_t workspace_bytes, void* stream) {
+                                  void* workspace, size_t workspace_bytes, int flags, void* stream) {
     using namespace bsp;
-    if (!L || !L->on_device || Z < 0 || D < 1) return BSP_ERR_INVALID_ARG;
+    if (!L || !L->on_device || Z < 0 || D < 1 || (flags & ~BSP_HOST_RESERVED_WORKSPACE)) return BSP_ERR_INVALID_ARG;
     if (Z == 0) return BSP_OK;
     if (!Qh || !Kh || !Vh || !Oh || !workspace) return BSP_ERR_INVALID_ARG;
     if (((uintptr_t)workspace & 255u) != 0) return BSP_ERR_ALIGNMENT;
@@ -86,10 +87,17 @@ extern "C" int bsp_attention_host(bsp_layout_t L, int dtype, const void* Qh, con
     const size_t slot_bytes = 4 * (size_t)zs * per_z;
     char* ws = static_cast<char*>(workspace);
     auto fail = [&]() { cudaGetLastError(); return BSP_ERR_CUDA; };
-    // everything after the work already queued on the caller's stream
+    // kernels and output copies after the work already queued on the caller's
+    // stream; input copies too, unless the workspace is reserved for this
+    // handle and was the previous call's: then they only wait (below) for
+    // the slot they fill to be free, and may overlap the previous call's tail
+    const bool early = (flags & BSP_HOST_RESERVED_WORKSPACE) && p->last_ws == workspace;
     if (cudaEventRecord(p->start, caller) != cudaSuccess) return fail();
-    for (cudaStream_t s : {p->h2d, p->comp, p->d2h})
+    for (cudaStream_t s : {p->h2d, p->comp, p->d2h}) {
+        if (early && s == p->h2d) continue;
         if (cudaStreamWaitEvent(s, p->start, 0) != cudaSuccess) return fail();
+    }
+    p->last_ws = workspace;
     const int nsl = (Z + zs - 1) / zs;
     for (int k = 0; k < nsl; ++k) {
         const int z0 = k * zs, nz = std::min(zs, Z - z0), slot = k & 1;
@@ -98,8 +106,9 @@ extern "C" int bsp_attention_host(bsp_layout_t L, int dtype, const void* Qh, con
         char* kk = q + (size_t)zs * per_z;
         char* v = kk + (size_t)zs * per_z;
         char* o = v + (size_t)zs * per_z;
-        // inputs, once the slot's previous output has been copied out
-        if (k >= 2 && cudaStreamWaitEvent(p->h2d, p->freed[slot], 0) != cudaSuccess) return fail();
+        // inputs, once the slot's previous output has been copied out (the
+        // previous call's, for the first two slices of an early start)
+        if ((k >= 2 || early) && cudaStreamWaitEvent(p->h2d, p->freed[slot], 0) != cudaSuccess) return fail();
         if (cudaMemcpyAsync(q, (const char*)Qh + off, bytes, cudaMemcpyHostToDevice, p->h2d) != cudaSuccess ||
             cudaMemcpyAsync(kk, (const char*)Kh + off, bytes, cudaMemcpyHostToDevice, p->h2d) != cudaSuccess ||
             cudaMemcpyAsync(v, (const char*)Vh + off, bytes, cudaMemcpyHostToDevice, p->h2d) != cudaSuccess ||

@@ -181,7 +181,7 @@ def test_compute_calls_reject_host_only_handle(lib):
     assert lib.bsp_attention(L.handle, 1, a, a, a, a, 1, 64, ctypes.c_float(1.0), 0, None, None) == -1
     assert lib.bsp_status_check(L.handle, None) == -1
     assert lib.bsp_attention_host(L.handle, 1, a, a, a, a, 1, 64, ctypes.c_float(1.0), 0, None, a,
-                                  ctypes.c_size_t(1 << 20), None) == -1
+                                  ctypes.c_size_t(1 << 20), 0, None) == -1
     # workspace for slices of one batch entry: 2 slots x (Q, K, V, O) x H S D x 2 bytes
     assert lib.bsp_attention_host_workspace(L.handle, 1, 64, 1) == 2 * 4 * 1 * 32 * 64 * 2
     assert lib.bsp_sdd(None, 1, a, a, a, 1, 16, 0, 1, None) == -1
@@ -382,7 +382,7 @@ def test_new_entry_points_validate_arguments(lib):
     assert lib.bsp_layout_geometry(None, None, None) == -1
     n = np.zeros(1, np.int32)
     assert lib.bsp_layout_geometry(L.handle, ctypes.c_void_p(n.ctypes.data), None) == 0 and n[0] == 1  # a full 2 x 2 head is one band
-    assert lib.bsp_attention_host(None, 1, a, a, a, a, 1, 64, one, 0, None, a, ctypes.c_size_t(1 << 20), None) == -1
+    assert lib.bsp_attention_host(None, 1, a, a, a, a, 1, 64, one, 0, None, a, ctypes.c_size_t(1 << 20), 0, None) == -1
     assert lib.bsp_attention_host_workspace(None, 1, 64, 1) == 0
     assert lib.bsp_attention_host_workspace(L.handle, 1, 64, 0) == 0
     assert lib.bsp_diag_geometry_steps(None, a, a) == -1

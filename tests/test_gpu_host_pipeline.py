@@ -70,15 +70,19 @@ def test_host_rejects_small_workspace_and_device_tensors(bsp):
         bsp.bsp_attention_host(L, Q.cuda(), Q, Q)
 
 
-def test_host_repeated_calls_reuse_slots(bsp):
-    # several calls in a row on one handle (the slot hand-off events are reused)
+@pytest.mark.parametrize("reserved", [False, True])
+def test_host_repeated_calls_reuse_slots(bsp, reserved):
+    # several calls in a row on one handle (the slot hand-off events are reused;
+    # with a reserved workspace a call's input copies overlap the previous
+    # call's tail)
     B, nb, H, D, Z = 128, 4, 2, 64, 6
     L = bsp.bsp_layout_compile(W.layout_band(nb, 1, H), B)
     S = nb * B
+    ws = torch.empty(bsp.bsp_attention_host_workspace(L, torch.bfloat16, D, 1), dtype=torch.uint8, device="cuda")
     outs = []
-    for rep in range(3):
+    for rep in range(4):
         Q, K, V = (W.randn((Z, H, S, D), "bf16", 420 + 3 * rep + s).pin_memory() for s in range(3))
-        O = bsp.bsp_attention_host(L, Q, K, V, None, 0.125)
+        O = bsp.bsp_attention_host(L, Q, K, V, None, 0.125, workspace=ws, reserved_workspace=reserved)
         outs.append((O, Q, K, V))
     torch.cuda.synchronize()
     for O, Q, K, V in outs:
