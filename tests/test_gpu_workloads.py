@@ -119,7 +119,7 @@ def test_sdd_softmax_chain_workload(bsp, oracle, name):
     assert_close(got, want, DT[w.dtype], f"{name} fused SDD+softmax chain, {sel.size} sampled rows")
 
 
-@pytest.mark.parametrize("name", ["tiny", "bigbird"])
+@pytest.mark.parametrize("name", ["tiny", "bigbird", "band", "strided"])
 def test_softmax_workload(bsp, oracle, name):
     """The softmax alone on random SDD-shaped input at full size: sampled rows
     against the oracle, every row of the whole output sums to 1."""
