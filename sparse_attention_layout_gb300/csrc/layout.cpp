@@ -181,6 +181,7 @@ int build_tables(bsp_layout_s* L, const uint8_t* lay) {
     // softmax chunk lists (element sizes 2 and 4 bytes)
     for (int e = 0; e < 2; ++e) {
         const int64_t elt = e ? 4 : 2;
+        const int64_t budget = softmax_chunk_budget((int64_t)L->max_row_nnz * L->B * elt);
         L->sm_items[e].clear();
         L->sm_max_bytes[e] = 0;
         L->sm_fits[e] = true;
@@ -188,8 +189,8 @@ int build_tables(bsp_layout_s* L, const uint8_t* lay) {
             const int64_t per_row = (int64_t)row_len[key] * L->B * elt;
             if (per_row == 0) continue;
             int R = L->B;
-            while (R > 1 && R * per_row > kSoftmaxChunkBudget) R >>= 1;
-            if (R * per_row > kSoftmaxChunkBudget) L->sm_fits[e] = false;
+            while (R > 1 && R * per_row > budget) R >>= 1;
+            if (R * per_row > budget) L->sm_fits[e] = false;
             L->sm_max_bytes[e] = std::max<int>(L->sm_max_bytes[e], (int)std::min<int64_t>(R * per_row, INT32_MAX));
             const int h = key / nb, i = key % nb;
             for (int r0 = 0; r0 < L->B; r0 += R) {

@@ -59,9 +59,8 @@ __global__ void __launch_bounds__(kScanThreads) k_scan(const int* __restrict__ i
     if (t == kScanThreads - 1) *total = part[t];
 }
 
-// per block-row: block count, validity, softmax chunk counts (both element sizes)
-__global__ void k_rows(const uint8_t* __restrict__ lay, int rows, int nb, int B, int* row_len, int* items0,
-                       int* items1, Totals* tot) {
+// per block-row: block count, validity
+__global__ void k_rows(const uint8_t* __restrict__ lay, int rows, int nb, int* row_len, Totals* tot) {
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= rows) return;
     const uint8_t* p = lay + (int64_t)r * nb;
@@ -74,13 +73,22 @@ __global__ void k_rows(const uint8_t* __restrict__ lay, int rows, int nb, int B,
     if (bad) atomicOr(&tot->err, 1);
     row_len[r] = c;
     atomicMax(&tot->max_row_nnz, c);
+}
+
+// per block-row: softmax chunk counts (both element sizes), once the longest
+// row, which sets the chunk budget, is known
+__global__ void k_row_items(int rows, int B, const int* row_len, int* items0, int* items1, Totals* tot) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= rows) return;
+    const int c = row_len[r];
     for (int e = 0; e < 2; ++e) {
         const int64_t per_row = (int64_t)c * B * (e ? 4 : 2);
+        const int64_t budget = softmax_chunk_budget((int64_t)tot->max_row_nnz * B * (e ? 4 : 2));
         int items = 0;
         if (per_row > 0) {
             int R = B;
-            while (R > 1 && R * per_row > kSoftmaxChunkBudget) R >>= 1;
-            if (R * per_row > kSoftmaxChunkBudget) atomicOr(&tot->sm_unfit[e], 1);
+            while (R > 1 && R * per_row > budget) R >>= 1;
+            if (R * per_row > budget) atomicOr(&tot->sm_unfit[e], 1);
             atomicMax(&tot->sm_max_bytes[e], (int)(R * per_row < INT32_MAX ? R * per_row : INT32_MAX));
             items = B / R;
         }
@@ -237,14 +245,15 @@ __global__ void k_fill_groups(const int32_t* __restrict__ ids, int H, int nb, in
     }
 }
 
-__global__ void k_fill_items(int rows, int B, const int* row_len, const int* row_start, const int* item_start0,
-                             const int* item_start1, Tables T) {
+__global__ void k_fill_items(int rows, int B, int max_row_nnz, const int* row_len, const int* row_start,
+                             const int* item_start0, const int* item_start1, Tables T) {
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= rows || row_len[r] == 0) return;
     for (int e = 0; e < 2; ++e) {
         const int64_t per_row = (int64_t)row_len[r] * B * (e ? 4 : 2);
+        const int64_t budget = softmax_chunk_budget((int64_t)max_row_nnz * B * (e ? 4 : 2));
         int R = B;
-        while (R > 1 && R * per_row > kSoftmaxChunkBudget) R >>= 1;
+        while (R > 1 && R * per_row > budget) R >>= 1;
         int32_t* it = T.sm_items[e] + 4 * (int64_t)(e ? item_start1[r] : item_start0[r]);
         for (int r0 = 0; r0 < B; r0 += R, it += 4) {
             it[0] = r;
@@ -381,7 +390,8 @@ extern "C" int bsp_layout_compile_device(const uint8_t* layout, int H, int nb, i
     // (1) sizes and starts
     const int tb = 256;
     bool ok = cudaMemsetAsync(dtot, 0, sizeof(Totals), s) == cudaSuccess;
-    k_rows<<<(rows + tb - 1) / tb, tb, 0, s>>>(layout, rows, nb, block, R(ROW_LEN), R(ITEMS0), R(ITEMS1), dtot);
+    k_rows<<<(rows + tb - 1) / tb, tb, 0, s>>>(layout, rows, nb, R(ROW_LEN), dtot);
+    k_row_items<<<(rows + tb - 1) / tb, tb, 0, s>>>(rows, block, R(ROW_LEN), R(ITEMS0), R(ITEMS1), dtot);
     k_cols<<<(rows + tb - 1) / tb, tb, 0, s>>>(layout, H, nb, R(COL_LEN), dtot);
     k_group_sizes<<<dim3(ntiles, 2), tb, 0, s>>>(layout, H, nb, G, ngroups, Tt(STEPS), Tt(SIZE0), Tt(SIZE1), dtot);
     k_scan<<<1, kScanThreads, 0, s>>>(R(ROW_LEN), R(ROW_START), rows, &dtot->nnz);
@@ -458,8 +468,8 @@ extern "C" int bsp_layout_compile_device(const uint8_t* layout, int H, int nb, i
     k_fill_cols<<<(rows + tb - 1) / tb, tb, 0, s>>>(H, nb, R(COL_START), ids, T);
     k_fill_groups<<<dim3(ntiles, 2), tb, 0, s>>>(ids, H, nb, G, ngroups, Tt(TILE_START), Tt(GL_START0),
                                                  Tt(GL_START1), T);
-    k_fill_items<<<(rows + tb - 1) / tb, tb, 0, s>>>(rows, block, R(ROW_LEN), R(ROW_START), R(ITEM_START0),
-                                                     R(ITEM_START1), T);
+    k_fill_items<<<(rows + tb - 1) / tb, tb, 0, s>>>(rows, block, tot.max_row_nnz, R(ROW_LEN), R(ROW_START),
+                                                     R(ITEM_START0), R(ITEM_START1), T);
     // (4) longest-first orders
     const OrderJob jobs[5] = {{R(ROW_LEN), T.row_order, rows}, {R(COL_LEN), T.col_order, rows},
                               {Tt(STEPS), T.tile_order, ntiles}, {Tt(SIZE0), T.gl_order[0], ntiles},
