@@ -14,7 +14,7 @@
 // Roles (512 threads, one CTA per SM):
 //   warps 0, 3  TMA producers: warp 0 the Q tile (2 stages) and K tiles, warp 3
 //               the V tiles (2 stages each), so that K never waits behind V
-//   warp 1      TMEM owner; one thread issues S[g%2] = Q K^T (M=128, N=128, K=D)
+//   warp 1      TMEM owner; one thread issues S[g%3] = Q K^T (M=128, N=128, K=D)
 //   warp 2      one thread issues O += P V (M=128, N=D, K=128; P from TMEM, V
 //               MN-major).  Two issuing threads halve each one's per-step
 //               barrier waits and commits, which cost about as much as the MMAs.
