@@ -190,13 +190,16 @@ softmax_rows_kernel(LayoutView L, const T* X, T* Y, int64_t rows_total, float c2
 // every HBM byte moves once, in large contiguous transfers.  Warps then own
 // rows: an online (max, sum) pass and a normalising pass over shared memory.
 // Several CTAs per SM overlap one CTA's transfers with another's arithmetic.
-constexpr int kChunkThreads = 256;
+// 4 warps: with 64 registers a thread, 8 CTAs share an SM, so that with
+// chunks of about 24 KB eight chunks are in flight per SM, each CTA in its own
+// phase (copy in, arithmetic, copy out)
+constexpr int kChunkThreads = 128;
 constexpr int kChunkRegElems = 40;  // row elements per lane held in registers
 
 // Chunks come from the layout's list for this element size: each block-row is
 // cut into chunks of the largest power-of-two row count that fits the budget.
 template <typename T, int BLK>
-__global__ void __launch_bounds__(kChunkThreads, 4)
+__global__ void __launch_bounds__(kChunkThreads, 8)
 softmax_chunk_kernel(LayoutView L, const T* X, T* Y, float c2, int kind, const uint8_t* __restrict__ mask) {
     constexpr int VEC = 16 / sizeof(T);
     constexpr int VPB = BLK / VEC;  // 16-byte vectors per row slice of one block
