@@ -92,6 +92,46 @@ def test_softmax_long_rows_and_in_place(bsp, oracle, dt, nb):
     assert_close(to_np(Xd), want, dtype, f"softmax long/in-place nb={nb}")
 
 
+@pytest.mark.parametrize("B,dt,nb,kind", [(128, "bf16", 260, 0), (128, "bf16", 260, 2),
+                                           (16, "f32", 1040, 0), (16, "f32", 1040, 1), (16, "f32", 1040, 2)])
+def test_softmax_rows_longer_than_a_chunk(bsp, oracle, B, dt, nb, kind):
+    # one block-row holds every block, so its rows exceed the largest softmax
+    # chunk (64 KB) and the whole layout takes the one-warp-per-row kernel
+    # (online pass and normalising pass for the long rows, registers for the
+    # others); sampled rows against the oracle
+    dtype = DTYPES[dt]
+    S = nb * B
+    assert S * torch.tensor([], dtype=dtype).element_size() > 64 * 1024
+    lay = np.eye(nb, dtype=np.uint8)[None].copy()
+    lay[0, nb // 2, :] = 1
+    lay[0, 3, :5] = 1
+    L = bsp.bsp_layout_compile(lay, B)
+    X = randn((1, L.nnz, B, B), dtype, 31)
+    mask = None
+    if kind == 1:
+        mask = (np.random.default_rng(4).integers(0, 5, size=(S, S), dtype=np.uint8) != 0).astype(np.uint8)
+    Y = bsp.bsp_softmax(L, dev(X), scale=0.6, mask_kind=kind,
+                        mask=None if mask is None else dev(torch.from_numpy(mask)))
+    torch.cuda.synchronize()
+    assert bsp.bsp_status_check(L) == 0
+    i_long = nb // 2
+    sel = sorted({0, B - 1, 3 * B, 3 * B + B - 1, S - 1, i_long * B, i_long * B + 1,
+                  i_long * B + B // 2, i_long * B + B - 1} |
+                 set(np.random.default_rng(5).choice(S, size=8, replace=False).tolist()))
+    sel = np.array(sel, dtype=np.int64)
+    want = oracle.softmax_rows(lay, B, X, 0.6, kind, mask, sel=sel)
+    ids = -np.ones(lay.shape, np.int64)
+    hs, is_, js = np.nonzero(lay)
+    ids[hs, is_, js] = np.arange(hs.size)
+    Yh = to_np(Y)
+    got = np.zeros_like(want)
+    for t, r in enumerate(sel):
+        i, a = divmod(int(r), B)
+        for j in np.flatnonzero(lay[0, i]):
+            got[t, j * B:(j + 1) * B] = Yh[0, ids[0, i, j], a]
+    assert_close(got, want, dtype, f"softmax rows > 64 KB B={B} {dt} kind={kind}")
+
+
 # --------------------------------------------------------------- SDD ----
 
 @pytest.mark.parametrize("B", [16, 32, 64, 128])
