@@ -190,6 +190,22 @@ int bsp_layout_tiles(bsp_layout_t layout, int* G, int* n_tiles, int64_t* n_steps
 int bsp_layout_groups(bsp_layout_t layout, int orient, int* G, int* n_groups, int64_t* n_slots,
                       int32_t* grp_ptr, int32_t* grp_order, int32_t* slot_idx, int32_t* slot_blk);
 
+/* Chunks of the block-sparse row softmax ("question on blocksparse", openai/
+ * triton issue 117: the softmax reduces each row of the SDD output across the
+ * row's present blocks) for elements of elt_bytes (2 or 4) bytes: host copy,
+ * for inspection; any pointer may be NULL (call first with items = NULL to
+ * get n_chunks).  A chunk is R consecutive rows of one block-row, moved through
+ * shared memory by one CTA: items [n_chunks*4] int32 = (h*nb + i, first block
+ * id of the block-row p0, its block count nnz_i, r0 | R << 16), block-rows in
+ * memory order and rows r0 .. r0+R-1.  R is the largest power of two (at most
+ * block) with R * nnz_i * block * elt_bytes <= the layout's chunk budget:
+ * twice the bytes of its longest row, at least 24 KB, at most 64 KB.
+ * max_bytes: the largest chunk.  fits: 0 when a single row exceeds the
+ * budget, in which case the softmax takes one warp per row instead of this
+ * list.  elt_bytes not 2 or 4: BSP_ERR_INVALID_ARG. */
+int bsp_layout_softmax_chunks(bsp_layout_t layout, int elt_bytes, int64_t* n_chunks, int* max_bytes, int* fits,
+                              int32_t* items);
+
 /* ---- matmul modes ------------------------------------------------------ */
 
 /* SDD: C = op(A) . op(B) evaluated on the present blocks only.

@@ -63,6 +63,7 @@ def lib():
         L.bsp_softmax_backward.argtypes = [P, i32, P, P, P, i32, f32, P]
         L.bsp_attention_backward.argtypes = [P, i32, P, P, P, P, P, P, P, i32, i32, f32, i32, P, P, P, P]
         L.bsp_layout_groups.argtypes = [P, i32, P, P, P, P, P, P, P]
+        L.bsp_layout_softmax_chunks.argtypes = [P, i32, P, P, P, P]
         L.bsp_layout_geometry.argtypes = [P, P, P]
         L.bsp_layout_compile_affine.argtypes = [P, P, i32, i32, i32, P, ctypes.POINTER(P)]
         L.bsp_attention_host.argtypes = [P, i32, P, P, P, P, i32, i32, f32, i32, P, P, ctypes.c_size_t, i32, P]
@@ -76,6 +77,7 @@ def lib():
                      "bsp_layout_info",
                      "bsp_layout_get_luts", "bsp_layout_tiles", "bsp_sdd", "bsp_dsd", "bsp_dds", "bsp_softmax",
                      "bsp_attention", "bsp_softmax_backward", "bsp_attention_backward", "bsp_layout_groups",
+                     "bsp_layout_softmax_chunks",
                      "bsp_status_check", "bsp_layout_geometry", "bsp_layout_compile_affine", "bsp_attention_host", "bsp_sdd_softmax"):
             getattr(L, name).restype = i32
         _lib = L
@@ -177,6 +179,19 @@ class Layout:
         out["slot_blk"] = out["slot_blk"][:ns * G].reshape(ns, G)
         out.update(G=G, n_groups=ng, n_slots=ns)
         return out
+
+    def softmax_chunks(self, elt_bytes: int) -> dict:
+        """Chunks of the softmax for 2- or 4-byte elements: items [n, 4] int32
+        (h*nb + i, first block id, blocks in the row, r0 | R << 16), the largest
+        chunk's bytes and whether every row fits one chunk."""
+        n, mb, fits = ctypes.c_int64(), ctypes.c_int(), ctypes.c_int()
+        f = lib().bsp_layout_softmax_chunks
+        _check(f(self.handle, int(elt_bytes), ctypes.byref(n), ctypes.byref(mb), ctypes.byref(fits), None),
+               "bsp_layout_softmax_chunks")
+        items = np.zeros((max(n.value, 1), 4), np.int32)
+        _check(f(self.handle, int(elt_bytes), None, None, None, ctypes.c_void_p(items.ctypes.data)),
+               "bsp_layout_softmax_chunks")
+        return {"items": items[:n.value], "max_bytes": mb.value, "fits": bool(fits.value)}
 
     def geometry(self):
         """Affine description per head: (n_terms [H] int32, -1 = none;

@@ -410,6 +410,28 @@ extern "C" int bsp_layout_groups(bsp_layout_t L, int orient, int* G, int* n_grou
     return BSP_OK;
 }
 
+extern "C" int bsp_layout_softmax_chunks(bsp_layout_t L, int elt_bytes, int64_t* n_chunks, int* max_bytes,
+                                         int* fits, int32_t* items) {
+    if (!L || (elt_bytes != 2 && elt_bytes != 4)) return BSP_ERR_INVALID_ARG;
+    const int e = elt_bytes == 4 ? 1 : 0;
+    if (max_bytes) *max_bytes = L->sm_max_bytes[e];
+    if (fits) *fits = L->sm_fits[e] ? 1 : 0;
+    if (!L->host_tables) {
+        const int64_t n = L->sm_n_items_dev[e];
+        if (n_chunks) *n_chunks = n;
+        if (items && n > 0) {
+            if (cudaDeviceSynchronize() != cudaSuccess) return BSP_ERR_CUDA;
+            if (cudaMemcpy(items, L->view.sm_items[e], (size_t)n * 4 * sizeof(int32_t), cudaMemcpyDeviceToHost) !=
+                cudaSuccess)
+                return BSP_ERR_CUDA;
+        }
+        return BSP_OK;
+    }
+    if (n_chunks) *n_chunks = (int64_t)(L->sm_items[e].size() / 4);
+    if (items && !L->sm_items[e].empty()) std::copy(L->sm_items[e].begin(), L->sm_items[e].end(), items);
+    return BSP_OK;
+}
+
 extern "C" int bsp_layout_tiles(bsp_layout_t L, int* G, int* n_tiles, int64_t* n_steps,
                                 int32_t* tile_step_ptr, int32_t* tile_order, int32_t* step_col,
                                 int32_t* step_blk) {

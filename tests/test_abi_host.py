@@ -151,6 +151,57 @@ def test_groups_cover_every_block_once(lib, name, orient):
     assert np.all(np.diff(np.diff(ptr)[order]) <= 0)
 
 
+def _chunk_layouts():
+    out = dict(LAYOUTS)
+    lay = np.eye(1100, dtype=np.uint8)[None].copy()
+    lay[0, 550, :] = 1  # one row of 1100 blocks of 16: 35 KB in bf16, 70 KB in fp32
+    out["one_long_row"] = (lay, 16)
+    return out
+
+
+CHUNK_LAYOUTS = _chunk_layouts()
+
+
+@pytest.mark.parametrize("elt", [2, 4])
+@pytest.mark.parametrize("name", sorted(CHUNK_LAYOUTS))
+def test_softmax_chunks_cover_every_row_once(lib, name, elt):
+    """The softmax chunk list: every row of every non-empty block-row exactly
+    once, block-rows in memory order; R a power of two, the largest within the
+    documented budget (twice the longest row's bytes, 24 KB to 64 KB); the first
+    block id is the block-row's first row-major position; the list is marked
+    unusable exactly when a row alone exceeds the budget."""
+    lay, B = CHUNK_LAYOUTS[name]
+    L = bsp.bsp_layout_plan(lay, B)
+    C = L.softmax_chunks(elt)
+    H, nb = lay.shape[0], lay.shape[1]
+    row_len = (lay.reshape(H * nb, nb) != 0).sum(axis=1)
+    first = np.concatenate([[0], np.cumsum(row_len)[:-1]])
+    budget = min(64 * 1024, max(24 * 1024, 2 * int(row_len.max()) * B * elt))
+    items = C["items"]
+    keys = items[:, 0]
+    assert np.all(np.diff(keys) >= 0)
+    covered = {}
+    for key, p0, n, w in items.tolist():
+        r0, R = w & 0xFFFF, w >> 16
+        assert p0 == first[key] and n == row_len[key] and n > 0
+        assert R >= 1 and R & (R - 1) == 0 and r0 % R == 0 and r0 + R <= B
+        if C["fits"]:
+            assert R * n * B * elt <= budget
+            assert R == B or 2 * R * n * B * elt > budget  # the largest such power of two
+        covered.setdefault(key, []).extend(range(r0, r0 + R))
+    assert sorted(covered) == [k for k in range(H * nb) if row_len[k] > 0]
+    for key, rows in covered.items():
+        assert sorted(rows) == list(range(B)), f"block-row {key}: rows {rows}"
+    assert C["fits"] == bool(int(row_len.max()) * B * elt <= budget)
+    if len(items):
+        assert C["max_bytes"] == max((w >> 16) * n * B * elt for _, _, n, w in items.tolist())
+
+
+def test_softmax_chunks_reject_bad_element_size(lib):
+    L = bsp.bsp_layout_plan(np.ones((1, 2, 2), np.uint8), 64)
+    assert lib.bsp_layout_softmax_chunks(L.handle, 8, None, None, None, None) == -1
+
+
 def test_groups_reject_bad_orient(lib):
     L = bsp.bsp_layout_plan(np.ones((1, 2, 2), np.uint8), 64)
     assert lib.bsp_layout_groups(L.handle, 2, None, None, None, None, None, None, None) == -1

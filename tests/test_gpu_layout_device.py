@@ -1,5 +1,6 @@
 """On-device layout compilation (bsp_layout_compile_device) against the host
-compiler: every table bit-exact on the workload layouts and edge layouts, the
+compiler: every table (softmax chunk lists included) bit-exact on the workload
+layouts and edge layouts, the
 compute calls give identical results with either handle, invalid values and
 oversize layouts are rejected."""
 
@@ -62,6 +63,10 @@ def test_device_tables_equal_host_tables(bsp, name):
         assert hg["n_slots"] == dg["n_slots"]
         for k in ("grp_ptr", "grp_order", "slot_idx", "slot_blk"):
             assert np.array_equal(hg[k], dg[k]), (o, k)
+    for elt in (2, 4):
+        hc, dc = host.softmax_chunks(elt), dev.softmax_chunks(elt)
+        assert hc["fits"] == dc["fits"] and hc["max_bytes"] == dc["max_bytes"], elt
+        assert np.array_equal(hc["items"], dc["items"]), elt
 
 
 @pytest.mark.parametrize("name", ["tiny", "strided"])
