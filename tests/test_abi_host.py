@@ -197,6 +197,29 @@ def test_softmax_chunks_cover_every_row_once(lib, name, elt):
         assert C["max_bytes"] == max((w >> 16) * n * B * elt for _, _, n, w in items.tolist())
 
 
+@pytest.mark.parametrize("n_long,budget,fits", [(96, 24 * 1024, True), (97, 2 * 97 * 128, True),
+                                                (256, 64 * 1024, True), (257, 64 * 1024, True),
+                                                (513, 64 * 1024, False)])
+def test_softmax_chunk_budget_boundaries(lib, n_long, budget, fits):
+    """Budget = twice the longest row (blocks of 64, bf16: 128 bytes a block),
+    24 KB at least and 64 KB at most; a 96-block row (12 KB) sits on the lower
+    bound, a 513-block row (65.7 KB) no longer fits a chunk."""
+    nb = max(n_long, 4)
+    lay = np.eye(nb, dtype=np.uint8)[None].copy()
+    lay[0, 1, :n_long] = 1
+    L = bsp.bsp_layout_plan(lay, 64)
+    C = L.softmax_chunks(2)
+    assert C["fits"] == fits
+    items = C["items"]
+    long_rows = items[items[:, 0] == 1]
+    R = int(long_rows[0, 3]) >> 16
+    row_bytes = n_long * 64 * 2
+    if fits:
+        assert R * row_bytes <= budget and (R == 64 or 2 * R * row_bytes > budget)
+    short = items[items[:, 0] == 0]
+    assert int(short[0, 3]) >> 16 == 64  # one-block rows: the whole block-row in one chunk
+
+
 def test_softmax_chunks_reject_bad_element_size(lib):
     L = bsp.bsp_layout_plan(np.ones((1, 2, 2), np.uint8), 64)
     assert lib.bsp_layout_softmax_chunks(L.handle, 8, None, None, None, None) == -1
