@@ -170,15 +170,17 @@ def test_softmax_is_stable_for_large_inputs(oracle):
     np.testing.assert_allclose(got_big, got, rtol=1e-9, atol=1e-12)
 
 
-def test_softmax_rows_matches_full(oracle):
+@pytest.mark.parametrize("kind", [W.MASK_NONE, W.MASK_DENSE, W.MASK_DIAG_CAUSAL])
+def test_softmax_rows_matches_full(oracle, kind):
     Z, H, nb, B = 2, 2, 5, 4
     S = nb * B
     lay = random_layout(H, nb, 0.5, 15)
     nnz = int(lay.sum())
     X = rand(Z, nnz, B, B, seed=16)
-    full = libref.blocks_to_dense(lay, B, oracle.softmax(lay, B, X, 0.8, W.MASK_DIAG_CAUSAL))
+    mask = W.random_mask(S, 0.7, 17) if kind == W.MASK_DENSE else None
+    full = libref.blocks_to_dense(lay, B, oracle.softmax(lay, B, X, 0.8, kind, mask))
     sel = np.array([0, 7, S + 3, 2 * H * S - 1])
-    got = oracle.softmax_rows(lay, B, X, 0.8, W.MASK_DIAG_CAUSAL, sel=sel)
+    got = oracle.softmax_rows(lay, B, X, 0.8, kind, mask, sel=sel)
     np.testing.assert_allclose(got, full.reshape(-1, S)[sel], rtol=1e-15, atol=0)
 
 
