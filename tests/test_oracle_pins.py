@@ -316,13 +316,16 @@ def test_attention_equals_sdd_softmax_dsd_chain(oracle, kind):
     np.testing.assert_allclose(chain, direct, rtol=1e-5, atol=1e-6)
 
 
-def test_attention_selection_matches_full(oracle):
+@pytest.mark.parametrize("kind", [W.MASK_NONE, W.MASK_DENSE, W.MASK_DIAG_CAUSAL])
+def test_attention_selection_matches_full(oracle, kind):
     Z, H, S, D, B = 2, 2, 32, 8, 8
     lay = random_layout(H, S // B, 0.5, 52)
     Q, K, V = rand(Z, H, S, D, seed=53), rand(Z, H, S, D, seed=54), rand(Z, H, S, D, seed=55)
-    full = oracle.attention(lay, B, Q, K, V, 0.5)
+    mask = W.random_mask(S, 0.7, 56) if kind == W.MASK_DENSE else None
+    full = oracle.attention(lay, B, Q, K, V, 0.5, kind, mask)
     sel = np.array([3, S + 5, 3 * S + 31])
-    np.testing.assert_array_equal(oracle.attention(lay, B, Q, K, V, 0.5, sel=sel), full.reshape(-1, D)[sel])
+    np.testing.assert_array_equal(oracle.attention(lay, B, Q, K, V, 0.5, kind, mask, sel=sel),
+                                  full.reshape(-1, D)[sel])
 
 
 # ------------------------------------------------------------ backward ----
