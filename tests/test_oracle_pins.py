@@ -242,6 +242,24 @@ def test_dds_empty_cols_are_zero(oracle):
     assert np.all(got[0, 0, :, 8:12] == 0.0)
 
 
+@pytest.mark.parametrize("trans_a,trans_b", [(0, 0), (1, 1)])
+def test_dsd_dds_selection_matches_full(oracle, trans_a, trans_b):
+    # the sampled-row forms used by the full-size GPU tests
+    Z, H, nb, B, N = 2, 2, 5, 4, 6
+    S = nb * B
+    lay = random_layout(H, nb, 0.4, 30)
+    nnz = int(lay.sum())
+    Sp = rand(Z, nnz, B, B, seed=31)
+    Bd = rand(Z, H, N, S, seed=32) if trans_b else rand(Z, H, S, N, seed=32)
+    full = oracle.dsd(lay, B, Sp, Bd, trans_a, trans_b)
+    sel = np.array([0, 9, S + 4, Z * H * S - 1])
+    np.testing.assert_array_equal(oracle.dsd(lay, B, Sp, Bd, trans_a, trans_b, sel=sel), full.reshape(-1, N)[sel])
+    Ad = rand(Z, H, S, N, seed=33) if trans_a else rand(Z, H, N, S, seed=33)
+    full = oracle.dds(lay, B, Ad, Sp, trans_a, trans_b)
+    sel = np.array([0, 5, N + 1, Z * H * N - 1])
+    np.testing.assert_array_equal(oracle.dds(lay, B, Ad, Sp, trans_a, trans_b, sel=sel), full.reshape(-1, S)[sel])
+
+
 # ----------------------------------------------------------- attention ----
 
 def test_attention_all_ones_is_dense_attention(oracle):
