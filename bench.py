@@ -32,6 +32,7 @@ sys.path.insert(0, ROOT)
 METRIC = "block-sparse attention TFLOP/s (nonzero-block FLOPs) and % of GB300 peak"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+W_ATTENTION = ("band", "strided", "bigbird", "tiny")
 
 
 def parse():
@@ -42,6 +43,8 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="band", choices=["band", "strided", "bigbird", "tiny"])
     p.add_argument("--no-ops", action="store_true", help="skip the per-op section")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip the other workloads' attention / softmax / spMM section")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="target oracle CPU time")
     p.add_argument("--skip-cpu", action="store_true", help="no CPU-baseline leg (profiling runs)")
     p.add_argument("--skip-e2e", action="store_true", help="no end-to-end leg (profiling runs)")
@@ -387,6 +390,119 @@ def per_op_section(w, lay, L, q, k, v, pk, bsp, stream):
     return out
 
 
+def ffma_peak(clocks, torch):
+    """fp32 FFMA peak from the unit counts and the highest sampled SM clock:
+    128 FP32 lanes per SM, 2 FLOP per FMA."""
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    mhz = clocks["sm_max_mhz"] if clocks else 2070.0
+    return sms * 128 * 2 * mhz * 1e6 / 1e12, f"derived: {sms} SMs x 128 FFMA/clk x 2 FLOP x {mhz:.0f} MHz"
+
+
+def attention_roofline(w, achieved, clocks, pk, pk_kind, torch):
+    if w.dtype != "f32":
+        bound, peak, src = "tensor", pk["bf16_tflops"], f"bf16_tflops (burst) of {pk_kind}"
+    else:
+        # fp32 runs on the FFMA path
+        bound = "alu"
+        peak, src = ffma_peak(clocks, torch)
+    return {"bound": bound, "kernel": "attention", "achieved": achieved, "peak": peak, "peak_source": src,
+            "unit": "TFLOP/s", "frac": achieved / peak if peak else None}
+
+
+def workload_section(w, bsp, stream, steps, warmup, pk, pk_kind, local):
+    """One attention workload timed the way the headline is (W warm-ups, K
+    timed launches, L2 flushed before each step when the inputs fit in L2,
+    clocks sampled during the timed steps), plus its softmax on SDD-shaped
+    input (every call cold in L2), each against its own roofline."""
+    import torch
+    lay = w.layout()
+    L = bsp.bsp_layout_compile(lay, w.B)
+    Qc, Kc, Vc = w.qkv()
+    q, k, v = (t.cuda() for t in (Qc, Kc, Vc))
+    o = torch.empty_like(q)
+    flops = nonzero_flops(lay, w.B, w.D, w.Z)
+    l2_bytes = torch.cuda.get_device_properties(local).L2_cache_size
+    flush = input_bytes(w) < 2 * l2_bytes
+    scratch = torch.empty(2 * l2_bytes if flush else 0, dtype=torch.uint8, device="cuda")
+    for _ in range(max(3, warmup)):
+        bsp.bsp_attention(L, q, k, v, o, w.scale, w.mask_kind)
+    torch.cuda.synchronize()
+    if bsp.bsp_status_check(L) != 0:
+        raise RuntimeError(f"device status after warm-up of {w.name}")
+    with ClockSampler(local) as clk:
+        spans = []
+        if flush:
+            for _ in range(steps):
+                scratch.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                bsp.bsp_attention(L, q, k, v, o, w.scale, w.mask_kind)
+                e1.record(stream)
+                spans.append((e0, e1))
+        else:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                bsp.bsp_attention(L, q, k, v, o, w.scale, w.mask_kind)
+            e1.record(stream)
+            spans.append((e0, e1))
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b_) for a, b_ in spans) / steps
+        # softmax of SDD-shaped input in the workload's dtype
+        X = W_randn((w.Z, L.nnz, w.B, w.B), w.dtype, 77).cuda()
+        Y = torch.empty_like(X)
+        sms = time_launches(lambda: bsp.bsp_softmax(L, X, Y, w.scale, w.mask_kind), steps, stream)
+    clocks = clk.summary()
+    achieved = flops / (ms * 1e-3) / 1e12
+    sbytes = 2.0 * X.numel() * X.element_size()
+    gbs = sbytes / sms / 1e6
+    out = {
+        "config": config_of(w, lay, "fused attention kernel", flush),
+        "attention": {"ms": ms, "TFLOP/s": achieved, "gpu_launches": steps,
+                      "roofline": attention_roofline(w, achieved, clocks, pk, pk_kind, torch)},
+        "softmax": {"ms": sms, "GB/s": gbs,
+                    "roofline": {"bound": "hbm", "kernel": "softmax", "achieved": gbs, "peak": pk["hbm_gbs"],
+                                 "peak_source": f"hbm_gbs of {pk_kind}", "unit": "GB/s",
+                                 "frac": gbs / pk["hbm_gbs"], "algorithmic_bytes_per_launch": sbytes}},
+        "clocks": clocks,
+    }
+    del X, Y, q, k, v, o, scratch
+    return out
+
+
+def spmm_section(bsp, stream, steps, pk, pk_kind, local, B=32, density=0.25):
+    """DSD and DDS on the general spMM workload (8192^2 sparse, 8192 x 4096
+    dense, bf16) at one block size and density, every call cold in L2."""
+    import torch
+    from sparse_attention_layout_gb300 import workloads as W
+    sp = W.SPMM_BLOCKS[B]
+    lay = sp.layout(density)
+    L = bsp.bsp_layout_compile(lay, B)
+    A = sp.sparse_values(L.nnz, density).cuda()
+    Bd, Ad = sp.dense_dsd(density).cuda(), sp.dense_dds(density).cuda()
+    C1, C2 = bsp.bsp_dsd(L, A, Bd), bsp.bsp_dds(L, Ad, A)
+    fl = 2.0 * B * B * sp.N * L.nnz
+    with ClockSampler(local) as clk:
+        ms1 = time_launches(lambda: bsp.bsp_dsd(L, A, Bd, C1), steps, stream)
+        ms2 = time_launches(lambda: bsp.bsp_dds(L, Ad, A, C2), steps, stream)
+    out = {"workload": f"spmm: sparse {sp.S}x{sp.S} (block {B}, {L.nnz} of {(sp.S // B) ** 2} blocks, "
+                       f"{100 * density:.0f}%) x dense {sp.S}x{sp.N}, bf16",
+           "clocks": clk.summary()}
+    for name, ms in (("dsd", ms1), ("dds", ms2)):
+        t = fl / ms / 1e9
+        out[name] = {"ms": ms, "TFLOP/s": t,
+                     "roofline": {"bound": "tensor", "kernel": "spmm_group", "achieved": t,
+                                  "peak": pk["bf16_tflops"], "peak_source": f"bf16_tflops (burst) of {pk_kind}",
+                                  "unit": "TFLOP/s", "frac": t / pk["bf16_tflops"]}}
+    del A, Bd, Ad, C1, C2
+    return out
+
+
+def W_randn(shape, dtype, seed):
+    from sparse_attention_layout_gb300 import workloads as W
+    return W.randn(shape, dtype, seed)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -506,6 +622,19 @@ def run_ours(args):
     if not args.no_ops and rank == 0:
         ops = per_op_section(w, lay, L, q, k, v, pk, bsp, stream)
     torch.cuda.synchronize()
+    # the other attention workloads and the spMM workload at 25 %, each with
+    # its own clocks and rooflines (rank 0; the headline above is the job's)
+    workloads = None
+    if not args.no_workloads and rank == 0:
+        del q, k, v, o
+        torch.cuda.empty_cache()
+        workloads = {}
+        for name in W_ATTENTION:
+            if name != w.name:
+                workloads[name] = workload_section(workload(name), bsp, stream, args.steps, args.warmup, pk,
+                                                   pk_kind, local)
+        workloads["spmm_B32_25pct"] = spmm_section(bsp, stream, min(args.steps, 10), pk, pk_kind, local)
+        torch.cuda.synchronize()
 
     if rank != 0:
         if world > 1:
@@ -519,15 +648,9 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     clocks = clk.summary()
-    if w.dtype != "f32":
-        bound, peak, peak_src = "tensor", pk["bf16_tflops"], f"bf16_tflops (burst) of {pk_kind}"
-    else:
-        # fp32 runs on the FFMA path: 128 FP32 lanes per SM, 2 FLOP per FMA, at
-        # the highest SM clock the sampler saw (else the GB300's 2070 MHz)
-        sms = torch.cuda.get_device_properties(0).multi_processor_count
-        mhz = clocks["sm_max_mhz"] if clocks else 2070.0
-        bound, peak = "alu", sms * 128 * 2 * mhz * 1e6 / 1e12
-        peak_src = f"derived: {sms} SMs x 128 FFMA/clk x 2 FLOP x {mhz:.0f} MHz"
+    roof = attention_roofline(w, achieved, clocks, pk, pk_kind, torch)
+    roof["traffic"] = traffic_for("attention", w.name)
+    roof["algorithmic_flops_per_launch"] = flops
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -535,13 +658,7 @@ def run_ours(args):
         "config": config_of(w, lay, "fused attention kernel" + (", replayed from a CUDA graph" if args.graph else ""),
                             flush),
         "gpu_launches": args.steps,
-        "roofline": {
-            "bound": bound, "kernel": "attention", "achieved": achieved, "peak": peak,
-            "peak_source": peak_src, "unit": "TFLOP/s",
-            "frac": (achieved / peak) if peak else None,
-            "traffic": traffic_for("attention", w.name),
-            "algorithmic_flops_per_launch": flops,
-        },
+        "roofline": roof,
         "e2e": None if e2e_ms is None else {
             "value": flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
@@ -552,6 +669,8 @@ def run_ours(args):
     }
     if ops is not None:
         line["ops"] = ops
+    if workloads is not None:
+        line["workloads"] = workloads
     print(json.dumps(line), flush=True)
 
 

@@ -268,7 +268,9 @@ int bsp_softmax(bsp_layout_t layout, int dtype, const void* X, void* Y, int Z, f
  *    softmax chunk list) exceed the array return BSP_ERR_OOM and launch
  *    nothing.
  *  - The first call on a device looks up the array's device address with that
- *    device current; make that first call before any stream capture.
+ *    device current; make that first call before any stream capture.  The
+ *    address is kept for the life of the process, so calls after a reset of
+ *    that device's context (cudaDeviceReset) are not supported.
  *  - Every call shares the array and it keeps the last call's tables; calls
  *    that overlap on the GPU (e.g. on two streams) race.  Calls ordered on one
  *    stream are safe.
@@ -329,9 +331,11 @@ int bsp_attention_backward(bsp_layout_t layout, int dtype, const void* Q, const 
  * mask: DEVICE [S][S] as in bsp_attention.  flags: 0, or
  * BSP_HOST_RESERVED_WORKSPACE — the caller promises that nothing but this
  * handle's calls touches the workspace between them; a call given the same
- * workspace as the handle's previous call then starts its input copies as
- * soon as the slots they fill are free (overlapping the previous call's last
- * kernel and output copy) instead of after all the work on `stream`.  Calls
+ * workspace as the handle's previous call, sliced into slots of the same size
+ * (same batch slicing, D and dtype), then starts its input copies as soon as
+ * the slots they fill are free (overlapping the previous call's last kernel
+ * and output copy) instead of after all the work on `stream`; a call whose
+ * slots differ in size waits for all the work on `stream` first.  Calls
  * that share a handle must not run concurrently from several host threads.
  * Workspace smaller than one slice or unknown flags: BSP_ERR_INVALID_ARG.
  * (Not from the pages: the end-to-end path through host memory.) */

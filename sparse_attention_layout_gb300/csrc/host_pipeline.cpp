@@ -16,6 +16,7 @@
 struct HostPipe {
     cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
     const void* last_ws = nullptr;  // workspace of the previous call
+    size_t last_slot_bytes = 0;     // and the size of each of its two slots
     cudaEvent_t start = nullptr, done = nullptr, in[2] = {nullptr, nullptr}, out[2] = {nullptr, nullptr},
                 freed[2] = {nullptr, nullptr};
 };
@@ -89,15 +90,21 @@ extern "C" int bsp_attention_host(bsp_layout_t L, int dtype, const void* Qh, con
     auto fail = [&]() { cudaGetLastError(); return BSP_ERR_CUDA; };
     // kernels and output copies after the work already queued on the caller's
     // stream; input copies too, unless the workspace is reserved for this
-    // handle and was the previous call's: then they only wait (below) for
-    // the slot they fill to be free, and may overlap the previous call's tail
-    const bool early = (flags & BSP_HOST_RESERVED_WORKSPACE) && p->last_ws == workspace;
+    // handle and was the previous call's, cut into slots of the same size:
+    // then slot k covers exactly the bytes of the previous call's slot k, so
+    // the input copies only wait (below) for that slot to be free and may
+    // overlap the previous call's tail.  Slots of another size (another batch
+    // slicing, head size or dtype) could overlap the previous call's other
+    // slot, so such a call waits for everything queued before it.
+    const bool early = (flags & BSP_HOST_RESERVED_WORKSPACE) && p->last_ws == workspace &&
+                       p->last_slot_bytes == slot_bytes;
     if (cudaEventRecord(p->start, caller) != cudaSuccess) return fail();
     for (cudaStream_t s : {p->h2d, p->comp, p->d2h}) {
         if (early && s == p->h2d) continue;
         if (cudaStreamWaitEvent(s, p->start, 0) != cudaSuccess) return fail();
     }
     p->last_ws = workspace;
+    p->last_slot_bytes = slot_bytes;
     const int nsl = (Z + zs - 1) / zs;
     for (int k = 0; k < nsl; ++k) {
         const int z0 = k * zs, nz = std::min(zs, Z - z0), slot = k & 1;

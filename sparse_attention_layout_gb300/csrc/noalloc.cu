@@ -31,7 +31,9 @@ std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of g_scratch on the current device.  The first call on a
-// device performs the lookup with that device current.
+// device performs the lookup with that device current; the address is kept
+// for the life of the process (a reset of the device's context, after which
+// the module is loaded again elsewhere, is not supported).
 int scratch_address(void** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BSP_ERR_CUDA;

@@ -87,3 +87,24 @@ def test_host_repeated_calls_reuse_slots(bsp, reserved):
     torch.cuda.synchronize()
     for O, Q, K, V in outs:
         assert torch.equal(O, bsp.bsp_attention(L, Q.cuda(), K.cuda(), V.cuda(), None, 0.125).cpu())
+
+
+def test_host_reserved_workspace_calls_of_changing_slot_size(bsp):
+    # calls on one handle and one reserved workspace whose slots change size
+    # from call to call (batch size, so the slicing, and head size change): a
+    # call whose slots differ from the previous call's must not start its
+    # input copies before that call's kernels and output copies are done, since
+    # its slot 0 can cover the previous call's slot 1
+    B, nb, H = 64, 4, 2
+    L = bsp.bsp_layout_compile(W.layout_band(nb, 1, H), B)
+    S = nb * B
+    ws = torch.empty(bsp.bsp_attention_host_workspace(L, torch.bfloat16, 128, 2), dtype=torch.uint8,
+                     device="cuda")
+    outs = []
+    for rep, (Z, D) in enumerate([(4, 128), (6, 64), (2, 64), (5, 128), (8, 64), (3, 128), (4, 128)]):
+        Q, K, V = (W.randn((Z, H, S, D), "bf16", 430 + 3 * rep + s).pin_memory() for s in range(3))
+        O = bsp.bsp_attention_host(L, Q, K, V, None, 0.125, workspace=ws, reserved_workspace=True)
+        outs.append((O, Q, K, V))
+    torch.cuda.synchronize()
+    for O, Q, K, V in outs:
+        assert torch.equal(O, bsp.bsp_attention(L, Q.cuda(), K.cuda(), V.cuda(), None, 0.125).cpu())

@@ -4,7 +4,11 @@ size, each dtype, each mask kind and both kernel paths (tensor-core where it
 applies, CUDA-core forced with BSP_FORCE_SIMT=1).
 
 Tolerance (normwise max |g - r| / max |r|): 1e-5 for fp32 outputs, 2e-2 for
-bf16 / fp16 outputs."""
+bf16 / fp16 outputs; on top of it every entry is bounded (tests/gpu_util.py):
+softmax outputs by an elementwise relative bound from the output's unit
+roundoff, with the entries the oracle defines as 0 (masked, empty rows) exactly
+0; products by their forward error bound against the same product of the
+operands' absolute values."""
 
 import os
 
@@ -12,7 +16,8 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import TOL, assert_close, dev, normwise_err, to_np
+from gpu_util import (PROB_TOL, assert_close, attention_acc, dev, gamma, softmax_rel_bound,
+                      softmax_zero_positions, to_np)
 from sparse_attention_layout_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -71,7 +76,8 @@ def test_softmax(bsp, oracle, B, dt, kind):
                         mask=None if mask is None else dev(torch.from_numpy(mask)))
     torch.cuda.synchronize()
     want = oracle.softmax(lay, B, X, 0.3, kind, mask)
-    assert_close(to_np(Y), want, dtype, f"softmax B={B} {dt} kind={kind}")
+    assert_close(to_np(Y), want, dtype, f"softmax B={B} {dt} kind={kind}", rel=PROB_TOL[dtype],
+                 zeros=softmax_zero_positions(lay, B, Z, kind, mask))
     assert bsp.bsp_status_check(L) == 0
 
 
@@ -89,7 +95,8 @@ def test_softmax_long_rows_and_in_place(bsp, oracle, dt, nb):
     bsp.bsp_softmax(L, Xd, Xd, scale=1.7, mask_kind=2)
     torch.cuda.synchronize()
     want = oracle.softmax(lay, B, X, 1.7, 2)
-    assert_close(to_np(Xd), want, dtype, f"softmax long/in-place nb={nb}")
+    assert_close(to_np(Xd), want, dtype, f"softmax long/in-place nb={nb}", rel=PROB_TOL[dtype],
+                 zeros=softmax_zero_positions(lay, B, 1, 2))
 
 
 @pytest.mark.parametrize("B,dt,nb,kind", [(128, "bf16", 260, 0), (128, "bf16", 260, 2),
@@ -129,7 +136,17 @@ def test_softmax_rows_longer_than_a_chunk(bsp, oracle, B, dt, nb, kind):
         i, a = divmod(int(r), B)
         for j in np.flatnonzero(lay[0, i]):
             got[t, j * B:(j + 1) * B] = Yh[0, ids[0, i, j], a]
-    assert_close(got, want, dtype, f"softmax rows > 64 KB B={B} {dt} kind={kind}")
+    # zeros of the dense rows: outside the row's blocks, masked, or the row keeps nothing
+    keep = np.ones((sel.size, S), dtype=bool)
+    for t, r in enumerate(sel):
+        keep[t] = np.repeat(lay[0, int(r) // B].astype(bool), B)
+        if kind == 1:
+            keep[t] &= mask[int(r)].astype(bool)
+        elif kind == 2:
+            keep[t] &= (np.arange(S) // B != int(r) // B) | (np.arange(S) <= int(r))
+    keep &= keep.any(axis=1, keepdims=True)
+    assert_close(got, want, dtype, f"softmax rows > 64 KB B={B} {dt} kind={kind}", rel=PROB_TOL[dtype],
+                 zeros=~keep)
 
 
 # --------------------------------------------------------------- SDD ----
@@ -150,7 +167,8 @@ def test_sdd(bsp, oracle, path, B, dt, trans):
     C = bsp.bsp_sdd(L, dev(A), dev(Bm), trans_a=ta, trans_b=tb)
     torch.cuda.synchronize()
     want = oracle.sdd(lay, B, A, Bm, ta, tb)
-    assert_close(to_np(C), want, dtype, f"sdd B={B} {dt} trans={trans} {path}")
+    mag = oracle.sdd(lay, B, A.abs(), Bm.abs(), ta, tb)
+    assert_close(to_np(C), want, dtype, f"sdd B={B} {dt} trans={trans} {path}", mag=mag, acc=gamma(K))
 
 
 @pytest.mark.parametrize("B", [32, 128])
@@ -171,7 +189,8 @@ def test_sdd_contraction_lengths(bsp, oracle, path, B, K, trans):
     Bm = randn((Z, H, S, K) if tb else (Z, H, K, S), dtype, 34)
     C = bsp.bsp_sdd(L, dev(A), dev(Bm), trans_a=ta, trans_b=tb)
     torch.cuda.synchronize()
-    assert_close(to_np(C), oracle.sdd(lay, B, A, Bm, ta, tb), dtype, f"sdd B={B} K={K} trans={trans} {path}")
+    assert_close(to_np(C), oracle.sdd(lay, B, A, Bm, ta, tb), dtype, f"sdd B={B} K={K} trans={trans} {path}",
+                 mag=oracle.sdd(lay, B, A.abs(), Bm.abs(), ta, tb), acc=gamma(K))
 
 
 @pytest.mark.parametrize("B", [16, 32, 64, 128])
@@ -192,8 +211,12 @@ def test_sdd_softmax(bsp, oracle, path, B, dt, kind):
     P = bsp.bsp_sdd_softmax(L, dev(A), dev(Bm), scale=0.2, mask_kind=kind,
                             mask=None if mask is None else dev(torch.from_numpy(mask)))
     torch.cuda.synchronize()
-    want = oracle.softmax(lay, B, oracle.sdd(lay, B, A, Bm), 0.2, kind, mask)
-    assert_close(to_np(P), want, dtype, f"sdd_softmax B={B} {dt} kind={kind} {path}")
+    s_ref = oracle.sdd(lay, B, A, Bm)
+    want = oracle.softmax(lay, B, s_ref, 0.2, kind, mask)
+    rel = softmax_rel_bound(lay, B, s_ref, oracle.sdd(lay, B, A.abs(), Bm.abs()), 0.2, K, dtype,
+                            scores_rounded=(path == "simt"))
+    assert_close(to_np(P), want, dtype, f"sdd_softmax B={B} {dt} kind={kind} {path}", rel=rel,
+                 zeros=softmax_zero_positions(lay, B, Z, kind, mask))
     assert bsp.bsp_status_check(L) == 0
 
 
@@ -208,8 +231,12 @@ def test_sdd_softmax_orientations(bsp, oracle, path, trans):
     Bm = randn((Z, H, S, K) if tb else (Z, H, K, S), torch.bfloat16, 39)
     P = bsp.bsp_sdd_softmax(L, dev(A), dev(Bm), scale=0.15, mask_kind=2, trans_a=ta, trans_b=tb)
     torch.cuda.synchronize()
-    want = oracle.softmax(lay, B, oracle.sdd(lay, B, A, Bm, ta, tb), 0.15, 2)
-    assert_close(to_np(P), want, torch.bfloat16, f"sdd_softmax trans={trans} {path}")
+    s_ref = oracle.sdd(lay, B, A, Bm, ta, tb)
+    want = oracle.softmax(lay, B, s_ref, 0.15, 2)
+    rel = softmax_rel_bound(lay, B, s_ref, oracle.sdd(lay, B, A.abs(), Bm.abs(), ta, tb), 0.15, K,
+                            torch.bfloat16, scores_rounded=(path == "simt"))
+    assert_close(to_np(P), want, torch.bfloat16, f"sdd_softmax trans={trans} {path}", rel=rel,
+                 zeros=softmax_zero_positions(lay, B, Z, 2))
 
 
 def test_sdd_leaves_absent_blocks_untouched(bsp, path):
@@ -247,7 +274,8 @@ def test_dsd(bsp, oracle, path, B, dt, trans, N):
     C = bsp.bsp_dsd(L, dev(Asp), dev(Bd), trans_a=ta, trans_b=tb)
     torch.cuda.synchronize()
     want = oracle.dsd(lay, B, Asp, Bd, ta, tb)
-    assert_close(to_np(C), want, dtype, f"dsd B={B} {dt} trans={trans} {path}")
+    mag = oracle.dsd(lay, B, Asp.abs(), Bd.abs(), ta, tb)
+    assert_close(to_np(C), want, dtype, f"dsd B={B} {dt} trans={trans} {path}", mag=mag, acc=gamma(S))
 
 
 # --------------------------------------------------------------- DDS ----
@@ -269,7 +297,8 @@ def test_dds(bsp, oracle, path, B, dt, trans, M):
     C = bsp.bsp_dds(L, dev(Ad), dev(Bsp), trans_a=ta, trans_b=tb)
     torch.cuda.synchronize()
     want = oracle.dds(lay, B, Ad, Bsp, ta, tb)
-    assert_close(to_np(C), want, dtype, f"dds B={B} {dt} trans={trans} {path}")
+    mag = oracle.dds(lay, B, Ad.abs(), Bsp.abs(), ta, tb)
+    assert_close(to_np(C), want, dtype, f"dds B={B} {dt} trans={trans} {path}", mag=mag, acc=gamma(S))
 
 
 # --------------------------------------------------------- attention ----
@@ -292,7 +321,9 @@ def test_attention(bsp, oracle, path, B, dt, D, kind):
                           mask=None if mask is None else dev(torch.from_numpy(mask)))
     torch.cuda.synchronize()
     want = oracle.attention(lay, B, Q, K, V, scale, kind, mask)
-    assert_close(to_np(O), want, dtype, f"attention B={B} {dt} D={D} kind={kind} {path}")
+    mag = oracle.attention(lay, B, Q, K, V.abs(), scale, kind, mask)
+    assert_close(to_np(O), want, dtype, f"attention B={B} {dt} D={D} kind={kind} {path}", mag=mag,
+                 acc=attention_acc(Q, K, scale, dtype, S))
     assert bsp.bsp_status_check(L) == 0
 
 
@@ -307,7 +338,10 @@ def test_unfused_chain_matches_oracle(bsp, oracle, dt):
     O = bsp.attention_unfused(L, dev(Q), dev(K), dev(V), 0.125, 2)
     torch.cuda.synchronize()
     want = oracle.attention(lay, B, Q, K, V, 0.125, 2)
-    assert_close(to_np(O), want, dtype, "unfused chain")
+    mag = oracle.attention(lay, B, Q, K, V.abs(), 0.125, 2)
+    # the chain rounds the scores and P to the data type between its steps
+    assert_close(to_np(O), want, dtype, "unfused chain", mag=mag,
+                 acc=attention_acc(Q, K, 0.125, dtype, nb * B, scores_rounded=True))
 
 
 def test_edge_empty_layout_and_zero_batch(bsp, oracle):

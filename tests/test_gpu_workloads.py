@@ -7,13 +7,19 @@ Workloads: tiny (Z1 H1 S256 D64 B16 fp32), bigbird (Z2 H12 S4096 D64 B64
 fp32, diagonal-causal), band (Z4 H16 S8192 D128 B128 bf16), strided (Z1 H32
 S16384 D128 B64 bf16, diagonal-causal) and the spMM workload (8192^2 sparse,
 block 32, bf16, 10/25/50 % density).  Tolerance: normwise max |g - r| / max |r|
-<= 1e-5 (fp32) or 2e-2 (bf16)."""
+<= 1e-5 (fp32) or 2e-2 (bf16), and every sampled entry within its own bound
+(tests/gpu_util.py): softmax rows elementwise, products by their forward error
+bound against the product of the operands' absolute values.  Row sums of the
+whole softmax output: |sum - 1| <= u + 1e-4 for 16-bit outputs (u the unit
+roundoff: each probability is rounded once, so the rounding moves a sum of 1
+by at most u) and <= 1e-5 for fp32; entries that the diagonal-causal mask
+removes are exactly 0 in the whole output."""
 
 import numpy as np
 import pytest
 import torch
 
-from gpu_util import TOL, assert_close, to_np
+from gpu_util import PROB_TOL, U, assert_close, attention_acc, gamma, to_np
 from sparse_attention_layout_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -29,6 +35,31 @@ def bsp():
     build.build()
     from sparse_attention_layout_gb300 import bsp as m
     return m
+
+
+def rowsum_tol(dtype):
+    """|sum of a softmax row - 1|: one rounding of each probability to the
+    output type moves the sum by at most u; the fp32 exponentials and the
+    normalisation by far less than 1e-4."""
+    return 1e-5 if dtype == torch.float32 else U[dtype] + 1e-4
+
+
+def check_rowsums_and_masked_zeros(w, lay, P):
+    """Every present row of the block-format softmax output P sums to 1, and
+    the entries above the diagonal of every diagonal block are exactly 0 when
+    the workload masks them (diagonal-causal)."""
+    hs, is_, js = np.nonzero(lay)
+    key = torch.from_numpy(hs * w.nb + is_).cuda()
+    rowsum = torch.zeros(w.Z, w.H * w.nb, w.B, device="cuda", dtype=torch.float64)
+    rowsum.index_add_(1, key, P.double().sum(dim=3))
+    present = torch.from_numpy(lay.sum(axis=2).reshape(-1) > 0).cuda()
+    dev = (rowsum[:, present] - 1.0).abs().max().item()
+    assert dev <= rowsum_tol(DT[w.dtype]), f"{w.name}: a row sums to 1 +- {dev:.3e}"
+    if w.mask_kind == W.MASK_DIAG_CAUSAL:
+        diag = torch.from_numpy(np.flatnonzero(is_ == js)).cuda()
+        upper = torch.triu(torch.ones(w.B, w.B, dtype=torch.bool, device="cuda"), 1)
+        leaked = (P[:, diag] != 0) & upper
+        assert not leaked.any(), f"{w.name}: {int(leaked.sum())} masked entries are not exactly 0"
 
 
 def sample_rows(w, lay, n, seed):
@@ -61,7 +92,9 @@ def test_attention_workload(bsp, oracle, name):
     sel = sample_rows(w, lay, 48, 7)
     got = to_np(o.reshape(-1, w.D)[torch.from_numpy(sel).cuda()])
     want = oracle.attention(lay, w.B, Q, K, V, w.scale, w.mask_kind, sel=sel)
-    assert_close(got, want, DT[w.dtype], f"{name} fused attention, {sel.size} sampled rows")
+    mag = oracle.attention(lay, w.B, Q, K, V.abs(), w.scale, w.mask_kind, sel=sel)
+    acc = attention_acc(q, k, w.scale, DT[w.dtype], w.S).reshape(-1, 1)[sel]
+    assert_close(got, want, DT[w.dtype], f"{name} fused attention, {sel.size} sampled rows", mag=mag, acc=acc)
 
 
 @pytest.mark.parametrize("name", ["tiny", "bigbird", "band", "strided"])
@@ -80,7 +113,9 @@ def test_unfused_chain_workload(bsp, oracle, name):
                                        [0, w.Z * L.nnz - 1]])).astype(np.int64)
     got_s = to_np(P.reshape(-1, w.B, w.B)[torch.from_numpy(blocks).cuda()])
     want_s = oracle.sdd(lay, w.B, Q, K, sel=blocks)
-    assert_close(got_s, want_s, DT[w.dtype], f"{name} SDD, {blocks.size} sampled blocks")
+    mag_s = oracle.sdd(lay, w.B, Q.abs(), K.abs(), sel=blocks)
+    assert_close(got_s, want_s, DT[w.dtype], f"{name} SDD, {blocks.size} sampled blocks", mag=mag_s,
+                 acc=gamma(w.D))
     bsp.bsp_softmax(L, P, P, w.scale, w.mask_kind)
     O = bsp.bsp_dsd(L, P, v)
     torch.cuda.synchronize()
@@ -88,9 +123,10 @@ def test_unfused_chain_workload(bsp, oracle, name):
     sel = sample_rows(w, lay, 48, 11)
     got = to_np(O.reshape(-1, w.D)[torch.from_numpy(sel).cuda()])
     want = oracle.attention(lay, w.B, Q, K, V, w.scale, w.mask_kind, sel=sel)
-    # the chain rounds the scores and the probabilities to the data type once more
-    # than the fused kernel; both stay inside the same bound
-    assert_close(got, want, DT[w.dtype], f"{name} unfused chain, {sel.size} sampled rows")
+    mag = oracle.attention(lay, w.B, Q, K, V.abs(), w.scale, w.mask_kind, sel=sel)
+    # the chain rounds the scores and the probabilities to the data type between its steps
+    acc = attention_acc(q, k, w.scale, DT[w.dtype], w.S, scores_rounded=True).reshape(-1, 1)[sel]
+    assert_close(got, want, DT[w.dtype], f"{name} unfused chain, {sel.size} sampled rows", mag=mag, acc=acc)
 
 
 @pytest.mark.parametrize("name", ["tiny", "bigbird", "band", "strided"])
@@ -106,17 +142,15 @@ def test_sdd_softmax_chain_workload(bsp, oracle, name):
     O = bsp.bsp_dsd(L, P, v)
     torch.cuda.synchronize()
     assert torch.isfinite(P).all() and torch.isfinite(O).all()
-    hs, is_, _ = np.nonzero(lay)
-    key = torch.from_numpy(hs * w.nb + is_).cuda()
-    rowsum = torch.zeros(w.Z, w.H * w.nb, w.B, device="cuda", dtype=torch.float64)
-    rowsum.index_add_(1, key, P.double().sum(dim=3))
-    present = torch.from_numpy(lay.sum(axis=2).reshape(-1) > 0).cuda()
-    tol = 1e-5 if w.dtype == "f32" else 2e-2
-    assert torch.allclose(rowsum[:, present], torch.ones_like(rowsum[:, present]), atol=tol * 8, rtol=0)
+    check_rowsums_and_masked_zeros(w, lay, P)
     sel = sample_rows(w, lay, 48, 13)
     got = to_np(O.reshape(-1, w.D)[torch.from_numpy(sel).cuda()])
     want = oracle.attention(lay, w.B, Q, K, V, w.scale, w.mask_kind, sel=sel)
-    assert_close(got, want, DT[w.dtype], f"{name} fused SDD+softmax chain, {sel.size} sampled rows")
+    mag = oracle.attention(lay, w.B, Q, K, V.abs(), w.scale, w.mask_kind, sel=sel)
+    # scores stay fp32 inside the fused kernel; P is rounded once before DSD
+    acc = attention_acc(q, k, w.scale, DT[w.dtype], w.S).reshape(-1, 1)[sel]
+    assert_close(got, want, DT[w.dtype], f"{name} fused SDD+softmax chain, {sel.size} sampled rows", mag=mag,
+                 acc=acc)
 
 
 @pytest.mark.parametrize("name", ["tiny", "bigbird", "band", "strided"])
@@ -130,27 +164,27 @@ def test_softmax_workload(bsp, oracle, name):
     Y = bsp.bsp_softmax(L, X.cuda(), None, w.scale, w.mask_kind)
     torch.cuda.synchronize()
     assert torch.isfinite(Y).all()
-    # row sums over the whole output: gather each row's slices through the layout
+    check_rowsums_and_masked_zeros(w, lay, Y)
     hs, is_, js = np.nonzero(lay)
-    key = torch.from_numpy(hs * w.nb + is_).cuda()
-    rowsum = torch.zeros(w.Z, w.H * w.nb, w.B, device="cuda", dtype=torch.float64)
-    rowsum.index_add_(1, key, Y.double().sum(dim=3))
-    present = torch.from_numpy(lay.sum(axis=2).reshape(-1) > 0).cuda()
-    tol = 1e-5 if w.dtype == "f32" else 2e-2
-    assert torch.allclose(rowsum[:, present], torch.ones_like(rowsum[:, present]), atol=tol * 8, rtol=0)
     sel = sample_rows(w, lay, 48, 5)
     want = oracle.softmax_rows(lay, w.B, X, w.scale, w.mask_kind, sel=sel)  # dense rows [n, S]
     Yh = to_np(Y)
     ids = -np.ones(lay.shape, np.int64)
     ids[hs, is_, js] = np.arange(hs.size)
     got = np.zeros_like(want)
+    keep = np.zeros(want.shape, dtype=bool)
+    cols = np.arange(w.S)
     for t, u in enumerate(sel):
         zh, r = divmod(int(u), w.S)
         z, h = divmod(zh, w.H)
         i, a = divmod(r, w.B)
         for j in np.flatnonzero(lay[h, i]):
             got[t, j * w.B:(j + 1) * w.B] = Yh[z, ids[h, i, j], a]
-    assert_close(got, want, DT[w.dtype], f"{name} softmax, {sel.size} sampled rows")
+        keep[t] = np.repeat(lay[h, i].astype(bool), w.B)
+        if w.mask_kind == W.MASK_DIAG_CAUSAL:
+            keep[t] &= (cols // w.B != i) | (cols <= r)
+    assert_close(got, want, DT[w.dtype], f"{name} softmax, {sel.size} sampled rows", rel=PROB_TOL[DT[w.dtype]],
+                 zeros=~keep)
 
 
 @pytest.mark.parametrize("B,density", [(32, d) for d in W.SPMM_DENSITIES] +
@@ -171,10 +205,12 @@ def test_spmm_workload(bsp, oracle, B, density):
     rows = np.unique(np.concatenate([rng.choice(sp.S, 10, replace=False), [0, sp.S - 1],
                                      empty_rows[:2] * sp.B])).astype(np.int64)
     got = to_np(C1[0, 0][torch.from_numpy(rows).cuda()])
-    assert_close(got, oracle.dsd(lay, sp.B, A, Bd, sel=rows), torch.bfloat16, f"DSD spMM B={B} {density}")
+    assert_close(got, oracle.dsd(lay, sp.B, A, Bd, sel=rows), torch.bfloat16, f"DSD spMM B={B} {density}",
+                 mag=oracle.dsd(lay, sp.B, A.abs(), Bd.abs(), sel=rows), acc=gamma(sp.S))
     mrows = np.unique(np.concatenate([rng.choice(sp.N, 6, replace=False), [0, sp.N - 1]])).astype(np.int64)
     got = to_np(C2[0, 0][torch.from_numpy(mrows).cuda()])
-    assert_close(got, oracle.dds(lay, sp.B, Ad, A, sel=mrows), torch.bfloat16, f"DDS spMM B={B} {density}")
+    assert_close(got, oracle.dds(lay, sp.B, Ad, A, sel=mrows), torch.bfloat16, f"DDS spMM B={B} {density}",
+                 mag=oracle.dds(lay, sp.B, Ad.abs(), A.abs(), sel=mrows), acc=gamma(sp.S))
     # block-rows without any block are exactly zero in the DSD output
     for i in empty_rows[:4]:
         assert (C1[0, 0, i * sp.B:(i + 1) * sp.B] == 0).all()
@@ -204,6 +240,8 @@ def test_long_sequence_band(bsp, oracle):
     w = SimpleNamespace(Z=Z, H=H, S=S, B=B)
     sel = sample_rows(w, lay, 40, 17)
     want = oracle.attention(lay, B, Q, K, V, scale, W.MASK_DIAG_CAUSAL, sel=sel)
+    mag = oracle.attention(lay, B, Q, K, V.abs(), scale, W.MASK_DIAG_CAUSAL, sel=sel)
+    acc = attention_acc(q, k, scale, torch.bfloat16, 5 * B).reshape(-1, 1)[sel]
     for got, what in ((o, "fused attention"), (o2, "fused SDD + softmax -> DSD")):
         g = to_np(got.reshape(-1, D)[torch.from_numpy(sel).cuda()])
-        assert_close(g, want, torch.bfloat16, f"S={S} {what}, {sel.size} sampled rows")
+        assert_close(g, want, torch.bfloat16, f"S={S} {what}, {sel.size} sampled rows", mag=mag, acc=acc)

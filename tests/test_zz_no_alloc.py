@@ -3,11 +3,14 @@ allocate device memory (a runtime that owns every byte of the GPU, a plugin
 handed only its buffers).  It keeps the layout tables in a fixed device array
 the library declares itself instead of a compiled handle.
 
-Checked through the C ABI against the existing entry point (bsp_softmax with a
-compiled handle), on two calls in a row with different layouts, block sizes,
-dtypes and masks, so the second call must not depend on what the first one
-left in the shared array.  Collected last (file name) so that a run stopping
-at the first failure has already run every other test."""
+Checked through the C ABI against the fp64 oracle (elementwise bound, masked
+entries exactly 0) and against the existing entry point (bsp_softmax with a
+compiled handle, which runs the same kernels on the same tables: identical
+bytes), on calls in a row with different layouts, block sizes, dtypes (fp32,
+bf16, fp16) and masks, so a call must not depend on what the previous one left
+in the shared array; one layout has a row longer than the largest softmax
+chunk, which takes the one-warp-per-row kernel.  Collected last (file name) so
+that a run stopping at the first failure has already run every other test."""
 
 import ctypes
 
@@ -15,7 +18,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import assert_close, to_np
+from gpu_util import PROB_TOL, assert_close, softmax_zero_positions, to_np
 from sparse_attention_layout_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -44,23 +47,43 @@ def _call(lib, lay, B, code, X, Y, scale, kind, mask):
                                    ctypes.c_void_p(0 if mask is None else mask.data_ptr()), stream)
 
 
-def test_noalloc_softmax_matches_compiled_handle_twice(lib):
+def _long_row_layout(nb):
+    lay = np.eye(nb, dtype=np.uint8)[None].copy()
+    lay[0, nb // 2, :] = 1
+    return lay
+
+
+def test_noalloc_softmax_matches_oracle_and_compiled_handle(lib, oracle):
     from sparse_attention_layout_gb300 import bsp
     cases = [  # (layout, block, dtype, mask kind, scale)
         (W.layout_strided_causal(16, local_blocks=4, stride=4, H=3), 64, torch.bfloat16, W.MASK_DIAG_CAUSAL, 0.09),
         (W.layout_random_diag(20, 0.3, H=2, seed=5), 32, torch.float32, W.MASK_DENSE, 0.3),
+        # 260 blocks of 128 fp16 in one block-row: 66 560-byte rows, past the
+        # 64 KB chunk budget (one warp per row)
+        (_long_row_layout(260), 128, torch.float16, W.MASK_DIAG_CAUSAL, 0.5),
+        (W.layout_random_diag(12, 0.4, H=2, seed=8), 16, torch.float16, W.MASK_NONE, 0.7),
     ]
-    codes = {torch.float32: bsp.F32, torch.bfloat16: bsp.BF16}
+    codes = {torch.float32: bsp.F32, torch.bfloat16: bsp.BF16, torch.float16: bsp.F16}
     for lay, B, dtype, kind, scale in cases:
         S = lay.shape[1] * B
         handle = bsp.bsp_layout_compile(lay, B)
-        X = torch.randn(2, handle.nnz, B, B, device="cuda").to(dtype)
-        mask = torch.from_numpy(W.random_mask(S, 0.8, 9)).cuda() if kind == W.MASK_DENSE else None
-        want = bsp.bsp_softmax(handle, X, None, scale, kind, mask)
-        got = torch.full_like(X, float("nan"))
-        assert _call(lib, lay, B, codes[dtype], X, got, scale, kind, mask) == 0
+        if lay.shape[1] == 260:
+            assert not handle.softmax_chunks(2)["fits"]  # the long-row kernel runs
+        Z = 2 if S < 8192 else 1
+        X = W.randn((Z, handle.nnz, B, B), {torch.float32: "f32", torch.bfloat16: "bf16",
+                                            torch.float16: "f16"}[dtype], 40 + B)
+        Xd = X.cuda()
+        maskh = W.random_mask(S, 0.8, 9) if kind == W.MASK_DENSE else None
+        mask = None if maskh is None else torch.from_numpy(maskh).cuda()
+        got = torch.full_like(Xd, float("nan"))
+        assert _call(lib, lay, B, codes[dtype], Xd, got, scale, kind, mask) == 0
         torch.cuda.synchronize()
-        assert_close(to_np(got), to_np(want), dtype, f"noalloc softmax B={B} {dtype}")
+        want = oracle.softmax(lay, B, X, scale, kind, maskh)
+        assert_close(to_np(got), want, dtype, f"noalloc softmax B={B} {dtype}", rel=PROB_TOL[dtype],
+                     zeros=softmax_zero_positions(lay, B, Z, kind, maskh))
+        ref = bsp.bsp_softmax(handle, Xd, None, scale, kind, mask)
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref), f"noalloc softmax B={B} {dtype}: differs from bsp_softmax"
 
 
 def test_noalloc_rejects_tables_beyond_the_array(lib):
