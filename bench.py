@@ -48,6 +48,9 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="target oracle CPU time")
     p.add_argument("--skip-cpu", action="store_true", help="no CPU-baseline leg (profiling runs)")
     p.add_argument("--skip-e2e", action="store_true", help="no end-to-end leg (profiling runs)")
+    p.add_argument("--split", action="store_true",
+                   help="under torchrun: split ONE batch of the workload across the ranks by nnz-balanced "
+                        "(batch, head) ranges (strong scaling) instead of one batch per rank (weak scaling)")
     p.add_argument("--graph", action="store_true",
                    help="replay each step from a captured CUDA graph (launch-bound workloads)")
     return p.parse_args()
@@ -520,21 +523,32 @@ def run_ours(args):
     from sparse_attention_layout_gb300 import bsp
 
     w = workload(args.workload)
-    lay = w.layout()
-    Qc, Kc, Vc = w.qkv(shard=rank)  # each rank: its own batch (weak scaling)
+    lay_full = lay = w.layout()
+    split = args.split and world > 1
+    if split:
+        # this rank's share of ONE batch: a contiguous range of (batch, head)
+        # pairs balanced by present blocks, run as batch 1 with those heads
+        from sparse_attention_layout_gb300 import partition
+        u0, u1, lay = partition.shard_layout(lay_full, w.Z, rank, world)
+        Qc, Kc, Vc = (t.reshape(1, w.Z * w.H, w.S, w.D)[:, u0:u1].contiguous() for t in w.qkv())
+        args.no_ops = args.no_workloads = args.skip_e2e = True
+    else:
+        Qc, Kc, Vc = w.qkv(shard=rank)  # each rank: its own batch (weak scaling)
+    Zr = 1 if split else w.Z
     stream = torch.cuda.current_stream()
-    L = bsp.bsp_layout_compile(lay, w.B)
+    L = bsp.bsp_layout_compile(lay, w.B) if lay.shape[0] else None
     q, k, v = (t.cuda() for t in (Qc, Kc, Vc))
     o = torch.empty_like(q)
     pk, pk_kind = peaks()
 
     def step():
-        bsp.bsp_attention(L, q, k, v, o, w.scale, w.mask_kind)
+        if L is not None:
+            bsp.bsp_attention(L, q, k, v, o, w.scale, w.mask_kind)
 
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
-    status = bsp.bsp_status_check(L)
+    status = bsp.bsp_status_check(L) if L is not None else 0
     if status != 0:
         raise RuntimeError(f"device status {status} after warm-up")
     if args.graph:
@@ -585,8 +599,11 @@ def run_ours(args):
             dist.barrier()
     ms = max_over_ranks(total_ms, world, "cuda")
     ms_step = ms / args.steps
-    flops = nonzero_flops(lay, w.B, w.D, w.Z)
-    value = weak_value(flops, world, ms_step)
+    flops = nonzero_flops(lay, w.B, w.D, Zr)  # this rank's launch
+    if split:
+        value = nonzero_flops(lay_full, w.B, w.D, w.Z) / (ms_step * 1e-3) / 1e12  # one batch / slowest rank
+    else:
+        value = weak_value(flops, world, ms_step)
     achieved = flops / (ms_step * 1e-3) / 1e12  # one attention launch per step
 
     # end to end through the C ABI with host buffers: bsp_attention_host takes
@@ -594,7 +611,8 @@ def run_ours(args):
     # out (slices of one batch entry, copies overlapped with the kernels)
     Qh, Kh, Vh = (t.pin_memory() for t in (Qc, Kc, Vc))
     Oh = torch.empty_like(Qc).pin_memory()
-    ws = torch.empty(bsp.bsp_attention_host_workspace(L, Qc.dtype, w.D, 1), dtype=torch.uint8, device="cuda")
+    ws = None if split else torch.empty(bsp.bsp_attention_host_workspace(L, Qc.dtype, w.D, 1), dtype=torch.uint8,
+                                        device="cuda")
 
     def e2e_step():
         bsp.bsp_attention_host(L, Qh, Kh, Vh, Oh, w.scale, w.mask_kind, workspace=ws, reserved_workspace=True)
@@ -642,7 +660,8 @@ def run_ours(args):
         return
     cpu = None
     if not args.skip_cpu:
-        cpu_val, cpu_rows, cpu_s, cores = cpu_oracle_sample(w, lay, Qc, Kc, Vc, args.cpu_seconds)
+        cpu_val, cpu_rows, cpu_s, cores = cpu_oracle_sample(w, lay_full, *((w.qkv() if split else (Qc, Kc, Vc))),
+                                                            args.cpu_seconds)
         cpu = {"value": cpu_val, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{cpu_rows} random rows of {w.Z * w.H * w.S} ({cpu_s:.1f} s, fp64, OpenMP)"}
     if world > 1:
@@ -653,11 +672,13 @@ def run_ours(args):
     roof["algorithmic_flops_per_launch"] = flops
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "strong" if split else "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": config_of(w, lay, "fused attention kernel" + (", replayed from a CUDA graph" if args.graph else ""),
-                            flush),
-        "gpu_launches": args.steps,
+        "config": config_of(w, lay_full, "fused attention kernel" + (", replayed from a CUDA graph" if args.graph else "")
+                            + (f", one batch split over {world} ranks by nnz-balanced (batch, head) ranges"
+                               if split else ""), flush),
+        "gpu_launches": args.steps if L is not None else 0,
         "roofline": roof,
         "e2e": None if e2e_ms is None else {
             "value": flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,

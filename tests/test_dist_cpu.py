@@ -47,3 +47,63 @@ def test_two_ranks_gloo():
         assert value == pytest.approx(2.0e12 / 11.0e-3 / 1e12)  # both ranks' work / slowest time
         assert not same_shards                            # each rank draws its own batch
         assert reproducible                               # seeded
+
+
+# ---------------------------------------------------- one workload split ----
+
+def test_balanced_ranges_cover_every_pair_once_with_bounded_imbalance():
+    import numpy as np
+    from sparse_attention_layout_gb300 import partition, workloads as W
+    layouts = [W.BIGBIRD.layout(), W.STRIDED.layout(), W.BAND.layout(),
+               W.layout_random_diag(12, 0.3, H=7, seed=3), np.zeros((3, 4, 4), np.uint8)]
+    for lay in layouts:
+        for Z in (1, 2, 5):
+            w = partition.pair_weights(lay, Z)
+            for world in (1, 2, 3, 4, 8, 64):
+                ranges = partition.balanced_ranges(w, world)
+                assert len(ranges) == world
+                covered = np.concatenate([np.arange(a, b) for a, b in ranges])
+                assert np.array_equal(covered, np.arange(w.size))           # each pair exactly once, in order
+                loads = [int(w[a:b].sum()) for a, b in ranges]
+                assert max(loads) <= w.sum() / world + (w.max() if w.size else 0)
+
+
+def _split_worker(rank, world, port, out):
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    sys.path.insert(0, root)
+    import numpy as np
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import oracle
+    from sparse_attention_layout_gb300 import partition, workloads as W
+    lay = W.layout_bigbird(8, H=3, seed=4)
+    Z, B, D = 2, 16, 32
+    S = 8 * B
+    Q, K, V = (W.randn((Z, 3, S, D), "f32", 90 + s) for s in range(3))
+    u0, u1, sub = partition.shard_layout(lay, Z, rank, world)
+    # this rank's pairs as one call: batch 1, u1 - u0 heads
+    part = [t.reshape(1, Z * 3, S, D)[:, u0:u1] for t in (Q, K, V)]
+    O = oracle.Oracle().attention(sub, B, *part, 0.2, W.MASK_DIAG_CAUSAL) if u1 > u0 else \
+        np.zeros((1, 0, S, D))
+    bounds = [None] * world
+    dist.all_gather_object(bounds, (u0, u1))   # test-side only: assemble the ranks' results
+    outs = [None] * world
+    dist.all_gather_object(outs, O)
+    if rank == 0:
+        full = oracle.Oracle().attention(lay, B, Q, K, V, 0.2, W.MASK_DIAG_CAUSAL).reshape(1, Z * 3, S, D)
+        joined = np.concatenate(outs, axis=1)
+        out["bounds"] = bounds
+        out["equal"] = bool(np.array_equal(joined, full))
+    dist.destroy_process_group()
+
+
+def test_two_ranks_split_one_workload_gloo():
+    world = 2
+    port = _free_port()
+    manager = mp.get_context("spawn").Manager()
+    out = manager.dict()
+    mp.start_processes(_split_worker, args=(world, port, out), nprocs=world, start_method="spawn", join=True)
+    (a0, a1), (b0, b1) = out["bounds"]
+    assert a0 == 0 and a1 == b0 and b1 == 6 and 0 < a1 < 6   # both ranks work, no pair twice
+    assert out["equal"]                                       # the pieces are the whole result, bit for bit
