@@ -30,8 +30,11 @@
  *    stream is.
  *  - Argument errors are detected before anything is launched; nothing aborts,
  *    throws or traps.  Kernels that detect an impossible state (a bounded wait
- *    that ran out, a bounds check that failed) skip the access, record a code
- *    in the handle's device status word and return; bsp_status_check reads it.
+ *    of the tensor-core kernels that ran out, or a block-column read from the
+ *    tables that lies outside the layout in the fused attention kernel) skip
+ *    the access, record a code in the handle's device status word, wait for
+ *    their own copies and products in flight and return; bsp_status_check
+ *    reads it (bsp_diag_wait_limit provokes both on purpose).
  *  - The handle is immutable after compilation and may be used concurrently
  *    from several streams of the device it was compiled on.
  */
@@ -363,6 +366,24 @@ int bsp_diag_exp2(const float* x, float* y, int64_t n, void* stream);
  * (row a, slot b) is in the layout, else 0), so that tests can compare them
  * with the step tables without a GPU.  Other handles: BSP_ERR_UNSUPPORTED. */
 int bsp_diag_geometry_steps(bsp_layout_t layout, int32_t* step_col, int32_t* step_blk);
+
+/* Set the limit of every bounded wait in the tensor-core kernels launched
+ * with this handle from now on (wait_ns; 0 restores the default of 2 s) and
+ * test injections that make one of those waits, or one of the kernels' bounds
+ * checks, fail on purpose without touching memory out of bounds:
+ *   inject & 1  the fused attention kernel never loads the first Q tile of
+ *               each CTA and never signals it, so the Q K^T issuer's wait
+ *               runs out: the call records BSP_ERR_TIMEOUT;
+ *   inject & 2  the fused attention kernel's K producer sees block-column nb
+ *               (out of range) for its first step; its bounds check of the
+ *               columns that become copy coordinates records
+ *               BSP_ERR_DEVICE_CHECK.
+ * Either way every role of the kernel stops, waits for the copies and matrix
+ * products it had already issued, frees its tensor memory and returns; the
+ * output is then undefined and bsp_status_check reports the code.  inject 0
+ * restores normal operation.  Other inject bits: BSP_ERR_INVALID_ARG.  Not
+ * from the pages: the robustness checks of this implementation. */
+int bsp_diag_wait_limit(bsp_layout_t layout, uint64_t wait_ns, int inject);
 
 /* ---- status ------------------------------------------------------------ */
 

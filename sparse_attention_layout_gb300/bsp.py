@@ -70,6 +70,8 @@ def lib():
         L.bsp_attention_host_workspace.argtypes = [P, i32, i32, i32]
         L.bsp_attention_host_workspace.restype = ctypes.c_size_t
         L.bsp_status_check.argtypes = [P, P]
+        L.bsp_diag_wait_limit.argtypes = [P, ctypes.c_uint64, i32]
+        L.bsp_diag_wait_limit.restype = i32
         L.bsp_status_string.restype = ctypes.c_char_p
         L.bsp_status_string.argtypes = [i32]
         L.bsp_version.restype = ctypes.c_char_p
@@ -361,6 +363,15 @@ def bsp_attention_host(L: Layout, Q, K, V, O=None, scale: float = 1.0, mask_kind
 
 def bsp_status_check(L: Layout, stream=None) -> int:
     return int(lib().bsp_status_check(L.handle, _stream(stream)))
+
+
+INJECT_SKIP_FIRST_Q, INJECT_BAD_COLUMN = 1, 2
+
+
+def bsp_diag_wait_limit(L: Layout, wait_ns: int = 0, inject: int = 0):
+    """Wait limit of the handle's tensor-core kernels (0 = the 2 s default)
+    and test injections (INJECT_* bits; 0 = none)."""
+    _check(lib().bsp_diag_wait_limit(L.handle, int(wait_ns), int(inject)), "bsp_diag_wait_limit")
 
 
 def attention_unfused(L: Layout, Q, K, V, scale: float, mask_kind: int = MASK_NONE, mask=None,

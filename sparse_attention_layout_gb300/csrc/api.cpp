@@ -168,6 +168,14 @@ extern "C" int bsp_status_check(bsp_layout_t L, void* stream) {
     return word;
 }
 
+extern "C" int bsp_diag_wait_limit(bsp_layout_t L, uint64_t wait_ns, int inject) {
+    if (!L || !L->on_device) return BSP_ERR_INVALID_ARG;
+    if (inject & ~(kInjectSkipFirstQ | kInjectBadColumn)) return BSP_ERR_INVALID_ARG;
+    L->view.wait_ns = wait_ns ? wait_ns : kDefaultWaitNs;
+    L->view.inject = inject;
+    return BSP_OK;
+}
+
 extern "C" const char* bsp_status_string(int status) {
     switch (status) {
         case BSP_OK: return "ok";

@@ -49,7 +49,16 @@ struct LayoutView {
     int* status;                  // device status word (0 = OK, else a BSP_ERR_* code)
     int H, nb, B, S, G, ngroups, n_tiles;
     int64_t nnz;
+    // limit of every bounded wait of the tensor-core kernels, in ns (0: the
+    // default kDefaultWaitNs), and test injections (kInject* bits, 0 in use)
+    uint64_t wait_ns;
+    int inject;
 };
+
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s: far beyond any legal wait
+// bsp_diag_wait_limit injections, read by the fused attention kernel only
+constexpr int kInjectSkipFirstQ = 1;   // the producer skips the first Q tile's load and its arrival
+constexpr int kInjectBadColumn = 2;    // the K producer sees block-column nb for the first step
 
 struct bsp_layout_s {
     int H = 0, nb = 0, B = 0, S = 0;

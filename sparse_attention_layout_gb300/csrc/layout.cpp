@@ -288,6 +288,8 @@ extern "C" int bsp_layout_compile(const uint8_t* layout, int H, int nb, int bloc
     }
     L->dmem = base;
     V.status = (int*)base;
+    V.wait_ns = kDefaultWaitNs;
+    V.inject = 0;
     size_t off = padded<int>(4);
     bool ok = cudaMemsetAsync(base, 0, padded<int>(4), s) == cudaSuccess;
     for (const Part& pt : parts) {

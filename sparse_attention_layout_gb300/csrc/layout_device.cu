@@ -438,6 +438,8 @@ extern "C" int bsp_layout_compile_device(const uint8_t* layout, int H, int nb, i
     if (cudaMalloc((void**)&base, total) != cudaSuccess) return fail(BSP_ERR_OOM);
     L->dmem = base;
     V.status = (int*)base;
+    V.wait_ns = kDefaultWaitNs;
+    V.inject = 0;
     size_t off = padded<int>(4);
     for (int k = 0; k < nparts; ++k) {
         *dst[k] = (const int32_t*)(base + off);

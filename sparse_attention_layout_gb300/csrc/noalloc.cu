@@ -89,6 +89,8 @@ extern "C" int bsp_softmax_noalloc(const uint8_t* layout, int H, int nb, int blo
     }
     cudaStream_t s = (cudaStream_t)stream;
     V.status = (int*)base;
+    V.wait_ns = kDefaultWaitNs;
+    V.inject = 0;
     bool ok = cudaMemsetAsync(base, 0, sizeof(int), s) == cudaSuccess;  // the status word starts at zero
     size_t off = align256(sizeof(int));
     for (const Part& p : parts) {

@@ -219,7 +219,7 @@ softmax_chunk_kernel(LayoutView L, const T* X, T* Y, float c2, int kind, const u
     const uint32_t slice = (uint32_t)R * BLK * sizeof(T);  // bytes of one block's part of the chunk
     T* buf = reinterpret_cast<T*>(smem_raw);
     int* scol = reinterpret_cast<int*>(smem_raw + L.sm_max_bytes[E]);
-    tc::Abort ab{&abort_flag, L.status};
+    tc::Abort ab{&abort_flag, L.status, L.wait_ns};
     if (threadIdx.x == 0) {
         abort_flag = 0;
         tc::mbar_init(&bar, 1);
@@ -348,6 +348,8 @@ softmax_chunk_kernel(LayoutView L, const T* X, T* Y, float c2, int kind, const u
             tc::bulk_commit();
             tc::bulk_wait_read_all();  // shared memory must outlive the reads of the stores
         }
+    } else if (threadIdx.x == 0) {
+        tc::mbar_drain(&bar, 0, ab);  // the wait ran out: the copies in land before the CTA exits
     }
 }
 

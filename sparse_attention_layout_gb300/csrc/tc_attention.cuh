@@ -24,20 +24,23 @@
 //               128-byte-swizzled shared-memory panel with TMA stores.  The
 //               next tile's softmax runs meanwhile, so the tensor core does not
 //               wait for the output write.
-//   warps 8..15 softmax, two warpgroups taking alternate steps: thread = one
-//               query row = one TMEM lane, whole rows of 128 scores.  Reads S
-//               from TMEM, masks, takes the row max, receives the running max
-//               of the previous step from the other warpgroup and passes its
-//               own on, writes P (bf16/fp16) over the step's scores in TMEM,
-//               rescales O in TMEM only when the running max grew by more than
-//               2^8 (the final O / l is exact either way), and hands the
-//               tile's row sums to the epilogue.
+//   warps 8..15 softmax, both warpgroups on every step, one half row each:
+//               thread = one query row = one TMEM lane, warpgroup wg the scores
+//               of keys [64 wg, 64 wg + 64).  Reads its half of S from TMEM,
+//               masks, takes the half-row max and swaps it with the other
+//               thread of the row through shared memory, writes its P
+//               (bf16/fp16) into the step's buffer, rescales its half of O in
+//               TMEM only when the running max grew by more than 2^8 (the final
+//               O / l is exact either way), and hands its half-row sums to the
+//               epilogue, which adds them.
 // TMEM columns: S0 [0,128), S1 [128,256), S2 [256,384), O [384, 384+D).  Step g
 // uses S buffer g % 3; its P (two 16-bit values per column) overwrites the
-// first 64 columns of the same buffer once the scores are in registers, and
-// P V takes its A operand from there.  With three buffers Q K^T of step g
-// waits only for P V of step g - 3, so the next scores are ready when a
-// softmax warpgroup finishes a step.
+// first 64 columns of the same buffer once the scores are in registers (keys
+// [0, 64) into columns [0, 32) by warpgroup 0, keys [64, 128) into columns
+// [32, 64) by warpgroup 1 after warpgroup 0 has announced its maximum, i.e.
+// loaded those columns), and P V takes its A operand from there.  With three
+// buffers Q K^T of step g waits only for P V of step g - 3, so the next scores
+// are ready when the softmax finishes a step.
 // GEO (opt-in): every head of the layout has an affine description (band
 // and / or column term); the TMA producers compute each step's key blocks
 // from it instead of reading the step tables.  The softmax keeps reading the tables:
@@ -124,19 +127,24 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     // l_full (softmax wrote them) and l_empty (the epilogue read them).
     __shared__ uint64_t o_full, o_empty, l_full[2], l_empty[2];
     __shared__ float lsum[2][2][128], lref[2][2][128];  // each warpgroup's sum and its reference max
-    // running max after step g, handed to the warpgroup of step g + 1:
-    // mrun[g % 2][row], published by m_pub[g % 2] (4 warp arrivals)
-    __shared__ float mrun[2][128];
-    __shared__ uint64_t m_pub[2];
+    // half-row maxima of step g, one per warpgroup: xm[g % 2][wg][row], both
+    // halves announced by x_full[g % 2] (8 warp arrivals)
+    __shared__ float xm[2][2][128];
+    __shared__ uint64_t x_full[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
+    // what each issuing thread had issued when it stopped: K steps, Q tiles
+    // (bit 31: the first was skipped by the test injection), V steps, Q K^T
+    // steps, P V steps -- drained after the roles stop if the kernel aborted
+    __shared__ uint32_t issued[5];
 
     const LayoutView& L = args.L;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    Abort ab{&abort_flag, L.status};
+    Abort ab{&abort_flag, L.status, L.wait_ns};
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
+        for (int i = 0; i < 5; ++i) issued[i] = 0;
         for (int i = 0; i < QST; ++i) {
             mbar_init(&q_full[i], 1);
             mbar_init(&q_empty[i], 1);
@@ -148,15 +156,15 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         for (int i = 0; i < 3; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&pv_done[i], 1);
-            // the 4 warps of the warpgroup that owns the step
-            mbar_init(&p_full[i], 4);
+            // the 8 softmax warps (each writes the P of its half rows)
+            mbar_init(&p_full[i], 8);
         }
         mbar_init(&o_full, 1);
         mbar_init(&o_empty, 4);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&l_full[i], 8);
             mbar_init(&l_empty[i], 4);
-            mbar_init(&m_pub[i], 4);
+            mbar_init(&x_full[i], 8);
         }
         fence_barrier_init();
     }
@@ -188,6 +196,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             if (!is_v) tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(tm);
             uint32_t q_it = 0, g = 0;
+            bool q_skipped = false;  // test injection: the first Q tile was never loaded
             for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
                 const int tile = L.tile_order[w / args.Z];
                 const int z = (int)(w % args.Z);
@@ -204,10 +213,14 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 if (!is_v) {
                     const uint32_t qs = q_it % QST;
                     if (!mbar_wait(&q_empty[qs], ((q_it / QST) & 1) ^ 1, ab)) break;
-                    mbar_arrive_expect_tx(&q_full[qs], kTileBytes);
-                    for (int p = 0; p < KP; ++p)
-                        tma_load_2d(smem_u32(smem + SM::kQ + qs * kTileBytes + p * 16384), &tmQ, p * 64,
-                                    (int32_t)(zh * S + gq * 128), &q_full[qs]);
+                    if (q_it == 0 && (L.inject & kInjectSkipFirstQ)) {
+                        q_skipped = true;  // neither the copy nor the arrival: Q K^T waits in vain
+                    } else {
+                        mbar_arrive_expect_tx(&q_full[qs], kTileBytes);
+                        for (int p = 0; p < KP; ++p)
+                            tma_load_2d(smem_u32(smem + SM::kQ + qs * kTileBytes + p * 16384), &tmQ, p * 64,
+                                        (int32_t)(zh * S + gq * 128), &q_full[qs]);
+                    }
                     ++q_it;
                 }
                 for (int n = 0; n < ns; ++n, ++g) {
@@ -223,6 +236,16 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                             const int c = L.step_col[s * G + b];
                             cols[b] = c >= 0 ? c : L.step_col[s * G];  // padding slot: any valid block
                         }
+                    }
+                    if (!is_v && g == 0 && (L.inject & kInjectBadColumn)) cols[0] = L.nb;
+                    // bounds check of the block-columns that become TMA coordinates:
+                    // a bad table entry stops the kernel with BSP_ERR_DEVICE_CHECK
+                    bool cols_ok = true;
+#pragma unroll
+                    for (int b = 0; b < G; ++b) cols_ok &= (unsigned)cols[b] < (unsigned)L.nb;
+                    if (!cols_ok) {
+                        ab.fail(BSP_ERR_DEVICE_CHECK);
+                        goto producer_done;
                     }
                     // stage g % 2 is free once step g - 2 has used it: Q K^T for a K
                     // tile, P V for a V tile
@@ -241,7 +264,13 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                                         (int32_t)(zh * S + (int64_t)cols[b] * BLK), full);
                 }
             }
-        producer_done:;
+        producer_done:
+            if (is_v) {
+                issued[2] = g;
+            } else {
+                issued[0] = g;
+                issued[1] = q_it | (q_skipped ? 0x80000000u : 0u);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------- Q K^T issuer (one thread) ----
@@ -274,7 +303,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 }
                 ++q_it;
             }
-        qk_done:;
+        qk_done:
+            issued[3] = g;
         }
     } else if (warp == 2) {
         // --------------------------------------------- P V issuer (one thread) ----
@@ -303,11 +333,13 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 mma_commit(&o_full);
                 ++tc;
             }
-        pv_done_label:;
+        pv_done_label:
+            issued[4] = g;
         }
     }
     } else if (warp < 8) {
-        if (kRegsEpi < kRegsLaunch) regs_dec<kRegsEpi>();
+        if constexpr (kRegsEpi < kRegsLaunch) regs_dec<kRegsEpi>();
+        else if constexpr (kRegsEpi > kRegsLaunch) regs_inc<kRegsEpi>();
         // ---------------------------------------------------- epilogue ----
         // Warp q owns rows [32 q, 32 q + 32) of the tile (TMEM lanes of its
         // quadrant).  O / l leaves through a 32 x 64 staging panel per warp in
@@ -347,43 +379,69 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 if (!__all_sync(0xffffffffu, ok)) goto epilogue_done;
                 tc_fence_after();
             }
-            // one 64-column panel at a time: TMEM -> registers (scaled, packed) ->
-            // staging panel -> TMA store; O is handed back after the last load
-#pragma unroll
-            for (int p = 0; p < KP; ++p) {
-                uint32_t pk[32];
-                if (live) {
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        uint32_t r[32];
-                        tmem_ld32_sync(tO + lane_base + p * 64 + hh * 32, r);
-#pragma unroll
-                        for (int k = 0; k < 16; ++k)
-                            pk[hh * 16 + k] =
-                                Pack2<T>::pack(__uint_as_float(r[2 * k]) * inv, __uint_as_float(r[2 * k + 1]) * inv);
-                    }
-                    if (p == KP - 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&o_empty);
-                    }
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) pk[k] = 0u;
-                }
-                if (y0 < S) {
-                    if (lane == 0) bulk_wait_read_all();  // the panel's previous store has read it
-                    __syncwarp();
-                    uint8_t* rp = stage + lane * 128;
+            // O leaves through the warp's 32 x 64 staging panel, one TMA store per
+            // 64 columns.  Every column of O is read out of TMEM before the
+            // accumulator is handed back to the next tile's P V, and before any
+            // wait on a store of this tile: the first panel goes to the staging
+            // panel as it is read (the panel's previous store, issued a tile
+            // ago, has long finished reading it), the second is held in
+            // registers until the first panel's store has read the staging.
+            {
+                const bool out = y0 < S;
+                uint8_t* rp = stage + lane * 128;
+                auto put = [&](const uint32_t (&pk)[32]) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
                         *reinterpret_cast<uint4*>(rp + ((j ^ (lane & 7)) << 4)) =
                             make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                };
+                auto store = [&](int p) {
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
                         tma_store_3d(&tmO, stage_s, p * 64, y0, zh);
                         bulk_commit();
+                    }
+                };
+                auto read_panel = [&](int p, uint32_t (&pk)[32]) {
+                    uint32_t r[64];  // 64 columns, two loads and one wait
+                    tmem_ld64_sync(tO + lane_base + p * 64, tO + lane_base + p * 64 + 32, r);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        pk[k] = Pack2<T>::pack(__uint_as_float(r[2 * k]) * inv, __uint_as_float(r[2 * k + 1]) * inv);
+                };
+                if (out) {
+                    if (lane == 0) bulk_wait_read_all();  // the staging panel is free
+                    __syncwarp();
+                }
+                uint32_t pk[32];
+                if (live) {
+                    read_panel(0, pk);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) pk[k] = 0u;
+                }
+                if (out) put(pk);
+                if constexpr (KP == 2) {
+                    if (live) {
+                        read_panel(1, pk);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) pk[k] = 0u;
+                    }
+                }
+                if (live) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&o_empty);
+                }
+                if (out) {
+                    store(0);
+                    if constexpr (KP == 2) {
+                        if (lane == 0) bulk_wait_read_all();  // the first panel's store has read the staging
+                        __syncwarp();
+                        put(pk);
+                        store(1);
                     }
                 }
             }
@@ -394,17 +452,21 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     } else {
         regs_inc<kRegsSoftmax>();
         // ---------------------------------------------------- softmax ----
-        // Warpgroup wg takes the steps g with g % 2 == wg, whole rows (thread =
-        // query row = TMEM lane): the two warps that share a sub-partition are
-        // then in different phases of their steps, one loading and reducing while
-        // the other exponentiates.  The running max m is handed from step g - 1 to
-        // step g through shared memory (m_pub barriers): every step waits for the
-        // previous step's hand-off, across tiles too, so each parity's value is
-        // read before it is rewritten.  Each warpgroup keeps its partial row sum
-        // against the last max it used; the epilogue rebases the two.
+        // Both warpgroups work on every step, each on one half of the row's
+        // 128 scores: warpgroup wg takes keys [64 wg, 64 wg + 64) of the rows
+        // of its warp's TMEM lane quadrant (thread = query row = TMEM lane).
+        // The two threads of a row (warp 8 + q and warp 12 + q, quadrant q)
+        // swap their half-row maxima through shared memory (x_full barriers),
+        // so both reach the same running max m and the same decisions; each
+        // writes the P of its keys (keys [0, 64) into columns [0, 32), keys
+        // [64, 128) into columns [32, 64) -- the latter over scores of the other
+        // half, which its owner has loaded before it announced its maximum),
+        // rescales its half of O when m moved, and keeps its half-row sum
+        // against m; the epilogue adds the two halves.  A step's critical path
+        // is half a row of work plus the exchange.
         constexpr int W = BLK < 64 ? BLK : 64;  // columns of one slot inside a half row
         constexpr int LS = 64 / W;              // slots (or slot parts) per half row
-        const int sw = warp - 8, wg = sw >> 2;
+        const int sw = warp - 8, wg = sw >> 2, hf = wg;
         const int quad = warp & 3;
         const int row = quad * 32 + lane;  // query row inside the tile = TMEM lane
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
@@ -414,7 +476,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         struct Half {
             int blk[LS], cb[LS];
         };
-        auto fetch = [&](int s, int hf, Half& o) {
+        auto fetch = [&](int s, Half& o) {
 #pragma unroll
             for (int ls = 0; ls < LS; ++ls) {
                 const int b = (hf * 64 + ls * W) / BLK;
@@ -422,8 +484,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 o.cb[ls] = L.step_col[s * G + b];
             }
         };
-        // mask one half (64 columns) of the row in place
-        auto mask_half = [&](float (&v)[64], int hf, const Half& md, int rb, int rseq) {
+        // mask this thread's half (64 columns) of the row in place
+        auto mask_half = [&](float (&v)[64], const Half& md, int rb, int rseq) {
 #pragma unroll
             for (int ls = 0; ls < LS; ++ls) {
                 const int kbase = (hf * 64 + ls * W) % BLK;  // in-block column of v[ls * W]
@@ -481,77 +543,83 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const float2 r2 = __fadd2_rn(__fadd2_rn(rs4[0], rs4[1]), __fadd2_rn(rs4[2], rs4[3]));
             return r2.x + r2.y;
         };
-        for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
-            const int tile = L.tile_order[w / args.Z];
+        // the CTA's tiles: (tile id, first step, step count); ns = -1 past the end
+        auto tile_info = [&](int64_t w, int& tile, int& s0, int& ns) {
+            if (w >= total) {
+                tile = 0;
+                s0 = 0;
+                ns = -1;
+                return;
+            }
+            tile = L.tile_order[w / args.Z];
+            s0 = L.tile_step_ptr[tile];
+            ns = L.tile_step_ptr[tile + 1] - s0;
+        };
+        int64_t w = blockIdx.x;
+        int tile, s0, ns;
+        tile_info(w, tile, s0, ns);
+        while (ns == 0) {  // the epilogue writes the zero rows of empty tiles
+            w += gridDim.x;
+            tile_info(w, tile, s0, ns);
+        }
+        Half hnext;
+        if (ns > 0) fetch(s0, hnext);
+        while (ns > 0) {
+            // the next tile's place in the tables: loaded now, first used at this
+            // tile's last step, so the loads overlap the steps
+            int64_t wn = w + gridDim.x;
+            int tn, s0n, nsn;
+            tile_info(wn, tn, s0n, nsn);
             const int gq = tile % L.ngroups;
-            const int s0 = L.tile_step_ptr[tile], ns = L.tile_step_ptr[tile + 1] - s0;
-            if (ns == 0) continue;            // the epilogue writes the zero rows
             const int rb = gq * G + a;        // block-row of this thread's query row
             const int rseq = gq * 128 + row;  // query position inside the sequence
-            float l = 0.f, mref = -INFINITY;  // this warpgroup's sum and the max it is relative to
-            // first own step of the tile and its metadata
-            int n = (int)((wg - g) & 1u);
-            g += n;
-            Half h0, h1;
-            if (n < ns) {
-                fetch(s0 + n, 0, h0);
-                fetch(s0 + n, 1, h1);
-            }
-            for (; n < ns; n += 2, g += 2) {
-                const Half c0 = h0, c1 = h1;
-                if (n + 2 < ns) {  // next own step: latency hidden behind this one
-                    fetch(s0 + n + 2, 0, h0);
-                    fetch(s0 + n + 2, 1, h1);
+            float l = 0.f, m = -INFINITY;     // this half row's sum and the running max it is relative to
+            for (int n = 0; n < ns; ++n, ++g) {
+                const Half c = hnext;
+                if (n + 1 < ns) {
+                    fetch(s0 + n + 1, hnext);  // latency hidden behind this step
+                } else if (nsn > 0) {
+                    fetch(s0n, hnext);         // the next tile's first step
                 }
-                const uint32_t sb = g % 3;
+                const uint32_t sb = g % 3, xb = g & 1;
                 bool ok = mbar_wait(&s_full[sb], (g / 3) & 1, ab);
                 if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
                 tc_fence_after();
                 const uint32_t srow = tS + sb * 128 + lane_base;
-                // row max over both halves; the first half stays in registers
                 float x[64];
-                tmem_ld64_sync(srow + 64, srow + 96, *reinterpret_cast<uint32_t(*)[64]>(x));
-                mask_half(x, 1, c1, rb, rseq);
-                float mx = max64(x);
-                tmem_ld64_sync(srow, srow + 32, *reinterpret_cast<uint32_t(*)[64]>(x));
-                mask_half(x, 0, c0, rb, rseq);
-                mx = fmaxf(mx, max64(x));
-                // running max after step g - 1 (the other warpgroup's step)
-                float mprev = -INFINITY;
-                if (g > 0) {
-                    ok = mbar_wait(&m_pub[(g - 1) & 1], ((g - 1) >> 1) & 1, ab);
-                    if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
-                    if (n > 0) mprev = mrun[(g - 1) & 1][row];
-                }
+                tmem_ld64_sync(srow + hf * 64, srow + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[64]>(x));
+                mask_half(x, c, rb, rseq);
+                const float mx = max64(x);
+                // swap half-row maxima with the other thread of the row; the arrival
+                // also tells it that this half's scores are in registers, so it may
+                // write its P over them
+                xm[xb][wg][row] = mx;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&x_full[xb]);
+                ok = mbar_wait(&x_full[xb], (g >> 1) & 1, ab);
+                if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
+                tc_fence_after();
+                const float mrow = fmaxf(mx, xm[xb][wg ^ 1][row]);
                 // m in the scaled log2 domain (scale > 0 commutes with max); it moves
                 // only when the row max grew by more than the threshold
-                const float m_new = fmaxf(mprev, mx * args.c2);
-                const bool need = m_new > mprev + kRescaleThreshold;  // also true for the first finite max
-                const float m = need ? m_new : mprev;
-                mrun[g & 1][row] = m;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&m_pub[g & 1]);
-                const float msub = (m == -INFINITY) ? 0.f : m;
-                // P over the scores: keys [0, 64) -> columns [0, 32) (those scores are
-                // in registers), then keys [64, 128) -> columns [32, 64) (scores of
-                // keys [32, 64), already consumed)
+                const float m_new = fmaxf(m, mrow * args.c2);
+                const bool need = m_new > m + kRescaleThreshold;  // also true for the first finite max
+                const float mnext = need ? m_new : m;
+                const float msub = (mnext == -INFINITY) ? 0.f : mnext;
                 uint32_t pk[32];
-                float rs = exp64(x, msub, pk);
-                tmem_st32_sync(srow, pk);
-                tmem_ld64_sync(srow + 64, srow + 96, *reinterpret_cast<uint32_t(*)[64]>(x));
-                mask_half(x, 1, c1, rb, rseq);
-                rs += exp64(x, msub, pk);
-                tmem_st32_sync(srow + 32, pk);
+                const float rs = exp64(x, msub, pk);
+                tmem_st32_sync(srow + hf * 32, pk);
                 if (n > 0 && __any_sync(0xffffffffu, need)) {
-                    // O (scaled by mprev) is rescaled after P V of step g - 1 has completed
+                    // this half of O (scaled by m) is rescaled after P V of step g - 1
                     ok = mbar_wait(&pv_done[(g - 1) % 3], ((g - 1) / 3) & 1, ab);
                     if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
                     tc_fence_after();
-                    const float alpha = need ? (mprev == -INFINITY ? 0.f : ex2_approx(mprev - m)) : 1.f;
+                    const float alpha = need ? (m == -INFINITY ? 0.f : ex2_approx(m - mnext)) : 1.f;
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int cc = 0; cc < D / 64; ++cc) {
                         uint32_t r[32];
-                        const uint32_t ta = tO + lane_base + c * 32;
+                        const uint32_t ta = tO + lane_base + hf * (D / 2) + cc * 32;
                         tmem_ld32_sync(ta, r);
 #pragma unroll
                         for (int k = 0; k < 32; k += 2) {
@@ -566,12 +634,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[sb]);
-                // this warpgroup's sum, rebased from its previous reference to m
-                l = (mref == -INFINITY ? 0.f : l * ex2_approx(mref - msub)) + rs;
-                mref = m;
+                // this half row's sum, rebased from the previous reference to mnext
+                l = (m == -INFINITY ? 0.f : l * ex2_approx(m - msub)) + rs;
+                m = mnext;
             }
-            g -= (uint32_t)(n - ns);  // back to the first step of the next tile
-            // this warpgroup's sum and reference max -> epilogue (buffer tc % 2,
+            // this half row's sum and its reference max -> epilogue (buffer tc % 2,
             // free once the epilogue has read the values of tile tc - 2)
             {
                 const uint32_t lb = tc & 1;
@@ -579,19 +646,41 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     bool ok = mbar_wait(&l_empty[lb], ((tc - 2) >> 1) & 1, ab);
                     if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
                 }
-                // with nothing kept the sum holds only the polynomial's tiny values
-                lsum[lb][wg][row] = mref == -INFINITY ? 0.f : l;
-                lref[lb][wg][row] = mref;
+                lsum[lb][wg][row] = m == -INFINITY ? 0.f : l;
+                lref[lb][wg][row] = m;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&l_full[lb]);
                 ++tc;
             }
+            while (nsn == 0) {  // empty tiles: nothing to compute
+                wn += gridDim.x;
+                tile_info(wn, tn, s0n, nsn);
+                if (nsn > 0) fetch(s0n, hnext);
+            }
+            w = wn;
+            tile = tn;
+            s0 = s0n;
+            ns = nsn;
         }
     softmax_done:;
     }
 
     tc_fence_before();
     __syncthreads();
+    if (abort_flag) {
+        // stopped early: the copies and products issued before the stop land
+        // before the CTA lets go of its shared memory and TMEM (a normal run's
+        // consumers have waited for all of them already)
+        if (threadIdx.x == 0) {
+            mbar_drain_ring(k_full, 2, issued[0], ab);
+            const uint32_t qi = issued[1] & 0x7fffffffu;
+            if (!((issued[1] >> 31) && qi == 1)) mbar_drain_ring(q_full, QST, qi, ab);
+            mbar_drain_ring(v_full, 2, issued[2], ab);
+            if (issued[3]) mbar_drain(&s_full[(issued[3] - 1) % 3], ((issued[3] - 1) / 3) & 1, ab);
+            if (issued[4]) mbar_drain(&pv_done[(issued[4] - 1) % 3], ((issued[4] - 1) / 3) & 1, ab);
+        }
+        __syncthreads();
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, 512);

@@ -77,18 +77,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return done != 0;
 }
 
-// Shared abort flag: set by the first wait that runs out; every other wait
-// gives up as soon as it sees it.
+// Shared abort flag: set by the first wait that runs out (or the first
+// failed bounds check); every other wait gives up as soon as it sees it.
+// limit_ns: the wait limit (0 = kDefaultWaitNs).
 struct Abort {
     volatile int* flag;
     int* status;
+    uint64_t limit_ns;
+    __device__ __forceinline__ uint64_t limit() const { return limit_ns ? limit_ns : kDefaultWaitNs; }
+    // record `code` in the status word (the first code wins) and stop every role
+    __device__ __forceinline__ void fail(int code) const {
+        *flag = 1;
+        if (status) atomicCAS(status, 0, code);
+    }
 };
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legal wait
-
-// Wait for the phase with the given parity to complete.  Bounded: after
-// kWaitLimitNs (or once another role has aborted) it records BSP_ERR_TIMEOUT
-// and returns false; the caller then leaves its loop.
+// Wait for the phase with the given parity to complete.  Bounded: after the
+// limit (or once another role has aborted) it records BSP_ERR_TIMEOUT and
+// returns false; the caller then leaves its loop.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Abort& ab) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
@@ -97,12 +103,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
         if (mbar_try_wait(bar, parity)) return true;
         if ((++n & 63) == 0) {
             if (*ab.flag) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                *ab.flag = 1;
-                if (ab.status) atomicCAS(ab.status, 0, (int)BSP_ERR_TIMEOUT);
+            if (globaltimer_ns() - t0 > ab.limit()) {
+                ab.fail(BSP_ERR_TIMEOUT);
                 return false;
             }
         }
+    }
+}
+
+// After an abort: wait, bounded by the limit but regardless of the abort
+// flag, for the phase of `bar` with the given parity, i.e. until the copies
+// or matrix products that signal it have landed.  A role calls it for every
+// asynchronous operation it issued before it returns, so that no copy writes
+// shared memory and no product writes TMEM after the CTA has released them.
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, const Abort& ab) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > ab.limit()) return;
+}
+
+// Drain a ring of nst stages whose phases were begun in order 0, 1, ...,
+// next - 1 (stage = index % nst, phase = index / nst): waits for the last
+// phase begun on each stage.
+__device__ __forceinline__ void mbar_drain_ring(uint64_t* bars, uint32_t nst, uint32_t next, const Abort& ab) {
+    for (uint32_t s = 0; s < nst; ++s) {
+        if (next <= s) continue;
+        const uint32_t last = s + ((next - 1 - s) / nst) * nst;  // largest index < next on stage s
+        mbar_drain(&bars[s], (last / nst) & 1, ab);
     }
 }
 

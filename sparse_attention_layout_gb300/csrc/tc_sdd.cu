@@ -92,12 +92,16 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     __shared__ uint64_t a_full[2], a_empty[2], b_full[BST], b_empty[BST], s_full[4], s_empty[4];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
+    // what the issuing threads had issued when they stopped (A tiles, B
+    // steps, MMA steps), drained after the roles stop if the kernel aborted
+    __shared__ uint32_t issued[3];
 
     const LayoutView& L = args.L;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    Abort ab{&abort_flag, L.status};
+    Abort ab{&abort_flag, L.status, L.wait_ns};
     if (threadIdx.x == 0) {
         abort_flag = 0;
+        for (int i = 0; i < 3; ++i) issued[i] = 0;
         for (int i = 0; i < 2; ++i) {
             mbar_init(&a_full[i], 1);
             mbar_init(&a_empty[i], 1);
@@ -172,7 +176,9 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     }
                 }
             }
-        producer_done:;
+        producer_done:
+            issued[0] = a_it;
+            issued[1] = g;
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -208,7 +214,8 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 }
                 ++a_it;
             }
-        mma_done:;
+        mma_done:
+            issued[2] = g;
         }
     } else {
         // Epilogue: each warp owns 32 rows of the tile (TMEM lanes 32q..32q+31).
@@ -357,6 +364,16 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     }
     tc_fence_before();
     __syncthreads();
+    if (abort_flag) {
+        // stopped early: the copies and products issued before the stop land
+        // before the CTA lets go of its shared memory and TMEM
+        if (threadIdx.x == 0) {
+            mbar_drain_ring(a_full, 2, issued[0], ab);
+            mbar_drain_ring(b_full, BST, issued[1], ab);
+            if (issued[2]) mbar_drain(&s_full[(issued[2] - 1) & 3], ((issued[2] - 1) >> 2) & 1, ab);
+        }
+        __syncthreads();
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, 512);

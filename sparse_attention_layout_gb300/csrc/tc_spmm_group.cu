@@ -90,12 +90,16 @@ spmm_group_kernel(const __grid_constant__ CUtensorMap tmSp, const __grid_constan
     __shared__ uint64_t full[ST], empty[ST], acc_full[2], acc_empty[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
+    // stages begun by each producer and by the MMA issuer when they stopped,
+    // drained after the roles stop if the kernel aborted
+    __shared__ uint32_t issued[kProducers + 1];
 
     const LayoutView& L = args.L;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    Abort ab{&abort_flag, L.status};
+    Abort ab{&abort_flag, L.status, L.wait_ns};
     if (threadIdx.x == 0) {
         abort_flag = 0;
+        for (int i = 0; i <= kProducers; ++i) issued[i] = 0;
         for (int i = 0; i < ST; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
@@ -240,7 +244,8 @@ spmm_group_kernel(const __grid_constant__ CUtensorMap tmSp, const __grid_constan
                 }
             }
         }
-    producer_done:;
+    producer_done:
+        if (lane == 0) issued[pid] = it;
     } else if (warp == 1) {
         // ---------------------------------------------- MMA issuer (one thread) ----
         if (lane == 0) {
@@ -283,7 +288,8 @@ spmm_group_kernel(const __grid_constant__ CUtensorMap tmSp, const __grid_constan
                 mma_commit(&acc_full[buf]);
                 ++k;
             }
-        mma_done:;
+        mma_done:
+            issued[kProducers] = it;
         }
     } else {
         // -------------------------------------------------------- epilogue ----
@@ -363,6 +369,29 @@ spmm_group_kernel(const __grid_constant__ CUtensorMap tmSp, const __grid_constan
     }
     tc_fence_before();
     __syncthreads();
+    if (abort_flag) {
+        // stopped early: the copies and products issued before the stop land
+        // before the CTA lets go of its shared memory and TMEM -- for each
+        // producer the last stage it began on each ring slot, for the MMA
+        // issuer its last commit
+        if (threadIdx.x == 0) {
+            constexpr uint32_t NP = kProducers < ST ? kProducers : ST;
+            for (uint32_t pid = 0; pid < NP; ++pid) {
+                const uint32_t it = issued[pid];
+                for (uint32_t st = 0; st < (uint32_t)ST; ++st) {
+                    for (uint32_t j = it; j-- > 0 && j + (uint32_t)(ST * NP) >= it;) {
+                        if (j % NP == pid && j % ST == st) {
+                            mbar_drain(&full[st], (j / ST) & 1, ab);
+                            break;
+                        }
+                    }
+                }
+            }
+            const uint32_t it = issued[kProducers];
+            if (it) mbar_drain(&empty[(it - 1) % ST], ((it - 1) / ST) & 1, ab);
+        }
+        __syncthreads();
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, 512);

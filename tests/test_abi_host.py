@@ -460,3 +460,10 @@ def test_new_entry_points_validate_arguments(lib):
     assert lib.bsp_attention_host_workspace(None, 1, 64, 1) == 0
     assert lib.bsp_attention_host_workspace(L.handle, 1, 64, 0) == 0
     assert lib.bsp_diag_geometry_steps(None, a, a) == -1
+
+
+def test_diag_wait_limit_needs_a_compiled_handle(lib):
+    # a host-only plan has no device status word or kernels: rejected without a GPU
+    L = bsp.bsp_layout_plan(np.ones((1, 2, 2), np.uint8), 32)
+    assert lib.bsp_diag_wait_limit(L.handle, ctypes.c_uint64(1000), 0) == -1
+    assert lib.bsp_diag_wait_limit(None, ctypes.c_uint64(0), 0) == -1
