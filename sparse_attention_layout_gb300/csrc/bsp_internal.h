@@ -24,6 +24,9 @@ struct LayoutView {
     // of their block-columns cut into steps of G slots
     const int32_t* tile_step_ptr; // [n_tiles+1]
     const int32_t* tile_order;    // [n_tiles] tile ids, most steps first
+    // [n_tiles][4] the same tiles in that order as (tile id, first step, step
+    // count, 0): one 16-byte load tells a role its next tile
+    const int32_t* tile_run;
     const int32_t* step_col;      // [n_steps*G] block-column of each slot, -1 = padding
     const int32_t* step_blk;      // [n_steps*G*G] block id at (row a, slot b), -1 = absent
     // line groups for the block-sparse matmuls, o = 0: G consecutive block-rows,
@@ -73,7 +76,7 @@ struct bsp_layout_s {
     int G = 1, ngroups = 0, n_tiles = 0;
     int64_t n_steps = 0;
     int max_tile_steps = 0;
-    std::vector<int32_t> tile_step_ptr, tile_order, step_col, step_blk;
+    std::vector<int32_t> tile_step_ptr, tile_order, tile_run, step_col, step_blk;
     std::vector<int32_t> gl_ptr[2], gl_order[2], gl_idx[2], gl_blk[2];
     std::vector<int32_t> sm_items[2];
     int sm_max_bytes[2] = {0, 0};

@@ -138,6 +138,14 @@ int build_tables(bsp_layout_s* L, const uint8_t* lay) {
     L->tile_step_ptr[L->n_tiles] = (int32_t)steps;
     L->n_steps = steps;
     L->tile_order = order_by_weight_desc(tile_steps);
+    L->tile_run.resize((size_t)4 * L->n_tiles);
+    for (int r = 0; r < L->n_tiles; ++r) {
+        const int t = L->tile_order[r];
+        L->tile_run[4 * r + 0] = t;
+        L->tile_run[4 * r + 1] = L->tile_step_ptr[t];
+        L->tile_run[4 * r + 2] = L->tile_step_ptr[t + 1] - L->tile_step_ptr[t];
+        L->tile_run[4 * r + 3] = 0;
+    }
 
     // Line groups for the block-sparse matmuls: G consecutive block-rows (o = 0,
     // CSR) or block-columns (o = 1, CSC) of one head, one slot per block index
@@ -268,7 +276,7 @@ extern "C" int bsp_layout_compile(const uint8_t* layout, int H, int nb, int bloc
         {&L->row_idx, &V.row_idx},       {&L->blk_id_csc, &V.blk_id_csc},
         {&L->blk_key, &V.blk_key},       {&L->row_order, &V.row_order},
         {&L->col_order, &V.col_order},   {&L->tile_step_ptr, &V.tile_step_ptr},
-        {&L->tile_order, &V.tile_order}, {&L->step_col, &V.step_col},
+        {&L->tile_order, &V.tile_order}, {&L->tile_run, &V.tile_run}, {&L->step_col, &V.step_col},
         {&L->step_blk, &V.step_blk},      {&L->sm_items[0], &V.sm_items[0]},
         {&L->sm_items[1], &V.sm_items[1]},
         {&L->gl_ptr[0], &V.gl_ptr[0]},   {&L->gl_order[0], &V.gl_order[0]},

@@ -163,7 +163,7 @@ __global__ void k_group_sizes(const uint8_t* __restrict__ lay, int H, int nb, in
 
 struct Tables {
     int32_t *row_ptr, *col_idx, *blk_id, *col_ptr, *row_idx, *blk_id_csc, *blk_key, *row_order, *col_order;
-    int32_t *tile_step_ptr, *tile_order, *step_col, *step_blk, *sm_items[2];
+    int32_t *tile_step_ptr, *tile_order, *tile_run, *step_col, *step_blk, *sm_items[2];
     int32_t *gl_ptr[2], *gl_order[2], *gl_idx[2], *gl_blk[2];
 };
 
@@ -272,6 +272,15 @@ struct OrderJob {
     int32_t* out;
     int n;
 };
+// tile_run[r] = (tile, first step, step count, 0) of the r-th tile of tile_order
+__global__ void k_tile_run(Tables T, int ntiles) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= ntiles) return;
+    const int t = T.tile_order[r];
+    const int s0 = T.tile_step_ptr[t];
+    reinterpret_cast<int4*>(T.tile_run)[r] = make_int4(t, s0, T.tile_step_ptr[t + 1] - s0, 0);
+}
+
 __global__ void k_orders(const OrderJob* jobs, int wmax) {
     extern __shared__ int sh[];
     int* start = sh;              // [wmax + 1]
@@ -421,14 +430,15 @@ extern "C" int bsp_layout_compile_device(const uint8_t* layout, int H, int nb, i
     }
     const size_t nnz = (size_t)tot.nnz, nst = (size_t)tot.n_steps;
     const size_t sizes[] = {(size_t)H * (nb + 1), nnz, nnz, (size_t)H * (nb + 1), nnz, nnz, nnz, (size_t)rows,
-                            (size_t)rows, (size_t)ntiles + 1, (size_t)ntiles, nst * G, nst * G * G,
+                            (size_t)rows, (size_t)ntiles + 1, (size_t)ntiles, 4 * (size_t)ntiles, nst * G,
+                            nst * G * G,
                             4 * (size_t)tot.items[0], 4 * (size_t)tot.items[1],
                             (size_t)ntiles + 1, (size_t)ntiles, (size_t)tot.slots[0], (size_t)tot.slots[0] * G,
                             (size_t)ntiles + 1, (size_t)ntiles, (size_t)tot.slots[1], (size_t)tot.slots[1] * G};
     LayoutView& V = L->view;
     const int32_t** dst[] = {&V.row_ptr, &V.col_idx, &V.blk_id, &V.col_ptr, &V.row_idx, &V.blk_id_csc, &V.blk_key,
-                             &V.row_order, &V.col_order, &V.tile_step_ptr, &V.tile_order, &V.step_col,
-                             &V.step_blk, &V.sm_items[0], &V.sm_items[1], &V.gl_ptr[0], &V.gl_order[0],
+                             &V.row_order, &V.col_order, &V.tile_step_ptr, &V.tile_order, &V.tile_run,
+                             &V.step_col, &V.step_blk, &V.sm_items[0], &V.sm_items[1], &V.gl_ptr[0], &V.gl_order[0],
                              &V.gl_idx[0], &V.gl_blk[0], &V.gl_ptr[1], &V.gl_order[1], &V.gl_idx[1],
                              &V.gl_blk[1]};
     constexpr int nparts = sizeof(sizes) / sizeof(sizes[0]);
@@ -447,7 +457,8 @@ extern "C" int bsp_layout_compile_device(const uint8_t* layout, int H, int nb, i
     }
     Tables T;
     int32_t** tptr[] = {&T.row_ptr, &T.col_idx, &T.blk_id, &T.col_ptr, &T.row_idx, &T.blk_id_csc, &T.blk_key,
-                        &T.row_order, &T.col_order, &T.tile_step_ptr, &T.tile_order, &T.step_col, &T.step_blk,
+                        &T.row_order, &T.col_order, &T.tile_step_ptr, &T.tile_order, &T.tile_run, &T.step_col,
+                        &T.step_blk,
                         &T.sm_items[0], &T.sm_items[1], &T.gl_ptr[0], &T.gl_order[0], &T.gl_idx[0], &T.gl_blk[0],
                         &T.gl_ptr[1], &T.gl_order[1], &T.gl_idx[1], &T.gl_blk[1]};
     for (int k = 0; k < nparts; ++k) *tptr[k] = const_cast<int32_t*>(*dst[k]);
@@ -478,6 +489,7 @@ extern "C" int bsp_layout_compile_device(const uint8_t* layout, int H, int nb, i
                               {Tt(SIZE1), T.gl_order[1], ntiles}};
     ok = ok && cudaMemcpyAsync(djobs, jobs, sizeof(jobs), cudaMemcpyHostToDevice, s) == cudaSuccess;
     k_orders<<<5, 32, 2 * (nb + 1) * sizeof(int), s>>>(djobs, nb);
+    if (ntiles > 0) k_tile_run<<<(ntiles + tb - 1) / tb, tb, 0, s>>>(T, ntiles);
     ok = ok && cudaGetLastError() == cudaSuccess && cudaStreamSynchronize(s) == cudaSuccess;
     if (!ok) return fail(BSP_ERR_CUDA);
     cudaFree(scratch);

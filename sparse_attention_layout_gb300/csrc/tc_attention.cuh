@@ -198,10 +198,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             uint32_t q_it = 0, g = 0;
             bool q_skipped = false;  // test injection: the first Q tile was never loaded
             for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
-                const int tile = L.tile_order[w / args.Z];
-                const int z = (int)(w % args.Z);
+                const int4 run = tile_run_at(L, w, args.Z);
+            const int tile = run.x;
+                const int z = (int)((uint32_t)w % (uint32_t)args.Z);
                 const int h = tile / L.ngroups, gq = tile % L.ngroups;
-                const int s0 = L.tile_step_ptr[tile], ns = L.tile_step_ptr[tile + 1] - s0;
+                const int s0 = run.y, ns = run.z;
                 if (ns == 0) continue;
                 const int64_t zh = (int64_t)z * L.H + h;
                 GeoHead gh{};
@@ -281,8 +282,9 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const uint64_t dk = smem_desc(smem_u32(smem + SM::kK), 16, 1024, kSw128);
             uint32_t q_it = 0, g = 0;
             for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
-                const int tile = L.tile_order[w / args.Z];
-                const int ns = L.tile_step_ptr[tile + 1] - L.tile_step_ptr[tile];
+                const int4 run = tile_run_at(L, w, args.Z);
+            const int tile = run.x;
+                const int ns = run.z;
                 if (ns == 0) continue;
                 const uint32_t qs = q_it % QST;
                 if (!mbar_wait(&q_full[qs], (q_it / QST) & 1, ab)) goto qk_done;
@@ -312,8 +314,9 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const uint64_t dv = smem_desc(smem_u32(smem + SM::kV), 128 * 128, 1024, kSw128);
             uint32_t g = 0, tc = 0;  // tc: tiles with at least one step so far
             for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
-                const int tile = L.tile_order[w / args.Z];
-                const int ns = L.tile_step_ptr[tile + 1] - L.tile_step_ptr[tile];
+                const int4 run = tile_run_at(L, w, args.Z);
+            const int tile = run.x;
+                const int ns = run.z;
                 if (ns == 0) continue;
                 // the previous tile's O must have been read by the epilogue
                 if (tc > 0 && !mbar_wait(&o_empty, (tc - 1) & 1, ab)) goto pv_done_label;
@@ -354,10 +357,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         const uint32_t stage_s = smem_u32(stage);
         uint32_t tc = 0;
         for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
-            const int tile = L.tile_order[w / args.Z];
-            const int z = (int)(w % args.Z);
+            const int4 run = tile_run_at(L, w, args.Z);
+            const int tile = run.x;
+            const int z = (int)((uint32_t)w % (uint32_t)args.Z);
             const int h = tile / L.ngroups, gq = tile % L.ngroups;
-            const int ns = L.tile_step_ptr[tile + 1] - L.tile_step_ptr[tile];
+            const int ns = run.z;
             const int y0 = gq * 128 + quad * 32;  // first sequence row of this warp
             const int32_t zh = (int32_t)((int64_t)z * L.H + h);
             const bool live = ns > 0;
@@ -551,9 +555,10 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 ns = -1;
                 return;
             }
-            tile = L.tile_order[w / args.Z];
-            s0 = L.tile_step_ptr[tile];
-            ns = L.tile_step_ptr[tile + 1] - s0;
+            const int4 run = tile_run_at(L, w, args.Z);
+            tile = run.x;
+            s0 = run.y;
+            ns = run.z;
         };
         int64_t w = blockIdx.x;
         int tile, s0, ns;

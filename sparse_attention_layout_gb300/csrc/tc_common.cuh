@@ -133,6 +133,13 @@ __device__ __forceinline__ void mbar_drain_ring(uint64_t* bars, uint32_t nst, ui
     }
 }
 
+// The w-th work item of a persistent tile loop (w = rank * Z + z): the tile of
+// rank w / Z in longest-first order as (tile id, first step, step count, 0) --
+// one 16-byte load, not a chain of dependent ones.  Callers keep w < 2^31.
+__device__ __forceinline__ int4 tile_run_at(const LayoutView& L, int64_t w, int Z) {
+    return reinterpret_cast<const int4*>(L.tile_run)[(uint32_t)w / (uint32_t)Z];
+}
+
 // ------------------------------------------------------------------- TMA --
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,

@@ -134,10 +134,11 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             tma_prefetch_desc(&tmB);
             uint32_t a_it = 0, g = 0;
             for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
-                const int tile = L.tile_order[w / args.Z];
-                const int z = (int)(w % args.Z);
+                const int4 run = tile_run_at(L, w, args.Z);
+            const int tile = run.x;
+                const int z = (int)((uint32_t)w % (uint32_t)args.Z);
                 const int h = tile / L.ngroups, gq = tile % L.ngroups;
-                const int s0 = L.tile_step_ptr[tile], ns = L.tile_step_ptr[tile + 1] - s0;
+                const int s0 = run.y, ns = run.z;
                 if (ns == 0) continue;
                 const int64_t zh = (int64_t)z * L.H + h;
                 const uint32_t as = a_it & 1;
@@ -188,8 +189,9 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             const int nks = (a_mn || b_mn) ? kd / 16 : KP * 4;
             uint32_t a_it = 0, g = 0;
             for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
-                const int tile = L.tile_order[w / args.Z];
-                const int ns = L.tile_step_ptr[tile + 1] - L.tile_step_ptr[tile];
+                const int4 run = tile_run_at(L, w, args.Z);
+            const int tile = run.x;
+                const int ns = run.z;
                 if (ns == 0) continue;
                 const uint32_t as = a_it & 1;
                 if (!mbar_wait(&a_full[as], (a_it >> 1) & 1, ab)) goto mma_done;
@@ -242,9 +244,10 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         if (lane == 0) tma_prefetch_desc(&tmC);
         uint32_t g = 0, uses = 0;
         for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
-            const int tile = L.tile_order[w / args.Z];
-            const int z = (int)(w % args.Z);
-            const int s0 = L.tile_step_ptr[tile], ns = L.tile_step_ptr[tile + 1] - s0;
+            const int4 run = tile_run_at(L, w, args.Z);
+            const int tile = run.x;
+            const int z = (int)((uint32_t)w % (uint32_t)args.Z);
+            const int s0 = run.y, ns = run.z;
             // fused softmax: this row's running max (scaled log2 domain) and sum
             const int gq = tile % L.ngroups, rb = gq * G + a, r_in = row % BLK;
             float m = -INFINITY, l = 0.f, msub = 0.f, inv = 0.f;
