@@ -128,9 +128,10 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     __shared__ uint64_t o_full, o_empty, l_full[2], l_empty[2];
     __shared__ float lsum[2][2][128], lref[2][2][128];  // each warpgroup's sum and its reference max
     // half-row maxima of step g, one per warpgroup: xm[g % 2][wg][row], both
-    // halves announced by x_full[g % 2] (8 warp arrivals)
+    // halves of quadrant q announced by x_full[g % 2][q] (the 2 warps of the
+    // quadrant, so each pair of warps proceeds at its own pace)
     __shared__ float xm[2][2][128];
-    __shared__ uint64_t x_full[2];
+    __shared__ uint64_t x_full[2][4];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     // what each issuing thread had issued when it stopped: K steps, Q tiles
@@ -164,7 +165,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         for (int i = 0; i < 2; ++i) {
             mbar_init(&l_full[i], 8);
             mbar_init(&l_empty[i], 4);
-            mbar_init(&x_full[i], 8);
+            for (int q = 0; q < 4; ++q) mbar_init(&x_full[i][q], 2);
         }
         fence_barrier_init();
     }
@@ -591,18 +592,32 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
                 tc_fence_after();
                 const uint32_t srow = tS + sb * 128 + lane_base;
+                // a half row whose every slot is absent for all of the warp's rows
+                // (the union's blocks of the other block-row, padding) has nothing
+                // to load or exponentiate: its P is 0.  With one block-row per tile
+                // (blocks of 128) every step's block is present.
+                bool skip = false;
+                if constexpr (G > 1) {
+                    bool absent = true;
+#pragma unroll
+                    for (int ls = 0; ls < LS; ++ls) absent &= c.blk[ls] < 0;
+                    skip = __all_sync(0xffffffffu, absent);
+                }
                 float x[64];
-                tmem_ld64_sync(srow + hf * 64, srow + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[64]>(x));
-                mask_half(x, c, rb, rseq);
-                const float mx = max64(x);
+                float mx = -INFINITY;
+                if (!skip) {
+                    tmem_ld64_sync(srow + hf * 64, srow + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[64]>(x));
+                    mask_half(x, c, rb, rseq);
+                    mx = max64(x);
+                }
                 // swap half-row maxima with the other thread of the row; the arrival
                 // also tells it that this half's scores are in registers, so it may
                 // write its P over them
                 xm[xb][wg][row] = mx;
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&x_full[xb]);
-                ok = mbar_wait(&x_full[xb], (g >> 1) & 1, ab);
+                if (lane == 0) mbar_arrive(&x_full[xb][quad]);
+                ok = mbar_wait(&x_full[xb][quad], (g >> 1) & 1, ab);
                 if (!__all_sync(0xffffffffu, ok)) goto softmax_done;
                 tc_fence_after();
                 const float mrow = fmaxf(mx, xm[xb][wg ^ 1][row]);
@@ -613,7 +628,13 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 const float mnext = need ? m_new : m;
                 const float msub = (mnext == -INFINITY) ? 0.f : mnext;
                 uint32_t pk[32];
-                const float rs = exp64(x, msub, pk);
+                float rs = 0.f;
+                if (!skip) {
+                    rs = exp64(x, msub, pk);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) pk[k] = 0u;
+                }
                 tmem_st32_sync(srow + hf * 32, pk);
                 if (n > 0 && __any_sync(0xffffffffu, need)) {
                     // this half of O (scaled by m) is rescaled after P V of step g - 1
