@@ -98,6 +98,9 @@ struct bsp_layout_s {
     void* geo_dmem = nullptr;
     // streams and events of bsp_attention_host (created on first use)
     struct HostPipe* pipe = nullptr;
+    // per-(batch size, grid) work schedules of the persistent attention
+    // kernels (built on first use, see schedule.cpp)
+    struct Schedules* schedules = nullptr;
 };
 
 constexpr int kGeoRec = 8;  // ints per head in LayoutView::geo
@@ -157,6 +160,14 @@ int layout_plan(const uint8_t* layout, int H, int nb, int block, bool analyse, b
 
 // streams and events of bsp_attention_host (host_pipeline.cpp)
 void host_pipe_destroy(bsp_layout_s* L);
+
+// The work items of each CTA of a persistent attention launch with batch Z on
+// `grid` CTAs: *ptr [grid + 1] offsets into *items [Z * n_tiles] (tile, first
+// step, step count, batch entry), every item assigned longest-first to the
+// least-loaded CTA.  Built and uploaded on the first launch with (Z, grid)
+// (synchronous), kept by the handle (schedule.cpp).
+int tile_schedule(bsp_layout_s* L, int Z, int grid, const int32_t** ptr, const int4** items);
+void schedules_destroy(bsp_layout_s* L);
 
 // affine geometry (geometry.cpp)
 int affine_validate(int nb, int n, const bsp_affine_term_t* t);

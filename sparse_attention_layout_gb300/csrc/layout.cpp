@@ -343,6 +343,7 @@ extern "C" int bsp_layout_destroy(bsp_layout_t L) {
         if (cur != L->device) cudaSetDevice(L->device);
         if (cudaDeviceSynchronize() != cudaSuccess) rc = BSP_ERR_CUDA;
         bsp::host_pipe_destroy(L);
+        bsp::schedules_destroy(L);
         if (cudaFree(L->dmem) != cudaSuccess) rc = BSP_ERR_CUDA;
         if (L->geo_dmem && cudaFree(L->geo_dmem) != cudaSuccess) rc = BSP_ERR_CUDA;
         if (cur >= 0 && cur != L->device) cudaSetDevice(cur);

@@ -97,6 +97,10 @@ struct AttnArgs {
     LayoutView L;
     void* O;
     const uint8_t* mask;
+    // the CTA's work items: sched_items[sched_ptr[c] .. sched_ptr[c + 1]) =
+    // (tile, first step, step count, batch entry), longest-first greedy
+    const int32_t* sched_ptr;
+    const int4* sched_items;
     int Z;
     int kind;
     float c2;  // scale * log2(e)
@@ -179,7 +183,6 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     const uint32_t tS = tmem_base;        // S buffers at columns 0, 128 and 256
     const uint32_t tO = tmem_base + 384;  // O at column 384
 
-    const int64_t total = (int64_t)args.Z * L.n_tiles;
     const int S = L.S;
 
     // Each warpgroup changes its register share first thing in its own branch
@@ -198,10 +201,10 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             tma_prefetch_desc(tm);
             uint32_t q_it = 0, g = 0;
             bool q_skipped = false;  // test injection: the first Q tile was never loaded
-            for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
-                const int4 run = tile_run_at(L, w, args.Z);
+            for (int it = args.sched_ptr[blockIdx.x], it_end = args.sched_ptr[blockIdx.x + 1]; it < it_end; ++it) {
+                const int4 run = args.sched_items[it];
             const int tile = run.x;
-                const int z = (int)((uint32_t)w % (uint32_t)args.Z);
+                const int z = run.w;
                 const int h = tile / L.ngroups, gq = tile % L.ngroups;
                 const int s0 = run.y, ns = run.z;
                 if (ns == 0) continue;
@@ -282,8 +285,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const uint64_t dq = smem_desc(smem_u32(smem + SM::kQ), 16, 1024, kSw128);
             const uint64_t dk = smem_desc(smem_u32(smem + SM::kK), 16, 1024, kSw128);
             uint32_t q_it = 0, g = 0;
-            for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
-                const int4 run = tile_run_at(L, w, args.Z);
+            for (int it = args.sched_ptr[blockIdx.x], it_end = args.sched_ptr[blockIdx.x + 1]; it < it_end; ++it) {
+                const int4 run = args.sched_items[it];
             const int tile = run.x;
                 const int ns = run.z;
                 if (ns == 0) continue;
@@ -314,8 +317,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         if (lane == 0) {
             const uint64_t dv = smem_desc(smem_u32(smem + SM::kV), 128 * 128, 1024, kSw128);
             uint32_t g = 0, tc = 0;  // tc: tiles with at least one step so far
-            for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
-                const int4 run = tile_run_at(L, w, args.Z);
+            for (int it = args.sched_ptr[blockIdx.x], it_end = args.sched_ptr[blockIdx.x + 1]; it < it_end; ++it) {
+                const int4 run = args.sched_items[it];
             const int tile = run.x;
                 const int ns = run.z;
                 if (ns == 0) continue;
@@ -357,10 +360,10 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         uint8_t* stage = smem + SM::kEpi + quad * 4096;
         const uint32_t stage_s = smem_u32(stage);
         uint32_t tc = 0;
-        for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
-            const int4 run = tile_run_at(L, w, args.Z);
+        for (int it = args.sched_ptr[blockIdx.x], it_end = args.sched_ptr[blockIdx.x + 1]; it < it_end; ++it) {
+            const int4 run = args.sched_items[it];
             const int tile = run.x;
-            const int z = (int)((uint32_t)w % (uint32_t)args.Z);
+            const int z = run.w;
             const int h = tile / L.ngroups, gq = tile % L.ngroups;
             const int ns = run.z;
             const int y0 = gq * 128 + quad * 32;  // first sequence row of this warp
@@ -548,34 +551,36 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const float2 r2 = __fadd2_rn(__fadd2_rn(rs4[0], rs4[1]), __fadd2_rn(rs4[2], rs4[3]));
             return r2.x + r2.y;
         };
-        // the CTA's tiles: (tile id, first step, step count); ns = -1 past the end
-        auto tile_info = [&](int64_t w, int& tile, int& s0, int& ns) {
-            if (w >= total) {
+        // the CTA's work items (tile id, first step, step count, batch entry);
+        // ns = -1 past the end
+        const int it_end = args.sched_ptr[blockIdx.x + 1];
+        auto tile_info = [&](int it, int& tile, int& s0, int& ns) {
+            if (it >= it_end) {
                 tile = 0;
                 s0 = 0;
                 ns = -1;
                 return;
             }
-            const int4 run = tile_run_at(L, w, args.Z);
+            const int4 run = args.sched_items[it];
             tile = run.x;
             s0 = run.y;
             ns = run.z;
         };
-        int64_t w = blockIdx.x;
+        int it = args.sched_ptr[blockIdx.x];
         int tile, s0, ns;
-        tile_info(w, tile, s0, ns);
+        tile_info(it, tile, s0, ns);
         while (ns == 0) {  // the epilogue writes the zero rows of empty tiles
-            w += gridDim.x;
-            tile_info(w, tile, s0, ns);
+            ++it;
+            tile_info(it, tile, s0, ns);
         }
         Half hnext;
         if (ns > 0) fetch(s0, hnext);
         while (ns > 0) {
             // the next tile's place in the tables: loaded now, first used at this
             // tile's last step, so the loads overlap the steps
-            int64_t wn = w + gridDim.x;
+            int itn = it + 1;
             int tn, s0n, nsn;
-            tile_info(wn, tn, s0n, nsn);
+            tile_info(itn, tn, s0n, nsn);
             const int gq = tile % L.ngroups;
             const int rb = gq * G + a;        // block-row of this thread's query row
             const int rseq = gq * 128 + row;  // query position inside the sequence
@@ -679,11 +684,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 ++tc;
             }
             while (nsn == 0) {  // empty tiles: nothing to compute
-                wn += gridDim.x;
-                tile_info(wn, tn, s0n, nsn);
+                ++itn;
+                tile_info(itn, tn, s0n, nsn);
                 if (nsn > 0) fetch(s0n, hnext);
             }
-            w = wn;
+            it = itn;
             tile = tn;
             s0 = s0n;
             ns = nsn;
@@ -725,7 +730,12 @@ int launch_attn(const bsp_layout_s* Lh, const void* Q, const void* K, const void
     CUtensorMap mo;
     if (!rc) rc = make_tmap_3d(&mo, O, is_bf16, D, Lh->S, (uint64_t)Z * Lh->H, 64, 32);
     if (rc) return rc;
-    AttnArgs args{Lh->view, O, mask, Z, kind, scale * kLog2e};
+    const int64_t total = (int64_t)Z * Lh->n_tiles;
+    const int grid = (int)std::min<int64_t>(total, sm_count());
+    const int32_t* sp = nullptr;
+    const int4* si = nullptr;
+    if ((rc = tile_schedule(const_cast<bsp_layout_s*>(Lh), Z, grid, &sp, &si))) return rc;
+    AttnArgs args{Lh->view, O, mask, sp, si, Z, kind, scale * kLog2e};
     auto kern = attention_tc_kernel<T, BLK, D, KIND, GEO>;
     constexpr int smem = AttnSmem<D>::kAlloc;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -734,8 +744,6 @@ int launch_attn(const bsp_layout_s* Lh, const void* Q, const void* K, const void
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return BSP_ERR_CUDA;
     if ((uint32_t)fa.numRegs != kRegsLaunch) return BSP_ERR_UNSUPPORTED;
-    const int64_t total = (int64_t)Z * Lh->n_tiles;
-    const int grid = (int)std::min<int64_t>(total, sm_count());
     kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, mo, args);
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }

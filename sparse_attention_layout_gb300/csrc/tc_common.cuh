@@ -408,6 +408,10 @@ template <> struct Pack2<__half> {
 // elements, box [box_rows][box_cols], 128-byte swizzle unless given)
 int make_tmap_2d(CUtensorMap* map, const void* base, int is_bf16, uint64_t rows, uint64_t cols,
                  uint32_t box_rows, uint32_t box_cols, int swizzle_bytes);
+// host: 2-D tiled tensor map of fp32 [rows][cols], box [box_rows][box_cols]
+// (box_cols * 4 <= 128), 128-byte swizzle
+int make_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                     uint32_t box_cols);
 // host: 3-D tiled tensor map of 2-byte elements [d2][d1][d0] (d0 contiguous),
 // box [1][box1][box0], swizzle 128 / 64 / 32 bytes or 0 (none)
 int make_tmap_3d(CUtensorMap* map, const void* base, int is_bf16, uint64_t d0, uint64_t d1, uint64_t d2,

@@ -43,6 +43,20 @@ int make_tmap_2d(CUtensorMap* map, const void* base, int is_bf16, uint64_t rows,
     return r == CUDA_SUCCESS ? BSP_OK : BSP_ERR_UNSUPPORTED;
 }
 
+int make_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                     uint32_t box_cols) {
+    auto fn = encode_fn();
+    if (!fn) return BSP_ERR_CUDA;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 4};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? BSP_OK : BSP_ERR_UNSUPPORTED;
+}
+
 int make_tmap_3d(CUtensorMap* map, const void* base, int is_bf16, uint64_t d0, uint64_t d1, uint64_t d2,
                  uint32_t box0, uint32_t box1, int swizzle_bytes) {
     auto fn = encode_fn();
