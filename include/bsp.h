@@ -288,7 +288,13 @@ int bsp_softmax_noalloc(const uint8_t* layout, int H, int nb, int block, int dty
 /* Fused block-sparse attention: O = softmax(scale Q K^T restricted to the
  * layout and mask) V, the SDD -> softmax -> DSD chain in one pass that never
  * writes the scores.  Q, K, V, O: [Z][H][S][D]; rows with nothing kept are 0.
- * D: 16..128, a multiple of 16.  mask as for bsp_softmax. */
+ * D: 16..128, a multiple of 16.  mask as for bsp_softmax.
+ * The tensor-core kernels (16-bit types with D 64 or 128; fp32 with D 64, as
+ * three TF32 products per fp32 product) run as one persistent CTA per SM over
+ * a work schedule that the first call with a given Z builds on the host and
+ * uploads synchronously into a device allocation kept by the handle (see
+ * bsp_diag_attention_schedule); make that first call outside any stream
+ * capture.  Other shapes run on the FFMA kernel. */
 int bsp_attention(bsp_layout_t layout, int dtype, const void* Q, const void* K, const void* V,
                   void* O, int Z, int D, float scale, int mask_kind, const uint8_t* mask,
                   void* stream);
@@ -366,6 +372,22 @@ int bsp_diag_exp2(const float* x, float* y, int64_t n, void* stream);
  * (row a, slot b) is in the layout, else 0), so that tests can compare them
  * with the step tables without a GPU.  Other handles: BSP_ERR_UNSUPPORTED. */
 int bsp_diag_geometry_steps(bsp_layout_t layout, int32_t* step_col, int32_t* step_blk);
+
+/* The work schedule with which the fused attention kernel's `grid`
+ * persistent CTAs would process a batch of Z entries on this handle,
+ * computed ON THE HOST (a handle with host tables: bsp_layout_plan or
+ * bsp_layout_compile).  The work items are the (tile, batch entry) pairs,
+ * Z * n_tiles of them (n_tiles as bsp_layout_tiles reports), taken
+ * longest-first (tile_order, then batch entry) and each given to the CTA
+ * with the least work so far (work of a tile = its step count + 1; ties: the
+ * lowest CTA index).  ptr: HOST int32 [grid + 1], CTA c runs items
+ * ptr[c] .. ptr[c + 1] - 1 in that order; items: HOST int32 [4 * Z * n_tiles],
+ * each (tile, first step, step count, batch entry).  The kernel builds the
+ * same schedule on its first launch with a given (Z, grid), keeps it in a
+ * device allocation of the handle and reuses it afterwards.  Z < 1, grid < 1,
+ * NULL arrays or a handle compiled on the device: BSP_ERR_INVALID_ARG.  Not
+ * from the pages: the load balance of this implementation. */
+int bsp_diag_attention_schedule(bsp_layout_t layout, int Z, int grid, int32_t* ptr, int32_t* items);
 
 /* Set the limit of every bounded wait in the tensor-core kernels launched
  * with this handle from now on (wait_ns; 0 restores the default of 2 s) and

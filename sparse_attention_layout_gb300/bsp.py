@@ -67,6 +67,7 @@ def lib():
         L.bsp_layout_geometry.argtypes = [P, P, P]
         L.bsp_layout_compile_affine.argtypes = [P, P, i32, i32, i32, P, ctypes.POINTER(P)]
         L.bsp_attention_host.argtypes = [P, i32, P, P, P, P, i32, i32, f32, i32, P, P, ctypes.c_size_t, i32, P]
+        L.bsp_diag_attention_schedule.argtypes = [P, i32, i32, P, P]
         L.bsp_attention_host_workspace.argtypes = [P, i32, i32, i32]
         L.bsp_attention_host_workspace.restype = ctypes.c_size_t
         L.bsp_status_check.argtypes = [P, P]
@@ -372,6 +373,19 @@ def bsp_diag_wait_limit(L: Layout, wait_ns: int = 0, inject: int = 0):
     """Wait limit of the handle's tensor-core kernels (0 = the 2 s default)
     and test injections (INJECT_* bits; 0 = none)."""
     _check(lib().bsp_diag_wait_limit(L.handle, int(wait_ns), int(inject)), "bsp_diag_wait_limit")
+
+
+def bsp_diag_attention_schedule(L: Layout, Z: int, grid: int):
+    """(ptr [grid + 1], items [Z * n_tiles, 4]) of the fused attention kernel's
+    work schedule, computed on the host: CTA c runs items[ptr[c]:ptr[c + 1]],
+    each (tile, first step, step count, batch entry)."""
+    n_tiles = L.tiles()["n_tiles"]
+    ptr = np.zeros(int(grid) + 1, np.int32)
+    items = np.zeros((max(int(Z) * n_tiles, 1), 4), np.int32)
+    _check(lib().bsp_diag_attention_schedule(L.handle, int(Z), int(grid), ctypes.c_void_p(ptr.ctypes.data),
+                                             ctypes.c_void_p(items.ctypes.data)),
+           "bsp_diag_attention_schedule")
+    return ptr, items[:int(Z) * n_tiles]
 
 
 def attention_unfused(L: Layout, Q, K, V, scale: float, mask_kind: int = MASK_NONE, mask=None,

@@ -36,6 +36,45 @@ void schedules_destroy(bsp_layout_s* L) {
     L->schedules = nullptr;
 }
 
+namespace {
+
+// Items of all CTAs for the tiles' (tile, first step, step count) rows `run`
+// (longest-first order, 4 ints each): offs [grid + 1], items [4 * Z * nt].
+void build_schedule(const int32_t* run, int nt, int Z, int grid, std::vector<int32_t>& offs,
+                    std::vector<int32_t>& items) {
+    // work item w = rank * Z + z, weights non-increasing in w; each to the CTA
+    // with the least work (ties: the lowest CTA index)
+    const int64_t total = (int64_t)Z * nt;
+    std::vector<int32_t> owner((size_t)total);
+    using Load = std::pair<int64_t, int>;
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int c = 0; c < grid; ++c) heap.push({0, c});
+    std::vector<int32_t> count((size_t)grid, 0);
+    for (int64_t w = 0; w < total; ++w) {
+        const int r = (int)(w / Z);
+        const int64_t weight = std::max<int32_t>(run[4 * r + 2], 0) + 1;  // steps (+1: a tile's fixed cost)
+        Load top = heap.top();
+        heap.pop();
+        owner[w] = top.second;
+        ++count[top.second];
+        heap.push({top.first + weight, top.second});
+    }
+    offs.assign((size_t)grid + 1, 0);
+    for (int c = 0; c < grid; ++c) offs[c + 1] = offs[c] + count[c];
+    items.assign((size_t)4 * total, 0);
+    std::vector<int32_t> fill(offs.begin(), offs.end() - 1);
+    for (int64_t w = 0; w < total; ++w) {  // each CTA's items in longest-first order
+        const int r = (int)(w / Z), c = owner[w];
+        int32_t* it = &items[(size_t)4 * fill[c]++];
+        it[0] = run[4 * r + 0];
+        it[1] = run[4 * r + 1];
+        it[2] = run[4 * r + 2];
+        it[3] = (int32_t)(w % Z);
+    }
+}
+
+}  // namespace
+
 int tile_schedule(bsp_layout_s* L, int Z, int grid, const int32_t** ptr, const int4** items) {
     if (!L->schedules) {
         static std::mutex create_mu;
@@ -65,38 +104,11 @@ int tile_schedule(bsp_layout_s* L, int Z, int grid, const int32_t** ptr, const i
             return BSP_ERR_CUDA;
         }
     }
-    // work item w = rank * Z + z, weights non-increasing in w; each to the CTA
-    // with the least work (ties: the lowest CTA index)
-    const int64_t total = (int64_t)Z * nt;
-    std::vector<int32_t> owner((size_t)total);
-    using Load = std::pair<int64_t, int>;
-    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
-    for (int c = 0; c < grid; ++c) heap.push({0, c});
-    std::vector<int32_t> count((size_t)grid, 0);
-    for (int64_t w = 0; w < total; ++w) {
-        const int r = (int)(w / Z);
-        const int64_t weight = std::max<int32_t>(run[4 * r + 2], 0) + 1;  // steps (+1: a tile's fixed cost)
-        Load top = heap.top();
-        heap.pop();
-        owner[w] = top.second;
-        ++count[top.second];
-        heap.push({top.first + weight, top.second});
-    }
-    std::vector<int32_t> offs((size_t)grid + 1, 0);
-    for (int c = 0; c < grid; ++c) offs[c + 1] = offs[c] + count[c];
-    std::vector<int32_t> items_h((size_t)4 * total);
-    std::vector<int32_t> fill(offs.begin(), offs.end() - 1);
-    for (int64_t w = 0; w < total; ++w) {  // each CTA's items in longest-first order
-        const int r = (int)(w / Z), c = owner[w];
-        int32_t* it = &items_h[(size_t)4 * fill[c]++];
-        it[0] = run[4 * r + 0];
-        it[1] = run[4 * r + 1];
-        it[2] = run[4 * r + 2];
-        it[3] = (int32_t)(w % Z);
-    }
+    std::vector<int32_t> offs, items_h;
+    build_schedule(run.data(), nt, Z, grid, offs, items_h);
     void* d = nullptr;
     const size_t bytes = off_bytes + items_h.size() * sizeof(int32_t);
-    if (cudaMalloc(&d, bytes ? bytes : 16) != cudaSuccess) {
+    if (cudaMalloc(&d, bytes) != cudaSuccess) {
         cudaGetLastError();
         return BSP_ERR_OOM;
     }
@@ -114,3 +126,13 @@ int tile_schedule(bsp_layout_s* L, int Z, int grid, const int32_t** ptr, const i
 }
 
 }  // namespace bsp
+
+extern "C" int bsp_diag_attention_schedule(bsp_layout_t L, int Z, int grid, int32_t* ptr, int32_t* items) {
+    if (!L || !L->host_tables || Z < 1 || grid < 1 || !ptr || (!items && L->n_tiles > 0))
+        return BSP_ERR_INVALID_ARG;
+    std::vector<int32_t> offs, it;
+    bsp::build_schedule(L->tile_run.data(), L->n_tiles, Z, grid, offs, it);
+    std::copy(offs.begin(), offs.end(), ptr);
+    std::copy(it.begin(), it.end(), items);
+    return BSP_OK;
+}

@@ -344,6 +344,36 @@ def test_unfused_chain_matches_oracle(bsp, oracle, dt):
                  acc=attention_acc(Q, K, 0.125, dtype, nb * B, scores_rounded=True))
 
 
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("where", ["host", "device"])
+def test_attention_batch_sizes_on_one_handle(bsp, oracle, dt, where):
+    # the tensor-core kernels keep one work schedule per batch size: calls of
+    # changing Z on one handle (a handle compiled on the host, or on the
+    # device, whose schedule is built from tables read back) each match the
+    # oracle, and a repeated Z gives the same bytes
+    dtype = DTYPES[dt]
+    B, H, D = 64, 3, 64
+    nb = 9
+    lay = rlayout(H, nb, 0.35, 90, diag=True)
+    lay[1, 0, :] = 1  # one long block-row
+    L = (bsp.bsp_layout_compile(lay, B) if where == "host"
+         else bsp.bsp_layout_compile_device(torch.from_numpy(lay).cuda(), B))
+    first = {}
+    for Z in (3, 1, 2, 3, 1):
+        Q, K, V = (randn((Z, H, nb * B, D), dtype, 91 + k) for k in range(3))
+        O = bsp.bsp_attention(L, dev(Q), dev(K), dev(V), scale=0.125, mask_kind=2)
+        torch.cuda.synchronize()
+        assert bsp.bsp_status_check(L) == 0
+        if Z in first:
+            assert torch.equal(O.cpu(), first[Z]), f"Z={Z} repeated"
+            continue
+        first[Z] = O.cpu()
+        want = oracle.attention(lay, B, Q, K, V, 0.125, 2)
+        mag = oracle.attention(lay, B, Q, K, V.abs(), 0.125, 2)
+        assert_close(to_np(O), want, dtype, f"attention Z={Z} {dt} {where}", mag=mag,
+                     acc=attention_acc(Q, K, 0.125, dtype, nb * B))
+
+
 def test_edge_empty_layout_and_zero_batch(bsp, oracle):
     B, H, nb, D = 64, 2, 4, 64
     lay = np.zeros((H, nb, nb), np.uint8)
