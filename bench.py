@@ -176,6 +176,16 @@ def kernel_source_sha():
     return h.hexdigest()[:16]
 
 
+def launches_per_call(bsp, L, Z, dtype, device):
+    """Kernels one bsp_attention call launches: the fused kernel, plus the
+    combine pass when its schedule cuts tiles."""
+    import torch
+    from sparse_attention_layout_gb300 import workloads as W
+    n_sm = torch.cuda.get_device_properties(device).multi_processor_count
+    sc = bsp.bsp_diag_attention_schedule(L, Z, n_sm, W.torch_dtype(dtype))
+    return 1 + (len(sc["combine"]) > 0)
+
+
 def traffic_for(kernel, wname):
     """DRAM bytes per launch from a committed ncu capture, if it was taken on
     the current kernel sources (else None)."""
@@ -465,7 +475,7 @@ def workload_section(w, bsp, stream, steps, warmup, pk, pk_kind, local):
     gbs = sbytes / sms / 1e6
     out = {
         "config": config_of(w, lay, "fused attention kernel", flush),
-        "attention": {"ms": ms, "TFLOP/s": achieved, "gpu_launches": steps,
+        "attention": {"ms": ms, "TFLOP/s": achieved, "gpu_launches": steps * launches_per_call(bsp, L, w.Z, w.dtype, local),
                       "roofline": dict(attention_roofline(w, achieved, pk, pk_kind),
                                        traffic=traffic_for("attention", w.name), algorithmic_flops_per_launch=flops)},
         "softmax": {"ms": sms, "GB/s": gbs,
@@ -683,7 +693,7 @@ def run_ours(args):
         "config": config_of(w, lay_full, "fused attention kernel" + (", replayed from a CUDA graph" if args.graph else "")
                             + (f", one batch split over {world} ranks by nnz-balanced (batch, head) ranges"
                                if split else ""), flush),
-        "gpu_launches": args.steps if L is not None else 0,
+        "gpu_launches": args.steps * launches_per_call(bsp, L, Zr, w.dtype, local) if L is not None else 0,
         "roofline": roof,
         "e2e": None if e2e_ms is None else {
             "value": flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,

@@ -292,9 +292,13 @@ int bsp_softmax_noalloc(const uint8_t* layout, int H, int nb, int block, int dty
  * The tensor-core kernels (16-bit types with D 64 or 128; fp32 with D 64, as
  * three TF32 products per fp32 product) run as one persistent CTA per SM over
  * a work schedule that the first call with a given Z builds on the host and
- * uploads synchronously into a device allocation kept by the handle (see
+ * uploads synchronously into device memory kept by the handle (see
  * bsp_diag_attention_schedule); make that first call outside any stream
- * capture.  Other shapes run on the FFMA kernel. */
+ * capture.  A schedule that cuts long tiles adds a combine pass and a
+ * workspace of the handle: calls on different streams then run one after
+ * the other (an event orders them; inside a stream capture the graph's own
+ * order holds, and two graphs replaying such calls of one handle must not run
+ * concurrently).  Other shapes run on the FFMA kernel. */
 int bsp_attention(bsp_layout_t layout, int dtype, const void* Q, const void* K, const void* V,
                   void* O, int Z, int D, float scale, int mask_kind, const uint8_t* mask,
                   void* stream);
@@ -373,21 +377,47 @@ int bsp_diag_exp2(const float* x, float* y, int64_t n, void* stream);
  * with the step tables without a GPU.  Other handles: BSP_ERR_UNSUPPORTED. */
 int bsp_diag_geometry_steps(bsp_layout_t layout, int32_t* step_col, int32_t* step_blk);
 
-/* The work schedule with which the fused attention kernel's `grid`
- * persistent CTAs would process a batch of Z entries on this handle,
- * computed ON THE HOST (a handle with host tables: bsp_layout_plan or
- * bsp_layout_compile).  The work items are the (tile, batch entry) pairs,
- * Z * n_tiles of them (n_tiles as bsp_layout_tiles reports), taken
- * longest-first (tile_order, then batch entry) and each given to the CTA
- * with the least work so far (work of a tile = its step count + 1; ties: the
- * lowest CTA index).  ptr: HOST int32 [grid + 1], CTA c runs items
- * ptr[c] .. ptr[c + 1] - 1 in that order; items: HOST int32 [4 * Z * n_tiles],
- * each (tile, first step, step count, batch entry).  The kernel builds the
- * same schedule on its first launch with a given (Z, grid), keeps it in a
- * device allocation of the handle and reuses it afterwards.  Z < 1, grid < 1,
- * NULL arrays or a handle compiled on the device: BSP_ERR_INVALID_ARG.  Not
- * from the pages: the load balance of this implementation. */
-int bsp_diag_attention_schedule(bsp_layout_t layout, int Z, int grid, int32_t* ptr, int32_t* items);
+/* The work schedule of the fused attention kernel for a batch of Z entries of
+ * type dtype on a GPU with n_sm SMs, computed ON THE HOST (a handle with host
+ * tables: bsp_layout_plan or bsp_layout_compile; the setting of
+ * bsp_diag_attention_split applies).  The work items are the (tile, batch
+ * entry) pairs (n_tiles as bsp_layout_tiles reports), or pieces of them: a
+ * tile may be cut into pieces of consecutive steps, each of which leaves a
+ * partial result (the rows' unnormalised output, running max and sum) that a
+ * combine pass merges by the running-max / running-sum recurrence of the
+ * Triton-Puzzles blog, Puzzle 9 "Simple FlashAttention".  For fp32 every
+ * tile of more than 32 steps of 128 keys is cut, whatever the split setting:
+ * the output keeps its 1e-5 accuracy while one accumulation in tensor memory
+ * spans at most 4096 keys (the pieces are merged in fp32 on the CUDA cores);
+ * 16-bit types are cut only for balance.  The items are
+ * taken longest-first and each given to the CTA with the least work so far
+ * (work of an item = its step count + 1; ties: the lowest CTA index).
+ * Outputs: *grid CTAs, *n_items items, *n_split cut tiles; with non-NULL
+ * arrays also ptr [grid + 1] (CTA c runs items ptr[c] .. ptr[c + 1] - 1 in
+ * that order), items [4 * n_items] (tile, first step, step count, batch
+ * entry), part [n_items] (the partial-result slot of a piece, else -1) and
+ * combine [4 * n_split] (tile, batch entry, first slot, pieces), all HOST
+ * int32.  The kernel builds the same schedule on its first launch with a
+ * given Z, dtype and split setting, keeps it in device memory of the handle
+ * and reuses it afterwards.  Z < 1, n_sm < 1, an unknown dtype, NULL counts
+ * or a handle compiled on the device: BSP_ERR_INVALID_ARG.  Not from the pages: the load balance of
+ * this implementation. */
+int bsp_diag_attention_schedule(bsp_layout_t layout, int dtype, int Z, int n_sm, int* grid, int* n_items,
+                                int* n_split, int32_t* ptr, int32_t* items, int32_t* part, int32_t* combine);
+
+/* How the fused attention kernels of this handle cut long tiles from now on:
+ * max_steps 0 (the default) cuts only when the greedy makespan of whole
+ * tiles is at least a tenth and 24 steps longer than with pieces of about
+ * half a CTA's fair share; max_steps > 0 cuts every tile of more than
+ * max_steps steps of 128 keys into pieces of at most max_steps steps;
+ * max_steps < 0 never cuts (fp32 launches still cut every tile of more than
+ * 32 steps, see bsp_diag_attention_schedule).  A launch with cut tiles adds
+ * the combine pass and
+ * uses a device workspace of the handle (128 x 130 floats per piece) that
+ * launches on different streams take in turn.  NULL handle:
+ * BSP_ERR_INVALID_ARG.  Not from the pages: the load balance of this
+ * implementation. */
+int bsp_diag_attention_split(bsp_layout_t layout, int max_steps);
 
 /* Set the limit of every bounded wait in the tensor-core kernels launched
  * with this handle from now on (wait_ns; 0 restores the default of 2 s) and

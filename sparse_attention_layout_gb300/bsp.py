@@ -67,7 +67,8 @@ def lib():
         L.bsp_layout_geometry.argtypes = [P, P, P]
         L.bsp_layout_compile_affine.argtypes = [P, P, i32, i32, i32, P, ctypes.POINTER(P)]
         L.bsp_attention_host.argtypes = [P, i32, P, P, P, P, i32, i32, f32, i32, P, P, ctypes.c_size_t, i32, P]
-        L.bsp_diag_attention_schedule.argtypes = [P, i32, i32, P, P]
+        L.bsp_diag_attention_schedule.argtypes = [P, i32, i32, i32, P, P, P, P, P, P, P]
+        L.bsp_diag_attention_split.argtypes = [P, i32]
         L.bsp_attention_host_workspace.argtypes = [P, i32, i32, i32]
         L.bsp_attention_host_workspace.restype = ctypes.c_size_t
         L.bsp_status_check.argtypes = [P, P]
@@ -375,17 +376,32 @@ def bsp_diag_wait_limit(L: Layout, wait_ns: int = 0, inject: int = 0):
     _check(lib().bsp_diag_wait_limit(L.handle, int(wait_ns), int(inject)), "bsp_diag_wait_limit")
 
 
-def bsp_diag_attention_schedule(L: Layout, Z: int, grid: int):
-    """(ptr [grid + 1], items [Z * n_tiles, 4]) of the fused attention kernel's
-    work schedule, computed on the host: CTA c runs items[ptr[c]:ptr[c + 1]],
-    each (tile, first step, step count, batch entry)."""
-    n_tiles = L.tiles()["n_tiles"]
-    ptr = np.zeros(int(grid) + 1, np.int32)
-    items = np.zeros((max(int(Z) * n_tiles, 1), 4), np.int32)
-    _check(lib().bsp_diag_attention_schedule(L.handle, int(Z), int(grid), ctypes.c_void_p(ptr.ctypes.data),
-                                             ctypes.c_void_p(items.ctypes.data)),
+def bsp_diag_attention_schedule(L: Layout, Z: int, n_sm: int, dtype=torch.bfloat16):
+    """The fused attention kernel's work schedule, computed on the host:
+    dict(grid, ptr [grid + 1], items [n, 4] (tile, first step, step count,
+    batch entry), part [n] (partial-result slot of a piece of a cut tile, else
+    -1), combine [n_split, 4] (tile, batch entry, first slot, pieces)); CTA c
+    runs items[ptr[c]:ptr[c + 1]]."""
+    f = lib().bsp_diag_attention_schedule
+    dt = _DTYPES[dtype]
+    g, n, ns = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(f(L.handle, dt, int(Z), int(n_sm), ctypes.byref(g), ctypes.byref(n), ctypes.byref(ns), None, None, None, None),
            "bsp_diag_attention_schedule")
-    return ptr, items[:int(Z) * n_tiles]
+    out = {"ptr": np.zeros(g.value + 1, np.int32), "items": np.zeros((max(n.value, 1), 4), np.int32),
+           "part": np.zeros(max(n.value, 1), np.int32), "combine": np.zeros((max(ns.value, 1), 4), np.int32)}
+    _check(f(L.handle, dt, int(Z), int(n_sm), ctypes.byref(g), ctypes.byref(n), ctypes.byref(ns),
+             *[ctypes.c_void_p(out[k].ctypes.data) for k in ("ptr", "items", "part", "combine")]),
+           "bsp_diag_attention_schedule")
+    out["items"], out["part"], out["combine"] = out["items"][:n.value], out["part"][:n.value], out["combine"][:ns.value]
+    out["grid"] = g.value
+    return out
+
+
+def bsp_diag_attention_split(L: Layout, max_steps: int):
+    """Cutting of long tiles by the handle's fused attention kernels: 0
+    automatic (default), > 0 every tile of more than max_steps steps, < 0
+    never."""
+    _check(lib().bsp_diag_attention_split(L.handle, int(max_steps)), "bsp_diag_attention_split")
 
 
 def attention_unfused(L: Layout, Q, K, V, scale: float, mask_kind: int = MASK_NONE, mask=None,

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 #include <vector>
 
 #include "../../include/bsp.h"
@@ -98,9 +99,12 @@ struct bsp_layout_s {
     void* geo_dmem = nullptr;
     // streams and events of bsp_attention_host (created on first use)
     struct HostPipe* pipe = nullptr;
-    // per-(batch size, grid) work schedules of the persistent attention
-    // kernels (built on first use, see schedule.cpp)
+    // work schedules of the persistent attention kernels per (batch size,
+    // SM count, split setting), built on first use (schedule.cpp)
     struct Schedules* schedules = nullptr;
+    // cutting of long tiles: 0 automatic, > 0 every tile of more steps than
+    // this, < 0 never (bsp_diag_attention_split)
+    int attn_split = 0;
 };
 
 constexpr int kGeoRec = 8;  // ints per head in LayoutView::geo
@@ -161,13 +165,50 @@ int layout_plan(const uint8_t* layout, int H, int nb, int block, bool analyse, b
 // streams and events of bsp_attention_host (host_pipeline.cpp)
 void host_pipe_destroy(bsp_layout_s* L);
 
-// The work items of each CTA of a persistent attention launch with batch Z on
-// `grid` CTAs: *ptr [grid + 1] offsets into *items [Z * n_tiles] (tile, first
-// step, step count, batch entry), every item assigned longest-first to the
-// least-loaded CTA.  Built and uploaded on the first launch with (Z, grid)
-// (synchronous), kept by the handle (schedule.cpp).
-int tile_schedule(bsp_layout_s* L, int Z, int grid, const int32_t** ptr, const int4** items);
+// Floats of one partial-result slot of a cut tile: 128 rows of O (head size
+// up to 128), then the rows' running maxima (log2 units) and sums.
+constexpr int kPartRows = 128, kPartMaxD = 128;
+constexpr size_t kPartFloats = (size_t)kPartRows * (kPartMaxD + 2);
+
+// The work schedule of a persistent attention launch with batch Z on a GPU
+// with `sms` SMs (schedule.cpp): CTA c of `grid` runs items ptr[c] ..
+// ptr[c + 1] - 1, each (tile, first step, step count, batch entry) with
+// part[i] = its partial-result slot when the item is a piece of a cut tile,
+// else -1; combine [n_split] = (tile, batch entry, first slot, pieces) of the
+// cut tiles, merged after the kernel by launch_attention_combine; ws: the
+// slots (n_split > 0 only), ordered between streams by the event `done`.
+struct AttnSchedule {
+    int grid;
+    int n_split;
+    const int32_t* ptr;
+    const int4* items;
+    const int32_t* part;
+    const int4* combine;
+    float* ws;
+    cudaEvent_t done;
+    std::mutex* mu;  // held from attn_schedule_begin to attn_schedule_end when n_split > 0
+};
+// Tiles of more steps than this are always cut for the given input type:
+// fp32 results keep their 1e-5 accuracy while one accumulation of O in
+// tensor memory spans at most 32 steps (4096 keys; measured: one accumulation
+// over 16384 keys gave a normwise error of 1.5e-5); the pieces are merged in
+// fp32 on the CUDA cores.  0: no forced cut.
+constexpr int kF32MaxSteps = 32;
+inline int attn_force_cap(int dtype) { return dtype == BSP_F32 ? kF32MaxSteps : 0; }
+// Built and uploaded (synchronously) on the first launch with (Z, sms, the
+// handle's split setting, force_cap), kept by the handle.
+int tile_schedule(bsp_layout_s* L, int Z, int sms, int force_cap, AttnSchedule* out);
 void schedules_destroy(bsp_layout_s* L);
+// O rows of the cut tiles from their pieces' partial results (attn_combine.cu)
+int launch_attention_combine(const bsp_layout_s* L, int dtype, const AttnSchedule& sc, void* O, int D,
+                             cudaStream_t s);
+// Around one persistent attention launch on stream s: begin fetches the
+// schedule and, when it cuts tiles, takes the workspace (lock, and a wait for
+// the workspace's previous launch); end (called whenever begin succeeded, with
+// the launch's status rc) merges the cut tiles and releases the workspace.
+int attn_schedule_begin(bsp_layout_s* L, int dtype, int Z, cudaStream_t s, AttnSchedule* sc);
+int attn_schedule_end(const bsp_layout_s* L, int dtype, const AttnSchedule& sc, void* O, int D, cudaStream_t s,
+                      int rc);
 
 // affine geometry (geometry.cpp)
 int affine_validate(int nb, int n, const bsp_affine_term_t* t);

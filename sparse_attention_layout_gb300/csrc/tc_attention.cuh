@@ -101,6 +101,10 @@ struct AttnArgs {
     // (tile, first step, step count, batch entry), longest-first greedy
     const int32_t* sched_ptr;
     const int4* sched_items;
+    // per item: the partial-result slot of a piece of a cut tile, else -1;
+    // a piece leaves its rows' raw O, running max and sum in part_ws
+    const int32_t* sched_part;
+    float* part_ws;
     int Z;
     int kind;
     float c2;  // scale * log2(e)
@@ -369,8 +373,10 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const int y0 = gq * 128 + quad * 32;  // first sequence row of this warp
             const int32_t zh = (int32_t)((int64_t)z * L.H + h);
             const bool live = ns > 0;
+            const int part = args.sched_part[it];
             const uint32_t lb = tc & 1;
             float inv = 0.f;  // rows with nothing kept are 0
+            float mf = -INFINITY, lt = 0.f;
             if (live) {
                 bool ok = mbar_wait(&l_full[lb], (tc >> 1) & 1, ab);
                 if (!__all_sync(0xffffffffu, ok)) goto epilogue_done;
@@ -380,12 +386,35 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 const float l0 = lsum[lb][0][row], l1 = lsum[lb][1][row];
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&l_empty[lb]);
-                const float mf = fmaxf(m0, m1);
-                const float lt = mf == -INFINITY ? 0.f : l0 * ex2_approx(m0 - mf) + l1 * ex2_approx(m1 - mf);
+                mf = fmaxf(m0, m1);
+                lt = mf == -INFINITY ? 0.f : l0 * ex2_approx(m0 - mf) + l1 * ex2_approx(m1 - mf);
                 inv = lt > 0.f ? 1.0f / lt : 0.f;
                 ok = mbar_wait(&o_full, tc & 1, ab);
                 if (!__all_sync(0xffffffffu, ok)) goto epilogue_done;
                 tc_fence_after();
+            }
+            if (part >= 0) {
+                // a piece of a cut tile: the row's O as accumulated (relative
+                // to its reference max mf), mf and the sum, for the combine
+                // pass; every piece has steps, so live holds
+                float* pw = args.part_ws + (size_t)part * kPartFloats;
+                float* orow = pw + (size_t)row * D;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32_sync(tO + lane_base + c * 32, r);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        *reinterpret_cast<uint4*>(orow + c * 32 + 4 * k) =
+                            make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&o_empty);
+                pw[kPartRows * kPartMaxD + row] = mf;
+                pw[kPartRows * kPartMaxD + kPartRows + row] = lt;
+                ++tc;
+                continue;
             }
             // O leaves through the warp's 32 x 64 staging panel, one TMA store per
             // 64 columns.  Every column of O is read out of TMEM before the
@@ -730,12 +759,6 @@ int launch_attn(const bsp_layout_s* Lh, const void* Q, const void* K, const void
     CUtensorMap mo;
     if (!rc) rc = make_tmap_3d(&mo, O, is_bf16, D, Lh->S, (uint64_t)Z * Lh->H, 64, 32);
     if (rc) return rc;
-    const int64_t total = (int64_t)Z * Lh->n_tiles;
-    const int grid = (int)std::min<int64_t>(total, sm_count());
-    const int32_t* sp = nullptr;
-    const int4* si = nullptr;
-    if ((rc = tile_schedule(const_cast<bsp_layout_s*>(Lh), Z, grid, &sp, &si))) return rc;
-    AttnArgs args{Lh->view, O, mask, sp, si, Z, kind, scale * kLog2e};
     auto kern = attention_tc_kernel<T, BLK, D, KIND, GEO>;
     constexpr int smem = AttnSmem<D>::kAlloc;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -744,8 +767,14 @@ int launch_attn(const bsp_layout_s* Lh, const void* Q, const void* K, const void
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return BSP_ERR_CUDA;
     if ((uint32_t)fa.numRegs != kRegsLaunch) return BSP_ERR_UNSUPPORTED;
-    kern<<<grid, kThreads, smem, s>>>(mq, mk, mv, mo, args);
-    return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
+    AttnSchedule sc;
+    if ((rc = attn_schedule_begin(const_cast<bsp_layout_s*>(Lh), is_bf16 ? BSP_BF16 : BSP_F16, Z, s, &sc))) return rc;
+    AttnArgs args{Lh->view, O, mask, sc.ptr, sc.items, sc.part, sc.ws, Z, kind, scale * kLog2e};
+    if (sc.grid > 0) {
+        kern<<<sc.grid, kThreads, smem, s>>>(mq, mk, mv, mo, args);
+        rc = cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
+    }
+    return attn_schedule_end(Lh, is_bf16 ? BSP_BF16 : BSP_F16, sc, O, D, s, rc);
 }
 
 template <typename T, int BLK, int KIND, bool GEO>

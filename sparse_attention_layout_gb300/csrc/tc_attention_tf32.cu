@@ -73,6 +73,10 @@ struct Attn32Args {
     // (tile, first step, step count, batch entry), longest-first greedy
     const int32_t* sched_ptr;
     const int4* sched_items;
+    // per item: the partial-result slot of a piece of a cut tile, else -1;
+    // a piece leaves its rows' raw O, running max and sum in part_ws
+    const int32_t* sched_part;
+    float* part_ws;
     int Z;
     float c2;  // scale * log2(e)
 };
@@ -534,7 +538,20 @@ attention_tf32_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&o_empty);
-                if (rseq < S) {
+                const int part = args.sched_part[it];
+                if (part >= 0) {
+                    // a piece of a cut tile: O as accumulated (relative to the
+                    // common reference m), m and the sum, for the combine pass
+                    float* pw = args.part_ws + (size_t)part * kPartFloats;
+                    float* prow = pw + (size_t)row * D + 32 * hf;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        reinterpret_cast<uint4*>(prow)[k] = make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+                    if (hf == 0) {
+                        pw[kPartRows * kPartMaxD + row] = m;
+                        pw[kPartRows * kPartMaxD + kPartRows + row] = lt;
+                    }
+                } else if (rseq < S) {
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
                         reinterpret_cast<float4*>(orow)[k] =
@@ -575,12 +592,6 @@ int launch32(const bsp_layout_s* Lh, const void* Q, const void* K, const void* V
     int rc = make_tmap_2d_f32(&mq, Q, rows, D, 128, 32);
     if (!rc) rc = make_tmap_2d_f32(&mk, K, rows, D, R, 32);
     if (rc) return rc;
-    const int64_t total = (int64_t)Z * Lh->n_tiles;
-    const int grid = (int)std::min<int64_t>(total, sm_count());
-    const int32_t* sp = nullptr;
-    const int4* si = nullptr;
-    if ((rc = tile_schedule(const_cast<bsp_layout_s*>(Lh), Z, grid, &sp, &si))) return rc;
-    Attn32Args args{Lh->view, (const float*)V, (float*)O, mask, sp, si, Z, scale * kLog2e};
     auto kern = attention_tf32_kernel<BLK, KIND>;
     constexpr int smem = Smem32::kAlloc;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -589,8 +600,14 @@ int launch32(const bsp_layout_s* Lh, const void* Q, const void* K, const void* V
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return BSP_ERR_CUDA;
     if ((uint32_t)fa.numRegs != kRegsLaunch) return BSP_ERR_UNSUPPORTED;
-    kern<<<grid, kThreads, smem, s>>>(mq, mk, args);
-    return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
+    AttnSchedule sc;
+    if ((rc = attn_schedule_begin(const_cast<bsp_layout_s*>(Lh), BSP_F32, Z, s, &sc))) return rc;
+    Attn32Args args{Lh->view, (const float*)V, (float*)O, mask, sc.ptr, sc.items, sc.part, sc.ws, Z, scale * kLog2e};
+    if (sc.grid > 0) {
+        kern<<<sc.grid, kThreads, smem, s>>>(mq, mk, args);
+        rc = cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
+    }
+    return attn_schedule_end(Lh, BSP_F32, sc, O, D, s, rc);
 }
 
 template <int BLK>

@@ -374,6 +374,76 @@ def test_attention_batch_sizes_on_one_handle(bsp, oracle, dt, where):
                      acc=attention_acc(Q, K, 0.125, dtype, nb * B))
 
 
+@pytest.mark.parametrize("B", [16, 64, 128])
+@pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("kind", [0, 1, 2])
+@pytest.mark.parametrize("cut", [1, 3])
+def test_attention_cut_tiles(bsp, oracle, B, dt, kind, cut):
+    # long block-rows cut into pieces of at most `cut` steps, merged by the
+    # combine pass: the oracle's result, the same bytes on a second call
+    # (the merge order is fixed), and the result without cuts for balance
+    # within the tolerance
+    dtype = DTYPES[dt]
+    Z, H, D = 2, 3, 64
+    nb = max(4, 1024 // B) + 1
+    S = nb * B
+    lay = rlayout(H, nb, 0.25, 95 + B + kind, diag=(kind == 2))
+    lay[0, 0, :] = 1           # a long first block-row
+    lay[2, nb - 1, :] = 1      # and a long last one (ragged tile)
+    if kind == 2:
+        lay[:, np.arange(nb), np.arange(nb)] = 1
+    L = bsp.bsp_layout_compile(lay, B)
+    mask = W.random_mask(S, 0.8, 96) if kind == 1 else None
+    dmask = None if mask is None else dev(torch.from_numpy(mask))
+    Q, K, V = (randn((Z, H, S, D), dtype, 97 + k) for k in range(3))
+    q, k, v = dev(Q), dev(K), dev(V)
+    bsp.bsp_diag_attention_split(L, cut)
+    sc = bsp.bsp_diag_attention_schedule(L, Z, torch.cuda.get_device_properties(0).multi_processor_count, dtype)
+    assert len(sc["combine"]) > 0
+    O1 = bsp.bsp_attention(L, q, k, v, scale=0.125, mask_kind=kind, mask=dmask)
+    O2 = bsp.bsp_attention(L, q, k, v, scale=0.125, mask_kind=kind, mask=dmask)
+    bsp.bsp_diag_attention_split(L, -1)
+    O0 = bsp.bsp_attention(L, q, k, v, scale=0.125, mask_kind=kind, mask=dmask)
+    torch.cuda.synchronize()
+    assert bsp.bsp_status_check(L) == 0
+    assert torch.equal(O1, O2)
+    want = oracle.attention(lay, B, Q, K, V, 0.125, kind, mask)
+    mag = oracle.attention(lay, B, Q, K, V.abs(), 0.125, kind, mask)
+    acc = attention_acc(Q, K, 0.125, dtype, S)
+    assert_close(to_np(O1), want, dtype, f"cut tiles B={B} {dt} kind={kind} cut={cut}", mag=mag, acc=acc)
+    assert_close(to_np(O0), want, dtype, f"uncut B={B} {dt} kind={kind}", mag=mag, acc=acc)
+
+
+def test_attention_cut_tiles_two_streams(bsp, oracle):
+    # two streams sharing one handle whose schedule cuts tiles: the workspace
+    # is taken in turn, both results equal the single-stream one
+    B, Z, H, D = 64, 2, 2, 64
+    nb = 17
+    lay = rlayout(H, nb, 0.3, 98, diag=True)
+    lay[:, 0, :] = 1
+    L = bsp.bsp_layout_compile(lay, B)
+    bsp.bsp_diag_attention_split(L, 2)
+    Q, K, V = (randn((Z, H, nb * B, D), torch.bfloat16, 99 + k) for k in range(3))
+    Q2 = randn((Z, H, nb * B, D), torch.bfloat16, 102)
+    q, k, v, q2 = dev(Q), dev(K), dev(V), dev(Q2)
+    ref1 = bsp.bsp_attention(L, q, k, v, scale=0.125, mask_kind=2)
+    ref2 = bsp.bsp_attention(L, q2, k, v, scale=0.125, mask_kind=2)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for _ in range(8):
+        o1, o2 = torch.empty_like(q), torch.empty_like(q)
+        bsp.bsp_attention(L, q, k, v, o1, 0.125, 2, stream=s1)
+        bsp.bsp_attention(L, q2, k, v, o2, 0.125, 2, stream=s2)
+        outs.append((o1, o2))
+    torch.cuda.synchronize()
+    assert bsp.bsp_status_check(L) == 0
+    for o1, o2 in outs:
+        assert torch.equal(o1, ref1) and torch.equal(o2, ref2)
+    want = oracle.attention(lay, B, Q, K, V, 0.125, 2)
+    assert_close(to_np(ref1), want, torch.bfloat16, "cut tiles, two streams")
+
+
 def test_edge_empty_layout_and_zero_batch(bsp, oracle):
     B, H, nb, D = 64, 2, 4, 64
     lay = np.zeros((H, nb, nb), np.uint8)

@@ -245,3 +245,38 @@ def test_long_sequence_band(bsp, oracle):
     for got, what in ((o, "fused attention"), (o2, "fused SDD + softmax -> DSD")):
         g = to_np(got.reshape(-1, D)[torch.from_numpy(sel).cuda()])
         assert_close(g, want, torch.bfloat16, f"S={S} {what}, {sel.size} sampled rows", mag=mag, acc=acc)
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_long_global_rows_cut(bsp, oracle, dt):
+    """BigBird over S = 16384 (Z1 H12 D64 B64, window 3, 2 global, 3 random,
+    diagonal-causal): each head's global-row tile has 128 steps against a fair
+    share of ~80, so the automatic schedule cuts those tiles and merges their
+    pieces.  Sampled rows (the global rows included) against the oracle; the
+    result without cuts for balance within the same bound."""
+    from types import SimpleNamespace
+    B, nb, H, Z, D = 64, 256, 12, 1, 64
+    S = nb * B
+    lay = W.layout_bigbird(nb, H, window=3, n_global=2, n_random=3, seed=2)
+    L = bsp.bsp_layout_compile(lay, B)
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert len(bsp.bsp_diag_attention_schedule(L, Z, n_sm, DT[dt])["combine"]) == H
+    Q, K, V = (W.randn((Z, H, S, D), dt, 520 + s) for s in range(3))
+    q, k, v = (t.cuda() for t in (Q, K, V))
+    o = bsp.bsp_attention(L, q, k, v, None, 0.125, W.MASK_DIAG_CAUSAL)
+    # no cuts for balance (fp32 still cuts at 32 steps: one accumulation of
+    # all 16384 keys in tensor memory missed 1e-5, normwise 1.5e-5)
+    bsp.bsp_diag_attention_split(L, -1)
+    assert len(bsp.bsp_diag_attention_schedule(L, Z, n_sm, DT[dt])["combine"]) == (H if dt == "f32" else 0)
+    o_whole = bsp.bsp_attention(L, q, k, v, None, 0.125, W.MASK_DIAG_CAUSAL)
+    torch.cuda.synchronize()
+    assert bsp.bsp_status_check(L) == 0
+    w = SimpleNamespace(Z=Z, H=H, S=S, B=B)
+    sel = np.unique(np.concatenate([sample_rows(w, lay, 40, 19),
+                                    [h * S + r for h in (0, 5, 11) for r in (0, 63, 64, 127)]])).astype(np.int64)
+    want = oracle.attention(lay, B, Q, K, V, 0.125, W.MASK_DIAG_CAUSAL, sel=sel)
+    mag = oracle.attention(lay, B, Q, K, V.abs(), 0.125, W.MASK_DIAG_CAUSAL, sel=sel)
+    acc = attention_acc(q, k, 0.125, DT[dt], S).reshape(-1, 1)[sel]
+    for got, what in ((o, "cut"), (o_whole, "whole tiles")):
+        g = to_np(got.reshape(-1, D)[torch.from_numpy(sel).cuda()])
+        assert_close(g, want, DT[dt], f"BigBird S={S} {dt} {what}, {sel.size} sampled rows", mag=mag, acc=acc)
