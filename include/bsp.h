@@ -315,16 +315,19 @@ int bsp_attention(bsp_layout_t layout, int dtype, const void* Q, const void* K, 
 int bsp_softmax_backward(bsp_layout_t layout, int dtype, const void* Y, const void* dY, void* dX, int Z,
                          float scale, void* stream);
 
-/* Gradients of bsp_attention for the output gradient dO, as the unfused chain
+/* Gradients of bsp_attention for the output gradient dO, as the chain
  *     P = softmax(scale Q K^T on the layout and mask)   (recomputed)
  *     dV = P^T dO,  dP = dO V^T (on the layout),  dX = bsp_softmax_backward(P, dP),
  *     dQ = dX K,  dK = dX^T Q
  * of this library's fused SDD + softmax, DSD, SDD and softmax backward calls
  * (bsp_sdd_softmax, bsp_dsd, bsp_sdd, bsp_softmax_backward), enqueued on
- * `stream`.  Q, K, V, dO, dQ, dK, dV: DEVICE [Z][H][S][D], D and the mask as for
- * bsp_attention.  P_ws, dP_ws: caller-owned DEVICE workspace of Z * nnz *
- * block * block elements each (P and dP / dX live there afterwards); they may
- * be NULL when the layout has no block, in which case dQ, dK, dV are zeroed.
+ * `stream`; for 16-bit types on the tensor-core shapes dP and dX come from one
+ * fused pass (dP = dO V^T kept in fp32 on chip, dX written), the other cases
+ * write dP and run the softmax backward in place.  Q, K, V, dO, dQ, dK, dV:
+ * DEVICE [Z][H][S][D], D and the mask as for bsp_attention.  P_ws, dP_ws:
+ * caller-owned DEVICE workspace of Z * nnz * block * block elements each (P
+ * and dX live there afterwards); they may be NULL when the layout has no
+ * block, in which case dQ, dK, dV are zeroed.
  * The pages state no backward (the chain rule on their definitions). */
 int bsp_attention_backward(bsp_layout_t layout, int dtype, const void* Q, const void* K, const void* V,
                            const void* dO, void* dQ, void* dK, void* dV, int Z, int D, float scale,

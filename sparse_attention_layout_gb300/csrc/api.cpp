@@ -226,9 +226,16 @@ extern "C" int bsp_attention_backward(bsp_layout_t L, int dtype, const void* Q, 
     if ((rc = bsp_sdd_softmax(L, dtype, Q, K, P_ws, Z, D, 0, 1, scale, mask_kind, mask, stream))) return rc;
     // dV = P^T dO
     if ((rc = bsp_dsd(L, dtype, P_ws, dO, dV, Z, D, 1, 0, stream))) return rc;
-    // dP = dO V^T on the layout, then the gradient of the raw scores Q K^T in place
-    if ((rc = bsp_sdd(L, dtype, dO, V, dP_ws, Z, D, 0, 1, stream))) return rc;
-    if ((rc = bsp_softmax_backward(L, dtype, P_ws, dP_ws, dP_ws, Z, scale, stream))) return rc;
+    // dX = scale P .* (dP - rowsum(P .* dP)) with dP = dO V^T on the layout: one
+    // fused pass on the tensor cores (dP stays on chip), else dP through memory
+    // and the softmax backward in place
+    rc = force_simt() ? BSP_ERR_UNSUPPORTED
+                      : bsp::launch_sdd_softmax_bwd_tc(L, dtype, dO, V, P_ws, dP_ws, Z, D, scale, s);
+    if (rc == BSP_ERR_UNSUPPORTED) {
+        if ((rc = bsp_sdd(L, dtype, dO, V, dP_ws, Z, D, 0, 1, stream))) return rc;
+        rc = bsp_softmax_backward(L, dtype, P_ws, dP_ws, dP_ws, Z, scale, stream);
+    }
+    if (rc) return rc;
     // dQ = dX K,  dK = dX^T Q
     if ((rc = bsp_dsd(L, dtype, dP_ws, K, dQ, Z, D, 0, 0, stream))) return rc;
     return bsp_dsd(L, dtype, dP_ws, Q, dK, Z, D, 1, 0, stream);

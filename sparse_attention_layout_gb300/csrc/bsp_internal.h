@@ -148,6 +148,10 @@ int launch_sdd_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B
 // fused SDD + row softmax (P = softmax(scale * SDD) on the layout's blocks)
 int launch_sdd_softmax_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* P, int Z, int K,
                           int ta, int tb, float scale, int kind, const uint8_t* mask, cudaStream_t s);
+// dX = scale P .* (dP - rowsum(P .* dP)) with dP = dO V^T on the layout
+// (fused SDD + softmax backward; 16-bit types, tensor-core shapes only)
+int launch_sdd_softmax_bwd_tc(const bsp_layout_s* L, int dtype, const void* dO, const void* V, const void* P,
+                              void* dX, int Z, int D, float scale, cudaStream_t s);
 int launch_dsd_group_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z,
                         int N, int ta, int tb, cudaStream_t s);
 int launch_dds_group_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z,

@@ -402,6 +402,20 @@ template <> struct Pack2<__half> {
     }
 };
 
+// two packed 16-bit values (element 0 in the low half) as floats
+template <typename T> struct Unpack2;
+template <> struct Unpack2<__nv_bfloat16> {
+    __device__ __forceinline__ static float2 unpack(uint32_t u) {
+        return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+    }
+};
+template <> struct Unpack2<__half> {
+    __device__ __forceinline__ static float2 unpack(uint32_t u) {
+        __half2 v = *reinterpret_cast<__half2*>(&u);
+        return __half22float2(v);
+    }
+};
+
 }  // namespace tc
 
 // host: encode a 2-D tiled tensor map (row-major [rows][cols] of 2-byte

@@ -28,6 +28,16 @@
 // P = 2^(scale log2(e) s - max) / sum instead of S.  The scores never reach
 // HBM; the second pass repeats the matrix products, which cost less than the
 // round trip of S they replace.
+//
+// SMB (fused SDD + softmax backward, for the attention backward): the product
+// is dP = dO V^T, and with the softmax output P of the same layout the
+// epilogue writes the gradient of the scaled scores,
+//     dX = scale P .* (dP - rowsum(P .* dP)),
+// the softmax backward of the chain rule.  The row sum needs the whole row,
+// so the tile's steps again run twice: the first pass accumulates
+// rowsum(P .* dP) (reading the thread's row of every present P block), the
+// second recomputes dP and writes dX.  dP never reaches memory and stays in
+// fp32; masked entries have P = 0 and so dX = 0.
 #include <algorithm>
 #include <type_traits>
 
@@ -53,30 +63,42 @@ struct SddArgs {
     float c2;
     int kind;
     const uint8_t* mask;
+    // fused softmax backward only: the softmax output [Z][nnz][B][B] and the scale
+    const void* P;
+    float scale;
 };
 
 __host__ __device__ constexpr uint32_t swz_of(int row_bytes) {
     return row_bytes == 128 ? kSw128 : (row_bytes == 64 ? kSw64 : kSw32);
 }
 
-template <int KP, int BLK>
+// MODE 2 (fused softmax backward): a key-tile stage also holds the step's P
+// tile (128 query rows x 128 keys, two 128-byte-swizzled panels of 64 keys,
+// copied by the producer with the V tile), and one query-tile stage and two
+// key-tile stages make room for it: the product is light there, the
+// epilogue is what a step waits for.
+template <int KP, int BLK, int MODE>
 struct SddCfg {
     static constexpr int kTile = 128 * 64 * KP * 2;  // 128 rows x K (KP panels of 64)
-    static constexpr int BST = 3;                    // key-tile stages
-    static constexpr int kA = 0;                     // 2 query-tile stages
-    static constexpr int kB = 2 * kTile;
-    static constexpr int kStg = kB + BST * kTile;    // staging: 2 buffers per epilogue warp
+    static constexpr int AST = MODE == 2 ? 1 : 2;    // query-tile stages
+    static constexpr int BST = MODE == 2 ? 2 : 3;    // key-tile stages
+    static constexpr int kPT = MODE == 2 ? 32768 : 0;  // P tile of a key-tile stage
+    static constexpr int kBStage = kTile + kPT;
+    static constexpr int kA = 0;
+    static constexpr int kB = AST * kTile;
+    static constexpr int kStg = kB + BST * kBStage;  // staging: 2 buffers per epilogue warp
     static constexpr int kBuf = 32 * BLK * 2;        // one buffer: a warp's 32 rows of one block
     static constexpr int kAlloc = kStg + 4 * 2 * kBuf + 1024;
 };
 
-template <typename T, int BLK, int KP, bool SMX>
+// MODE: 0 plain SDD, 1 fused softmax (SMX), 2 fused softmax backward (SMB)
+template <typename T, int BLK, int KP, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-              const __grid_constant__ CUtensorMap tmC, const SddArgs args) {
-    using C = SddCfg<KP, BLK>;
+              const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP, const SddArgs args) {
+    using C = SddCfg<KP, BLK, MODE>;
     constexpr int G = 128 / BLK;
-    constexpr int BST = C::BST;
+    constexpr int AST = C::AST, BST = C::BST;
     constexpr uint32_t kTileBytes = C::kTile;
     // MN-major key tiles: panels of W keys (RB bytes per K row), KPB per block
     constexpr int W = BLK < 64 ? BLK : 64, RB = 2 * W, KPB = BLK / W;
@@ -85,11 +107,12 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     // bytes one stage's copies deliver: K-major boxes are 64 * KP columns wide
     // (zero-filled past K), MN-major ones exactly K rows
     const uint32_t a_bytes = a_mn ? 256u * kd : kTileBytes, b_bytes = b_mn ? 256u * kd : kTileBytes;
-    constexpr int NPASS = SMX ? 2 : 1;  // passes over a tile's steps
+    constexpr bool SMX = MODE == 1, SMB = MODE == 2;
+    constexpr int NPASS = MODE != 0 ? 2 : 1;  // passes over a tile's steps
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    __shared__ uint64_t a_full[2], a_empty[2], b_full[BST], b_empty[BST], s_full[4], s_empty[4];
+    __shared__ uint64_t a_full[AST], a_empty[AST], b_full[BST], b_empty[BST], s_full[4], s_empty[4];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     // what the issuing threads had issued when they stopped (A tiles, B
@@ -102,13 +125,13 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int i = 0; i < 3; ++i) issued[i] = 0;
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < AST; ++i) {
             mbar_init(&a_full[i], 1);
             mbar_init(&a_empty[i], 1);
         }
         for (int i = 0; i < BST; ++i) {
             mbar_init(&b_full[i], 1);
-            mbar_init(&b_empty[i], 1);
+            mbar_init(&b_empty[i], SMB ? 5 : 1);  // SMB: the epilogue warps also read the stage's P
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&s_full[i], 1);
@@ -141,8 +164,8 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 const int s0 = run.y, ns = run.z;
                 if (ns == 0) continue;
                 const int64_t zh = (int64_t)z * L.H + h;
-                const uint32_t as = a_it & 1;
-                if (!mbar_wait(&a_empty[as], ((a_it >> 1) & 1) ^ 1, ab)) goto producer_done;
+                const uint32_t as = a_it % AST;
+                if (!mbar_wait(&a_empty[as], ((a_it / AST) & 1) ^ 1, ab)) goto producer_done;
                 mbar_arrive_expect_tx(&a_full[as], a_bytes);
                 if (a_mn) {
                     // [K rows][128 query columns]: two panels of 64 columns
@@ -159,7 +182,15 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     const int s = s0 + it % ns;
                     const uint32_t st = g % BST;
                     if (!mbar_wait(&b_empty[st], ((g / BST) & 1) ^ 1, ab)) goto producer_done;
-                    mbar_arrive_expect_tx(&b_full[st], b_bytes);
+                    uint32_t p_bytes = 0;  // SMB: the step's present P blocks
+                    if constexpr (SMB) {
+#pragma unroll
+                        for (int ra = 0; ra < G; ++ra)
+#pragma unroll
+                            for (int b = 0; b < G; ++b)
+                                if (L.step_blk[(s * G + ra) * G + b] >= 0) p_bytes += BLK * BLK * 2;
+                    }
+                    mbar_arrive_expect_tx(&b_full[st], b_bytes + p_bytes);
 #pragma unroll
                     for (int b = 0; b < G; ++b) {
                         int c = L.step_col[s * G + b];
@@ -167,13 +198,30 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                         if (b_mn) {
                             // [K rows][B key columns]: KPB panels of W columns
                             for (int p = 0; p < KPB; ++p)
-                                tma_load_2d(smem_u32(smem + C::kB + st * kTileBytes + (b * KPB + p) * (kd * RB)),
+                                tma_load_2d(smem_u32(smem + C::kB + st * C::kBStage + (b * KPB + p) * (kd * RB)),
                                             &tmB, c * BLK + W * p, (int32_t)(zh * kd), &b_full[st]);
                         } else {
                             for (int p = 0; p < KP; ++p)
-                                tma_load_2d(smem_u32(smem + C::kB + st * kTileBytes + p * 16384 + b * BLK * 128),
+                                tma_load_2d(smem_u32(smem + C::kB + st * C::kBStage + p * 16384 + b * BLK * 128),
                                             &tmB, p * 64, (int32_t)(zh * S + (int64_t)c * BLK), &b_full[st]);
                         }
+                    }
+                    if constexpr (SMB) {
+                        // P block (row block ra, slot b) -> rows [ra B, ra B + B) of the
+                        // panel(s) of keys [b B, b B + B)
+                        const uint32_t pt = smem_u32(smem + C::kB + st * C::kBStage + C::kTile);
+#pragma unroll
+                        for (int ra = 0; ra < G; ++ra)
+#pragma unroll
+                            for (int b = 0; b < G; ++b) {
+                                const int blk = L.step_blk[(s * G + ra) * G + b];
+                                if (blk < 0) continue;
+                                const int32_t prow = (int32_t)(((int64_t)z * L.nnz + blk) * BLK);
+#pragma unroll
+                                for (int p = 0; p < BLK / 64; ++p)
+                                    tma_load_2d(pt + (b * (BLK / 64) + p) * 16384 + ra * BLK * 128, &tmP, p * 64, prow,
+                                                &b_full[st]);
+                            }
                     }
                 }
             }
@@ -193,15 +241,15 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             const int tile = run.x;
                 const int ns = run.z;
                 if (ns == 0) continue;
-                const uint32_t as = a_it & 1;
-                if (!mbar_wait(&a_full[as], (a_it >> 1) & 1, ab)) goto mma_done;
+                const uint32_t as = a_it % AST;
+                if (!mbar_wait(&a_full[as], (a_it / AST) & 1, ab)) goto mma_done;
                 for (int it = 0; it < NPASS * ns; ++it, ++g) {
                     const uint32_t sb = g & 3, st = g % BST;  // TMEM accumulator, key-tile stage
                     if (!mbar_wait(&s_empty[sb], ((g >> 2) & 1) ^ 1, ab)) goto mma_done;
                     if (!mbar_wait(&b_full[st], (g / BST) & 1, ab)) goto mma_done;
                     tc_fence_after();
                     const uint32_t abase = smem_u32(smem + C::kA + as * kTileBytes);
-                    const uint32_t bbase = smem_u32(smem + C::kB + st * kTileBytes);
+                    const uint32_t bbase = smem_u32(smem + C::kB + st * C::kBStage);
                     for (int ks = 0; ks < nks; ++ks) {
                         const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;  // K-major step
                         const uint64_t da = a_mn ? smem_desc(abase + ks * 2048, kd * 128, 1024, kSw128)
@@ -251,9 +299,10 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             // fused softmax: this row's running max (scaled log2 domain) and sum
             const int gq = tile % L.ngroups, rb = gq * G + a, r_in = row % BLK;
             float m = -INFINITY, l = 0.f, msub = 0.f, inv = 0.f;
+            float dsum = 0.f;  // fused softmax backward: rowsum(P .* dP)
             for (int it = 0; it < NPASS * ns; ++it, ++g) {
                 const int n = it % ns, s = s0 + n;
-                const bool write = !SMX || it >= ns;  // the pass that writes
+                const bool write = MODE == 0 || it >= ns;  // the pass that writes
                 const uint32_t sb = g & 3;
                 bool ok = mbar_wait(&s_full[sb], (g >> 2) & 1, ab);
                 if (!__all_sync(0xffffffffu, ok)) goto epi_done;
@@ -267,6 +316,47 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s_empty[sb]);
+                if constexpr (SMB) {
+                    float* xf = reinterpret_cast<float*>(x);
+                    // this row of the stage's P tile (the copies landed: wait on the
+                    // stage's full barrier), zeros for absent pairs; then the
+                    // stage is released by this warp
+                    const uint32_t st = g % BST;
+                    ok = mbar_wait(&b_full[st], (g / BST) & 1, ab);
+                    if (!__all_sync(0xffffffffu, ok)) goto epi_done;
+                    uint32_t pv[64];
+                    const uint8_t* pb = smem + C::kB + st * C::kBStage + C::kTile + row * 128;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const int b = (c * 8) / BLK;
+                        const bool present = L.step_blk[(s * G + a) * G + b] >= 0;
+                        const uint4 v = present ? *reinterpret_cast<const uint4*>(pb + (c >> 3) * 16384 +
+                                                                                   (((c & 7) ^ (row & 7)) << 4))
+                                                : make_uint4(0u, 0u, 0u, 0u);
+                        pv[4 * c + 0] = v.x;
+                        pv[4 * c + 1] = v.y;
+                        pv[4 * c + 2] = v.z;
+                        pv[4 * c + 3] = v.w;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&b_empty[st]);
+                    if (!write) {
+                        // first pass: rowsum(P .* dP)
+#pragma unroll
+                        for (int j = 0; j < 64; ++j) {
+                            const float2 pf = Unpack2<T>::unpack(pv[j]);
+                            dsum = fmaf(pf.x, xf[2 * j], dsum);
+                            dsum = fmaf(pf.y, xf[2 * j + 1], dsum);
+                        }
+                        continue;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) {
+                        const float2 pf = Unpack2<T>::unpack(pv[j]);
+                        xf[2 * j] = args.scale * pf.x * (xf[2 * j] - dsum);
+                        xf[2 * j + 1] = args.scale * pf.y * (xf[2 * j + 1] - dsum);
+                    }
+                }
                 if constexpr (SMX) {
                     // masked entries -> -inf: absent (row block, key block) pairs,
                     // columns past the diagonal inside diagonal blocks, dense-mask zeros
@@ -371,7 +461,7 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         // stopped early: the copies and products issued before the stop land
         // before the CTA lets go of its shared memory and TMEM
         if (threadIdx.x == 0) {
-            mbar_drain_ring(a_full, 2, issued[0], ab);
+            mbar_drain_ring(a_full, AST, issued[0], ab);
             mbar_drain_ring(b_full, BST, issued[1], ab);
             if (issued[2]) mbar_drain(&s_full[(issued[2] - 1) & 3], ((issued[2] - 1) >> 2) & 1, ab);
         }
@@ -385,13 +475,13 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
 
 // --------------------------------------------------------------- launch ----
 
-template <typename T, int BLK, int KP, bool SMX>
+template <typename T, int BLK, int KP, int MODE>
 int sdd_launch(const bsp_layout_s* Lh, const void* A, const void* B, void* Cout, int Z, int K, int ta, int tb,
-               float c2, int kind, const uint8_t* mask, cudaStream_t s) {
+               float c2, int kind, const uint8_t* mask, const void* P, float scale, cudaStream_t s) {
     const int bf = std::is_same<T, __nv_bfloat16>::value;
     const uint64_t ZH = (uint64_t)Z * Lh->H, rows = ZH * Lh->S;
     constexpr int W = BLK < 64 ? BLK : 64;
-    CUtensorMap ma, mb, mc;
+    CUtensorMap ma, mb, mc, mp;
     // [S][K] operands: boxes of 128 (A) or B (B) rows x 64 columns; [K][S]
     // operands: boxes of K rows x 64 (A) or W (B) columns
     int rc = ta ? make_tmap_2d(&ma, A, bf, ZH * K, Lh->S, K, 64, 128) : make_tmap_2d(&ma, A, bf, rows, K, 128, 64, 128);
@@ -402,33 +492,39 @@ int sdd_launch(const bsp_layout_s* Lh, const void* A, const void* B, void* Cout,
     if (!rc)
         rc = make_tmap_3d(&mc, Cout, bf, BLK, (uint64_t)Z * Lh->nnz * BLK, 1, W, BLK < 32 ? BLK : 32,
                           BLK >= 64 ? 128 : 0);
+    // fused softmax backward: P rows [Z * nnz * B][B], boxes of B rows x 64
+    // columns, 128-byte swizzle (the other modes never read this map)
+    if (!rc) {
+        if constexpr (MODE == 2) rc = make_tmap_2d(&mp, P, bf, (uint64_t)Z * Lh->nnz * BLK, BLK, BLK, 64, 128);
+        else mp = mc;
+    }
     if (rc) return rc;
-    SddArgs a{Lh->view, Cout, Z, K, ta, tb, c2, kind, mask};
-    auto kern = sdd_tc_kernel<T, BLK, KP, SMX>;
-    constexpr int smem = SddCfg<KP, BLK>::kAlloc;
+    SddArgs a{Lh->view, Cout, Z, K, ta, tb, c2, kind, mask, P, scale};
+    auto kern = sdd_tc_kernel<T, BLK, KP, MODE>;
+    constexpr int smem = SddCfg<KP, BLK, MODE>::kAlloc;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return BSP_ERR_CUDA;
     const int64_t total = (int64_t)Z * Lh->n_tiles;
     const int grid = (int)std::min<int64_t>(total, sm_count());
-    kern<<<grid, kThreads, smem, s>>>(ma, mb, mc, a);
+    kern<<<grid, kThreads, smem, s>>>(ma, mb, mc, mp, a);
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }
 
-template <typename T, int BLK, bool SMX>
+template <typename T, int BLK, int MODE>
 int sdd_by_k(const bsp_layout_s* L, const void* A, const void* B, void* C, int Z, int K, int ta, int tb, float c2,
-             int kind, const uint8_t* mask, cudaStream_t s) {
-    if (K <= 64) return sdd_launch<T, BLK, 1, SMX>(L, A, B, C, Z, K, ta, tb, c2, kind, mask, s);
-    return sdd_launch<T, BLK, 2, SMX>(L, A, B, C, Z, K, ta, tb, c2, kind, mask, s);
+             int kind, const uint8_t* mask, const void* P, float scale, cudaStream_t s) {
+    if (K <= 64) return sdd_launch<T, BLK, 1, MODE>(L, A, B, C, Z, K, ta, tb, c2, kind, mask, P, scale, s);
+    return sdd_launch<T, BLK, 2, MODE>(L, A, B, C, Z, K, ta, tb, c2, kind, mask, P, scale, s);
 }
 
-template <typename T, bool SMX>
+template <typename T, int MODE>
 int sdd_by_block(const bsp_layout_s* L, const void* A, const void* B, void* C, int Z, int K, int ta, int tb,
-                 float c2, int kind, const uint8_t* mask, cudaStream_t s) {
+                 float c2, int kind, const uint8_t* mask, const void* P, float scale, cudaStream_t s) {
     switch (L->B) {
-        case 16: return sdd_by_k<T, 16, SMX>(L, A, B, C, Z, K, ta, tb, c2, kind, mask, s);
-        case 32: return sdd_by_k<T, 32, SMX>(L, A, B, C, Z, K, ta, tb, c2, kind, mask, s);
-        case 64: return sdd_by_k<T, 64, SMX>(L, A, B, C, Z, K, ta, tb, c2, kind, mask, s);
-        case 128: return sdd_by_k<T, 128, SMX>(L, A, B, C, Z, K, ta, tb, c2, kind, mask, s);
+        case 16: return sdd_by_k<T, 16, MODE>(L, A, B, C, Z, K, ta, tb, c2, kind, mask, P, scale, s);
+        case 32: return sdd_by_k<T, 32, MODE>(L, A, B, C, Z, K, ta, tb, c2, kind, mask, P, scale, s);
+        case 64: return sdd_by_k<T, 64, MODE>(L, A, B, C, Z, K, ta, tb, c2, kind, mask, P, scale, s);
+        case 128: return sdd_by_k<T, 128, MODE>(L, A, B, C, Z, K, ta, tb, c2, kind, mask, P, scale, s);
         default: return BSP_ERR_UNSUPPORTED;
     }
 }
@@ -447,8 +543,9 @@ bool sdd_tc_shape(const bsp_layout_s* L, int Z, int K, int ta, int tb) {
 int launch_sdd_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z, int K, int ta,
                   int tb, cudaStream_t s) {
     if (!sdd_tc_shape(L, Z, K, ta, tb)) return BSP_ERR_UNSUPPORTED;
-    if (dtype == BSP_BF16) return sdd_by_block<__nv_bfloat16, false>(L, A, B, C, Z, K, ta, tb, 0.f, 0, nullptr, s);
-    if (dtype == BSP_F16) return sdd_by_block<__half, false>(L, A, B, C, Z, K, ta, tb, 0.f, 0, nullptr, s);
+    if (dtype == BSP_BF16)
+        return sdd_by_block<__nv_bfloat16, 0>(L, A, B, C, Z, K, ta, tb, 0.f, 0, nullptr, nullptr, 0.f, s);
+    if (dtype == BSP_F16) return sdd_by_block<__half, 0>(L, A, B, C, Z, K, ta, tb, 0.f, 0, nullptr, nullptr, 0.f, s);
     return BSP_ERR_UNSUPPORTED;
 }
 
@@ -456,8 +553,19 @@ int launch_sdd_softmax_tc(const bsp_layout_s* L, int dtype, const void* A, const
                           int ta, int tb, float scale, int kind, const uint8_t* mask, cudaStream_t s) {
     if (!sdd_tc_shape(L, Z, K, ta, tb)) return BSP_ERR_UNSUPPORTED;
     const float c2 = scale * kLog2e;
-    if (dtype == BSP_BF16) return sdd_by_block<__nv_bfloat16, true>(L, A, B, P, Z, K, ta, tb, c2, kind, mask, s);
-    if (dtype == BSP_F16) return sdd_by_block<__half, true>(L, A, B, P, Z, K, ta, tb, c2, kind, mask, s);
+    if (dtype == BSP_BF16)
+        return sdd_by_block<__nv_bfloat16, 1>(L, A, B, P, Z, K, ta, tb, c2, kind, mask, nullptr, 0.f, s);
+    if (dtype == BSP_F16) return sdd_by_block<__half, 1>(L, A, B, P, Z, K, ta, tb, c2, kind, mask, nullptr, 0.f, s);
+    return BSP_ERR_UNSUPPORTED;
+}
+
+int launch_sdd_softmax_bwd_tc(const bsp_layout_s* L, int dtype, const void* dO, const void* V, const void* P,
+                              void* dX, int Z, int D, float scale, cudaStream_t s) {
+    // P arrives in 64-key panels: blocks of 64 and 128 only
+    if (!sdd_tc_shape(L, Z, D, 0, 1) || L->B < 64) return BSP_ERR_UNSUPPORTED;
+    if (dtype == BSP_BF16)
+        return sdd_by_block<__nv_bfloat16, 2>(L, dO, V, dX, Z, D, 0, 1, 0.f, 0, nullptr, P, scale, s);
+    if (dtype == BSP_F16) return sdd_by_block<__half, 2>(L, dO, V, dX, Z, D, 0, 1, 0.f, 0, nullptr, P, scale, s);
     return BSP_ERR_UNSUPPORTED;
 }
 
