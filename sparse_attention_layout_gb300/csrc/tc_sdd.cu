@@ -15,10 +15,13 @@
 // descriptor and the instruction's major-ness bits change.  No transpose
 // happens in memory.
 //
-// Roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner and
-// single-thread MMA issuer, warps 2..5 epilogue (thread = TMEM lane).  The
-// epilogue stages each present block's rows in shared memory and writes them
-// with asynchronous bulk copies, so its warps never wait on the global writes.
+// Roles (320 threads): warp 0 TMA producer, warp 1 TMEM owner and
+// single-thread MMA issuer, warps 2..9 epilogue (thread = TMEM lane; warps
+// 2..5 take columns 0..63 of the 128-column score tile, warps 6..9 columns
+// 64..127).  The epilogue stages each present piece's rows in shared memory
+// and writes them with asynchronous bulk copies, so its warps never wait on
+// the global writes.  Halving each thread's columns (against four warps on
+// whole rows) is what the fused modes' epilogue-bound passes need.
 //
 // SMX (fused SDD + row softmax): the whole key stream of a row tile is one
 // CTA's, and an epilogue thread owns one query row, so the row softmax fits
@@ -49,7 +52,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer, MMA issuer, 8 epilogue warps
 
 // ------------------------------------------------------------------ SDD ----
 
@@ -80,15 +83,18 @@ __host__ __device__ constexpr uint32_t swz_of(int row_bytes) {
 template <int KP, int BLK, int MODE>
 struct SddCfg {
     static constexpr int kTile = 128 * 64 * KP * 2;  // 128 rows x K (KP panels of 64)
-    static constexpr int AST = MODE == 2 ? 1 : 2;    // query-tile stages
-    static constexpr int BST = MODE == 2 ? 2 : 3;    // key-tile stages
+    static constexpr int AST = MODE == 2 ? 1 : 2;                // query-tile stages
+    // key-tile stages: two in the fused modes at K = 128 (their per-tile
+    // exchange arrays leave no room for a third)
+    static constexpr int BST = (MODE == 2 || (MODE == 1 && KP == 2)) ? 2 : 3;
     static constexpr int kPT = MODE == 2 ? 32768 : 0;  // P tile of a key-tile stage
     static constexpr int kBStage = kTile + kPT;
     static constexpr int kA = 0;
     static constexpr int kB = AST * kTile;
-    static constexpr int kStg = kB + BST * kBStage;  // staging: 2 buffers per epilogue warp
-    static constexpr int kBuf = 32 * BLK * 2;        // one buffer: a warp's 32 rows of one block
-    static constexpr int kAlloc = kStg + 4 * 2 * kBuf + 1024;
+    static constexpr int kStg = kB + BST * kBStage;  // staging: NBUF buffers per epilogue warp
+    static constexpr int NBUF = MODE == 2 ? 1 : 2;
+    static constexpr int kBuf = 32 * (BLK < 64 ? BLK : 64) * 2;  // a warp's 32 rows of one piece
+    static constexpr int kAlloc = kStg + 8 * NBUF * kBuf + 1024;
 };
 
 // MODE: 0 plain SDD, 1 fused softmax (SMX), 2 fused softmax backward (SMB)
@@ -113,6 +119,10 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     __shared__ uint64_t a_full[AST], a_empty[AST], b_full[BST], b_empty[BST], s_full[4], s_empty[4];
+    // fused modes: the two halves of every row exchange their statistics once
+    // per tile (the two warps of lane quadrant q: xq[q]; values in xs)
+    __shared__ uint64_t xq[4];
+    __shared__ float2 xs[MODE != 0 ? 2 : 1][2][MODE != 0 ? 128 : 1];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     // what the issuing threads had issued when they stopped (A tiles, B
@@ -131,12 +141,13 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         }
         for (int i = 0; i < BST; ++i) {
             mbar_init(&b_full[i], 1);
-            mbar_init(&b_empty[i], SMB ? 5 : 1);  // SMB: the epilogue warps also read the stage's P
+            mbar_init(&b_empty[i], SMB ? 9 : 1);  // SMB: the eight epilogue warps also read the stage's P
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], 4);
+            mbar_init(&s_empty[i], 8);
         }
+        for (int i = 0; i < 4; ++i) mbar_init(&xq[i], 2);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -237,9 +248,7 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             const int nks = (a_mn || b_mn) ? kd / 16 : KP * 4;
             uint32_t a_it = 0, g = 0;
             for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
-                const int4 run = tile_run_at(L, w, args.Z);
-            const int tile = run.x;
-                const int ns = run.z;
+                const int ns = tile_run_at(L, w, args.Z).z;
                 if (ns == 0) continue;
                 const uint32_t as = a_it % AST;
                 if (!mbar_wait(&a_full[as], (a_it / AST) & 1, ab)) goto mma_done;
@@ -268,38 +277,42 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             issued[2] = g;
         }
     } else {
-        // Epilogue: each warp owns 32 rows of the tile (TMEM lanes 32q..32q+31).
-        // Per present block it stages its rows in one of its two buffers, laid
-        // out as the output rows they become (RS = min(32, B) consecutive rows
-        // of one output block per copy unit), and lane 0 issues the copies: a
-        // 128-byte-swizzled tensor store per 64 columns for blocks of 64 and
-        // 128 (conflict-free row-per-lane staging), one contiguous bulk copy
-        // otherwise.  Before refilling a buffer the warp waits only until the
-        // copy issued from it two uses ago has read it.
+        // Epilogue: eight warps; warp w owns 32 rows of the tile (TMEM lanes of
+        // quadrant q = w % 4) and one half of the 128 columns (hf = (w - 2) / 4:
+        // keys [64 hf, 64 hf + 64)).  A half holds NPH pieces of CW columns:
+        // whole blocks when B <= 64, one 64-column half of a block when B = 128.
+        // Per present piece the warp stages its rows as the output rows they
+        // become and lane 0 issues the copies: a 128-byte-swizzled tensor store
+        // (32 rows x 64 columns) for blocks of 64 and 128, one contiguous bulk
+        // copy of RS rows otherwise.  The fused modes keep per-half row
+        // statistics through their first pass and combine the two halves of
+        // every row once per tile (xq barriers, values in xs).
         constexpr int RS = BLK < 32 ? BLK : 32;
-        constexpr int BW = BLK < 64 ? BLK : 64;  // columns per staged row of one box
-        constexpr int RBY = BW * 2;              // bytes per such row
-        constexpr int NBX = BLK / BW;            // boxes across a block row
-        constexpr int C16 = BLK * 2 / 16;        // 16-byte chunks per block row
-        constexpr int kSeg = RS * BLK * 2;       // one copy unit
-        const int quad = warp & 3;
+        constexpr int CW = BLK < 64 ? BLK : 64;  // columns of one piece
+        constexpr int NPH = 64 / CW;             // pieces per half row
+        constexpr int RBY = CW * 2;              // bytes per staged row of a piece
+        constexpr int C16 = CW * 2 / 16;         // 16-byte chunks per staged row
+        constexpr int kSeg = RS * CW * 2;        // one copy unit
+        constexpr int NBUF = C::NBUF;
+        const int quad = warp & 3, hf = (warp - 2) >> 2;
         const int row = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const int a = row / BLK;
         const int seg = lane / RS, rin = lane % RS;
-        uint8_t* stg = smem + C::kStg + quad * 2 * C::kBuf;
+        uint8_t* stg = smem + C::kStg + (warp - 2) * NBUF * C::kBuf;
         T* Cp = reinterpret_cast<T*>(args.C);
         if (lane == 0) tma_prefetch_desc(&tmC);
-        uint32_t g = 0, uses = 0;
+        uint32_t g = 0, uses = 0, xc = 0;  // xc: row-statistics exchanges so far
         for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
             const int4 run = tile_run_at(L, w, args.Z);
             const int tile = run.x;
             const int z = (int)((uint32_t)w % (uint32_t)args.Z);
             const int s0 = run.y, ns = run.z;
-            // fused softmax: this row's running max (scaled log2 domain) and sum
+            // fused softmax: this half row's running max (scaled log2 domain) and
+            // sum, then the row's; fused softmax backward: rowsum(P .* dP)
             const int gq = tile % L.ngroups, rb = gq * G + a, r_in = row % BLK;
             float m = -INFINITY, l = 0.f, msub = 0.f, inv = 0.f;
-            float dsum = 0.f;  // fused softmax backward: rowsum(P .* dP)
+            float dsum = 0.f;
             for (int it = 0; it < NPASS * ns; ++it, ++g) {
                 const int n = it % ns, s = s0 + n;
                 const bool write = MODE == 0 || it >= ns;  // the pass that writes
@@ -307,31 +320,31 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 bool ok = mbar_wait(&s_full[sb], (g >> 2) & 1, ab);
                 if (!__all_sync(0xffffffffu, ok)) goto epi_done;
                 tc_fence_after();
-                uint32_t x[128];
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    tmem_ld32_sync(tS + sb * 128 + lane_base + c * 32,
-                                   *reinterpret_cast<uint32_t(*)[32]>(x + 32 * c));
-                // the accumulator is free as soon as it is in registers
+                uint32_t x[64];
+                tmem_ld32_sync(tS + sb * 128 + lane_base + 64 * hf, *reinterpret_cast<uint32_t(*)[32]>(x));
+                tmem_ld32_sync(tS + sb * 128 + lane_base + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
+                // the accumulator is free once both halves are in registers
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s_empty[sb]);
+                float* xf = reinterpret_cast<float*>(x);
+                // the pieces of this half: slot and block id of (row block a, slot)
+                int pblk[NPH];
+#pragma unroll
+                for (int p = 0; p < NPH; ++p) pblk[p] = L.step_blk[(s * G + a) * G + (64 * hf + p * CW) / BLK];
                 if constexpr (SMB) {
-                    float* xf = reinterpret_cast<float*>(x);
-                    // this row of the stage's P tile (the copies landed: wait on the
-                    // stage's full barrier), zeros for absent pairs; then the
-                    // stage is released by this warp
+                    // this half row of the stage's P tile (panel hf; the copies
+                    // landed: wait on the stage's full barrier), zeros for absent
+                    // pieces; then the stage is released by this warp
                     const uint32_t st = g % BST;
                     ok = mbar_wait(&b_full[st], (g / BST) & 1, ab);
                     if (!__all_sync(0xffffffffu, ok)) goto epi_done;
-                    uint32_t pv[64];
-                    const uint8_t* pb = smem + C::kB + st * C::kBStage + C::kTile + row * 128;
+                    uint32_t pv[32];
+                    const uint8_t* pb = smem + C::kB + st * C::kBStage + C::kTile + hf * 16384 + row * 128;
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const int b = (c * 8) / BLK;
-                        const bool present = L.step_blk[(s * G + a) * G + b] >= 0;
-                        const uint4 v = present ? *reinterpret_cast<const uint4*>(pb + (c >> 3) * 16384 +
-                                                                                   (((c & 7) ^ (row & 7)) << 4))
+                    for (int c = 0; c < 8; ++c) {
+                        const bool present = pblk[(c * 8) / CW] >= 0;
+                        const uint4 v = present ? *reinterpret_cast<const uint4*>(pb + ((c ^ (row & 7)) << 4))
                                                 : make_uint4(0u, 0u, 0u, 0u);
                         pv[4 * c + 0] = v.x;
                         pv[4 * c + 1] = v.y;
@@ -341,88 +354,114 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&b_empty[st]);
                     if (!write) {
-                        // first pass: rowsum(P .* dP)
+                        // first pass: this half's rowsum(P .* dP); at the tile's last
+                        // step the two halves of the row are added
 #pragma unroll
-                        for (int j = 0; j < 64; ++j) {
+                        for (int j = 0; j < 32; ++j) {
                             const float2 pf = Unpack2<T>::unpack(pv[j]);
                             dsum = fmaf(pf.x, xf[2 * j], dsum);
                             dsum = fmaf(pf.y, xf[2 * j + 1], dsum);
                         }
+                        if (it == ns - 1) {
+                            xs[xc & 1][hf][row] = make_float2(dsum, 0.f);
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&xq[quad]);
+                            ok = mbar_wait(&xq[quad], xc & 1, ab);
+                            if (!__all_sync(0xffffffffu, ok)) goto epi_done;
+                            dsum += xs[xc & 1][hf ^ 1][row].x;
+                            ++xc;
+                        }
                         continue;
                     }
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) {
+                    for (int j = 0; j < 32; ++j) {
                         const float2 pf = Unpack2<T>::unpack(pv[j]);
                         xf[2 * j] = args.scale * pf.x * (xf[2 * j] - dsum);
                         xf[2 * j + 1] = args.scale * pf.y * (xf[2 * j + 1] - dsum);
                     }
                 }
                 if constexpr (SMX) {
-                    // masked entries -> -inf: absent (row block, key block) pairs,
-                    // columns past the diagonal inside diagonal blocks, dense-mask zeros
-                    float* xf = reinterpret_cast<float*>(x);
+                    // masked entries -> -inf: absent pieces, columns past the
+                    // diagonal inside diagonal blocks, dense-mask zeros
 #pragma unroll
-                    for (int b = 0; b < G; ++b) {
-                        const int blk = L.step_blk[(s * G + a) * G + b];
+                    for (int p = 0; p < NPH; ++p) {
+                        const int b = (64 * hf + p * CW) / BLK, co = (64 * hf + p * CW) % BLK;
+                        const int blk = pblk[p];
                         const int col = L.step_col[s * G + b];
-                        const int lim = blk < 0 ? -1 : ((args.kind == BSP_MASK_DIAG_CAUSAL && col == rb) ? r_in : BLK);
-                        if (__any_sync(0xffffffffu, lim < BLK - 1)) {
+                        // in-piece column j is kept iff j <= lim
+                        const int lim =
+                            blk < 0 ? -1 : ((args.kind == BSP_MASK_DIAG_CAUSAL && col == rb) ? r_in - co : CW);
+                        if (__any_sync(0xffffffffu, lim < CW - 1)) {
 #pragma unroll
-                            for (int j = 0; j < BLK; ++j) xf[b * BLK + j] = j > lim ? -INFINITY : xf[b * BLK + j];
+                            for (int j = 0; j < CW; ++j) xf[p * CW + j] = j > lim ? -INFINITY : xf[p * CW + j];
                         }
                         if (args.kind == BSP_MASK_DENSE && blk >= 0) {
-                            const uint8_t* mp = args.mask + (int64_t)(gq * 128 + row) * S + (int64_t)col * BLK;
+                            const uint8_t* mp = args.mask + (int64_t)(gq * 128 + row) * S + (int64_t)col * BLK + co;
 #pragma unroll
-                            for (int q = 0; q < BLK / 16; ++q) {
+                            for (int q = 0; q < CW / 16; ++q) {
                                 const uint4 mv = *reinterpret_cast<const uint4*>(mp + q * 16);
                                 const uint8_t* mb = reinterpret_cast<const uint8_t*>(&mv);
 #pragma unroll
                                 for (int k = 0; k < 16; ++k)
-                                    if (!mb[k]) xf[b * BLK + q * 16 + k] = -INFINITY;
+                                    if (!mb[k]) xf[p * CW + q * 16 + k] = -INFINITY;
                             }
                         }
                     }
                     if (!write) {
-                        // first pass: running max and sum
+                        // first pass: this half row's running max and sum; at the
+                        // tile's last step the halves of the row are combined
                         float mx = -INFINITY;
 #pragma unroll
-                        for (int j = 0; j < 128; ++j) mx = fmaxf(mx, xf[j]);
+                        for (int j = 0; j < 64; ++j) mx = fmaxf(mx, xf[j]);
                         const float mn = fmaxf(m, mx * args.c2);
                         if (mn != -INFINITY) {
                             float acc = 0.f;
 #pragma unroll
-                            for (int j = 0; j < 128; ++j) acc += ex2_approx(fmaf(xf[j], args.c2, -mn));
+                            for (int j = 0; j < 64; ++j) acc += ex2_approx(fmaf(xf[j], args.c2, -mn));
                             l = (m == -INFINITY ? 0.f : l * ex2_approx(m - mn)) + acc;
                             m = mn;
                         }
                         if (it == ns - 1) {
-                            msub = m == -INFINITY ? 0.f : m;
-                            inv = l > 0.f ? 1.0f / l : 0.f;
+                            xs[xc & 1][hf][row] = make_float2(m, l);
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&xq[quad]);
+                            ok = mbar_wait(&xq[quad], xc & 1, ab);
+                            if (!__all_sync(0xffffffffu, ok)) goto epi_done;
+                            const float2 o = xs[xc & 1][hf ^ 1][row];
+                            const float mr = fmaxf(m, o.x);
+                            const float lr = mr == -INFINITY ? 0.f
+                                                             : (m == -INFINITY ? 0.f : l * ex2_approx(m - mr)) +
+                                                                   (o.x == -INFINITY ? 0.f : o.y * ex2_approx(o.x - mr));
+                            msub = mr == -INFINITY ? 0.f : mr;
+                            inv = lr > 0.f ? 1.0f / lr : 0.f;
+                            ++xc;
                         }
                         continue;
                     }
 #pragma unroll
-                    for (int j = 0; j < 128; ++j) xf[j] = ex2_approx(fmaf(xf[j], args.c2, -msub)) * inv;
+                    for (int j = 0; j < 64; ++j) xf[j] = ex2_approx(fmaf(xf[j], args.c2, -msub)) * inv;
                 }
 
 #pragma unroll
-                for (int b = 0; b < G; ++b) {
-                    const int blk = L.step_blk[(s * G + a) * G + b];
+                for (int p = 0; p < NPH; ++p) {
+                    const int blk = pblk[p];
                     if (__all_sync(0xffffffffu, blk < 0)) continue;
                     int sblk[32 / RS];
 #pragma unroll
                     for (int sg = 0; sg < 32 / RS; ++sg) sblk[sg] = __shfl_sync(0xffffffffu, blk, sg * RS);
-                    uint8_t* buf = stg + (uses & 1) * C::kBuf;
-                    if (lane == 0) bulk_wait_read<1>();  // the copy from this buffer two uses ago has read it
+                    uint8_t* buf = stg + (uses % NBUF) * C::kBuf;
+                    if (lane == 0) {  // the copy that last read this buffer has read it
+                        if constexpr (NBUF == 2) bulk_wait_read<1>();
+                        else bulk_wait_read<0>();
+                    }
                     __syncwarp();
                     if (blk >= 0) {
                         uint8_t* rbase = buf + seg * kSeg + rin * RBY;
 #pragma unroll
                         for (int j = 0; j < C16; ++j) {
-                            const int o = b * BLK + 8 * j;
-                            const int box = j / (BW / 8), jj = j % (BW / 8);
-                            const int pos = BLK >= 64 ? (jj ^ (rin & 7)) : jj;
-                            *reinterpret_cast<uint4*>(rbase + box * (RS * RBY) + pos * 16) = make_uint4(
+                            const int o = p * CW + 8 * j;
+                            const int pos = CW == 64 ? (j ^ (rin & 7)) : j;
+                            *reinterpret_cast<uint4*>(rbase + pos * 16) = make_uint4(
                                 Pack2<T>::pack(__uint_as_float(x[o]), __uint_as_float(x[o + 1])),
                                 Pack2<T>::pack(__uint_as_float(x[o + 2]), __uint_as_float(x[o + 3])),
                                 Pack2<T>::pack(__uint_as_float(x[o + 4]), __uint_as_float(x[o + 5])),
@@ -437,14 +476,11 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                             if (sblk[sg] < 0) continue;
                             const int r_in0 = (quad * 32 + sg * RS) % BLK;
                             const int64_t orow = ((int64_t)z * L.nnz + sblk[sg]) * BLK + r_in0;
-                            if (BLK >= 64) {
-#pragma unroll
-                                for (int bx = 0; bx < NBX; ++bx)
-                                    tma_store_3d(&tmC, smem_u32(buf + sg * kSeg + bx * (RS * RBY)), bx * BW,
-                                                 (int32_t)orow, 0);
-                            } else {
+                            if (BLK >= 64)
+                                tma_store_3d(&tmC, smem_u32(buf + sg * kSeg), (64 * hf + p * CW) % BLK, (int32_t)orow,
+                                             0);
+                            else
                                 bulk_store(Cp + orow * BLK, smem_u32(buf + sg * kSeg), kSeg);
-                            }
                         }
                         bulk_commit();
                     }
