@@ -84,15 +84,17 @@ template <int KP, int BLK, int MODE>
 struct SddCfg {
     static constexpr int kTile = 128 * 64 * KP * 2;  // 128 rows x K (KP panels of 64)
     static constexpr int AST = MODE == 2 ? 1 : 2;                // query-tile stages
-    // key-tile stages: two in the fused modes at K = 128 (their per-tile
-    // exchange arrays leave no room for a third)
-    static constexpr int BST = (MODE == 2 || (MODE == 1 && KP == 2)) ? 2 : 3;
+    // key-tile stages: three, except in the backward mode (two stages of V
+    // and P); at K = 128 the fused softmax makes room for the third with one
+    // staging buffer per epilogue warp (its per-tile exchange arrays take the
+    // rest)
+    static constexpr int BST = MODE == 2 ? 2 : 3;
     static constexpr int kPT = MODE == 2 ? 32768 : 0;  // P tile of a key-tile stage
     static constexpr int kBStage = kTile + kPT;
     static constexpr int kA = 0;
     static constexpr int kB = AST * kTile;
     static constexpr int kStg = kB + BST * kBStage;  // staging: NBUF buffers per epilogue warp
-    static constexpr int NBUF = MODE == 2 ? 1 : 2;
+    static constexpr int NBUF = (MODE == 2 || (MODE == 1 && KP == 2)) ? 1 : 2;
     static constexpr int kBuf = 32 * (BLK < 64 ? BLK : 64) * 2;  // a warp's 32 rows of one piece
     static constexpr int kAlloc = kStg + 8 * NBUF * kBuf + 1024;
 };
