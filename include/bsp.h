@@ -303,6 +303,16 @@ int bsp_attention(bsp_layout_t layout, int dtype, const void* Q, const void* K, 
                   void* O, int Z, int D, float scale, int mask_kind, const uint8_t* mask,
                   void* stream);
 
+/* bsp_attention that also writes each query row's log-sum-exp of its kept
+ * scaled scores, lse[z][h][r] = ln sum_{c kept} exp(scale q_r . k_c) (the
+ * softmax's normaliser; -inf for rows with nothing kept), for
+ * bsp_attention_backward_lse.  lse: DEVICE float [Z][H][S], 16-byte aligned
+ * (else BSP_ERR_ALIGNMENT), NULL only when Z == 0 (else BSP_ERR_INVALID_ARG).
+ * Every other argument and the output O as for bsp_attention.  The pages
+ * define no such output; it is the forward half of the backward below. */
+int bsp_attention_lse(bsp_layout_t layout, int dtype, const void* Q, const void* K, const void* V, void* O,
+                      float* lse, int Z, int D, float scale, int mask_kind, const uint8_t* mask, void* stream);
+
 /* ---- backward ---------------------------------------------------------- */
 
 /* Backward of bsp_softmax.  Y: the forward's output (0 at masked entries),
@@ -332,6 +342,21 @@ int bsp_softmax_backward(bsp_layout_t layout, int dtype, const void* Y, const vo
 int bsp_attention_backward(bsp_layout_t layout, int dtype, const void* Q, const void* K, const void* V,
                            const void* dO, void* dQ, void* dK, void* dV, int Z, int D, float scale,
                            int mask_kind, const uint8_t* mask, void* P_ws, void* dP_ws, void* stream);
+
+/* Gradients of bsp_attention as bsp_attention_backward, given also the
+ * forward's output O and its rows' log-sum-exp lse (bsp_attention_lse, same
+ * inputs): P = exp(scale Q K^T - lse) on the layout is rebuilt in one pass
+ * (no statistics pass), and rowsum(P .* dP) = rowsum(dO .* O) per row, so
+ * dX = scale P .* (dP - rowsum(dO .* O)) also takes one pass.  O, dO: DEVICE
+ * [Z][H][S][D]; lse: DEVICE float [Z][H][S], 16-byte aligned; the rest as for
+ * bsp_attention_backward.  fp32, and shapes the one-pass tensor-core kernels
+ * do not cover, take bsp_attention_backward's recomputing chain (O and lse
+ * unused).  Not from the pages: the chain rule with the forward's statistics
+ * kept. */
+int bsp_attention_backward_lse(bsp_layout_t layout, int dtype, const void* Q, const void* K, const void* V,
+                               const void* O, const void* dO, const float* lse, void* dQ, void* dK, void* dV,
+                               int Z, int D, float scale, int mask_kind, const uint8_t* mask, void* P_ws,
+                               void* dP_ws, void* stream);
 
 /* Attention on HOST tensors (Q, K, V, O as in bsp_attention, in host memory;
  * pinned memory lets the copies overlap the kernels, pageable memory works

@@ -56,6 +56,7 @@ def _bind(lib):
     lib.oracle_dsd.argtypes = [P, i32, i32, i32, i32, i32, i32, i32, P, P, i64, P, P]
     lib.oracle_dds.argtypes = [P, i32, i32, i32, i32, i32, i32, i32, P, P, i64, P, P]
     lib.oracle_attention.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, dbl, i32, P, i64, P, P]
+    lib.oracle_attention_lse.argtypes = [P, i32, i32, i32, i32, i32, P, P, dbl, i32, P, i64, P, P]
     lib.oracle_softmax_backward.argtypes = [P, i32, i32, i32, i32, P, P, dbl, P]
     lib.oracle_attention_backward.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, P, dbl, i32, P, P, P, P]
     lib.oracle_affine_expand.argtypes = [P, P, i32, i32, P]
@@ -203,6 +204,19 @@ class Oracle:
         self.lib.oracle_attention(_ptr(lay), H, nb, B, Z, D, _ptr(Q), _ptr(K), _ptr(V),
                                   float(scale), int(kind), _ptr(m), ns, _ptr(s), _ptr(out))
         return out.reshape(Z, H, S, D) if sel is None else out
+
+    def attention_lse(self, layout, B, Q, K, scale, kind=MASK_NONE, mask=None, sel=None):
+        """Log-sum-exp of every row's kept scaled scores (-inf for rows with
+        nothing kept).  Q, K [Z, H, S, D].  Returns [Z, H, S] or [len(sel)]."""
+        lay, Q, K = _u8(layout), _f32(Q), _f32(K)
+        m = None if mask is None else _u8(mask)
+        H, nb = lay.shape[0], lay.shape[1]
+        Z, S, D = Q.shape[0], Q.shape[2], Q.shape[3]
+        s, ns = _sel(sel, Z * H * S)
+        out = np.zeros(ns, dtype=np.float64)
+        self.lib.oracle_attention_lse(_ptr(lay), H, nb, B, Z, D, _ptr(Q), _ptr(K), float(scale), int(kind), _ptr(m),
+                                      ns, _ptr(s), _ptr(out))
+        return out.reshape(Z, H, S) if sel is None else out
 
     def softmax_backward(self, layout, B, Y, dY, scale):
         """Softmax backward in the block format: Y (the forward's output) and

@@ -400,6 +400,49 @@ void oracle_attention(const uint8_t* layout, int H, int nb, int B, int Z, int D,
     (void)Z;
 }
 
+/* Log-sum-exp of a row's kept scores, the normaliser of the softmax above
+ * (not in the pages; what a backward needs to rebuild P = exp(x - lse)):
+ *     lse[z,h,r] = log sum_{c in R} exp(scale * q_r . k_c),
+ * -inf when R is empty.  Q, K: [Z][H][S][D]; out [nsel]; unit u as above. */
+void oracle_attention_lse(const uint8_t* layout, int H, int nb, int B, int Z, int D,
+                          const float* Q, const float* K, double scale, int kind,
+                          const uint8_t* mask, int64_t nsel, const int64_t* sel, double* out) {
+    const int64_t S = (int64_t)nb * B;
+    #pragma omp parallel
+    {
+        double* t = (double*)malloc(sizeof(double) * (size_t)S);
+        #pragma omp for schedule(dynamic, 4)
+        for (int64_t s = 0; s < nsel; ++s) {
+            const int64_t u = sel ? sel[s] : s;
+            const int64_t row = u % S, zh = u / S;
+            const int hh = (int)(zh % H);
+            const float* qr = Q + (zh * S + row) * D;
+            double top = -INFINITY;
+            for (int64_t c = 0; c < S; ++c) {
+                const int present = layout[((int64_t)hh * nb + row / B) * nb + c / B];
+                if (!present || !keep(kind, mask, S, B, row, c)) {
+                    t[c] = -INFINITY;  /* not in R */
+                    continue;
+                }
+                const float* kc = K + (zh * S + c) * D;
+                double acc = 0.0;
+                for (int d = 0; d < D; ++d) acc += (double)qr[d] * (double)kc[d];
+                t[c] = acc * scale;
+                top = t[c] > top ? t[c] : top;
+            }
+            if (top == -INFINITY) {  /* R empty */
+                out[s] = -INFINITY;
+                continue;
+            }
+            double total = 0.0;
+            for (int64_t c = 0; c < S; ++c) total += exp(t[c] - top);  /* exp(-inf) = 0 outside R */
+            out[s] = top + log(total);
+        }
+        free(t);
+    }
+    (void)Z;
+}
+
 /* ---------------------------------------------------------------------- */
 /* backward  [next row: dV = P^T dO, dP = dO V^T, softmax backward,        */
 /*            dQ / dK from dS]; the chain rule applied to the definitions  */

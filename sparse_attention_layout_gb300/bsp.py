@@ -62,6 +62,9 @@ def lib():
         L.bsp_attention.argtypes = [P, i32, P, P, P, P, i32, i32, f32, i32, P, P]
         L.bsp_softmax_backward.argtypes = [P, i32, P, P, P, i32, f32, P]
         L.bsp_attention_backward.argtypes = [P, i32, P, P, P, P, P, P, P, i32, i32, f32, i32, P, P, P, P]
+        L.bsp_attention_lse.argtypes = [P, i32, P, P, P, P, P, i32, i32, f32, i32, P, P]
+        L.bsp_attention_backward_lse.argtypes = [P, i32, P, P, P, P, P, P, P, P, P, i32, i32, f32, i32, P, P, P,
+                                                 P]
         L.bsp_layout_groups.argtypes = [P, i32, P, P, P, P, P, P, P]
         L.bsp_layout_softmax_chunks.argtypes = [P, i32, P, P, P, P]
         L.bsp_layout_geometry.argtypes = [P, P, P]
@@ -82,7 +85,8 @@ def lib():
                      "bsp_layout_get_luts", "bsp_layout_tiles", "bsp_sdd", "bsp_dsd", "bsp_dds", "bsp_softmax",
                      "bsp_attention", "bsp_softmax_backward", "bsp_attention_backward", "bsp_layout_groups",
                      "bsp_layout_softmax_chunks",
-                     "bsp_status_check", "bsp_layout_geometry", "bsp_layout_compile_affine", "bsp_attention_host", "bsp_sdd_softmax"):
+                     "bsp_status_check", "bsp_layout_geometry", "bsp_layout_compile_affine", "bsp_attention_host", "bsp_sdd_softmax",
+                     "bsp_attention_lse", "bsp_attention_backward_lse"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -441,20 +445,56 @@ def attention_backward(L: Layout, Q, K, V, dO, scale: float, mask_kind: int = MA
     return dQ, dK, dV
 
 
+def bsp_attention_lse(L: Layout, Q, K, V, O=None, lse=None, scale: float = 1.0, mask_kind: int = MASK_NONE,
+                      mask=None, stream=None):
+    """Fused attention that also returns each row's log-sum-exp of its kept
+    scaled scores: (O [Z, H, S, D], lse fp32 [Z, H, S])."""
+    if O is None:
+        O = torch.empty_like(Q)
+    if lse is None:
+        lse = torch.empty(Q.shape[:3], dtype=torch.float32, device=Q.device)
+    dt = _dtype(Q, K, V, O)
+    if lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 tensor")
+    _check(lib().bsp_attention_lse(L.handle, dt, _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), Q.shape[0],
+                                   Q.shape[3], float(scale), int(mask_kind), _ptr(mask), _stream(stream)),
+           "bsp_attention_lse")
+    return O, lse
+
+
+def attention_backward_lse(L: Layout, Q, K, V, O, dO, lse, scale: float, mask_kind: int = MASK_NONE, mask=None,
+                           stream=None):
+    """(dQ, dK, dV) given the forward's output O and lse (bsp_attention_lse).
+    Allocates the two [Z, nnz, B, B] workspaces the C call takes."""
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    ws = (Q.shape[0], max(L.nnz, 1), L.B, L.B)
+    P_ws = torch.empty(ws, dtype=Q.dtype, device=Q.device) if L.nnz else None
+    dP_ws = torch.empty(ws, dtype=Q.dtype, device=Q.device) if L.nnz else None
+    dt = _dtype(Q, K, V, O, dO, dQ, dK, dV)
+    _check(lib().bsp_attention_backward_lse(L.handle, dt, _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(lse),
+                                            _ptr(dQ), _ptr(dK), _ptr(dV), Q.shape[0], Q.shape[3], float(scale),
+                                            int(mask_kind), _ptr(mask), _ptr(P_ws), _ptr(dP_ws), _stream(stream)),
+           "bsp_attention_backward_lse")
+    return dQ, dK, dV
+
+
 class _BlockSparseAttention(torch.autograd.Function):
-    """Fused forward (bsp_attention); backward through bsp_attention_backward."""
+    """Fused forward keeping the rows' log-sum-exp (bsp_attention_lse);
+    backward through bsp_attention_backward_lse."""
 
     @staticmethod
     def forward(ctx, Q, K, V, L, scale, mask_kind, mask):
         Q, K, V = Q.contiguous(), K.contiguous(), V.contiguous()
-        ctx.save_for_backward(Q, K, V)
+        O, lse = bsp_attention_lse(L, Q, K, V, None, None, scale, mask_kind, mask)
+        ctx.save_for_backward(Q, K, V, O, lse)
         ctx.L, ctx.scale, ctx.mask_kind, ctx.mask = L, scale, mask_kind, mask
-        return bsp_attention(L, Q, K, V, None, scale, mask_kind, mask)
+        return O
 
     @staticmethod
     def backward(ctx, dO):
-        Q, K, V = ctx.saved_tensors
-        dQ, dK, dV = attention_backward(ctx.L, Q, K, V, dO.contiguous(), ctx.scale, ctx.mask_kind, ctx.mask)
+        Q, K, V, O, lse = ctx.saved_tensors
+        dQ, dK, dV = attention_backward_lse(ctx.L, Q, K, V, O, dO.contiguous(), lse, ctx.scale, ctx.mask_kind,
+                                            ctx.mask)
         return dQ, dK, dV, None, None, None, None
 
 

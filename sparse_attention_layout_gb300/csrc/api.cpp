@@ -133,9 +133,9 @@ extern "C" int bsp_softmax(bsp_layout_t L, int dtype, const void* X, void* Y, in
                                mask_kind == BSP_MASK_DENSE ? mask : nullptr, (cudaStream_t)stream);
 }
 
-extern "C" int bsp_attention(bsp_layout_t L, int dtype, const void* Q, const void* K, const void* V,
-                             void* O, int Z, int D, float scale, int mask_kind, const uint8_t* mask,
-                             void* stream) {
+namespace {
+int attention_impl(bsp_layout_t L, int dtype, const void* Q, const void* K, const void* V, void* O, float* lse,
+                   int Z, int D, float scale, int mask_kind, const uint8_t* mask, void* stream) {
     int rc = check_common(L, dtype, Z, {Q, K, V, O});
     if (rc) return rc;
     if (Z < 0 || D < 16 || D > 128 || D % 16 || !valid_kind(mask_kind) || !(scale > 0.f) ||
@@ -147,10 +147,25 @@ extern "C" int bsp_attention(bsp_layout_t L, int dtype, const void* Q, const voi
     cudaStream_t s = (cudaStream_t)stream;
     const uint8_t* m = mask_kind == BSP_MASK_DENSE ? mask : nullptr;
     if (!force_simt()) {
-        rc = bsp::launch_attention_tc(L, dtype, Q, K, V, O, Z, D, scale, mask_kind, m, s);
+        rc = bsp::launch_attention_tc(L, dtype, Q, K, V, O, lse, Z, D, scale, mask_kind, m, s);
         if (rc != BSP_ERR_UNSUPPORTED) return rc;
     }
-    return bsp::launch_attention_simt(L, dtype, Q, K, V, O, Z, D, scale, mask_kind, m, s);
+    return bsp::launch_attention_simt(L, dtype, Q, K, V, O, lse, Z, D, scale, mask_kind, m, s);
+}
+}  // namespace
+
+extern "C" int bsp_attention(bsp_layout_t L, int dtype, const void* Q, const void* K, const void* V,
+                             void* O, int Z, int D, float scale, int mask_kind, const uint8_t* mask,
+                             void* stream) {
+    return attention_impl(L, dtype, Q, K, V, O, nullptr, Z, D, scale, mask_kind, mask, stream);
+}
+
+extern "C" int bsp_attention_lse(bsp_layout_t L, int dtype, const void* Q, const void* K, const void* V, void* O,
+                                 float* lse, int Z, int D, float scale, int mask_kind, const uint8_t* mask,
+                                 void* stream) {
+    if (Z > 0 && !lse) return BSP_ERR_INVALID_ARG;
+    if (!aligned16(lse)) return BSP_ERR_ALIGNMENT;
+    return attention_impl(L, dtype, Q, K, V, O, lse, Z, D, scale, mask_kind, mask, stream);
 }
 
 extern "C" int bsp_status_check(bsp_layout_t L, void* stream) {
@@ -231,6 +246,46 @@ extern "C" int bsp_attention_backward(bsp_layout_t L, int dtype, const void* Q, 
     // and the softmax backward in place
     rc = force_simt() ? BSP_ERR_UNSUPPORTED
                       : bsp::launch_sdd_softmax_bwd_tc(L, dtype, dO, V, P_ws, dP_ws, Z, D, scale, s);
+    if (rc == BSP_ERR_UNSUPPORTED) {
+        if ((rc = bsp_sdd(L, dtype, dO, V, dP_ws, Z, D, 0, 1, stream))) return rc;
+        rc = bsp_softmax_backward(L, dtype, P_ws, dP_ws, dP_ws, Z, scale, stream);
+    }
+    if (rc) return rc;
+    // dQ = dX K,  dK = dX^T Q
+    if ((rc = bsp_dsd(L, dtype, dP_ws, K, dQ, Z, D, 0, 0, stream))) return rc;
+    return bsp_dsd(L, dtype, dP_ws, Q, dK, Z, D, 1, 0, stream);
+}
+
+extern "C" int bsp_attention_backward_lse(bsp_layout_t L, int dtype, const void* Q, const void* K, const void* V,
+                                          const void* O, const void* dO, const float* lse, void* dQ, void* dK,
+                                          void* dV, int Z, int D, float scale, int mask_kind, const uint8_t* mask,
+                                          void* P_ws, void* dP_ws, void* stream) {
+    int rc = check_common(L, dtype, Z, {Q, K, V, O, dO, dQ, dK, dV});
+    if (rc) return rc;
+    if (D < 16 || D > 128 || D % 16 || !valid_kind(mask_kind) || !(scale > 0.f) || scale > 3.0e38f)
+        return BSP_ERR_INVALID_ARG;
+    if (mask_kind == BSP_MASK_DENSE && !mask) return BSP_ERR_INVALID_ARG;
+    if (mask_kind == BSP_MASK_DENSE && ((uintptr_t)mask & 15u)) return BSP_ERR_ALIGNMENT;
+    if (Z > 0 && (!lse || !O)) return BSP_ERR_INVALID_ARG;
+    if (!aligned16(lse)) return BSP_ERR_ALIGNMENT;
+    if (Z == 0 || L->nnz == 0 || dtype == BSP_F32 || force_simt())  // the chain recomputes what it needs
+        return bsp_attention_backward(L, dtype, Q, K, V, dO, dQ, dK, dV, Z, D, scale, mask_kind, mask, P_ws, dP_ws,
+                                      stream);
+    if (!P_ws || !dP_ws) return BSP_ERR_INVALID_ARG;
+    if (!aligned16(P_ws) || !aligned16(dP_ws)) return BSP_ERR_ALIGNMENT;
+    cudaStream_t s = (cudaStream_t)stream;
+    const uint8_t* m = mask_kind == BSP_MASK_DENSE ? mask : nullptr;
+    // P = exp(scale Q K^T - lse) on the layout: one pass
+    rc = bsp::launch_sdd_softmax_lse_tc(L, dtype, Q, K, lse, P_ws, Z, D, scale, mask_kind, m, s);
+    if (rc == BSP_ERR_UNSUPPORTED)
+        return bsp_attention_backward(L, dtype, Q, K, V, dO, dQ, dK, dV, Z, D, scale, mask_kind, mask, P_ws, dP_ws,
+                                      stream);
+    if (rc) return rc;
+    // dV = P^T dO
+    if ((rc = bsp_dsd(L, dtype, P_ws, dO, dV, Z, D, 1, 0, stream))) return rc;
+    // dX = scale P .* (dP - rowsum(dO .* O)), dP = dO V^T: one pass (blocks of
+    // 64 and 128), else dP through memory and the softmax backward in place
+    rc = bsp::launch_sdd_softmax_bwd_o_tc(L, dtype, dO, V, P_ws, O, dP_ws, Z, D, scale, s);
     if (rc == BSP_ERR_UNSUPPORTED) {
         if ((rc = bsp_sdd(L, dtype, dO, V, dP_ws, Z, D, 0, 1, stream))) return rc;
         rc = bsp_softmax_backward(L, dtype, P_ws, dP_ws, dP_ws, Z, scale, stream);

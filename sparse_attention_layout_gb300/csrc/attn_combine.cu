@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "bsp_internal.h"
+#include "common.cuh"
 
 namespace bsp {
 namespace {
@@ -33,8 +34,8 @@ __device__ __forceinline__ void store4(__half* o, float4 v) {
 
 template <typename T>
 __global__ void __launch_bounds__(kCombineThreads)
-attn_combine_kernel(const int4* __restrict__ comb, const float* __restrict__ ws, T* __restrict__ O, int H, int S,
-                    int D, int ngroups) {
+attn_combine_kernel(const int4* __restrict__ comb, const float* __restrict__ ws, T* __restrict__ O,
+                    float* __restrict__ lse, int H, int S, int D, int ngroups) {
     const int4 c = comb[blockIdx.x];  // tile, batch entry, first slot, pieces
     const int tile = c.x, z = c.y, slot0 = c.z, np = c.w;
     const int h = tile / ngroups, gq = tile % ngroups;
@@ -62,6 +63,8 @@ attn_combine_kernel(const int4* __restrict__ comb, const float* __restrict__ ws,
             }
         }
         const float inv = Ls > 0.f ? 1.0f / Ls : 0.f;
+        // the row's log-sum-exp (natural log) from the merged statistics
+        if (lse && d0 == 0) lse[((int64_t)z * H + h) * S + rseq] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
         acc.x *= inv;
         acc.y *= inv;
         acc.z *= inv;
@@ -83,17 +86,17 @@ bool capturing(cudaStream_t s) {
 
 }  // namespace
 
-int launch_attention_combine(const bsp_layout_s* L, int dtype, const AttnSchedule& sc, void* O, int D,
+int launch_attention_combine(const bsp_layout_s* L, int dtype, const AttnSchedule& sc, void* O, float* lse, int D,
                              cudaStream_t s) {
     if (sc.n_split == 0) return BSP_OK;
     if (D % 4 != 0 || D > kPartMaxD || kCombineThreads % (D / 4) != 0) return BSP_ERR_UNSUPPORTED;
     const dim3 grid(sc.n_split), block(kCombineThreads);
     if (dtype == BSP_BF16)
-        attn_combine_kernel<<<grid, block, 0, s>>>(sc.combine, sc.ws, (__nv_bfloat16*)O, L->H, L->S, D, L->ngroups);
+        attn_combine_kernel<<<grid, block, 0, s>>>(sc.combine, sc.ws, (__nv_bfloat16*)O, lse, L->H, L->S, D, L->ngroups);
     else if (dtype == BSP_F16)
-        attn_combine_kernel<<<grid, block, 0, s>>>(sc.combine, sc.ws, (__half*)O, L->H, L->S, D, L->ngroups);
+        attn_combine_kernel<<<grid, block, 0, s>>>(sc.combine, sc.ws, (__half*)O, lse, L->H, L->S, D, L->ngroups);
     else
-        attn_combine_kernel<<<grid, block, 0, s>>>(sc.combine, sc.ws, (float*)O, L->H, L->S, D, L->ngroups);
+        attn_combine_kernel<<<grid, block, 0, s>>>(sc.combine, sc.ws, (float*)O, lse, L->H, L->S, D, L->ngroups);
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }
 
@@ -112,10 +115,10 @@ int attn_schedule_begin(bsp_layout_s* L, int dtype, int Z, cudaStream_t s, AttnS
     return BSP_OK;
 }
 
-int attn_schedule_end(const bsp_layout_s* L, int dtype, const AttnSchedule& sc, void* O, int D, cudaStream_t s,
-                      int rc) {
+int attn_schedule_end(const bsp_layout_s* L, int dtype, const AttnSchedule& sc, void* O, float* lse, int D,
+                      cudaStream_t s, int rc) {
     if (sc.n_split == 0) return rc;
-    if (rc == BSP_OK) rc = launch_attention_combine(L, dtype, sc, O, D, s);
+    if (rc == BSP_OK) rc = launch_attention_combine(L, dtype, sc, O, lse, D, s);
     if (rc == BSP_OK && !capturing(s) && cudaEventRecord(sc.done, s) != cudaSuccess) {
         cudaGetLastError();
         rc = BSP_ERR_CUDA;

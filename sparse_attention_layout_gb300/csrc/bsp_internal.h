@@ -135,13 +135,13 @@ int launch_dsd_simt(const bsp_layout_s* L, int dtype, const void* A, const void*
 int launch_dds_simt(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z,
                     int M, int ta, int tb, cudaStream_t s);
 int launch_attention_simt(const bsp_layout_s* L, int dtype, const void* Q, const void* K,
-                          const void* V, void* O, int Z, int D, float scale, int kind,
+                          const void* V, void* O, float* lse, int Z, int D, float scale, int kind,
                           const uint8_t* mask, cudaStream_t s);
 
 // tensor-core (tcgen05) paths; return BSP_ERR_UNSUPPORTED when the shape is
 // not covered so that the caller can take the SIMT path instead
 int launch_attention_tc(const bsp_layout_s* L, int dtype, const void* Q, const void* K,
-                        const void* V, void* O, int Z, int D, float scale, int kind,
+                        const void* V, void* O, float* lse, int Z, int D, float scale, int kind,
                         const uint8_t* mask, cudaStream_t s);
 int launch_sdd_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z,
                   int K, int ta, int tb, cudaStream_t s);
@@ -152,6 +152,14 @@ int launch_sdd_softmax_tc(const bsp_layout_s* L, int dtype, const void* A, const
 // (fused SDD + softmax backward; 16-bit types, tensor-core shapes only)
 int launch_sdd_softmax_bwd_tc(const bsp_layout_s* L, int dtype, const void* dO, const void* V, const void* P,
                               void* dX, int Z, int D, float scale, cudaStream_t s);
+// P = exp(scale Q K^T - lse) on the layout and mask, from the rows'
+// log-sum-exp of the forward (one pass; 16-bit types, tensor-core shapes)
+int launch_sdd_softmax_lse_tc(const bsp_layout_s* L, int dtype, const void* Q, const void* K, const float* lse,
+                              void* P, int Z, int D, float scale, int kind, const uint8_t* mask, cudaStream_t s);
+// dX as launch_sdd_softmax_bwd_tc with rowsum(P .* dP) = rowsum(dO .* O) from
+// the forward's output O (one pass)
+int launch_sdd_softmax_bwd_o_tc(const bsp_layout_s* L, int dtype, const void* dO, const void* V, const void* P,
+                                const void* O, void* dX, int Z, int D, float scale, cudaStream_t s);
 int launch_dsd_group_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z,
                         int N, int ta, int tb, cudaStream_t s);
 int launch_dds_group_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z,
@@ -204,15 +212,15 @@ inline int attn_force_cap(int dtype) { return dtype == BSP_F32 ? kF32MaxSteps : 
 int tile_schedule(bsp_layout_s* L, int Z, int sms, int force_cap, AttnSchedule* out);
 void schedules_destroy(bsp_layout_s* L);
 // O rows of the cut tiles from their pieces' partial results (attn_combine.cu)
-int launch_attention_combine(const bsp_layout_s* L, int dtype, const AttnSchedule& sc, void* O, int D,
+int launch_attention_combine(const bsp_layout_s* L, int dtype, const AttnSchedule& sc, void* O, float* lse, int D,
                              cudaStream_t s);
 // Around one persistent attention launch on stream s: begin fetches the
 // schedule and, when it cuts tiles, takes the workspace (lock, and a wait for
 // the workspace's previous launch); end (called whenever begin succeeded, with
 // the launch's status rc) merges the cut tiles and releases the workspace.
 int attn_schedule_begin(bsp_layout_s* L, int dtype, int Z, cudaStream_t s, AttnSchedule* sc);
-int attn_schedule_end(const bsp_layout_s* L, int dtype, const AttnSchedule& sc, void* O, int D, cudaStream_t s,
-                      int rc);
+int attn_schedule_end(const bsp_layout_s* L, int dtype, const AttnSchedule& sc, void* O, float* lse, int D,
+                      cudaStream_t s, int rc);
 
 // affine geometry (geometry.cpp)
 int affine_validate(int nb, int n, const bsp_affine_term_t* t);

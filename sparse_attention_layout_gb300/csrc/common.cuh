@@ -45,5 +45,6 @@ __device__ __forceinline__ void set_status(int* status, int code) {
 }
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 }  // namespace bsp

@@ -257,7 +257,7 @@ dds_simt_kernel(LayoutView L, const T* __restrict__ Ad, const T* __restrict__ Bs
 template <typename T, int TR>
 __global__ void __launch_bounds__(kThreads)
 attention_simt_kernel(LayoutView L, const T* __restrict__ Q, const T* __restrict__ K,
-                      const T* __restrict__ V, T* __restrict__ O, int Z, int D, float c2,
+                      const T* __restrict__ V, T* __restrict__ O, float* __restrict__ lse, int Z, int D, float c2,
                       int kind, const uint8_t* __restrict__ mask) {
     constexpr int R = TR / 16;
     constexpr int DMAX = 128;
@@ -385,6 +385,9 @@ attention_simt_kernel(LayoutView L, const T* __restrict__ Q, const T* __restrict
         for (int u = 0; u < R; ++u) {
             const float inv = l[u] > 0.f ? 1.0f / l[u] : 0.f;
             const int64_t r = r0 + ty + 16 * u;
+            // the row's log-sum-exp of the scaled scores (natural log; -inf when
+            // nothing is kept): m is in scaled log2 units
+            if (lse && tx == 0) lse[zh * S + r] = l[u] > 0.f ? (m[u] + log2f(l[u])) * kLn2 : -INFINITY;
 #pragma unroll
             for (int d = 0; d < DR; ++d) {
                 const int dd = tx + 16 * d;
@@ -464,7 +467,8 @@ int dds_t(const bsp_layout_s* L, const void* A, const void* B, void* C, int Z, i
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 2)
 attention_simt_v4_kernel(LayoutView L, const T* __restrict__ Q, const T* __restrict__ K,
-                         const T* __restrict__ V, T* __restrict__ O, int Z, float c2, int kind,
+                         const T* __restrict__ V, T* __restrict__ O, float* __restrict__ lse, int Z, float c2,
+                         int kind,
                          const uint8_t* __restrict__ mask) {
     constexpr int TR = 64, R = 4, DP = D + 4, PP = TR + 4, NG = D / 64, D4 = D / 4;
     // fp32 inputs: K and V chunks arrive by asynchronous 16-byte copies into two
@@ -650,6 +654,7 @@ attention_simt_v4_kernel(LayoutView L, const T* __restrict__ Q, const T* __restr
         for (int u = 0; u < R; ++u) {
             const float inv = l[u] > 0.f ? 1.0f / l[u] : 0.f;
             const int64_t r = r0 + ty + 16 * u;
+            if (lse && tx == 0) lse[zh * S + r] = l[u] > 0.f ? (m[u] + log2f(l[u])) * kLn2 : -INFINITY;
 #pragma unroll
             for (int g = 0; g < NG; ++g) {
                 T* dst = O + (zh * S + r) * D + 64 * g + 4 * tx;
@@ -664,7 +669,7 @@ attention_simt_v4_kernel(LayoutView L, const T* __restrict__ Q, const T* __restr
 }
 
 template <typename T, int D>
-int attn_v4(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, int Z, float scale,
+int attn_v4(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, float* lse, int Z, float scale,
             int kind, const uint8_t* mask, cudaStream_t s) {
     const int64_t total = (int64_t)L->H * L->nb * Z * (L->B / 64);
     if (total == 0) return BSP_OK;
@@ -673,13 +678,13 @@ int attn_v4(const bsp_layout_s* L, const void* Q, const void* K, const void* V, 
     auto kern = attention_simt_v4_kernel<T, D>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return BSP_ERR_CUDA;
-    kern<<<grid_for(total), kThreads, smem, s>>>(L->view, (const T*)Q, (const T*)K, (const T*)V, (T*)O, Z,
+    kern<<<grid_for(total), kThreads, smem, s>>>(L->view, (const T*)Q, (const T*)K, (const T*)V, (T*)O, lse, Z,
                                                   scale * kLog2e, kind, mask);
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }
 
 template <typename T, int TR>
-int attn_tr(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, int Z,
+int attn_tr(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, float* lse, int Z,
             int D, float scale, int kind, const uint8_t* mask, cudaStream_t s) {
     const int64_t total = (int64_t)L->H * L->nb * Z * (L->B / TR);
     if (total == 0) return BSP_OK;
@@ -688,19 +693,19 @@ int attn_tr(const bsp_layout_s* L, const void* Q, const void* K, const void* V, 
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return BSP_ERR_CUDA;
     kern<<<grid_for(total), kThreads, smem, s>>>(L->view, (const T*)Q, (const T*)K, (const T*)V,
-                                                  (T*)O, Z, D, scale * kLog2e, kind, mask);
+                                                  (T*)O, lse, Z, D, scale * kLog2e, kind, mask);
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }
 
 template <typename T>
-int attn_t(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, int Z, int D,
+int attn_t(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, float* lse, int Z, int D,
            float scale, int kind, const uint8_t* mask, cudaStream_t s) {
-    if (L->B >= 64 && D == 64) return attn_v4<T, 64>(L, Q, K, V, O, Z, scale, kind, mask, s);
-    if (L->B >= 64 && D == 128) return attn_v4<T, 128>(L, Q, K, V, O, Z, scale, kind, mask, s);
+    if (L->B >= 64 && D == 64) return attn_v4<T, 64>(L, Q, K, V, O, lse, Z, scale, kind, mask, s);
+    if (L->B >= 64 && D == 128) return attn_v4<T, 128>(L, Q, K, V, O, lse, Z, scale, kind, mask, s);
     switch (L->B) {
-        case 16: return attn_tr<T, 16>(L, Q, K, V, O, Z, D, scale, kind, mask, s);
-        case 32: return attn_tr<T, 32>(L, Q, K, V, O, Z, D, scale, kind, mask, s);
-        default: return attn_tr<T, 64>(L, Q, K, V, O, Z, D, scale, kind, mask, s);
+        case 16: return attn_tr<T, 16>(L, Q, K, V, O, lse, Z, D, scale, kind, mask, s);
+        case 32: return attn_tr<T, 32>(L, Q, K, V, O, lse, Z, D, scale, kind, mask, s);
+        default: return attn_tr<T, 64>(L, Q, K, V, O, lse, Z, D, scale, kind, mask, s);
     }
 }
 
@@ -727,9 +732,9 @@ int launch_dds_simt(const bsp_layout_s* L, int dtype, const void* A, const void*
     BSP_DISPATCH(dds_t, L, A, B, C, Z, M, ta, tb, s)
 }
 int launch_attention_simt(const bsp_layout_s* L, int dtype, const void* Q, const void* K,
-                          const void* V, void* O, int Z, int D, float scale, int kind,
+                          const void* V, void* O, float* lse, int Z, int D, float scale, int kind,
                           const uint8_t* mask, cudaStream_t s) {
-    BSP_DISPATCH(attn_t, L, Q, K, V, O, Z, D, scale, kind, mask, s)
+    BSP_DISPATCH(attn_t, L, Q, K, V, O, lse, Z, D, scale, kind, mask, s)
 }
 
 }  // namespace bsp

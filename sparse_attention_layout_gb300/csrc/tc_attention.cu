@@ -7,14 +7,14 @@
 namespace bsp {
 
 #define BSP_ATTN_LAUNCHER(name)                                                                                   \
-    int name(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, int Z, int D, float scale, \
+    int name(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, float* lse, int Z, int D, float scale, \
              int kind, const uint8_t* mask, cudaStream_t s);
 BSP_ATTN_LAUNCHER(launch_attention_tc_bf16)
 BSP_ATTN_LAUNCHER(launch_attention_tc_f16)
 BSP_ATTN_LAUNCHER(launch_attention_tc_bf16_geo)
 BSP_ATTN_LAUNCHER(launch_attention_tc_f16_geo)
 #undef BSP_ATTN_LAUNCHER
-int launch_attention_tc_tf32(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, int Z,
+int launch_attention_tc_tf32(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, float* lse, int Z,
                              int D, float scale, int kind, const uint8_t* mask, cudaStream_t s);
 
 namespace {
@@ -29,15 +29,15 @@ bool geometry_on() {
 }  // namespace
 
 int launch_attention_tc(const bsp_layout_s* L, int dtype, const void* Q, const void* K, const void* V, void* O,
-                        int Z, int D, float scale, int kind, const uint8_t* mask, cudaStream_t s) {
+                        float* lse, int Z, int D, float scale, int kind, const uint8_t* mask, cudaStream_t s) {
     if ((uint64_t)Z * L->H * L->S >= (1ull << 31)) return BSP_ERR_UNSUPPORTED;  // TMA coordinates are int32
     const bool geo = L->view.geo != nullptr && geometry_on();
     if (dtype == BSP_BF16)
-        return (geo ? launch_attention_tc_bf16_geo : launch_attention_tc_bf16)(L, Q, K, V, O, Z, D, scale, kind, mask, s);
+        return (geo ? launch_attention_tc_bf16_geo : launch_attention_tc_bf16)(L, Q, K, V, O, lse, Z, D, scale, kind, mask, s);
     if (dtype == BSP_F16)
-        return (geo ? launch_attention_tc_f16_geo : launch_attention_tc_f16)(L, Q, K, V, O, Z, D, scale, kind, mask, s);
+        return (geo ? launch_attention_tc_f16_geo : launch_attention_tc_f16)(L, Q, K, V, O, lse, Z, D, scale, kind, mask, s);
     // fp32: the three-term tf32 split on the tensor cores (head size 64)
-    if (dtype == BSP_F32) return launch_attention_tc_tf32(L, Q, K, V, O, Z, D, scale, kind, mask, s);
+    if (dtype == BSP_F32) return launch_attention_tc_tf32(L, Q, K, V, O, lse, Z, D, scale, kind, mask, s);
     return BSP_ERR_UNSUPPORTED;
 }
 

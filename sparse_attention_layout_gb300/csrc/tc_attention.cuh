@@ -105,6 +105,7 @@ struct AttnArgs {
     // a piece leaves its rows' raw O, running max and sum in part_ws
     const int32_t* sched_part;
     float* part_ws;
+    float* lse;  // the rows' log-sum-exp of the scaled scores [Z][H][S] (natural log), or null
     int Z;
     int kind;
     float c2;  // scale * log2(e)
@@ -393,6 +394,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 if (!__all_sync(0xffffffffu, ok)) goto epilogue_done;
                 tc_fence_after();
             }
+            if (args.lse && part < 0 && y0 + lane < S)  // cut tiles: the combine pass writes it
+                args.lse[(int64_t)zh * S + y0 + lane] = lt > 0.f ? (mf + log2f(lt)) * kLn2 : -INFINITY;
             if (part >= 0) {
                 // a piece of a cut tile: the row's O as accumulated (relative
                 // to its reference max mf), mf and the sum, for the combine
@@ -748,7 +751,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
 }
 
 template <typename T, int BLK, int D, int KIND, bool GEO>
-int launch_attn(const bsp_layout_s* Lh, const void* Q, const void* K, const void* V, void* O, int Z,
+int launch_attn(const bsp_layout_s* Lh, const void* Q, const void* K, const void* V, void* O, float* lse, int Z,
                 float scale, int kind, const uint8_t* mask, cudaStream_t s) {
     const int is_bf16 = std::is_same<T, __nv_bfloat16>::value;
     const uint64_t rows = (uint64_t)Z * Lh->H * Lh->S;
@@ -769,42 +772,42 @@ int launch_attn(const bsp_layout_s* Lh, const void* Q, const void* K, const void
     if ((uint32_t)fa.numRegs != kRegsLaunch) return BSP_ERR_UNSUPPORTED;
     AttnSchedule sc;
     if ((rc = attn_schedule_begin(const_cast<bsp_layout_s*>(Lh), is_bf16 ? BSP_BF16 : BSP_F16, Z, s, &sc))) return rc;
-    AttnArgs args{Lh->view, O, mask, sc.ptr, sc.items, sc.part, sc.ws, Z, kind, scale * kLog2e};
+    AttnArgs args{Lh->view, O, mask, sc.ptr, sc.items, sc.part, sc.ws, lse, Z, kind, scale * kLog2e};
     if (sc.grid > 0) {
         kern<<<sc.grid, kThreads, smem, s>>>(mq, mk, mv, mo, args);
         rc = cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
     }
-    return attn_schedule_end(Lh, is_bf16 ? BSP_BF16 : BSP_F16, sc, O, D, s, rc);
+    return attn_schedule_end(Lh, is_bf16 ? BSP_BF16 : BSP_F16, sc, O, lse, D, s, rc);
 }
 
 template <typename T, int BLK, int KIND, bool GEO>
-int by_d(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, int Z, int D, float scale,
+int by_d(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, float* lse, int Z, int D, float scale,
          int kind, const uint8_t* mask, cudaStream_t s) {
-    if (D == 128) return launch_attn<T, BLK, 128, KIND, GEO>(L, Q, K, V, O, Z, scale, kind, mask, s);
-    if (D == 64) return launch_attn<T, BLK, 64, KIND, GEO>(L, Q, K, V, O, Z, scale, kind, mask, s);
+    if (D == 128) return launch_attn<T, BLK, 128, KIND, GEO>(L, Q, K, V, O, lse, Z, scale, kind, mask, s);
+    if (D == 64) return launch_attn<T, BLK, 64, KIND, GEO>(L, Q, K, V, O, lse, Z, scale, kind, mask, s);
     return BSP_ERR_UNSUPPORTED;
 }
 
 template <typename T, int BLK, bool GEO>
-int by_kind(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, int Z, int D,
+int by_kind(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, float* lse, int Z, int D,
             float scale, int kind, const uint8_t* mask, cudaStream_t s) {
     switch (kind) {
-        case BSP_MASK_NONE: return by_d<T, BLK, BSP_MASK_NONE, GEO>(L, Q, K, V, O, Z, D, scale, kind, mask, s);
-        case BSP_MASK_DENSE: return by_d<T, BLK, BSP_MASK_DENSE, GEO>(L, Q, K, V, O, Z, D, scale, kind, mask, s);
+        case BSP_MASK_NONE: return by_d<T, BLK, BSP_MASK_NONE, GEO>(L, Q, K, V, O, lse, Z, D, scale, kind, mask, s);
+        case BSP_MASK_DENSE: return by_d<T, BLK, BSP_MASK_DENSE, GEO>(L, Q, K, V, O, lse, Z, D, scale, kind, mask, s);
         case BSP_MASK_DIAG_CAUSAL:
-            return by_d<T, BLK, BSP_MASK_DIAG_CAUSAL, GEO>(L, Q, K, V, O, Z, D, scale, kind, mask, s);
+            return by_d<T, BLK, BSP_MASK_DIAG_CAUSAL, GEO>(L, Q, K, V, O, lse, Z, D, scale, kind, mask, s);
         default: return BSP_ERR_INVALID_ARG;
     }
 }
 
 template <typename T, bool GEO>
-int by_block(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, int Z, int D,
+int by_block(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, float* lse, int Z, int D,
              float scale, int kind, const uint8_t* mask, cudaStream_t s) {
     switch (L->B) {
-        case 128: return by_kind<T, 128, GEO>(L, Q, K, V, O, Z, D, scale, kind, mask, s);
-        case 64: return by_kind<T, 64, GEO>(L, Q, K, V, O, Z, D, scale, kind, mask, s);
-        case 32: return by_kind<T, 32, GEO>(L, Q, K, V, O, Z, D, scale, kind, mask, s);
-        case 16: return by_kind<T, 16, GEO>(L, Q, K, V, O, Z, D, scale, kind, mask, s);
+        case 128: return by_kind<T, 128, GEO>(L, Q, K, V, O, lse, Z, D, scale, kind, mask, s);
+        case 64: return by_kind<T, 64, GEO>(L, Q, K, V, O, lse, Z, D, scale, kind, mask, s);
+        case 32: return by_kind<T, 32, GEO>(L, Q, K, V, O, lse, Z, D, scale, kind, mask, s);
+        case 16: return by_kind<T, 16, GEO>(L, Q, K, V, O, lse, Z, D, scale, kind, mask, s);
         default: return BSP_ERR_UNSUPPORTED;
     }
 }

@@ -4,9 +4,9 @@
 
 namespace bsp {
 
-int launch_attention_tc_f16_geo(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O,
+int launch_attention_tc_f16_geo(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, float* lse,
                               int Z, int D, float scale, int kind, const uint8_t* mask, cudaStream_t s) {
-    return attn::by_block<__half, true>(L, Q, K, V, O, Z, D, scale, kind, mask, s);
+    return attn::by_block<__half, true>(L, Q, K, V, O, lse, Z, D, scale, kind, mask, s);
 }
 
 }  // namespace bsp

@@ -77,6 +77,7 @@ struct Attn32Args {
     // a piece leaves its rows' raw O, running max and sum in part_ws
     const int32_t* sched_part;
     float* part_ws;
+    float* lse;  // the rows' log-sum-exp of the scaled scores [Z][H][S] (natural log), or null
     int Z;
     float c2;  // scale * log2(e)
 };
@@ -429,6 +430,7 @@ attention_tf32_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
             const int rseq = gq * 128 + row;  // query position inside the sequence
             float* orow = args.O + (((int64_t)z * L.H + h) * S + rseq) * D + 32 * hf;
             if (ns == 0) {  // nothing kept anywhere in the tile: rows of zeros
+                if (args.lse && hf == 0 && rseq < S) args.lse[((int64_t)z * L.H + h) * S + rseq] = -INFINITY;
                 if (rseq < S)
 #pragma unroll
                     for (int k = 0; k < 8; ++k) reinterpret_cast<float4*>(orow)[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -539,6 +541,8 @@ attention_tf32_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&o_empty);
                 const int part = args.sched_part[it];
+                if (args.lse && part < 0 && hf == 0 && rseq < S)  // cut tiles: the combine pass writes it
+                    args.lse[((int64_t)z * L.H + h) * S + rseq] = lt > 0.f ? (m + log2f(lt)) * kLn2 : -INFINITY;
                 if (part >= 0) {
                     // a piece of a cut tile: O as accumulated (relative to the
                     // common reference m), m and the sum, for the combine pass
@@ -584,7 +588,7 @@ attention_tf32_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
 }
 
 template <int BLK, int KIND>
-int launch32(const bsp_layout_s* Lh, const void* Q, const void* K, const void* V, void* O, int Z, float scale,
+int launch32(const bsp_layout_s* Lh, const void* Q, const void* K, const void* V, void* O, float* lse, int Z, float scale,
              const uint8_t* mask, cudaStream_t s) {
     const uint64_t rows = (uint64_t)Z * Lh->H * Lh->S;
     constexpr uint32_t R = BLK < 64 ? BLK : 64;
@@ -602,35 +606,36 @@ int launch32(const bsp_layout_s* Lh, const void* Q, const void* K, const void* V
     if ((uint32_t)fa.numRegs != kRegsLaunch) return BSP_ERR_UNSUPPORTED;
     AttnSchedule sc;
     if ((rc = attn_schedule_begin(const_cast<bsp_layout_s*>(Lh), BSP_F32, Z, s, &sc))) return rc;
-    Attn32Args args{Lh->view, (const float*)V, (float*)O, mask, sc.ptr, sc.items, sc.part, sc.ws, Z, scale * kLog2e};
+    Attn32Args args{Lh->view, (const float*)V, (float*)O, mask, sc.ptr, sc.items, sc.part, sc.ws, lse, Z,
+                    scale * kLog2e};
     if (sc.grid > 0) {
         kern<<<sc.grid, kThreads, smem, s>>>(mq, mk, args);
         rc = cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
     }
-    return attn_schedule_end(Lh, BSP_F32, sc, O, D, s, rc);
+    return attn_schedule_end(Lh, BSP_F32, sc, O, lse, D, s, rc);
 }
 
 template <int BLK>
-int by_kind32(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, int Z, float scale,
+int by_kind32(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, float* lse, int Z, float scale,
               int kind, const uint8_t* mask, cudaStream_t s) {
     switch (kind) {
-        case BSP_MASK_NONE: return launch32<BLK, BSP_MASK_NONE>(L, Q, K, V, O, Z, scale, mask, s);
-        case BSP_MASK_DENSE: return launch32<BLK, BSP_MASK_DENSE>(L, Q, K, V, O, Z, scale, mask, s);
-        case BSP_MASK_DIAG_CAUSAL: return launch32<BLK, BSP_MASK_DIAG_CAUSAL>(L, Q, K, V, O, Z, scale, mask, s);
+        case BSP_MASK_NONE: return launch32<BLK, BSP_MASK_NONE>(L, Q, K, V, O, lse, Z, scale, mask, s);
+        case BSP_MASK_DENSE: return launch32<BLK, BSP_MASK_DENSE>(L, Q, K, V, O, lse, Z, scale, mask, s);
+        case BSP_MASK_DIAG_CAUSAL: return launch32<BLK, BSP_MASK_DIAG_CAUSAL>(L, Q, K, V, O, lse, Z, scale, mask, s);
         default: return BSP_ERR_INVALID_ARG;
     }
 }
 
 }  // namespace attn32
 
-int launch_attention_tc_tf32(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, int Z,
+int launch_attention_tc_tf32(const bsp_layout_s* L, const void* Q, const void* K, const void* V, void* O, float* lse, int Z,
                              int D, float scale, int kind, const uint8_t* mask, cudaStream_t s) {
     if (D != attn32::D) return BSP_ERR_UNSUPPORTED;
     switch (L->B) {
-        case 128: return attn32::by_kind32<128>(L, Q, K, V, O, Z, scale, kind, mask, s);
-        case 64: return attn32::by_kind32<64>(L, Q, K, V, O, Z, scale, kind, mask, s);
-        case 32: return attn32::by_kind32<32>(L, Q, K, V, O, Z, scale, kind, mask, s);
-        case 16: return attn32::by_kind32<16>(L, Q, K, V, O, Z, scale, kind, mask, s);
+        case 128: return attn32::by_kind32<128>(L, Q, K, V, O, lse, Z, scale, kind, mask, s);
+        case 64: return attn32::by_kind32<64>(L, Q, K, V, O, lse, Z, scale, kind, mask, s);
+        case 32: return attn32::by_kind32<32>(L, Q, K, V, O, lse, Z, scale, kind, mask, s);
+        case 16: return attn32::by_kind32<16>(L, Q, K, V, O, lse, Z, scale, kind, mask, s);
         default: return BSP_ERR_UNSUPPORTED;
     }
 }

@@ -1,0 +1,653 @@
+// Tensor-core (tcgen05) SDD for bf16 / fp16 with fp32 accumulation: the
+// sampled dense x dense product of "question on blocksparse" (openai/triton
+// issue 117), evaluated on the layout's blocks only.
+//
+// Row tiles of 128 query rows (the attention work list); each step computes
+// the 128 x 128 score tile against G = 128/B key blocks into one of four TMEM
+// accumulators; eight epilogue warps write the present blocks while the MMA
+// works ahead.  The kernel template and its launch helpers live here; the
+// plain and softmax modes are instantiated in tc_sdd.cu, the backward modes in
+// tc_sdd_bwd.cu (separate translation units compile in parallel).
+//
+// Operand orientation: op(A) rows and op(B) columns are what the tiles hold.
+// trans_a = 0 / trans_b = 1 store them as rows ([S][K]: K-major tiles, 64-column
+// panels); trans_a = 1 / trans_b = 0 store them as columns ([K][S]): the tile is
+// then loaded as it lies, MN-major (panels of 64 rows, or of one key block of
+// 16 / 32 columns with a 32 / 64-byte swizzle), and only the shared-memory
+// descriptor and the instruction's major-ness bits change.  No transpose
+// happens in memory.
+//
+// Roles (320 threads): warp 0 TMA producer, warp 1 TMEM owner and
+// single-thread MMA issuer, warps 2..9 epilogue (thread = TMEM lane; warps
+// 2..5 take columns 0..63 of the 128-column score tile, warps 6..9 columns
+// 64..127).  The epilogue stages each present piece's rows in shared memory
+// and writes them with asynchronous bulk copies, so its warps never wait on
+// the global writes.  Halving each thread's columns (against four warps on
+// whole rows) is what the fused modes' epilogue-bound passes need.
+//
+// SMX (fused SDD + row softmax): the whole key stream of a row tile is one
+// CTA's, and an epilogue thread owns one query row, so the row softmax fits
+// in the epilogue: every tile's steps run twice, the first pass keeping each
+// row's running max and sum of 2^(scale log2(e) s - max) (masked entries
+// excluded), the second recomputing the scores and writing
+// P = 2^(scale log2(e) s - max) / sum instead of S.  The scores never reach
+// HBM; the second pass repeats the matrix products, which cost less than the
+// round trip of S they replace.
+//
+// SMB (fused SDD + softmax backward, for the attention backward): the product
+// is dP = dO V^T, and with the softmax output P of the same layout the
+// epilogue writes the gradient of the scaled scores,
+//     dX = scale P .* (dP - rowsum(P .* dP)),
+// the softmax backward of the chain rule.  The row sum needs the whole row,
+// so the tile's steps again run twice: the first pass accumulates
+// rowsum(P .* dP) (reading the thread's row of every present P block), the
+// second recomputes dP and writes dX.  dP never reaches memory and stays in
+// fp32; masked entries have P = 0 and so dX = 0.
+//
+// One-pass variants, given what the forward already knows: MODE 3 writes
+// P = exp(scale s - lse) from the rows' log-sum-exp of the forward (no
+// statistics pass); MODE 4 writes dX with rowsum(P .* dP) = dO_row . O_row
+// computed from the forward's output O at the start of each tile (no
+// accumulation pass).
+#pragma once
+
+#include <algorithm>
+#include <type_traits>
+
+#include "common.cuh"
+#include "tc_common.cuh"
+
+namespace bsp {
+namespace sddk {
+
+using namespace tc;
+
+constexpr int kThreads = 320;  // producer, MMA issuer, 8 epilogue warps
+
+// ------------------------------------------------------------------ SDD ----
+
+struct SddArgs {
+    LayoutView L;
+    void* C;
+    int Z;
+    int kd;      // contraction length K
+    int ta, tb;  // trans flags (ta = 1: A tile MN-major; tb = 0: B tile MN-major)
+    // fused softmax only: scale * log2(e), mask kind, dense keep-mask [S][S]
+    float c2;
+    int kind;
+    const uint8_t* mask;
+    // fused softmax backward only: the softmax output [Z][nnz][B][B] and the scale
+    const void* P;
+    float scale;
+    // one-pass modes: the rows' log-sum-exp [Z][H][S] (natural log) of the
+    // forward (MODE 3), the forward's output O [Z][H][S][D] (MODE 4)
+    const float* lse;
+    const void* O;
+    const void* dO;  // MODE 4: the A operand's raw pointer, for rowsum(dO .* O)
+};
+
+__host__ __device__ constexpr uint32_t swz_of(int row_bytes) {
+    return row_bytes == 128 ? kSw128 : (row_bytes == 64 ? kSw64 : kSw32);
+}
+
+// MODE 2 (fused softmax backward): a key-tile stage also holds the step's P
+// tile (128 query rows x 128 keys, two 128-byte-swizzled panels of 64 keys,
+// copied by the producer with the V tile), and one query-tile stage and two
+// key-tile stages make room for it: the product is light there, the
+// epilogue is what a step waits for.
+template <int KP, int BLK, int MODE>
+struct SddCfg {
+    static constexpr bool SMB = MODE == 2 || MODE == 4;
+    static constexpr int kTile = 128 * 64 * KP * 2;  // 128 rows x K (KP panels of 64)
+    static constexpr int AST = SMB ? 1 : 2;  // query-tile stages
+    // key-tile stages: three, except in the backward mode (two stages of V
+    // and P); at K = 128 the fused softmax makes room for the third with one
+    // staging buffer per epilogue warp (its per-tile exchange arrays take the
+    // rest)
+    static constexpr int BST = SMB ? 2 : 3;
+    static constexpr int kPT = SMB ? 32768 : 0;  // P tile of a key-tile stage
+    static constexpr int kBStage = kTile + kPT;
+    static constexpr int kA = 0;
+    static constexpr int kB = AST * kTile;
+    static constexpr int kStg = kB + BST * kBStage;  // staging: NBUF buffers per epilogue warp
+    static constexpr int NBUF = (SMB || (MODE == 1 && KP == 2)) ? 1 : 2;
+    static constexpr int kBuf = 32 * (BLK < 64 ? BLK : 64) * 2;  // a warp's 32 rows of one piece
+    static constexpr int kAlloc = kStg + 8 * NBUF * kBuf + 1024;
+};
+
+// MODE: 0 plain SDD; 1 fused softmax (SMX, two passes); 2 fused softmax
+// backward (SMB, two passes); 3 fused softmax with the rows' log-sum-exp given
+// (one pass); 4 fused softmax backward with rowsum(P .* dP) = rowsum(dO .* O)
+// from the forward's output (one pass)
+template <typename T, int BLK, int KP, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP, const SddArgs args) {
+    using C = SddCfg<KP, BLK, MODE>;
+    constexpr int G = 128 / BLK;
+    constexpr int AST = C::AST, BST = C::BST;
+    constexpr uint32_t kTileBytes = C::kTile;
+    // MN-major key tiles: panels of W keys (RB bytes per K row), KPB per block
+    constexpr int W = BLK < 64 ? BLK : 64, RB = 2 * W, KPB = BLK / W;
+    const int kd = args.kd;
+    const bool a_mn = args.ta != 0, b_mn = args.tb == 0;
+    // bytes one stage's copies deliver: K-major boxes are 64 * KP columns wide
+    // (zero-filled past K), MN-major ones exactly K rows
+    const uint32_t a_bytes = a_mn ? 256u * kd : kTileBytes, b_bytes = b_mn ? 256u * kd : kTileBytes;
+    constexpr bool SMX = MODE == 1 || MODE == 3, SMB = MODE == 2 || MODE == 4;
+    constexpr bool XCH = MODE == 1 || MODE == 2;  // two passes, row statistics exchanged between them
+    constexpr int NPASS = XCH ? 2 : 1;            // passes over a tile's steps
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    __shared__ uint64_t a_full[AST], a_empty[AST], b_full[BST], b_empty[BST], s_full[4], s_empty[4];
+    // fused modes: the two halves of every row exchange their statistics once
+    // per tile (the two warps of lane quadrant q: xq[q]; values in xs)
+    __shared__ uint64_t xq[4];
+    __shared__ float2 xs[XCH ? 2 : 1][2][XCH ? 128 : 1];
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+    // what the issuing threads had issued when they stopped (A tiles, B
+    // steps, MMA steps), drained after the roles stop if the kernel aborted
+    __shared__ uint32_t issued[3];
+
+    const LayoutView& L = args.L;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    Abort ab{&abort_flag, L.status, L.wait_ns};
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < 3; ++i) issued[i] = 0;
+        for (int i = 0; i < AST; ++i) {
+            mbar_init(&a_full[i], 1);
+            mbar_init(&a_empty[i], 1);
+        }
+        for (int i = 0; i < BST; ++i) {
+            mbar_init(&b_full[i], 1);
+            mbar_init(&b_empty[i], SMB ? 9 : 1);  // SMB: the eight epilogue warps also read the stage's P
+        }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], 8);
+        }
+        for (int i = 0; i < 4; ++i) mbar_init(&xq[i], 2);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tS = tmem_base;
+
+    const int64_t total = (int64_t)args.Z * L.n_tiles;
+    const int S = L.S;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            uint32_t a_it = 0, g = 0;
+            for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+                const int4 run = tile_run_at(L, w, args.Z);
+            const int tile = run.x;
+                const int z = (int)((uint32_t)w % (uint32_t)args.Z);
+                const int h = tile / L.ngroups, gq = tile % L.ngroups;
+                const int s0 = run.y, ns = run.z;
+                if (ns == 0) continue;
+                const int64_t zh = (int64_t)z * L.H + h;
+                const uint32_t as = a_it % AST;
+                if (!mbar_wait(&a_empty[as], ((a_it / AST) & 1) ^ 1, ab)) goto producer_done;
+                mbar_arrive_expect_tx(&a_full[as], a_bytes);
+                if (a_mn) {
+                    // [K rows][128 query columns]: two panels of 64 columns
+                    for (int p = 0; p < 2; ++p)
+                        tma_load_2d(smem_u32(smem + C::kA + as * kTileBytes + p * (kd * 128)), &tmA,
+                                    gq * 128 + 64 * p, (int32_t)(zh * kd), &a_full[as]);
+                } else {
+                    for (int p = 0; p < KP; ++p)
+                        tma_load_2d(smem_u32(smem + C::kA + as * kTileBytes + p * 16384), &tmA, p * 64,
+                                    (int32_t)(zh * S + gq * 128), &a_full[as]);
+                }
+                ++a_it;
+                for (int it = 0; it < NPASS * ns; ++it, ++g) {
+                    const int s = s0 + it % ns;
+                    const uint32_t st = g % BST;
+                    if (!mbar_wait(&b_empty[st], ((g / BST) & 1) ^ 1, ab)) goto producer_done;
+                    uint32_t p_bytes = 0;  // SMB: the step's present P blocks
+                    if constexpr (SMB) {
+#pragma unroll
+                        for (int ra = 0; ra < G; ++ra)
+#pragma unroll
+                            for (int b = 0; b < G; ++b)
+                                if (L.step_blk[(s * G + ra) * G + b] >= 0) p_bytes += BLK * BLK * 2;
+                    }
+                    mbar_arrive_expect_tx(&b_full[st], b_bytes + p_bytes);
+#pragma unroll
+                    for (int b = 0; b < G; ++b) {
+                        int c = L.step_col[s * G + b];
+                        if (c < 0) c = L.step_col[s * G];
+                        if (b_mn) {
+                            // [K rows][B key columns]: KPB panels of W columns
+                            for (int p = 0; p < KPB; ++p)
+                                tma_load_2d(smem_u32(smem + C::kB + st * C::kBStage + (b * KPB + p) * (kd * RB)),
+                                            &tmB, c * BLK + W * p, (int32_t)(zh * kd), &b_full[st]);
+                        } else {
+                            for (int p = 0; p < KP; ++p)
+                                tma_load_2d(smem_u32(smem + C::kB + st * C::kBStage + p * 16384 + b * BLK * 128),
+                                            &tmB, p * 64, (int32_t)(zh * S + (int64_t)c * BLK), &b_full[st]);
+                        }
+                    }
+                    if constexpr (SMB) {
+                        // P block (row block ra, slot b) -> rows [ra B, ra B + B) of the
+                        // panel(s) of keys [b B, b B + B)
+                        const uint32_t pt = smem_u32(smem + C::kB + st * C::kBStage + C::kTile);
+#pragma unroll
+                        for (int ra = 0; ra < G; ++ra)
+#pragma unroll
+                            for (int b = 0; b < G; ++b) {
+                                const int blk = L.step_blk[(s * G + ra) * G + b];
+                                if (blk < 0) continue;
+                                const int32_t prow = (int32_t)(((int64_t)z * L.nnz + blk) * BLK);
+#pragma unroll
+                                for (int p = 0; p < BLK / 64; ++p)
+                                    tma_load_2d(pt + (b * (BLK / 64) + p) * 16384 + ra * BLK * 128, &tmP, p * 64, prow,
+                                                &b_full[st]);
+                            }
+                    }
+                }
+            }
+        producer_done:
+            issued[0] = a_it;
+            issued[1] = g;
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16(128, 128, std::is_same<T, __nv_bfloat16>::value, a_mn ? 1 : 0, b_mn ? 1 : 0);
+            // 16-deep contraction steps: every K-major panel of 64 (zeros past K)
+            // when both tiles are K-major, else exactly K / 16
+            const int nks = (a_mn || b_mn) ? kd / 16 : KP * 4;
+            uint32_t a_it = 0, g = 0;
+            for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+                const int ns = tile_run_at(L, w, args.Z).z;
+                if (ns == 0) continue;
+                const uint32_t as = a_it % AST;
+                if (!mbar_wait(&a_full[as], (a_it / AST) & 1, ab)) goto mma_done;
+                for (int it = 0; it < NPASS * ns; ++it, ++g) {
+                    const uint32_t sb = g & 3, st = g % BST;  // TMEM accumulator, key-tile stage
+                    if (!mbar_wait(&s_empty[sb], ((g >> 2) & 1) ^ 1, ab)) goto mma_done;
+                    if (!mbar_wait(&b_full[st], (g / BST) & 1, ab)) goto mma_done;
+                    tc_fence_after();
+                    const uint32_t abase = smem_u32(smem + C::kA + as * kTileBytes);
+                    const uint32_t bbase = smem_u32(smem + C::kB + st * C::kBStage);
+                    for (int ks = 0; ks < nks; ++ks) {
+                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;  // K-major step
+                        const uint64_t da = a_mn ? smem_desc(abase + ks * 2048, kd * 128, 1024, kSw128)
+                                                 : smem_desc(abase + off, 16, 1024, kSw128);
+                        const uint64_t db = b_mn ? smem_desc(bbase + ks * 16 * RB, kd * RB, 8 * RB, swz_of(RB))
+                                                 : smem_desc(bbase + off, 16, 1024, kSw128);
+                        mma_f16(tS + sb * 128, da, db, idesc, ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&s_full[sb]);
+                    mma_commit(&b_empty[st]);
+                    if (it == NPASS * ns - 1) mma_commit(&a_empty[as]);
+                }
+                ++a_it;
+            }
+        mma_done:
+            issued[2] = g;
+        }
+    } else {
+        // Epilogue: eight warps; warp w owns 32 rows of the tile (TMEM lanes of
+        // quadrant q = w % 4) and one half of the 128 columns (hf = (w - 2) / 4:
+        // keys [64 hf, 64 hf + 64)).  A half holds NPH pieces of CW columns:
+        // whole blocks when B <= 64, one 64-column half of a block when B = 128.
+        // Per present piece the warp stages its rows as the output rows they
+        // become and lane 0 issues the copies: a 128-byte-swizzled tensor store
+        // (32 rows x 64 columns) for blocks of 64 and 128, one contiguous bulk
+        // copy of RS rows otherwise.  The fused modes keep per-half row
+        // statistics through their first pass and combine the two halves of
+        // every row once per tile (xq barriers, values in xs).
+        constexpr int RS = BLK < 32 ? BLK : 32;
+        constexpr int CW = BLK < 64 ? BLK : 64;  // columns of one piece
+        constexpr int NPH = 64 / CW;             // pieces per half row
+        constexpr int RBY = CW * 2;              // bytes per staged row of a piece
+        constexpr int C16 = CW * 2 / 16;         // 16-byte chunks per staged row
+        constexpr int kSeg = RS * CW * 2;        // one copy unit
+        constexpr int NBUF = C::NBUF;
+        const int quad = warp & 3, hf = (warp - 2) >> 2;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const int a = row / BLK;
+        const int seg = lane / RS, rin = lane % RS;
+        uint8_t* stg = smem + C::kStg + (warp - 2) * NBUF * C::kBuf;
+        T* Cp = reinterpret_cast<T*>(args.C);
+        if (lane == 0) tma_prefetch_desc(&tmC);
+        uint32_t g = 0, uses = 0, xc = 0;  // xc: row-statistics exchanges so far
+        for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+            const int4 run = tile_run_at(L, w, args.Z);
+            const int tile = run.x;
+            const int z = (int)((uint32_t)w % (uint32_t)args.Z);
+            const int s0 = run.y, ns = run.z;
+            // fused softmax: this half row's running max (scaled log2 domain) and
+            // sum, then the row's; fused softmax backward: rowsum(P .* dP)
+            const int gq = tile % L.ngroups, rb = gq * G + a, r_in = row % BLK;
+            float m = -INFINITY, l = 0.f, msub = 0.f, inv = 0.f;
+            float dsum = 0.f;
+            if constexpr (MODE == 3 || MODE == 4) {
+                // this row's place in [Z][H][S]; rows past the sequence end are
+                // never written
+                const int rseq = gq * 128 + row;
+                const int64_t rg = ((int64_t)z * L.H + tile / L.ngroups) * S + rseq;
+                if constexpr (MODE == 3) {
+                    // P = 2^(c s - lse / ln 2): a row with nothing kept (lse =
+                    // -inf) has every score masked and gets 0
+                    const float lse2 = rseq < S ? args.lse[rg] * kLog2e : -INFINITY;
+                    msub = lse2 == -INFINITY ? 0.f : lse2;
+                    inv = lse2 == -INFINITY ? 0.f : 1.f;
+                } else if (rseq < S) {
+                    // rowsum(P .* dP) = dO_row . O_row, in fp32
+                    const uint4* po = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(args.O) + rg * kd);
+                    const uint4* pg = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(args.dO) + rg * kd);
+                    for (int q = 0; q < kd / 8; ++q) {
+                        const uint4 vo = __ldg(po + q), vg = __ldg(pg + q);
+                        const uint32_t wo[4] = {vo.x, vo.y, vo.z, vo.w}, wg[4] = {vg.x, vg.y, vg.z, vg.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float2 fo = Unpack2<T>::unpack(wo[k]), fg = Unpack2<T>::unpack(wg[k]);
+                            dsum = fmaf(fo.x, fg.x, dsum);
+                            dsum = fmaf(fo.y, fg.y, dsum);
+                        }
+                    }
+                }
+            }
+            for (int it = 0; it < NPASS * ns; ++it, ++g) {
+                const int n = it % ns, s = s0 + n;
+                const bool write = !XCH || it >= ns;  // the pass that writes
+                const uint32_t sb = g & 3;
+                bool ok = mbar_wait(&s_full[sb], (g >> 2) & 1, ab);
+                if (!__all_sync(0xffffffffu, ok)) goto epi_done;
+                tc_fence_after();
+                uint32_t x[64];
+                tmem_ld32_sync(tS + sb * 128 + lane_base + 64 * hf, *reinterpret_cast<uint32_t(*)[32]>(x));
+                tmem_ld32_sync(tS + sb * 128 + lane_base + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
+                // the accumulator is free once both halves are in registers
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_empty[sb]);
+                float* xf = reinterpret_cast<float*>(x);
+                // the pieces of this half: slot and block id of (row block a, slot)
+                int pblk[NPH];
+#pragma unroll
+                for (int p = 0; p < NPH; ++p) pblk[p] = L.step_blk[(s * G + a) * G + (64 * hf + p * CW) / BLK];
+                if constexpr (SMB) {
+                    // this half row of the stage's P tile (panel hf; the copies
+                    // landed: wait on the stage's full barrier), zeros for absent
+                    // pieces; then the stage is released by this warp
+                    const uint32_t st = g % BST;
+                    ok = mbar_wait(&b_full[st], (g / BST) & 1, ab);
+                    if (!__all_sync(0xffffffffu, ok)) goto epi_done;
+                    uint32_t pv[32];
+                    const uint8_t* pb = smem + C::kB + st * C::kBStage + C::kTile + hf * 16384 + row * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const bool present = pblk[(c * 8) / CW] >= 0;
+                        const uint4 v = present ? *reinterpret_cast<const uint4*>(pb + ((c ^ (row & 7)) << 4))
+                                                : make_uint4(0u, 0u, 0u, 0u);
+                        pv[4 * c + 0] = v.x;
+                        pv[4 * c + 1] = v.y;
+                        pv[4 * c + 2] = v.z;
+                        pv[4 * c + 3] = v.w;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&b_empty[st]);
+                    if (!write) {
+                        // first pass: this half's rowsum(P .* dP); at the tile's last
+                        // step the two halves of the row are added
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float2 pf = Unpack2<T>::unpack(pv[j]);
+                            dsum = fmaf(pf.x, xf[2 * j], dsum);
+                            dsum = fmaf(pf.y, xf[2 * j + 1], dsum);
+                        }
+                        if (it == ns - 1) {
+                            xs[xc & 1][hf][row] = make_float2(dsum, 0.f);
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&xq[quad]);
+                            ok = mbar_wait(&xq[quad], xc & 1, ab);
+                            if (!__all_sync(0xffffffffu, ok)) goto epi_done;
+                            dsum += xs[xc & 1][hf ^ 1][row].x;
+                            ++xc;
+                        }
+                        continue;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float2 pf = Unpack2<T>::unpack(pv[j]);
+                        xf[2 * j] = args.scale * pf.x * (xf[2 * j] - dsum);
+                        xf[2 * j + 1] = args.scale * pf.y * (xf[2 * j + 1] - dsum);
+                    }
+                }
+                if constexpr (SMX) {
+                    // masked entries -> -inf: absent pieces, columns past the
+                    // diagonal inside diagonal blocks, dense-mask zeros
+#pragma unroll
+                    for (int p = 0; p < NPH; ++p) {
+                        const int b = (64 * hf + p * CW) / BLK, co = (64 * hf + p * CW) % BLK;
+                        const int blk = pblk[p];
+                        const int col = L.step_col[s * G + b];
+                        // in-piece column j is kept iff j <= lim
+                        const int lim =
+                            blk < 0 ? -1 : ((args.kind == BSP_MASK_DIAG_CAUSAL && col == rb) ? r_in - co : CW);
+                        if (__any_sync(0xffffffffu, lim < CW - 1)) {
+#pragma unroll
+                            for (int j = 0; j < CW; ++j) xf[p * CW + j] = j > lim ? -INFINITY : xf[p * CW + j];
+                        }
+                        if (args.kind == BSP_MASK_DENSE && blk >= 0) {
+                            const uint8_t* mp = args.mask + (int64_t)(gq * 128 + row) * S + (int64_t)col * BLK + co;
+#pragma unroll
+                            for (int q = 0; q < CW / 16; ++q) {
+                                const uint4 mv = *reinterpret_cast<const uint4*>(mp + q * 16);
+                                const uint8_t* mb = reinterpret_cast<const uint8_t*>(&mv);
+#pragma unroll
+                                for (int k = 0; k < 16; ++k)
+                                    if (!mb[k]) xf[p * CW + q * 16 + k] = -INFINITY;
+                            }
+                        }
+                    }
+                    if (!write) {
+                        // first pass: this half row's running max and sum; at the
+                        // tile's last step the halves of the row are combined
+                        float mx = -INFINITY;
+#pragma unroll
+                        for (int j = 0; j < 64; ++j) mx = fmaxf(mx, xf[j]);
+                        const float mn = fmaxf(m, mx * args.c2);
+                        if (mn != -INFINITY) {
+                            float acc = 0.f;
+#pragma unroll
+                            for (int j = 0; j < 64; ++j) acc += ex2_approx(fmaf(xf[j], args.c2, -mn));
+                            l = (m == -INFINITY ? 0.f : l * ex2_approx(m - mn)) + acc;
+                            m = mn;
+                        }
+                        if (it == ns - 1) {
+                            xs[xc & 1][hf][row] = make_float2(m, l);
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&xq[quad]);
+                            ok = mbar_wait(&xq[quad], xc & 1, ab);
+                            if (!__all_sync(0xffffffffu, ok)) goto epi_done;
+                            const float2 o = xs[xc & 1][hf ^ 1][row];
+                            const float mr = fmaxf(m, o.x);
+                            const float lr = mr == -INFINITY ? 0.f
+                                                             : (m == -INFINITY ? 0.f : l * ex2_approx(m - mr)) +
+                                                                   (o.x == -INFINITY ? 0.f : o.y * ex2_approx(o.x - mr));
+                            msub = mr == -INFINITY ? 0.f : mr;
+                            inv = lr > 0.f ? 1.0f / lr : 0.f;
+                            ++xc;
+                        }
+                        continue;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) xf[j] = ex2_approx(fmaf(xf[j], args.c2, -msub)) * inv;
+                }
+
+#pragma unroll
+                for (int p = 0; p < NPH; ++p) {
+                    const int blk = pblk[p];
+                    if (__all_sync(0xffffffffu, blk < 0)) continue;
+                    int sblk[32 / RS];
+#pragma unroll
+                    for (int sg = 0; sg < 32 / RS; ++sg) sblk[sg] = __shfl_sync(0xffffffffu, blk, sg * RS);
+                    uint8_t* buf = stg + (uses % NBUF) * C::kBuf;
+                    if (lane == 0) {  // the copy that last read this buffer has read it
+                        if constexpr (NBUF == 2) bulk_wait_read<1>();
+                        else bulk_wait_read<0>();
+                    }
+                    __syncwarp();
+                    if (blk >= 0) {
+                        uint8_t* rbase = buf + seg * kSeg + rin * RBY;
+#pragma unroll
+                        for (int j = 0; j < C16; ++j) {
+                            const int o = p * CW + 8 * j;
+                            const int pos = CW == 64 ? (j ^ (rin & 7)) : j;
+                            *reinterpret_cast<uint4*>(rbase + pos * 16) = make_uint4(
+                                Pack2<T>::pack(__uint_as_float(x[o]), __uint_as_float(x[o + 1])),
+                                Pack2<T>::pack(__uint_as_float(x[o + 2]), __uint_as_float(x[o + 3])),
+                                Pack2<T>::pack(__uint_as_float(x[o + 4]), __uint_as_float(x[o + 5])),
+                                Pack2<T>::pack(__uint_as_float(x[o + 6]), __uint_as_float(x[o + 7])));
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+#pragma unroll
+                        for (int sg = 0; sg < 32 / RS; ++sg) {
+                            if (sblk[sg] < 0) continue;
+                            const int r_in0 = (quad * 32 + sg * RS) % BLK;
+                            const int64_t orow = ((int64_t)z * L.nnz + sblk[sg]) * BLK + r_in0;
+                            if (BLK >= 64)
+                                tma_store_3d(&tmC, smem_u32(buf + sg * kSeg), (64 * hf + p * CW) % BLK, (int32_t)orow,
+                                             0);
+                            else
+                                bulk_store(Cp + orow * BLK, smem_u32(buf + sg * kSeg), kSeg);
+                        }
+                        bulk_commit();
+                    }
+                    ++uses;
+                }
+            }
+        }
+    epi_done:
+        if (lane == 0) bulk_wait_all();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (abort_flag) {
+        // stopped early: the copies and products issued before the stop land
+        // before the CTA lets go of its shared memory and TMEM
+        if (threadIdx.x == 0) {
+            mbar_drain_ring(a_full, AST, issued[0], ab);
+            mbar_drain_ring(b_full, BST, issued[1], ab);
+            if (issued[2]) mbar_drain(&s_full[(issued[2] - 1) & 3], ((issued[2] - 1) >> 2) & 1, ab);
+        }
+        __syncthreads();
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+// --------------------------------------------------------------- launch ----
+
+// what the fused modes read besides the two operands
+struct SddExtra {
+    float c2 = 0.f;                 // scale * log2(e) (softmax modes)
+    int kind = 0;                   // mask kind (softmax modes)
+    const uint8_t* mask = nullptr;  // dense keep-mask (softmax modes)
+    const void* P = nullptr;        // softmax output (backward modes)
+    float scale = 0.f;              // softmax scale (backward modes)
+    const float* lse = nullptr;     // MODE 3
+    const void* O = nullptr;        // MODE 4
+};
+
+template <typename T, int BLK, int KP, int MODE>
+int sdd_launch(const bsp_layout_s* Lh, const void* A, const void* B, void* Cout, int Z, int K, int ta, int tb,
+               const SddExtra& e, cudaStream_t s) {
+    const int bf = std::is_same<T, __nv_bfloat16>::value;
+    const uint64_t ZH = (uint64_t)Z * Lh->H, rows = ZH * Lh->S;
+    constexpr int W = BLK < 64 ? BLK : 64;
+    CUtensorMap ma, mb, mc, mp;
+    // [S][K] operands: boxes of 128 (A) or B (B) rows x 64 columns; [K][S]
+    // operands: boxes of K rows x 64 (A) or W (B) columns
+    int rc = ta ? make_tmap_2d(&ma, A, bf, ZH * K, Lh->S, K, 64, 128) : make_tmap_2d(&ma, A, bf, rows, K, 128, 64, 128);
+    if (!rc)
+        rc = tb ? make_tmap_2d(&mb, B, bf, rows, K, BLK, 64, 128) : make_tmap_2d(&mb, B, bf, ZH * K, Lh->S, K, W, 2 * W);
+    // output rows: [Z * nnz * B][B], boxes of min(32, B) rows x W columns
+    // (128-byte swizzle for W = 64)
+    if (!rc)
+        rc = make_tmap_3d(&mc, Cout, bf, BLK, (uint64_t)Z * Lh->nnz * BLK, 1, W, BLK < 32 ? BLK : 32,
+                          BLK >= 64 ? 128 : 0);
+    // fused softmax backward: P rows [Z * nnz * B][B], boxes of B rows x 64
+    // columns, 128-byte swizzle (the other modes never read this map)
+    if (!rc) {
+        if constexpr (MODE == 2 || MODE == 4)
+            rc = make_tmap_2d(&mp, e.P, bf, (uint64_t)Z * Lh->nnz * BLK, BLK, BLK, 64, 128);
+        else mp = mc;
+    }
+    if (rc) return rc;
+    SddArgs a{Lh->view, Cout, Z, K, ta, tb, e.c2, e.kind, e.mask, e.P, e.scale, e.lse, e.O, A};
+    auto kern = sdd_tc_kernel<T, BLK, KP, MODE>;
+    constexpr int smem = SddCfg<KP, BLK, MODE>::kAlloc;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return BSP_ERR_CUDA;
+    const int64_t total = (int64_t)Z * Lh->n_tiles;
+    const int grid = (int)std::min<int64_t>(total, sm_count());
+    kern<<<grid, kThreads, smem, s>>>(ma, mb, mc, mp, a);
+    return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
+}
+
+template <typename T, int BLK, int MODE>
+int sdd_by_k(const bsp_layout_s* L, const void* A, const void* B, void* C, int Z, int K, int ta, int tb,
+             const SddExtra& e, cudaStream_t s) {
+    if (K <= 64) return sdd_launch<T, BLK, 1, MODE>(L, A, B, C, Z, K, ta, tb, e, s);
+    return sdd_launch<T, BLK, 2, MODE>(L, A, B, C, Z, K, ta, tb, e, s);
+}
+
+// the backward modes read P in 64-key panels: blocks of 64 and 128 only
+template <typename T, int MODE>
+int sdd_by_block(const bsp_layout_s* L, const void* A, const void* B, void* C, int Z, int K, int ta, int tb,
+                 const SddExtra& e, cudaStream_t s) {
+    constexpr bool small_ok = !(MODE == 2 || MODE == 4);
+    switch (L->B) {
+        case 16:
+            if constexpr (small_ok) return sdd_by_k<T, 16, MODE>(L, A, B, C, Z, K, ta, tb, e, s);
+            return BSP_ERR_UNSUPPORTED;
+        case 32:
+            if constexpr (small_ok) return sdd_by_k<T, 32, MODE>(L, A, B, C, Z, K, ta, tb, e, s);
+            return BSP_ERR_UNSUPPORTED;
+        case 64: return sdd_by_k<T, 64, MODE>(L, A, B, C, Z, K, ta, tb, e, s);
+        case 128: return sdd_by_k<T, 128, MODE>(L, A, B, C, Z, K, ta, tb, e, s);
+        default: return BSP_ERR_UNSUPPORTED;
+    }
+}
+
+template <int MODE>
+int sdd_by_dtype(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z, int K, int ta,
+                 int tb, const SddExtra& e, cudaStream_t s) {
+    if (dtype == BSP_BF16) return sdd_by_block<__nv_bfloat16, MODE>(L, A, B, C, Z, K, ta, tb, e, s);
+    if (dtype == BSP_F16) return sdd_by_block<__half, MODE>(L, A, B, C, Z, K, ta, tb, e, s);
+    return BSP_ERR_UNSUPPORTED;
+}
+
+// shapes the tensor-core SDD covers: K at most 128 (one shared-memory tile);
+// both operands [S][K]: K a multiple of 8 (the row pitch of a TMA map is a
+// multiple of 16 bytes); an operand stored [K][S]: K a multiple of 16 (its
+// tile has exactly K rows)
+inline bool sdd_tc_shape(const bsp_layout_s* L, int Z, int K, int ta, int tb) {
+    if (K > 128 || K % 8 != 0 || ((ta || !tb) && K % 16 != 0)) return false;
+    return (uint64_t)Z * L->H * std::max(L->S, K) < (1ull << 31);
+}
+
+}  // namespace sddk
+}  // namespace bsp

@@ -460,6 +460,9 @@ def test_new_entry_points_validate_arguments(lib):
     assert lib.bsp_attention_host_workspace(None, 1, 64, 1) == 0
     assert lib.bsp_attention_host_workspace(L.handle, 1, 64, 0) == 0
     assert lib.bsp_diag_geometry_steps(None, a, a) == -1
+    assert lib.bsp_attention_lse(None, 1, a, a, a, a, a, 1, 64, one, 0, None, None) == -1
+    assert lib.bsp_attention_lse(L.handle, 1, a, a, a, a, a, 1, 64, one, 0, None, None) == -1  # host-only handle
+    assert lib.bsp_attention_backward_lse(None, 1, a, a, a, a, a, a, a, a, a, 1, 64, one, 0, None, a, a, None) == -1
 
 
 def test_diag_wait_limit_needs_a_compiled_handle(lib):

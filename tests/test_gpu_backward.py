@@ -146,3 +146,97 @@ def test_softmax_backward_long_rows(bsp, oracle, B, dt, nb):
     got = bsp.bsp_softmax_backward(L, Y, dY, None, scale)
     torch.cuda.synchronize()
     check(got, oracle.softmax_backward(lay, B, Y, dY, scale), TOL[dtype], f"long rows B={B} {dt}")
+
+
+# ------------------------------------------- forward lse + backward_lse ----
+
+def lse_bound(Q, K, scale, n_keys):
+    """|lse_gpu - lse_oracle| per row: the score error of an fp32 accumulation
+    of D products, scale * gamma(D) * |q| * max|k| (Cauchy-Schwarz), plus the
+    relative error of a sum of n_keys exponentials (2^-22 each, 2^-24 per
+    addition with a factor 4 for tensor-core adders), plus the rounding of
+    the logarithm and the final products (2^-22 of |lse| and an absolute
+    2^-22)."""
+    from gpu_util import gamma
+    q = Q.double().norm(dim=-1)                      # [Z, H, S]
+    kmax = K.double().norm(dim=-1).amax(dim=-1, keepdim=True)
+    return (scale * gamma(Q.shape[-1]) * q * kmax + (n_keys + 4) * 2.0 ** -22).numpy()
+
+
+@pytest.mark.parametrize("B", [16, 64, 128])
+@pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("kind", [0, 1, 2])
+def test_attention_lse(bsp, oracle, path, B, dt, D, kind):
+    # the forward's O is the plain forward's, byte for byte; lse matches the
+    # oracle's log-sum-exp row by row (-inf exactly for rows with nothing kept)
+    dtype = DTYPES[dt]
+    Z, H, scale = 2, 2, 1.0 / np.sqrt(D)
+    nb = max(4, 384 // B) + 1
+    S = nb * B
+    lay = rlayout(H, nb, 0.35, 110 + B)
+    mask = W.random_mask(S, 0.7, 111) if kind == W.MASK_DENSE else None
+    dmask = None if mask is None else torch.from_numpy(mask).cuda()
+    Q, K, V = (randn((Z, H, S, D), dtype, s) for s in (112, 113, 114))
+    q, k, v = dev(Q), dev(K), dev(V)
+    L = bsp.bsp_layout_compile(lay, B)
+    O, lse = bsp.bsp_attention_lse(L, q, k, v, None, None, scale, kind, dmask)
+    O0 = bsp.bsp_attention(L, q, k, v, None, scale, kind, dmask)
+    torch.cuda.synchronize()
+    assert bsp.bsp_status_check(L) == 0
+    assert torch.equal(O, O0), "bsp_attention_lse's O differs from bsp_attention's"
+    want = oracle.attention_lse(lay, B, Q, K, scale, kind, mask)
+    got = lse.cpu().double().numpy()
+    empty = np.isneginf(want)
+    assert empty.any()
+    assert np.all(np.isneginf(got[empty])), "rows with nothing kept must have lse = -inf"
+    err = np.abs(got[~empty] - want[~empty])
+    bound = lse_bound(Q, K, scale, S)[~empty] + 2.0 ** -22 * np.abs(want[~empty])
+    worst = np.argmax(err - bound)
+    assert np.all(err <= bound), f"lse B={B} {dt} D={D} kind={kind} {path}: error {err[worst]:.3e} > {bound[worst]:.3e}"
+
+
+@pytest.mark.parametrize("B", [16, 32, 64, 128])
+@pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("kind", [0, 1, 2])
+def test_attention_backward_lse(bsp, oracle, path, B, dt, D, kind):
+    # gradients from the forward's O and lse: the oracle's, within the same
+    # tolerance as the recomputing chain
+    dtype = DTYPES[dt]
+    Z, H, scale = 2, 2, 1.0 / np.sqrt(D)
+    nb = max(4, 384 // B)  # >= 4: block-row 2 is empty
+    S = nb * B
+    lay = rlayout(H, nb, 0.4, 70 + B)
+    L = bsp.bsp_layout_compile(lay, B)
+    Q, K, V, G = (randn((Z, H, S, D), dtype, s) for s in (71, 72, 73, 74))
+    mask = W.random_mask(S, 0.7, 75) if kind == W.MASK_DENSE else None
+    dmask = None if mask is None else torch.from_numpy(mask).cuda()
+    q, k, v, g = dev(Q), dev(K), dev(V), dev(G)
+    O, lse = bsp.bsp_attention_lse(L, q, k, v, None, None, scale, kind, dmask)
+    dQ, dK, dV = bsp.attention_backward_lse(L, q, k, v, O, g, lse, scale, kind, dmask)
+    torch.cuda.synchronize()
+    assert bsp.bsp_status_check(L) == 0
+    wQ, wK, wV = oracle.attention_backward(lay, B, Q, K, V, G, scale, kind, mask)
+    tol = GRAD_TOL[dtype]
+    check(dV, wV, tol, f"dV (lse) B={B} {dt} D={D} kind={kind} {path}")
+    check(dQ, wQ, tol, f"dQ (lse) B={B} {dt} D={D} kind={kind} {path}")
+    check(dK, wK, tol, f"dK (lse) B={B} {dt} D={D} kind={kind} {path}")
+    assert (dQ[0, 0, 2 * B:3 * B] == 0).all()
+
+
+def test_backward_lse_rejects_missing_statistics(bsp):
+    L = bsp.bsp_layout_compile(np.ones((1, 2, 2), np.uint8), 64)
+    Q = torch.randn(1, 1, 128, 64, device="cuda", dtype=torch.bfloat16)
+    ws = torch.empty(1, 4, 64, 64, device="cuda", dtype=torch.bfloat16)
+    f = bsp.lib().bsp_attention_backward_lse
+    p = bsp._ptr
+    lse = torch.zeros(1, 1, 128, device="cuda")
+    # no lse, no O: BSP_ERR_INVALID_ARG; misaligned lse: BSP_ERR_ALIGNMENT
+    assert f(L.handle, 1, p(Q), p(Q), p(Q), p(Q), p(Q), None, p(Q), p(Q), p(Q), 1, 64, 0.1, 0, None, p(ws), p(ws),
+             None) == -1
+    assert f(L.handle, 1, p(Q), p(Q), p(Q), None, p(Q), p(lse), p(Q), p(Q), p(Q), 1, 64, 0.1, 0, None, p(ws), p(ws),
+             None) == -1
+    bad = bsp.ctypes.c_void_p(lse.data_ptr() + 4)
+    assert f(L.handle, 1, p(Q), p(Q), p(Q), p(Q), p(Q), bad, p(Q), p(Q), p(Q), 1, 64, 0.1, 0, None, p(ws), p(ws),
+             None) == -3

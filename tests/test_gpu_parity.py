@@ -404,9 +404,17 @@ def test_attention_cut_tiles(bsp, oracle, B, dt, kind, cut):
     O2 = bsp.bsp_attention(L, q, k, v, scale=0.125, mask_kind=kind, mask=dmask)
     bsp.bsp_diag_attention_split(L, -1)
     O0 = bsp.bsp_attention(L, q, k, v, scale=0.125, mask_kind=kind, mask=dmask)
+    # the combine pass also writes the cut rows' log-sum-exp
+    bsp.bsp_diag_attention_split(L, cut)
+    _, lse = bsp.bsp_attention_lse(L, q, k, v, None, None, 0.125, kind, dmask)
     torch.cuda.synchronize()
     assert bsp.bsp_status_check(L) == 0
     assert torch.equal(O1, O2)
+    want_lse = oracle.attention_lse(lay, B, Q, K, 0.125, kind, mask)
+    kept = ~np.isneginf(want_lse)
+    got_lse = lse.cpu().double().numpy()
+    assert np.all(np.isneginf(got_lse[~kept]))
+    assert np.abs(got_lse[kept] - want_lse[kept]).max() < 1e-3, "lse of cut tiles"
     want = oracle.attention(lay, B, Q, K, V, 0.125, kind, mask)
     mag = oracle.attention(lay, B, Q, K, V.abs(), 0.125, kind, mask)
     acc = attention_acc(Q, K, 0.125, dtype, S)

@@ -58,6 +58,9 @@ MUTANTS = {
     "affine_causal_ignored": ("if (causal && j > i) return 0;", "(void)causal;"),
     "affine_kappa_off_by_one": ("return d / sigma < kappa;", "return d / sigma <= kappa;"),
     "affine_row_slope_dropped": ("const int64_t d = j - alpha * i - beta;", "const int64_t d = j - beta;"),
+    "lse_ignores_intra_block_mask": ("if (!present || !keep(kind, mask, S, B, row, c)) {", "if (!present) {"),
+    "lse_drops_max": ("out[s] = top + log(total);", "out[s] = log(total);"),
+    "lse_log2": ("out[s] = top + log(total);", "out[s] = top + log2(total);"),
 }
 
 

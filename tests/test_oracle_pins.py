@@ -315,6 +315,47 @@ def test_attention_unit_values_give_ones(oracle):
     assert np.all(got[0, 0][~rows] == 0.0)
 
 
+# the rows' log-sum-exp of the kept scaled scores (the softmax normaliser)
+
+@pytest.mark.parametrize("kind", [W.MASK_NONE, W.MASK_DENSE, W.MASK_DIAG_CAUSAL])
+def test_attention_lse_is_scipy_logsumexp_of_masked_scores(oracle, kind):
+    from scipy.special import logsumexp
+    Z, H, S, D, B = 2, 2, 48, 8, 8
+    lay = random_layout(H, S // B, 0.35, 60)
+    mask = W.random_mask(S, 0.6, 61) if kind == W.MASK_DENSE else None
+    Q, K = rand(Z, H, S, D, seed=62), rand(Z, H, S, D, seed=63)
+    M = libref.expand_mask(lay, B).astype(bool) & libref.keep_mask(S, B, kind, mask)[None]  # [H, S, S]
+    s = 0.45 * np.einsum("zhrd,zhcd->zhrc", Q.astype(np.float64), K.astype(np.float64))
+    want = logsumexp(np.where(M[None], s, -np.inf), axis=-1)  # -inf for empty rows
+    got = oracle.attention_lse(lay, B, Q, K, 0.45, kind, mask)
+    empty = ~M.any(-1)
+    assert empty.any()  # the random layout has an empty block-row
+    assert np.all(np.isneginf(got[:, empty]))
+    np.testing.assert_allclose(got[:, ~empty], want[:, ~empty], rtol=1e-12, atol=1e-12)
+
+
+def test_attention_lse_zero_query_is_log_of_count(oracle):
+    # every kept score is 0: lse = log |R|
+    Z, H, S, D, B = 1, 2, 40, 6, 8
+    lay = random_layout(H, S // B, 0.5, 64)
+    Q = np.zeros((Z, H, S, D), np.float32)
+    K = rand(Z, H, S, D, seed=65)
+    cnt = libref.expand_mask(lay, B).sum(-1)  # [H, S]
+    got = oracle.attention_lse(lay, B, Q, K, 1.0)[0]
+    np.testing.assert_allclose(got[cnt > 0], np.log(cnt[cnt > 0]), rtol=1e-14)
+    assert np.all(np.isneginf(got[cnt == 0]))
+
+
+def test_attention_lse_selection_matches_full(oracle):
+    Z, H, S, D, B = 2, 2, 32, 8, 16
+    lay = random_layout(H, S // B, 0.6, 66)
+    Q, K = rand(Z, H, S, D, seed=67), rand(Z, H, S, D, seed=68)
+    full = oracle.attention_lse(lay, B, Q, K, 0.3, W.MASK_DIAG_CAUSAL).reshape(-1)
+    sel = np.array([0, 5, 17, 33, 64, 127], np.int64)
+    got = oracle.attention_lse(lay, B, Q, K, 0.3, W.MASK_DIAG_CAUSAL, sel=sel)
+    np.testing.assert_array_equal(got, full[sel])
+
+
 @pytest.mark.parametrize("kind", [W.MASK_NONE, W.MASK_DENSE, W.MASK_DIAG_CAUSAL])
 def test_attention_equals_sdd_softmax_dsd_chain(oracle, kind):
     # the page's chain: SDD output reduced by the block softmax, then DSD with V
