@@ -367,8 +367,15 @@ def per_op_section(w, lay, L, q, k, v, pk, bsp, stream):
     gO = torch.randn_like(q)
     ms = time_launches(lambda: bsp.attention_backward(L, q, k, v, gO, w.scale, w.mask_kind), 5, stream)
     fl = 10.0 * B * B * D * nnz * Z
-    out["attention_backward"] = {"ms": ms, "TFLOP/s": fl / ms / 1e9, "flops_counted": "10 B^2 D per block"}
-    del P, X, O, gO
+    out["attention_backward"] = {"ms": ms, "TFLOP/s": fl / ms / 1e9, "flops_counted": "10 B^2 D per block",
+                                 "api": "bsp_attention_backward (recomputes the softmax statistics)"}
+    # the autograd path: the forward keeps O and the rows' log-sum-exp
+    Of, lse = bsp.bsp_attention_lse(L, q, k, v, None, None, w.scale, w.mask_kind)
+    ms = time_launches(lambda: bsp.attention_backward_lse(L, q, k, v, Of, gO, lse, w.scale, w.mask_kind), 5,
+                       stream)
+    out["attention_backward_lse"] = {"ms": ms, "TFLOP/s": fl / ms / 1e9, "flops_counted": "10 B^2 D per block",
+                                     "api": "bsp_attention_backward_lse (O and lse of bsp_attention_lse)"}
+    del P, X, O, gO, Of, lse
     # general spMM at 10 % density (8192^2 sparse, 8192x4096 dense, block 32)
     sp = W.SPMM
     lay4 = sp.layout(0.10)
