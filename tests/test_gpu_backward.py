@@ -225,6 +225,23 @@ def test_attention_backward_lse(bsp, oracle, path, B, dt, D, kind):
     assert (dQ[0, 0, 2 * B:3 * B] == 0).all()
 
 
+def test_lse_pair_empty_layout_and_zero_batch(bsp):
+    # nothing kept anywhere: O = 0, lse = -inf, every gradient 0; Z = 0: no work
+    lay = np.zeros((2, 4, 4), np.uint8)
+    L = bsp.bsp_layout_compile(lay, 32)
+    Q = torch.randn(1, 2, 128, 64, device="cuda", dtype=torch.bfloat16)
+    O, lse = bsp.bsp_attention_lse(L, Q, Q, Q, None, None, 0.1)
+    dQ, dK, dV = bsp.attention_backward_lse(L, Q, Q, Q, O, Q, lse, 0.1)
+    torch.cuda.synchronize()
+    assert (O == 0).all() and torch.isneginf(lse).all()
+    assert all((t == 0).all() for t in (dQ, dK, dV))
+    E = torch.empty(0, 2, 128, 64, device="cuda", dtype=torch.bfloat16)
+    L1 = bsp.bsp_layout_compile(np.ones((2, 4, 4), np.uint8), 32)
+    O, lse = bsp.bsp_attention_lse(L1, E, E, E, None, None, 0.1)
+    dQ, dK, dV = bsp.attention_backward_lse(L1, E, E, E, O, E, lse, 0.1)
+    assert dQ.shape == E.shape and lse.shape == (0, 2, 128)
+
+
 def test_backward_lse_rejects_missing_statistics(bsp):
     L = bsp.bsp_layout_compile(np.ones((1, 2, 2), np.uint8), 64)
     Q = torch.randn(1, 1, 128, 64, device="cuda", dtype=torch.bfloat16)
