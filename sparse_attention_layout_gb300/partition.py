@@ -54,3 +54,41 @@ def shard_layout(layout: np.ndarray, Z: int, rank: int, world: int):
     u0, u1 = balanced_ranges(pair_weights(lay, Z), world)[rank]
     heads = np.arange(u0, u1) % H
     return u0, u1, np.ascontiguousarray(lay[heads])
+
+
+# ------------------------------------------------------ DSD / DDS shards ----
+#
+# DSD (C = A_sp B, output rows follow A_sp's block-rows) shards over
+# block-rows, DDS (C = A B_sp, output columns follow B_sp's block-columns)
+# over block-columns; each rank produces disjoint output rows / columns, so
+# the pieces are the result with no reduction.  A rank's problem is a layout
+# of the same shape with every block outside its lines removed, and the
+# sparse operand restricted to the blocks that remain (block order is
+# row-major (h, i, j), so the remaining blocks keep their relative order).
+
+def line_weights(layout: np.ndarray, orient: int) -> np.ndarray:
+    """Present blocks of every line, flattened over heads: block-rows
+    (orient 0, index h * nb + i) or block-columns (orient 1, h * nb + j)."""
+    lay = np.asarray(layout)
+    counts = lay.sum(axis=2 if orient == 0 else 1)  # [H, nb]
+    return counts.reshape(-1).astype(np.int64)
+
+
+def shard_lines(layout: np.ndarray, orient: int, rank: int, world: int):
+    """(l0, l1, sub_layout, block_ids) of this rank: its lines [l0, l1) in the
+    flattened (h, line) order, the layout with every other line's blocks
+    removed, and the ids (row-major (h, i, j) ranks in the full layout) of
+    the blocks it keeps, ascending -- the rows of the sparse operand it
+    takes, in the sub-layout's own block order."""
+    lay = np.asarray(layout)
+    H, nb = lay.shape[0], lay.shape[1]
+    l0, l1 = balanced_ranges(line_weights(lay, orient), world)[rank]
+    keep = np.zeros((H, nb), dtype=bool)
+    keep.reshape(-1)[l0:l1] = True
+    sub = lay.copy()
+    if orient == 0:
+        sub[~keep] = 0                                   # rows outside [l0, l1)
+    else:
+        sub = np.where(keep[:, None, :], sub, 0).astype(lay.dtype)  # columns outside
+    ids = np.flatnonzero(sub[lay.astype(bool)])          # the kept blocks' full-layout ids, ascending
+    return l0, l1, np.ascontiguousarray(sub), ids

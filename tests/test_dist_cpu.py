@@ -107,3 +107,65 @@ def test_two_ranks_split_one_workload_gloo():
     (a0, a1), (b0, b1) = out["bounds"]
     assert a0 == 0 and a1 == b0 and b1 == 6 and 0 < a1 < 6   # both ranks work, no pair twice
     assert out["equal"]                                       # the pieces are the whole result, bit for bit
+
+
+def test_line_shards_cover_every_block_once():
+    import numpy as np
+    from sparse_attention_layout_gb300 import partition, workloads as W
+    for lay in (W.layout_random_diag(12, 0.3, H=3, seed=3), W.BIGBIRD.layout(), np.zeros((2, 4, 4), np.uint8)):
+        for orient in (0, 1):
+            w = partition.line_weights(lay, orient)
+            for world in (1, 2, 3, 8):
+                ids, loads, prev = [], [], 0
+                for r in range(world):
+                    l0, l1, sub, kept = partition.shard_lines(lay, orient, r, world)
+                    assert l0 == prev and l1 >= l0                     # contiguous lines, in order
+                    prev = l1
+                    assert sub.shape == lay.shape and int(sub.sum()) == kept.size
+                    assert np.all(sub <= lay)                          # only the layout's own blocks
+                    ids.append(kept)
+                    loads.append(kept.size)
+                assert prev == w.size
+                assert np.array_equal(np.sort(np.concatenate(ids)), np.arange(int(lay.sum())))
+                assert max(loads) <= w.sum() / world + (w.max() if w.size else 0)
+
+
+def _spmm_split_worker(rank, world, port, out):
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    sys.path.insert(0, root)
+    import numpy as np
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import oracle
+    from sparse_attention_layout_gb300 import partition, workloads as W
+    orc = oracle.Oracle()
+    lay = W.layout_random_diag(10, 0.35, H=2, seed=7)
+    Z, B, N = 2, 16, 24
+    S = 10 * B
+    nnz = int(lay.sum())
+    Asp = W.uniform((Z, nnz, B, B), "f32", 70)
+    Bd = W.uniform((Z, 2, S, N), "f32", 71)
+    Ad = W.uniform((Z, 2, N, S), "f32", 72)
+    res = {}
+    for orient, name in ((0, "dsd"), (1, "dds")):
+        _, _, sub, ids = partition.shard_lines(lay, orient, rank, world)
+        part = Asp[:, ids]
+        C = orc.dsd(sub, B, part, Bd) if orient == 0 else orc.dds(sub, B, Ad, part)
+        pieces = [None] * world
+        dist.all_gather_object(pieces, C)   # test-side only: assemble the ranks' disjoint outputs
+        if rank == 0:
+            full = orc.dsd(lay, B, Asp, Bd) if orient == 0 else orc.dds(lay, B, Ad, Asp)
+            res[name] = bool(np.array_equal(sum(pieces), full)) and all(np.any(p) for p in pieces)
+    if rank == 0:
+        out.update(res)
+    dist.destroy_process_group()
+
+
+def test_two_ranks_split_dsd_and_dds_gloo():
+    world = 2
+    port = _free_port()
+    manager = mp.get_context("spawn").Manager()
+    out = manager.dict()
+    mp.start_processes(_spmm_split_worker, args=(world, port, out), nprocs=world, start_method="spawn", join=True)
+    assert out["dsd"] and out["dds"]   # disjoint rows / columns: the pieces add up to the whole, bit for bit
