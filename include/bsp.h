@@ -349,8 +349,9 @@ int bsp_attention_backward(bsp_layout_t layout, int dtype, const void* Q, const 
  * (no statistics pass), and rowsum(P .* dP) = rowsum(dO .* O) per row, so
  * dX = scale P .* (dP - rowsum(dO .* O)) also takes one pass.  O, dO: DEVICE
  * [Z][H][S][D]; lse: DEVICE float [Z][H][S], 16-byte aligned; the rest as for
- * bsp_attention_backward.  fp32, and shapes the one-pass tensor-core kernels
- * do not cover, take bsp_attention_backward's recomputing chain (O and lse
+ * bsp_attention_backward; dQ's memory holds the rows' dO . O (fp32) until it
+ * receives dQ.  fp32, and shapes the one-pass tensor-core kernels do not
+ * cover, take bsp_attention_backward's recomputing chain (O and lse
  * unused).  Not from the pages: the chain rule with the forward's statistics
  * kept. */
 int bsp_attention_backward_lse(bsp_layout_t layout, int dtype, const void* Q, const void* K, const void* V,

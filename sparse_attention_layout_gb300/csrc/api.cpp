@@ -284,8 +284,15 @@ extern "C" int bsp_attention_backward_lse(bsp_layout_t L, int dtype, const void*
     // dV = P^T dO
     if ((rc = bsp_dsd(L, dtype, P_ws, dO, dV, Z, D, 1, 0, stream))) return rc;
     // dX = scale P .* (dP - rowsum(dO .* O)), dP = dO V^T: one pass (blocks of
-    // 64 and 128), else dP through memory and the softmax backward in place
-    rc = bsp::launch_sdd_softmax_bwd_o_tc(L, dtype, dO, V, P_ws, O, dP_ws, Z, D, scale, s);
+    // 64 and 128), else dP through memory and the softmax backward in place.
+    // The rows' dO . O go to dQ's memory first (fp32 [Z][H][S] fits in any
+    // [Z][H][S][D] tensor of D >= 2); dQ receives its own values last.
+    rc = BSP_ERR_UNSUPPORTED;
+    if (L->B >= 64) {
+        float* dvec = static_cast<float*>(dQ);
+        if ((rc = bsp::launch_row_dot(dtype, dO, O, dvec, (int64_t)Z * L->H * L->S, D, s))) return rc;
+        rc = bsp::launch_sdd_softmax_bwd_o_tc(L, dtype, dO, V, P_ws, dvec, dP_ws, Z, D, scale, s);
+    }
     if (rc == BSP_ERR_UNSUPPORTED) {
         if ((rc = bsp_sdd(L, dtype, dO, V, dP_ws, Z, D, 0, 1, stream))) return rc;
         rc = bsp_softmax_backward(L, dtype, P_ws, dP_ws, dP_ws, Z, scale, stream);

@@ -144,7 +144,50 @@ int bwd_t(const bsp_layout_s* L, const void* Y, const void* dY, void* dX, int Z,
     }
 }
 
+// out[r] = sum_d A[r][d] B[r][d] in fp32 (the rowsum(dO .* O) of the attention
+// backward): one warp per row, 16-byte loads, grid-stride over the rows.
+template <typename T>
+__global__ void __launch_bounds__(256) row_dot_kernel(const T* __restrict__ A, const T* __restrict__ B,
+                                                      float* __restrict__ out, int64_t rows, int D) {
+    constexpr int E = 16 / sizeof(T);  // elements per 16-byte load
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
+        const T* a = A + r * D;
+        const T* b = B + r * D;
+        float acc = 0.f;
+        for (int d = lane * E; d < D; d += 32 * E) {
+            float fa[E], fb[E];
+            Vec16<T>::load(a + d, fa);
+            Vec16<T>::load(b + d, fb);
+#pragma unroll
+            for (int k = 0; k < E; ++k) acc = fmaf(fa[k], fb[k], acc);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) out[r] = acc;
+    }
+}
+
+template <typename T>
+int row_dot_t(const void* A, const void* B, float* out, int64_t rows, int D, cudaStream_t s) {
+    if (rows == 0) return BSP_OK;
+    const int64_t blocks = std::min<int64_t>((rows + 7) / 8, (int64_t)sm_count() * 16);
+    row_dot_kernel<T><<<(unsigned)blocks, 256, 0, s>>>((const T*)A, (const T*)B, out, rows, D);
+    return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
+}
+
 }  // namespace
+
+int launch_row_dot(int dtype, const void* A, const void* B, float* out, int64_t rows, int D, cudaStream_t s) {
+    if (D % 8 != 0) return BSP_ERR_UNSUPPORTED;  // whole 16-byte loads
+    switch (dtype) {
+        case BSP_F32: return row_dot_t<float>(A, B, out, rows, D, s);
+        case BSP_BF16: return row_dot_t<__nv_bfloat16>(A, B, out, rows, D, s);
+        case BSP_F16: return row_dot_t<__half>(A, B, out, rows, D, s);
+        default: return BSP_ERR_INVALID_ARG;
+    }
+}
 
 int launch_softmax_backward(const bsp_layout_s* L, int dtype, const void* Y, const void* dY, void* dX, int Z,
                             float scale, cudaStream_t s) {

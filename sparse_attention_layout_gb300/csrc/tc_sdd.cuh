@@ -47,7 +47,7 @@
 // One-pass variants, given what the forward already knows: MODE 3 writes
 // P = exp(scale s - lse) from the rows' log-sum-exp of the forward (no
 // statistics pass); MODE 4 writes dX with rowsum(P .* dP) = dO_row . O_row
-// computed from the forward's output O at the start of each tile (no
+// taken from a vector computed beforehand from the forward's output O (no
 // accumulation pass).
 #pragma once
 
@@ -80,10 +80,9 @@ struct SddArgs {
     const void* P;
     float scale;
     // one-pass modes: the rows' log-sum-exp [Z][H][S] (natural log) of the
-    // forward (MODE 3), the forward's output O [Z][H][S][D] (MODE 4)
+    // forward (MODE 3), the rows' rowsum(dO .* O) [Z][H][S] (MODE 4)
     const float* lse;
-    const void* O;
-    const void* dO;  // MODE 4: the A operand's raw pointer, for rowsum(dO .* O)
+    const float* dvec;
 };
 
 __host__ __device__ constexpr uint32_t swz_of(int row_bytes) {
@@ -346,20 +345,9 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     const float lse2 = rseq < S ? args.lse[rg] * kLog2e : -INFINITY;
                     msub = lse2 == -INFINITY ? 0.f : lse2;
                     inv = lse2 == -INFINITY ? 0.f : 1.f;
-                } else if (rseq < S) {
-                    // rowsum(P .* dP) = dO_row . O_row, in fp32
-                    const uint4* po = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(args.O) + rg * kd);
-                    const uint4* pg = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(args.dO) + rg * kd);
-                    for (int q = 0; q < kd / 8; ++q) {
-                        const uint4 vo = __ldg(po + q), vg = __ldg(pg + q);
-                        const uint32_t wo[4] = {vo.x, vo.y, vo.z, vo.w}, wg[4] = {vg.x, vg.y, vg.z, vg.w};
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const float2 fo = Unpack2<T>::unpack(wo[k]), fg = Unpack2<T>::unpack(wg[k]);
-                            dsum = fmaf(fo.x, fg.x, dsum);
-                            dsum = fmaf(fo.y, fg.y, dsum);
-                        }
-                    }
+                } else {
+                    // rowsum(P .* dP) = dO_row . O_row, computed beforehand
+                    dsum = rseq < S ? args.dvec[rg] : 0.f;
                 }
             }
             for (int it = 0; it < NPASS * ns; ++it, ++g) {
@@ -568,7 +556,7 @@ struct SddExtra {
     const void* P = nullptr;        // softmax output (backward modes)
     float scale = 0.f;              // softmax scale (backward modes)
     const float* lse = nullptr;     // MODE 3
-    const void* O = nullptr;        // MODE 4
+    const float* dvec = nullptr;    // MODE 4
 };
 
 template <typename T, int BLK, int KP, int MODE>
@@ -596,7 +584,7 @@ int sdd_launch(const bsp_layout_s* Lh, const void* A, const void* B, void* Cout,
         else mp = mc;
     }
     if (rc) return rc;
-    SddArgs a{Lh->view, Cout, Z, K, ta, tb, e.c2, e.kind, e.mask, e.P, e.scale, e.lse, e.O, A};
+    SddArgs a{Lh->view, Cout, Z, K, ta, tb, e.c2, e.kind, e.mask, e.P, e.scale, e.lse, e.dvec};
     auto kern = sdd_tc_kernel<T, BLK, KP, MODE>;
     constexpr int smem = SddCfg<KP, BLK, MODE>::kAlloc;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)

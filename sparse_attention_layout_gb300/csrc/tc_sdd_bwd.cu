@@ -19,12 +19,12 @@ int launch_sdd_softmax_bwd_tc(const bsp_layout_s* L, int dtype, const void* dO, 
 }
 
 int launch_sdd_softmax_bwd_o_tc(const bsp_layout_s* L, int dtype, const void* dO, const void* V, const void* P,
-                                const void* O, void* dX, int Z, int D, float scale, cudaStream_t s) {
+                                const float* dvec, void* dX, int Z, int D, float scale, cudaStream_t s) {
     if (!sdd_tc_shape(L, Z, D, 0, 1) || L->B < 64) return BSP_ERR_UNSUPPORTED;
     SddExtra e;
     e.P = P;
     e.scale = scale;
-    e.O = O;
+    e.dvec = dvec;
     return sdd_by_dtype<4>(L, dtype, dO, V, dX, Z, D, 0, 1, e, s);
 }
 
