@@ -17,6 +17,7 @@
 // global memory (register-resident when the row fits, else an online pass and
 // a normalising pass).
 #include <cfloat>
+#include <type_traits>
 
 #include "common.cuh"
 #include "tc_common.cuh"
@@ -236,107 +237,125 @@ softmax_chunk_kernel(LayoutView L, const T* X, T* Y, float c2, int kind, const u
     if (__syncthreads_and(ok)) {
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
         const int nvec = nq * VPB;
-        for (int rr = warp; rr < R; rr += kChunkThreads / 32) {
+        // raw values of vector v of row rr (the scale is folded into the
+        // exponent), masked -> -inf
+        auto load = [&](int rr, int v, float (&x)[VEC], T*& p) {
             const int r = r0 + rr;           // row inside the block-row
             const int rseq = i * BLK + r;    // row inside the sequence
-            // raw values (the scale is folded into the exponent), masked -> -inf
-            auto load = [&](int v, float (&x)[VEC], T*& p) {
-                const int q = v / VPB, e = v % VPB;
-                p = buf + ((size_t)q * R + rr) * BLK + e * VEC;
-                Vec16<T>::load(p, x);
-                const int col = scol[q] * BLK + e * VEC;
-                if (kind == BSP_MASK_DIAG_CAUSAL) {
-                    if (scol[q] == i) {
-#pragma unroll
-                        for (int k = 0; k < VEC; ++k)
-                            if (e * VEC + k > r) x[k] = -INFINITY;
-                    }
-                } else if (kind == BSP_MASK_DENSE) {
-                    const uint8_t* mp = mask + (int64_t)rseq * L.S + col;
+            const int q = v / VPB, e = v % VPB;
+            p = buf + ((size_t)q * R + rr) * BLK + e * VEC;
+            Vec16<T>::load(p, x);
+            const int col = scol[q] * BLK + e * VEC;
+            if (kind == BSP_MASK_DIAG_CAUSAL) {
+                if (scol[q] == i) {
 #pragma unroll
                     for (int k = 0; k < VEC; ++k)
-                        if (!mp[k]) x[k] = -INFINITY;
+                        if (e * VEC + k > r) x[k] = -INFINITY;
                 }
-            };
-            constexpr int kRegVec = kChunkRegElems / VEC;  // vectors per lane kept in registers
-            if (nvec <= 32 * kRegVec) {
-                // the row in registers: max, then 2^(x c2 - m c2) (one FFMA + one
-                // MUFU per entry), sum, normalise, store -- one pass over shared memory
-                float x[kRegVec][VEC];
-                float m = -INFINITY;
+            } else if (kind == BSP_MASK_DENSE) {
+                const uint8_t* mp = mask + (int64_t)rseq * L.S + col;
 #pragma unroll
-                for (int k = 0; k < kRegVec; ++k) {
-                    if (lane + 32 * k < nvec) {
-                        T* p;
-                        load(lane + 32 * k, x[k], p);
+                for (int k = 0; k < VEC; ++k)
+                    if (!mp[k]) x[k] = -INFINITY;
+            }
+        };
+        constexpr int kRegVec = kChunkRegElems / VEC;  // vectors per lane kept in registers
+        if (nvec <= 32 * kRegVec) {
+            // rows in registers: GS lanes per row (the fewest of 8, 16, 32 that
+            // hold the row), 32 / GS rows per warp, reductions within the lane
+            // group; max, then 2^(x c2 - m c2) (one FFMA + one MUFU per entry),
+            // sum, normalise, store -- one pass over shared memory.  A chunk's
+            // rows all have nvec vectors (one block-row), so GS is uniform.
+            auto rows_in_registers = [&](auto gs_tag) {
+                constexpr int GS = decltype(gs_tag)::value;
+                constexpr int RPW = 32 / GS;
+                const int sub = lane / GS, gl = lane % GS;
+                for (int base = warp * RPW; base < R; base += (kChunkThreads / 32) * RPW) {
+                    const int rr = base + sub;
+                    const int nv = rr < R ? nvec : 0;  // lanes of rows past the chunk hold nothing
+                    float x[kRegVec][VEC];
+                    float m = -INFINITY;
 #pragma unroll
-                        for (int e = 0; e < VEC; ++e) m = fmaxf(m, x[k][e]);
+                    for (int k = 0; k < kRegVec; ++k) {
+                        if (gl + GS * k < nv) {
+                            T* p;
+                            load(rr, gl + GS * k, x[k], p);
+#pragma unroll
+                            for (int e = 0; e < VEC; ++e) m = fmaxf(m, x[k][e]);
+                        }
                     }
-                }
-                m = warp_max(m);
-                const float ms = (m == -INFINITY) ? 0.f : m * c2;
-                float l = 0.f;
 #pragma unroll
-                for (int k = 0; k < kRegVec; ++k) {
-                    if (lane + 32 * k < nvec) {
+                    for (int o = GS >> 1; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                    const float ms = (m == -INFINITY) ? 0.f : m * c2;
+                    float l = 0.f;
 #pragma unroll
-                        for (int e = 0; e < VEC; ++e) {
-                            x[k][e] = tc::ex2_approx(fmaf(x[k][e], c2, -ms));
-                            l += x[k][e];
+                    for (int k = 0; k < kRegVec; ++k) {
+                        if (gl + GS * k < nv) {
+#pragma unroll
+                            for (int e = 0; e < VEC; ++e) {
+                                x[k][e] = tc::ex2_approx(fmaf(x[k][e], c2, -ms));
+                                l += x[k][e];
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int o = GS >> 1; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+                    const float inv = l > 0.f ? 1.0f / l : 0.f;
+#pragma unroll
+                    for (int k = 0; k < kRegVec; ++k) {
+                        const int v = gl + GS * k;
+                        if (v < nv) {
+#pragma unroll
+                            for (int e = 0; e < VEC; ++e) x[k][e] *= inv;
+                            Vec16<T>::store(buf + ((size_t)(v / VPB) * R + rr) * BLK + (v % VPB) * VEC, x[k]);
                         }
                     }
                 }
-                l = warp_sum(l);
-                const float inv = l > 0.f ? 1.0f / l : 0.f;
-#pragma unroll
-                for (int k = 0; k < kRegVec; ++k) {
-                    const int v = lane + 32 * k;
-                    if (v < nvec) {
-#pragma unroll
-                        for (int e = 0; e < VEC; ++e) x[k][e] *= inv;
-                        Vec16<T>::store(buf + ((size_t)(v / VPB) * R + rr) * BLK + (v % VPB) * VEC, x[k]);
+            };
+            if (nvec <= 8 * kRegVec) rows_in_registers(std::integral_constant<int, 8>{});
+            else if (nvec <= 16 * kRegVec) rows_in_registers(std::integral_constant<int, 16>{});
+            else rows_in_registers(std::integral_constant<int, 32>{});
+        } else {
+            for (int rr = warp; rr < R; rr += kChunkThreads / 32) {
+                // long row: online (max, sum) per lane in the scaled log2 domain,
+                // merged across the warp, then a normalising pass
+                float m = -INFINITY, l = 0.f;
+                for (int v = lane; v < nvec; v += 32) {
+                    float x[VEC];
+                    T* p;
+                    load(rr, v, x, p);
+                    float vm = -INFINITY;
+    #pragma unroll
+                    for (int k = 0; k < VEC; ++k) vm = fmaxf(vm, x[k]);
+                    vm *= c2;
+                    if (vm > m) {
+                        l = (m == -INFINITY) ? 0.f : l * tc::ex2_approx(m - vm);
+                        m = vm;
+                    }
+                    if (m != -INFINITY) {
+    #pragma unroll
+                        for (int k = 0; k < VEC; ++k) l += tc::ex2_approx(fmaf(x[k], c2, -m));
                     }
                 }
-                continue;
-            }
-            // long row: online (max, sum) per lane in the scaled log2 domain,
-            // merged across the warp, then a normalising pass
-            float m = -INFINITY, l = 0.f;
-            for (int v = lane; v < nvec; v += 32) {
-                float x[VEC];
-                T* p;
-                load(v, x, p);
-                float vm = -INFINITY;
-#pragma unroll
-                for (int k = 0; k < VEC; ++k) vm = fmaxf(vm, x[k]);
-                vm *= c2;
-                if (vm > m) {
-                    l = (m == -INFINITY) ? 0.f : l * tc::ex2_approx(m - vm);
-                    m = vm;
+    #pragma unroll
+                for (int o = 16; o; o >>= 1) {
+                    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+                    const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+                    const float mn = fmaxf(m, m2);
+                    l = ((m == -INFINITY) ? 0.f : l * tc::ex2_approx(m - mn)) +
+                        ((m2 == -INFINITY) ? 0.f : l2 * tc::ex2_approx(m2 - mn));
+                    m = mn;
                 }
-                if (m != -INFINITY) {
-#pragma unroll
-                    for (int k = 0; k < VEC; ++k) l += tc::ex2_approx(fmaf(x[k], c2, -m));
+                const float inv = l > 0.f ? 1.0f / l : 0.f;
+                const float ms = (m == -INFINITY) ? 0.f : m;
+                for (int v = lane; v < nvec; v += 32) {
+                    float x[VEC];
+                    T* p;
+                    load(rr, v, x, p);
+    #pragma unroll
+                    for (int k = 0; k < VEC; ++k) x[k] = tc::ex2_approx(fmaf(x[k], c2, -ms)) * inv;
+                    Vec16<T>::store(p, x);
                 }
-            }
-#pragma unroll
-            for (int o = 16; o; o >>= 1) {
-                const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-                const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
-                const float mn = fmaxf(m, m2);
-                l = ((m == -INFINITY) ? 0.f : l * tc::ex2_approx(m - mn)) +
-                    ((m2 == -INFINITY) ? 0.f : l2 * tc::ex2_approx(m2 - mn));
-                m = mn;
-            }
-            const float inv = l > 0.f ? 1.0f / l : 0.f;
-            const float ms = (m == -INFINITY) ? 0.f : m;
-            for (int v = lane; v < nvec; v += 32) {
-                float x[VEC];
-                T* p;
-                load(v, x, p);
-#pragma unroll
-                for (int k = 0; k < VEC; ++k) x[k] = tc::ex2_approx(fmaf(x[k], c2, -ms)) * inv;
-                Vec16<T>::store(p, x);
             }
         }
         tc::fence_proxy_async_smem();  // generic-proxy writes -> visible to the bulk copy engine
