@@ -216,7 +216,7 @@ softmax_chunk_kernel(LayoutView L, const T* X, T* Y, float c2, int kind, const u
     const int4 item = reinterpret_cast<const int4*>(L.sm_items[E])[it];
     const int key = item.x, p0 = item.y, nq = item.z;
     const int r0 = item.w & 0xffff, R = item.w >> 16;
-    const int h = key / L.nb, i = key % L.nb;
+    const int i = key % L.nb;  // block-row (the chunk's head is key / nb)
     const uint32_t slice = (uint32_t)R * BLK * sizeof(T);  // bytes of one block's part of the chunk
     T* buf = reinterpret_cast<T*>(smem_raw);
     int* scol = reinterpret_cast<int*>(smem_raw + L.sm_max_bytes[E]);

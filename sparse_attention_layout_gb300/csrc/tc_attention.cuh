@@ -291,9 +291,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const uint64_t dk = smem_desc(smem_u32(smem + SM::kK), 16, 1024, kSw128);
             uint32_t q_it = 0, g = 0;
             for (int it = args.sched_ptr[blockIdx.x], it_end = args.sched_ptr[blockIdx.x + 1]; it < it_end; ++it) {
-                const int4 run = args.sched_items[it];
-            const int tile = run.x;
-                const int ns = run.z;
+                const int ns = args.sched_items[it].z;
                 if (ns == 0) continue;
                 const uint32_t qs = q_it % QST;
                 if (!mbar_wait(&q_full[qs], (q_it / QST) & 1, ab)) goto qk_done;
@@ -323,9 +321,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
             const uint64_t dv = smem_desc(smem_u32(smem + SM::kV), 128 * 128, 1024, kSw128);
             uint32_t g = 0, tc = 0;  // tc: tiles with at least one step so far
             for (int it = args.sched_ptr[blockIdx.x], it_end = args.sched_ptr[blockIdx.x + 1]; it < it_end; ++it) {
-                const int4 run = args.sched_items[it];
-            const int tile = run.x;
-                const int ns = run.z;
+                const int ns = args.sched_items[it].z;
                 if (ns == 0) continue;
                 // the previous tile's O must have been read by the epilogue
                 if (tc > 0 && !mbar_wait(&o_empty, (tc - 1) & 1, ab)) goto pv_done_label;

@@ -293,8 +293,7 @@ spmm_group_kernel(const __grid_constant__ CUtensorMap tmSp, const __grid_constan
         }
     } else {
         // -------------------------------------------------------- epilogue ----
-        const int quad = warp & 3;
-        const int row = quad * 32 + lane;  // slab row = TMEM lane
+        const int quad = warp & 3;  // slab rows 32 quad + lane = TMEM lanes
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         uint8_t* stage = smem + C::kEpi + quad * 4096;
         const uint32_t stage_s = smem_u32(stage);
