@@ -345,15 +345,17 @@ int bsp_attention_backward(bsp_layout_t layout, int dtype, const void* Q, const 
 
 /* Gradients of bsp_attention as bsp_attention_backward, given also the
  * forward's output O and its rows' log-sum-exp lse (bsp_attention_lse, same
- * inputs): P = exp(scale Q K^T - lse) on the layout is rebuilt in one pass
- * (no statistics pass), and rowsum(P .* dP) = rowsum(dO .* O) per row, so
- * dX = scale P .* (dP - rowsum(dO .* O)) also takes one pass.  O, dO: DEVICE
- * [Z][H][S][D]; lse: DEVICE float [Z][H][S], 16-byte aligned; the rest as for
+ * inputs).  With the statistics known, P = exp(scale Q K^T - lse) needs no
+ * statistics pass, and rowsum(P .* dP) = rowsum(dO .* O) per row (O = P V),
+ * so one tensor-core pass over the row tiles computes both products of a
+ * step, S = Q K^T and dP = dO V^T, and writes P and
+ * dX = scale P .* (dP - rowsum(dO .* O)) together (P is not read back); then
+ * dV = P^T dO, dQ = dX K, dK = dX^T Q.  O, dO: DEVICE [Z][H][S][D]; lse:
+ * DEVICE float [Z][H][S], 16-byte aligned; the rest as for
  * bsp_attention_backward; dQ's memory holds the rows' dO . O (fp32) until it
- * receives dQ.  fp32, and shapes the one-pass tensor-core kernels do not
- * cover, take bsp_attention_backward's recomputing chain (O and lse
- * unused).  Not from the pages: the chain rule with the forward's statistics
- * kept. */
+ * receives dQ.  fp32, and shapes the one-pass kernel does not cover, take
+ * bsp_attention_backward's recomputing chain (O and lse unused).  Not from
+ * the pages: the chain rule with the forward's statistics kept. */
 int bsp_attention_backward_lse(bsp_layout_t layout, int dtype, const void* Q, const void* K, const void* V,
                                const void* O, const void* dO, const float* lse, void* dQ, void* dK, void* dV,
                                int Z, int D, float scale, int mask_kind, const uint8_t* mask, void* P_ws,

@@ -275,30 +275,21 @@ extern "C" int bsp_attention_backward_lse(bsp_layout_t L, int dtype, const void*
     if (!aligned16(P_ws) || !aligned16(dP_ws)) return BSP_ERR_ALIGNMENT;
     cudaStream_t s = (cudaStream_t)stream;
     const uint8_t* m = mask_kind == BSP_MASK_DENSE ? mask : nullptr;
-    // P = exp(scale Q K^T - lse) on the layout: one pass
-    rc = bsp::launch_sdd_softmax_lse_tc(L, dtype, Q, K, lse, P_ws, Z, D, scale, mask_kind, m, s);
+    // the rows' dO . O (= rowsum(P .* dP), as O = P V) go to dQ's memory first
+    // (fp32 [Z][H][S] fits in any [Z][H][S][D] tensor of D >= 2); dQ receives
+    // its own values last
+    float* dvec = static_cast<float*>(dQ);
+    if ((rc = bsp::launch_row_dot(dtype, dO, O, dvec, (int64_t)Z * L->H * L->S, D, s))) return rc;
+    // P = exp(scale Q K^T - lse) and dX = scale P .* (dO V^T - dvec) on the
+    // layout: one pass
+    rc = bsp::launch_sdd_attention_bwd_tc(L, dtype, Q, K, dO, V, lse, dvec, P_ws, dP_ws, Z, D, scale, mask_kind, m,
+                                          s);
     if (rc == BSP_ERR_UNSUPPORTED)
         return bsp_attention_backward(L, dtype, Q, K, V, dO, dQ, dK, dV, Z, D, scale, mask_kind, mask, P_ws, dP_ws,
                                       stream);
     if (rc) return rc;
-    // dV = P^T dO
+    // dV = P^T dO,  dQ = dX K,  dK = dX^T Q
     if ((rc = bsp_dsd(L, dtype, P_ws, dO, dV, Z, D, 1, 0, stream))) return rc;
-    // dX = scale P .* (dP - rowsum(dO .* O)), dP = dO V^T: one pass (blocks of
-    // 64 and 128), else dP through memory and the softmax backward in place.
-    // The rows' dO . O go to dQ's memory first (fp32 [Z][H][S] fits in any
-    // [Z][H][S][D] tensor of D >= 2); dQ receives its own values last.
-    rc = BSP_ERR_UNSUPPORTED;
-    if (L->B >= 64) {
-        float* dvec = static_cast<float*>(dQ);
-        if ((rc = bsp::launch_row_dot(dtype, dO, O, dvec, (int64_t)Z * L->H * L->S, D, s))) return rc;
-        rc = bsp::launch_sdd_softmax_bwd_o_tc(L, dtype, dO, V, P_ws, dvec, dP_ws, Z, D, scale, s);
-    }
-    if (rc == BSP_ERR_UNSUPPORTED) {
-        if ((rc = bsp_sdd(L, dtype, dO, V, dP_ws, Z, D, 0, 1, stream))) return rc;
-        rc = bsp_softmax_backward(L, dtype, P_ws, dP_ws, dP_ws, Z, scale, stream);
-    }
-    if (rc) return rc;
-    // dQ = dX K,  dK = dX^T Q
     if ((rc = bsp_dsd(L, dtype, dP_ws, K, dQ, Z, D, 0, 0, stream))) return rc;
     return bsp_dsd(L, dtype, dP_ws, Q, dK, Z, D, 1, 0, stream);
 }

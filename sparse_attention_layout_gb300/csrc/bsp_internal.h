@@ -152,14 +152,11 @@ int launch_sdd_softmax_tc(const bsp_layout_s* L, int dtype, const void* A, const
 // (fused SDD + softmax backward; 16-bit types, tensor-core shapes only)
 int launch_sdd_softmax_bwd_tc(const bsp_layout_s* L, int dtype, const void* dO, const void* V, const void* P,
                               void* dX, int Z, int D, float scale, cudaStream_t s);
-// P = exp(scale Q K^T - lse) on the layout and mask, from the rows'
-// log-sum-exp of the forward (one pass; 16-bit types, tensor-core shapes)
-int launch_sdd_softmax_lse_tc(const bsp_layout_s* L, int dtype, const void* Q, const void* K, const float* lse,
-                              void* P, int Z, int D, float scale, int kind, const uint8_t* mask, cudaStream_t s);
-// dX as launch_sdd_softmax_bwd_tc with rowsum(P .* dP) = rowsum(dO .* O)
-// given per row in dvec [Z][H][S] (one pass)
-int launch_sdd_softmax_bwd_o_tc(const bsp_layout_s* L, int dtype, const void* dO, const void* V, const void* P,
-                                const float* dvec, void* dX, int Z, int D, float scale, cudaStream_t s);
+// P = exp(scale Q K^T - lse) and dX = scale P .* (dO V^T - dvec) on the layout,
+// one pass (tensor cores; BSP_ERR_UNSUPPORTED outside their shapes)
+int launch_sdd_attention_bwd_tc(const bsp_layout_s* L, int dtype, const void* Q, const void* K, const void* dO,
+                                const void* V, const float* lse, const float* dvec, void* P, void* dX, int Z, int D,
+                                float scale, int kind, const uint8_t* mask, cudaStream_t s);
 // out[r] = sum_d A[r][d] B[r][d] (fp32) for rows of D elements (D a multiple of 8)
 int launch_row_dot(int dtype, const void* A, const void* B, float* out, int64_t rows, int D, cudaStream_t s);
 int launch_dsd_group_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z,

@@ -24,15 +24,4 @@ int launch_sdd_softmax_tc(const bsp_layout_s* L, int dtype, const void* A, const
     return sdd_by_dtype<1>(L, dtype, A, B, P, Z, K, ta, tb, e, s);
 }
 
-int launch_sdd_softmax_lse_tc(const bsp_layout_s* L, int dtype, const void* Q, const void* K, const float* lse,
-                              void* P, int Z, int D, float scale, int kind, const uint8_t* mask, cudaStream_t s) {
-    if (!sdd_tc_shape(L, Z, D, 0, 1)) return BSP_ERR_UNSUPPORTED;
-    SddExtra e;
-    e.c2 = scale * kLog2e;
-    e.kind = kind;
-    e.mask = mask;
-    e.lse = lse;
-    return sdd_by_dtype<3>(L, dtype, Q, K, P, Z, D, 0, 1, e, s);
-}
-
 }  // namespace bsp

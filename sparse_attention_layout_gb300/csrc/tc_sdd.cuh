@@ -6,8 +6,9 @@
 // the 128 x 128 score tile against G = 128/B key blocks into one of four TMEM
 // accumulators; eight epilogue warps write the present blocks while the MMA
 // works ahead.  The kernel template and its launch helpers live here; the
-// plain and softmax modes are instantiated in tc_sdd.cu, the backward modes in
-// tc_sdd_bwd.cu (separate translation units compile in parallel).
+// plain and softmax modes are instantiated in tc_sdd.cu, the fused softmax
+// backward in tc_sdd_bwd.cu and the attention backward's one-pass mode in
+// tc_sdd_attn_bwd.cu (separate translation units compile in parallel).
 //
 // Operand orientation: op(A) rows and op(B) columns are what the tiles hold.
 // trans_a = 0 / trans_b = 1 store them as rows ([S][K]: K-major tiles, 64-column
@@ -44,11 +45,15 @@
 // second recomputes dP and writes dX.  dP never reaches memory and stays in
 // fp32; masked entries have P = 0 and so dX = 0.
 //
-// One-pass variants, given what the forward already knows: MODE 3 writes
-// P = exp(scale s - lse) from the rows' log-sum-exp of the forward (no
-// statistics pass); MODE 4 writes dX with rowsum(P .* dP) = dO_row . O_row
-// taken from a vector computed beforehand from the forward's output O (no
-// accumulation pass).
+// DUO (MODE 3, the attention backward given what the forward already knows):
+// every step runs two products, S = Q K^T and dP = dO V^T, into a pair of
+// TMEM accumulators (two pairs, 4 x 128 columns), and the epilogue writes
+// both P = exp(scale S - lse), from the rows' log-sum-exp of the forward (no
+// statistics pass), and dX = scale P .* (dP - dO_row . O_row), with
+// rowsum(P .* dP) = dO_row . O_row (O = P V) taken from a vector computed
+// beforehand (no accumulation pass).  P goes out from registers and is never
+// read back.  The query-side tiles (Q, dO) share one stage and the key-side
+// tiles (K, V) two.
 #pragma once
 
 #include <algorithm>
@@ -79,10 +84,11 @@ struct SddArgs {
     // fused softmax backward only: the softmax output [Z][nnz][B][B] and the scale
     const void* P;
     float scale;
-    // one-pass modes: the rows' log-sum-exp [Z][H][S] (natural log) of the
-    // forward (MODE 3), the rows' rowsum(dO .* O) [Z][H][S] (MODE 4)
+    // DUO: the rows' log-sum-exp [Z][H][S] (natural log) of the forward and
+    // their rowsum(dO .* O) [Z][H][S]; P, written beside dX (which goes to C)
     const float* lse;
     const float* dvec;
+    void* C2;
 };
 
 __host__ __device__ constexpr uint32_t swz_of(int row_bytes) {
@@ -96,35 +102,42 @@ __host__ __device__ constexpr uint32_t swz_of(int row_bytes) {
 // epilogue is what a step waits for.
 template <int KP, int BLK, int MODE>
 struct SddCfg {
-    static constexpr bool SMB = MODE == 2 || MODE == 4;
+    static constexpr bool SMB = MODE == 2;
+    static constexpr bool DUO = MODE == 3;  // two products per step
     static constexpr int kTile = 128 * 64 * KP * 2;  // 128 rows x K (KP panels of 64)
-    static constexpr int AST = SMB ? 1 : 2;  // query-tile stages
-    // key-tile stages: three, except in the backward mode (two stages of V
-    // and P); at K = 128 the fused softmax makes room for the third with one
-    // staging buffer per epilogue warp (its per-tile exchange arrays take the
-    // rest)
-    static constexpr int BST = SMB ? 2 : 3;
+    static constexpr int AST = (SMB || DUO) ? 1 : 2;  // query-tile stages
+    // key-tile stages: three, except in the backward modes (two stages of V
+    // and P, or of K and V); at K = 128 the fused softmax makes room for the
+    // third with one staging buffer per epilogue warp (its per-tile exchange
+    // arrays take the rest)
+    static constexpr int BST = (SMB || DUO) ? 2 : 3;
     static constexpr int kPT = SMB ? 32768 : 0;  // P tile of a key-tile stage
-    static constexpr int kBStage = kTile + kPT;
+    static constexpr int kAStage = DUO ? 2 * kTile : kTile;  // Q (and dO)
+    static constexpr int kBStage = DUO ? 2 * kTile : kTile + kPT;  // K (and V, or P)
     static constexpr int kA = 0;
-    static constexpr int kB = AST * kTile;
+    static constexpr int kB = AST * kAStage;
     static constexpr int kStg = kB + BST * kBStage;  // staging: NBUF buffers per epilogue warp
-    static constexpr int NBUF = (SMB || (MODE == 1 && KP == 2)) ? 1 : 2;
+    static constexpr int NBUF = (SMB || (MODE == 1 && KP == 2) || (DUO && KP == 2)) ? 1 : 2;
+    // TMEM accumulators: four of 128 columns, or two pairs (S, dP)
+    static constexpr int NACC = DUO ? 2 : 4;
     static constexpr int kBuf = 32 * (BLK < 64 ? BLK : 64) * 2;  // a warp's 32 rows of one piece
     static constexpr int kAlloc = kStg + 8 * NBUF * kBuf + 1024;
 };
 
 // MODE: 0 plain SDD; 1 fused softmax (SMX, two passes); 2 fused softmax
-// backward (SMB, two passes); 3 fused softmax with the rows' log-sum-exp given
-// (one pass); 4 fused softmax backward with rowsum(P .* dP) = rowsum(dO .* O)
-// from the forward's output (one pass)
+// backward (SMB, two passes); 3 attention backward from the forward's
+// statistics (DUO, one pass: A = Q, A2 = dO, B = K, B2 = V; C = dX, C2 = P)
 template <typename T, int BLK, int KP, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-              const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP, const SddArgs args) {
+              const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
+              const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2, const SddArgs args) {
     using C = SddCfg<KP, BLK, MODE>;
     constexpr int G = 128 / BLK;
     constexpr int AST = C::AST, BST = C::BST;
+    constexpr bool DUO = C::DUO;
+    constexpr int NACC = C::NACC;
+    constexpr uint32_t kAccCols = 512 / NACC;  // TMEM columns per accumulator (pair)
     constexpr uint32_t kTileBytes = C::kTile;
     // MN-major key tiles: panels of W keys (RB bytes per K row), KPB per block
     constexpr int W = BLK < 64 ? BLK : 64, RB = 2 * W, KPB = BLK / W;
@@ -132,14 +145,15 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     const bool a_mn = args.ta != 0, b_mn = args.tb == 0;
     // bytes one stage's copies deliver: K-major boxes are 64 * KP columns wide
     // (zero-filled past K), MN-major ones exactly K rows
-    const uint32_t a_bytes = a_mn ? 256u * kd : kTileBytes, b_bytes = b_mn ? 256u * kd : kTileBytes;
-    constexpr bool SMX = MODE == 1 || MODE == 3, SMB = MODE == 2 || MODE == 4;
+    const uint32_t a_bytes = (a_mn ? 256u * kd : kTileBytes) * (DUO ? 2u : 1u);
+    const uint32_t b_bytes = (b_mn ? 256u * kd : kTileBytes) * (DUO ? 2u : 1u);
+    constexpr bool SMX = MODE == 1 || DUO, SMB = MODE == 2;
     constexpr bool XCH = MODE == 1 || MODE == 2;  // two passes, row statistics exchanged between them
     constexpr int NPASS = XCH ? 2 : 1;            // passes over a tile's steps
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    __shared__ uint64_t a_full[AST], a_empty[AST], b_full[BST], b_empty[BST], s_full[4], s_empty[4];
+    __shared__ uint64_t a_full[AST], a_empty[AST], b_full[BST], b_empty[BST], s_full[NACC], s_empty[NACC];
     // fused modes: the two halves of every row exchange their statistics once
     // per tile (the two warps of lane quadrant q: xq[q]; values in xs)
     __shared__ uint64_t xq[4];
@@ -164,7 +178,7 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             mbar_init(&b_full[i], 1);
             mbar_init(&b_empty[i], SMB ? 9 : 1);  // SMB: the eight epilogue warps also read the stage's P
         }
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < NACC; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&s_empty[i], 8);
         }
@@ -187,6 +201,10 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         if (lane == 0) {
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
+            if constexpr (DUO) {
+                tma_prefetch_desc(&tmA2);
+                tma_prefetch_desc(&tmB2);
+            }
             uint32_t a_it = 0, g = 0;
             for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
                 const int4 run = tile_run_at(L, w, args.Z);
@@ -202,12 +220,16 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 if (a_mn) {
                     // [K rows][128 query columns]: two panels of 64 columns
                     for (int p = 0; p < 2; ++p)
-                        tma_load_2d(smem_u32(smem + C::kA + as * kTileBytes + p * (kd * 128)), &tmA,
+                        tma_load_2d(smem_u32(smem + C::kA + as * C::kAStage + p * (kd * 128)), &tmA,
                                     gq * 128 + 64 * p, (int32_t)(zh * kd), &a_full[as]);
                 } else {
-                    for (int p = 0; p < KP; ++p)
-                        tma_load_2d(smem_u32(smem + C::kA + as * kTileBytes + p * 16384), &tmA, p * 64,
+                    for (int p = 0; p < KP; ++p) {
+                        tma_load_2d(smem_u32(smem + C::kA + as * C::kAStage + p * 16384), &tmA, p * 64,
                                     (int32_t)(zh * S + gq * 128), &a_full[as]);
+                        if constexpr (DUO)  // dO beside Q
+                            tma_load_2d(smem_u32(smem + C::kA + as * C::kAStage + kTileBytes + p * 16384), &tmA2,
+                                        p * 64, (int32_t)(zh * S + gq * 128), &a_full[as]);
+                    }
                 }
                 ++a_it;
                 for (int it = 0; it < NPASS * ns; ++it, ++g) {
@@ -233,9 +255,14 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                                 tma_load_2d(smem_u32(smem + C::kB + st * C::kBStage + (b * KPB + p) * (kd * RB)),
                                             &tmB, c * BLK + W * p, (int32_t)(zh * kd), &b_full[st]);
                         } else {
-                            for (int p = 0; p < KP; ++p)
+                            for (int p = 0; p < KP; ++p) {
                                 tma_load_2d(smem_u32(smem + C::kB + st * C::kBStage + p * 16384 + b * BLK * 128),
                                             &tmB, p * 64, (int32_t)(zh * S + (int64_t)c * BLK), &b_full[st]);
+                                if constexpr (DUO)  // V beside K
+                                    tma_load_2d(smem_u32(smem + C::kB + st * C::kBStage + kTileBytes + p * 16384 +
+                                                         b * BLK * 128),
+                                                &tmB2, p * 64, (int32_t)(zh * S + (int64_t)c * BLK), &b_full[st]);
+                            }
                         }
                     }
                     if constexpr (SMB) {
@@ -274,19 +301,25 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 const uint32_t as = a_it % AST;
                 if (!mbar_wait(&a_full[as], (a_it / AST) & 1, ab)) goto mma_done;
                 for (int it = 0; it < NPASS * ns; ++it, ++g) {
-                    const uint32_t sb = g & 3, st = g % BST;  // TMEM accumulator, key-tile stage
-                    if (!mbar_wait(&s_empty[sb], ((g >> 2) & 1) ^ 1, ab)) goto mma_done;
+                    const uint32_t sb = g % NACC, st = g % BST;  // TMEM accumulator, key-tile stage
+                    if (!mbar_wait(&s_empty[sb], ((g / NACC) & 1) ^ 1, ab)) goto mma_done;
                     if (!mbar_wait(&b_full[st], (g / BST) & 1, ab)) goto mma_done;
                     tc_fence_after();
-                    const uint32_t abase = smem_u32(smem + C::kA + as * kTileBytes);
+                    const uint32_t abase = smem_u32(smem + C::kA + as * C::kAStage);
                     const uint32_t bbase = smem_u32(smem + C::kB + st * C::kBStage);
-                    for (int ks = 0; ks < nks; ++ks) {
-                        const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;  // K-major step
-                        const uint64_t da = a_mn ? smem_desc(abase + ks * 2048, kd * 128, 1024, kSw128)
-                                                 : smem_desc(abase + off, 16, 1024, kSw128);
-                        const uint64_t db = b_mn ? smem_desc(bbase + ks * 16 * RB, kd * RB, 8 * RB, swz_of(RB))
-                                                 : smem_desc(bbase + off, 16, 1024, kSw128);
-                        mma_f16(tS + sb * 128, da, db, idesc, ks > 0 ? 1u : 0u);
+                    // DUO: S = Q K^T into the pair's first 128 columns, then
+                    // dP = dO V^T (the stages' second tiles) into the next 128
+#pragma unroll
+                    for (int pr = 0; pr < (DUO ? 2 : 1); ++pr) {
+                        const uint32_t ab0 = abase + pr * kTileBytes, bb0 = bbase + pr * kTileBytes;
+                        for (int ks = 0; ks < nks; ++ks) {
+                            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;  // K-major step
+                            const uint64_t da = a_mn ? smem_desc(ab0 + ks * 2048, kd * 128, 1024, kSw128)
+                                                     : smem_desc(ab0 + off, 16, 1024, kSw128);
+                            const uint64_t db = b_mn ? smem_desc(bb0 + ks * 16 * RB, kd * RB, 8 * RB, swz_of(RB))
+                                                     : smem_desc(bb0 + off, 16, 1024, kSw128);
+                            mma_f16(tS + sb * kAccCols + pr * 128, da, db, idesc, ks > 0 ? 1u : 0u);
+                        }
                     }
                     mma_commit(&s_full[sb]);
                     mma_commit(&b_empty[st]);
@@ -322,7 +355,10 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         const int seg = lane / RS, rin = lane % RS;
         uint8_t* stg = smem + C::kStg + (warp - 2) * NBUF * C::kBuf;
         T* Cp = reinterpret_cast<T*>(args.C);
-        if (lane == 0) tma_prefetch_desc(&tmC);
+        if (lane == 0) {
+            tma_prefetch_desc(&tmC);
+            if constexpr (DUO) tma_prefetch_desc(&tmP);
+        }
         uint32_t g = 0, uses = 0, xc = 0;  // xc: row-statistics exchanges so far
         for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
             const int4 run = tile_run_at(L, w, args.Z);
@@ -334,36 +370,36 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             const int gq = tile % L.ngroups, rb = gq * G + a, r_in = row % BLK;
             float m = -INFINITY, l = 0.f, msub = 0.f, inv = 0.f;
             float dsum = 0.f;
-            if constexpr (MODE == 3 || MODE == 4) {
+            if constexpr (DUO) {
                 // this row's place in [Z][H][S]; rows past the sequence end are
-                // never written
+                // never written.  P = 2^(c s - lse / ln 2): a row with nothing
+                // kept (lse = -inf) has every score masked and gets 0;
+                // rowsum(P .* dP) = dO_row . O_row, computed beforehand
                 const int rseq = gq * 128 + row;
                 const int64_t rg = ((int64_t)z * L.H + tile / L.ngroups) * S + rseq;
-                if constexpr (MODE == 3) {
-                    // P = 2^(c s - lse / ln 2): a row with nothing kept (lse =
-                    // -inf) has every score masked and gets 0
-                    const float lse2 = rseq < S ? args.lse[rg] * kLog2e : -INFINITY;
-                    msub = lse2 == -INFINITY ? 0.f : lse2;
-                    inv = lse2 == -INFINITY ? 0.f : 1.f;
-                } else {
-                    // rowsum(P .* dP) = dO_row . O_row, computed beforehand
-                    dsum = rseq < S ? args.dvec[rg] : 0.f;
-                }
+                const float lse2 = rseq < S ? args.lse[rg] * kLog2e : -INFINITY;
+                msub = lse2 == -INFINITY ? 0.f : lse2;
+                inv = lse2 == -INFINITY ? 0.f : 1.f;
+                dsum = rseq < S ? args.dvec[rg] : 0.f;
             }
             for (int it = 0; it < NPASS * ns; ++it, ++g) {
                 const int n = it % ns, s = s0 + n;
                 const bool write = !XCH || it >= ns;  // the pass that writes
-                const uint32_t sb = g & 3;
-                bool ok = mbar_wait(&s_full[sb], (g >> 2) & 1, ab);
+                const uint32_t sb = g % NACC;
+                bool ok = mbar_wait(&s_full[sb], (g / NACC) & 1, ab);
                 if (!__all_sync(0xffffffffu, ok)) goto epi_done;
                 tc_fence_after();
+                const uint32_t tacc = tS + sb * kAccCols + lane_base + 64 * hf;
                 uint32_t x[64];
-                tmem_ld32_sync(tS + sb * 128 + lane_base + 64 * hf, *reinterpret_cast<uint32_t(*)[32]>(x));
-                tmem_ld32_sync(tS + sb * 128 + lane_base + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
-                // the accumulator is free once both halves are in registers
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s_empty[sb]);
+                tmem_ld32_sync(tacc, *reinterpret_cast<uint32_t(*)[32]>(x));
+                tmem_ld32_sync(tacc + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
+                if constexpr (!DUO) {
+                    // the accumulator is free once both halves are in registers
+                    // (DUO: once dP is in registers too, below)
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&s_empty[sb]);
+                }
                 float* xf = reinterpret_cast<float*>(x);
                 // the pieces of this half: slot and block id of (row block a, slot)
                 int pblk[NPH];
@@ -479,50 +515,74 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     for (int j = 0; j < 64; ++j) xf[j] = ex2_approx(fmaf(xf[j], args.c2, -msub)) * inv;
                 }
 
+                // stage this warp's rows of every present piece of v (pairs of
+                // 16-bit values) and copy them to the output rows of map (base:
+                // the same rows, for the contiguous copies of blocks under 64)
+                auto store = [&](const uint32_t (&v)[32], const CUtensorMap* map, T* base) {
 #pragma unroll
-                for (int p = 0; p < NPH; ++p) {
-                    const int blk = pblk[p];
-                    if (__all_sync(0xffffffffu, blk < 0)) continue;
-                    int sblk[32 / RS];
+                    for (int p = 0; p < NPH; ++p) {
+                        const int blk = pblk[p];
+                        if (__all_sync(0xffffffffu, blk < 0)) continue;
+                        int sblk[32 / RS];
 #pragma unroll
-                    for (int sg = 0; sg < 32 / RS; ++sg) sblk[sg] = __shfl_sync(0xffffffffu, blk, sg * RS);
-                    uint8_t* buf = stg + (uses % NBUF) * C::kBuf;
-                    if (lane == 0) {  // the copy that last read this buffer has read it
-                        if constexpr (NBUF == 2) bulk_wait_read<1>();
-                        else bulk_wait_read<0>();
-                    }
-                    __syncwarp();
-                    if (blk >= 0) {
-                        uint8_t* rbase = buf + seg * kSeg + rin * RBY;
-#pragma unroll
-                        for (int j = 0; j < C16; ++j) {
-                            const int o = p * CW + 8 * j;
-                            const int pos = CW == 64 ? (j ^ (rin & 7)) : j;
-                            *reinterpret_cast<uint4*>(rbase + pos * 16) = make_uint4(
-                                Pack2<T>::pack(__uint_as_float(x[o]), __uint_as_float(x[o + 1])),
-                                Pack2<T>::pack(__uint_as_float(x[o + 2]), __uint_as_float(x[o + 3])),
-                                Pack2<T>::pack(__uint_as_float(x[o + 4]), __uint_as_float(x[o + 5])),
-                                Pack2<T>::pack(__uint_as_float(x[o + 6]), __uint_as_float(x[o + 7])));
+                        for (int sg = 0; sg < 32 / RS; ++sg) sblk[sg] = __shfl_sync(0xffffffffu, blk, sg * RS);
+                        uint8_t* buf = stg + (uses % NBUF) * C::kBuf;
+                        if (lane == 0) {  // the copy that last read this buffer has read it
+                            if constexpr (NBUF == 2) bulk_wait_read<1>();
+                            else bulk_wait_read<0>();
                         }
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
+                        __syncwarp();
+                        if (blk >= 0) {
+                            uint8_t* rbase = buf + seg * kSeg + rin * RBY;
 #pragma unroll
-                        for (int sg = 0; sg < 32 / RS; ++sg) {
-                            if (sblk[sg] < 0) continue;
-                            const int r_in0 = (quad * 32 + sg * RS) % BLK;
-                            const int64_t orow = ((int64_t)z * L.nnz + sblk[sg]) * BLK + r_in0;
-                            if (BLK >= 64)
-                                tma_store_3d(&tmC, smem_u32(buf + sg * kSeg), (64 * hf + p * CW) % BLK, (int32_t)orow,
-                                             0);
-                            else
-                                bulk_store(Cp + orow * BLK, smem_u32(buf + sg * kSeg), kSeg);
+                            for (int j = 0; j < C16; ++j) {
+                                const int o = (p * CW + 8 * j) / 2;
+                                const int pos = CW == 64 ? (j ^ (rin & 7)) : j;
+                                *reinterpret_cast<uint4*>(rbase + pos * 16) =
+                                    make_uint4(v[o], v[o + 1], v[o + 2], v[o + 3]);
+                            }
                         }
-                        bulk_commit();
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+#pragma unroll
+                            for (int sg = 0; sg < 32 / RS; ++sg) {
+                                if (sblk[sg] < 0) continue;
+                                const int r_in0 = (quad * 32 + sg * RS) % BLK;
+                                const int64_t orow = ((int64_t)z * L.nnz + sblk[sg]) * BLK + r_in0;
+                                if (BLK >= 64)
+                                    tma_store_3d(map, smem_u32(buf + sg * kSeg), (64 * hf + p * CW) % BLK,
+                                                 (int32_t)orow, 0);
+                                else
+                                    bulk_store(base + orow * BLK, smem_u32(buf + sg * kSeg), kSeg);
+                            }
+                            bulk_commit();
+                        }
+                        ++uses;
                     }
-                    ++uses;
+                };
+                uint32_t pk[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) pk[j] = Pack2<T>::pack(xf[2 * j], xf[2 * j + 1]);
+                if constexpr (DUO) {
+                    // P out first; then this half row of dP, which frees the
+                    // accumulator pair, and dX = scale P .* (dP - dO_row . O_row)
+                    // from the rounded P (0 where masked)
+                    store(pk, &tmP, reinterpret_cast<T*>(args.C2));
+                    uint32_t y[64];
+                    tmem_ld32_sync(tacc + 128, *reinterpret_cast<uint32_t(*)[32]>(y));
+                    tmem_ld32_sync(tacc + 160, *reinterpret_cast<uint32_t(*)[32]>(y + 32));
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&s_empty[sb]);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float2 pf = Unpack2<T>::unpack(pk[j]);
+                        pk[j] = Pack2<T>::pack(args.scale * pf.x * (__uint_as_float(y[2 * j]) - dsum),
+                                               args.scale * pf.y * (__uint_as_float(y[2 * j + 1]) - dsum));
+                    }
                 }
+                store(pk, &tmC, Cp);
             }
         }
     epi_done:
@@ -536,7 +596,7 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         if (threadIdx.x == 0) {
             mbar_drain_ring(a_full, AST, issued[0], ab);
             mbar_drain_ring(b_full, BST, issued[1], ab);
-            if (issued[2]) mbar_drain(&s_full[(issued[2] - 1) & 3], ((issued[2] - 1) >> 2) & 1, ab);
+            if (issued[2]) mbar_drain(&s_full[(issued[2] - 1) % NACC], ((issued[2] - 1) / NACC) & 1, ab);
         }
         __syncthreads();
     }
@@ -555,8 +615,11 @@ struct SddExtra {
     const uint8_t* mask = nullptr;  // dense keep-mask (softmax modes)
     const void* P = nullptr;        // softmax output (backward modes)
     float scale = 0.f;              // softmax scale (backward modes)
-    const float* lse = nullptr;     // MODE 3
-    const float* dvec = nullptr;    // MODE 4
+    const float* lse = nullptr;     // DUO: the forward's log-sum-exp
+    const float* dvec = nullptr;    // DUO: rowsum(dO .* O)
+    const void* A2 = nullptr;       // DUO: dO (A is Q)
+    const void* B2 = nullptr;       // DUO: V (B is K)
+    void* C2 = nullptr;             // DUO: P (C is dX)
 };
 
 template <typename T, int BLK, int KP, int MODE>
@@ -565,7 +628,7 @@ int sdd_launch(const bsp_layout_s* Lh, const void* A, const void* B, void* Cout,
     const int bf = std::is_same<T, __nv_bfloat16>::value;
     const uint64_t ZH = (uint64_t)Z * Lh->H, rows = ZH * Lh->S;
     constexpr int W = BLK < 64 ? BLK : 64;
-    CUtensorMap ma, mb, mc, mp;
+    CUtensorMap ma, mb, mc, mp, ma2, mb2;
     // [S][K] operands: boxes of 128 (A) or B (B) rows x 64 columns; [K][S]
     // operands: boxes of K rows x 64 (A) or W (B) columns
     int rc = ta ? make_tmap_2d(&ma, A, bf, ZH * K, Lh->S, K, 64, 128) : make_tmap_2d(&ma, A, bf, rows, K, 128, 64, 128);
@@ -579,19 +642,32 @@ int sdd_launch(const bsp_layout_s* Lh, const void* A, const void* B, void* Cout,
     // fused softmax backward: P rows [Z * nnz * B][B], boxes of B rows x 64
     // columns, 128-byte swizzle (the other modes never read this map)
     if (!rc) {
-        if constexpr (MODE == 2 || MODE == 4)
+        if constexpr (MODE == 2)
             rc = make_tmap_2d(&mp, e.P, bf, (uint64_t)Z * Lh->nnz * BLK, BLK, BLK, 64, 128);
+        else if constexpr (MODE == 3)  // P is written like C
+            rc = make_tmap_3d(&mp, e.C2, bf, BLK, (uint64_t)Z * Lh->nnz * BLK, 1, W, BLK < 32 ? BLK : 32,
+                              BLK >= 64 ? 128 : 0);
         else mp = mc;
     }
+    // MODE 3: dO and V, [S][K] like Q and K
+    if (!rc) {
+        if constexpr (MODE == 3) {
+            rc = make_tmap_2d(&ma2, e.A2, bf, rows, K, 128, 64, 128);
+            if (!rc) rc = make_tmap_2d(&mb2, e.B2, bf, rows, K, BLK, 64, 128);
+        } else {
+            ma2 = ma;
+            mb2 = mb;
+        }
+    }
     if (rc) return rc;
-    SddArgs a{Lh->view, Cout, Z, K, ta, tb, e.c2, e.kind, e.mask, e.P, e.scale, e.lse, e.dvec};
+    SddArgs a{Lh->view, Cout, Z, K, ta, tb, e.c2, e.kind, e.mask, e.P, e.scale, e.lse, e.dvec, e.C2};
     auto kern = sdd_tc_kernel<T, BLK, KP, MODE>;
     constexpr int smem = SddCfg<KP, BLK, MODE>::kAlloc;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return BSP_ERR_CUDA;
     const int64_t total = (int64_t)Z * Lh->n_tiles;
     const int grid = (int)std::min<int64_t>(total, sm_count());
-    kern<<<grid, kThreads, smem, s>>>(ma, mb, mc, mp, a);
+    kern<<<grid, kThreads, smem, s>>>(ma, mb, mc, mp, ma2, mb2, a);
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }
 
@@ -602,11 +678,12 @@ int sdd_by_k(const bsp_layout_s* L, const void* A, const void* B, void* C, int Z
     return sdd_launch<T, BLK, 2, MODE>(L, A, B, C, Z, K, ta, tb, e, s);
 }
 
-// the backward modes read P in 64-key panels: blocks of 64 and 128 only
+// the fused softmax backward reads P in 64-key panels: blocks of 64 and 128
+// only
 template <typename T, int MODE>
 int sdd_by_block(const bsp_layout_s* L, const void* A, const void* B, void* C, int Z, int K, int ta, int tb,
                  const SddExtra& e, cudaStream_t s) {
-    constexpr bool small_ok = !(MODE == 2 || MODE == 4);
+    constexpr bool small_ok = MODE != 2;
     switch (L->B) {
         case 16:
             if constexpr (small_ok) return sdd_by_k<T, 16, MODE>(L, A, B, C, Z, K, ta, tb, e, s);
