@@ -145,36 +145,54 @@ int bwd_t(const bsp_layout_s* L, const void* Y, const void* dY, void* dX, int Z,
 }
 
 // out[r] = sum_d A[r][d] B[r][d] in fp32 (the rowsum(dO .* O) of the attention
-// backward): one warp per row, 16-byte loads, grid-stride over the rows.
-template <typename T>
+// backward): LPR lanes per row (the row's 16-byte chunks, at most 32), 32 / LPR
+// rows per warp, grid-stride over groups of rows.
+template <typename T, int LPR>
 __global__ void __launch_bounds__(256) row_dot_kernel(const T* __restrict__ A, const T* __restrict__ B,
                                                       float* __restrict__ out, int64_t rows, int D) {
     constexpr int E = 16 / sizeof(T);  // elements per 16-byte load
-    const int lane = threadIdx.x & 31;
+    constexpr int RPW = 32 / LPR;      // rows per warp
+    const int lane = threadIdx.x & 31, sub = lane % LPR;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
-        const T* a = A + r * D;
-        const T* b = B + r * D;
+    for (int64_t r0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * RPW; r0 < rows;
+         r0 += warps * RPW) {
+        const int64_t r = r0 + lane / LPR;
         float acc = 0.f;
-        for (int d = lane * E; d < D; d += 32 * E) {
-            float fa[E], fb[E];
-            Vec16<T>::load(a + d, fa);
-            Vec16<T>::load(b + d, fb);
+        if (r < rows) {
+            const T* a = A + r * D;
+            const T* b = B + r * D;
+            for (int d = sub * E; d < D; d += LPR * E) {
+                float fa[E], fb[E];
+                Vec16<T>::load(a + d, fa);
+                Vec16<T>::load(b + d, fb);
 #pragma unroll
-            for (int k = 0; k < E; ++k) acc = fmaf(fa[k], fb[k], acc);
+                for (int k = 0; k < E; ++k) acc = fmaf(fa[k], fb[k], acc);
+            }
         }
+        // every lane of the warp reaches the shuffles (r0 is warp-uniform)
 #pragma unroll
-        for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) out[r] = acc;
+        for (int o = LPR / 2; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (r < rows && sub == 0) out[r] = acc;
     }
+}
+
+template <typename T, int LPR>
+int row_dot_launch(const void* A, const void* B, float* out, int64_t rows, int D, cudaStream_t s) {
+    constexpr int RPB = 256 / LPR;  // rows per block
+    const int64_t blocks = std::min<int64_t>((rows + RPB - 1) / RPB, (int64_t)sm_count() * 16);
+    row_dot_kernel<T, LPR><<<(unsigned)blocks, 256, 0, s>>>((const T*)A, (const T*)B, out, rows, D);
+    return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }
 
 template <typename T>
 int row_dot_t(const void* A, const void* B, float* out, int64_t rows, int D, cudaStream_t s) {
     if (rows == 0) return BSP_OK;
-    const int64_t blocks = std::min<int64_t>((rows + 7) / 8, (int64_t)sm_count() * 16);
-    row_dot_kernel<T><<<(unsigned)blocks, 256, 0, s>>>((const T*)A, (const T*)B, out, rows, D);
-    return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
+    const int chunks = D / (int)(16 / sizeof(T));  // 16-byte chunks per row
+    if (chunks <= 2) return row_dot_launch<T, 2>(A, B, out, rows, D, s);
+    if (chunks <= 4) return row_dot_launch<T, 4>(A, B, out, rows, D, s);
+    if (chunks <= 8) return row_dot_launch<T, 8>(A, B, out, rows, D, s);
+    if (chunks <= 16) return row_dot_launch<T, 16>(A, B, out, rows, D, s);
+    return row_dot_launch<T, 32>(A, B, out, rows, D, s);
 }
 
 }  // namespace

@@ -382,9 +382,29 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 inv = lse2 == -INFINITY ? 0.f : 1.f;
                 dsum = rseq < S ? args.dvec[rg] : 0.f;
             }
+            // the pieces of a step (block id of (row block a, slot), the slot's
+            // block-column), loaded a step ahead so that their latency passes
+            // under the wait for the accumulator
+            int nblk[NPH], ncol[NPH];
+            auto fetch = [&](int s) {
+#pragma unroll
+                for (int p = 0; p < NPH; ++p) {
+                    const int b = (64 * hf + p * CW) / BLK;
+                    nblk[p] = L.step_blk[(s * G + a) * G + b];
+                    if constexpr (SMX) ncol[p] = L.step_col[s * G + b];
+                    else ncol[p] = 0;
+                }
+            };
+            if (ns > 0) fetch(s0);
             for (int it = 0; it < NPASS * ns; ++it, ++g) {
-                const int n = it % ns, s = s0 + n;
                 const bool write = !XCH || it >= ns;  // the pass that writes
+                int pblk[NPH], pcol[NPH];
+#pragma unroll
+                for (int p = 0; p < NPH; ++p) {
+                    pblk[p] = nblk[p];
+                    pcol[p] = ncol[p];
+                }
+                if (it + 1 < NPASS * ns) fetch(s0 + (it + 1) % ns);
                 const uint32_t sb = g % NACC;
                 bool ok = mbar_wait(&s_full[sb], (g / NACC) & 1, ab);
                 if (!__all_sync(0xffffffffu, ok)) goto epi_done;
@@ -401,10 +421,6 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     if (lane == 0) mbar_arrive(&s_empty[sb]);
                 }
                 float* xf = reinterpret_cast<float*>(x);
-                // the pieces of this half: slot and block id of (row block a, slot)
-                int pblk[NPH];
-#pragma unroll
-                for (int p = 0; p < NPH; ++p) pblk[p] = L.step_blk[(s * G + a) * G + (64 * hf + p * CW) / BLK];
                 if constexpr (SMB) {
                     // this half row of the stage's P tile (panel hf; the copies
                     // landed: wait on the stage's full barrier), zeros for absent
@@ -458,9 +474,9 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     // diagonal inside diagonal blocks, dense-mask zeros
 #pragma unroll
                     for (int p = 0; p < NPH; ++p) {
-                        const int b = (64 * hf + p * CW) / BLK, co = (64 * hf + p * CW) % BLK;
+                        const int co = (64 * hf + p * CW) % BLK;
                         const int blk = pblk[p];
-                        const int col = L.step_col[s * G + b];
+                        const int col = pcol[p];
                         // in-piece column j is kept iff j <= lim
                         const int lim =
                             blk < 0 ? -1 : ((args.kind == BSP_MASK_DIAG_CAUSAL && col == rb) ? r_in - co : CW);
