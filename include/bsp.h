@@ -349,11 +349,13 @@ int bsp_attention_backward(bsp_layout_t layout, int dtype, const void* Q, const 
  * statistics pass, and rowsum(P .* dP) = rowsum(dO .* O) per row (O = P V),
  * so one tensor-core pass over the row tiles computes both products of a
  * step, S = Q K^T and dP = dO V^T, and writes P and
- * dX = scale P .* (dP - rowsum(dO .* O)) together (P is not read back); then
- * dV = P^T dO, dQ = dX K, dK = dX^T Q.  O, dO: DEVICE [Z][H][S][D]; lse:
+ * dX = scale P .* (dP - rowsum(dO .* O)) together (P is not read back); for
+ * head size 128 and blocks of 64 and 128 the same pass accumulates
+ * dQ = dX K per row tile on the tensor cores.  Then dV = P^T dO, dK = dX^T Q
+ * (and dQ = dX K where the pass did not).  O, dO: DEVICE [Z][H][S][D]; lse:
  * DEVICE float [Z][H][S], 16-byte aligned; the rest as for
- * bsp_attention_backward; dQ's memory holds the rows' dO . O (fp32) until it
- * receives dQ.  fp32, and shapes the one-pass kernel does not cover, take
+ * bsp_attention_backward; dK's memory holds the rows' dO . O (fp32) until it
+ * receives dK.  fp32, and shapes the one-pass kernel does not cover, take
  * bsp_attention_backward's recomputing chain (O and lse unused).  Not from
  * the pages: the chain rule with the forward's statistics kept. */
 int bsp_attention_backward_lse(bsp_layout_t layout, int dtype, const void* Q, const void* K, const void* V,

@@ -275,21 +275,27 @@ extern "C" int bsp_attention_backward_lse(bsp_layout_t L, int dtype, const void*
     if (!aligned16(P_ws) || !aligned16(dP_ws)) return BSP_ERR_ALIGNMENT;
     cudaStream_t s = (cudaStream_t)stream;
     const uint8_t* m = mask_kind == BSP_MASK_DENSE ? mask : nullptr;
-    // the rows' dO . O (= rowsum(P .* dP), as O = P V) go to dQ's memory first
-    // (fp32 [Z][H][S] fits in any [Z][H][S][D] tensor of D >= 2); dQ receives
+    // the rows' dO . O (= rowsum(P .* dP), as O = P V) go to dK's memory first
+    // (fp32 [Z][H][S] fits in any [Z][H][S][D] tensor of D >= 2); dK receives
     // its own values last
-    float* dvec = static_cast<float*>(dQ);
+    float* dvec = static_cast<float*>(dK);
     if ((rc = bsp::launch_row_dot(dtype, dO, O, dvec, (int64_t)Z * L->H * L->S, D, s))) return rc;
     // P = exp(scale Q K^T - lse) and dX = scale P .* (dO V^T - dvec) on the
-    // layout: one pass
-    rc = bsp::launch_sdd_attention_bwd_tc(L, dtype, Q, K, dO, V, lse, dvec, P_ws, dP_ws, Z, D, scale, mask_kind, m,
-                                          s);
+    // layout, and dQ = dX K accumulated over each row tile's steps: one pass
+    // (head size 128, blocks of 64 and 128); else P and dX in one pass and dQ
+    // by a DSD
+    rc = bsp::launch_sdd_attention_bwd_dq_tc(L, dtype, Q, K, dO, V, lse, dvec, P_ws, dP_ws, dQ, Z, D, scale,
+                                             mask_kind, m, s);
+    const bool dq_done = rc == BSP_OK;
+    if (rc == BSP_ERR_UNSUPPORTED)
+        rc = bsp::launch_sdd_attention_bwd_tc(L, dtype, Q, K, dO, V, lse, dvec, P_ws, dP_ws, Z, D, scale, mask_kind,
+                                              m, s);
     if (rc == BSP_ERR_UNSUPPORTED)
         return bsp_attention_backward(L, dtype, Q, K, V, dO, dQ, dK, dV, Z, D, scale, mask_kind, mask, P_ws, dP_ws,
                                       stream);
     if (rc) return rc;
     // dV = P^T dO,  dQ = dX K,  dK = dX^T Q
     if ((rc = bsp_dsd(L, dtype, P_ws, dO, dV, Z, D, 1, 0, stream))) return rc;
-    if ((rc = bsp_dsd(L, dtype, dP_ws, K, dQ, Z, D, 0, 0, stream))) return rc;
+    if (!dq_done && (rc = bsp_dsd(L, dtype, dP_ws, K, dQ, Z, D, 0, 0, stream))) return rc;
     return bsp_dsd(L, dtype, dP_ws, Q, dK, Z, D, 1, 0, stream);
 }

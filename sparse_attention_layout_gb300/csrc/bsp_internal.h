@@ -157,6 +157,10 @@ int launch_sdd_softmax_bwd_tc(const bsp_layout_s* L, int dtype, const void* dO, 
 int launch_sdd_attention_bwd_tc(const bsp_layout_s* L, int dtype, const void* Q, const void* K, const void* dO,
                                 const void* V, const float* lse, const float* dvec, void* P, void* dX, int Z, int D,
                                 float scale, int kind, const uint8_t* mask, cudaStream_t s);
+// the same, also writing dQ = dX K [Z][H][S][D] (D = 128, blocks of 64 and 128)
+int launch_sdd_attention_bwd_dq_tc(const bsp_layout_s* L, int dtype, const void* Q, const void* K, const void* dO,
+                                   const void* V, const float* lse, const float* dvec, void* P, void* dX, void* dQ,
+                                   int Z, int D, float scale, int kind, const uint8_t* mask, cudaStream_t s);
 // out[r] = sum_d A[r][d] B[r][d] (fp32) for rows of D elements (D a multiple of 8)
 int launch_row_dot(int dtype, const void* A, const void* B, float* out, int64_t rows, int D, cudaStream_t s);
 int launch_dsd_group_tc(const bsp_layout_s* L, int dtype, const void* A, const void* B, void* C, int Z,

@@ -103,41 +103,51 @@ __host__ __device__ constexpr uint32_t swz_of(int row_bytes) {
 template <int KP, int BLK, int MODE>
 struct SddCfg {
     static constexpr bool SMB = MODE == 2;
-    static constexpr bool DUO = MODE == 3;  // two products per step
+    static constexpr bool DUO = MODE == 3 || MODE == 4;  // two products per step
     static constexpr int kTile = 128 * 64 * KP * 2;  // 128 rows x K (KP panels of 64)
     static constexpr int AST = (SMB || DUO) ? 1 : 2;  // query-tile stages
     // key-tile stages: three, except in the backward modes (two stages of V
     // and P, or of K and V); at K = 128 the fused softmax makes room for the
     // third with one staging buffer per epilogue warp (its per-tile exchange
     // arrays take the rest)
-    static constexpr int BST = (SMB || DUO) ? 2 : 3;
+    // MODE 4: three stages of K (held until the step's dQ product) and one of
+    // V (released by dP) in the room of two (K, V) stages
+    static constexpr bool DQF = MODE == 4;
+    static constexpr int BST = DQF ? 3 : ((SMB || DUO) ? 2 : 3);
     static constexpr int kPT = SMB ? 32768 : 0;  // P tile of a key-tile stage
     static constexpr int kAStage = DUO ? 2 * kTile : kTile;  // Q (and dO)
-    static constexpr int kBStage = DUO ? 2 * kTile : kTile + kPT;  // K (and V, or P)
+    static constexpr int kBStage = (DUO && !DQF) ? 2 * kTile : kTile + kPT;  // K (and V, or P)
     static constexpr int kA = 0;
     static constexpr int kB = AST * kAStage;
-    static constexpr int kStg = kB + BST * kBStage;  // staging: NBUF buffers per epilogue warp
+    static constexpr int kV = kB + BST * kBStage;  // MODE 4: the V stage
+    static constexpr int kStg = kV + (DQF ? kTile : 0);  // staging: NBUF buffers per epilogue warp
     static constexpr int NBUF = (SMB || (MODE == 1 && KP == 2) || (DUO && KP == 2)) ? 1 : 2;
-    // TMEM accumulators: four of 128 columns, or two pairs (S, dP)
-    static constexpr int NACC = DUO ? 2 : 4;
+    // TMEM accumulators: four of 128 columns, two pairs (S, dP), or one pair
+    // plus dQ (columns 256 .. 384) and two buffers of dX as 16-bit pairs
+    // (columns 384 .. 448 .. 512)
+    static constexpr int NACC = MODE == 4 ? 1 : (DUO ? 2 : 4);
     static constexpr int kBuf = 32 * (BLK < 64 ? BLK : 64) * 2;  // a warp's 32 rows of one piece
     static constexpr int kAlloc = kStg + 8 * NBUF * kBuf + 1024;
 };
 
 // MODE: 0 plain SDD; 1 fused softmax (SMX, two passes); 2 fused softmax
 // backward (SMB, two passes); 3 attention backward from the forward's
-// statistics (DUO, one pass: A = Q, A2 = dO, B = K, B2 = V; C = dX, C2 = P)
+// statistics (DUO, one pass: A = Q, A2 = dO, B = K, B2 = V; C = dX, C2 = P);
+// 4 mode 3 that also accumulates dQ = dX K (DQF; tmD: dQ, [Z H][S][D])
 template <typename T, int BLK, int KP, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmP,
-              const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2, const SddArgs args) {
+              const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
+              const __grid_constant__ CUtensorMap tmD, const SddArgs args) {
     using C = SddCfg<KP, BLK, MODE>;
     constexpr int G = 128 / BLK;
     constexpr int AST = C::AST, BST = C::BST;
     constexpr bool DUO = C::DUO;
     constexpr int NACC = C::NACC;
-    constexpr uint32_t kAccCols = 512 / NACC;  // TMEM columns per accumulator (pair)
+    constexpr bool DQF = C::DQF;
+    static_assert(!DQF || (KP == 2 && BLK >= 64), "dQ fusion: D = 128, blocks of 64 and 128");
+    constexpr uint32_t kAccCols = DUO ? 256 : 128;  // TMEM columns per accumulator (pair)
     constexpr uint32_t kTileBytes = C::kTile;
     // MN-major key tiles: panels of W keys (RB bytes per K row), KPB per block
     constexpr int W = BLK < 64 ? BLK : 64, RB = 2 * W, KPB = BLK / W;
@@ -146,7 +156,7 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     // bytes one stage's copies deliver: K-major boxes are 64 * KP columns wide
     // (zero-filled past K), MN-major ones exactly K rows
     const uint32_t a_bytes = (a_mn ? 256u * kd : kTileBytes) * (DUO ? 2u : 1u);
-    const uint32_t b_bytes = (b_mn ? 256u * kd : kTileBytes) * (DUO ? 2u : 1u);
+    const uint32_t b_bytes = (b_mn ? 256u * kd : kTileBytes) * ((DUO && !DQF) ? 2u : 1u);
     constexpr bool SMX = MODE == 1 || DUO, SMB = MODE == 2;
     constexpr bool XCH = MODE == 1 || MODE == 2;  // two passes, row statistics exchanged between them
     constexpr int NPASS = XCH ? 2 : 1;            // passes over a tile's steps
@@ -159,17 +169,28 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     __shared__ uint64_t xq[4];
     __shared__ float2 xs[XCH ? 2 : 1][2][XCH ? 128 : 1];
     __shared__ uint32_t tmem_base;
+    // DQF: dP of the step computed (dp_full) and read (dp_empty) -- S and dP
+    // have barriers of their own, so the next step's S starts as soon as this
+    // step's S is in registers; the step's dX in TMEM buffer g % 2 written by
+    // the eight epilogue warps (ds_full) and read by the dQ product
+    // (ds_free); the tile's dQ accumulated (dq_full) and read out (dq_empty)
+    __shared__ uint64_t dp_full, dp_empty, ds_full[2], ds_free[2], dq_full, dq_empty;
+    __shared__ uint64_t v_full, v_empty;  // DQF: the V stage loaded, read by dP
+    // after an abort: the MMA issuer's last commit, which lands once every
+    // product it issued has completed
+    __shared__ uint64_t mma_fin;
     __shared__ int abort_flag;
     // what the issuing threads had issued when they stopped (A tiles, B
-    // steps, MMA steps), drained after the roles stop if the kernel aborted
-    __shared__ uint32_t issued[3];
+    // steps, MMA steps, dQ steps, V tiles), drained after the roles stop if
+    // the kernel aborted
+    __shared__ uint32_t issued[5];
 
     const LayoutView& L = args.L;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     Abort ab{&abort_flag, L.status, L.wait_ns};
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        for (int i = 0; i < 3; ++i) issued[i] = 0;
+        for (int i = 0; i < 5; ++i) issued[i] = 0;
         for (int i = 0; i < AST; ++i) {
             mbar_init(&a_full[i], 1);
             mbar_init(&a_empty[i], 1);
@@ -183,6 +204,17 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             mbar_init(&s_empty[i], 8);
         }
         for (int i = 0; i < 4; ++i) mbar_init(&xq[i], 2);
+        mbar_init(&dp_full, 1);
+        mbar_init(&dp_empty, 8);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ds_full[i], 8);
+            mbar_init(&ds_free[i], 1);
+        }
+        mbar_init(&dq_full, 1);
+        mbar_init(&dq_empty, 8);
+        mbar_init(&mma_fin, 1);
+        mbar_init(&v_full, 1);
+        mbar_init(&v_empty, 1);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -205,7 +237,7 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 tma_prefetch_desc(&tmA2);
                 tma_prefetch_desc(&tmB2);
             }
-            uint32_t a_it = 0, g = 0;
+            uint32_t a_it = 0, g = 0, nv = 0;  // nv: V tiles issued (DQF)
             for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
                 const int4 run = tile_run_at(L, w, args.Z);
             const int tile = run.x;
@@ -258,11 +290,25 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                             for (int p = 0; p < KP; ++p) {
                                 tma_load_2d(smem_u32(smem + C::kB + st * C::kBStage + p * 16384 + b * BLK * 128),
                                             &tmB, p * 64, (int32_t)(zh * S + (int64_t)c * BLK), &b_full[st]);
-                                if constexpr (DUO)  // V beside K
+                                if constexpr (DUO && !DQF)  // V beside K
                                     tma_load_2d(smem_u32(smem + C::kB + st * C::kBStage + kTileBytes + p * 16384 +
                                                          b * BLK * 128),
                                                 &tmB2, p * 64, (int32_t)(zh * S + (int64_t)c * BLK), &b_full[st]);
                             }
+                        }
+                    }
+                    if constexpr (DQF) {
+                        // V into its single stage once dP of the previous step has read it
+                        if (!mbar_wait(&v_empty, (g & 1) ^ 1, ab)) goto producer_done;
+                        mbar_arrive_expect_tx(&v_full, kTileBytes);
+                        ++nv;
+#pragma unroll
+                        for (int b = 0; b < G; ++b) {
+                            int c = L.step_col[s * G + b];
+                            if (c < 0) c = L.step_col[s * G];
+                            for (int p = 0; p < KP; ++p)
+                                tma_load_2d(smem_u32(smem + C::kV + p * 16384 + b * BLK * 128), &tmB2, p * 64,
+                                            (int32_t)(zh * S + (int64_t)c * BLK), &v_full);
                         }
                     }
                     if constexpr (SMB) {
@@ -287,6 +333,7 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         producer_done:
             issued[0] = a_it;
             issued[1] = g;
+            issued[4] = nv;
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -295,6 +342,37 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             // when both tiles are K-major, else exactly K / 16
             const int nks = (a_mn || b_mn) ? kd / 16 : KP * 4;
             uint32_t a_it = 0, g = 0;
+            // DQF: dQ += dX K of step g - 1 is issued after the products of
+            // step g, once the epilogue has written that step's dX into TMEM
+            // buffer (g - 1) % 2 (the A operand: 8 columns of 16-bit pairs per
+            // 16 keys) -- the K tile (the B operand, MN-major) still sits in
+            // its stage, which the dQ product releases
+            constexpr uint32_t kIdescDQ = idesc_f16(128, 128, std::is_same<T, __nv_bfloat16>::value, 0, 1);
+            uint32_t nq = 0, tq = 0;  // dQ steps issued, tiles whose dQ has started
+            int pend = 0;             // a dQ step pending: 0 none, else 1 | 2 (first of its tile) | 4 (last)
+            uint32_t pend_st = 0;
+            auto issue_dq = [&]() -> bool {
+                const uint32_t db = nq & 1;  // dX buffer
+                if (!mbar_wait(&ds_full[db], (nq >> 1) & 1, ab)) return false;
+                if ((pend & 2) && tq > 0 && !mbar_wait(&dq_empty, (tq - 1) & 1, ab)) return false;
+                tc_fence_after();
+                const uint32_t dk0 = smem_u32(smem + C::kB + pend_st * C::kBStage);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {  // 16 keys per product
+                    const uint64_t dk = smem_desc(dk0 + ks * 2048, 16384, 1024, kSw128);
+                    mma_f16_tmem_a(tS + 256, tS + 384 + db * 64 + ks * 8, dk, kIdescDQ,
+                                   ((pend & 2) && ks == 0) ? 0u : 1u);
+                }
+                mma_commit(&ds_free[db]);
+                mma_commit(&b_empty[pend_st]);
+                if (pend & 4) {
+                    mma_commit(&dq_full);
+                    ++tq;
+                }
+                ++nq;
+                pend = 0;
+                return true;
+            };
             for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
                 const int ns = tile_run_at(L, w, args.Z).z;
                 if (ns == 0) continue;
@@ -308,10 +386,19 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     const uint32_t abase = smem_u32(smem + C::kA + as * C::kAStage);
                     const uint32_t bbase = smem_u32(smem + C::kB + st * C::kBStage);
                     // DUO: S = Q K^T into the pair's first 128 columns, then
-                    // dP = dO V^T (the stages' second tiles) into the next 128
+                    // dP = dO V^T (the stages' second tiles) into the next 128;
+                    // DQF: dP once the previous step's dP has been read
 #pragma unroll
                     for (int pr = 0; pr < (DUO ? 2 : 1); ++pr) {
-                        const uint32_t ab0 = abase + pr * kTileBytes, bb0 = bbase + pr * kTileBytes;
+                        uint32_t bb0 = bbase + pr * kTileBytes;
+                        if (DQF && pr == 1) {
+                            mma_commit(&s_full[sb]);
+                            if (!mbar_wait(&dp_empty, (g & 1) ^ 1, ab)) goto mma_done;
+                            if (!mbar_wait(&v_full, g & 1, ab)) goto mma_done;
+                            tc_fence_after();
+                            bb0 = smem_u32(smem + C::kV);
+                        }
+                        const uint32_t ab0 = abase + pr * kTileBytes;
                         for (int ks = 0; ks < nks; ++ks) {
                             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;  // K-major step
                             const uint64_t da = a_mn ? smem_desc(ab0 + ks * 2048, kd * 128, 1024, kSw128)
@@ -321,14 +408,29 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                             mma_f16(tS + sb * kAccCols + pr * 128, da, db, idesc, ks > 0 ? 1u : 0u);
                         }
                     }
-                    mma_commit(&s_full[sb]);
-                    mma_commit(&b_empty[st]);
+                    mma_commit(DQF ? &dp_full : &s_full[sb]);
+                    if constexpr (DQF) mma_commit(&v_empty);
                     if (it == NPASS * ns - 1) mma_commit(&a_empty[as]);
+                    if constexpr (DQF) {
+                        if (pend && !issue_dq()) goto mma_done;
+                        pend = 1 | (it == 0 ? 2 : 0) | (it == ns - 1 ? 4 : 0);
+                        pend_st = st;
+                    } else {
+                        mma_commit(&b_empty[st]);
+                    }
                 }
                 ++a_it;
             }
+            if constexpr (DQF) {
+                if (pend && !issue_dq()) goto mma_done;
+            }
         mma_done:
             issued[2] = g;
+            issued[3] = nq;
+            if (*ab.flag) {  // stopped early: every product issued lands before the roles stop
+                mma_commit(&mma_fin);
+                mbar_drain(&mma_fin, 0, ab);
+            }
         }
     } else {
         // Epilogue: eight warps; warp w owns 32 rows of the tile (TMEM lanes of
@@ -360,6 +462,7 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             if constexpr (DUO) tma_prefetch_desc(&tmP);
         }
         uint32_t g = 0, uses = 0, xc = 0;  // xc: row-statistics exchanges so far
+        uint32_t tqe = 0;                  // DQF: tiles whose dQ was read out of TMEM
         for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
             const int4 run = tile_run_at(L, w, args.Z);
             const int tile = run.x;
@@ -396,6 +499,52 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 }
             };
             if (ns > 0) fetch(s0);
+            // DQF: this warp's 32 rows x 64 columns of the tile's dQ (zeros for
+            // a tile without steps) out through its staging buffer
+            const int64_t zh = (int64_t)z * L.H + tile / L.ngroups;
+            auto dq_out = [&](bool acc) -> bool {
+                uint32_t q[32];
+                if (acc) {
+                    const bool ok = mbar_wait(&dq_full, tqe & 1, ab);
+                    if (!__all_sync(0xffffffffu, ok)) return false;
+                    tc_fence_after();
+                    uint32_t r[64];
+                    tmem_ld64_sync(tS + 256 + lane_base + 64 * hf, tS + 256 + lane_base + 64 * hf + 32, r);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&dq_empty);
+                    ++tqe;
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        q[k] = Pack2<T>::pack(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]));
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) q[k] = 0u;
+                }
+                const int y0 = gq * 128 + quad * 32;
+                if (y0 >= S) return true;  // rows past the sequence end
+                if (lane == 0) bulk_wait_read<0>();
+                __syncwarp();
+                uint8_t* rp = stg + lane * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<uint4*>(rp + ((j ^ (lane & 7)) << 4)) =
+                        make_uint4(q[4 * j], q[4 * j + 1], q[4 * j + 2], q[4 * j + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(&tmD, smem_u32(stg), 64 * hf, y0, (int32_t)zh);
+                    bulk_commit();
+                }
+                ++uses;
+                return true;
+            };
+            if constexpr (DQF) {
+                if (ns == 0) {
+                    if (!dq_out(false)) goto epi_done;
+                    continue;
+                }
+            }
             for (int it = 0; it < NPASS * ns; ++it, ++g) {
                 const bool write = !XCH || it >= ns;  // the pass that writes
                 int pblk[NPH], pcol[NPH];
@@ -413,9 +562,10 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 uint32_t x[64];
                 tmem_ld32_sync(tacc, *reinterpret_cast<uint32_t(*)[32]>(x));
                 tmem_ld32_sync(tacc + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
-                if constexpr (!DUO) {
+                if constexpr (!DUO || DQF) {
                     // the accumulator is free once both halves are in registers
-                    // (DUO: once dP is in registers too, below)
+                    // (DUO: once dP is in registers too, below; DQF: S has a
+                    // barrier of its own)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&s_empty[sb]);
@@ -585,20 +735,41 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     // accumulator pair, and dX = scale P .* (dP - dO_row . O_row)
                     // from the rounded P (0 where masked)
                     store(pk, &tmP, reinterpret_cast<T*>(args.C2));
+                    if constexpr (DQF) {
+                        ok = mbar_wait(&dp_full, g & 1, ab);
+                        if (!__all_sync(0xffffffffu, ok)) goto epi_done;
+                        tc_fence_after();
+                    }
                     uint32_t y[64];
                     tmem_ld32_sync(tacc + 128, *reinterpret_cast<uint32_t(*)[32]>(y));
                     tmem_ld32_sync(tacc + 160, *reinterpret_cast<uint32_t(*)[32]>(y + 32));
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&s_empty[sb]);
+                    if (lane == 0) mbar_arrive(DQF ? &dp_empty : &s_empty[sb]);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const float2 pf = Unpack2<T>::unpack(pk[j]);
                         pk[j] = Pack2<T>::pack(args.scale * pf.x * (__uint_as_float(y[2 * j]) - dsum),
                                                args.scale * pf.y * (__uint_as_float(y[2 * j + 1]) - dsum));
                     }
+                    if constexpr (DQF) {
+                        // this half row of dX into TMEM buffer g % 2 (keys 64 hf ..
+                        // 64 hf + 63 as 32 columns of pairs), once the dQ product
+                        // of step g - 2 has read the buffer
+                        const uint32_t db = g & 1;
+                        ok = mbar_wait(&ds_free[db], ((g >> 1) & 1) ^ 1, ab);
+                        if (!__all_sync(0xffffffffu, ok)) goto epi_done;
+                        tc_fence_after();
+                        tmem_st32_sync(tS + 384 + db * 64 + lane_base + 32 * hf, pk);
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&ds_full[db]);
+                    }
                 }
                 store(pk, &tmC, Cp);
+                if constexpr (DQF) {
+                    if (it == ns - 1 && !dq_out(true)) goto epi_done;
+                }
             }
         }
     epi_done:
@@ -612,7 +783,9 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         if (threadIdx.x == 0) {
             mbar_drain_ring(a_full, AST, issued[0], ab);
             mbar_drain_ring(b_full, BST, issued[1], ab);
+            if (issued[4]) mbar_drain(&v_full, (issued[4] - 1) & 1, ab);
             if (issued[2]) mbar_drain(&s_full[(issued[2] - 1) % NACC], ((issued[2] - 1) / NACC) & 1, ab);
+            if (issued[3]) mbar_drain(&ds_free[(issued[3] - 1) & 1], ((issued[3] - 1) >> 1) & 1, ab);
         }
         __syncthreads();
     }
@@ -636,6 +809,7 @@ struct SddExtra {
     const void* A2 = nullptr;       // DUO: dO (A is Q)
     const void* B2 = nullptr;       // DUO: V (B is K)
     void* C2 = nullptr;             // DUO: P (C is dX)
+    void* D2 = nullptr;             // MODE 4: dQ [Z][H][S][K]
 };
 
 template <typename T, int BLK, int KP, int MODE>
@@ -643,8 +817,9 @@ int sdd_launch(const bsp_layout_s* Lh, const void* A, const void* B, void* Cout,
                const SddExtra& e, cudaStream_t s) {
     const int bf = std::is_same<T, __nv_bfloat16>::value;
     const uint64_t ZH = (uint64_t)Z * Lh->H, rows = ZH * Lh->S;
+    constexpr bool DUO = SddCfg<KP, BLK, MODE>::DUO;
     constexpr int W = BLK < 64 ? BLK : 64;
-    CUtensorMap ma, mb, mc, mp, ma2, mb2;
+    CUtensorMap ma, mb, mc, mp, ma2, mb2, md;
     // [S][K] operands: boxes of 128 (A) or B (B) rows x 64 columns; [K][S]
     // operands: boxes of K rows x 64 (A) or W (B) columns
     int rc = ta ? make_tmap_2d(&ma, A, bf, ZH * K, Lh->S, K, 64, 128) : make_tmap_2d(&ma, A, bf, rows, K, 128, 64, 128);
@@ -660,20 +835,26 @@ int sdd_launch(const bsp_layout_s* Lh, const void* A, const void* B, void* Cout,
     if (!rc) {
         if constexpr (MODE == 2)
             rc = make_tmap_2d(&mp, e.P, bf, (uint64_t)Z * Lh->nnz * BLK, BLK, BLK, 64, 128);
-        else if constexpr (MODE == 3)  // P is written like C
+        else if constexpr (DUO)  // P is written like C
             rc = make_tmap_3d(&mp, e.C2, bf, BLK, (uint64_t)Z * Lh->nnz * BLK, 1, W, BLK < 32 ? BLK : 32,
                               BLK >= 64 ? 128 : 0);
         else mp = mc;
     }
-    // MODE 3: dO and V, [S][K] like Q and K
+    // DUO: dO and V, [S][K] like Q and K
     if (!rc) {
-        if constexpr (MODE == 3) {
+        if constexpr (DUO) {
             rc = make_tmap_2d(&ma2, e.A2, bf, rows, K, 128, 64, 128);
             if (!rc) rc = make_tmap_2d(&mb2, e.B2, bf, rows, K, BLK, 64, 128);
         } else {
             ma2 = ma;
             mb2 = mb;
         }
+    }
+    // MODE 4: dQ rows [Z * H][S][K], boxes of 32 rows x 64 columns (rows past
+    // the sequence end clipped)
+    if (!rc) {
+        if constexpr (MODE == 4) rc = make_tmap_3d(&md, e.D2, bf, K, Lh->S, ZH, 64, 32);
+        else md = mc;
     }
     if (rc) return rc;
     SddArgs a{Lh->view, Cout, Z, K, ta, tb, e.c2, e.kind, e.mask, e.P, e.scale, e.lse, e.dvec, e.C2};
@@ -683,23 +864,27 @@ int sdd_launch(const bsp_layout_s* Lh, const void* A, const void* B, void* Cout,
         return BSP_ERR_CUDA;
     const int64_t total = (int64_t)Z * Lh->n_tiles;
     const int grid = (int)std::min<int64_t>(total, sm_count());
-    kern<<<grid, kThreads, smem, s>>>(ma, mb, mc, mp, ma2, mb2, a);
+    kern<<<grid, kThreads, smem, s>>>(ma, mb, mc, mp, ma2, mb2, md, a);
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }
 
 template <typename T, int BLK, int MODE>
 int sdd_by_k(const bsp_layout_s* L, const void* A, const void* B, void* C, int Z, int K, int ta, int tb,
              const SddExtra& e, cudaStream_t s) {
-    if (K <= 64) return sdd_launch<T, BLK, 1, MODE>(L, A, B, C, Z, K, ta, tb, e, s);
+    if constexpr (MODE == 4) {  // dQ fused: one 128-column accumulator and D = 128 panels
+        if (K != 128) return BSP_ERR_UNSUPPORTED;
+    } else {
+        if (K <= 64) return sdd_launch<T, BLK, 1, MODE>(L, A, B, C, Z, K, ta, tb, e, s);
+    }
     return sdd_launch<T, BLK, 2, MODE>(L, A, B, C, Z, K, ta, tb, e, s);
 }
 
-// the fused softmax backward reads P in 64-key panels: blocks of 64 and 128
-// only
+// the fused softmax backward reads P in 64-key panels, and the dQ-fused mode
+// stages dX in them: blocks of 64 and 128 only
 template <typename T, int MODE>
 int sdd_by_block(const bsp_layout_s* L, const void* A, const void* B, void* C, int Z, int K, int ta, int tb,
                  const SddExtra& e, cudaStream_t s) {
-    constexpr bool small_ok = MODE != 2;
+    constexpr bool small_ok = MODE != 2 && MODE != 4;
     switch (L->B) {
         case 16:
             if constexpr (small_ok) return sdd_by_k<T, 16, MODE>(L, A, B, C, Z, K, ta, tb, e, s);

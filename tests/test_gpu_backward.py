@@ -225,6 +225,35 @@ def test_attention_backward_lse(bsp, oracle, path, B, dt, D, kind):
     assert (dQ[0, 0, 2 * B:3 * B] == 0).all()
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("kind", [0, 1, 2])
+def test_attention_backward_lse_partial_row_tile(bsp, oracle, dt, kind):
+    # blocks of 64 and an odd block count: the last row tile holds one block-row
+    # and rows past the sequence end; the one-pass kernel that also accumulates
+    # dQ (head size 128) writes only the rows inside the sequence
+    dtype = DTYPES[dt]
+    B, nb, D, Z, H = 64, 7, 128, 3, 2
+    S, scale = nb * B, 1.0 / np.sqrt(D)
+    lay = rlayout(H, nb, 0.45, 90 + kind)
+    lay[:, nb - 1, :] = 0
+    lay[0, nb - 1, nb - 1] = 1  # head 0: the last block-row keeps its diagonal block only
+    L = bsp.bsp_layout_compile(lay, B)
+    Q, K, V, G = (randn((Z, H, S, D), dtype, s) for s in (91, 92, 93, 94))
+    mask = W.random_mask(S, 0.7, 95) if kind == W.MASK_DENSE else None
+    dmask = None if mask is None else torch.from_numpy(mask).cuda()
+    q, k, v, g = dev(Q), dev(K), dev(V), dev(G)
+    O, lse = bsp.bsp_attention_lse(L, q, k, v, None, None, scale, kind, dmask)
+    dQ, dK, dV = bsp.attention_backward_lse(L, q, k, v, O, g, lse, scale, kind, dmask)
+    torch.cuda.synchronize()
+    assert bsp.bsp_status_check(L) == 0
+    wQ, wK, wV = oracle.attention_backward(lay, B, Q, K, V, G, scale, kind, mask)
+    tol = GRAD_TOL[dtype]
+    check(dV, wV, tol, f"dV (lse, partial tile) {dt} kind={kind}")
+    check(dQ, wQ, tol, f"dQ (lse, partial tile) {dt} kind={kind}")
+    check(dK, wK, tol, f"dK (lse, partial tile) {dt} kind={kind}")
+    assert (dQ[:, 1, (nb - 1) * B:] == 0).all(), "head 1's last block-row keeps nothing: dQ = 0 there"
+
+
 def test_lse_pair_empty_layout_and_zero_batch(bsp):
     # nothing kept anywhere: O = 0, lse = -inf, every gradient 0; Z = 0: no work
     lay = np.zeros((2, 4, 4), np.uint8)
