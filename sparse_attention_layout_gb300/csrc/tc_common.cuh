@@ -357,16 +357,16 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // y = j + f with j = round-to-nearest(y), found by adding and subtracting
 // 1.5 * 2^23 (which leaves j in the low mantissa bits of the sum), and
 // f in [-1/2, 1/2]; 2^f by the cubic 1 + f (c1 + f (c2 + f c3)), its
-// coefficients fitted here by iteratively reweighted least squares for the
+// coefficients fitted by iteratively reweighted least squares for the
 // smallest maximum relative error over [-1/2, 1/2] with p(0) = 1 held (so
-// integer y give exact powers of two); 2^j is added to the exponent field.
-// Maximum relative error 1.02e-4, far below the 2^-9 of the 16-bit P it
-// feeds.  y is clamped to >= -125 (the exponent field stays normal), so -inf
+// integer y give exact powers of two; fit_exp2_poly.py in the package
+// prints them); 2^j is added to the exponent field.  Maximum relative error
+// 1.01e-4, far below the 2^-9 of the 16-bit P it feeds.  y is clamped to >= -125 (the exponent field stays normal), so -inf
 // and very negative inputs give a value <= 2^-124.5 instead of 0: callers
 // must not rely on exact zeros from masked entries.
 __device__ __forceinline__ float2 exp2_poly2(float2 y) {
     constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
-    constexpr float c1 = 0.6932829f, c2 = 0.24221097f, c3 = 0.055008933f;
+    constexpr float c1 = 0.693282902f, c2 = 0.242210373f, c3 = 0.0550085828f;
     y.x = fmaxf(y.x, -125.0f);
     y.y = fmaxf(y.y, -125.0f);
     const float2 t = __fadd2_rn(y, make_float2(kMagic, kMagic));

@@ -1,6 +1,6 @@
 """The FMA-pipe 2^x used by the fused attention softmax for part of its
 columns, held to its stated bound against fp64 exp2: relative error <= 1.1e-4
-for x >= -125 (fitted 1.02e-4 plus fp32 rounding), exact powers of two at
+for x >= -125 (fitted 1.01e-4 plus fp32 rounding), exact powers of two at
 integers, and a tiny positive value (<= 2^-124.5) for x < -125 and -inf."""
 
 import ctypes
