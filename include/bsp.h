@@ -329,11 +329,14 @@ int bsp_softmax_backward(bsp_layout_t layout, int dtype, const void* Y, const vo
  *     P = softmax(scale Q K^T on the layout and mask)   (recomputed)
  *     dV = P^T dO,  dP = dO V^T (on the layout),  dX = bsp_softmax_backward(P, dP),
  *     dQ = dX K,  dK = dX^T Q
- * of this library's fused SDD + softmax, DSD, SDD and softmax backward calls
- * (bsp_sdd_softmax, bsp_dsd, bsp_sdd, bsp_softmax_backward), enqueued on
- * `stream`; for 16-bit types on the tensor-core shapes dP and dX come from one
- * fused pass (dP = dO V^T kept in fp32 on chip, dX written), the other cases
- * write dP and run the softmax backward in place.  Q, K, V, dO, dQ, dK, dV:
+ * enqueued on `stream`.  For 16-bit types with head size 64 or 128 the fused
+ * forward first recomputes O and the rows' log-sum-exp (O in dV's memory, lse
+ * in dK's), and the backward from them (bsp_attention_backward_lse) follows;
+ * otherwise the chain runs as this library's fused SDD + softmax, DSD, SDD and
+ * softmax backward calls (bsp_sdd_softmax, bsp_dsd, bsp_sdd,
+ * bsp_softmax_backward), with dP and dX from one fused pass on the tensor-core
+ * shapes (dP = dO V^T kept in fp32 on chip, dX written), else dP written and
+ * the softmax backward run in place.  Q, K, V, dO, dQ, dK, dV:
  * DEVICE [Z][H][S][D], D and the mask as for bsp_attention.  P_ws, dP_ws:
  * caller-owned DEVICE workspace of Z * nnz * block * block elements each (P
  * and dX live there afterwards); they may be NULL when the layout has no

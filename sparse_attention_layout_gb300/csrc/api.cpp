@@ -216,6 +216,70 @@ extern "C" int bsp_softmax_backward(bsp_layout_t L, int dtype, const void* Y, co
     return bsp::launch_softmax_backward(L, dtype, Y, dY, dX, Z, scale, (cudaStream_t)stream);
 }
 
+namespace {
+
+// The recomputing chain: P = softmax(scale Q K^T) on the layout, as the forward
+// computes it (one fused pass: the scores never reach memory), dV = P^T dO,
+// dX = scale P .* (dP - rowsum(P .* dP)) with dP = dO V^T, dQ = dX K,
+// dK = dX^T Q; P and dX in the workspaces.
+int backward_chain(bsp_layout_t L, int dtype, const void* Q, const void* K, const void* V, const void* dO, void* dQ,
+                   void* dK, void* dV, int Z, int D, float scale, int mask_kind, const uint8_t* mask, void* P_ws,
+                   void* dP_ws, void* stream) {
+    cudaStream_t s = (cudaStream_t)stream;
+    int rc = bsp_sdd_softmax(L, dtype, Q, K, P_ws, Z, D, 0, 1, scale, mask_kind, mask, stream);
+    if (rc) return rc;
+    if ((rc = bsp_dsd(L, dtype, P_ws, dO, dV, Z, D, 1, 0, stream))) return rc;
+    // dX: one fused pass on the tensor cores (dP stays on chip), else dP
+    // through memory and the softmax backward in place
+    rc = force_simt() ? BSP_ERR_UNSUPPORTED
+                      : bsp::launch_sdd_softmax_bwd_tc(L, dtype, dO, V, P_ws, dP_ws, Z, D, scale, s);
+    if (rc == BSP_ERR_UNSUPPORTED) {
+        if ((rc = bsp_sdd(L, dtype, dO, V, dP_ws, Z, D, 0, 1, stream))) return rc;
+        rc = bsp_softmax_backward(L, dtype, P_ws, dP_ws, dP_ws, Z, scale, stream);
+    }
+    if (rc) return rc;
+    if ((rc = bsp_dsd(L, dtype, dP_ws, K, dQ, Z, D, 0, 0, stream))) return rc;
+    return bsp_dsd(L, dtype, dP_ws, Q, dK, Z, D, 1, 0, stream);
+}
+
+// The backward from the forward's O and rows' log-sum-exp (16-bit types,
+// arguments checked, Z > 0, a layout with blocks): shapes the one-pass
+// kernels do not cover take the recomputing chain.  O may live in dV's
+// memory and lse in dK's beyond its first Z H S floats: O is read only by
+// the row dot, lse only by the one-pass kernel, both before dV and dK are
+// written.
+int backward_from_stats(bsp_layout_t L, int dtype, const void* Q, const void* K, const void* V, const void* O,
+                        const void* dO, const float* lse, void* dQ, void* dK, void* dV, int Z, int D, float scale,
+                        int mask_kind, const uint8_t* mask, void* P_ws, void* dP_ws, void* stream) {
+    cudaStream_t s = (cudaStream_t)stream;
+    const uint8_t* m = mask_kind == BSP_MASK_DENSE ? mask : nullptr;
+    // the rows' dO . O (= rowsum(P .* dP), as O = P V) go to dK's memory first
+    // (fp32 [Z][H][S] fits in any [Z][H][S][D] tensor of D >= 2); dK receives
+    // its own values last
+    float* dvec = static_cast<float*>(dK);
+    int rc = bsp::launch_row_dot(dtype, dO, O, dvec, (int64_t)Z * L->H * L->S, D, s);
+    if (rc) return rc;
+    // P = exp(scale Q K^T - lse) and dX = scale P .* (dO V^T - dvec) on the
+    // layout, and dQ = dX K accumulated over each row tile's steps: one pass
+    // (head size 128, blocks of 64 and 128); else P and dX in one pass and dQ
+    // by a DSD
+    rc = bsp::launch_sdd_attention_bwd_dq_tc(L, dtype, Q, K, dO, V, lse, dvec, P_ws, dP_ws, dQ, Z, D, scale,
+                                             mask_kind, m, s);
+    const bool dq_done = rc == BSP_OK;
+    if (rc == BSP_ERR_UNSUPPORTED)
+        rc = bsp::launch_sdd_attention_bwd_tc(L, dtype, Q, K, dO, V, lse, dvec, P_ws, dP_ws, Z, D, scale, mask_kind,
+                                              m, s);
+    if (rc == BSP_ERR_UNSUPPORTED)
+        return backward_chain(L, dtype, Q, K, V, dO, dQ, dK, dV, Z, D, scale, mask_kind, mask, P_ws, dP_ws, stream);
+    if (rc) return rc;
+    // dV = P^T dO,  dQ = dX K,  dK = dX^T Q
+    if ((rc = bsp_dsd(L, dtype, P_ws, dO, dV, Z, D, 1, 0, stream))) return rc;
+    if (!dq_done && (rc = bsp_dsd(L, dtype, dP_ws, K, dQ, Z, D, 0, 0, stream))) return rc;
+    return bsp_dsd(L, dtype, dP_ws, Q, dK, Z, D, 1, 0, stream);
+}
+
+}  // namespace
+
 extern "C" int bsp_attention_backward(bsp_layout_t L, int dtype, const void* Q, const void* K, const void* V,
                                       const void* dO, void* dQ, void* dK, void* dV, int Z, int D, float scale,
                                       int mask_kind, const uint8_t* mask, void* P_ws, void* dP_ws,
@@ -236,24 +300,17 @@ extern "C" int bsp_attention_backward(bsp_layout_t L, int dtype, const void* Q, 
     }
     if (!P_ws || !dP_ws) return BSP_ERR_INVALID_ARG;
     if (!aligned16(P_ws) || !aligned16(dP_ws)) return BSP_ERR_ALIGNMENT;
-    // P = softmax(scale Q K^T) on the layout, as the forward computes it (one
-    // fused pass: the scores never reach memory)
-    if ((rc = bsp_sdd_softmax(L, dtype, Q, K, P_ws, Z, D, 0, 1, scale, mask_kind, mask, stream))) return rc;
-    // dV = P^T dO
-    if ((rc = bsp_dsd(L, dtype, P_ws, dO, dV, Z, D, 1, 0, stream))) return rc;
-    // dX = scale P .* (dP - rowsum(P .* dP)) with dP = dO V^T on the layout: one
-    // fused pass on the tensor cores (dP stays on chip), else dP through memory
-    // and the softmax backward in place
-    rc = force_simt() ? BSP_ERR_UNSUPPORTED
-                      : bsp::launch_sdd_softmax_bwd_tc(L, dtype, dO, V, P_ws, dP_ws, Z, D, scale, s);
-    if (rc == BSP_ERR_UNSUPPORTED) {
-        if ((rc = bsp_sdd(L, dtype, dO, V, dP_ws, Z, D, 0, 1, stream))) return rc;
-        rc = bsp_softmax_backward(L, dtype, P_ws, dP_ws, dP_ws, Z, scale, stream);
+    if (dtype != BSP_F32 && !force_simt() && (D == 64 || D == 128)) {
+        // 16-bit types, head sizes of the fused tensor-core forward: it
+        // recomputes O (into dV's memory) and the rows' log-sum-exp (into
+        // dK's, after the Z H S floats the row dot takes), and the backward
+        // from those statistics follows
+        float* lse = reinterpret_cast<float*>(static_cast<char*>(dK) + (size_t)Z * L->H * L->S * sizeof(float));
+        if ((rc = attention_impl(L, dtype, Q, K, V, dV, lse, Z, D, scale, mask_kind, mask, stream))) return rc;
+        return backward_from_stats(L, dtype, Q, K, V, dV, dO, lse, dQ, dK, dV, Z, D, scale, mask_kind, mask, P_ws,
+                                   dP_ws, stream);
     }
-    if (rc) return rc;
-    // dQ = dX K,  dK = dX^T Q
-    if ((rc = bsp_dsd(L, dtype, dP_ws, K, dQ, Z, D, 0, 0, stream))) return rc;
-    return bsp_dsd(L, dtype, dP_ws, Q, dK, Z, D, 1, 0, stream);
+    return backward_chain(L, dtype, Q, K, V, dO, dQ, dK, dV, Z, D, scale, mask_kind, mask, P_ws, dP_ws, stream);
 }
 
 extern "C" int bsp_attention_backward_lse(bsp_layout_t L, int dtype, const void* Q, const void* K, const void* V,
@@ -273,29 +330,6 @@ extern "C" int bsp_attention_backward_lse(bsp_layout_t L, int dtype, const void*
                                       stream);
     if (!P_ws || !dP_ws) return BSP_ERR_INVALID_ARG;
     if (!aligned16(P_ws) || !aligned16(dP_ws)) return BSP_ERR_ALIGNMENT;
-    cudaStream_t s = (cudaStream_t)stream;
-    const uint8_t* m = mask_kind == BSP_MASK_DENSE ? mask : nullptr;
-    // the rows' dO . O (= rowsum(P .* dP), as O = P V) go to dK's memory first
-    // (fp32 [Z][H][S] fits in any [Z][H][S][D] tensor of D >= 2); dK receives
-    // its own values last
-    float* dvec = static_cast<float*>(dK);
-    if ((rc = bsp::launch_row_dot(dtype, dO, O, dvec, (int64_t)Z * L->H * L->S, D, s))) return rc;
-    // P = exp(scale Q K^T - lse) and dX = scale P .* (dO V^T - dvec) on the
-    // layout, and dQ = dX K accumulated over each row tile's steps: one pass
-    // (head size 128, blocks of 64 and 128); else P and dX in one pass and dQ
-    // by a DSD
-    rc = bsp::launch_sdd_attention_bwd_dq_tc(L, dtype, Q, K, dO, V, lse, dvec, P_ws, dP_ws, dQ, Z, D, scale,
-                                             mask_kind, m, s);
-    const bool dq_done = rc == BSP_OK;
-    if (rc == BSP_ERR_UNSUPPORTED)
-        rc = bsp::launch_sdd_attention_bwd_tc(L, dtype, Q, K, dO, V, lse, dvec, P_ws, dP_ws, Z, D, scale, mask_kind,
-                                              m, s);
-    if (rc == BSP_ERR_UNSUPPORTED)
-        return bsp_attention_backward(L, dtype, Q, K, V, dO, dQ, dK, dV, Z, D, scale, mask_kind, mask, P_ws, dP_ws,
-                                      stream);
-    if (rc) return rc;
-    // dV = P^T dO,  dQ = dX K,  dK = dX^T Q
-    if ((rc = bsp_dsd(L, dtype, P_ws, dO, dV, Z, D, 1, 0, stream))) return rc;
-    if (!dq_done && (rc = bsp_dsd(L, dtype, dP_ws, K, dQ, Z, D, 0, 0, stream))) return rc;
-    return bsp_dsd(L, dtype, dP_ws, Q, dK, Z, D, 1, 0, stream);
+    return backward_from_stats(L, dtype, Q, K, V, O, dO, lse, dQ, dK, dV, Z, D, scale, mask_kind, mask, P_ws, dP_ws,
+                               stream);
 }
