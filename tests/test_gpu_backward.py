@@ -101,6 +101,40 @@ def test_attention_backward(bsp, oracle, path, B, dt, D, kind):
     assert (dQ[0, 0, 2 * B:3 * B] == 0).all()
 
 
+@pytest.mark.parametrize("B", [64, 128])
+@pytest.mark.parametrize("D", [32, 96])
+@pytest.mark.parametrize("kind", [0, 1, 2])
+@pytest.mark.parametrize("with_stats", [False, True])
+def test_attention_backward_other_head_sizes(bsp, oracle, B, D, kind, with_stats):
+    # head sizes outside the fused forward's (64, 128): the recomputing backward
+    # takes its chain (fused dP + softmax backward on the tensor cores), the
+    # backward from O and lse the one-pass P + dX kernel and a DSD for dQ
+    dtype = torch.bfloat16
+    Z, H, scale = 2, 2, 1.0 / np.sqrt(D)
+    nb = max(4, 384 // B)
+    S = nb * B
+    lay = rlayout(H, nb, 0.4, 60 + B)
+    L = bsp.bsp_layout_compile(lay, B)
+    Q, K, V, G = (randn((Z, H, S, D), dtype, s) for s in (61, 62, 63, 64))
+    mask = W.random_mask(S, 0.7, 65) if kind == W.MASK_DENSE else None
+    dmask = None if mask is None else torch.from_numpy(mask).cuda()
+    q, k, v, g = dev(Q), dev(K), dev(V), dev(G)
+    if with_stats:
+        O, lse = bsp.bsp_attention_lse(L, q, k, v, None, None, scale, kind, dmask)
+        dQ, dK, dV = bsp.attention_backward_lse(L, q, k, v, O, g, lse, scale, kind, dmask)
+    else:
+        dQ, dK, dV = bsp.attention_backward(L, q, k, v, g, scale, kind, dmask)
+    torch.cuda.synchronize()
+    assert bsp.bsp_status_check(L) == 0
+    wQ, wK, wV = oracle.attention_backward(lay, B, Q, K, V, G, scale, kind, mask)
+    tol = GRAD_TOL[dtype]
+    what = f"B={B} D={D} kind={kind} stats={with_stats}"
+    check(dV, wV, tol, f"dV {what}")
+    check(dQ, wQ, tol, f"dQ {what}")
+    check(dK, wK, tol, f"dK {what}")
+    assert (dQ[0, 0, 2 * B:3 * B] == 0).all()
+
+
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
 def test_autograd_wrapper(bsp, oracle, dt):
     dtype = DTYPES[dt]
