@@ -476,6 +476,19 @@ def workload_section(w, bsp, stream, steps, warmup, pk, pk_kind, local):
         X = W_randn((w.Z, L.nnz, w.B, w.B), w.dtype, 77).cuda()
         Y = torch.empty_like(X)
         sms = time_launches(lambda: bsp.bsp_softmax(L, X, Y, w.scale, w.mask_kind), steps, stream)
+        del Y
+        # 16-bit workloads: the backward from the forward's O and log-sum-exp
+        # (the autograd path), every call cold in L2
+        bwd = None
+        if w.dtype != "f32":
+            gO = W_randn(tuple(q.shape), w.dtype, 78).cuda()
+            Of, lse = bsp.bsp_attention_lse(L, q, k, v, None, None, w.scale, w.mask_kind)
+            bms = time_launches(lambda: bsp.attention_backward_lse(L, q, k, v, Of, gO, lse, w.scale, w.mask_kind),
+                                5, stream)
+            bfl = 2.5 * flops  # 10 B^2 D per block against the forward's 4 B^2 D
+            bwd = {"ms": bms, "TFLOP/s": bfl / bms / 1e9, "flops_counted": "10 B^2 D per block",
+                   "api": "bsp_attention_backward_lse (O and lse of bsp_attention_lse)"}
+            del gO, Of, lse
     clocks = clk.summary()
     achieved = flops / (ms * 1e-3) / 1e12
     sbytes = 2.0 * X.numel() * X.element_size()
@@ -491,7 +504,9 @@ def workload_section(w, bsp, stream, steps, warmup, pk, pk_kind, local):
                                  "frac": gbs / pk["hbm_gbs"], "algorithmic_bytes_per_launch": sbytes}},
         "clocks": clocks,
     }
-    del X, Y, q, k, v, o, scratch
+    if bwd is not None:
+        out["attention_backward_lse"] = bwd
+    del X, q, k, v, o, scratch
     return out
 
 
