@@ -327,6 +327,41 @@ def test_attention(bsp, oracle, path, B, dt, D, kind):
     assert bsp.bsp_status_check(L) == 0
 
 
+@pytest.mark.parametrize("B", [16, 64])
+@pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("D", [16, 32, 96])
+@pytest.mark.parametrize("kind", [0, 2])
+def test_attention_other_head_sizes(bsp, oracle, B, dt, D, kind):
+    # head sizes outside the tensor-core kernels' (64, 128) take the CUDA-core
+    # kernel; its O and log-sum-exp against the oracle's
+    dtype = DTYPES[dt]
+    Z, H = 2, 2
+    nb = max(3, 384 // B) + 1
+    S = nb * B
+    lay = rlayout(H, nb, 0.3, 90 + B + kind, diag=(kind == 2))
+    L = bsp.bsp_layout_compile(lay, B)
+    Q, K, V = (randn((Z, H, S, D), dtype, 92 + k) for k in range(3))
+    scale = 1.0 / np.sqrt(D)
+    O, lse = bsp.bsp_attention_lse(L, dev(Q), dev(K), dev(V), None, None, scale, kind)
+    O0 = bsp.bsp_attention(L, dev(Q), dev(K), dev(V), scale=scale, mask_kind=kind)
+    torch.cuda.synchronize()
+    assert bsp.bsp_status_check(L) == 0
+    assert torch.equal(O, O0), "bsp_attention_lse's O differs from bsp_attention's"
+    want = oracle.attention(lay, B, Q, K, V, scale, kind, None)
+    mag = oracle.attention(lay, B, Q, K, V.abs(), scale, kind, None)
+    assert_close(to_np(O), want, dtype, f"attention B={B} {dt} D={D} kind={kind}", mag=mag,
+                 acc=attention_acc(Q, K, scale, dtype, S))
+    wl = oracle.attention_lse(lay, B, Q, K, scale, kind, None)
+    got = lse.cpu().double().numpy()
+    empty = np.isneginf(wl)
+    assert np.all(np.isneginf(got[empty]))
+    qn = Q.double().norm(dim=-1)
+    kmax = K.double().norm(dim=-1).amax(dim=-1, keepdim=True)
+    bound = (scale * gamma(D) * qn * kmax + (S + 4) * 2.0 ** -22).numpy() + 2.0 ** -22 * np.abs(wl)
+    err = np.abs(got[~empty] - wl[~empty])
+    assert np.all(err <= bound[~empty]), f"lse B={B} {dt} D={D} kind={kind}: {err.max():.3e}"
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_unfused_chain_matches_oracle(bsp, oracle, dt):
     dtype = DTYPES[dt]
