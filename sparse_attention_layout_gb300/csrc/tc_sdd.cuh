@@ -376,6 +376,11 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
                 const int ns = tile_run_at(L, w, args.Z).z;
                 if (ns == 0) continue;
+                if constexpr (DQF) {
+                    // the previous tile's last dQ product before waiting for
+                    // this tile's operands, so that its dQ leaves without that wait
+                    if (pend && !issue_dq()) goto mma_done;
+                }
                 const uint32_t as = a_it % AST;
                 if (!mbar_wait(&a_full[as], (a_it / AST) & 1, ab)) goto mma_done;
                 for (int it = 0; it < NPASS * ns; ++it, ++g) {
