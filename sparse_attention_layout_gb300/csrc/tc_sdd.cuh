@@ -155,7 +155,10 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     const bool a_mn = args.ta != 0, b_mn = args.tb == 0;
     // bytes one stage's copies deliver: K-major boxes are 64 * KP columns wide
     // (zero-filled past K), MN-major ones exactly K rows
-    const uint32_t a_bytes = (a_mn ? 256u * kd : kTileBytes) * (DUO ? 2u : 1u);
+    // DQF: the query-side stage's Q and dO have barriers of their own (a_*
+    // for Q, do_* for dO), so that the next tile's Q loads as soon as this
+    // tile's last S has read Q, not after its last dP
+    const uint32_t a_bytes = (a_mn ? 256u * kd : kTileBytes) * ((DUO && !DQF) ? 2u : 1u);
     const uint32_t b_bytes = (b_mn ? 256u * kd : kTileBytes) * ((DUO && !DQF) ? 2u : 1u);
     constexpr bool SMX = MODE == 1 || DUO, SMB = MODE == 2;
     constexpr bool XCH = MODE == 1 || MODE == 2;  // two passes, row statistics exchanged between them
@@ -176,21 +179,22 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     // (ds_free); the tile's dQ accumulated (dq_full) and read out (dq_empty)
     __shared__ uint64_t dp_full, dp_empty, ds_full[2], ds_free[2], dq_full, dq_empty;
     __shared__ uint64_t v_full, v_empty;  // DQF: the V stage loaded, read by dP
+    __shared__ uint64_t do_full, do_empty;  // DQF: the tile's dO loaded, read by its last dP
     // after an abort: the MMA issuer's last commit, which lands once every
     // product it issued has completed
     __shared__ uint64_t mma_fin;
     __shared__ int abort_flag;
     // what the issuing threads had issued when they stopped (A tiles, B
-    // steps, MMA steps, dQ steps, V tiles), drained after the roles stop if
-    // the kernel aborted
-    __shared__ uint32_t issued[5];
+    // steps, MMA steps, dQ steps, V tiles, dO tiles), drained after the roles
+    // stop if the kernel aborted
+    __shared__ uint32_t issued[6];
 
     const LayoutView& L = args.L;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     Abort ab{&abort_flag, L.status, L.wait_ns};
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        for (int i = 0; i < 5; ++i) issued[i] = 0;
+        for (int i = 0; i < 6; ++i) issued[i] = 0;
         for (int i = 0; i < AST; ++i) {
             mbar_init(&a_full[i], 1);
             mbar_init(&a_empty[i], 1);
@@ -215,6 +219,8 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         mbar_init(&mma_fin, 1);
         mbar_init(&v_full, 1);
         mbar_init(&v_empty, 1);
+        mbar_init(&do_full, 1);
+        mbar_init(&do_empty, 1);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -237,7 +243,7 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 tma_prefetch_desc(&tmA2);
                 tma_prefetch_desc(&tmB2);
             }
-            uint32_t a_it = 0, g = 0, nv = 0;  // nv: V tiles issued (DQF)
+            uint32_t a_it = 0, g = 0, nv = 0, d_it = 0;  // nv, d_it: V and dO tiles issued (DQF)
             for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
                 const int4 run = tile_run_at(L, w, args.Z);
             const int tile = run.x;
@@ -258,7 +264,7 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     for (int p = 0; p < KP; ++p) {
                         tma_load_2d(smem_u32(smem + C::kA + as * C::kAStage + p * 16384), &tmA, p * 64,
                                     (int32_t)(zh * S + gq * 128), &a_full[as]);
-                        if constexpr (DUO)  // dO beside Q
+                        if constexpr (DUO && !DQF)  // dO beside Q
                             tma_load_2d(smem_u32(smem + C::kA + as * C::kAStage + kTileBytes + p * 16384), &tmA2,
                                         p * 64, (int32_t)(zh * S + gq * 128), &a_full[as]);
                     }
@@ -298,6 +304,15 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                         }
                     }
                     if constexpr (DQF) {
+                        if (it == 0) {
+                            // the tile's dO beside Q, once the previous tile's last dP has read it
+                            if (!mbar_wait(&do_empty, (d_it & 1) ^ 1, ab)) goto producer_done;
+                            mbar_arrive_expect_tx(&do_full, kTileBytes);
+                            for (int p = 0; p < KP; ++p)
+                                tma_load_2d(smem_u32(smem + C::kA + as * C::kAStage + kTileBytes + p * 16384), &tmA2,
+                                            p * 64, (int32_t)(zh * S + gq * 128), &do_full);
+                            ++d_it;
+                        }
                         // V into its single stage once dP of the previous step has read it
                         if (!mbar_wait(&v_empty, (g & 1) ^ 1, ab)) goto producer_done;
                         mbar_arrive_expect_tx(&v_full, kTileBytes);
@@ -334,6 +349,7 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             issued[0] = a_it;
             issued[1] = g;
             issued[4] = nv;
+            issued[5] = d_it;
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -398,6 +414,8 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                         uint32_t bb0 = bbase + pr * kTileBytes;
                         if (DQF && pr == 1) {
                             mma_commit(&s_full[sb]);
+                            if (it == ns - 1) mma_commit(&a_empty[as]);  // Q read by the tile's last S
+                            if (it == 0 && !mbar_wait(&do_full, a_it & 1, ab)) goto mma_done;
                             if (!mbar_wait(&dp_empty, (g & 1) ^ 1, ab)) goto mma_done;
                             if (!mbar_wait(&v_full, g & 1, ab)) goto mma_done;
                             tc_fence_after();
@@ -414,8 +432,12 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                         }
                     }
                     mma_commit(DQF ? &dp_full : &s_full[sb]);
-                    if constexpr (DQF) mma_commit(&v_empty);
-                    if (it == NPASS * ns - 1) mma_commit(&a_empty[as]);
+                    if constexpr (DQF) {
+                        mma_commit(&v_empty);
+                        if (it == ns - 1) mma_commit(&do_empty);  // dO read by the tile's last dP
+                    } else {
+                        if (it == NPASS * ns - 1) mma_commit(&a_empty[as]);
+                    }
                     if constexpr (DQF) {
                         if (pend && !issue_dq()) goto mma_done;
                         pend = 1 | (it == 0 ? 2 : 0) | (it == ns - 1 ? 4 : 0);
@@ -789,6 +811,7 @@ sdd_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             mbar_drain_ring(a_full, AST, issued[0], ab);
             mbar_drain_ring(b_full, BST, issued[1], ab);
             if (issued[4]) mbar_drain(&v_full, (issued[4] - 1) & 1, ab);
+            if (issued[5]) mbar_drain(&do_full, (issued[5] - 1) & 1, ab);
             if (issued[2]) mbar_drain(&s_full[(issued[2] - 1) % NACC], ((issued[2] - 1) / NACC) & 1, ab);
             if (issued[3]) mbar_drain(&ds_free[(issued[3] - 1) & 1], ((issued[3] - 1) >> 1) & 1, ab);
         }
