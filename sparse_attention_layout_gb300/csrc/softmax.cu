@@ -208,6 +208,7 @@ softmax_chunk_kernel(LayoutView L, const T* X, T* Y, float c2, int kind, const u
     extern __shared__ __align__(128) uint8_t smem_raw[];
     __shared__ uint64_t bar;
     __shared__ int abort_flag;
+    __shared__ float2 part[kChunkThreads / 32];  // long rows: each warp's (max, sum) of its part
     const int n_items = L.sm_n_items[E];
     const int64_t z = blockIdx.x / n_items;
     const int it = (int)(blockIdx.x % n_items);
@@ -316,11 +317,18 @@ softmax_chunk_kernel(LayoutView L, const T* X, T* Y, float c2, int kind, const u
             else if (nvec <= 16 * kRegVec) rows_in_registers(std::integral_constant<int, 16>{});
             else rows_in_registers(std::integral_constant<int, 32>{});
         } else {
-            for (int rr = warp; rr < R; rr += kChunkThreads / 32) {
-                // long row: online (max, sum) per lane in the scaled log2 domain,
-                // merged across the warp, then a normalising pass
+            // long rows: wpr warps per row when the chunk has fewer rows than
+            // warps (R is a power of two), each taking every wpr-th 32-vector
+            // slice of it; R >= warps: one warp per row
+            constexpr int NW = kChunkThreads / 32;
+            const int wpr = R >= NW ? 1 : NW / R;
+            const int wr = warp % wpr;
+            for (int rr = warp / wpr; rr < R; rr += NW / wpr) {
+                // online (max, sum) per lane in the scaled log2 domain, merged
+                // across the warp (and across the row's warps through shared
+                // memory), then a normalising pass
                 float m = -INFINITY, l = 0.f;
-                for (int v = lane; v < nvec; v += 32) {
+                for (int v = lane + 32 * wr; v < nvec; v += 32 * wpr) {
                     float x[VEC];
                     T* p;
                     load(rr, v, x, p);
@@ -346,9 +354,26 @@ softmax_chunk_kernel(LayoutView L, const T* X, T* Y, float c2, int kind, const u
                         ((m2 == -INFINITY) ? 0.f : l2 * tc::ex2_approx(m2 - mn));
                     m = mn;
                 }
+                if (wpr > 1) {
+                    // every warp runs exactly one row here (R < NW), so the
+                    // barriers are reached by all of them
+                    if (lane == 0) part[warp] = make_float2(m, l);
+                    __syncthreads();
+                    const int w0 = (warp / wpr) * wpr;
+                    float mr = -INFINITY;
+                    for (int k = 0; k < wpr; ++k) mr = fmaxf(mr, part[w0 + k].x);
+                    float lr = 0.f;
+                    if (mr != -INFINITY)
+                        for (int k = 0; k < wpr; ++k) {
+                            const float2 pk = part[w0 + k];
+                            if (pk.x != -INFINITY) lr += pk.y * tc::ex2_approx(pk.x - mr);
+                        }
+                    m = mr;
+                    l = lr;
+                }
                 const float inv = l > 0.f ? 1.0f / l : 0.f;
                 const float ms = (m == -INFINITY) ? 0.f : m;
-                for (int v = lane; v < nvec; v += 32) {
+                for (int v = lane + 32 * wr; v < nvec; v += 32 * wpr) {
                     float x[VEC];
                     T* p;
                     load(rr, v, x, p);
