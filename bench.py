@@ -476,7 +476,11 @@ def workload_section(w, bsp, stream, steps, warmup, pk, pk_kind, local):
         X = W_randn((w.Z, L.nnz, w.B, w.B), w.dtype, 77).cuda()
         Y = torch.empty_like(X)
         sms = time_launches(lambda: bsp.bsp_softmax(L, X, Y, w.scale, w.mask_kind), steps, stream)
-        del Y
+        # its backward: Y that softmax's output, dY random of the same shape
+        G = W_randn((w.Z, L.nnz, w.B, w.B), w.dtype, 79).cuda()
+        dX = torch.empty_like(X)
+        sbms = time_launches(lambda: bsp.bsp_softmax_backward(L, Y, G, dX, w.scale), steps, stream)
+        del Y, G, dX
         # 16-bit workloads: the backward from the forward's O and log-sum-exp
         # (the autograd path), every call cold in L2
         bwd = None
@@ -493,6 +497,8 @@ def workload_section(w, bsp, stream, steps, warmup, pk, pk_kind, local):
     achieved = flops / (ms * 1e-3) / 1e12
     sbytes = 2.0 * X.numel() * X.element_size()
     gbs = sbytes / sms / 1e6
+    sbbytes = 1.5 * sbytes  # Y and dY read, dX written
+    sbgbs = sbbytes / sbms / 1e6
     out = {
         "config": config_of(w, lay, "fused attention kernel", flush),
         "attention": {"ms": ms, "TFLOP/s": achieved, "gpu_launches": steps * launches_per_call(bsp, L, w.Z, w.dtype, local),
@@ -502,6 +508,11 @@ def workload_section(w, bsp, stream, steps, warmup, pk, pk_kind, local):
                     "roofline": {"bound": "hbm", "kernel": "softmax", "achieved": gbs, "peak": pk["hbm_gbs"],
                                  "peak_source": f"hbm_gbs of {pk_kind}", "unit": "GB/s",
                                  "frac": gbs / pk["hbm_gbs"], "algorithmic_bytes_per_launch": sbytes}},
+        "softmax_backward": {"ms": sbms, "GB/s": sbgbs,
+                             "roofline": {"bound": "hbm", "kernel": "softmax backward", "achieved": sbgbs,
+                                          "peak": pk["hbm_gbs"], "peak_source": f"hbm_gbs of {pk_kind}",
+                                          "unit": "GB/s", "frac": sbgbs / pk["hbm_gbs"],
+                                          "algorithmic_bytes_per_launch": sbbytes}},
         "clocks": clocks,
     }
     if bwd is not None:

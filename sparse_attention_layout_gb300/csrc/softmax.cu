@@ -408,7 +408,8 @@ int launch_chunk(const bsp_layout_s* Lh, const void* X, void* Y, int Z, float sc
     const int64_t grid = (int64_t)Z * V.sm_n_items[E];
     if (grid > INT32_MAX) return BSP_ERR_UNSUPPORTED;
     auto kern = softmax_chunk_kernel<T, BLK>;
-    if (smem > 48 * 1024 &&
+    // the opt-in counts the kernel's static shared memory as well
+    if (smem + 1024 > 48 * 1024 &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return BSP_ERR_CUDA;
     kern<<<(unsigned)grid, kChunkThreads, smem, s>>>(V, (const T*)X, (T*)Y, scale * kLog2e, kind, mask);

@@ -5,18 +5,32 @@
 //     dX = scale * Y .* (dY - rowsum(Y .* dY)),
 // which is 0 wherever Y is 0 (masked entries, rows with nothing kept).
 //
-// One warp per query row.  A row is nnz_i segments of B contiguous elements
-// (row a of each of its block-row's blocks; the blocks of a block-row are
-// consecutive in storage), read with 16-byte loads.  Rows of up to 160 chunks
-// stay in registers (one pass: load, reduce the dot product, write dX); longer
-// rows take two passes, the second re-reading the row.  A lane touches the
-// same chunks for reading and writing, so dX may alias dY.  HBM-bound: 2
-// reads and 1 write of Z * nnz * B^2 elements.
+// HBM-bound: 2 reads and 1 write of Z * nnz * B^2 elements.  Two kernels,
+// chosen by the layout's longest row:
+//
+// softmax_bwd_kernel (every row within 160 vectors of 16 bytes, and layouts
+// whose chunks would not fit twice in shared memory): one warp per query row,
+// a row's nnz_i segments of B contiguous elements (row a of each of its
+// block-row's blocks, which are consecutive in storage) read with 16-byte
+// loads from global memory.  Rows of up to 160 vectors stay in registers (one
+// pass); longer rows take two passes, the second re-reading the row.  A lane
+// touches the same vectors for reading and writing, so dX may alias dY.
+//
+// softmax_bwd_chunk_kernel (layouts with longer rows) takes the forward's
+// chunk list: a CTA moves R consecutive rows of one block-row of Y and of dY
+// into shared memory with one bulk copy per present block and array, reduces
+// each row's dot product there (8, 16 or 32 lanes a row with the row in
+// registers; rows too long for registers shared by several warps), writes dX
+// over dY's copy and sends it back with one bulk store per block.  Every byte
+// crosses HBM once, in transfers of R * B elements.  A CTA reads its whole
+// chunk before it writes any of it, so dX may alias dY.
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
+#include "tc_common.cuh"
 
 namespace bsp {
 namespace {
@@ -123,9 +137,182 @@ softmax_bwd_kernel(LayoutView L, const T* __restrict__ Y, const T* dY, T* dX, in
     }
 }
 
+// ---------------------------------------------------------------- chunks ----
+constexpr int kBwdChunkThreads = 128;
+constexpr int kBwdChunkWarps = kBwdChunkThreads / 32;
+constexpr int kBwdRegElems = 40;                 // row elements per lane and array held in registers
+constexpr int kBwdChunkMaxBytes = 48 * 1024;     // largest chunk per array: two CTAs per SM at least
+
+// Offset of dY's copy in shared memory (Y's copy starts at 0).
+__host__ __device__ inline size_t bwd_chunk_second(int max_bytes) { return ((size_t)max_bytes + 127) & ~(size_t)127; }
+
+template <typename T, int BLK>
+__global__ void __launch_bounds__(kBwdChunkThreads, 4)
+softmax_bwd_chunk_kernel(LayoutView L, const T* Y, const T* dY, T* dX, float scale) {
+    constexpr int VEC = 16 / sizeof(T);
+    constexpr int VPB = BLK / VEC;  // 16-byte vectors per row slice of one block
+    constexpr int E = sizeof(T) == 4 ? 1 : 0;
+    constexpr int KR = kBwdRegElems / VEC;  // vectors per lane and array kept in registers
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    __shared__ float part[kBwdChunkWarps];  // long rows: each warp's part of the dot product
+    const int n_items = L.sm_n_items[E];
+    const int64_t z = blockIdx.x / n_items;
+    const int it = (int)(blockIdx.x % n_items);
+    // the chunk: rows r0 .. r0+R-1 of the block-row whose blocks are the
+    // consecutive ids p0 .. p0+nq-1
+    const int4 item = reinterpret_cast<const int4*>(L.sm_items[E])[it];
+    const int p0 = item.y, nq = item.z;
+    const int r0 = item.w & 0xffff, R = item.w >> 16;
+    const uint32_t slice = (uint32_t)R * BLK * sizeof(T);  // bytes of one block's part of the chunk
+    uint8_t* gbuf_raw = smem_raw + bwd_chunk_second(L.sm_max_bytes[E]);
+    const T* ys = reinterpret_cast<const T*>(smem_raw);
+    T* gs = reinterpret_cast<T*>(gbuf_raw);
+    const size_t first = ((z * L.nnz + p0) * BLK + r0) * BLK;  // element offset of the chunk's first slice
+    tc::Abort ab{&abort_flag, L.status, L.wait_ns};
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        tc::mbar_init(&bar, 1);
+        tc::fence_barrier_init();
+        tc::mbar_arrive_expect_tx(&bar, 2 * slice * nq);
+        for (int q = 0; q < nq; ++q) {
+            const size_t o = first + (size_t)q * BLK * BLK;
+            tc::bulk_load(tc::smem_u32(smem_raw + (size_t)q * slice), Y + o, slice, &bar);
+            tc::bulk_load(tc::smem_u32(gbuf_raw + (size_t)q * slice), dY + o, slice, &bar);
+        }
+    }
+    __syncthreads();
+    const bool ok = tc::mbar_wait(&bar, 0, ab);
+    if (__syncthreads_and(ok)) {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const int nvec = nq * VPB;
+        // element index of vector v of row rr inside either copy
+        auto at = [&](int rr, int v) { return ((size_t)(v / VPB) * R + rr) * BLK + (v % VPB) * VEC; };
+        auto dot16 = [](const uint4& a, const uint4& b, float acc) {
+            float x[VEC], y[VEC];
+            unpack16<T>(a, x);
+            unpack16<T>(b, y);
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) acc = fmaf(x[k], y[k], acc);
+            return acc;
+        };
+        // dX = scale * y * (g - dot), written over g's place in dY's copy
+        auto write16 = [&](size_t e, const uint4& a, const uint4& b, float dot) {
+            float y[VEC], g[VEC];
+            unpack16<T>(a, y);
+            unpack16<T>(b, g);
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) y[k] = scale * y[k] * (g[k] - dot);
+            *reinterpret_cast<uint4*>(gs + e) = pack16<T>(y);
+        };
+        if (nvec <= 32 * KR) {
+            // rows in registers: GS lanes a row (the fewest of 8, 16, 32 that
+            // hold it), 32 / GS rows a warp, the dot product reduced within
+            // the lane group.  All rows of a chunk have nvec vectors.
+            auto rows_in_registers = [&](auto gs_tag) {
+                constexpr int GS = decltype(gs_tag)::value;
+                constexpr int RPW = 32 / GS;
+                const int sub = lane / GS, gl = lane % GS;
+                for (int base = warp * RPW; base < R; base += kBwdChunkWarps * RPW) {
+                    const int rr = base + sub;
+                    const int nv = rr < R ? nvec : 0;  // lanes of rows past the chunk hold nothing
+                    uint4 yv[KR], gv[KR];
+                    float dot = 0.f;
+#pragma unroll
+                    for (int k = 0; k < KR; ++k) {
+                        const int v = gl + GS * k;
+                        if (v < nv) {
+                            yv[k] = *reinterpret_cast<const uint4*>(ys + at(rr, v));
+                            gv[k] = *reinterpret_cast<const uint4*>(gs + at(rr, v));
+                            dot = dot16(yv[k], gv[k], dot);
+                        }
+                    }
+#pragma unroll
+                    for (int o = GS >> 1; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+#pragma unroll
+                    for (int k = 0; k < KR; ++k) {
+                        const int v = gl + GS * k;
+                        if (v < nv) write16(at(rr, v), yv[k], gv[k], dot);
+                    }
+                }
+            };
+            if (nvec <= 8 * KR) rows_in_registers(std::integral_constant<int, 8>{});
+            else if (nvec <= 16 * KR) rows_in_registers(std::integral_constant<int, 16>{});
+            else rows_in_registers(std::integral_constant<int, 32>{});
+        } else {
+            // long rows: wpr warps a row when the chunk has fewer rows than
+            // warps (R is a power of two), each taking every wpr-th 32-vector
+            // slice; a pass for the dot product and one that writes dX
+            const int wpr = R >= kBwdChunkWarps ? 1 : kBwdChunkWarps / R;
+            const int wr = warp % wpr;
+            for (int rr = warp / wpr; rr < R; rr += kBwdChunkWarps / wpr) {
+                float dot = 0.f;
+                for (int v = lane + 32 * wr; v < nvec; v += 32 * wpr)
+                    dot = dot16(*reinterpret_cast<const uint4*>(ys + at(rr, v)),
+                                *reinterpret_cast<const uint4*>(gs + at(rr, v)), dot);
+#pragma unroll
+                for (int o = 16; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+                if (wpr > 1) {
+                    // every warp runs exactly one row here (R < warps), so the
+                    // barrier is reached by all of them
+                    if (lane == 0) part[warp] = dot;
+                    __syncthreads();
+                    const int w0 = (warp / wpr) * wpr;
+                    dot = 0.f;
+                    for (int k = 0; k < wpr; ++k) dot += part[w0 + k];
+                }
+                for (int v = lane + 32 * wr; v < nvec; v += 32 * wpr) {
+                    const size_t e = at(rr, v);
+                    write16(e, *reinterpret_cast<const uint4*>(ys + e), *reinterpret_cast<const uint4*>(gs + e), dot);
+                }
+            }
+        }
+        tc::fence_proxy_async_smem();  // generic-proxy writes -> visible to the bulk copy engine
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int q = 0; q < nq; ++q)
+                tc::bulk_store(dX + first + (size_t)q * BLK * BLK, tc::smem_u32(gbuf_raw + (size_t)q * slice), slice);
+            tc::bulk_commit();
+            tc::bulk_wait_read_all();  // shared memory must outlive the reads of the stores
+        }
+    } else if (threadIdx.x == 0) {
+        tc::mbar_drain(&bar, 0, ab);  // the wait ran out: the copies in land before the CTA exits
+    }
+}
+
+// BSP_ERR_UNSUPPORTED: the layout's chunks are missing or too large for this
+// kernel (the caller then takes softmax_bwd_kernel)
+template <typename T, int BLK>
+int bwd_chunk_launch(const bsp_layout_s* Lh, const void* Y, const void* dY, void* dX, int Z, float scale,
+                     cudaStream_t s) {
+    constexpr int E = sizeof(T) == 4 ? 1 : 0;
+    const LayoutView& V = Lh->view;
+    if (!V.sm_fits[E] || V.sm_max_bytes[E] > kBwdChunkMaxBytes) return BSP_ERR_UNSUPPORTED;
+    const int64_t grid = (int64_t)Z * V.sm_n_items[E];
+    if (grid == 0) return BSP_OK;
+    if (grid > INT32_MAX) return BSP_ERR_UNSUPPORTED;
+    const size_t smem = bwd_chunk_second(V.sm_max_bytes[E]) + (size_t)V.sm_max_bytes[E];
+    auto kern = softmax_bwd_chunk_kernel<T, BLK>;
+    // the opt-in counts the kernel's static shared memory as well
+    if (smem + 1024 > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return BSP_ERR_CUDA;
+    kern<<<(unsigned)grid, kBwdChunkThreads, smem, s>>>(V, (const T*)Y, (const T*)dY, (T*)dX, scale);
+    return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
+}
+
 template <typename T, int BLK>
 int bwd_launch(const bsp_layout_s* L, const void* Y, const void* dY, void* dX, int Z, float scale,
                cudaStream_t s) {
+    // the chunk kernel when a row is too long for this kernel's registers
+    // (which would take the two-pass loop over global memory); with every row
+    // in registers this kernel keeps more loads in flight than a chunk's
+    // copy-compute-store sequence
+    if ((int64_t)L->max_row_nnz * BLK * (int64_t)sizeof(T) / 16 > 32 * kRegChunks) {
+        const int rc = bwd_chunk_launch<T, BLK>(L, Y, dY, dX, Z, scale, s);
+        if (rc != BSP_ERR_UNSUPPORTED) return rc;
+    }
     const int64_t rows = (int64_t)Z * L->H * L->nb * BLK;
     const int64_t blocks = std::min<int64_t>((rows + 7) / 8, (int64_t)sm_count() * 16);
     softmax_bwd_kernel<T, BLK><<<(unsigned)std::max<int64_t>(blocks, 1), kBwdThreads, 0, s>>>(

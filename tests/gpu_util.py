@@ -192,3 +192,41 @@ def to_np(t):
 
 def dev(t):
     return t.to("cuda").contiguous()
+
+
+# ---------------------------------------------------------- softmax backward --
+
+def row_reduce(lay, B, M):
+    """Sum of M over each query row's blocks, broadcast back onto the block
+    format: M [Z, nnz, B, B] -> [Z, nnz, B, 1] (the blocks of one block-row
+    are consecutive ids, CSR order)."""
+    cnt = np.asarray(lay).reshape(-1, lay.shape[2]).sum(axis=1).astype(np.int64)
+    ptr = np.concatenate([[0], np.cumsum(cnt)])
+    out = np.zeros(M.shape[:3] + (1,), np.float64)
+    for k in np.nonzero(cnt)[0]:
+        a, b = ptr[k], ptr[k + 1]
+        out[:, a:b] = M[:, a:b].sum(axis=(1, 3))[:, None, :, None]
+    return out
+
+
+def check_softmax_backward_elementwise(lay, B, Y, dY, got, want, scale, dtype, what):
+    """Every entry of dX = scale * y * (g - d), d = rowsum(y .* g), within the
+    forward error bound of an fp32 evaluation: the dot product of a row of n
+    entries is off by at most n 2^-23 sum|y g|; scale * y * (g - d) adds three
+    fp32 roundings (2^-21 of scale |y| (|g| + |d|)); the stored value one
+    rounding of the output type (U) plus, for fp16, its subnormal spacing
+    2^-24.  dX is exactly 0 wherever Y is 0."""
+    y, g = _np64(Y), _np64(dY)
+    n = row_reduce(lay, B, np.ones_like(y))
+    A = row_reduce(lay, B, np.abs(y * g))
+    d = np.abs(row_reduce(lay, B, y * g))
+    r = _np64(want)
+    bound = (U[dtype] * np.abs(r)
+             + (1 + U[dtype]) * scale * np.abs(y) * (n * 2.0 ** -23 * A + 2.0 ** -21 * (np.abs(g) + d))
+             + (2.0 ** -24 if dtype == torch.float16 else 0.0))
+    x = _np64(got)
+    err = np.abs(x - r)
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} entries out of bound, worst excess "
+                           f"{float((err - bound).max()):.3e}")
+    assert (x[y == 0] == 0).all(), f"{what}: nonzero gradient where Y is 0"

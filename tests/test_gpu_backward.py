@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import TOL, dev, normwise_err, to_np
+from gpu_util import TOL, check_softmax_backward_elementwise, dev, normwise_err, to_np
 from sparse_attention_layout_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -166,20 +166,93 @@ def test_backward_empty_layout_and_zero_batch(bsp):
     assert dQ.shape == E.shape
 
 
-@pytest.mark.parametrize("B,dt,nb", [(128, "bf16", 16), (64, "f32", 16), (32, "f16", 48)])
+@pytest.mark.parametrize("B,dt,nb", [(128, "bf16", 16), (64, "f32", 24), (32, "f16", 48)])
 def test_softmax_backward_long_rows(bsp, oracle, B, dt, nb):
-    """Rows longer than the register-resident limit (160 chunks of 16 bytes)
-    take the two-pass path."""
+    """Rows longer than the register-resident limit (160 vectors of 16 bytes
+    a row for 16-bit types, 320 for fp32) take the two-pass path."""
     dtype = DTYPES[dt]
     scale = 0.2
     lay = np.ones((1, nb, nb), np.uint8)
     L = bsp.bsp_layout_compile(lay, B)
-    assert nb * B * torch.tensor([], dtype=dtype).element_size() // 16 > 160
+    elt = torch.tensor([], dtype=dtype).element_size()
+    assert nb * B * elt // 16 > 160 * elt // 2
     Y = bsp.bsp_softmax(L, dev(randn((1, L.nnz, B, B), dtype, 91)), None, 0.4)
     dY = dev(randn((1, L.nnz, B, B), dtype, 92))
     got = bsp.bsp_softmax_backward(L, Y, dY, None, scale)
     torch.cuda.synchronize()
     check(got, oracle.softmax_backward(lay, B, Y, dY, scale), TOL[dtype], f"long rows B={B} {dt}")
+
+
+# ------------------------------------------ softmax backward: kernel paths ----
+
+def eye_plus_row(nb, i):
+    lay = np.eye(nb, dtype=np.uint8)[None].copy()
+    lay[0, i, :] = 1
+    return lay
+
+
+# (B, dtype, layout, kernel): the backward runs on the chunk kernel when the
+# layout has a row past 160 vectors of 16 bytes and the largest chunk of the
+# softmax's list is at most 48 KB per array, else on the one-warp-per-row
+# kernel
+SMB_CASES = {
+    # rows of 1..24 blocks of 64 bf16: 8, 16 and 32 lanes a row in registers,
+    # and rows past 160 vectors (one warp a row, eight rows a chunk)
+    "lanes_8_16_32_and_long_bf16": (64, "bf16", lambda: W.layout_causal_blocks(24), "chunk"),
+    # the same for fp32 (4 elements a vector, 10 vectors a lane): rows of
+    # 1..48 blocks of 32
+    "lanes_8_16_32_and_long_f32": (32, "f32", lambda: W.layout_causal_blocks(48), "chunk"),
+    # a bf16 row of 100 blocks of 64 (12.5 KB): two rows a chunk, two warps
+    # a row
+    "two_warps_a_row": (64, "bf16", lambda: eye_plus_row(100, 50), "chunk"),
+    # one fp32 row of 600 blocks of 16 (37.5 KB): one row a chunk, four warps
+    "four_warps_a_row": (16, "f32", lambda: eye_plus_row(600, 300), "chunk"),
+    # rows of at most 9 blocks of 128 bf16 (144 vectors): every row in the
+    # row kernel's registers
+    "row_kernel_registers": (128, "bf16", lambda: W.layout_band(16, 4), "rows"),
+    # fp16, a row of 200 blocks of 128 (50 KB): the row kernel (its
+    # register path for the diagonal rows, two passes for the long row)
+    "row_kernel_fallback": (128, "f16", lambda: eye_plus_row(200, 7), "rows"),
+    # a row longer than the largest chunk (66.5 KB): the row kernel
+    "row_kernel_unchunked": (128, "bf16", lambda: eye_plus_row(260, 0), "rows"),
+}
+
+
+@pytest.mark.parametrize("case", list(SMB_CASES))
+def test_softmax_backward_kernel_paths(bsp, oracle, case):
+    B, dt, mk, kernel = SMB_CASES[case]
+    dtype = DTYPES[dt]
+    scale = 0.35
+    lay = mk()
+    L = bsp.bsp_layout_compile(lay, B)
+    elt = torch.tensor([], dtype=dtype).element_size()
+    ch = L.softmax_chunks(elt)
+    R = ch["items"][:, 3] >> 16
+    rows_blocks = ch["items"][:, 2]
+    vec_per_row = rows_blocks * B * elt // 16
+    on_chunks = ch["fits"] and ch["max_bytes"] <= 48 * 1024 and vec_per_row.max() > 160
+    assert on_chunks == (kernel == "chunk"), (case, ch["fits"], ch["max_bytes"])
+    if case.startswith("lanes"):
+        regs = 40 * elt // 16  # vectors a lane holds
+        for lo, hi in ((0, 8 * regs), (8 * regs, 16 * regs), (16 * regs, 32 * regs), (32 * regs, 1 << 30)):
+            assert ((vec_per_row > lo) & (vec_per_row <= hi)).any(), (case, lo, hi)
+    if case == "two_warps_a_row":
+        assert (R == 2).any() and (vec_per_row[R == 2] > 160).all()
+    if case == "four_warps_a_row":
+        assert (R == 1).any()
+    Z = 2 if L.nnz * B * B <= 4 << 20 else 1
+    Y = bsp.bsp_softmax(L, dev(randn((Z, L.nnz, B, B), dtype, 95)), None, 0.7)
+    dY = dev(randn((Z, L.nnz, B, B), dtype, 96))
+    got = bsp.bsp_softmax_backward(L, Y, dY, None, scale)
+    torch.cuda.synchronize()
+    assert bsp.bsp_status_check(L) == 0
+    want = oracle.softmax_backward(lay, B, Y, dY, scale)
+    check_softmax_backward_elementwise(lay, B, Y, dY, got, want, scale, dtype, case)
+    # in place (dX = dY): the same bytes
+    dY2 = dY.clone()
+    bsp.bsp_softmax_backward(L, Y, dY2, dY2, scale)
+    torch.cuda.synchronize()
+    assert torch.equal(dY2, got)
 
 
 # ------------------------------------------- forward lse + backward_lse ----

@@ -19,7 +19,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import PROB_TOL, U, assert_close, attention_acc, gamma, to_np
+from gpu_util import PROB_TOL, U, assert_close, attention_acc, check_softmax_backward_elementwise, gamma, to_np
 from sparse_attention_layout_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -151,6 +151,40 @@ def test_sdd_softmax_chain_workload(bsp, oracle, name):
     acc = attention_acc(q, k, w.scale, DT[w.dtype], w.S).reshape(-1, 1)[sel]
     assert_close(got, want, DT[w.dtype], f"{name} fused SDD+softmax chain, {sel.size} sampled rows", mag=mag,
                  acc=acc)
+
+
+@pytest.mark.parametrize("name", ["tiny", "bigbird", "band", "strided"])
+def test_softmax_backward_workload(bsp, oracle, name):
+    """The softmax backward at full size on a softmax output: sampled
+    block-rows (the longest, the first and last, random ones), each against
+    the oracle run on a layout holding that block-row alone, every entry
+    within the fp32 evaluation's error bound; over the whole output, dX is
+    exactly 0 wherever Y is 0."""
+    w = W.ATTENTION_WORKLOADS[name]
+    lay = w.layout()
+    L = bsp.bsp_layout_compile(lay, w.B)
+    Y = bsp.bsp_softmax(L, W.randn((w.Z, L.nnz, w.B, w.B), w.dtype, 81).cuda(), None, w.scale, w.mask_kind)
+    dY = W.randn((w.Z, L.nnz, w.B, w.B), w.dtype, 82).cuda()
+    dX = bsp.bsp_softmax_backward(L, Y, dY, None, w.scale)
+    torch.cuda.synchronize()
+    assert bsp.bsp_status_check(L) == 0
+    assert not dX.masked_select(Y == 0).any()
+    H, nb = lay.shape[0], lay.shape[1]
+    cnt = lay.reshape(-1, nb).sum(axis=1).astype(np.int64)
+    ptr = np.concatenate([[0], np.cumsum(cnt)])
+    keys = set(np.random.default_rng(83).choice(H * nb, 6, replace=False).tolist())
+    keys |= {int(np.argmax(cnt)), 0, H * nb - 1}
+    for k in sorted(keys):
+        a, b = int(ptr[k]), int(ptr[k + 1])
+        if a == b:
+            continue
+        h, i = divmod(k, nb)
+        sub = np.zeros((1, nb, nb), np.uint8)
+        sub[0, i] = lay[h, i]
+        ys, gs, xs = Y[:, a:b].cpu(), dY[:, a:b].cpu(), dX[:, a:b].cpu()
+        want = oracle.softmax_backward(sub, w.B, ys, gs, w.scale)
+        check_softmax_backward_elementwise(sub, w.B, ys, gs, xs, want, w.scale, DT[w.dtype],
+                                           f"{name} softmax backward, head {h} block-row {i}")
 
 
 @pytest.mark.parametrize("name", ["tiny", "bigbird", "band", "strided"])
