@@ -37,8 +37,8 @@ namespace {
 
 constexpr int kBwdThreads = 256;
 // 16-byte chunks per lane kept in registers (rows up to 160 chunks, e.g. 9 blocks
-// of 128 bf16); few enough registers for 3 blocks of 256 threads per SM, which
-// a memory-bound kernel needs (8 chunks and 1 block per SM ran at 3.8 TB/s)
+// of 128 bf16); few enough registers for 3 or 4 blocks of 256 threads per SM,
+// which a memory-bound kernel needs (8 chunks and 1 block per SM ran at 3.8 TB/s)
 constexpr int kRegChunks = 5;
 
 template <typename T>
@@ -57,8 +57,12 @@ __device__ __forceinline__ uint4 pack16(const float (&f)[16 / sizeof(T)]) {
     return v;
 }
 
-template <typename T, int BLK>
-__global__ void __launch_bounds__(kBwdThreads, 3)
+// MINB blocks of 256 threads per SM: 3 (79 registers) for layouts whose rows
+// average more than 4 vectors per lane and for fp32, 4 (64 registers) for
+// 16-bit layouts of shorter rows, which need the extra warps to keep as many
+// bytes in flight
+template <typename T, int BLK, int MINB>
+__global__ void __launch_bounds__(kBwdThreads, MINB)
 softmax_bwd_kernel(LayoutView L, const T* __restrict__ Y, const T* dY, T* dX, int Z, float scale) {
     constexpr int E = 16 / sizeof(T);           // elements per 16-byte chunk
     constexpr int CH = BLK * (int)sizeof(T) / 16;  // chunks per row segment
@@ -315,8 +319,18 @@ int bwd_launch(const bsp_layout_s* L, const void* Y, const void* dY, void* dX, i
     }
     const int64_t rows = (int64_t)Z * L->H * L->nb * BLK;
     const int64_t blocks = std::min<int64_t>((rows + 7) / 8, (int64_t)sm_count() * 16);
-    softmax_bwd_kernel<T, BLK><<<(unsigned)std::max<int64_t>(blocks, 1), kBwdThreads, 0, s>>>(
-        L->view, (const T*)Y, (const T*)dY, (T*)dX, Z, scale);
+    // mean 16-byte vectors per row over the layout's block-rows
+    const int64_t per_row = L->nnz * BLK * (int64_t)sizeof(T) / 16 / std::max<int64_t>((int64_t)L->H * L->nb, 1);
+    const unsigned g = (unsigned)std::max<int64_t>(blocks, 1);
+    bool four = false;
+    if constexpr (sizeof(T) == 2) four = per_row <= 4 * 32;  // fp32 spills at 64 registers
+    if (four) {
+        if constexpr (sizeof(T) == 2)
+            softmax_bwd_kernel<T, BLK, 4><<<g, kBwdThreads, 0, s>>>(L->view, (const T*)Y, (const T*)dY, (T*)dX, Z,
+                                                                     scale);
+    } else {
+        softmax_bwd_kernel<T, BLK, 3><<<g, kBwdThreads, 0, s>>>(L->view, (const T*)Y, (const T*)dY, (T*)dX, Z, scale);
+    }
     return cudaGetLastError() == cudaSuccess ? BSP_OK : BSP_ERR_CUDA;
 }
 

@@ -191,10 +191,22 @@ def eye_plus_row(nb, i):
     return lay
 
 
+def band_plus_row(nb, w, i):
+    lay = W.layout_band(nb, w)
+    lay[0, i, :] = 1
+    return lay
+
+
+def cyclic_band(nb, w):
+    d = (np.arange(nb)[None, :] - np.arange(nb)[:, None]) % nb
+    return ((d <= w) | (d >= nb - w)).astype(np.uint8)[None]
+
+
 # (B, dtype, layout, kernel): the backward runs on the chunk kernel when the
 # layout has a row past 160 vectors of 16 bytes and the largest chunk of the
 # softmax's list is at most 48 KB per array, else on the one-warp-per-row
-# kernel
+# kernel, launched for 3 blocks per SM (fp32, or rows averaging more than 128
+# vectors) or 4
 SMB_CASES = {
     # rows of 1..24 blocks of 64 bf16: 8, 16 and 32 lanes a row in registers,
     # and rows past 160 vectors (one warp a row, eight rows a chunk)
@@ -207,14 +219,21 @@ SMB_CASES = {
     "two_warps_a_row": (64, "bf16", lambda: eye_plus_row(100, 50), "chunk"),
     # one fp32 row of 600 blocks of 16 (37.5 KB): one row a chunk, four warps
     "four_warps_a_row": (16, "f32", lambda: eye_plus_row(600, 300), "chunk"),
-    # rows of at most 9 blocks of 128 bf16 (144 vectors): every row in the
-    # row kernel's registers
-    "row_kernel_registers": (128, "bf16", lambda: W.layout_band(16, 4), "rows"),
+    # rows of 5 to 9 blocks of 128 bf16 (at most 144 vectors, 124 on
+    # average): every row in the row kernel's registers, 4 blocks per SM
+    "row_kernel_registers_4": (128, "bf16", lambda: W.layout_band(16, 4), "rows4"),
+    # every row 9 blocks of 128 bf16 (144 vectors): 3 blocks per SM
+    "row_kernel_registers_3": (128, "bf16", lambda: cyclic_band(16, 4), "rows3"),
+    # fp32 rows of up to 7 blocks of 32: 3 blocks per SM
+    "row_kernel_registers_f32": (32, "f32", lambda: W.layout_band(32, 3), "rows3"),
     # fp16, a row of 200 blocks of 128 (50 KB): the row kernel (its
     # register path for the diagonal rows, two passes for the long row)
-    "row_kernel_fallback": (128, "f16", lambda: eye_plus_row(200, 7), "rows"),
+    "row_kernel_fallback": (128, "f16", lambda: eye_plus_row(200, 7), "rows4"),
+    # the same long row over a band of 9 blocks a row (159 vectors on
+    # average): two passes at 3 blocks per SM
+    "row_kernel_fallback_3": (128, "f16", lambda: band_plus_row(200, 4, 7), "rows3"),
     # a row longer than the largest chunk (66.5 KB): the row kernel
-    "row_kernel_unchunked": (128, "bf16", lambda: eye_plus_row(260, 0), "rows"),
+    "row_kernel_unchunked": (128, "bf16", lambda: eye_plus_row(260, 0), "rows4"),
 }
 
 
@@ -232,6 +251,9 @@ def test_softmax_backward_kernel_paths(bsp, oracle, case):
     vec_per_row = rows_blocks * B * elt // 16
     on_chunks = ch["fits"] and ch["max_bytes"] <= 48 * 1024 and vec_per_row.max() > 160
     assert on_chunks == (kernel == "chunk"), (case, ch["fits"], ch["max_bytes"])
+    if not on_chunks:
+        mean_vec = L.nnz * B * elt // 16 // (lay.shape[0] * lay.shape[1])
+        assert kernel == ("rows3" if elt == 4 or mean_vec > 128 else "rows4"), (case, mean_vec)
     if case.startswith("lanes"):
         regs = 40 * elt // 16  # vectors a lane holds
         for lo, hi in ((0, 8 * regs), (8 * regs, 16 * regs), (16 * regs, 32 * regs), (32 * regs, 1 << 30)):
