@@ -90,6 +90,31 @@ def test_short_wait_limit_without_injection_is_harmless(bsp, oracle):
     assert_close(to_np(O2), want, torch.bfloat16, "fused SDD + softmax -> DSD, 50 ms limit")
 
 
+def test_short_wait_limit_softmax_chunk_kernels(bsp, oracle):
+    """The softmax's chunk kernel and the softmax backward's (a layout with a
+    row past the backward row kernel's registers) wait on their bulk copies
+    with the handle's limit: a 50 ms limit leaves them correct, and the
+    backward's row kernel (no waits) on a short-row layout as well."""
+    from gpu_util import PROB_TOL, check_softmax_backward_elementwise, softmax_zero_positions
+    B, scale = 64, 0.5
+    long_rows = W.layout_causal_blocks(24)          # rows of 1..24 blocks of 64 bf16
+    short_rows = W.layout_band(24, 2)               # rows of at most 5 blocks
+    for lay in (long_rows, short_rows):
+        L = bsp.bsp_layout_compile(lay, B)
+        bsp.bsp_diag_wait_limit(L, 50_000_000, 0)
+        X = W.randn((2, L.nnz, B, B), "bf16", 41)
+        Y = bsp.bsp_softmax(L, X.cuda(), None, scale, W.MASK_DIAG_CAUSAL)
+        dY = W.randn((2, L.nnz, B, B), "bf16", 42).cuda()
+        dX = bsp.bsp_softmax_backward(L, Y, dY, None, scale)
+        torch.cuda.synchronize()
+        assert bsp.bsp_status_check(L) == 0
+        want = oracle.softmax(lay, B, X, scale, W.MASK_DIAG_CAUSAL)
+        assert_close(to_np(Y), want, torch.bfloat16, "softmax, 50 ms limit", rel=PROB_TOL[torch.bfloat16],
+                     zeros=softmax_zero_positions(lay, B, 2, W.MASK_DIAG_CAUSAL))
+        check_softmax_backward_elementwise(lay, B, Y, dY, dX, oracle.softmax_backward(lay, B, Y, dY, scale),
+                                           scale, torch.bfloat16, "softmax backward, 50 ms limit")
+
+
 def test_wait_limit_rejects_unknown_injection(bsp):
     L = bsp.bsp_layout_compile(np.ones((1, 2, 2), np.uint8), 64)
     with pytest.raises(bsp.BspError) as e:
