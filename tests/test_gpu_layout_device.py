@@ -69,7 +69,7 @@ def test_device_tables_equal_host_tables(bsp, name):
         assert np.array_equal(hc["items"], dc["items"]), elt
 
 
-@pytest.mark.parametrize("name", ["tiny", "strided"])
+@pytest.mark.parametrize("name", ["tiny", "strided", "bigbird"])
 def test_ops_identical_with_either_handle(bsp, name):
     w = W.ATTENTION_WORKLOADS[name]
     lay = w.layout()
@@ -86,8 +86,12 @@ def test_ops_identical_with_either_handle(bsp, name):
     p1 = bsp.bsp_softmax(Lh, bsp.bsp_sdd(Lh, q, k), None, w.scale, w.mask_kind)
     p2 = bsp.bsp_softmax(Ld, bsp.bsp_sdd(Ld, q, k), None, w.scale, w.mask_kind)
     d1, d2 = bsp.bsp_dsd(Lh, p1, v), bsp.bsp_dsd(Ld, p2, v)
+    # the softmax backward (BigBird's global rows take its chunk kernel, the
+    # other layouts its row kernel)
+    g = W.randn(tuple(p1.shape), w.dtype, 9).cuda()
+    b1, b2 = bsp.bsp_softmax_backward(Lh, p1, g, None, w.scale), bsp.bsp_softmax_backward(Ld, p2, g, None, w.scale)
     torch.cuda.synchronize()
-    assert torch.equal(o1, o2) and torch.equal(p1, p2) and torch.equal(d1, d2)
+    assert torch.equal(o1, o2) and torch.equal(p1, p2) and torch.equal(d1, d2) and torch.equal(b1, b2)
 
 
 def test_device_compile_rejects_bad_values_and_sizes(bsp):
