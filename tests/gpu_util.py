@@ -1,6 +1,6 @@
 """Shared helpers of the GPU parity tests.
 
-Every check applies the spec bar to the whole tensor -- normwise
+Every check applies the parity bar to the whole tensor -- normwise
 max |g - r| / max |r| <= 1e-5 for fp32 outputs, <= 2e-2 for bf16 / fp16 --
 and, on top of it, a bound on each entry:
 
@@ -26,7 +26,7 @@ TOL = {torch.float32: 1e-5, torch.bfloat16: 2e-2, torch.float16: 2e-2}
 U = {torch.float32: 2.0 ** -24, torch.bfloat16: 2.0 ** -8, torch.float16: 2.0 ** -11}
 # elementwise relative error of a softmax output computed in fp32 from exact
 # inputs: one rounding to the output type plus the fp32 exponentials and
-# normalisation (< 1e-4); fp32 outputs are held to the benchmark spec's 1e-5 per entry
+# normalisation (< 1e-4); fp32 outputs are held to the 1e-5 parity bar per entry
 PROB_TOL = {torch.float32: 1e-5, torch.bfloat16: 2.0 ** -8 + 1e-4, torch.float16: 2.0 ** -11 + 1e-4}
 # below these magnitudes an output type is subnormal (fp16) or flushed to zero
 # by the fp32 exponentials: there only the absolute error is bounded, by the floor
